@@ -1,0 +1,318 @@
+/*
+ * gqaq_oracle.c -- plain, slow, fp64 CPU oracle for the decode-attention path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this file's library.  It shares no code, header,
+ * table or helper with the CUDA library: fp16 decoding below is its own
+ * IEEE-754 bit-field routine and nothing here includes a CUDA header.
+ *
+ * Sources (page title + section):
+ *  [OPT]   "Core ML Decode Optimization: Removing the 1.9 GiB Per-Token Copy
+ *          Caused by GQA repeat_kv" (OptAI engineering blog), sections
+ *          2 "Why Does GQA Replicate KV?" and 3 "Fold Q Instead of Expanding KV".
+ *  [QUEST] "Quest: Query-Aware Sparsity for Efficient Long-Context LLM
+ *          Inference" (reviewer's summary, jaehun.me), sections "page score is
+ *          not an attention probability" (the U(p,q) equation and its upper
+ *          bound), "separating page count and token budget" (B = K*S) and
+ *          "how the bytes read shrink" (the bytes model).
+ *
+ * Every function works on double arrays.  Layouts are row-major:
+ *   q      [Hq][D]              one sequence's query heads
+ *   k, v   [Hkv][Lmax][D]       one sequence's key / value cache
+ *   meta   [Hkv][Pmax][2][D]    page minimum row, then page maximum row
+ *   scores [Hkv][Pmax]
+ *   idx    [Hkv][K]             selected page indices, ascending, -1 padded
+ * L is the number of valid tokens (rows [0, L) are attended to), S the page
+ * size, Pmax = ceil(Lmax / S) and P = ceil(L / S) the number of valid pages.
+ *
+ * Parity status: every function below is pinned by a CPU test against
+ * something other than itself (a library routine, a closed form, the pages'
+ * worked example or brute force); none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* IEEE-754 binary16 -> binary64, from the bit fields (exact).               */
+/* ------------------------------------------------------------------------ */
+double oracle_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int mant = h & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)mant, -24);              /* subnormal: mant * 2^-24 */
+    } else if (expo == 31) {
+        v = mant ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(mant + 1024), expo - 25); /* (1024+mant) * 2^(e-25) */
+    }
+    return sign ? -v : v;
+}
+
+void oracle_f16_array_to_f64(const uint16_t *src, double *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = oracle_f16_to_f64(src[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Softmax attention of one query row over n key/value rows (fp64).          */
+/* s_t = scale * q . k_t ; p = softmax(s) ; out = sum_t p_t v_t              */
+/* ------------------------------------------------------------------------ */
+static void attend_rows(int d, int64_t n, const double *qrow, const double *krows,
+                        const double *vrows, double scale, double *s, double *out)
+{
+    double smax = -INFINITY;
+    for (int64_t t = 0; t < n; ++t) {
+        double dot = 0.0;
+        for (int i = 0; i < d; ++i)
+            dot += qrow[i] * krows[t * d + i];
+        s[t] = scale * dot;
+        if (s[t] > smax)
+            smax = s[t];
+    }
+    double sum = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        s[t] = exp(s[t] - smax);
+        sum += s[t];
+    }
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < n; ++t)
+            acc += s[t] * vrows[t * d + i];
+        out[i] = acc / sum;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* [OPT] section 2: attention with an explicit repeat_kv.  For each query    */
+/* head h the KV head h / G is copied into a fresh buffer (the replica the   */
+/* "tile" op makes), then ordinary per-head attention runs on the replica.   */
+/* The valid-length prefix mask plays the role of the additive context mask. */
+/* Returns 0, or -1 on bad arguments / allocation failure.                   */
+/* ------------------------------------------------------------------------ */
+int oracle_attn_repeat_kv(int hq, int hkv, int d, int64_t lmax, int64_t l,
+                          const double *q, const double *k, const double *v,
+                          double scale, double *out)
+{
+    if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || l <= 0 || l > lmax)
+        return -1;
+    int group = hq / hkv;
+    double *krep = (double *)malloc(sizeof(double) * (size_t)(l * d));
+    double *vrep = (double *)malloc(sizeof(double) * (size_t)(l * d));
+    double *s = (double *)malloc(sizeof(double) * (size_t)l);
+    if (!krep || !vrep || !s) {
+        free(krep); free(vrep); free(s);
+        return -1;
+    }
+    for (int h = 0; h < hq; ++h) {
+        int kv = h / group;                 /* repeat_kv order: h = G*kv + g */
+        memcpy(krep, k + (int64_t)kv * lmax * d, sizeof(double) * (size_t)(l * d));
+        memcpy(vrep, v + (int64_t)kv * lmax * d, sizeof(double) * (size_t)(l * d));
+        attend_rows(d, l, q + (int64_t)h * d, krep, vrep, scale, s, out + (int64_t)h * d);
+    }
+    free(krep); free(vrep); free(s);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [OPT] section 3: the folded form.  Q [Hq][D] is read as [Hkv][G][D]       */
+/* (a reshape, no copy) and each KV head is read in place for its G rows.    */
+/* Same arithmetic per row as the repeat_kv form, so the two agree bit for   */
+/* bit when the (kv, g) order matches.                                       */
+/* ------------------------------------------------------------------------ */
+int oracle_attn_folded(int hq, int hkv, int d, int64_t lmax, int64_t l,
+                       const double *q, const double *k, const double *v,
+                       double scale, double *out)
+{
+    if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || l <= 0 || l > lmax)
+        return -1;
+    int group = hq / hkv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)l);
+    if (!s)
+        return -1;
+    for (int kv = 0; kv < hkv; ++kv) {
+        const double *kh = k + (int64_t)kv * lmax * d;
+        const double *vh = v + (int64_t)kv * lmax * d;
+        for (int g = 0; g < group; ++g) {
+            const double *qrow = q + ((int64_t)kv * group + g) * d;  /* q_fold[kv][g] */
+            double *orow = out + ((int64_t)kv * group + g) * d;      /* out_fold[kv][g] */
+            attend_rows(d, l, qrow, kh, vh, scale, s, orow);
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [QUEST] page metadata: for page p and channel i, m_{p,i} is the minimum   */
+/* and M_{p,i} the maximum of the keys stored in the page.  Page p holds     */
+/* tokens [p*S, min(p*S+S, L)).  Pages at or beyond ceil(L/S) are untouched. */
+/* ------------------------------------------------------------------------ */
+int oracle_page_minmax(int hkv, int d, int64_t lmax, int64_t l, int s,
+                       const double *k, double *meta)
+{
+    if (hkv <= 0 || d <= 0 || s <= 0 || l < 0 || l > lmax)
+        return -1;
+    int64_t pmax = (lmax + s - 1) / s;
+    int64_t pvalid = (l + s - 1) / s;
+    for (int kv = 0; kv < hkv; ++kv) {
+        for (int64_t p = 0; p < pvalid; ++p) {
+            int64_t t0 = p * s;
+            int64_t t1 = t0 + s < l ? t0 + s : l;
+            double *mn = meta + (((int64_t)kv * pmax + p) * 2 + 0) * d;
+            double *mx = meta + (((int64_t)kv * pmax + p) * 2 + 1) * d;
+            for (int i = 0; i < d; ++i) {
+                double lo = k[((int64_t)kv * lmax + t0) * d + i];
+                double hi = lo;
+                for (int64_t t = t0 + 1; t < t1; ++t) {
+                    double x = k[((int64_t)kv * lmax + t) * d + i];
+                    if (x < lo) lo = x;
+                    if (x > hi) hi = x;
+                }
+                mn[i] = lo;
+                mx[i] = hi;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [QUEST] page score U(p,q) = sum_i max(q_i m_{p,i}, q_i M_{p,i}).  With    */
+/* grouped query heads, one page set serves a KV head's G query heads, so    */
+/* the KV head's score is the largest U over its G folded query rows.        */
+/* Pages at or beyond P get -inf.                                            */
+/* ------------------------------------------------------------------------ */
+int oracle_page_scores(int hq, int hkv, int d, int64_t pmax, int64_t pvalid,
+                       const double *q, const double *meta, double *scores)
+{
+    if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || pvalid < 0 || pvalid > pmax)
+        return -1;
+    int group = hq / hkv;
+    for (int kv = 0; kv < hkv; ++kv) {
+        for (int64_t p = 0; p < pmax; ++p) {
+            if (p >= pvalid) {
+                scores[(int64_t)kv * pmax + p] = -INFINITY;
+                continue;
+            }
+            const double *mn = meta + (((int64_t)kv * pmax + p) * 2 + 0) * d;
+            const double *mx = meta + (((int64_t)kv * pmax + p) * 2 + 1) * d;
+            double best = -INFINITY;
+            for (int g = 0; g < group; ++g) {
+                const double *qrow = q + ((int64_t)kv * group + g) * d;
+                double u = 0.0;
+                for (int i = 0; i < d; ++i) {
+                    double a = qrow[i] * mn[i];
+                    double b = qrow[i] * mx[i];
+                    u += (a > b) ? a : b;
+                }
+                if (u > best)
+                    best = u;
+            }
+            scores[(int64_t)kv * pmax + p] = best;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [QUEST] top-K page selection: sort the pages by descending score (lower   */
+/* page index first on equal scores), keep the first min(K, P), and return   */
+/* them in ascending page order, padded with -1 up to K.                     */
+/* ------------------------------------------------------------------------ */
+typedef struct { double score; int64_t page; } scored_page;
+
+static int by_score_desc_then_page(const void *a, const void *b)
+{
+    const scored_page *x = (const scored_page *)a, *y = (const scored_page *)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->page > y->page) - (x->page < y->page);
+}
+
+static int by_int32(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+int oracle_topk_pages(int hkv, int64_t pmax, int64_t pvalid, int kpages,
+                      const double *scores, int32_t *idx)
+{
+    if (hkv <= 0 || kpages <= 0 || pvalid < 0 || pvalid > pmax)
+        return -1;
+    scored_page *tmp = (scored_page *)malloc(sizeof(scored_page) * (size_t)(pvalid > 0 ? pvalid : 1));
+    if (!tmp)
+        return -1;
+    for (int kv = 0; kv < hkv; ++kv) {
+        for (int64_t p = 0; p < pvalid; ++p) {
+            tmp[p].score = scores[(int64_t)kv * pmax + p];
+            tmp[p].page = p;
+        }
+        qsort(tmp, (size_t)pvalid, sizeof(scored_page), by_score_desc_then_page);
+        int64_t n = pvalid < kpages ? pvalid : kpages;
+        int32_t *row = idx + (int64_t)kv * kpages;
+        for (int64_t j = 0; j < n; ++j)
+            row[j] = (int32_t)tmp[j].page;
+        qsort(row, (size_t)n, sizeof(int32_t), by_int32);
+        for (int64_t j = n; j < kpages; ++j)
+            row[j] = -1;
+    }
+    free(tmp);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [QUEST] attention over the selected pages only: for each query head h,    */
+/* gather the rows of KV head h/G that lie in its listed pages (page p       */
+/* contributes tokens [p*S, min(p*S+S, L))) into fresh buffers, then run     */
+/* ordinary softmax attention over the gathered rows.  Entries < 0 or >= P   */
+/* are skipped.  Returns -1 if a head ends up with no token.                 */
+/* ------------------------------------------------------------------------ */
+int oracle_sparse_attn(int hq, int hkv, int d, int64_t lmax, int64_t l, int s,
+                       int kpages, const double *q, const double *k, const double *v,
+                       const int32_t *idx, double scale, double *out)
+{
+    if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || s <= 0 || l <= 0 || l > lmax ||
+        kpages <= 0)
+        return -1;
+    int group = hq / hkv;
+    int64_t pvalid = (l + s - 1) / s;
+    int64_t cap = (int64_t)kpages * s;
+    double *kg = (double *)malloc(sizeof(double) * (size_t)(cap * d));
+    double *vg = (double *)malloc(sizeof(double) * (size_t)(cap * d));
+    double *sc = (double *)malloc(sizeof(double) * (size_t)cap);
+    if (!kg || !vg || !sc) {
+        free(kg); free(vg); free(sc);
+        return -1;
+    }
+    int rc = 0;
+    for (int h = 0; h < hq && rc == 0; ++h) {
+        int kv = h / group;
+        const int32_t *row = idx + (int64_t)kv * kpages;
+        int64_t n = 0;
+        for (int j = 0; j < kpages; ++j) {
+            int64_t p = row[j];
+            if (p < 0 || p >= pvalid)
+                continue;
+            int64_t t1 = p * s + s < l ? p * s + s : l;
+            for (int64_t t = p * s; t < t1; ++t) {
+                memcpy(kg + n * d, k + ((int64_t)kv * lmax + t) * d, sizeof(double) * (size_t)d);
+                memcpy(vg + n * d, v + ((int64_t)kv * lmax + t) * d, sizeof(double) * (size_t)d);
+                ++n;
+            }
+        }
+        if (n == 0) {
+            rc = -1;
+            break;
+        }
+        attend_rows(d, n, q + (int64_t)h * d, kg, vg, scale, sc, out + (int64_t)h * d);
+    }
+    free(kg); free(vg); free(sc);
+    return rc;
+}

@@ -1,0 +1,281 @@
+"""Pins for the fp64 CPU oracle, each against something other than the oracle.
+
+The oracle is only trusted as a parity reference once these pass: library
+routines (numpy's fp16 decoder, numpy min/max and sorting, torch's fp64
+scaled-dot-product attention), the pages' printed worked example and byte
+arithmetic, closed forms (L=1, identical keys) and brute force on tiny inputs.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+RNG = np.random.default_rng(7)
+
+
+def rand_f16(*shape, scale=1.0, rng=RNG):
+    return (rng.standard_normal(shape) * scale).astype(np.float16)
+
+
+# ---------------------------------------------------------------------------
+# fp16 decoding: every bit pattern against numpy's own conversion
+# ---------------------------------------------------------------------------
+def test_f16_decoder_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.f16_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # the sign of zero survives
+    assert np.signbit(ours[0x8000]) and not np.signbit(ours[0x0000])
+
+
+# ---------------------------------------------------------------------------
+# The Quest page's worked example (golden values printed on the page)
+# ---------------------------------------------------------------------------
+def test_quest_worked_example(golden_dir):
+    ex = json.load(open(os.path.join(golden_dir, "quest_worked_example.json")))
+    q = np.array(ex["q"], dtype=np.float64)
+    keys = np.array(ex["page_A_keys"] + ex["page_B_keys"], dtype=np.float64)  # 3 tokens
+    # page size 2: page A = tokens 0-1, page B = token 2 (a partial last page)
+    k = np.zeros((1, 1, 4, 3)); k[0, 0, :3] = keys
+    meta = oracle.page_minmax(k, [3], page_size=2)
+    assert np.array_equal(meta[0, 0, 0, 0], [-0.5, -0.1, -0.3])     # m_A
+    assert np.array_equal(meta[0, 0, 0, 1], [0.7, 1.2, 0.9])        # M_A
+    assert np.array_equal(meta[0, 0, 1, 0], [1.2, 0.0, 0.0])        # m_B = M_B
+    u = oracle.page_scores(q[None, None, :], meta, [3], page_size=2)[0, 0]
+    assert u[0] == pytest.approx(ex["U_A"], abs=1e-12)
+    assert u[0] == pytest.approx(sum(ex["U_A_terms"]), abs=1e-12)
+    assert u[1] == pytest.approx(ex["U_B"], abs=1e-12)
+    assert keys[:2] @ q == pytest.approx(ex["dots_A"], abs=1e-12)
+    assert keys[2] @ q == pytest.approx(ex["dot_B"], abs=1e-12)
+    # A outranks B under U, although B holds the larger true dot product
+    top1 = oracle.topk_pages(u[None, None, :], [3], page_size=2, k=1)[0, 0]
+    assert list(top1) == [0]
+    assert max(keys[:2] @ q) < keys[2] @ q
+
+
+def test_score_uses_min_channel_for_negative_query():
+    # the third channel's term is q_3 * m_3 = (-0.2)(-0.3) = +0.06, not q_3 * M_3
+    q = np.array([[[0.0, 0.0, -0.2]]])
+    k = np.zeros((1, 1, 2, 3)); k[0, 0, 0] = [-0.5, -0.1, -0.3]; k[0, 0, 1] = [0.7, 1.2, 0.9]
+    meta = oracle.page_minmax(k, [2], page_size=2)
+    u = oracle.page_scores(q, meta, [2], page_size=2)[0, 0, 0]
+    assert u == pytest.approx(0.06, abs=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# Metadata against numpy's min/max; the upper bound q.k <= U by brute force
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L,Lmax,S", [(37, 40, 4), (16, 16, 16), (1, 8, 4), (50, 64, 16)])
+def test_page_minmax_matches_numpy(L, Lmax, S):
+    k = rand_f16(2, 3, Lmax, 5)
+    meta = oracle.page_minmax(k, [L, max(1, L - 3)], page_size=S)
+    k64 = k.astype(np.float64)
+    for b, lb in enumerate([L, max(1, L - 3)]):
+        P = (lb + S - 1) // S
+        for p in range(P):
+            rows = k64[b, :, p * S:min(p * S + S, lb)]
+            assert np.array_equal(meta[b, :, p, 0], rows.min(axis=1))
+            assert np.array_equal(meta[b, :, p, 1], rows.max(axis=1))
+        assert np.all(np.isnan(meta[b, :, P:]))
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_upper_bound_every_key(G):
+    S, Hkv, D, L = 4, 3, 8, 45
+    Hq = Hkv * G
+    q = rand_f16(1, Hq, D, scale=2.0)
+    q[0, 0, :4] = -np.abs(q[0, 0, :4])                 # negative components
+    k = rand_f16(1, Hkv, 48, D)
+    k[0, 1, 8:12] += np.float16(2.0)                   # a planted page
+    meta = oracle.page_minmax(k, [L], page_size=S)
+    u = oracle.page_scores(q, meta, [L], page_size=S)
+    q64, k64 = q.astype(np.float64), k.astype(np.float64)
+    for kv in range(Hkv):
+        for t in range(L):
+            dots = q64[0, kv * G:(kv + 1) * G] @ k64[0, kv, t]
+            assert dots.max() <= u[0, kv, t // S] + 1e-12
+
+
+def test_score_is_tight_for_single_token_page():
+    # with one token per page the bound is attained: U = q.k exactly
+    q = rand_f16(1, 2, 8)
+    k = rand_f16(1, 2, 5, 8)
+    meta = oracle.page_minmax(k, [5], page_size=1)
+    u = oracle.page_scores(q, meta, [5], page_size=1)
+    dots = np.einsum("hd,htd->ht", q[0].astype(np.float64), k[0].astype(np.float64))
+    assert np.allclose(u[0], dots, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Top-K: against numpy's lexsort; K >= P; scale invariance of the ranking
+# ---------------------------------------------------------------------------
+def _numpy_topk(scores, P, K):
+    order = np.lexsort((np.arange(P), -scores[:P]))   # by -score, then by page index
+    return np.sort(order[:min(K, P)])
+
+
+@pytest.mark.parametrize("P,Pmax,K", [(37, 40, 5), (40, 40, 40), (9, 12, 20), (100, 100, 1)])
+def test_topk_against_lexsort(P, Pmax, K):
+    rng = np.random.default_rng(P * 31 + K)
+    s = rng.standard_normal((2, 3, Pmax))
+    s[0, 0, 3] = s[0, 0, 7] = s[0, 0, 11] = 5.0          # exact ties at the top
+    s[1, 2, :] = 1.0                                     # all equal
+    idx = oracle.topk_pages(s, [P * 16, P * 16], page_size=16, k=K)
+    for b in range(2):
+        for h in range(3):
+            ref = _numpy_topk(s[b, h], P, K)
+            n = len(ref)
+            assert np.array_equal(idx[b, h, :n], ref)
+            assert np.all(idx[b, h, n:] == -1)
+    # all-equal scores: ties go to the lowest page indices
+    assert np.array_equal(idx[1, 2, :min(K, P)], np.arange(min(K, P)))
+
+
+def test_topk_ranking_invariant_under_positive_scale():
+    S, Hkv, D, L, K = 16, 2, 16, 16 * 30, 7
+    q = rand_f16(1, Hkv, D)
+    k = rand_f16(1, Hkv, L, D)
+    meta = oracle.page_minmax(k, [L], page_size=S)
+    base = oracle.topk_pages(oracle.page_scores(q, meta, [L], S), [L], S, K)
+    for c in (0.25, 2.0, 8.0):                        # powers of two scale exactly
+        qc = (q.astype(np.float64) * c)
+        sel = oracle.topk_pages(oracle.page_scores(qc, meta, [L], S), [L], S, K)
+        assert np.array_equal(sel, base)
+
+
+# ---------------------------------------------------------------------------
+# Dense attention: repeat_kv form vs torch fp64 SDPA, vs the folded form,
+# closed forms, and the head mapping h = G*kv + g
+# ---------------------------------------------------------------------------
+def _sdpa_reference(q, k, v, valid_len, scale, G):
+    out = []
+    for b in range(q.shape[0]):
+        L = int(valid_len[b])
+        qb = torch.from_numpy(q[b].astype(np.float64))[:, None, :]          # [Hq,1,D]
+        kb = torch.from_numpy(k[b, :, :L].astype(np.float64)).repeat_interleave(G, dim=0)
+        vb = torch.from_numpy(v[b, :, :L].astype(np.float64)).repeat_interleave(G, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(qb, kb, vb, scale=scale)
+        out.append(o[:, 0, :].numpy())
+    return np.stack(out)
+
+
+@pytest.mark.parametrize("B,Hkv,G,D,Lmax", [(2, 3, 4, 8, 37), (1, 2, 1, 16, 20), (2, 1, 8, 4, 9)])
+def test_dense_matches_torch_sdpa(B, Hkv, G, D, Lmax):
+    q = rand_f16(B, Hkv * G, D)
+    k = rand_f16(B, Hkv, Lmax, D)
+    v = rand_f16(B, Hkv, Lmax, D)
+    valid = np.array([Lmax, max(1, Lmax // 3)][:B])
+    scale = 1.0 / np.sqrt(D)
+    ours = oracle.attn_repeat_kv(q, k, v, valid, scale)
+    ref = _sdpa_reference(q, k, v, valid, scale, G)
+    assert np.allclose(ours, ref, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,Hkv,G,D,Lmax", [(2, 3, 4, 8, 37), (1, 2, 2, 16, 20), (2, 1, 8, 4, 9)])
+def test_folded_equals_repeat_kv_bitwise(B, Hkv, G, D, Lmax):
+    q = rand_f16(B, Hkv * G, D)
+    k = rand_f16(B, Hkv, Lmax, D)
+    v = rand_f16(B, Hkv, Lmax, D)
+    valid = np.array([Lmax, 5][:B])
+    a = oracle.attn_repeat_kv(q, k, v, valid, 0.3)
+    f = oracle.attn_folded(q, k, v, valid, 0.3)
+    assert np.array_equal(a, f)
+
+
+def test_head_mapping_contiguous_groups():
+    # each KV head's values are one constant, so output row h must equal that
+    # constant for kv = h // G; an interleaved mapping (kv = h % Hkv) would not
+    Hkv, G, D, L = 3, 4, 8, 11
+    q = rand_f16(1, Hkv * G, D)
+    k = rand_f16(1, Hkv, L, D)
+    v = np.zeros((1, Hkv, L, D), dtype=np.float16)
+    for kv in range(Hkv):
+        v[0, kv] = np.float16(kv + 1)
+    out = oracle.attn_repeat_kv(q, k, v, [L], 0.5)[0]
+    for h in range(Hkv * G):
+        assert np.allclose(out[h], h // G + 1, rtol=0, atol=1e-14)
+        if h % Hkv != h // G:   # the interleaved reading would give another constant
+            assert not np.allclose(out[h], h % Hkv + 1, rtol=0, atol=1e-3)
+
+
+def test_single_token_returns_its_value():
+    q = rand_f16(1, 8, 16); k = rand_f16(1, 2, 7, 16); v = rand_f16(1, 2, 7, 16)
+    out = oracle.attn_repeat_kv(q, k, v, [1], 0.25)
+    for h in range(8):
+        assert np.array_equal(out[0, h], v[0, h // 4, 0].astype(np.float64))
+
+
+def test_identical_keys_average_values():
+    q = rand_f16(1, 4, 8)
+    k = np.repeat(rand_f16(1, 1, 1, 8), 9, axis=2)
+    v = rand_f16(1, 1, 9, 8)
+    out = oracle.attn_repeat_kv(q, k, v, [9], 0.35)
+    assert np.allclose(out[0], v[0, 0].astype(np.float64).mean(axis=0)[None, :], atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# Sparse attention: K >= P equals dense; otherwise SDPA over gathered tokens
+# ---------------------------------------------------------------------------
+def test_sparse_with_all_pages_equals_dense():
+    Hkv, G, D, Lmax, S, L = 2, 4, 8, 70, 16, 67
+    q = rand_f16(1, Hkv * G, D); k = rand_f16(1, Hkv, Lmax, D); v = rand_f16(1, Hkv, Lmax, D)
+    P = (L + S - 1) // S
+    idx = np.full((1, Hkv, P + 3), -1, dtype=np.int32)
+    idx[0, :, :P] = np.arange(P)
+    sp = oracle.sparse_attn(q, k, v, [L], idx, S, 0.3)
+    dn = oracle.attn_repeat_kv(q, k, v, [L], 0.3)
+    assert np.array_equal(sp, dn)
+
+
+def test_sparse_matches_sdpa_on_gathered_tokens():
+    Hkv, G, D, Lmax, S, L = 2, 2, 8, 80, 16, 75
+    q = rand_f16(1, Hkv * G, D); k = rand_f16(1, Hkv, Lmax, D); v = rand_f16(1, Hkv, Lmax, D)
+    idx = np.array([[[0, 2, 4, -1], [1, 3, -1, -1]]], dtype=np.int32)
+    sp = oracle.sparse_attn(q, k, v, [L], idx, S, 0.4)
+    for kv in range(Hkv):
+        toks = [t for p in idx[0, kv] if p >= 0 for t in range(p * S, min(p * S + S, L))]
+        kk = k[:, kv:kv + 1, toks]; vv = v[:, kv:kv + 1, toks]
+        ref = _sdpa_reference(q[:, kv * G:(kv + 1) * G], kk, vv, [len(toks)], 0.4, G)
+        assert np.allclose(sp[0, kv * G:(kv + 1) * G], ref[0], rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Byte arithmetic the pages print
+# ---------------------------------------------------------------------------
+def test_quest_bytes_model(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "byte_arithmetic.json")))["quest"]
+    ex = g["budget_example"]
+    assert oracle.token_budget(ex["K"], ex["S"]) == ex["B_tokens"]
+    ex = g["ratio_example"]
+    assert oracle.token_budget(ex["K"], ex["S"]) == ex["B_tokens"]
+    assert oracle.quest_read_ratio(ex["L"], ex["S"], ex["K"]) == ex["ratio"]
+    assert ex["B_tokens"] // ex["S"] == ex["pages_for_4k_tokens"]
+    M, L, S, K = 256, ex["L"], ex["S"], ex["K"]
+    quest = oracle.bytes_meta(M, L, S) + oracle.bytes_selected(M, K, S)
+    assert quest / oracle.bytes_full(M, L) == ex["ratio"]
+
+
+def test_repeat_kv_storage_and_byte_counts(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "byte_arithmetic.json")))["opt"]
+    k = torch.zeros(1, *g["layer_cache_shape"], dtype=torch.float16)      # [1,8,4096,64]
+    assert k.untyped_storage().nbytes() == g["layer_cache_bytes"]
+    e = k[:, :, None].expand(1, 8, 4, 4096, 64)                           # view, stride 0
+    assert e.untyped_storage().data_ptr() == k.untyped_storage().data_ptr()
+    assert e.untyped_storage().nbytes() == g["expand_storage_bytes"]
+    r = e.reshape(1, 32, 4096, 64)                                        # copies
+    assert r.untyped_storage().data_ptr() != k.untyped_storage().data_ptr()
+    assert r.untyped_storage().nbytes() == g["reshape_storage_bytes"] == g["tile_output_bytes"]
+    assert 2 * g["num_layers"] * g["layer_cache_bytes"] == g["all_layers_kv_bytes"]
+    assert g["num_layers"] * 2 * 8 * 64 * 2 == g["per_token_write_bytes"]
+    assert g["tile_ops"] * g["tile_output_bytes"] == g["tile_outputs_total_bytes"]
+    assert 2 * g["tile_outputs_total_bytes"] == g["tile_write_plus_read_bytes"]
+    q = torch.zeros(*g["q_decode_shape"], dtype=torch.float16)
+    assert q.numel() * 2 == g["q_decode_bytes"]
+    assert q.reshape(1, 8, 4, 64).data_ptr() == q.data_ptr()              # the fold is a view
