@@ -1,0 +1,270 @@
+"""GB300 (sm_103a) decode attention: GQA query-head folding + Quest page sparsity.
+
+A thin ctypes binding over the C ABI in ``include/gqaq.h`` (``libgqaq.so``).
+Every function here only marshals arguments: it reads shapes and pointers
+from torch tensors, builds a ``gqaq_dims``, passes
+``torch.cuda.current_stream()`` and raises ``GqaqError`` on a non-zero status.
+All arithmetic runs in the library's CUDA kernels. When the library is
+missing, the import still succeeds but every call raises: there is no CPU
+fallback.
+
+Function names follow the C ABI: gqa_decode_attn, quest_append_kv,
+quest_update_meta, quest_score_pages, quest_topk_pages, quest_sparse_attn.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqaq.so")
+
+GQAQ_OK = 0
+GQAQ_ERR_INVALID_ARG = 1
+GQAQ_ERR_UNSUPPORTED = 2
+GQAQ_ERR_WORKSPACE = 3
+GQAQ_ERR_CUDA = 4
+GQAQ_ERR_TIMEOUT = 5
+
+GQAQ_DEV_TIMEOUT = 1
+GQAQ_DEV_BAD_LEN = 2
+GQAQ_DEV_BAD_PAGE = 4
+GQAQ_DEV_BAD_POS = 8
+
+GQAQ_OPT_MAX_CTAS = 1
+GQAQ_OPT_WAIT_TIMEOUT_NS = 2
+GQAQ_OPT_TEST_STALL = 3
+
+PAGE_SIZE = 16
+
+
+class GqaqError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("num_q_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("max_len", ctypes.c_int), ("page_size", ctypes.c_int)]
+
+
+# Exported symbols, in the order include/gqaq.h declares them.
+EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_update_meta",
+           "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "gqaq_status_string",
+           "gqaq_set_option", "gqaq_device_status", "gqaq_version")
+
+_lib = None
+
+
+def lib():
+    """Load ``libgqaq.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, dp = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(Dims)
+        L.gqaq_workspace_bytes.argtypes = [dp, i32]
+        L.gqaq_workspace_bytes.restype = ctypes.c_size_t
+        L.gqa_decode_attn.argtypes = [dp, vp, vp, vp, vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+        L.quest_append_kv.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
+        L.quest_update_meta.argtypes = [dp, vp, vp, vp, i32, i32, vp]
+        L.quest_score_pages.argtypes = [dp, vp, vp, vp, vp, vp]
+        L.quest_topk_pages.argtypes = [dp, vp, vp, i32, vp, vp, ctypes.c_size_t, vp]
+        L.quest_sparse_attn.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp,
+                                        ctypes.c_size_t, vp]
+        L.gqaq_status_string.argtypes = [i32]
+        L.gqaq_status_string.restype = ctypes.c_char_p
+        L.gqaq_set_option.argtypes = [i32, ctypes.c_int64]
+        L.gqaq_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
+        L.gqaq_version.argtypes = []
+        for name in EXPORTS:
+            if name not in ("gqaq_workspace_bytes", "gqaq_status_string"):
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gqaq_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != GQAQ_OK:
+        raise GqaqError(fn, status, status_string(status))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_dims(batch, num_q_heads, num_kv_heads, head_dim, max_len, page_size=PAGE_SIZE) -> Dims:
+    return Dims(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(max_len),
+                int(page_size))
+
+
+def dims_of(q: torch.Tensor, k_cache: torch.Tensor, page_size: int = PAGE_SIZE) -> Dims:
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    return make_dims(B, Hq, Hkv, D, Lmax, page_size)
+
+
+def set_option(option: int, value: int):
+    _check("gqaq_set_option", lib().gqaq_set_option(int(option), int(value)))
+
+
+def device_status(reset: bool = True) -> int:
+    """Return the current device's GQAQ_DEV_* flags (synchronises the device)."""
+    flags = ctypes.c_int(0)
+    rc = lib().gqaq_device_status(ctypes.byref(flags), 1 if reset else 0)
+    if rc not in (GQAQ_OK, GQAQ_ERR_TIMEOUT):
+        _check("gqaq_device_status", rc)
+    return flags.value
+
+
+def workspace_bytes(dims: Dims, max_selected_pages: int = 0) -> int:
+    n = lib().gqaq_workspace_bytes(ctypes.byref(dims), int(max_selected_pages))
+    if n == 0:
+        raise GqaqError("gqaq_workspace_bytes", GQAQ_ERR_UNSUPPORTED, "dims rejected")
+    return int(n)
+
+
+def alloc_workspace(dims: Dims, device) -> torch.Tensor:
+    return torch.empty(workspace_bytes(dims), dtype=torch.uint8, device=device)
+
+
+def num_pages(max_len: int, page_size: int = PAGE_SIZE) -> int:
+    return (int(max_len) + page_size - 1) // page_size
+
+
+# ---------------------------------------------------------------------------
+# Entry points
+# ---------------------------------------------------------------------------
+def gqa_decode_attn(q, k_cache, v_cache, valid_len, scale: float, out=None, workspace=None):
+    """Dense folded-GQA decode attention. q [B,Hq,D], caches [B,Hkv,Lmax,D] fp16."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    d = dims_of(q, k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 3)
+    if workspace is None:
+        workspace = alloc_workspace(d, q.device)
+    _check("gqa_decode_attn", lib().gqa_decode_attn(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(valid_len), float(scale),
+        _ptr(out), _ptr(workspace), workspace.numel(), _stream(q)))
+    return out
+
+
+def quest_append_kv(k_cache, v_cache, meta, k_new, v_new, pos, page_size: int = PAGE_SIZE):
+    """Write k_new/v_new [B,Hkv,D] at row pos[b] and update that page's min/max."""
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(meta, "meta", torch.float16, 5)
+    _need(k_new, "k_new", torch.float16, 3)
+    _need(v_new, "v_new", torch.float16, 3)
+    _need(pos, "pos", torch.int32, 1)
+    B, Hkv, Lmax, D = k_cache.shape
+    d = make_dims(B, Hkv, Hkv, D, Lmax, page_size)
+    _check("quest_append_kv", lib().quest_append_kv(
+        ctypes.byref(d), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(k_new), _ptr(v_new),
+        _ptr(pos), _stream(k_cache)))
+
+
+def quest_update_meta(k_cache, valid_len, meta, page_begin: int = 0, page_end: Optional[int] = None,
+                      page_size: int = PAGE_SIZE):
+    """Rebuild page min/max [B,Hkv,Pmax,2,D] for pages [page_begin, page_end)."""
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    _need(meta, "meta", torch.float16, 5)
+    B, Hkv, Lmax, D = k_cache.shape
+    d = make_dims(B, Hkv, Hkv, D, Lmax, page_size)
+    if page_end is None:
+        page_end = num_pages(Lmax, page_size)
+    _check("quest_update_meta", lib().quest_update_meta(
+        ctypes.byref(d), _ptr(k_cache), _ptr(valid_len), _ptr(meta), int(page_begin), int(page_end),
+        _stream(k_cache)))
+    return meta
+
+
+def quest_score_pages(q, meta, valid_len, max_len: int, scores=None, page_size: int = PAGE_SIZE):
+    """U(p,q) per KV head (max over its G folded query rows) -> scores [B,Hkv,Pmax] fp32."""
+    _need(q, "q", torch.float16, 3)
+    _need(meta, "meta", torch.float16, 5)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    B, Hq, D = q.shape
+    Hkv = meta.shape[1]
+    d = make_dims(B, Hq, Hkv, D, max_len, page_size)
+    if scores is None:
+        scores = torch.empty(B, Hkv, num_pages(max_len, page_size), dtype=torch.float32, device=q.device)
+    _need(scores, "scores", torch.float32, 3)
+    _check("quest_score_pages", lib().quest_score_pages(
+        ctypes.byref(d), _ptr(q), _ptr(meta), _ptr(valid_len), _ptr(scores), _stream(q)))
+    return scores
+
+
+def quest_topk_pages(scores, valid_len, k: int, max_len: int, page_idx=None, page_size: int = PAGE_SIZE):
+    """Top-k pages per (b, kv) -> page_idx [B,Hkv,k] int32, ascending, -1 padded."""
+    _need(scores, "scores", torch.float32, 3)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    B, Hkv, _ = scores.shape
+    d = make_dims(B, Hkv, Hkv, 64, max_len, page_size)
+    if page_idx is None:
+        page_idx = torch.empty(B, Hkv, int(k), dtype=torch.int32, device=scores.device)
+    _need(page_idx, "page_idx", torch.int32, 3)
+    _check("quest_topk_pages", lib().quest_topk_pages(
+        ctypes.byref(d), _ptr(scores), _ptr(valid_len), int(k), _ptr(page_idx), None, 0,
+        _stream(scores)))
+    return page_idx
+
+
+def quest_sparse_attn(q, k_cache, v_cache, valid_len, page_idx, scale: float, out=None, workspace=None,
+                      page_size: int = PAGE_SIZE):
+    """Attention over the selected pages only (page_idx [B,Hkv,k])."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    _need(page_idx, "page_idx", torch.int32, 3)
+    d = dims_of(q, k_cache, page_size)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 3)
+    if workspace is None:
+        workspace = alloc_workspace(d, q.device)
+    _check("quest_sparse_attn", lib().quest_sparse_attn(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(valid_len), _ptr(page_idx),
+        int(page_idx.shape[2]), float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(q)))
+    return out
+
+
+def new_meta(batch: int, num_kv_heads: int, max_len: int, head_dim: int, device,
+             page_size: int = PAGE_SIZE) -> torch.Tensor:
+    """Allocate a metadata buffer [B,Hkv,Pmax,2,D] fp16 (contents undefined)."""
+    return torch.empty(batch, num_kv_heads, num_pages(max_len, page_size), 2, head_dim,
+                       dtype=torch.float16, device=device)

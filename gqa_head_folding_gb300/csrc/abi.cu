@@ -1,0 +1,295 @@
+// abi.cu -- the extern "C" entry points declared in include/gqaq.h: host-side
+// argument validation, per-device launch context, TMA descriptor encoding,
+// options and the device status word.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace gqaq {
+
+// Device status word, one per device that loads the library.
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::atomic<int64_t> g_opt_max_ctas{0};
+std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
+std::atomic<int64_t> g_opt_test_stall{0};
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int *status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Per-device set-up: SM count and the device address of the status word.
+int device_state(DeviceState **out, int *dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GQAQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GQAQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GQAQ_ERR_CUDA;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess || addr == nullptr)
+            return GQAQ_ERR_CUDA;
+        s.num_sms = sms;
+        s.status = static_cast<int *>(addr);
+        s.ready = true;
+    }
+    *out = &s;
+    *dev_out = dev;
+    return GQAQ_OK;
+}
+
+int make_ctx(LaunchCtx *ctx, void *stream) {
+    DeviceState *s = nullptr;
+    int dev = 0;
+    const int rc = device_state(&s, &dev);
+    if (rc != GQAQ_OK) return rc;
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    ctx->device = dev;
+    ctx->num_sms = s->num_sms;
+    ctx->max_ctas = (int)g_opt_max_ctas.load();
+    ctx->timeout_ns = (uint64_t)g_opt_timeout_ns.load();
+    ctx->test_stall = (int)g_opt_test_stall.load();
+    ctx->status = s->status;
+    return GQAQ_OK;
+}
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every entry point.
+int check_dims(const gqaq_dims *d, bool quest) {
+    if (d == nullptr) return GQAQ_ERR_INVALID_ARG;
+    if (d->batch < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1 || d->max_len < 1 || d->head_dim < 1)
+        return GQAQ_ERR_INVALID_ARG;
+    if (d->num_q_heads % d->num_kv_heads != 0) return GQAQ_ERR_INVALID_ARG;
+    if (quest && d->page_size < 1) return GQAQ_ERR_INVALID_ARG;
+    const int G = d->num_q_heads / d->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return GQAQ_ERR_UNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128) return GQAQ_ERR_UNSUPPORTED;
+    if (quest && d->page_size != 16) return GQAQ_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)d->batch * d->num_kv_heads * d->max_len;
+    if (rows > (int64_t)INT32_MAX - 1024) return GQAQ_ERR_UNSUPPORTED;
+    return GQAQ_OK;
+}
+
+}  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                          uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace gqaq
+
+using namespace gqaq;
+
+extern "C" {
+
+int gqaq_version(void) { return 100; }
+
+const char *gqaq_status_string(int status) {
+    switch (status) {
+        case GQAQ_OK: return "GQAQ_OK";
+        case GQAQ_ERR_INVALID_ARG: return "GQAQ_ERR_INVALID_ARG";
+        case GQAQ_ERR_UNSUPPORTED: return "GQAQ_ERR_UNSUPPORTED";
+        case GQAQ_ERR_WORKSPACE: return "GQAQ_ERR_WORKSPACE";
+        case GQAQ_ERR_CUDA: return "GQAQ_ERR_CUDA";
+        case GQAQ_ERR_TIMEOUT: return "GQAQ_ERR_TIMEOUT";
+        default: return "GQAQ_ERR_UNKNOWN";
+    }
+}
+
+int gqaq_set_option(int option, int64_t value) {
+    switch (option) {
+        case GQAQ_OPT_MAX_CTAS:
+            if (value < 0 || value > INT32_MAX) return GQAQ_ERR_INVALID_ARG;
+            g_opt_max_ctas.store(value);
+            return GQAQ_OK;
+        case GQAQ_OPT_WAIT_TIMEOUT_NS:
+            if (value < 0) return GQAQ_ERR_INVALID_ARG;
+            g_opt_timeout_ns.store(value);
+            return GQAQ_OK;
+        case GQAQ_OPT_TEST_STALL:
+            g_opt_test_stall.store(value != 0 ? 1 : 0);
+            return GQAQ_OK;
+        default:
+            return GQAQ_ERR_INVALID_ARG;
+    }
+}
+
+int gqaq_device_status(int *flags, int reset) {
+    if (flags == nullptr) return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    const int rc = make_ctx(&ctx, nullptr);
+    if (rc != GQAQ_OK) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GQAQ_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ctx.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GQAQ_ERR_CUDA;
+    if (reset) {
+        const int zero = 0;
+        if (cudaMemcpy(ctx.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return GQAQ_ERR_CUDA;
+    }
+    *flags = v;
+    return (v & GQAQ_DEV_TIMEOUT) ? GQAQ_ERR_TIMEOUT : GQAQ_OK;
+}
+
+size_t gqaq_workspace_bytes(const gqaq_dims *dims, int max_selected_pages) {
+    (void)max_selected_pages;
+    if (check_dims(dims, false) != GQAQ_OK) return 0;
+    LaunchCtx ctx;
+    if (make_ctx(&ctx, nullptr) != GQAQ_OK) return 0;
+    return attention_workspace_bytes(dims, ctx);
+}
+
+int gqa_decode_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
+                    const gqaq_half *v_cache, const int32_t *valid_len, float scale, gqaq_half *out,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_dims(dims, false);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        !aligned16(valid_len))
+        return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return GQAQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace)) return GQAQ_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    AttnArgs a;
+    a.dims = dims;
+    a.q = reinterpret_cast<const __half *>(q);
+    a.k_cache = reinterpret_cast<const __half *>(k_cache);
+    a.v_cache = reinterpret_cast<const __half *>(v_cache);
+    a.valid_len = valid_len;
+    a.page_idx = nullptr;
+    a.kpages = 0;
+    a.scale = scale;
+    a.out = reinterpret_cast<__half *>(out);
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launch_attention(a, ctx);
+}
+
+int quest_append_kv(const gqaq_dims *dims, gqaq_half *k_cache, gqaq_half *v_cache, gqaq_half *meta,
+                    const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(meta) || !aligned16(k_new) ||
+        !aligned16(v_new) || !aligned16(pos))
+        return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_append_kv(dims, reinterpret_cast<__half *>(k_cache), reinterpret_cast<__half *>(v_cache),
+                            reinterpret_cast<__half *>(meta), reinterpret_cast<const __half *>(k_new),
+                            reinterpret_cast<const __half *>(v_new), pos, ctx);
+}
+
+int quest_update_meta(const gqaq_dims *dims, const gqaq_half *k_cache, const int32_t *valid_len,
+                      gqaq_half *meta, int page_begin, int page_end, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(k_cache) || !aligned16(valid_len) || !aligned16(meta)) return GQAQ_ERR_INVALID_ARG;
+    const int pmax = (dims->max_len + dims->page_size - 1) / dims->page_size;
+    if (page_begin < 0 || page_end < page_begin || page_end > pmax) return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_update_meta(dims, reinterpret_cast<const __half *>(k_cache), valid_len,
+                              reinterpret_cast<__half *>(meta), page_begin, page_end, ctx);
+}
+
+int quest_score_pages(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *meta,
+                      const int32_t *valid_len, float *scores, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(meta) || !aligned16(valid_len) || !aligned16(scores))
+        return GQAQ_ERR_INVALID_ARG;
+    const int64_t pmax = (dims->max_len + dims->page_size - 1) / dims->page_size;
+    if ((int64_t)dims->batch * dims->num_kv_heads * pmax > (int64_t)INT32_MAX - 1024) return GQAQ_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_score_pages(dims, reinterpret_cast<const __half *>(q), reinterpret_cast<const __half *>(meta),
+                              valid_len, scores, ctx);
+}
+
+int quest_topk_pages(const gqaq_dims *dims, const float *scores, const int32_t *valid_len, int k,
+                     int32_t *page_idx, void *workspace, size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(scores) || !aligned16(valid_len) || !aligned16(page_idx)) return GQAQ_ERR_INVALID_ARG;
+    if (k < 1 || k > 65536) return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_topk_pages(dims, scores, valid_len, k, page_idx, ctx);
+}
+
+int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
+                      const gqaq_half *v_cache, const int32_t *valid_len, const int32_t *page_idx, int k,
+                      float scale, gqaq_half *out, void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        !aligned16(valid_len) || !aligned16(page_idx))
+        return GQAQ_ERR_INVALID_ARG;
+    if (k < 1 || k > 65536) return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return GQAQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace)) return GQAQ_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    AttnArgs a;
+    a.dims = dims;
+    a.q = reinterpret_cast<const __half *>(q);
+    a.k_cache = reinterpret_cast<const __half *>(k_cache);
+    a.v_cache = reinterpret_cast<const __half *>(v_cache);
+    a.valid_len = valid_len;
+    a.page_idx = page_idx;
+    a.kpages = k;
+    a.scale = scale;
+    a.out = reinterpret_cast<__half *>(out);
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launch_attention(a, ctx);
+}
+
+}  // extern "C"

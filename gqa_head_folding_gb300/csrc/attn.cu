@@ -1,0 +1,737 @@
+// attn.cu -- split-context decode attention with folded query heads.
+//
+// "Core ML Decode Optimization: Removing the 1.9 GiB Per-Token Copy Caused by
+// GQA repeat_kv", section 3 ("Fold Q Instead of Expanding KV"): the G query
+// rows that share a KV head are handled together as a [G, D] block, so each K
+// and V row is read from HBM once and used for all G rows. No replica of K or
+// V is made. Scale, mask and softmax act per row and along the context axis.
+// prob @ V acts per row. So the context can be split across CTAs and merged
+// with a log-sum-exp combine.
+//
+// "Quest: Query-Aware Sparsity ..." (review), flowchart: the sparse variant
+// reads only the K/V rows of the selected pages. It is the same kernel with
+// the tile rows taken from a page list instead of a contiguous range.
+//
+// Kernel shape (one persistent CTA per resident slot):
+//  - work tiles: 128 consecutive tokens (dense) or 8 selected pages of 16
+//    tokens (sparse) of one (sequence, KV head) unit. The tiles of all units
+//    are split into equal contiguous ranges, one per CTA (balanced split).
+//  - warp 8 (producer): TMA 2-D tile loads of K (128-byte swizzled) and V
+//    into a 2-3 stage shared-memory ring, with mbarrier completion.
+//  - warps 0-7 (consumers): warp w owns 16 tokens of each tile. Two lanes share
+//    a token for q.k (each covers D/2 channels with fp16 x fp16 -> fp32
+//    FMAs), then online softmax in the log2 domain. For p @ V, lane l owns D/32
+//    output channels of all G rows.
+//  - at the end of each unit segment the 8 warp states merge in shared
+//    memory. A segment that covers its whole unit writes the fp16 output. A
+//    segment cut by the range boundary writes an fp32 partial (m, l, acc),
+//    which attn_combine_kernel merges.
+#include <math.h>
+
+#include "internal.h"
+
+namespace gqaq {
+
+template <int D, int G>
+struct AttnCfg {
+    static constexpr int NCW = 8;                 // consumer warps
+    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int TILE = 128;              // tokens per stage (8 pages when sparse)
+    static constexpr int SUB = 16;                // tokens per consumer warp
+    static constexpr int KH = D / 64;             // 128-byte column blocks per K row
+    static constexpr int KBLK = TILE * 128;       // bytes of one K column block
+    static constexpr int KBYTES = KH * KBLK;      // = TILE * D * 2
+    static constexpr int VBYTES = TILE * D * 2;
+    static constexpr int STAGE = KBYTES + VBYTES;
+    static constexpr int QBYTES = G * D * 2;
+    static constexpr int MERGE = NCW * G * (D + 2) * 4;
+    static constexpr int PBYTES = NCW * SUB * G * 4;
+    static constexpr int MISC = 256;
+    static constexpr int FIXED = QBYTES + MERGE + PBYTES + MISC;
+    static constexpr int NSTAGE = (3 * STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2;
+    static constexpr int SMEM = 1024 + NSTAGE * STAGE + FIXED;
+    static constexpr int LPT = 4;                 // lanes sharing one token in q.k
+    static constexpr int TPP = 32 / LPT;          // tokens per lane pass (8)
+    static constexpr int NTL = SUB / TPP;         // tokens per lane (2)
+    static constexpr int DQ = D / LPT;            // channels per lane in q.k
+    static constexpr int NCH = DQ / 8;            // 16-byte chunks per lane in q.k
+    static constexpr int DPL = D / 32;            // channels per lane in p @ V
+    static constexpr bool QREG = (G * D <= 512);  // q block held in registers
+    static constexpr int GQ = QREG ? G : 4;       // query rows per q.k pass
+    static constexpr int NPASS = G / GQ;
+    static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
+};
+
+struct AttnParams {
+    const __half *q;
+    const int *valid_len;
+    const int *page_idx;
+    __half *out;
+    float *part;     // [grid][2][G][D+2]
+    int *status;
+    int B, Hkv, Lmax, kpages, S;
+    float scale_log2;
+    uint64_t timeout_ns;
+    int test_stall;
+};
+
+struct Sched {
+    int64_t t_begin, t_end, off_b;
+    int b;
+    int abort;
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Walk over the unit segments of one CTA's tile range.
+struct Walk {
+    int b, kv, local, tiles_b;
+    int64_t remaining;
+    bool first;
+    __device__ __forceinline__ void init(const Sched &s, const int *valid_len, int Hkv,
+                                         const TileRule &rule) {
+        b = s.b;
+        tiles_b = rule.tiles(valid_len[b]);
+        const int64_t rel = s.t_begin - s.off_b;
+        kv = (int)(rel / tiles_b);
+        local = (int)(rel % tiles_b);
+        remaining = s.t_end - s.t_begin;
+        first = true;
+        (void)Hkv;
+    }
+    __device__ __forceinline__ int seg_len() const {
+        const int64_t r = tiles_b - local;
+        return (int)(r < remaining ? r : remaining);
+    }
+    // Move past a segment of n tiles; returns false when the range is done.
+    __device__ __forceinline__ bool next(int n, const int *valid_len, int B, int Hkv,
+                                         const TileRule &rule) {
+        remaining -= n;
+        first = false;
+        if (remaining <= 0) return false;
+        local = 0;
+        if (++kv == Hkv) {
+            kv = 0;
+            do {
+                ++b;
+                tiles_b = (b < B) ? rule.tiles(valid_len[b]) : 1;
+            } while (b < B && tiles_b == 0);
+            if (b >= B) return false;
+        }
+        return true;
+    }
+};
+
+template <int D, int G, bool SPARSE>
+__global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLOCKS)
+    attn_partial_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+    using C = AttnCfg<D, G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stages = smem;
+    __half *q_s = reinterpret_cast<__half *>(stages + C::NSTAGE * C::STAGE);
+    float *merge = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(q_s) + C::QBYTES);
+    float *pbuf = merge + C::NCW * G * (D + 2);
+    uint64_t *full = reinterpret_cast<uint64_t *>(pbuf + C::NCW * C::SUB * G);
+    uint64_t *empty = full + C::NSTAGE;
+    Sched *sched = reinterpret_cast<Sched *>(empty + C::NSTAGE);
+    volatile int *abort_flag = &sched->abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int Hq = p.Hkv * G;
+
+    TileRule rule;
+    rule.sparse = SPARSE ? 1 : 0;
+    rule.lmax = p.Lmax;
+    rule.page_size = p.S;
+    rule.kpages = p.kpages;
+    rule.tile_tokens = C::TILE;
+    rule.pages_per_tile = C::NCW;
+
+    if (warp == C::NCW) {
+        int64_t T, off_b;
+        int b;
+        locate_tile(p.valid_len, p.B, p.Hkv, rule, 0, T, b, off_b);  // T
+        const int64_t tb = tile_begin(blockIdx.x, T, gridDim.x);
+        const int64_t te = tile_begin(blockIdx.x + 1, T, gridDim.x);
+        if (tb < te) locate_tile(p.valid_len, p.B, p.Hkv, rule, tb, T, b, off_b);
+        if (lane == 0) {
+            sched->t_begin = tb;
+            sched->t_end = te;
+            sched->off_b = off_b;
+            sched->b = b;
+            sched->abort = 0;
+            for (int s = 0; s < C::NSTAGE; ++s) {
+                mbar_init(smem_u32(&full[s]), 1);
+                mbar_init(smem_u32(&empty[s]), C::NCW);
+            }
+            fence_mbar_init();
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+        }
+    }
+    __syncthreads();
+    if (sched->t_begin >= sched->t_end) return;
+
+    if (warp == C::NCW) {
+        // ------------------------------------------------------------------
+        // Producer warp
+        // ------------------------------------------------------------------
+        if (p.test_stall) return;  // issue nothing: every consumer wait runs out
+        const uint64_t pol = l2_policy_evict_first();
+        Walk w;
+        w.init(*sched, p.valid_len, p.Hkv, rule);
+        int i = 0;
+        bool failed = false;
+        do {
+            const int n = w.seg_len();
+            const int unit = w.b * p.Hkv + w.kv;
+            const int row0 = unit * p.Lmax;
+            const int len = clamp_len(p.valid_len[w.b], p.Lmax);
+            const int P = (len + p.S - 1) / p.S;
+            const int nsel = P < p.kpages ? P : p.kpages;
+            for (int t = 0; t < n; ++t, ++i) {
+                const int s = i % C::NSTAGE;
+                const uint32_t ph = (uint32_t)(i / C::NSTAGE) & 1u;
+                if (i >= C::NSTAGE) {
+                    bool ok = true;
+                    if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.timeout_ns, abort_flag);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        failed = true;
+                        break;
+                    }
+                }
+                const uint32_t kdst = smem_u32(stages + s * C::STAGE);
+                const uint32_t vdst = kdst + C::KBYTES;
+                const uint32_t fb = smem_u32(&full[s]);
+                const int local = w.local + t;
+                if (SPARSE) {
+                    const int e = local * C::NCW + lane;
+                    int page = -1;
+                    if (lane < C::NCW && e < nsel) page = p.page_idx[(int64_t)unit * p.kpages + e];
+                    const bool ok = lane < C::NCW && e < nsel && page >= 0 && page < P;
+                    if (lane < C::NCW && e < nsel && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
+                    const unsigned m = __ballot_sync(0xffffffffu, ok);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(C::SUB * D * 2 * 2));
+#pragma unroll
+                    for (int j = 0; j < C::NCW; ++j) {
+                        const int pj = __shfl_sync(0xffffffffu, page, j);
+                        if (lane == 0 && ((m >> j) & 1u)) {
+                            const int y = row0 + pj * p.S;
+#pragma unroll
+                            for (int kh = 0; kh < C::KH; ++kh)
+                                tma_load_2d(kdst + kh * C::KBLK + j * C::SUB * 128, &kmap, 64 * kh, y, fb, pol);
+                            tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
+                        }
+                    }
+                } else {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
+                        const int y = row0 + local * C::TILE;
+#pragma unroll
+                        for (int kh = 0; kh < C::KH; ++kh)
+                            tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
+                        tma_load_2d(vdst, &vmap, 0, y, fb, pol);
+                    }
+                }
+            }
+            if (failed) break;
+        } while (w.next(w.seg_len(), p.valid_len, p.B, p.Hkv, rule));
+        if (failed) {
+            // Let every copy already issued land before this CTA may retire.
+            if (lane == 0) {
+                raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                *abort_flag = 1;
+                const int first = i - C::NSTAGE > 0 ? i - C::NSTAGE : 0;
+                for (int it = first; it < i; ++it)
+                    mbar_wait(smem_u32(&full[it % C::NSTAGE]), (uint32_t)(it / C::NSTAGE) & 1u,
+                              p.timeout_ns, nullptr);
+            }
+            __syncwarp();
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------------------
+    // Consumer warps
+    // ----------------------------------------------------------------------
+    const int cw = warp;
+    const int part = lane / C::TPP;  // which D/4 channel slice this lane covers in q.k
+    const int jt = lane % C::TPP;    // this lane handles tokens jt and jt + 8 of the sub-tile
+    const int tid = threadIdx.x;     // 0..255 among consumers
+    // q.k chunk addressing inside a swizzled 128-byte K row. Rows jt and jt+8
+    // share (row & 7) = jt, so one XOR key serves both tokens.
+    const int c0 = part * C::DQ;
+    const uint32_t krow_off = (uint32_t)((c0 / 64) * C::KBLK + (cw * C::SUB + jt) * 128);
+    const uint32_t kx0 = (uint32_t)(((c0 % 64) / 8) ^ jt);
+    const uint32_t pb_warp = smem_u32(pbuf + cw * C::SUB * G);
+
+    Walk w;
+    w.init(*sched, p.valid_len, p.Hkv, rule);
+    int i = 0;
+    do {
+        const int n = w.seg_len();
+        const bool complete = (w.local == 0 && n == w.tiles_b);
+        const int slot = w.first ? 0 : 1;
+        const int unit = w.b * p.Hkv + w.kv;
+        const int len = clamp_len(p.valid_len[w.b], p.Lmax);
+        const int P = (len + p.S - 1) / p.S;
+        const int nsel = P < p.kpages ? P : p.kpages;
+        const __half *qg = p.q + ((int64_t)w.b * Hq + (int64_t)w.kv * G) * D;
+
+        uint4 qr[C::GQ][C::NCH];
+        if (C::QREG) {
+#pragma unroll
+            for (int g = 0; g < C::GQ; ++g)
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c)
+                    qr[g][c] = *reinterpret_cast<const uint4 *>(qg + g * D + c0 + c * 8);
+        } else {
+            for (int e = tid; e < G * D / 8; e += C::NCW * 32)
+                reinterpret_cast<uint4 *>(q_s)[e] = reinterpret_cast<const uint4 *>(qg)[e];
+            named_bar_sync(1, C::NCW * 32);
+        }
+
+        float m[G], l[G], acc[G][C::DPL];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < C::DPL; ++e) acc[g][e] = 0.f;
+        }
+
+        for (int t = 0; t < n; ++t, ++i) {
+            const int s = i % C::NSTAGE;
+            const uint32_t ph = (uint32_t)(i / C::NSTAGE) & 1u;
+            bool ok = (*abort_flag == 0);
+            if (ok) {
+                if (lane == 0) ok = mbar_wait(smem_u32(&full[s]), ph, p.timeout_ns, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok && lane == 0) {
+                    raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+            }
+            const int local = w.local + t;
+            int nvalid = 0;
+            if (SPARSE) {
+                const int e = local * C::NCW + cw;
+                if (e < nsel) {
+                    const int page = p.page_idx[(int64_t)unit * p.kpages + e];
+                    if (page >= 0 && page < P) {
+                        const int rem = len - page * p.S;
+                        nvalid = rem < C::SUB ? rem : C::SUB;
+                    }
+                }
+            } else {
+                const int rem = len - (local * C::TILE + cw * C::SUB);
+                nvalid = rem < 0 ? 0 : (rem < C::SUB ? rem : C::SUB);
+            }
+            if (ok && nvalid > 0) {
+                const uint32_t kbase = smem_u32(stages + s * C::STAGE);
+                const uint32_t vbase = kbase + C::KBYTES;
+                // ---- scores: q . k, this lane's D/4 channels of tokens jt, jt+8 ----
+                float sc[C::NTL][G];
+#pragma unroll
+                for (int pass = 0; pass < C::NPASS; ++pass) {
+                    if (!C::QREG) {
+#pragma unroll
+                        for (int g = 0; g < C::GQ; ++g)
+#pragma unroll
+                            for (int c = 0; c < C::NCH; ++c)
+                                qr[g][c] = lds128(smem_u32(q_s + (pass * C::GQ + g) * D + c0 + c * 8));
+                    }
+#pragma unroll
+                    for (int u = 0; u < C::NTL; ++u) {
+                        float a0[C::GQ], a1[C::GQ];
+#pragma unroll
+                        for (int g = 0; g < C::GQ; ++g) a0[g] = a1[g] = 0.f;
+                        const uint32_t kro = kbase + krow_off + (uint32_t)(u * C::TPP * 128);
+#pragma unroll
+                        for (int c = 0; c < C::NCH; ++c) {
+                            const uint4 kc = lds128(kro + ((kx0 ^ (uint32_t)c) << 4));
+#pragma unroll
+                            for (int g = 0; g < C::GQ; ++g) {
+                                a0[g] = fma_h_lo(qr[g][c].x, kc.x, a0[g]);
+                                a1[g] = fma_h_hi(qr[g][c].x, kc.x, a1[g]);
+                                a0[g] = fma_h_lo(qr[g][c].y, kc.y, a0[g]);
+                                a1[g] = fma_h_hi(qr[g][c].y, kc.y, a1[g]);
+                                a0[g] = fma_h_lo(qr[g][c].z, kc.z, a0[g]);
+                                a1[g] = fma_h_hi(qr[g][c].z, kc.z, a1[g]);
+                                a0[g] = fma_h_lo(qr[g][c].w, kc.w, a0[g]);
+                                a1[g] = fma_h_hi(qr[g][c].w, kc.w, a1[g]);
+                            }
+                        }
+#pragma unroll
+                        for (int g = 0; g < C::GQ; ++g) sc[u][pass * C::GQ + g] = a0[g] + a1[g];
+                    }
+                }
+                // ---- online softmax over the 16 tokens (log2 domain) ----
+                float tmax[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) tmax[g] = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < C::NTL; ++u) {
+                    const bool valid = jt + u * C::TPP < nvalid;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float x = sc[u][g];
+#pragma unroll
+                        for (int o = C::TPP; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                        sc[u][g] = valid ? x * p.scale_log2 : -INFINITY;
+                        tmax[g] = fmaxf(tmax[g], sc[u][g]);
+                    }
+                }
+#pragma unroll
+                for (int o = C::TPP / 2; o > 0; o >>= 1)
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        tmax[g] = fmaxf(tmax[g], __shfl_xor_sync(0xffffffffu, tmax[g], o));
+                float pg[C::NTL][G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float mnew = fmaxf(m[g], tmax[g]);
+                    const float alpha = fast_exp2(m[g] - mnew);
+                    float psum = 0.f;
+#pragma unroll
+                    for (int u = 0; u < C::NTL; ++u) {
+                        pg[u][g] = fast_exp2(sc[u][g] - mnew);
+                        psum += pg[u][g];
+                    }
+                    l[g] = l[g] * alpha + (part == 0 ? psum : 0.f);
+                    m[g] = mnew;
+#pragma unroll
+                    for (int e = 0; e < C::DPL; ++e) acc[g][e] *= alpha;
+                }
+                if (part == 0) {
+#pragma unroll
+                    for (int u = 0; u < C::NTL; ++u) {
+                        float *dst = pbuf + (cw * C::SUB + jt + u * C::TPP) * G;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) dst[g] = pg[u][g];
+                    }
+                }
+                __syncwarp();
+                // ---- acc += p @ V (lane owns D/32 channels of all G rows) ----
+#pragma unroll 4
+                for (int jj = 0; jj < nvalid; ++jj) {
+                    {
+                        float pj[G];
+                        const uint32_t pa = pb_warp + (uint32_t)(jj * G * 4);
+                        if (G == 8) {
+                            const uint4 x0 = lds128(pa), x1 = lds128(pa + 16);
+                            const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                            for (int g = 0; g < G; ++g) pj[g] = __uint_as_float(xs[g]);
+                        } else if (G == 4) {
+                            const uint4 x = lds128(pa);
+                            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int g = 0; g < G; ++g) pj[g] = __uint_as_float(xs[g]);
+                        } else if (G == 2) {
+                            const uint2 x = lds64(pa);
+                            pj[0] = __uint_as_float(x.x);
+                            pj[G - 1] = __uint_as_float(x.y);
+                        } else {
+                            pj[0] = __uint_as_float(lds32(pa));
+                        }
+                        const int row = cw * C::SUB + jj;
+                        float vf[C::DPL];
+                        if (D == 128) {
+                            const uint2 vv = lds64(vbase + (uint32_t)(row * D * 2 + lane * 8));
+                            const float2 f0 = half2_bits_to_float2(vv.x);
+                            const float2 f1 = half2_bits_to_float2(vv.y);
+                            vf[0] = f0.x; vf[1] = f0.y; vf[C::DPL > 2 ? 2 : 0] = f1.x; vf[C::DPL > 3 ? 3 : 0] = f1.y;
+                        } else {
+                            const float2 f0 = half2_bits_to_float2(lds32(vbase + (uint32_t)(row * D * 2 + lane * 4)));
+                            vf[0] = f0.x; vf[C::DPL > 1 ? 1 : 0] = f0.y;
+                        }
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+#pragma unroll
+                            for (int e = 0; e < C::DPL; ++e) acc[g][e] = fmaf(pj[g], vf[e], acc[g][e]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        }
+
+        // ---- merge the 8 warp states of this segment ----
+#pragma unroll
+        for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
+        float *mw = merge + cw * G * (D + 2);
+        if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                mw[g * (D + 2)] = m[g];
+                mw[g * (D + 2) + 1] = l[g];
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < C::DPL; ++e) mw[g * (D + 2) + 2 + lane * C::DPL + e] = acc[g][e];
+        named_bar_sync(1, C::NCW * 32);
+        for (int idx = tid; idx < G * D; idx += C::NCW * 32) {
+            const int g = idx / D, d = idx - (idx / D) * D;
+            float mst = -INFINITY;
+#pragma unroll
+            for (int ww = 0; ww < C::NCW; ++ww) mst = fmaxf(mst, merge[(ww * G + g) * (D + 2)]);
+            float ls = 0.f, as = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < C::NCW; ++ww) {
+                const float* st = merge + (ww * G + g) * (D + 2);
+                if (st[0] != -INFINITY) {
+                    const float f = fast_exp2(st[0] - mst);
+                    ls += f * st[1];
+                    as += f * st[2 + d];
+                }
+            }
+            if (complete) {
+                p.out[((int64_t)w.b * Hq + (int64_t)w.kv * G + g) * D + d] =
+                    __float2half_rn(ls > 0.f ? as / ls : 0.f);
+            } else {
+                float *ps = p.part + (((int64_t)blockIdx.x * 2 + slot) * G + g) * (D + 2);
+                ps[2 + d] = as;
+                if (d == 0) {
+                    ps[0] = mst;
+                    ps[1] = ls;
+                }
+            }
+        }
+        named_bar_sync(1, C::NCW * 32);
+    } while (w.next(w.seg_len(), p.valid_len, p.B, p.Hkv, rule));
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp combine of the partials of units that were split across CTAs:
+//   out_g = sum_c 2^(m_c - m*) acc_c / sum_c 2^(m_c - m*) l_c,  m* = max_c m_c.
+// One CTA per (KV head, sequence).
+// ---------------------------------------------------------------------------
+struct CombineParams {
+    const int *valid_len;
+    const float *part;
+    __half *out;
+    int *status;
+    int B, Hkv, Lmax, kpages, S;
+    int sparse, tile_tokens, pages_per_tile;
+    int grid;  // grid of the partial kernel
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
+    const int kv = blockIdx.x, b = blockIdx.y;
+    TileRule rule;
+    rule.sparse = p.sparse;
+    rule.lmax = p.Lmax;
+    rule.page_size = p.S;
+    rule.kpages = p.kpages;
+    rule.tile_tokens = p.tile_tokens;
+    rule.pages_per_tile = p.pages_per_tile;
+
+    __shared__ long long red_tot[4], red_before[4];
+    long long tot = 0, before = 0;
+    for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
+        const long long n = (long long)p.Hkv * rule.tiles(p.valid_len[bb]);
+        tot += n;
+        if (bb < b) before += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red_tot[threadIdx.x >> 5] = tot;
+        red_before[threadIdx.x >> 5] = before;
+    }
+    __syncthreads();
+    const int64_t T = red_tot[0] + red_tot[1] + red_tot[2] + red_tot[3];
+    const int64_t off_b = red_before[0] + red_before[1] + red_before[2] + red_before[3];
+
+    const int raw = p.valid_len[b];
+    if (threadIdx.x == 0 && kv == 0 && (raw < 1 || raw > p.Lmax)) raise_flag(p.status, GQAQ_DEV_BAD_LEN);
+    const int tiles_b = rule.tiles(raw);
+    const int Hq = p.Hkv * G;
+    __half *outg = p.out + ((int64_t)b * Hq + (int64_t)kv * G) * D;
+    if (tiles_b == 0) {  // no valid token: defined as a zero output
+        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) outg[idx] = __float2half_rn(0.f);
+        return;
+    }
+    const int64_t o = off_b + (int64_t)kv * tiles_b;
+    const int64_t grid = p.grid;
+    const int64_t c_lo = tile_owner(o, T, grid);
+    const int64_t c_hi = tile_owner(o + tiles_b - 1, T, grid);
+    if (c_lo == c_hi) return;  // written directly by the partial kernel
+    const int slot_lo = (tile_begin(c_lo, T, grid) == o) ? 0 : 1;
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int g = idx / D, d = idx - (idx / D) * D;
+        float mst = -INFINITY;
+        for (int64_t c = c_lo; c <= c_hi; ++c) {
+            if (tile_begin(c, T, grid) == tile_begin(c + 1, T, grid)) continue;
+            const int slot = (c == c_lo) ? slot_lo : 0;
+            mst = fmaxf(mst, p.part[((c * 2 + slot) * G + g) * (D + 2)]);
+        }
+        float ls = 0.f, as = 0.f;
+        for (int64_t c = c_lo; c <= c_hi; ++c) {
+            if (tile_begin(c, T, grid) == tile_begin(c + 1, T, grid)) continue;
+            const int slot = (c == c_lo) ? slot_lo : 0;
+            const float *ps = p.part + ((c * 2 + slot) * G + g) * (D + 2);
+            if (ps[0] != -INFINITY) {
+                const float f = fast_exp2(ps[0] - mst);
+                ls += f * ps[1];
+                as += f * ps[2 + d];
+            }
+        }
+        outg[idx] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+template <int D, int G, bool SPARSE>
+int grid_for(const LaunchCtx &ctx) {
+    using C = AttnCfg<D, G>;
+    static int occ[kMaxDevices] = {0};
+    if (ctx.device < 0 || ctx.device >= kMaxDevices) return -1;
+    if (occ[ctx.device] == 0) {
+        auto kern = attn_partial_kernel<D, G, SPARSE>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM) != cudaSuccess || n < 1)
+            return -1;
+        occ[ctx.device] = n;
+    }
+    int grid = occ[ctx.device] * ctx.num_sms;
+    if (ctx.max_ctas > 0 && ctx.max_ctas < grid) grid = ctx.max_ctas;
+    return grid;
+}
+
+template <int D, int G, bool SPARSE>
+int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
+    using C = AttnCfg<D, G>;
+    const gqaq_dims &dm = *a.dims;
+    const int grid = grid_for<D, G, SPARSE>(ctx);
+    if (grid < 1) return GQAQ_ERR_CUDA;
+    const size_t need = (size_t)grid * 2 * G * (D + 2) * sizeof(float);
+    if (a.workspace == nullptr || a.workspace_bytes < need) return GQAQ_ERR_WORKSPACE;
+
+    const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
+    const uint32_t box_rows = SPARSE ? (uint32_t)C::SUB : (uint32_t)C::TILE;
+    CUtensorMap kmap, vmap;
+    if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, box_rows, false)) return GQAQ_ERR_CUDA;
+
+    AttnParams p;
+    p.q = a.q;
+    p.valid_len = a.valid_len;
+    p.page_idx = a.page_idx;
+    p.out = a.out;
+    p.part = reinterpret_cast<float *>(a.workspace);
+    p.status = ctx.status;
+    p.B = dm.batch;
+    p.Hkv = dm.num_kv_heads;
+    p.Lmax = dm.max_len;
+    p.kpages = SPARSE ? a.kpages : 1;
+    p.S = SPARSE ? dm.page_size : 16;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.timeout_ns = ctx.timeout_ns;
+    p.test_stall = ctx.test_stall;
+    attn_partial_kernel<D, G, SPARSE><<<grid, C::THREADS, C::SMEM, ctx.stream>>>(kmap, vmap, p);
+    if (cudaGetLastError() != cudaSuccess) return GQAQ_ERR_CUDA;
+
+    CombineParams cp;
+    cp.valid_len = a.valid_len;
+    cp.part = p.part;
+    cp.out = a.out;
+    cp.status = ctx.status;
+    cp.B = dm.batch;
+    cp.Hkv = dm.num_kv_heads;
+    cp.Lmax = dm.max_len;
+    cp.kpages = p.kpages;
+    cp.S = p.S;
+    cp.sparse = SPARSE ? 1 : 0;
+    cp.tile_tokens = C::TILE;
+    cp.pages_per_tile = C::NCW;
+    cp.grid = grid;
+    attn_combine_kernel<D, G><<<dim3(dm.num_kv_heads, dm.batch), 128, 0, ctx.stream>>>(cp);
+    if (cudaGetLastError() != cudaSuccess) return GQAQ_ERR_CUDA;
+    return GQAQ_OK;
+}
+
+template <int D, int G>
+int dispatch_sparse(const AttnArgs &a, const LaunchCtx &ctx) {
+    return a.page_idx ? launch_t<D, G, true>(a, ctx) : launch_t<D, G, false>(a, ctx);
+}
+
+template <int D>
+int dispatch_g(const AttnArgs &a, const LaunchCtx &ctx, int G) {
+    switch (G) {
+        case 1: return dispatch_sparse<D, 1>(a, ctx);
+        case 2: return dispatch_sparse<D, 2>(a, ctx);
+        case 4: return dispatch_sparse<D, 4>(a, ctx);
+        case 8: return dispatch_sparse<D, 8>(a, ctx);
+        default: return GQAQ_ERR_UNSUPPORTED;
+    }
+}
+
+template <int D, int G>
+size_t ws_t(const LaunchCtx &ctx) {
+    const int g0 = grid_for<D, G, false>(ctx);
+    const int g1 = grid_for<D, G, true>(ctx);
+    if (g0 < 1 || g1 < 1) return 0;
+    const int grid = g0 > g1 ? g0 : g1;
+    return (size_t)grid * 2 * G * (D + 2) * sizeof(float);
+}
+
+template <int D>
+size_t ws_g(const LaunchCtx &ctx, int G) {
+    switch (G) {
+        case 1: return ws_t<D, 1>(ctx);
+        case 2: return ws_t<D, 2>(ctx);
+        case 4: return ws_t<D, 4>(ctx);
+        case 8: return ws_t<D, 8>(ctx);
+        default: return 0;
+    }
+}
+
+}  // namespace
+
+int launch_attention(const AttnArgs &a, const LaunchCtx &ctx) {
+    const int G = a.dims->num_q_heads / a.dims->num_kv_heads;
+    switch (a.dims->head_dim) {
+        case 64: return dispatch_g<64>(a, ctx, G);
+        case 128: return dispatch_g<128>(a, ctx, G);
+        default: return GQAQ_ERR_UNSUPPORTED;
+    }
+}
+
+size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx) {
+    const int G = dims->num_q_heads / dims->num_kv_heads;
+    switch (dims->head_dim) {
+        case 64: return ws_g<64>(ctx, G);
+        case 128: return ws_g<128>(ctx, G);
+        default: return 0;
+    }
+}
+
+}  // namespace gqaq

@@ -1,0 +1,51 @@
+// internal.h -- host-side interfaces between the C-ABI layer (abi.cu) and the
+// kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gqaq.h"
+#include "common.cuh"
+
+namespace gqaq {
+
+// Encodes a 2-D fp16 tensor map: rows x cols (cols innermost), box of
+// box_cols x box_rows, 128-byte swizzle or none. Returns false on failure.
+bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                          uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+
+// Dense (page_idx == nullptr) or sparse split-context attention + combine.
+struct AttnArgs {
+    const gqaq_dims *dims;
+    const __half *q;
+    const __half *k_cache;
+    const __half *v_cache;
+    const int *valid_len;
+    const int *page_idx;  // sparse only
+    int kpages;           // sparse only
+    float scale;
+    __half *out;
+    void *workspace;
+    size_t workspace_bytes;
+};
+int launch_attention(const AttnArgs &a, const LaunchCtx &ctx);
+size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx);
+
+// Quest kernels.
+int launch_append_kv(const gqaq_dims *dims, __half *k_cache, __half *v_cache, __half *meta,
+                     const __half *k_new, const __half *v_new, const int *pos, const LaunchCtx &ctx);
+int launch_update_meta(const gqaq_dims *dims, const __half *k_cache, const int *valid_len,
+                       __half *meta, int page_begin, int page_end, const LaunchCtx &ctx);
+int launch_score_pages(const gqaq_dims *dims, const __half *q, const __half *meta,
+                       const int *valid_len, float *scores, const LaunchCtx &ctx);
+int launch_topk_pages(const gqaq_dims *dims, const float *scores, const int *valid_len, int k,
+                      int *page_idx, const LaunchCtx &ctx);
+
+// Largest Pmax the top-K kernel keeps in shared memory.
+constexpr int kTopkMaxPages = 32768;
+
+}  // namespace gqaq

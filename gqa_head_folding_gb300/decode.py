@@ -1,0 +1,87 @@
+"""One decode step over a stack of attention layers, through the C ABI.
+
+Layer policy ("Quest: Query-Aware Sparsity ..." review, the note that the
+first two attention layers keep full attention): layers with index below
+``dense_layers`` run dense folded-GQA attention over every valid token.
+Later layers run the Quest path: score every page from its key min/max,
+pick the top ``k_pages``, and attend over those pages only. When a step
+carries a new token, every layer first appends it (``quest_append_kv``), so
+each layer's page metadata stays current whatever path reads it.
+
+This module only sequences library calls and owns the scratch buffers they
+share. Every arithmetic step runs in the CUDA kernels.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional
+
+import torch
+
+from . import (alloc_workspace, gqa_decode_attn, make_dims, new_meta, num_pages, quest_append_kv,
+               quest_score_pages, quest_sparse_attn, quest_topk_pages, quest_update_meta)
+
+
+@dataclasses.dataclass
+class Layer:
+    """Device tensors of one attention layer for one step."""
+    q: torch.Tensor                       # [B,Hq,D] fp16
+    k_cache: torch.Tensor                 # [B,Hkv,Lmax,D] fp16
+    v_cache: torch.Tensor
+    valid_len: torch.Tensor               # [B] int32 (tokens attended after the append)
+    out: torch.Tensor                     # [B,Hq,D] fp16
+    meta: Optional[torch.Tensor] = None   # [B,Hkv,Pmax,2,D] fp16 (Quest layers / appends)
+    k_new: Optional[torch.Tensor] = None  # [B,Hkv,D] fp16
+    v_new: Optional[torch.Tensor] = None
+    pos: Optional[torch.Tensor] = None    # [B] int32 row the new token goes to
+
+
+class DecodeStack:
+    def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_len: int,
+                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16):
+        self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
+        self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
+        self.k_pages, self.dense_layers = k_pages, dense_layers
+        self.scale = 1.0 / math.sqrt(head_dim)
+        self.device = torch.device(device)
+        dims = make_dims(batch, num_q_heads, num_kv_heads, head_dim, max_len, page_size)
+        self.workspace = alloc_workspace(dims, self.device)
+        pmax = num_pages(max_len, page_size)
+        self.scores = torch.empty(batch, num_kv_heads, pmax, dtype=torch.float32, device=self.device)
+        self.page_idx = (torch.empty(batch, num_kv_heads, k_pages, dtype=torch.int32, device=self.device)
+                         if k_pages else None)
+
+    def is_dense(self, layer: int) -> bool:
+        return self.k_pages is None or layer < self.dense_layers
+
+    def new_meta(self) -> torch.Tensor:
+        return new_meta(self.batch, self.num_kv_heads, self.max_len, self.head_dim, self.device,
+                        self.page_size)
+
+    def build_meta(self, layer: Layer, valid_len: torch.Tensor):
+        """Metadata of the pages already in the cache (after a prefill)."""
+        quest_update_meta(layer.k_cache, valid_len, layer.meta, page_size=self.page_size)
+
+    def launches_per_step(self, num_layers: int, append: bool) -> int:
+        """Kernels one step launches (append 1, dense 2, Quest 4)."""
+        n = 0
+        for i in range(num_layers):
+            n += 1 if append else 0
+            n += 2 if self.is_dense(i) else 4
+        return n
+
+    def step(self, layers: List[Layer]):
+        for i, L in enumerate(layers):
+            if L.k_new is not None:
+                quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos, self.page_size)
+            if self.is_dense(i):
+                gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale, out=L.out,
+                                workspace=self.workspace)
+            else:
+                quest_score_pages(L.q, L.meta, L.valid_len, self.max_len, scores=self.scores,
+                                  page_size=self.page_size)
+                quest_topk_pages(self.scores, L.valid_len, self.k_pages, self.max_len,
+                                 page_idx=self.page_idx, page_size=self.page_size)
+                quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.page_idx, self.scale,
+                                  out=L.out, workspace=self.workspace, page_size=self.page_size)

@@ -1,0 +1,189 @@
+/*
+ * gqaq.h -- C ABI of the GB300 (sm_103a) decode-attention library:
+ * GQA attention with the query heads folded onto their KV heads, and Quest
+ * query-aware page sparsity on top of it.
+ *
+ * Sources (page title + section):
+ *  [OPT]   "Core ML Decode Optimization: Removing the 1.9 GiB Per-Token Copy
+ *          Caused by GQA repeat_kv" (OptAI engineering blog). Section 3, "Fold
+ *          Q Instead of Expanding KV" (the [B,Hq,1,D] -> [B,Hkv,G,D] reshape,
+ *          h = G*kv + g, the decode code with scale, additive mask, softmax over
+ *          the context axis and prob @ V). Section 5, "Query Heads Must Be
+ *          Ordered by KV Group" (the contiguous-group precondition).
+ *  [QUEST] "Quest: Query-Aware Sparsity for Efficient Long-Context LLM
+ *          Inference" (reviewer's summary). The flowchart (score pages from
+ *          min/max metadata, pick the top pages, read only their K and V,
+ *          attend). The page-score section: m_{p,i} and M_{p,i} are kept per
+ *          page and channel and updated when a key arrives, and
+ *          U(p,q) = sum_i max(q_i m_{p,i}, q_i M_{p,i}). The token-budget section
+ *          (B = K*S). The note that the first two layers stay dense.
+ *
+ * Conventions for every entry point
+ *  - Tensors are dense row-major fp16 (IEEE binary16, passed as gqaq_half
+ *    bits), int32 or fp32. Every pointer is a DEVICE pointer on the current
+ *    CUDA device, 16-byte aligned, except `dims` (host).
+ *  - The caller owns every buffer: caches, metadata, outputs and workspace.
+ *    The library never allocates device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream). They can be captured in a CUDA graph after one eager
+ *    call on the device, because that first call loads the kernels. The
+ *    return value reports host-side validation and launch errors only.
+ *  - Layouts (B = batch, Hq/Hkv query/KV heads, G = Hq/Hkv, D = head_dim,
+ *    Lmax = max_len, S = page_size, Pmax = ceil(Lmax/S)):
+ *      q, out           [B][Hq][D]     fp16 (query heads grouped: h = G*kv + g)
+ *      k_cache, v_cache [B][Hkv][Lmax][D] fp16 (one page = S consecutive rows)
+ *      meta             [B][Hkv][Pmax][2][D] fp16 (page minimum row, then maximum)
+ *      scores           [B][Hkv][Pmax] fp32
+ *      page_idx         [B][Hkv][k] int32 (ascending, -1 padded)
+ *      valid_len, pos   [B] int32
+ *  - Supported: D in {64, 128}; G in {1, 2, 4, 8}; S = 16 for the Quest calls;
+ *    B*Hkv*Lmax < 2^31. Other shapes return GQAQ_ERR_UNSUPPORTED.
+ *  - Values that live on the device are checked there. This covers valid_len
+ *    outside [1, Lmax], page indices outside [0, ceil(valid_len/S)) and pos
+ *    outside [0, Lmax). The kernels clamp or skip such values and raise a flag
+ *    in the device status word (gqaq_device_status). They never read or write
+ *    outside the buffers described here.
+ *  - Every wait inside a kernel is bounded (GQAQ_OPT_WAIT_TIMEOUT_NS). On
+ *    timeout the kernel sets GQAQ_DEV_TIMEOUT, lets its own copies in flight
+ *    land and returns. It never traps.
+ */
+#ifndef GQAQ_H
+#define GQAQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GQAQ_API __attribute__((visibility("default")))
+#else
+#define GQAQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gqaq_half; /* IEEE-754 binary16 bit pattern */
+
+typedef enum {
+    GQAQ_OK = 0,
+    GQAQ_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad dims, k < 1, ... */
+    GQAQ_ERR_UNSUPPORTED = 2, /* valid but not implemented (D, G, S, size limits) */
+    GQAQ_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    GQAQ_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
+    GQAQ_ERR_TIMEOUT = 5      /* reported by gqaq_device_status only */
+} gqaq_status;
+
+/* Device status word flags (bitwise OR), read with gqaq_device_status. */
+enum {
+    GQAQ_DEV_TIMEOUT = 1,  /* a bounded wait gave up */
+    GQAQ_DEV_BAD_LEN = 2,  /* a valid_len outside [1, Lmax] was clamped */
+    GQAQ_DEV_BAD_PAGE = 4, /* a page index outside [0, P) was skipped */
+    GQAQ_DEV_BAD_POS = 8   /* an append position outside [0, Lmax) was skipped */
+};
+
+typedef struct {
+    int batch;        /* B >= 1 */
+    int num_q_heads;  /* Hq >= 1, a multiple of Hkv */
+    int num_kv_heads; /* Hkv >= 1 */
+    int head_dim;     /* D: 64 or 128 */
+    int max_len;      /* Lmax >= 1: allocated rows per (sequence, KV head) */
+    int page_size;    /* S: 16 (Quest calls); ignored by gqa_decode_attn */
+} gqaq_dims;
+
+/* Bytes of workspace that gqa_decode_attn and quest_sparse_attn need on the
+ * current device for these dims (enough for both). The library sizes its
+ * grid from the SM count, so the figure depends on the device.
+ * `max_selected_pages` is accepted for future use and is not needed today.
+ * Returns 0 when the dims are invalid or unsupported. */
+GQAQ_API size_t gqaq_workspace_bytes(const gqaq_dims *dims, int max_selected_pages);
+
+/* [OPT] section 3: dense decode attention with the query heads folded.
+ * For every sequence b, KV head kv and group member g (h = G*kv + g):
+ *   out[b][h] = sum_{t < valid_len[b]} softmax_t(scale * q[b][h] . k[b][kv][t]) v[b][kv][t].
+ * Each KV head's K and V rows are read from HBM once for its G query rows.
+ * No repeat_kv copy is ever made. The valid-length prefix stands in for the
+ * additive context mask. fp32 accumulation; out is rounded to fp16 once
+ * (round to nearest even). The context is split across the GPU's SMs, and
+ * the split partials are combined by log-sum-exp.
+ * workspace: >= gqaq_workspace_bytes(dims, 0) bytes of device scratch. Its
+ * contents on entry do not matter. Two calls that overlap must not share it. */
+GQAQ_API int gqa_decode_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
+                    const gqaq_half *v_cache, const int32_t *valid_len, float scale,
+                    gqaq_half *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* [QUEST] page-score section: append one token per (sequence, KV head) and
+ * update its page's metadata. Writes k_new[b][kv] / v_new[b][kv] ([B][Hkv][D])
+ * to row pos[b] of the caches. For page p = pos[b] / S: if pos[b] % S == 0 the
+ * page's min and max rows become k_new, otherwise they become the elementwise
+ * min / max of their old value and k_new. Appending rows in order keeps the
+ * exact page bounds. */
+GQAQ_API int quest_append_kv(const gqaq_dims *dims, gqaq_half *k_cache, gqaq_half *v_cache,
+                    gqaq_half *meta, const gqaq_half *k_new, const gqaq_half *v_new,
+                    const int32_t *pos, void *stream);
+
+/* [QUEST] page-score section: build the metadata from the cache. For each page
+ * p in [page_begin, page_end) that holds a valid token, meta[b][kv][p] =
+ * elementwise (min, max) over rows [p*S, min(p*S+S, valid_len[b])) of
+ * k_cache[b][kv]. Pages with no valid token are left untouched.
+ * Requires 0 <= page_begin <= page_end <= Pmax. */
+GQAQ_API int quest_update_meta(const gqaq_dims *dims, const gqaq_half *k_cache, const int32_t *valid_len,
+                      gqaq_half *meta, int page_begin, int page_end, void *stream);
+
+/* [QUEST] page-score section: for every valid page p < ceil(valid_len[b]/S),
+ *   scores[b][kv][p] = max_g sum_i max(q[b][G*kv+g][i] * m_{p,i}, q[b][G*kv+g][i] * M_{p,i}),
+ * i.e. U(p,q), maximised over the KV head's G folded query rows. q is unscaled.
+ * The page ranking is the same under any positive scale. Entries for pages
+ * at or beyond P are not written. fp32 (every product of two fp16 values is
+ * exact in fp32; the sums are rounded). */
+GQAQ_API int quest_score_pages(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *meta,
+                      const int32_t *valid_len, float *scores, void *stream);
+
+/* [QUEST] token-budget section: per (b, kv), select the k pages with the
+ * largest score among the P = ceil(valid_len[b]/S) valid pages. Equal scores go
+ * to the lower page index. If P <= k, every page is selected. The selection
+ * is written to page_idx[b][kv][0..k) in ascending page order, padded with -1.
+ * Requires 1 <= k <= 65536 and Pmax <= 32768. workspace / workspace_bytes are
+ * reserved (may be NULL / 0). */
+GQAQ_API int quest_topk_pages(const gqaq_dims *dims, const float *scores, const int32_t *valid_len,
+                     int k, int32_t *page_idx, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/* [QUEST] flowchart, last two steps: attention over only the selected pages.
+ * It is the same as gqa_decode_attn, except that sequence b / KV head kv
+ * attends only to the tokens of pages page_idx[b][kv][j], for
+ * j < min(k, ceil(valid_len[b]/S)). Page p contributes its rows
+ * [p*S, min(p*S+S, valid_len[b])). Negative or out-of-range entries are
+ * skipped. Indices must be distinct. workspace: as for gqa_decode_attn. */
+GQAQ_API int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
+                      const gqaq_half *v_cache, const int32_t *valid_len, const int32_t *page_idx,
+                      int k, float scale, gqaq_half *out, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* Human-readable name of a gqaq_status value (static string). */
+GQAQ_API const char *gqaq_status_string(int status);
+
+/* Library options (process-wide, read at launch time). */
+enum {
+    GQAQ_OPT_MAX_CTAS = 1,        /* cap on the persistent grid of the attention and
+                                     score kernels; 0 = one wave of resident CTAs */
+    GQAQ_OPT_WAIT_TIMEOUT_NS = 2, /* bound on every in-kernel wait; default 2e9 */
+    GQAQ_OPT_TEST_STALL = 3       /* nonzero: the attention kernels' producer issues
+                                     no copy, so every consumer wait runs out
+                                     (exercises the timeout path; outputs undefined) */
+};
+GQAQ_API int gqaq_set_option(int option, int64_t value);
+
+/* Copy the current device's status word (GQAQ_DEV_* flags) to *flags and
+ * optionally reset it to 0. Synchronises the device. Returns GQAQ_OK, or
+ * GQAQ_ERR_TIMEOUT if the word holds GQAQ_DEV_TIMEOUT. */
+GQAQ_API int gqaq_device_status(int *flags, int reset);
+
+/* Library version: major*10000 + minor*100 + patch. */
+GQAQ_API int gqaq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQAQ_H */

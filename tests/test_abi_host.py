@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI: no GPU and no kernel launch needed.
+
+Loads libgqaq.so, checks that it exports every function include/gqaq.h
+declares, and drives the argument validation paths that return before any
+CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gqa_head_folding_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqaq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(g.LIB_PATH):
+        from gqa_head_folding_gb300 import _build
+        _build.build()
+    return g.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GQAQ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gqa_decode_attn", "quest_append_kv", "quest_update_meta", "quest_score_pages",
+                     "quest_topk_pages", "quest_sparse_attn"):
+        assert required in names
+    assert tuple(names) == g.EXPORTS
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"libgqaq.so does not export {name}"
+
+
+def test_status_strings(L):
+    assert g.status_string(0) == "GQAQ_OK"
+    assert g.status_string(g.GQAQ_ERR_WORKSPACE) == "GQAQ_ERR_WORKSPACE"
+    assert g.status_string(99) == "GQAQ_ERR_UNKNOWN"
+    assert L.gqaq_version() == 100
+
+
+FAKE = ctypes.c_void_p(0x10000)        # 16-byte aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def dims(**kw):
+    base = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=64, max_len=4096, page_size=16)
+    base.update(kw)
+    return g.make_dims(**base)
+
+
+def decode(L, d, q=FAKE, k=FAKE, v=FAKE, vl=FAKE, scale=0.125, out=FAKE, ws=FAKE, wsb=1 << 20):
+    return L.gqa_decode_attn(None if d is None else ctypes.byref(d), q, k, v, vl, scale, out, ws, wsb, None)
+
+
+def test_decode_rejects_bad_arguments(L):
+    assert decode(L, None) == g.GQAQ_ERR_INVALID_ARG
+    assert decode(L, dims(num_q_heads=30)) == g.GQAQ_ERR_INVALID_ARG      # Hq % Hkv != 0
+    assert decode(L, dims(batch=0)) == g.GQAQ_ERR_INVALID_ARG
+    assert decode(L, dims(max_len=0)) == g.GQAQ_ERR_INVALID_ARG
+    assert decode(L, dims(), q=None) == g.GQAQ_ERR_INVALID_ARG
+    assert decode(L, dims(), k=MISALIGNED) == g.GQAQ_ERR_INVALID_ARG
+    assert decode(L, dims(), vl=None) == g.GQAQ_ERR_INVALID_ARG
+    assert decode(L, dims(), scale=float("nan")) == g.GQAQ_ERR_INVALID_ARG
+    assert decode(L, dims(), ws=None) == g.GQAQ_ERR_WORKSPACE
+    assert decode(L, dims(), ws=MISALIGNED) == g.GQAQ_ERR_WORKSPACE
+
+
+def test_decode_reports_unsupported_shapes(L):
+    assert decode(L, dims(head_dim=96)) == g.GQAQ_ERR_UNSUPPORTED
+    assert decode(L, dims(num_q_heads=24, num_kv_heads=8)) == g.GQAQ_ERR_UNSUPPORTED   # G = 3
+    assert decode(L, dims(num_q_heads=128, num_kv_heads=8)) == g.GQAQ_ERR_UNSUPPORTED  # G = 16
+    assert decode(L, dims(batch=4096, num_kv_heads=8, num_q_heads=8, max_len=1 << 17)) == \
+        g.GQAQ_ERR_UNSUPPORTED                                                          # > 2^31 rows
+
+
+def test_quest_calls_reject_bad_arguments(L):
+    d = dims(head_dim=128)
+    assert L.quest_append_kv(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_append_kv(ctypes.byref(dims(page_size=8)), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == \
+        g.GQAQ_ERR_UNSUPPORTED
+    assert L.quest_update_meta(ctypes.byref(d), FAKE, FAKE, FAKE, 3, 2, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_update_meta(ctypes.byref(d), FAKE, FAKE, FAKE, 0, 257, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_score_pages(ctypes.byref(d), FAKE, MISALIGNED, FAKE, FAKE, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_topk_pages(ctypes.byref(d), FAKE, FAKE, 0, FAKE, None, 0, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_topk_pages(ctypes.byref(d), FAKE, FAKE, 70000, FAKE, None, 0, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_sparse_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0.1, FAKE, FAKE, 1 << 20,
+                               None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_sparse_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, 8, 0.1, FAKE, None, 0,
+                               None) == g.GQAQ_ERR_WORKSPACE
+
+
+def test_options(L):
+    assert L.gqaq_set_option(g.GQAQ_OPT_MAX_CTAS, -1) == g.GQAQ_ERR_INVALID_ARG
+    assert L.gqaq_set_option(12345, 0) == g.GQAQ_ERR_INVALID_ARG
+    assert L.gqaq_set_option(g.GQAQ_OPT_MAX_CTAS, 0) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_WAIT_TIMEOUT_NS, 2_000_000_000) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_TEST_STALL, 0) == g.GQAQ_OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 8, 64, dtype=torch.float16)
+    k = torch.zeros(1, 2, 16, 64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        g.gqa_decode_attn(q, k, k, torch.ones(1, dtype=torch.int32), 0.125)

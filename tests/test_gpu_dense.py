@@ -1,0 +1,138 @@
+"""GPU parity of gqa_decode_attn (dense folded-GQA decode) against the fp64
+oracle's explicit-repeat_kv attention, element by element.
+
+Covers D in {64, 128}, G in {1, 2, 4, 8}, ragged and tiny valid lengths, an
+allocated length that is not a multiple of the tile, persistent grids forced
+small (so units split across CTAs and go through the log-sum-exp combine)
+and the first workload at its full size.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_head_folding_gb300 as g
+import oracle
+import workloads
+from _util import assert_attn_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def _reset_options():
+    yield
+    g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
+
+
+def run_case(B, Hq, Hkv, D, Lmax, valid, seed, max_ctas=0):
+    w = workloads.Workload(0, "case", batch=B, num_layers=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax)
+    x = workloads.make_layer(w, 0, device="cpu", seed=seed)
+    vl = torch.tensor(valid, dtype=torch.int32)
+    g.set_option(g.GQAQ_OPT_MAX_CTAS, max_ctas)
+    scale = 1.0 / math.sqrt(D)
+    out = g.gqa_decode_attn(x["q"].to(DEV), x["k_cache"].to(DEV), x["v_cache"].to(DEV), vl.to(DEV), scale)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    ref = oracle.attn_repeat_kv(x["q"].numpy(), x["k_cache"].numpy(), x["v_cache"].numpy(), valid, scale)
+    return assert_attn_close(out, ref)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_dense_group_sizes(D, G):
+    Hkv = 2 if G == 8 else 3
+    run_case(2, Hkv * G, Hkv, D, 700, [700, 333], seed=D * 10 + G)
+
+
+@pytest.mark.parametrize("max_ctas", [0, 1, 2, 3, 7, 50])
+def test_dense_split_and_combine(max_ctas):
+    # ragged lengths and a tail tile; small grids force units across CTAs
+    run_case(3, 32, 8, 64, 1000, [1000, 129, 1], seed=11, max_ctas=max_ctas)
+
+
+@pytest.mark.parametrize("valid", [[1], [15], [16], [17], [127], [128], [129], [300]])
+def test_dense_edge_lengths(valid):
+    run_case(1, 8, 2, 128, 300, valid, seed=valid[0])
+
+
+def test_dense_first_workload_full_size():
+    # 32 query heads on 8 KV heads, D=64, 4096 valid tokens, batch 1
+    w = workloads.WORKLOADS[1]
+    x = workloads.make_layer(w, 0, device="cpu")
+    scale = 1.0 / math.sqrt(w.head_dim)
+    out = g.gqa_decode_attn(x["q"].to(DEV), x["k_cache"].to(DEV), x["v_cache"].to(DEV),
+                            x["valid_len"].to(DEV), scale)
+    ref = oracle.attn_repeat_kv(x["q"].numpy(), x["k_cache"].numpy(), x["v_cache"].numpy(),
+                                x["valid_len"].numpy(), scale)
+    assert_attn_close(out, ref)
+
+
+def test_dense_second_workload_two_layers():
+    # EXAONE-shaped caches, allocated 4096, valid lengths uniform in [1024, 4096]
+    w = workloads.WORKLOADS[2].with_(batch=3)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    for layer in range(2):
+        x = workloads.make_layer(w, layer, device="cpu")
+        out = g.gqa_decode_attn(x["q"].to(DEV), x["k_cache"].to(DEV), x["v_cache"].to(DEV),
+                                x["valid_len"].to(DEV), scale)
+        ref = oracle.attn_repeat_kv(x["q"].numpy(), x["k_cache"].numpy(), x["v_cache"].numpy(),
+                                    x["valid_len"].numpy(), scale)
+        assert_attn_close(out, ref, f"layer {layer}")
+
+
+def test_dense_invalid_lengths_are_clamped_and_flagged():
+    w = workloads.Workload(0, "case", batch=3, num_layers=1, num_q_heads=8, num_kv_heads=2,
+                           head_dim=64, max_len=64)
+    x = workloads.make_layer(w, 0, device="cpu", seed=5)
+    vl = torch.tensor([0, 64, 500], dtype=torch.int32)
+    g.device_status(reset=True)
+    out = g.gqa_decode_attn(x["q"].to(DEV), x["k_cache"].to(DEV), x["v_cache"].to(DEV), vl.to(DEV), 0.125)
+    flags = g.device_status(reset=True)
+    assert flags & g.GQAQ_DEV_BAD_LEN
+    o = out.float().cpu()
+    assert torch.all(o[0] == 0)                                  # no valid token -> zeros
+    ref = oracle.attn_repeat_kv(x["q"].numpy()[1:], x["k_cache"].numpy()[1:], x["v_cache"].numpy()[1:],
+                                [64, 64], 0.125)                 # 500 clamps to Lmax = 64
+    assert_attn_close(out[1:], ref)
+
+
+def test_dense_uninitialised_tail_is_never_used():
+    # rows past valid_len hold NaN; the output must not see them
+    w = workloads.Workload(0, "case", batch=2, num_layers=1, num_q_heads=16, num_kv_heads=4,
+                           head_dim=128, max_len=256)
+    x = workloads.make_layer(w, 0, device="cpu", seed=9)
+    k, v = x["k_cache"].clone(), x["v_cache"].clone()
+    valid = [100, 37]
+    for b, n in enumerate(valid):
+        k[b, :, n:] = float("nan")
+        v[b, :, n:] = float("nan")
+    out = g.gqa_decode_attn(x["q"].to(DEV), k.to(DEV), v.to(DEV), torch.tensor(valid, dtype=torch.int32).to(DEV),
+                            0.1)
+    ref = oracle.attn_repeat_kv(x["q"].numpy(), k.numpy(), v.numpy(), valid, 0.1)
+    assert_attn_close(out, ref)
+
+
+def test_dense_repeatable_and_graph_capturable():
+    w = workloads.WORKLOADS[2].with_(batch=4)
+    x = workloads.make_layer(w, 0, device=DEV)
+    args = (x["q"], x["k_cache"], x["v_cache"], x["valid_len"])
+    d = g.dims_of(x["q"], x["k_cache"])
+    ws = g.alloc_workspace(d, DEV)
+    out = torch.empty_like(x["q"])
+    g.gqa_decode_attn(*args, 0.125, out=out, workspace=ws)
+    first = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            g.gqa_decode_attn(*args, 0.125, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, first)
