@@ -1,0 +1,538 @@
+"""Decode-step attention benchmark: dense folded-GQA attention + Quest top-K.
+
+One step = one decode step over every layer of the workload, run through the
+library's C ABI:
+  - dense layers: attend over every valid token;
+  - Quest layers: append the new token and update its page's min/max, score
+    every page, pick the top-K pages, attend over them.
+The whole step is captured in one CUDA graph and replayed. The default
+workload is the Llama-2-7B-shaped Quest stack: 32 layers, 32 heads, D=128,
+32768 tokens, 16-token pages, K=128 (a 2048-token budget), layers 0-1 dense,
+batch 1. It is the one workload whose single step runs every stage. Each
+step streams about 3.1 GB of distinct cache and metadata, far more than the
+129 MB L2, so no L2 flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--batch B]
+                       [--impl ours|reference]
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "decode-attn µs/step and achieved HBM GB/s vs peak (dense GQA-fold; Quest top-K)"
+UNIT = "us/step"
+
+
+# ---------------------------------------------------------------------------
+# Bytes model ("Quest ..." review, bytes-model section): M bytes per key or
+# value vector; dense reads 2ML per KV head, Quest reads ~2ML/S of metadata
+# plus 2MKS of selected keys and values.
+# ---------------------------------------------------------------------------
+def kv_vector_bytes(head_dim: int) -> int:
+    return 2 * head_dim
+
+
+def dense_unit_bytes(head_dim: int, length: int) -> int:
+    """Keys and values of one (sequence, KV head): 2 M L."""
+    return 2 * kv_vector_bytes(head_dim) * length
+
+
+def meta_unit_bytes(head_dim: int, length: int, page_size: int) -> int:
+    """Min and max vectors of every page of one (sequence, KV head): 2 M ceil(L/S)."""
+    return 2 * kv_vector_bytes(head_dim) * ((length + page_size - 1) // page_size)
+
+
+def selected_unit_bytes(head_dim: int, length: int, page_size: int, k_pages: int) -> int:
+    """Keys and values of the selected pages: 2 M S min(K, P)."""
+    pages = (length + page_size - 1) // page_size
+    return 2 * kv_vector_bytes(head_dim) * page_size * min(k_pages, pages)
+
+
+def step_bytes(w: workloads.Workload, lens_per_layer) -> dict:
+    """Algorithmic bytes of one step, by kernel family (per-step totals)."""
+    M, D, S, G = kv_vector_bytes(w.head_dim), w.head_dim, w.page_size, w.group
+    fam = {"dense": 0, "score": 0, "topk": 0, "sparse": 0, "append": 0}
+    launches = {"dense": 0, "score": 0, "topk": 0, "sparse": 0, "append": 0}
+    qo = 2 * G * M  # q read + out write per unit
+    for layer, lens in enumerate(lens_per_layer):
+        if w.append:
+            launches["append"] += 1
+            # new k,v read + cache row write + page min/max read and write
+            fam["append"] += w.batch * w.num_kv_heads * (2 * M + 2 * M + 4 * M)
+        if w.layer_is_dense(layer):
+            launches["dense"] += 1
+            for L in lens:
+                fam["dense"] += w.num_kv_heads * (dense_unit_bytes(D, L) + qo)
+        else:
+            launches["score"] += 1
+            launches["topk"] += 1
+            launches["sparse"] += 1
+            for L in lens:
+                P = (L + S - 1) // S
+                n = min(w.k_pages, P)
+                fam["score"] += w.num_kv_heads * (meta_unit_bytes(D, L, S) + G * M + 4 * P)
+                fam["topk"] += w.num_kv_heads * (4 * P + 4 * w.k_pages)
+                fam["sparse"] += w.num_kv_heads * (selected_unit_bytes(D, L, S, w.k_pages) + 4 * n + qo)
+    return {"bytes": fam, "launches": launches, "total": sum(fam.values())}
+
+
+def roofline_unit_bytes(w: workloads.Workload, family: str, lens) -> int:
+    """Per-launch bytes of the survey's per-unit figures (K/V or metadata only)."""
+    D, S = w.head_dim, w.page_size
+    if family == "dense":
+        return sum(w.num_kv_heads * dense_unit_bytes(D, L) for L in lens)
+    if family == "score":
+        return sum(w.num_kv_heads * meta_unit_bytes(D, L, S) for L in lens)
+    if family == "sparse":
+        return sum(w.num_kv_heads * selected_unit_bytes(D, L, S, w.k_pages) for L in lens)
+    raise ValueError(family)
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU; every rank runs its own
+# sequences, so no collective touches the data path)
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    return 7919 * rank
+
+
+# ---------------------------------------------------------------------------
+# Clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), float(f[2]), float(f[3]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r[3] >= 50] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[4][i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in busy), "reasons": reasons, "samples": len(busy)}
+
+
+# ---------------------------------------------------------------------------
+# Workload state on the device
+# ---------------------------------------------------------------------------
+def build_state(w: workloads.Workload, device, seed_offset: int = 0):
+    import gqa_head_folding_gb300 as g
+    from gqa_head_folding_gb300.decode import DecodeStack, Layer
+    stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
+                        w.dense_layers, device, w.page_size)
+    layers, lens = [], []
+    for layer in range(w.num_layers):
+        x = workloads.make_layer(w, layer, device=device,
+                                 seed=workloads.layer_seed(w, layer) + seed_offset if seed_offset else None)
+        L = Layer(q=x["q"], k_cache=x["k_cache"], v_cache=x["v_cache"], valid_len=x["valid_len"],
+                  out=torch.empty_like(x["q"]))
+        if w.append or not w.layer_is_dense(layer):
+            L.meta = stack.new_meta()
+            prefill = x["valid_len"] - 1 if w.append else x["valid_len"]
+            g.quest_update_meta(L.k_cache, prefill, L.meta, page_size=w.page_size)
+        if w.append:
+            L.k_new, L.v_new, L.pos = x["k_new"], x["v_new"], x["pos"]
+        layers.append(L)
+        lens.append([int(v) for v in x["valid_len"].cpu()])
+    torch.cuda.synchronize(device)
+    return stack, layers, lens
+
+
+def capture(fn, device):
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        fn()                                   # eager call: loads kernels, sets attributes
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            fn()
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    return graph
+
+
+def time_graph(graph, reps: int, device) -> float:
+    """Mean seconds per replay, CUDA events on the replay stream."""
+    st = torch.cuda.current_stream(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    a.record(st)
+    for _ in range(reps):
+        graph.replay()
+    b.record(st)
+    b.synchronize()
+    return a.elapsed_time(b) / 1e3 / reps
+
+
+def family_timings(stack, layers, w, device, reps: int) -> dict:
+    """Per-launch time of each ABI call family, each replayed alone in a graph."""
+    import gqa_head_folding_gb300 as g
+    fams = {}
+    dense = [L for i, L in enumerate(layers) if stack.is_dense(i)]
+    quest = [L for i, L in enumerate(layers) if not stack.is_dense(i)]
+    if dense:
+        fams["dense"] = (lambda: [g.gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, stack.scale,
+                                                    out=L.out, workspace=stack.workspace) for L in dense], len(dense))
+    if quest:
+        fams["score"] = (lambda: [g.quest_score_pages(L.q, L.meta, L.valid_len, stack.max_len, scores=stack.scores,
+                                                      page_size=w.page_size) for L in quest], len(quest))
+        fams["topk"] = (lambda: [g.quest_topk_pages(stack.scores, L.valid_len, stack.k_pages, stack.max_len,
+                                                    page_idx=stack.page_idx, page_size=w.page_size)
+                                 for L in quest], len(quest))
+        fams["sparse"] = (lambda: [g.quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, stack.page_idx,
+                                                       stack.scale, out=L.out, workspace=stack.workspace,
+                                                       page_size=w.page_size) for L in quest], len(quest))
+    if w.append:
+        fams["append"] = (lambda: [g.quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos,
+                                                     w.page_size) for L in layers], len(layers))
+    out = {}
+    for name, (fn, n) in fams.items():
+        graph = capture(fn, device)
+        for _ in range(2):
+            graph.replay()
+        out[name] = {"s_per_launch": time_graph(graph, reps, device) / n, "launches": n}
+        del graph
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample, scaled to one step
+# ---------------------------------------------------------------------------
+def oracle_step_seconds(w: workloads.Workload, layers, lens, budget_s: float = 15.0) -> dict:
+    """Time the oracle per (sequence, KV head) unit on sampled units of one
+    dense and one Quest layer, and scale by the units of a whole step."""
+    import numpy as np
+
+    import oracle
+    S, G = w.page_size, w.group
+    scale = 1.0 / math.sqrt(w.head_dim)
+
+    def unit_arrays(L, b, kv):
+        q = L.q[b, kv * G:(kv + 1) * G].unsqueeze(0).cpu().numpy()
+        k = L.k_cache[b, kv].unsqueeze(0).unsqueeze(0).cpu().numpy()
+        v = L.v_cache[b, kv].unsqueeze(0).unsqueeze(0).cpu().numpy()
+        return q, k, v
+
+    def dense_unit(L, b, kv, length):
+        q, k, v = unit_arrays(L, b, kv)
+        t0 = time.perf_counter()
+        oracle.attn_repeat_kv(q, k, v, [length], scale)
+        return time.perf_counter() - t0
+
+    def quest_unit(L, b, kv, length):
+        q, k, v = unit_arrays(L, b, kv)
+        meta = oracle.page_minmax(k, [length], S)          # prefill state, not timed
+        t0 = time.perf_counter()
+        if w.append:                                        # the appended token's page
+            p = (length - 1) // S
+            rows = k[:, :, p * S:length]
+            meta[:, :, p] = oracle.page_minmax(rows, [rows.shape[2]], S)[:, :, 0]
+        sc = oracle.page_scores(q, meta, [length], S)
+        idx = oracle.topk_pages(sc, [length], S, w.k_pages)
+        oracle.sparse_attn(q, k, v, [length], idx, S, scale)
+        return time.perf_counter() - t0
+
+    dense_layers = [i for i in range(w.num_layers) if w.layer_is_dense(i)]
+    quest_layers = [i for i in range(w.num_layers) if not w.layer_is_dense(i)]
+    units = [(b, kv) for b in range(w.batch) for kv in range(w.num_kv_heads)]
+    rng = np.random.default_rng(0)
+    order = [units[i] for i in rng.permutation(len(units))]
+    per_layer = {}
+    spent = 0.0
+    sampled = {"dense": 0, "quest": 0}
+    for kind, lyr in (("dense", dense_layers), ("quest", quest_layers)):
+        if not lyr:
+            continue
+        li = lyr[0]
+        times = []
+        for (b, kv) in order:
+            fn = dense_unit if kind == "dense" else quest_unit
+            times.append(fn(layers[li], b, kv, lens[li][b]) / max(1, lens[li][b]))  # seconds per token
+            spent += times[-1] * lens[li][b]
+            if spent > budget_s / 2 and len(times) >= 1:
+                break
+        sampled[kind] = len(times)
+        per_layer[kind] = statistics.mean(times)
+    est = 0.0
+    for i in range(w.num_layers):
+        kind = "dense" if w.layer_is_dense(i) else "quest"
+        est += per_layer[kind] * w.num_kv_heads * sum(lens[i])
+    return {"seconds_per_step": est, "sampled_units": sampled,
+            "sample": f"fp64 oracle on {sampled['dense']} dense and {sampled['quest']} Quest (sequence, KV head) "
+                      f"units of one layer each, scaled per token to all {w.num_layers} layers x "
+                      f"{w.batch * w.num_kv_heads} units"}
+
+
+# ---------------------------------------------------------------------------
+# Arms
+# ---------------------------------------------------------------------------
+def workload_from_args(args) -> workloads.Workload:
+    w = workloads.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(batch=args.batch)
+    if args.k_pages:
+        w = w.with_(k_pages=args.k_pages)
+    if args.layers:
+        w = w.with_(num_layers=args.layers)
+    return w
+
+
+def config_of(w: workloads.Workload, world: int) -> dict:
+    return {"workload": f"{w.name} (config {w.id})", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
+            "layers": w.num_layers, "dense_layers": w.num_layers if w.k_pages is None else w.dense_layers,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "max_len": w.max_len, "valid_len": "full" if w.valid_lo is None else f"uniform[{w.valid_lo},{w.max_len}]",
+            "page_size": w.page_size, "k_pages": w.k_pages,
+            "token_budget": None if w.k_pages is None else w.k_pages * w.page_size,
+            "append": w.append, "planted_pages_per_head": w.n_plant, "parallelism": f"replicas x{world}",
+            "l2": "per-step working set > 4x L2; no flush"}
+
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle as it stands, on the host cores, on this workload."""
+    if rank != 0:
+        return
+    w = workload_from_args(args)
+    device = torch.device("cuda:0") if torch.cuda.is_available() else None
+    if device is None:
+        print(json.dumps({"impl": "reference", "unavailable": "inputs are drawn on the GPU; no CUDA device"}))
+        return
+    import gqa_head_folding_gb300 as g  # noqa: F401  (prefill metadata on the device)
+    stack, layers, lens = build_state(w, device)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget)
+        if i >= args.warmup:
+            per_step.append(r["seconds_per_step"])
+    value = statistics.mean(per_step) * 1e6
+    sb = step_bytes(w, lens)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, 1),
+            "achieved_gbs": sb["total"] / (value / 1e6) / 1e9,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def run_ours(args, rank, world, local):
+    import gqa_head_folding_gb300 as g
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    w = workload_from_args(args)
+    g.lib()
+    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank))
+    sb = step_bytes(w, lens)
+    step = lambda: stack.step(layers)  # noqa: E731
+    graph = capture(step, device)
+
+    # warm-up, then a short soak so the clock sampler sees the GPU under load
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        for _ in range(8):
+            graph.replay()
+        torch.cuda.synchronize(device)
+
+    # timed region: exactly K steps
+    st = torch.cuda.current_stream(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    ev0.record(st)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(st)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    clocks = sampler.stop()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    elapsed = max_over_ranks(elapsed, dist, device)
+    s_per_step = elapsed / args.steps
+
+    # per-family timings for the roofline of the dominant kernel
+    fam = family_timings(stack, layers, w, device, reps=max(3, min(50, args.steps)))
+    per_step_fam = {k: v["s_per_launch"] * sb["launches"][k] for k, v in fam.items()}
+    dominant = max(per_step_fam, key=per_step_fam.get)
+    peaks = load_peaks()
+    roof = None
+    if dominant in ("dense", "score", "sparse"):
+        layer_of = next(i for i in range(w.num_layers)
+                        if (stack.is_dense(i) if dominant == "dense" else not stack.is_dense(i)))
+        per_launch = roofline_unit_bytes(w, dominant, lens[layer_of])
+        achieved = per_launch / fam[dominant]["s_per_launch"] / 1e9
+        roof = {"bound": "hbm", "kernel": {"dense": "gqa_decode_attn", "score": "quest_score_pages",
+                                           "sparse": "quest_sparse_attn"}[dominant],
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                "traffic": None, "bytes_per_launch": per_launch,
+                "us_per_launch": round(fam[dominant]["s_per_launch"] * 1e6, 2)}
+
+    # end to end through the public API: host inputs in, host outputs out
+    h2d = [(L.q, torch.empty(L.q.shape, dtype=L.q.dtype, pin_memory=True)) for L in layers]
+    if w.append:
+        h2d += [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for L in layers for t in (L.k_new, L.v_new)]
+    for dst, src in h2d:
+        src.copy_(dst.cpu())
+    d2h = [(L.out, torch.empty(L.out.shape, dtype=L.out.dtype, pin_memory=True)) for L in layers]
+    h2d_bytes = sum(s.numel() * s.element_size() for _, s in h2d)
+    d2h_bytes = sum(d.numel() * d.element_size() for _, d in d2h)
+    e2e_steps = max(3, args.steps)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for dst, src in h2d:
+            dst.copy_(src, non_blocking=True)
+        graph.replay()
+        for src, dst in d2h:
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(device)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dist, device)
+    barrier(dist)
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget)
+        cpu = {"value": r["seconds_per_step"] * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": r["sample"]}
+    launches = stack.launches_per_step(w.num_layers, w.append)
+    total_bytes = sb["total"] * world
+    line = {
+        "metric": METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16 in/out, f32 accumulate",
+        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world),
+        "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
+        "achieved_frac_of_peak": round(sb["total"] / s_per_step / 1e9 / peaks["hbm_gbs"], 4),
+        "bytes_per_step": total_bytes,
+        "bytes_by_family": sb["bytes"],
+        "us_per_launch_by_family": {k: round(v["s_per_launch"] * 1e6, 2) for k, v in fam.items()},
+        "us_per_step_by_family": {k: round(v * 1e6, 2) for k, v in per_step_fam.items()},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_s * 1e6, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes},
+        "gpu_launches": launches * args.steps,
+        "gpu_launches_per_step": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--k-pages", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed replays before timing")
+    ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,93 @@
+"""Host-side pieces of bench.py: the bytes model against the closed forms the
+Quest review prints, and the multi-rank timing reduction on gloo (CPU)."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import workloads
+
+
+def test_bytes_model_matches_quest_closed_forms(golden_dir):
+    ex = json.load(open(os.path.join(golden_dir, "byte_arithmetic.json")))["quest"]["ratio_example"]
+    L, S, K, D = ex["L"], ex["S"], ex["K"], 128
+    full = bench.dense_unit_bytes(D, L)
+    quest = bench.meta_unit_bytes(D, L, S) + bench.selected_unit_bytes(D, L, S, K)
+    assert quest / full == ex["ratio"] == 1 / S + K * S / L
+    assert K * S == ex["B_tokens"]
+    # K >= number of pages reads every key and value once
+    assert bench.selected_unit_bytes(D, 100, 16, 1000) == 2 * 2 * D * 16 * 7
+
+
+def test_step_bytes_of_the_workloads():
+    # Llama-2-7B-shaped Quest stack: 2 x 512 MiB dense + 30 x (32 MiB meta + 32 MiB selected)
+    w = workloads.WORKLOADS[3]
+    lens = [[w.max_len]] * w.num_layers
+    kv = 2 * bench.roofline_unit_bytes(w, "dense", lens[0])
+    q = 30 * (bench.roofline_unit_bytes(w, "score", lens[2]) + bench.roofline_unit_bytes(w, "sparse", lens[2]))
+    assert kv + q == 3_087_007_744
+    sb = bench.step_bytes(w, lens)
+    assert sb["launches"] == {"dense": 2, "score": 30, "topk": 30, "sparse": 30, "append": 32}
+    assert 0 < sb["total"] - (kv + q) < 0.01 * (kv + q)          # q/out/scores/append are small
+    # EXAONE-shaped dense: 8 MiB for one full 4096-token layer at batch 1
+    w1 = workloads.WORKLOADS[1]
+    assert bench.roofline_unit_bytes(w1, "dense", [4096]) == 8 * 2 ** 20
+    # GQA Quest at 64K: 32 MiB per sequence per layer (2 MiB metadata... per KV head)
+    w4 = workloads.WORKLOADS[4].with_(batch=1)
+    assert bench.roofline_unit_bytes(w4, "score", [65536]) + \
+        bench.roofline_unit_bytes(w4, "sparse", [65536]) == 32 * 2 ** 20
+
+
+def test_workload_recipes():
+    w = workloads.WORKLOADS[5]
+    assert w.n_plant == 82                                          # 1% of 8192 pages
+    lens = workloads.valid_lengths(workloads.WORKLOADS[2], 3)
+    assert lens.min() >= 1024 and lens.max() <= 4096 and lens.dtype == torch.int32
+    assert torch.equal(lens, workloads.valid_lengths(workloads.WORKLOADS[2], 3))   # seeded
+    x = workloads.make_layer(w.with_(batch=1, max_len=16 * 50, n_plant=3, num_kv_heads=2, num_q_heads=4),
+                             0, "cpu")
+    assert x["k_cache"].dtype == torch.float16 and x["pos"].tolist() == [16 * 50 - 1]
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        t = bench.max_over_ranks(0.5 + rank, dist)
+        bench.barrier(dist)
+        results[rank] = (t, bench.rank_seed(rank))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_size_2():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    results = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, results)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert results[0][0] == results[1][0] == 1.5          # every rank sees the slowest rank's time
+    assert results[0][1] != results[1][1]                 # ranks draw different sequences
+
+
+def test_single_rank_needs_no_collective():
+    assert bench.max_over_ranks(0.25, None) == 0.25
+    bench.barrier(None)
