@@ -55,8 +55,8 @@ class Dims(ctypes.Structure):
 
 # Exported symbols, in the order include/gqaq.h declares them.
 EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_update_meta",
-           "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "gqaq_status_string",
-           "gqaq_set_option", "gqaq_device_status", "gqaq_version")
+           "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "gqa_decode_attn_noalloc",
+           "gqaq_status_string", "gqaq_set_option", "gqaq_device_status", "gqaq_version")
 
 _lib = None
 
@@ -79,6 +79,7 @@ def lib():
         L.quest_topk_pages.argtypes = [dp, vp, vp, i32, vp, vp, ctypes.c_size_t, vp]
         L.quest_sparse_attn.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp,
                                         ctypes.c_size_t, vp]
+        L.gqa_decode_attn_noalloc.argtypes = [dp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
         L.gqaq_status_string.argtypes = [i32]
         L.gqaq_status_string.restype = ctypes.c_char_p
         L.gqaq_set_option.argtypes = [i32, ctypes.c_int64]
@@ -178,6 +179,22 @@ def gqa_decode_attn(q, k_cache, v_cache, valid_len, scale: float, out=None, work
     _check("gqa_decode_attn", lib().gqa_decode_attn(
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(valid_len), float(scale),
         _ptr(out), _ptr(workspace), workspace.numel(), _stream(q)))
+    return out
+
+
+def gqa_decode_attn_noalloc(q, k_cache, v_cache, valid_len, scale: float, out):
+    """gqa_decode_attn without a workspace, for callers that cannot allocate
+    device memory (the library keeps the scratch in its own fixed 1 MiB array).
+    ``out`` must be given. Overlapping calls race on the shared scratch."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    _need(out, "out", torch.float16, 3)
+    d = dims_of(q, k_cache)
+    _check("gqa_decode_attn_noalloc", lib().gqa_decode_attn_noalloc(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(valid_len), float(scale),
+        _ptr(out), _stream(q)))
     return out
 
 

@@ -160,6 +160,27 @@ GQAQ_API int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const 
                       int k, float scale, gqaq_half *out, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* gqa_decode_attn for callers that cannot allocate device memory. The source
+ * pages have no counterpart to this call. A plugin or custom operator inside a
+ * host framework is often handed only its input and output pointers: the
+ * framework owns all device memory and forbids allocation while it runs. A
+ * latency-critical decode loop may also refuse cudaMalloc/cudaFree, which can
+ * synchronise the device. Such callers cannot supply gqa_decode_attn's
+ * workspace, so this variant keeps its split-context scratch in a fixed 1 MiB
+ * array inside the library's device memory. Every GPU that loads the library
+ * holds that array until the process exits.
+ * Arguments, layouts and results are those of gqa_decode_attn, without the
+ * workspace. Returns GQAQ_ERR_WORKSPACE, launching nothing, when the shape needs
+ * more scratch than 1 MiB. That happens for G = 8 with D = 128 on a 152-SM
+ * GB300, for example (gqaq_workspace_bytes reports the need).
+ * The first call on each device looks up the array's device address with that
+ * device current. Make that first call before any stream capture.
+ * All calls share the one array. Nothing in it needs to start at zero, but
+ * calls that overlap on the GPU race on it. It allocates nothing. */
+GQAQ_API int gqa_decode_attn_noalloc(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
+                                     const gqaq_half *v_cache, const int32_t *valid_len, float scale,
+                                     gqaq_half *out, void *stream);
+
 /* Human-readable name of a gqaq_status value (static string). */
 GQAQ_API const char *gqaq_status_string(int status);
 
