@@ -64,36 +64,51 @@ def selected_unit_bytes(head_dim: int, length: int, page_size: int, k_pages: int
     return 2 * kv_vector_bytes(head_dim) * page_size * min(k_pages, pages)
 
 
-def step_bytes(w: workloads.Workload, lens_per_layer) -> dict:
-    """Algorithmic bytes of one step, by kernel family (per-step totals)."""
+def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True) -> dict:
+    """Algorithmic bytes of one step, by call family (per-step totals).
+
+    Families follow the calls a step makes: "dense" (dense layers), "append"
+    (appends outside the fused call), and either "quest" (one fused call per
+    Quest layer) or "score" / "topk" / "sparse" (the step-by-step calls)."""
     M, D, S, G = kv_vector_bytes(w.head_dim), w.head_dim, w.page_size, w.group
-    fam = {"dense": 0, "score": 0, "topk": 0, "sparse": 0, "append": 0}
-    launches = {"dense": 0, "score": 0, "topk": 0, "sparse": 0, "append": 0}
-    qo = 2 * G * M  # q read + out write per unit
+    fam, launches = {}, {}
+
+    def add(name, nbytes):
+        fam[name] = fam.get(name, 0) + nbytes
+
+    def count(name):
+        launches[name] = launches.get(name, 0) + 1
+
+    qo = 2 * G * M                                   # q read + out write per unit
+    app_unit = 2 * M + 2 * M + 4 * M                 # new k,v read, row write, page min/max read+write
     for layer, lens in enumerate(lens_per_layer):
-        if w.append:
-            launches["append"] += 1
-            # new k,v read + cache row write + page min/max read and write
-            fam["append"] += w.batch * w.num_kv_heads * (2 * M + 2 * M + 4 * M)
-        if w.layer_is_dense(layer):
-            launches["dense"] += 1
+        dense = w.layer_is_dense(layer)
+        if w.append and (dense or not fused):
+            count("append")
+            add("append", w.batch * w.num_kv_heads * app_unit)
+        if dense:
+            count("dense")
             for L in lens:
-                fam["dense"] += w.num_kv_heads * (dense_unit_bytes(D, L) + qo)
+                add("dense", w.num_kv_heads * (dense_unit_bytes(D, L) + qo))
+        elif fused:
+            count("quest")
+            for L in lens:
+                add("quest", w.num_kv_heads * ((app_unit if w.append else 0) + meta_unit_bytes(D, L, S) +
+                                               selected_unit_bytes(D, L, S, w.k_pages) + qo))
         else:
-            launches["score"] += 1
-            launches["topk"] += 1
-            launches["sparse"] += 1
+            for name in ("score", "topk", "sparse"):
+                count(name)
             for L in lens:
                 P = (L + S - 1) // S
                 n = min(w.k_pages, P)
-                fam["score"] += w.num_kv_heads * (meta_unit_bytes(D, L, S) + G * M + 4 * P)
-                fam["topk"] += w.num_kv_heads * (4 * P + 4 * w.k_pages)
-                fam["sparse"] += w.num_kv_heads * (selected_unit_bytes(D, L, S, w.k_pages) + 4 * n + qo)
+                add("score", w.num_kv_heads * (meta_unit_bytes(D, L, S) + G * M + 4 * P))
+                add("topk", w.num_kv_heads * (4 * P + 4 * w.k_pages))
+                add("sparse", w.num_kv_heads * (selected_unit_bytes(D, L, S, w.k_pages) + 4 * n + qo))
     return {"bytes": fam, "launches": launches, "total": sum(fam.values())}
 
 
 def roofline_unit_bytes(w: workloads.Workload, family: str, lens) -> int:
-    """Per-launch bytes of the survey's per-unit figures (K/V or metadata only)."""
+    """Per-launch bytes of the per-unit figures (K/V, metadata, selected K/V)."""
     D, S = w.head_dim, w.page_size
     if family == "dense":
         return sum(w.num_kv_heads * dense_unit_bytes(D, L) for L in lens)
@@ -101,6 +116,8 @@ def roofline_unit_bytes(w: workloads.Workload, family: str, lens) -> int:
         return sum(w.num_kv_heads * meta_unit_bytes(D, L, S) for L in lens)
     if family == "sparse":
         return sum(w.num_kv_heads * selected_unit_bytes(D, L, S, w.k_pages) for L in lens)
+    if family == "quest":
+        return roofline_unit_bytes(w, "score", lens) + roofline_unit_bytes(w, "sparse", lens)
     raise ValueError(family)
 
 
@@ -191,11 +208,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Workload state on the device
 # ---------------------------------------------------------------------------
-def build_state(w: workloads.Workload, device, seed_offset: int = 0):
+def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True):
     import gqa_head_folding_gb300 as g
     from gqa_head_folding_gb300.decode import DecodeStack, Layer
     stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
-                        w.dense_layers, device, w.page_size)
+                        w.dense_layers, device, w.page_size, fused=fused)
     layers, lens = [], []
     for layer in range(w.num_layers):
         x = workloads.make_layer(w, layer, device=device,
@@ -242,32 +259,13 @@ def time_graph(graph, reps: int, device) -> float:
 
 
 def family_timings(stack, layers, w, device, reps: int) -> dict:
-    """Per-launch time of each ABI call family, each replayed alone in a graph."""
-    import gqa_head_folding_gb300 as g
-    fams = {}
-    dense = [L for i, L in enumerate(layers) if stack.is_dense(i)]
-    quest = [L for i, L in enumerate(layers) if not stack.is_dense(i)]
-    if dense:
-        fams["dense"] = (lambda: [g.gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, stack.scale,
-                                                    out=L.out, workspace=stack.workspace) for L in dense], len(dense))
-    if quest:
-        fams["score"] = (lambda: [g.quest_score_pages(L.q, L.meta, L.valid_len, stack.max_len, scores=stack.scores,
-                                                      page_size=w.page_size) for L in quest], len(quest))
-        fams["topk"] = (lambda: [g.quest_topk_pages(stack.scores, L.valid_len, stack.k_pages, stack.max_len,
-                                                    page_idx=stack.page_idx, page_size=w.page_size)
-                                 for L in quest], len(quest))
-        fams["sparse"] = (lambda: [g.quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, stack.page_idx,
-                                                       stack.scale, out=L.out, workspace=stack.workspace,
-                                                       page_size=w.page_size) for L in quest], len(quest))
-    if w.append:
-        fams["append"] = (lambda: [g.quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos,
-                                                     w.page_size) for L in layers], len(layers))
+    """Per-call time of each family of the step's calls, each replayed alone in a graph."""
     out = {}
-    for name, (fn, n) in fams.items():
-        graph = capture(fn, device)
+    for name, fns in stack.families(layers).items():
+        graph = capture(lambda: [fn() for fn in fns], device)
         for _ in range(2):
             graph.replay()
-        out[name] = {"s_per_launch": time_graph(graph, reps, device) / n, "launches": n}
+        out[name] = {"s_per_launch": time_graph(graph, reps, device) / len(fns), "launches": len(fns)}
         del graph
     return out
 
@@ -354,7 +352,7 @@ def workload_from_args(args) -> workloads.Workload:
     return w
 
 
-def config_of(w: workloads.Workload, world: int) -> dict:
+def config_of(w: workloads.Workload, world: int, fused: bool = True) -> dict:
     return {"workload": f"{w.name} (config {w.id})", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
             "layers": w.num_layers, "dense_layers": w.num_layers if w.k_pages is None else w.dense_layers,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
@@ -362,6 +360,7 @@ def config_of(w: workloads.Workload, world: int) -> dict:
             "page_size": w.page_size, "k_pages": w.k_pages,
             "token_budget": None if w.k_pages is None else w.k_pages * w.page_size,
             "append": w.append, "planted_pages_per_head": w.n_plant, "parallelism": f"replicas x{world}",
+            "quest_path": "fused (quest_decode_attn)" if fused else "step-by-step calls",
             "l2": "per-step working set > 4x L2; no flush"}
 
 
@@ -408,8 +407,8 @@ def run_ours(args, rank, world, local):
     dist = init_dist(world, "nccl")
     w = workload_from_args(args)
     g.lib()
-    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank))
-    sb = step_bytes(w, lens)
+    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused)
+    sb = step_bytes(w, lens, fused=not args.unfused)
     step = lambda: stack.step(layers)  # noqa: E731
     graph = capture(step, device)
 
@@ -447,13 +446,13 @@ def run_ours(args, rank, world, local):
     dominant = max(per_step_fam, key=per_step_fam.get)
     peaks = load_peaks()
     roof = None
-    if dominant in ("dense", "score", "sparse"):
+    if dominant in ("dense", "score", "sparse", "quest"):
         layer_of = next(i for i in range(w.num_layers)
                         if (stack.is_dense(i) if dominant == "dense" else not stack.is_dense(i)))
         per_launch = roofline_unit_bytes(w, dominant, lens[layer_of])
         achieved = per_launch / fam[dominant]["s_per_launch"] / 1e9
         roof = {"bound": "hbm", "kernel": {"dense": "gqa_decode_attn", "score": "quest_score_pages",
-                                           "sparse": "quest_sparse_attn"}[dominant],
+                                           "sparse": "quest_sparse_attn", "quest": "quest_decode_attn"}[dominant],
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
                 "traffic": None, "bytes_per_launch": per_launch,
@@ -489,13 +488,13 @@ def run_ours(args, rank, world, local):
         r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget)
         cpu = {"value": r["seconds_per_step"] * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": r["sample"]}
-    launches = stack.launches_per_step(w.num_layers, w.append)
+    launches = stack.launches_per_step(layers)
     total_bytes = sb["total"] * world
     line = {
         "metric": METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16 in/out, f32 accumulate",
-        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world),
+        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused),
         "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
         "achieved_frac_of_peak": round(sb["total"] / s_per_step / 1e9 / peaks["hbm_gbs"], 4),
         "bytes_per_step": total_bytes,
@@ -526,6 +525,7 @@ def main(argv=None):
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed replays before timing")
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="run Quest layers as the step-by-step calls")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":

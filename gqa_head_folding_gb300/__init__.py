@@ -37,6 +37,7 @@ GQAQ_DEV_BAD_POS = 8
 GQAQ_OPT_MAX_CTAS = 1
 GQAQ_OPT_WAIT_TIMEOUT_NS = 2
 GQAQ_OPT_TEST_STALL = 3
+GQAQ_OPT_CLUSTER_SIZE = 4
 
 PAGE_SIZE = 16
 
@@ -55,7 +56,8 @@ class Dims(ctypes.Structure):
 
 # Exported symbols, in the order include/gqaq.h declares them.
 EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_update_meta",
-           "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "gqa_decode_attn_noalloc",
+           "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "quest_decode_attn",
+           "gqa_decode_attn_noalloc",
            "gqaq_status_string", "gqaq_set_option", "gqaq_device_status", "gqaq_version")
 
 _lib = None
@@ -79,6 +81,8 @@ def lib():
         L.quest_topk_pages.argtypes = [dp, vp, vp, i32, vp, vp, ctypes.c_size_t, vp]
         L.quest_sparse_attn.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp,
                                         ctypes.c_size_t, vp]
+        L.quest_decode_attn.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp,
+                                        vp]
         L.gqa_decode_attn_noalloc.argtypes = [dp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
         L.gqaq_status_string.argtypes = [i32]
         L.gqaq_status_string.restype = ctypes.c_char_p
@@ -179,6 +183,35 @@ def gqa_decode_attn(q, k_cache, v_cache, valid_len, scale: float, out=None, work
     _check("gqa_decode_attn", lib().gqa_decode_attn(
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(valid_len), float(scale),
         _ptr(out), _ptr(workspace), workspace.numel(), _stream(q)))
+    return out
+
+
+def quest_decode_attn(q, k_cache, v_cache, meta, valid_len, k: int, scale: float, k_new=None, v_new=None,
+                      pos=None, out=None, scores=None, page_idx=None, page_size: int = PAGE_SIZE):
+    """Fused Quest step in one launch: optional append (k_new, v_new at pos),
+    page scores, top-k pages and attention over them. scores/page_idx are
+    optional outputs."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(meta, "meta", torch.float16, 5)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    if pos is not None:
+        _need(k_new, "k_new", torch.float16, 3)
+        _need(v_new, "v_new", torch.float16, 3)
+        _need(pos, "pos", torch.int32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 3)
+    if scores is not None:
+        _need(scores, "scores", torch.float32, 3)
+    if page_idx is not None:
+        _need(page_idx, "page_idx", torch.int32, 3)
+    d = dims_of(q, k_cache, page_size)
+    _check("quest_decode_attn", lib().quest_decode_attn(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(k_new), _ptr(v_new),
+        _ptr(pos), _ptr(valid_len), int(k), float(scale), _ptr(out), _ptr(scores), _ptr(page_idx),
+        _stream(q)))
     return out
 
 

@@ -22,6 +22,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int64_t> g_opt_max_ctas{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 std::atomic<int64_t> g_opt_test_stall{0};
+std::atomic<int64_t> g_opt_cluster_size{0};
 
 struct DeviceState {
     bool ready = false;
@@ -68,6 +69,7 @@ int make_ctx(LaunchCtx *ctx, void *stream) {
     ctx->max_ctas = (int)g_opt_max_ctas.load();
     ctx->timeout_ns = (uint64_t)g_opt_timeout_ns.load();
     ctx->test_stall = (int)g_opt_test_stall.load();
+    ctx->cluster_size = (int)g_opt_cluster_size.load();
     ctx->status = s->status;
     return GQAQ_OK;
 }
@@ -146,6 +148,10 @@ int gqaq_set_option(int option, int64_t value) {
             return GQAQ_OK;
         case GQAQ_OPT_TEST_STALL:
             g_opt_test_stall.store(value != 0 ? 1 : 0);
+            return GQAQ_OK;
+        case GQAQ_OPT_CLUSTER_SIZE:
+            if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return GQAQ_ERR_INVALID_ARG;
+            g_opt_cluster_size.store(value);
             return GQAQ_OK;
         default:
             return GQAQ_ERR_INVALID_ARG;
@@ -277,6 +283,21 @@ int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half
     LaunchCtx ctx;
     rc = make_ctx(&ctx, stream);
     if (rc != GQAQ_OK) return rc;
+    if (k <= kFusedMaxPages) {
+        // cluster kernel: attention and the log-sum-exp merge in one launch
+        FusedArgs f = {};
+        f.dims = dims;
+        f.q = reinterpret_cast<const __half *>(q);
+        f.k_cache = const_cast<__half *>(reinterpret_cast<const __half *>(k_cache));
+        f.v_cache = const_cast<__half *>(reinterpret_cast<const __half *>(v_cache));
+        f.meta = nullptr;
+        f.valid_len = valid_len;
+        f.page_idx = const_cast<int32_t *>(page_idx);
+        f.kpages = k;
+        f.scale = scale;
+        f.out = reinterpret_cast<__half *>(out);
+        return launch_quest_fused(f, ctx);
+    }
     AttnArgs a;
     a.dims = dims;
     a.q = reinterpret_cast<const __half *>(q);
@@ -290,6 +311,44 @@ int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     return launch_attention(a, ctx);
+}
+
+int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_cache, gqaq_half *v_cache,
+                      gqaq_half *meta, const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos,
+                      const int32_t *valid_len, int k, float scale, gqaq_half *out, float *scores,
+                      int32_t *page_idx, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(meta) ||
+        !aligned16(valid_len) || !aligned16(out))
+        return GQAQ_ERR_INVALID_ARG;
+    if (pos != nullptr && (!aligned16(pos) || !aligned16(k_new) || !aligned16(v_new))) return GQAQ_ERR_INVALID_ARG;
+    if ((scores != nullptr && !aligned16(scores)) || (page_idx != nullptr && !aligned16(page_idx)))
+        return GQAQ_ERR_INVALID_ARG;
+    if (k < 1 || k > 65536) return GQAQ_ERR_INVALID_ARG;
+    if (k > kFusedMaxPages) return GQAQ_ERR_UNSUPPORTED;
+    if (!isfinite(scale)) return GQAQ_ERR_INVALID_ARG;
+    const int64_t pmax = (dims->max_len + dims->page_size - 1) / dims->page_size;
+    if ((int64_t)dims->batch * dims->num_kv_heads * pmax > (int64_t)INT32_MAX - 1024) return GQAQ_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    FusedArgs f = {};
+    f.dims = dims;
+    f.q = reinterpret_cast<const __half *>(q);
+    f.k_cache = reinterpret_cast<__half *>(k_cache);
+    f.v_cache = reinterpret_cast<__half *>(v_cache);
+    f.meta = reinterpret_cast<__half *>(meta);
+    f.k_new = reinterpret_cast<const __half *>(k_new);
+    f.v_new = reinterpret_cast<const __half *>(v_new);
+    f.pos = pos;
+    f.valid_len = valid_len;
+    f.page_idx = page_idx;
+    f.scores = scores;
+    f.kpages = k;
+    f.scale = scale;
+    f.out = reinterpret_cast<__half *>(out);
+    return launch_quest_fused(f, ctx);
 }
 
 }  // extern "C"

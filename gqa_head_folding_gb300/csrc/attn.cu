@@ -28,40 +28,20 @@
 //    which attn_combine_kernel merges.
 #include <math.h>
 
+#include "attn_tile.cuh"
 #include "internal.h"
 
 namespace gqaq {
 
 template <int D, int G>
-struct AttnCfg {
-    static constexpr int NCW = 8;                 // consumer warps
-    static constexpr int THREADS = (NCW + 1) * 32;
-    static constexpr int TILE = 128;              // tokens per stage (8 pages when sparse)
-    static constexpr int SUB = 16;                // tokens per consumer warp
-    static constexpr int KH = D / 64;             // 128-byte column blocks per K row
-    static constexpr int KBLK = TILE * 128;       // bytes of one K column block
-    static constexpr int KBYTES = KH * KBLK;      // = TILE * D * 2
-    static constexpr int VBYTES = TILE * D * 2;
-    static constexpr int STAGE = KBYTES + VBYTES;
-    static constexpr int QBYTES = G * D * 2;
-    static constexpr int MERGE = NCW * G * (D + 2) * 4;
-    static constexpr int PBYTES = NCW * SUB * G * 4;
+struct AttnCfg : TileCfg<D, G> {
+    using T = TileCfg<D, G>;
+    static constexpr int THREADS = (T::NCW + 1) * 32;
     static constexpr int MISC = 256;
-    static constexpr int FIXED = QBYTES + MERGE + PBYTES + MISC;
-    static constexpr int NSTAGE = (3 * STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2;
-    static constexpr int SMEM = 1024 + NSTAGE * STAGE + FIXED;
-    static constexpr int LPT = 4;                 // lanes sharing one token in q.k
-    static constexpr int TPP = 32 / LPT;          // tokens per lane pass (8)
-    static constexpr int NTL = SUB / TPP;         // tokens per lane (2)
-    static constexpr int DQ = D / LPT;            // channels per lane in q.k
-    static constexpr int NCH = DQ / 8;            // 16-byte chunks per lane in q.k
-    static constexpr int DPL = D / 32;            // channels per lane in p @ V
-    static constexpr bool QREG = (G * D <= 512);  // q block held in registers
-    static constexpr int GQ = QREG ? G : 4;       // query rows per q.k pass
-    static constexpr int NPASS = G / GQ;
+    static constexpr int FIXED = T::QBYTES + T::MERGE + T::PBYTES + MISC;
+    static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2;
+    static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
     static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
-    static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
 };
 
 struct AttnParams {
@@ -266,16 +246,9 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     // ----------------------------------------------------------------------
     // Consumer warps
     // ----------------------------------------------------------------------
-    const int cw = warp;
-    const int part = lane / C::TPP;  // which D/4 channel slice this lane covers in q.k
-    const int jt = lane % C::TPP;    // this lane handles tokens jt and jt + 8 of the sub-tile
-    const int tid = threadIdx.x;     // 0..255 among consumers
-    // q.k chunk addressing inside a swizzled 128-byte K row. Rows jt and jt+8
-    // share (row & 7) = jt, so one XOR key serves both tokens.
-    const int c0 = part * C::DQ;
-    const uint32_t krow_off = (uint32_t)((c0 / 64) * C::KBLK + (cw * C::SUB + jt) * 128);
-    const uint32_t kx0 = (uint32_t)(((c0 % 64) / 8) ^ jt);
-    const uint32_t pb_warp = smem_u32(pbuf + cw * C::SUB * G);
+    const int tid = threadIdx.x;  // 0..255 among consumers
+    WarpAttn<D, G> wa;
+    wa.init(warp, lane, smem_u32(pbuf));
 
     Walk w;
     w.init(*sched, p.valid_len, p.Hkv, rule);
@@ -289,28 +262,14 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
         const int P = (len + p.S - 1) / p.S;
         const int nsel = P < p.kpages ? P : p.kpages;
         const __half *qg = p.q + ((int64_t)w.b * Hq + (int64_t)w.kv * G) * D;
-
-        uint4 qr[C::GQ][C::NCH];
         if (C::QREG) {
-#pragma unroll
-            for (int g = 0; g < C::GQ; ++g)
-#pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                    qr[g][c] = *reinterpret_cast<const uint4 *>(qg + g * D + c0 + c * 8);
+            wa.load_q(qg);
         } else {
             for (int e = tid; e < G * D / 8; e += C::NCW * 32)
                 reinterpret_cast<uint4 *>(q_s)[e] = reinterpret_cast<const uint4 *>(qg)[e];
             named_bar_sync(1, C::NCW * 32);
         }
-
-        float m[G], l[G], acc[G][C::DPL];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            m[g] = -INFINITY;
-            l[g] = 0.f;
-#pragma unroll
-            for (int e = 0; e < C::DPL; ++e) acc[g][e] = 0.f;
-        }
+        wa.reset();
 
         for (int t = 0; t < n; ++t, ++i) {
             const int s = i % C::NSTAGE;
@@ -327,7 +286,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
             const int local = w.local + t;
             int nvalid = 0;
             if (SPARSE) {
-                const int e = local * C::NCW + cw;
+                const int e = local * C::NCW + warp;
                 if (e < nsel) {
                     const int page = p.page_idx[(int64_t)unit * p.kpages + e];
                     if (page >= 0 && page < P) {
@@ -336,170 +295,24 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
                     }
                 }
             } else {
-                const int rem = len - (local * C::TILE + cw * C::SUB);
+                const int rem = len - (local * C::TILE + warp * C::SUB);
                 nvalid = rem < 0 ? 0 : (rem < C::SUB ? rem : C::SUB);
             }
             if (ok && nvalid > 0) {
                 const uint32_t kbase = smem_u32(stages + s * C::STAGE);
-                const uint32_t vbase = kbase + C::KBYTES;
-                // ---- scores: q . k, this lane's D/4 channels of tokens jt, jt+8 ----
-                float sc[C::NTL][G];
-#pragma unroll
-                for (int pass = 0; pass < C::NPASS; ++pass) {
-                    if (!C::QREG) {
-#pragma unroll
-                        for (int g = 0; g < C::GQ; ++g)
-#pragma unroll
-                            for (int c = 0; c < C::NCH; ++c)
-                                qr[g][c] = lds128(smem_u32(q_s + (pass * C::GQ + g) * D + c0 + c * 8));
-                    }
-#pragma unroll
-                    for (int u = 0; u < C::NTL; ++u) {
-                        float a0[C::GQ], a1[C::GQ];
-#pragma unroll
-                        for (int g = 0; g < C::GQ; ++g) a0[g] = a1[g] = 0.f;
-                        const uint32_t kro = kbase + krow_off + (uint32_t)(u * C::TPP * 128);
-#pragma unroll
-                        for (int c = 0; c < C::NCH; ++c) {
-                            const uint4 kc = lds128(kro + ((kx0 ^ (uint32_t)c) << 4));
-#pragma unroll
-                            for (int g = 0; g < C::GQ; ++g) {
-                                a0[g] = fma_h_lo(qr[g][c].x, kc.x, a0[g]);
-                                a1[g] = fma_h_hi(qr[g][c].x, kc.x, a1[g]);
-                                a0[g] = fma_h_lo(qr[g][c].y, kc.y, a0[g]);
-                                a1[g] = fma_h_hi(qr[g][c].y, kc.y, a1[g]);
-                                a0[g] = fma_h_lo(qr[g][c].z, kc.z, a0[g]);
-                                a1[g] = fma_h_hi(qr[g][c].z, kc.z, a1[g]);
-                                a0[g] = fma_h_lo(qr[g][c].w, kc.w, a0[g]);
-                                a1[g] = fma_h_hi(qr[g][c].w, kc.w, a1[g]);
-                            }
-                        }
-#pragma unroll
-                        for (int g = 0; g < C::GQ; ++g) sc[u][pass * C::GQ + g] = a0[g] + a1[g];
-                    }
-                }
-                // ---- online softmax over the 16 tokens (log2 domain) ----
-                float tmax[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) tmax[g] = -INFINITY;
-#pragma unroll
-                for (int u = 0; u < C::NTL; ++u) {
-                    const bool valid = jt + u * C::TPP < nvalid;
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        float x = sc[u][g];
-#pragma unroll
-                        for (int o = C::TPP; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                        sc[u][g] = valid ? x * p.scale_log2 : -INFINITY;
-                        tmax[g] = fmaxf(tmax[g], sc[u][g]);
-                    }
-                }
-#pragma unroll
-                for (int o = C::TPP / 2; o > 0; o >>= 1)
-#pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        tmax[g] = fmaxf(tmax[g], __shfl_xor_sync(0xffffffffu, tmax[g], o));
-                float pg[C::NTL][G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float mnew = fmaxf(m[g], tmax[g]);
-                    const float alpha = fast_exp2(m[g] - mnew);
-                    float psum = 0.f;
-#pragma unroll
-                    for (int u = 0; u < C::NTL; ++u) {
-                        pg[u][g] = fast_exp2(sc[u][g] - mnew);
-                        psum += pg[u][g];
-                    }
-                    l[g] = l[g] * alpha + (part == 0 ? psum : 0.f);
-                    m[g] = mnew;
-#pragma unroll
-                    for (int e = 0; e < C::DPL; ++e) acc[g][e] *= alpha;
-                }
-                if (part == 0) {
-#pragma unroll
-                    for (int u = 0; u < C::NTL; ++u) {
-                        float *dst = pbuf + (cw * C::SUB + jt + u * C::TPP) * G;
-#pragma unroll
-                        for (int g = 0; g < G; ++g) dst[g] = pg[u][g];
-                    }
-                }
-                __syncwarp();
-                // ---- acc += p @ V (lane owns D/32 channels of all G rows) ----
-#pragma unroll 4
-                for (int jj = 0; jj < nvalid; ++jj) {
-                    {
-                        float pj[G];
-                        const uint32_t pa = pb_warp + (uint32_t)(jj * G * 4);
-                        if (G == 8) {
-                            const uint4 x0 = lds128(pa), x1 = lds128(pa + 16);
-                            const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                            for (int g = 0; g < G; ++g) pj[g] = __uint_as_float(xs[g]);
-                        } else if (G == 4) {
-                            const uint4 x = lds128(pa);
-                            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                            for (int g = 0; g < G; ++g) pj[g] = __uint_as_float(xs[g]);
-                        } else if (G == 2) {
-                            const uint2 x = lds64(pa);
-                            pj[0] = __uint_as_float(x.x);
-                            pj[G - 1] = __uint_as_float(x.y);
-                        } else {
-                            pj[0] = __uint_as_float(lds32(pa));
-                        }
-                        const int row = cw * C::SUB + jj;
-                        float vf[C::DPL];
-                        if (D == 128) {
-                            const uint2 vv = lds64(vbase + (uint32_t)(row * D * 2 + lane * 8));
-                            const float2 f0 = half2_bits_to_float2(vv.x);
-                            const float2 f1 = half2_bits_to_float2(vv.y);
-                            vf[0] = f0.x; vf[1] = f0.y; vf[C::DPL > 2 ? 2 : 0] = f1.x; vf[C::DPL > 3 ? 3 : 0] = f1.y;
-                        } else {
-                            const float2 f0 = half2_bits_to_float2(lds32(vbase + (uint32_t)(row * D * 2 + lane * 4)));
-                            vf[0] = f0.x; vf[C::DPL > 1 ? 1 : 0] = f0.y;
-                        }
-#pragma unroll
-                        for (int g = 0; g < G; ++g)
-#pragma unroll
-                            for (int e = 0; e < C::DPL; ++e) acc[g][e] = fmaf(pj[g], vf[e], acc[g][e]);
-                    }
-                }
+                wa.tile(kbase, kbase + C::KBYTES, nvalid, p.scale_log2, q_s);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
 
         // ---- merge the 8 warp states of this segment ----
-#pragma unroll
-        for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
-        float *mw = merge + cw * G * (D + 2);
-        if (lane == 0) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                mw[g * (D + 2)] = m[g];
-                mw[g * (D + 2) + 1] = l[g];
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < C::DPL; ++e) mw[g * (D + 2) + 2 + lane * C::DPL + e] = acc[g][e];
+        wa.store_state(merge);
         named_bar_sync(1, C::NCW * 32);
         for (int idx = tid; idx < G * D; idx += C::NCW * 32) {
             const int g = idx / D, d = idx - (idx / D) * D;
-            float mst = -INFINITY;
-#pragma unroll
-            for (int ww = 0; ww < C::NCW; ++ww) mst = fmaxf(mst, merge[(ww * G + g) * (D + 2)]);
-            float ls = 0.f, as = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < C::NCW; ++ww) {
-                const float* st = merge + (ww * G + g) * (D + 2);
-                if (st[0] != -INFINITY) {
-                    const float f = fast_exp2(st[0] - mst);
-                    ls += f * st[1];
-                    as += f * st[2 + d];
-                }
-            }
+            float mst, ls, as;
+            merge_warps<D, G>(merge, g, d, mst, ls, as);
             if (complete) {
                 p.out[((int64_t)w.b * Hq + (int64_t)w.kv * G + g) * D + d] =
                     __float2half_rn(ls > 0.f ? as / ls : 0.f);

@@ -22,6 +22,7 @@ struct LaunchCtx {
     int max_ctas;          // 0 = automatic
     uint64_t timeout_ns;   // bound on every in-kernel wait
     int test_stall;        // attention producer issues nothing (timeout test)
+    int cluster_size;      // fused Quest kernel: forced CTAs per cluster, 0 = automatic
     int *status;           // device status word
 };
 

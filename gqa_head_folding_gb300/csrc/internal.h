@@ -35,6 +35,28 @@ struct AttnArgs {
 int launch_attention(const AttnArgs &a, const LaunchCtx &ctx);
 size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx);
 
+// Fused Quest step (quest_fused.cu). meta == nullptr selects attention over a
+// given page list (page_idx is then an input); otherwise append (pos may be
+// null), score, select and attend, with scores/page_idx optional outputs.
+struct FusedArgs {
+    const gqaq_dims *dims;
+    const __half *q;
+    __half *k_cache;
+    __half *v_cache;
+    __half *meta;
+    const __half *k_new;
+    const __half *v_new;
+    const int *pos;
+    const int *valid_len;
+    int *page_idx;
+    float *scores;
+    int kpages;
+    float scale;
+    __half *out;
+};
+int launch_quest_fused(const FusedArgs &a, const LaunchCtx &ctx);
+constexpr int kFusedMaxPages = 1024;
+
 // Quest kernels.
 int launch_append_kv(const gqaq_dims *dims, __half *k_cache, __half *v_cache, __half *meta,
                      const __half *k_new, const __half *v_new, const int *pos, const LaunchCtx &ctx);

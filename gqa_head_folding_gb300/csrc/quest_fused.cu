@@ -1,0 +1,726 @@
+// quest_fused.cu -- one decode step of a Quest layer in a single launch.
+//
+// "Quest: Query-Aware Sparsity for Efficient Long-Context LLM Inference"
+// (reviewer's summary), flowchart: score every page from its key min/max,
+// keep the top pages, read only their K and V, attend over those tokens. The
+// page-score section: the min/max metadata is updated when a key arrives,
+// and U(p,q) = sum_i max(q_i m_{p,i}, q_i M_{p,i}). The token-budget section:
+// K pages are kept per query (budget K*S tokens). With grouped query heads
+// ("Core ML Decode Optimization ...", section 3), one page set serves the G
+// query rows that share a KV head, scored by the largest U over those rows.
+//
+// GB300 mapping: a thread-block cluster of C CTAs owns one (sequence, KV
+// head) unit at a time (persistent clusters loop over units). Per unit:
+//  1. the CTA holding the appended token's page writes the new k, v rows and
+//     that page's min/max (producer warp, made visible to TMA by a proxy
+//     fence); every CTA streams the metadata of its 1/C of the pages with TMA
+//     and scores them into shared-memory keys (U as a dot of
+//     [min(q,0); max(q,0)] with [m; M], since m <= M);
+//  2. the cluster finds the K-th largest key with four 8-bit radix passes,
+//     summing the C per-CTA histograms through distributed shared memory;
+//  3. each CTA compacts its selected pages (ties to the lower page index)
+//     into the ascending page list, written into every CTA's shared memory;
+//  4. each CTA attends over 1/C of the selected pages (TMA page loads, the
+//     shared warp tile of attn_tile.cuh);
+//  5. the C CTA states (m, l, acc) merge by log-sum-exp through distributed
+//     shared memory, and the fp16 output is written.
+// No workspace, no second launch. ATTEND mode runs only steps 4-5 on a page
+// list given in global memory.
+#include <math.h>
+#include <string.h>
+
+#include "attn_tile.cuh"
+#include "internal.h"
+
+namespace gqaq {
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// Whole-cluster barrier: every thread of every CTA arrives (release) and waits
+// (acquire). Shared memory of every CTA in the cluster is visible afterwards.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t score_key(float f) {
+    uint32_t x = __float_as_uint(f);
+    if (x == 0x80000000u) x = 0u;  // -0 ranks with +0
+    return (x & 0x80000000u) ? ~x : (x | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t hmin0_bits(uint32_t x) {
+    __half2 h = *reinterpret_cast<__half2 *>(&x);
+    __half2 r = __hmin2(h, __float2half2_rn(0.f));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t hmax0_bits(uint32_t x) {
+    __half2 h = *reinterpret_cast<__half2 *>(&x);
+    __half2 r = __hmax2(h, __float2half2_rn(0.f));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+enum { FUSED_FULL = 0, FUSED_ATTEND = 1 };
+
+template <int D, int G>
+struct FusedCfg : TileCfg<D, G> {
+    using T = TileCfg<D, G>;
+    static constexpr int THREADS = (T::NCW + 1) * 32;
+    static constexpr int MT = 128;                  // pages per metadata tile
+    static constexpr int NB = 2 * D / 64;           // 128-byte column blocks per [m; M] record
+    static constexpr int MBLK = MT * 128;
+    static_assert(NB * MBLK == T::STAGE, "a metadata tile fills one ring stage");
+    static constexpr int KEYS_MAX = 4096;           // pages one CTA scores per unit
+    static constexpr int KSEL_MAX = 1024;           // selected pages per unit
+    static constexpr int KEYMERGE = (KEYS_MAX * 4 > T::MERGE) ? KEYS_MAX * 4 : T::MERGE;
+    static constexpr int QT_BYTES = G * 2 * D * 2;  // [G][2D] fp16 [q_neg | q_pos]
+    static constexpr int QREGION = (QT_BYTES > T::QBYTES) ? QT_BYTES : T::QBYTES;
+    static constexpr int CSTATE = G * (D + 2) * 4;
+    static constexpr int MISC = 2048;               // hist x2, totals, tile info, barriers, counters
+    static constexpr int FIXED = KEYMERGE + QREGION + T::PBYTES + KSEL_MAX * 4 + CSTATE + MISC + 1024;
+    static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
+    static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
+    static constexpr int NCHQ = D / 16;             // 16-byte chunks per record quarter
+    static constexpr bool QTREG = (G * D <= 512);
+    static constexpr int GQT = QTREG ? G : 4;
+    static constexpr int NPASST = G / GQT;
+};
+
+struct FusedParams {
+    const __half *q;
+    const int *valid_len;
+    const int *pos;          // FULL: row of the appended token, or null (no append)
+    const __half *k_new, *v_new;
+    __half *k_cache, *v_cache, *meta;
+    float *scores;           // FULL: optional output
+    int *page_idx;           // FULL: optional output; ATTEND: input
+    __half *out;
+    int *status;
+    int B, Hkv, Lmax, Pmax, S, kpages;
+    float scale_log2;
+    uint64_t timeout_ns;
+};
+
+template <int D, int G, int MODE>
+__global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
+    quest_fused_kernel(const __grid_constant__ CUtensorMap mmap, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const FusedParams p) {
+    using C = FusedCfg<D, G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *ring = smem;
+    uint8_t *fixed = ring + C::NSTAGE * C::STAGE;
+    uint32_t *keys = reinterpret_cast<uint32_t *>(fixed);      // aliased by merge after step 3
+    float *merge = reinterpret_cast<float *>(fixed);
+    __half *qreg_s = reinterpret_cast<__half *>(fixed + C::KEYMERGE);
+    float *pbuf = reinterpret_cast<float *>(fixed + C::KEYMERGE + C::QREGION);
+    int *list = reinterpret_cast<int *>(fixed + C::KEYMERGE + C::QREGION + C::PBYTES);
+    float *cstate = reinterpret_cast<float *>(list + C::KSEL_MAX);
+    int *misc = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(cstate) + C::CSTATE);
+    int *hist = misc;                     // [2][256]
+    int *tots = misc + 512;               // [256]
+    int *tinfo = misc + 768;              // [NSTAGE][8] valid tokens per page of a stage
+    int *cnt = misc + 800;                // [2] this CTA's (> kth, == kth) counts
+    int *wsum = misc + 808;               // [2][9] block-scan scratch
+    int *sh = misc + 832;                 // [0] digit, [1] remaining, [2] abort
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc + 848);
+    uint64_t *empty = full + C::NSTAGE;
+    volatile int *abort_flag = &sh[2];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = cluster_rank();
+    const uint32_t nct = cluster_ctas();
+    const int cid = (int)(blockIdx.x / nct);
+    const int ncl = (int)(gridDim.x / nct);
+    const int Hq = p.Hkv * G;
+    const int units = p.B * p.Hkv;
+    const bool producer = (warp == C::NCW);
+
+    if (tid == 0) {
+        sh[2] = 0;
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), C::NCW);
+        }
+        fence_mbar_init();
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+        if (MODE == FUSED_FULL) prefetch_tensormap(&mmap);
+    }
+    __syncthreads();
+    cluster_sync_all();  // every CTA of the cluster is running before any remote access
+
+    const uint64_t pol = l2_policy_evict_first();
+    WarpAttn<D, G> wa;
+    wa.init(warp, lane, smem_u32(pbuf));
+    int it = 0;  // position in the stage ring (same sequence in producer and consumers)
+
+    for (int u = cid; u < units; u += ncl) {
+        const int b = u / p.Hkv, kv = u - (u / p.Hkv) * p.Hkv;
+        const int raw = p.valid_len[b];
+        if (tid == 0 && crank == 0 && (raw < 1 || raw > p.Lmax)) raise_flag(p.status, GQAQ_DEV_BAD_LEN);
+        const int len = clamp_len(raw, p.Lmax);
+        const int P = (len + p.S - 1) / p.S;
+        const int nsel = P < p.kpages ? P : p.kpages;
+        const __half *qg = p.q + ((int64_t)b * Hq + (int64_t)kv * G) * D;
+
+        if (MODE == FUSED_FULL) {
+            // ================= 1. append + page scores =================
+            const int pr0 = (int)(((int64_t)crank * P) / nct);
+            const int pr1 = (int)(((int64_t)(crank + 1) * P) / nct);
+            const int ntile = (pr1 - pr0 + C::MT - 1) / C::MT;
+            if (producer) {
+                if (p.pos != nullptr) {
+                    const int pos = p.pos[b];
+                    const int papp = pos / p.S;
+                    const bool mine = (papp >= pr0 && papp < pr1) || (crank == nct - 1 && papp >= pr1);
+                    if (pos < 0 || pos >= p.Lmax) {
+                        if (lane == 0 && crank == 0) raise_flag(p.status, GQAQ_DEV_BAD_POS);
+                    } else if (mine) {
+                        constexpr int EPL = D / 32;
+                        const int64_t row = (int64_t)u * p.Lmax + pos;
+                        __half *mrow = p.meta + ((int64_t)u * p.Pmax + papp) * 2 * D;
+                        const bool fresh = (pos % p.S) == 0;
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) {
+                            const int c = lane * EPL + e;
+                            const __half kn = p.k_new[(int64_t)u * D + c];
+                            p.k_cache[row * D + c] = kn;
+                            p.v_cache[row * D + c] = p.v_new[(int64_t)u * D + c];
+                            __half mn = kn, mx = kn;
+                            if (!fresh) {
+                                const __half om = mrow[c], oM = mrow[D + c];
+                                const float kf = __half2float(kn);
+                                mn = (kf < __half2float(om)) ? kn : om;
+                                mx = (kf > __half2float(oM)) ? kn : oM;
+                            }
+                            mrow[c] = mn;
+                            mrow[D + c] = mx;
+                        }
+                        fence_proxy_async_global();  // the TMA reads below see these rows
+                    }
+                    __syncwarp();
+                    fence_proxy_async_global();
+                }
+                for (int t = 0; t < ntile; ++t, ++it) {
+                    const int s = it % C::NSTAGE;
+                    const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
+                    if (it >= C::NSTAGE) {
+                        bool ok = (*abort_flag == 0);
+                        if (ok && lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.timeout_ns, abort_flag);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) {
+                            if (lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
+                            continue;  // keep the ring count in step; issue nothing
+                        }
+                    }
+                    if (lane == 0 && *abort_flag == 0) {
+                        const uint32_t fb = smem_u32(&full[s]);
+                        const uint32_t dst = smem_u32(ring + s * C::STAGE);
+                        mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
+                        const int y = u * p.Pmax + pr0 + t * C::MT;
+#pragma unroll
+                        for (int kb = 0; kb < C::NB; ++kb) tma_load_2d(dst + kb * C::MBLK, &mmap, 64 * kb, y, fb, pol);
+                    }
+                    __syncwarp();
+                }
+            } else {
+                // consumer warps: lane = 8*quarter + page; 16 pages per warp per tile
+                const int jp = lane & 7, qq = lane >> 3;
+                const int cq0 = qq * (D / 2);
+                const bool negq = qq < 2;
+                const int qch0 = (qq & 1) * (D / 2);
+                uint4 qt[C::GQT][C::NCHQ];
+                if (C::QTREG) {
+#pragma unroll
+                    for (int g = 0; g < C::GQT; ++g)
+#pragma unroll
+                        for (int c = 0; c < C::NCHQ; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(qg + g * D + qch0 + c * 8);
+                            qt[g][c] = negq ? make_uint4(hmin0_bits(v.x), hmin0_bits(v.y), hmin0_bits(v.z), hmin0_bits(v.w))
+                                            : make_uint4(hmax0_bits(v.x), hmax0_bits(v.y), hmax0_bits(v.z), hmax0_bits(v.w));
+                        }
+                } else {
+                    for (int e = tid; e < G * D / 8; e += C::NCW * 32) {
+                        const int g = e / (D / 8), c = e % (D / 8);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(qg + g * D + c * 8);
+                        reinterpret_cast<uint4 *>(qreg_s + g * 2 * D)[c] =
+                            make_uint4(hmin0_bits(v.x), hmin0_bits(v.y), hmin0_bits(v.z), hmin0_bits(v.w));
+                        reinterpret_cast<uint4 *>(qreg_s + g * 2 * D + D)[c] =
+                            make_uint4(hmax0_bits(v.x), hmax0_bits(v.y), hmax0_bits(v.z), hmax0_bits(v.w));
+                    }
+                    named_bar_sync(1, C::NCW * 32);
+                }
+                for (int t = 0; t < ntile; ++t, ++it) {
+                    const int s = it % C::NSTAGE;
+                    const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
+                    bool ok = (*abort_flag == 0);
+                    if (ok) {
+                        if (lane == 0) ok = mbar_wait(smem_u32(&full[s]), ph, p.timeout_ns, abort_flag);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok && lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
+                    }
+                    const uint32_t sbase = smem_u32(ring + s * C::STAGE);
+#pragma unroll
+                    for (int pass = 0; pass < 2; ++pass) {
+                        const int row = warp * 16 + pass * 8 + jp;
+                        const int first = pr0 + t * C::MT + warp * 16 + pass * 8;
+                        if (!ok || first >= pr1) continue;  // warp-uniform
+                        const uint32_t base = sbase + (uint32_t)((cq0 / 64) * C::MBLK + row * 128);
+                        const uint32_t x0 = (uint32_t)(((cq0 % 64) / 8) ^ (row & 7));
+                        float uu[G];
+#pragma unroll
+                        for (int ps = 0; ps < C::NPASST; ++ps) {
+                            if (!C::QTREG) {
+#pragma unroll
+                                for (int g = 0; g < C::GQT; ++g)
+#pragma unroll
+                                    for (int c = 0; c < C::NCHQ; ++c)
+                                        qt[g][c] = lds128(smem_u32(qreg_s + (ps * C::GQT + g) * 2 * D + cq0 + c * 8));
+                            }
+                            float a0[C::GQT], a1[C::GQT];
+#pragma unroll
+                            for (int g = 0; g < C::GQT; ++g) a0[g] = a1[g] = 0.f;
+#pragma unroll
+                            for (int c = 0; c < C::NCHQ; ++c) {
+                                const uint4 mc = lds128(base + ((x0 ^ (uint32_t)c) << 4));
+#pragma unroll
+                                for (int g = 0; g < C::GQT; ++g) {
+                                    a0[g] = fma_h_lo(qt[g][c].x, mc.x, a0[g]);
+                                    a1[g] = fma_h_hi(qt[g][c].x, mc.x, a1[g]);
+                                    a0[g] = fma_h_lo(qt[g][c].y, mc.y, a0[g]);
+                                    a1[g] = fma_h_hi(qt[g][c].y, mc.y, a1[g]);
+                                    a0[g] = fma_h_lo(qt[g][c].z, mc.z, a0[g]);
+                                    a1[g] = fma_h_hi(qt[g][c].z, mc.z, a1[g]);
+                                    a0[g] = fma_h_lo(qt[g][c].w, mc.w, a0[g]);
+                                    a1[g] = fma_h_hi(qt[g][c].w, mc.w, a1[g]);
+                                }
+                            }
+#pragma unroll
+                            for (int g = 0; g < C::GQT; ++g) uu[ps * C::GQT + g] = a0[g] + a1[g];
+                        }
+                        float best = -INFINITY;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            float x = uu[g];
+                            x += __shfl_xor_sync(0xffffffffu, x, 8);
+                            x += __shfl_xor_sync(0xffffffffu, x, 16);
+                            best = fmaxf(best, x);
+                        }
+                        const int page = first + jp;
+                        if (qq == 0 && page < pr1) {
+                            keys[page - pr0] = score_key(best);
+                            if (p.scores != nullptr) p.scores[(int64_t)u * p.Pmax + page] = best;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+                }
+            }
+            __syncthreads();
+
+            // ================= 2. cluster top-K threshold =================
+            const int nloc = pr1 - pr0;
+            uint32_t kth = 0;
+            int need_eq = 0;
+            if (P > p.kpages) {
+                uint32_t prefix = 0, mask = 0;
+                int rem = p.kpages;
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int shift = 24 - 8 * pass;
+                    int *hb = hist + (pass & 1) * 256;
+                    for (int i = tid; i < 256; i += C::THREADS) hb[i] = 0;
+                    __syncthreads();
+                    for (int i = tid; i < nloc; i += C::THREADS) {
+                        const uint32_t key = keys[i];
+                        if ((key & mask) == prefix) atomicAdd(&hb[(key >> shift) & 255u], 1);
+                    }
+                    cluster_sync_all();
+                    for (int i = tid; i < 256; i += C::THREADS) {
+                        int tot = 0;
+                        for (uint32_t r = 0; r < nct; ++r) tot += (int)ld_dsmem_u32(dsmem_map(smem_u32(hb + i), r));
+                        tots[i] = tot;
+                    }
+                    __syncthreads();
+                    if (warp == 0) {
+                        int c[8], sum = 0;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            c[e] = tots[255 - 8 * lane - e];
+                            sum += c[e];
+                        }
+                        int incl = sum;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += y;
+                        }
+                        const int excl = incl - sum;
+                        if (excl < rem && rem <= incl) {
+                            int cum = excl;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                if (cum + c[e] >= rem) {
+                                    sh[0] = 255 - 8 * lane - e;
+                                    sh[1] = rem - cum;
+                                    break;
+                                }
+                                cum += c[e];
+                            }
+                        }
+                    }
+                    __syncthreads();
+                    prefix |= (uint32_t)sh[0] << shift;
+                    mask |= 255u << shift;
+                    rem = sh[1];
+                    __syncthreads();
+                }
+                kth = prefix;
+                need_eq = rem;
+            }
+
+            // ================= 3. compaction into the page list =================
+            if (P > p.kpages) {
+                const int chunk = (nloc + C::THREADS - 1) / C::THREADS;
+                const int c0 = tid * chunk < nloc ? tid * chunk : nloc;
+                const int c1 = c0 + chunk < nloc ? c0 + chunk : nloc;
+                int ngt = 0, neq = 0;
+                for (int i = c0; i < c1; ++i) {
+                    ngt += keys[i] > kth;
+                    neq += keys[i] == kth;
+                }
+                int ig = ngt, ie = neq;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int yg = __shfl_up_sync(0xffffffffu, ig, o);
+                    const int ye = __shfl_up_sync(0xffffffffu, ie, o);
+                    if (lane >= o) { ig += yg; ie += ye; }
+                }
+                if (lane == 31) { wsum[warp] = ig; wsum[9 + warp] = ie; }
+                __syncthreads();
+                int bg = 0, be = 0, tg = 0, te = 0;
+                for (int w = 0; w < C::NCW + 1; ++w) {
+                    if (w < warp) { bg += wsum[w]; be += wsum[9 + w]; }
+                    tg += wsum[w];
+                    te += wsum[9 + w];
+                }
+                if (tid == 0) { cnt[0] = tg; cnt[1] = te; }
+                cluster_sync_all();
+                int gt_before = 0, eq_before = 0;
+                for (uint32_t r = 0; r < crank; ++r) {
+                    gt_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[0]), r));
+                    eq_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[1]), r));
+                }
+                int eqr = eq_before + be + ie - neq;             // global rank among equal keys
+                int pos = gt_before + bg + ig - ngt + (eqr < need_eq ? eqr : need_eq);
+                for (int i = c0; i < c1; ++i) {
+                    const uint32_t key = keys[i];
+                    const bool take = key > kth || (key == kth && eqr < need_eq);
+                    eqr += key == kth;
+                    if (take) {
+                        const int page = pr0 + i;
+                        if (pos < p.kpages && pos < C::KSEL_MAX) {
+                            for (uint32_t r = 0; r < nct; ++r) st_dsmem_u32(dsmem_map(smem_u32(&list[pos]), r), (uint32_t)page);
+                            if (p.page_idx != nullptr) p.page_idx[(int64_t)u * p.kpages + pos] = page;
+                        }
+                        ++pos;
+                    }
+                }
+            } else {
+                for (int i = tid; i < P && i < C::KSEL_MAX; i += C::THREADS) list[i] = i;
+                if (p.page_idx != nullptr && crank == 0)
+                    for (int i = tid; i < P; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = i;
+            }
+            if (p.page_idx != nullptr && crank == 0)
+                for (int i = nsel + tid; i < p.kpages; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = -1;
+            cluster_sync_all();  // the page list is complete in every CTA
+        }
+
+        // ================= 4. attention over this CTA's share of the pages =================
+        const int e0 = (int)(((int64_t)crank * nsel) / nct);
+        const int e1 = (int)(((int64_t)(crank + 1) * nsel) / nct);
+        const int ntile4 = (e1 - e0 + C::NCW - 1) / C::NCW;
+        if (producer) {
+            for (int t = 0; t < ntile4; ++t, ++it) {
+                const int s = it % C::NSTAGE;
+                const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
+                if (it >= C::NSTAGE) {
+                    bool ok = (*abort_flag == 0);
+                    if (ok && lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.timeout_ns, abort_flag);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
+                        continue;
+                    }
+                }
+                if (*abort_flag) continue;
+                const int e = e0 + t * C::NCW + lane;
+                int page = -1;
+                if (lane < C::NCW && e < e1)
+                    page = (MODE == FUSED_FULL) ? list[e] : p.page_idx[(int64_t)u * p.kpages + e];
+                const bool ok = lane < C::NCW && e < e1 && page >= 0 && page < P;
+                if (MODE == FUSED_ATTEND && lane < C::NCW && e < e1 && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
+                if (lane < C::NCW) {
+                    const int rem = ok ? len - page * p.S : 0;
+                    tinfo[s * 8 + lane] = rem < C::SUB ? rem : C::SUB;
+                }
+                const unsigned m = __ballot_sync(0xffffffffu, ok);
+                __syncwarp();
+                const uint32_t kdst = smem_u32(ring + s * C::STAGE);
+                const uint32_t vdst = kdst + C::KBYTES;
+                const uint32_t fb = smem_u32(&full[s]);
+                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(C::SUB * D * 2 * 2));
+#pragma unroll
+                for (int j = 0; j < C::NCW; ++j) {
+                    const int pj = __shfl_sync(0xffffffffu, page, j);
+                    if (lane == 0 && ((m >> j) & 1u)) {
+                        const int y = u * p.Lmax + pj * p.S;
+#pragma unroll
+                        for (int kh = 0; kh < C::KH; ++kh)
+                            tma_load_2d(kdst + kh * C::KBLK + j * C::SUB * 128, &kmap, 64 * kh, y, fb, pol);
+                        tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
+                    }
+                }
+                __syncwarp();
+            }
+        } else {
+            if (C::QREG) {
+                wa.load_q(qg);
+            } else {
+                for (int e = tid; e < G * D / 8; e += C::NCW * 32)
+                    reinterpret_cast<uint4 *>(qreg_s)[e] = reinterpret_cast<const uint4 *>(qg)[e];
+                named_bar_sync(1, C::NCW * 32);
+            }
+            wa.reset();
+            for (int t = 0; t < ntile4; ++t, ++it) {
+                const int s = it % C::NSTAGE;
+                const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
+                bool ok = (*abort_flag == 0);
+                if (ok) {
+                    if (lane == 0) ok = mbar_wait(smem_u32(&full[s]), ph, p.timeout_ns, abort_flag);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok && lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
+                }
+                const int nv = ok ? tinfo[s * 8 + warp] : 0;
+                if (nv > 0) {
+                    const uint32_t kbase = smem_u32(ring + s * C::STAGE);
+                    wa.tile(kbase, kbase + C::KBYTES, nv, p.scale_log2, qreg_s);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            }
+            // ---- merge the 8 warp states into this CTA's state ----
+            wa.store_state(merge);
+            named_bar_sync(1, C::NCW * 32);
+            for (int idx = tid; idx < G * D; idx += C::NCW * 32) {
+                const int g = idx / D, d = idx - (idx / D) * D;
+                float mst, ls, as;
+                merge_warps<D, G>(merge, g, d, mst, ls, as);
+                cstate[g * (D + 2) + 2 + d] = as;
+                if (d == 0) {
+                    cstate[g * (D + 2)] = mst;
+                    cstate[g * (D + 2) + 1] = ls;
+                }
+            }
+        }
+        cluster_sync_all();  // every CTA's state is complete
+
+        // ================= 5. log-sum-exp merge across the cluster =================
+        {
+            const int per = (G * D + (int)nct - 1) / (int)nct;
+            const int i0 = (int)crank * per;
+            const int i1 = i0 + per < G * D ? i0 + per : G * D;
+            for (int idx = i0 + tid; idx < i1; idx += C::THREADS) {
+                const int g = idx / D, d = idx - (idx / D) * D;
+                const uint32_t mloc = smem_u32(cstate + g * (D + 2));
+                float mst = -INFINITY;
+                for (uint32_t r = 0; r < nct; ++r) mst = fmaxf(mst, ld_dsmem_f32(dsmem_map(mloc, r)));
+                float ls = 0.f, as = 0.f;
+                for (uint32_t r = 0; r < nct; ++r) {
+                    const uint32_t base = dsmem_map(mloc, r);
+                    const float mr = ld_dsmem_f32(base);
+                    if (mr != -INFINITY) {
+                        const float f = fast_exp2(mr - mst);
+                        ls += f * ld_dsmem_f32(base + 4);
+                        as += f * ld_dsmem_f32(base + (uint32_t)(8 + 4 * d));
+                    }
+                }
+                p.out[((int64_t)b * Hq + (int64_t)kv * G + g) * D + d] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
+            }
+        }
+        cluster_sync_all();  // before the next unit reuses keys, list and state
+    }
+
+    // If a wait gave up, let this CTA's copies in flight land before it retires.
+    if (producer && lane == 0 && *abort_flag) {
+        const int first = it - C::NSTAGE > 0 ? it - C::NSTAGE : 0;
+        for (int k = first; k < it; ++k)
+            mbar_wait(smem_u32(&full[k % C::NSTAGE]), (uint32_t)(k / C::NSTAGE) & 1u, p.timeout_ns, nullptr);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kMaxDev = 64;
+
+template <int D, int G, int MODE>
+int active_clusters(int device, int csize, int *out) {
+    using C = FusedCfg<D, G>;
+    static int cache[kMaxDev][4] = {};
+    static bool attr[kMaxDev] = {};
+    const int ci = csize == 1 ? 0 : csize == 2 ? 1 : csize == 4 ? 2 : 3;
+    auto kern = quest_fused_kernel<D, G, MODE>;
+    if (!attr[device]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return GQAQ_ERR_CUDA;
+        attr[device] = true;
+    }
+    if (cache[device][ci] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(csize * 64, 1, 1);
+        cfg.blockDim = dim3(C::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = csize;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        cache[device][ci] = n > 0 ? n : -1;
+    }
+    *out = cache[device][ci];
+    return GQAQ_OK;
+}
+
+template <int D, int G, int MODE>
+int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
+    using C = FusedCfg<D, G>;
+    const gqaq_dims &dm = *a.dims;
+    const int Pmax = (dm.max_len + dm.page_size - 1) / dm.page_size;
+    const int units = dm.batch * dm.num_kv_heads;
+    if (a.kpages > C::KSEL_MAX) return GQAQ_ERR_UNSUPPORTED;
+    if (ctx.device < 0 || ctx.device >= kMaxDev) return GQAQ_ERR_CUDA;
+    // cluster size: smallest C minimising ceil(units / clusters) / C, with Pmax / C <= KEYS_MAX
+    int best_c = 0, best_n = 0;
+    double best_cost = 1e30;
+    for (int csize = 1; csize <= 8; csize *= 2) {
+        if (MODE == FUSED_FULL && (Pmax + csize - 1) / csize > C::KEYS_MAX) continue;
+        if (ctx.cluster_size > 0 && csize != ctx.cluster_size) continue;
+        int n = 0;
+        if (active_clusters<D, G, MODE>(ctx.device, csize, &n) != GQAQ_OK) return GQAQ_ERR_CUDA;
+        if (n <= 0) continue;
+        if (ctx.max_ctas > 0) n = n < ctx.max_ctas / csize ? n : (ctx.max_ctas / csize > 0 ? ctx.max_ctas / csize : 1);
+        const double cost = (double)((units + n - 1) / n) / csize;
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best_c = csize;
+            best_n = n;
+        }
+    }
+    if (best_c == 0) return GQAQ_ERR_UNSUPPORTED;
+    const int nclusters = units < best_n ? units : best_n;
+
+    const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
+    CUtensorMap mmap, kmap, vmap;
+    if (MODE == FUSED_FULL) {
+        const uint64_t mrows = (uint64_t)dm.batch * dm.num_kv_heads * Pmax;
+        if (!encode_tensor_map_2d(&mmap, a.meta, mrows, 2 * D, 64, C::MT, true)) return GQAQ_ERR_CUDA;
+    } else {
+        memset(&mmap, 0, sizeof(mmap));
+    }
+    if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, C::SUB, true)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, C::SUB, false)) return GQAQ_ERR_CUDA;
+
+    FusedParams p;
+    p.q = a.q;
+    p.valid_len = a.valid_len;
+    p.pos = a.pos;
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
+    p.meta = a.meta;
+    p.scores = a.scores;
+    p.page_idx = a.page_idx;
+    p.out = a.out;
+    p.status = ctx.status;
+    p.B = dm.batch;
+    p.Hkv = dm.num_kv_heads;
+    p.Lmax = dm.max_len;
+    p.Pmax = Pmax;
+    p.S = dm.page_size;
+    p.kpages = a.kpages;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.timeout_ns = ctx.timeout_ns;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nclusters * best_c, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = best_c;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, quest_fused_kernel<D, G, MODE>, mmap, kmap, vmap, p) != cudaSuccess)
+        return GQAQ_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
+}
+
+template <int D, int MODE>
+int fused_g(const FusedArgs &a, const LaunchCtx &ctx) {
+    switch (a.dims->num_q_heads / a.dims->num_kv_heads) {
+        case 1: return launch_fused_t<D, 1, MODE>(a, ctx);
+        case 2: return launch_fused_t<D, 2, MODE>(a, ctx);
+        case 4: return launch_fused_t<D, 4, MODE>(a, ctx);
+        case 8: return launch_fused_t<D, 8, MODE>(a, ctx);
+        default: return GQAQ_ERR_UNSUPPORTED;
+    }
+}
+}  // namespace
+
+int launch_quest_fused(const FusedArgs &a, const LaunchCtx &ctx) {
+    const bool attend_only = a.meta == nullptr;
+    switch (a.dims->head_dim) {
+        case 64: return attend_only ? fused_g<64, FUSED_ATTEND>(a, ctx) : fused_g<64, FUSED_FULL>(a, ctx);
+        case 128: return attend_only ? fused_g<128, FUSED_ATTEND>(a, ctx) : fused_g<128, FUSED_FULL>(a, ctx);
+        default: return GQAQ_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace gqaq

@@ -8,6 +8,10 @@ pick the top ``k_pages``, and attend over those pages only. When a step
 carries a new token, every layer first appends it (``quest_append_kv``), so
 each layer's page metadata stays current whatever path reads it.
 
+By default a Quest layer is one fused launch (``quest_decode_attn``: append,
+score, top-K and sparse attention in one thread-block-cluster kernel). With
+``fused=False`` the same layer runs as the four step-by-step calls.
+
 This module only sequences library calls and owns the scratch buffers they
 share. Every arithmetic step runs in the CUDA kernels.
 """
@@ -20,7 +24,8 @@ from typing import List, Optional
 import torch
 
 from . import (alloc_workspace, gqa_decode_attn, make_dims, new_meta, num_pages, quest_append_kv,
-               quest_score_pages, quest_sparse_attn, quest_topk_pages, quest_update_meta)
+               quest_decode_attn, quest_score_pages, quest_sparse_attn, quest_topk_pages,
+               quest_update_meta)
 
 
 @dataclasses.dataclass
@@ -39,7 +44,8 @@ class Layer:
 
 class DecodeStack:
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_len: int,
-                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16):
+                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True):
+        self.fused = fused
         self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
         self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
         self.k_pages, self.dense_layers = k_pages, dense_layers
@@ -63,21 +69,58 @@ class DecodeStack:
         """Metadata of the pages already in the cache (after a prefill)."""
         quest_update_meta(layer.k_cache, valid_len, layer.meta, page_size=self.page_size)
 
-    def launches_per_step(self, num_layers: int, append: bool) -> int:
-        """Kernels one step launches (append 1, dense 2, Quest 4)."""
-        n = 0
-        for i in range(num_layers):
-            n += 1 if append else 0
-            n += 2 if self.is_dense(i) else 4
-        return n
+    def families(self, layers: List[Layer]):
+        """The library calls of one step, grouped by kind: name -> list of thunks."""
+        fam = {}
+
+        def add(name, fn):
+            fam.setdefault(name, []).append(fn)
+
+        for i, L in enumerate(layers):
+            dense = self.is_dense(i)
+            if L.k_new is not None and (dense or not self.fused):
+                add("append", lambda L=L: quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos,
+                                                          self.page_size))
+            if dense:
+                add("dense", lambda L=L: gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale,
+                                                         out=L.out, workspace=self.workspace))
+            elif self.fused:
+                add("quest", lambda L=L: quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len,
+                                                           self.k_pages, self.scale, k_new=L.k_new, v_new=L.v_new,
+                                                           pos=L.pos, out=L.out, page_size=self.page_size))
+            else:
+                add("score", lambda L=L: quest_score_pages(L.q, L.meta, L.valid_len, self.max_len,
+                                                           scores=self.scores, page_size=self.page_size))
+                add("topk", lambda L=L: quest_topk_pages(self.scores, L.valid_len, self.k_pages, self.max_len,
+                                                         page_idx=self.page_idx, page_size=self.page_size))
+                add("sparse", lambda L=L: quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.page_idx,
+                                                            self.scale, out=L.out, workspace=self.workspace,
+                                                            page_size=self.page_size))
+        return fam
+
+    @staticmethod
+    def kernels_per_call(name: str, k_pages: Optional[int]) -> int:
+        """Kernel launches behind one call of a family."""
+        if name == "dense":
+            return 2                       # split-context partials + combine
+        if name == "sparse":
+            return 1 if k_pages is not None and k_pages <= 1024 else 2
+        return 1
+
+    def launches_per_step(self, layers: List[Layer]) -> int:
+        return sum(len(v) * self.kernels_per_call(k, self.k_pages) for k, v in self.families(layers).items())
 
     def step(self, layers: List[Layer]):
         for i, L in enumerate(layers):
-            if L.k_new is not None:
+            dense = self.is_dense(i)
+            if L.k_new is not None and (dense or not self.fused):
                 quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos, self.page_size)
-            if self.is_dense(i):
+            if dense:
                 gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale, out=L.out,
                                 workspace=self.workspace)
+            elif self.fused:
+                quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages, self.scale,
+                                  k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out, page_size=self.page_size)
             else:
                 quest_score_pages(L.q, L.meta, L.valid_len, self.max_len, scores=self.scores,
                                   page_size=self.page_size)

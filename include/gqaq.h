@@ -160,6 +160,23 @@ GQAQ_API int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const 
                       int k, float scale, gqaq_half *out, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* Fused Quest decode step, one launch per layer. It does, in order, what
+ * quest_append_kv, quest_score_pages, quest_topk_pages and quest_sparse_attn
+ * do: when pos is not NULL, append k_new/v_new at row pos[b] and update that
+ * page's min/max; score every valid page; select the k best pages (ties to
+ * the lower index); attend over only their tokens ([QUEST] flowchart). One
+ * thread-block cluster handles one (sequence, KV head) at a time: its CTAs
+ * split the pages, agree on the K-th score through distributed shared memory,
+ * split the selected pages and merge their softmax states there. So the
+ * call needs no workspace. scores ([B][Hkv][Pmax] fp32) and page_idx
+ * ([B][Hkv][k] int32, ascending, -1 padded) are optional outputs (NULL to
+ * skip). Requires 1 <= k <= 1024 (GQAQ_ERR_UNSUPPORTED above), S = 16. */
+GQAQ_API int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_cache,
+                               gqaq_half *v_cache, gqaq_half *meta, const gqaq_half *k_new,
+                               const gqaq_half *v_new, const int32_t *pos, const int32_t *valid_len,
+                               int k, float scale, gqaq_half *out, float *scores, int32_t *page_idx,
+                               void *stream);
+
 /* gqa_decode_attn for callers that cannot allocate device memory. The source
  * pages have no counterpart to this call. A plugin or custom operator inside a
  * host framework is often handed only its input and output pointers: the
@@ -189,9 +206,11 @@ enum {
     GQAQ_OPT_MAX_CTAS = 1,        /* cap on the persistent grid of the attention and
                                      score kernels; 0 = one wave of resident CTAs */
     GQAQ_OPT_WAIT_TIMEOUT_NS = 2, /* bound on every in-kernel wait; default 2e9 */
-    GQAQ_OPT_TEST_STALL = 3       /* nonzero: the attention kernels' producer issues
+    GQAQ_OPT_TEST_STALL = 3,      /* nonzero: the attention kernels' producer issues
                                      no copy, so every consumer wait runs out
                                      (exercises the timeout path; outputs undefined) */
+    GQAQ_OPT_CLUSTER_SIZE = 4     /* CTAs per cluster of the fused Quest kernel (1, 2,
+                                     4 or 8); 0 = chosen from the SM count and shape */
 };
 GQAQ_API int gqaq_set_option(int option, int64_t value);
 

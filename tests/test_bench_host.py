@@ -31,9 +31,13 @@ def test_step_bytes_of_the_workloads():
     kv = 2 * bench.roofline_unit_bytes(w, "dense", lens[0])
     q = 30 * (bench.roofline_unit_bytes(w, "score", lens[2]) + bench.roofline_unit_bytes(w, "sparse", lens[2]))
     assert kv + q == 3_087_007_744
-    sb = bench.step_bytes(w, lens)
+    sb = bench.step_bytes(w, lens, fused=False)
     assert sb["launches"] == {"dense": 2, "score": 30, "topk": 30, "sparse": 30, "append": 32}
     assert 0 < sb["total"] - (kv + q) < 0.01 * (kv + q)          # q/out/scores/append are small
+    sf = bench.step_bytes(w, lens, fused=True)
+    assert sf["launches"] == {"dense": 2, "quest": 30, "append": 2}
+    assert 0 < sf["total"] - (kv + q) < sb["total"] - (kv + q)   # no score / page-list traffic
+    assert bench.roofline_unit_bytes(w, "quest", lens[2]) == 2 * 2 ** 20 * 32
     # EXAONE-shaped dense: 8 MiB for one full 4096-token layer at batch 1
     w1 = workloads.WORKLOADS[1]
     assert bench.roofline_unit_bytes(w1, "dense", [4096]) == 8 * 2 ** 20

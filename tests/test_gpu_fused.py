@@ -1,0 +1,152 @@
+"""GPU parity of quest_decode_attn, the fused Quest step (append, page scores,
+top-K, sparse attention in one cluster kernel), against the fp64 oracle.
+
+Cluster sizes 1, 2, 4 and 8 are forced so the cross-CTA paths (radix
+threshold from summed histograms, page-list compaction, log-sum-exp merge
+through distributed shared memory) all run, including CTAs whose page range
+or page share is empty.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_head_folding_gb300 as g
+import oracle
+import workloads
+from _util import assert_attn_close, check_topk, score_tolerance, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+S = 16
+
+
+@pytest.fixture(autouse=True)
+def _reset_options():
+    yield
+    g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, 0)
+    g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
+
+
+def run_fused(D, G, K, csize, B=3, Hkv=2, Lmax=16 * 45 + 3, valid=(16 * 45 + 3, 16 * 23 + 7, 20), seed=0,
+              append=True):
+    g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, csize)
+    w = workloads.Workload(0, "fused", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax, k_pages=K, n_plant=3, append=True)
+    x = workloads.make_layer(w, 0, device="cpu", seed=seed)
+    vl = np.array(valid[:B])
+    kd, vd = x["k_cache"].to(DEV), x["v_cache"].to(DEV)
+    vld = torch.tensor(vl, dtype=torch.int32, device=DEV)
+    meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+    pos = torch.tensor(vl - 1, dtype=torch.int32)
+    g.quest_update_meta(kd, vld - 1 if append else vld, meta)
+    scores = torch.full((B, Hkv, g.num_pages(Lmax)), float("nan"), dtype=torch.float32, device=DEV)
+    idx = torch.full((B, Hkv, K), -7, dtype=torch.int32, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+    kw = dict(k_new=x["k_new"].to(DEV), v_new=x["v_new"].to(DEV), pos=pos.to(DEV)) if append else {}
+    out = g.quest_decode_attn(x["q"].to(DEV), kd, vd, meta, vld, K, scale, scores=scores, page_idx=idx, **kw)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+
+    kc = x["k_cache"].numpy().copy(); vc = x["v_cache"].numpy().copy()
+    if append:
+        for b in range(B):
+            kc[b, :, vl[b] - 1] = x["k_new"][b].numpy(); vc[b, :, vl[b] - 1] = x["v_new"][b].numpy()
+    assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(vd.cpu().numpy(), vc)
+    ref_meta = oracle.page_minmax(kc, vl, S)
+    got_meta = to64(meta)
+    ref_scores = oracle.page_scores(x["q"].numpy(), ref_meta, vl, S)
+    tol = score_tolerance(oracle.f16_to_f64(x["q"].numpy()), ref_meta, G)
+    got_scores = scores.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        P = (vl[b] + S - 1) // S
+        assert np.array_equal(got_meta[b, :, :P], ref_meta[b, :, :P]), f"meta b={b}"
+        assert np.all(np.abs(got_scores[b, :, :P] - ref_scores[b, :, :P]) <= tol[b, :, :P]), f"scores b={b}"
+    sel = idx.cpu().numpy()
+    check_topk(sel, ref_scores, vl, S, K)
+    ref = oracle.sparse_attn(x["q"].numpy(), kc, vc, vl, sel, S, scale)
+    assert_attn_close(out, ref)
+    return out, sel
+
+
+@pytest.mark.parametrize("D,G,K,csize", [
+    (128, 4, 8, 0), (128, 4, 8, 1), (128, 4, 8, 2), (128, 4, 16, 4), (128, 1, 16, 8),
+    (64, 4, 5, 2), (64, 2, 40, 0), (128, 8, 3, 2), (64, 8, 7, 4), (64, 1, 12, 1), (128, 2, 30, 8),
+])
+def test_fused_matches_oracle(D, G, K, csize):
+    run_fused(D, G, K, csize, seed=D + 10 * G + K + csize)
+
+
+@pytest.mark.parametrize("csize", [1, 4])
+def test_fused_without_append(csize):
+    run_fused(128, 4, 9, csize, append=False, seed=77)
+
+
+@pytest.mark.parametrize("csize", [2, 8])
+def test_fused_with_every_page_selected_equals_dense(csize):
+    B, Hkv, D, G, Lmax = 2, 2, 128, 4, 16 * 12 + 5
+    g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, csize)
+    w = workloads.Workload(0, "fused", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax)
+    x = workloads.make_layer(w, 0, device=DEV, seed=5)
+    vl = torch.tensor([Lmax, 33], dtype=torch.int32, device=DEV)
+    meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+    g.quest_update_meta(x["k_cache"], vl, meta)
+    idx = torch.empty(B, Hkv, 20, dtype=torch.int32, device=DEV)
+    sp = g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, vl, 20, 0.1, page_idx=idx)
+    ref = oracle.attn_repeat_kv(x["q"].cpu().numpy(), x["k_cache"].cpu().numpy(), x["v_cache"].cpu().numpy(),
+                                vl.cpu().numpy(), 0.1)
+    assert_attn_close(sp, ref)
+    for b, P in enumerate([13, 3]):
+        assert idx[b, :, :P].tolist() == [list(range(P))] * Hkv
+        assert bool((idx[b, :, P:] == -1).all())
+
+
+def test_fused_repeatable_and_graph_capturable():
+    w = workloads.WORKLOADS[4].with_(batch=3, max_len=16 * 300)
+    x = workloads.make_layer(w, 0, device=DEV)
+    B, Hkv, Lmax, D = x["k_cache"].shape
+    meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+    g.quest_update_meta(x["k_cache"], x["valid_len"] - 1, meta)
+    out = torch.empty_like(x["q"])
+    idx = torch.empty(B, Hkv, 64, dtype=torch.int32, device=DEV)
+
+    def step():
+        g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], 64, 0.088,
+                            k_new=x["k_new"], v_new=x["v_new"], pos=x["pos"], out=out, page_idx=idx)
+
+    step()
+    first_out, first_idx = out.clone(), idx.clone()
+    step()                                              # re-appending the same token is idempotent
+    assert torch.equal(out, first_out) and torch.equal(idx, first_idx)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_(); idx.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, first_out) and torch.equal(idx, first_idx)
+
+
+def test_sparse_call_above_the_fused_page_limit():
+    # k > 1024 selected pages goes through the split-context kernel + combine
+    B, Hkv, D, G, Lmax = 1, 2, 64, 4, 16 * 1200
+    w = workloads.Workload(0, "big-k", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax)
+    x = workloads.make_layer(w, 0, device=DEV, seed=2)
+    K = 1100
+    rng = np.random.default_rng(0)
+    sel = np.sort(np.stack([rng.choice(1200, K, replace=False) for _ in range(Hkv)]), axis=1)[None].astype(np.int32)
+    vl = x["valid_len"]
+    out = g.quest_sparse_attn(x["q"], x["k_cache"], x["v_cache"], vl, torch.from_numpy(sel).to(DEV), 0.125)
+    ref = oracle.sparse_attn(x["q"].cpu().numpy(), x["k_cache"].cpu().numpy(), x["v_cache"].cpu().numpy(),
+                             vl.cpu().numpy(), sel, S, 0.125)
+    assert_attn_close(out, ref)
+    with pytest.raises(g.GqaqError):
+        meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+        g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, vl, K, 0.125)
