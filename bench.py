@@ -352,7 +352,7 @@ def workload_from_args(args) -> workloads.Workload:
     return w
 
 
-def config_of(w: workloads.Workload, world: int, fused: bool = True) -> dict:
+def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool = True) -> dict:
     return {"workload": f"{w.name} (config {w.id})", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
             "layers": w.num_layers, "dense_layers": w.num_layers if w.k_pages is None else w.dense_layers,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
@@ -361,6 +361,7 @@ def config_of(w: workloads.Workload, world: int, fused: bool = True) -> dict:
             "token_budget": None if w.k_pages is None else w.k_pages * w.page_size,
             "append": w.append, "planted_pages_per_head": w.n_plant, "parallelism": f"replicas x{world}",
             "quest_path": "fused (quest_decode_attn)" if fused else "step-by-step calls",
+            "launch": "programmatic dependent launch" if pdl else "plain stream order",
             "l2": "per-step working set > 4x L2; no flush"}
 
 
@@ -407,6 +408,7 @@ def run_ours(args, rank, world, local):
     dist = init_dist(world, "nccl")
     w = workload_from_args(args)
     g.lib()
+    g.set_option(g.GQAQ_OPT_PDL, 0 if args.no_pdl else 1)
     stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused)
     sb = step_bytes(w, lens, fused=not args.unfused)
     step = lambda: stack.step(layers)  # noqa: E731
@@ -494,7 +496,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16 in/out, f32 accumulate",
-        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused),
+        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl),
         "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
         "achieved_frac_of_peak": round(sb["total"] / s_per_step / 1e9 / peaks["hbm_gbs"], 4),
         "bytes_per_step": total_bytes,
@@ -526,6 +528,7 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="run Quest layers as the step-by-step calls")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":

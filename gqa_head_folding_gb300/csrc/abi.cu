@@ -23,6 +23,7 @@ std::atomic<int64_t> g_opt_max_ctas{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cluster_size{0};
+std::atomic<int64_t> g_opt_pdl{1};
 
 struct DeviceState {
     bool ready = false;
@@ -70,6 +71,7 @@ int make_ctx(LaunchCtx *ctx, void *stream) {
     ctx->timeout_ns = (uint64_t)g_opt_timeout_ns.load();
     ctx->test_stall = (int)g_opt_test_stall.load();
     ctx->cluster_size = (int)g_opt_cluster_size.load();
+    ctx->pdl = (int)g_opt_pdl.load();
     ctx->status = s->status;
     return GQAQ_OK;
 }
@@ -148,6 +150,9 @@ int gqaq_set_option(int option, int64_t value) {
             return GQAQ_OK;
         case GQAQ_OPT_TEST_STALL:
             g_opt_test_stall.store(value != 0 ? 1 : 0);
+            return GQAQ_OK;
+        case GQAQ_OPT_PDL:
+            g_opt_pdl.store(value != 0 ? 1 : 0);
             return GQAQ_OK;
         case GQAQ_OPT_CLUSTER_SIZE:
             if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return GQAQ_ERR_INVALID_ARG;

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     const int lane = threadIdx.x & 31;
     const int Hq = p.Hkv * G;
 
+    pdl_wait_and_release();
     TileRule rule;
     rule.sparse = SPARSE ? 1 : 0;
     rule.lmax = p.Lmax;
@@ -346,6 +347,7 @@ struct CombineParams {
 
 template <int D, int G>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
+    pdl_wait_and_release();
     const int kv = blockIdx.x, b = blockIdx.y;
     TileRule rule;
     rule.sparse = p.sparse;
@@ -469,8 +471,9 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_ns = ctx.timeout_ns;
     p.test_stall = ctx.test_stall;
-    attn_partial_kernel<D, G, SPARSE><<<grid, C::THREADS, C::SMEM, ctx.stream>>>(kmap, vmap, p);
-    if (cudaGetLastError() != cudaSuccess) return GQAQ_ERR_CUDA;
+    if (launch_kernel(attn_partial_kernel<D, G, SPARSE>, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, kmap, vmap,
+                      p) != cudaSuccess)
+        return GQAQ_ERR_CUDA;
 
     CombineParams cp;
     cp.valid_len = a.valid_len;
@@ -486,8 +489,9 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     cp.tile_tokens = C::TILE;
     cp.pages_per_tile = C::NCW;
     cp.grid = grid;
-    attn_combine_kernel<D, G><<<dim3(dm.num_kv_heads, dm.batch), 128, 0, ctx.stream>>>(cp);
-    if (cudaGetLastError() != cudaSuccess) return GQAQ_ERR_CUDA;
+    if (launch_kernel(attn_combine_kernel<D, G>, dim3(dm.num_kv_heads, dm.batch), dim3(128), 0, ctx, 0, cp) !=
+        cudaSuccess)
+        return GQAQ_ERR_CUDA;
     return GQAQ_OK;
 }
 

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/gqaq.h"
 
 namespace gqaq {
@@ -23,6 +25,7 @@ struct LaunchCtx {
     uint64_t timeout_ns;   // bound on every in-kernel wait
     int test_stall;        // attention producer issues nothing (timeout test)
     int cluster_size;      // fused Quest kernel: forced CTAs per cluster, 0 = automatic
+    int pdl;               // launch with programmatic stream serialization
     int *status;           // device status word
 };
 
@@ -159,8 +162,47 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// running. It must wait here before touching global memory that the previous
+// kernel writes or reads. It lets its own dependents launch at once: they
+// wait in the same way for this grid to finish.
+__device__ __forceinline__ void pdl_wait_and_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_flag(int *status, int flag) {
     if (status != nullptr) atomicOr(status, flag);
+}
+
+// Host: launch `kern` on ctx.stream, optionally as a cluster of `cluster`
+// CTAs, with programmatic stream serialization when ctx.pdl is set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, const LaunchCtx &ctx,
+                                 int cluster, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute at[2];
+    int n = 0;
+    if (cluster > 0) {
+        at[n].id = cudaLaunchAttributeClusterDimension;
+        at[n].val.clusterDim.x = (unsigned)cluster;
+        at[n].val.clusterDim.y = 1;
+        at[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (ctx.pdl) {
+        at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = (unsigned)n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------

@@ -35,6 +35,7 @@ struct AppendParams {
 
 template <int D>
 __global__ void __launch_bounds__(128) append_kv_kernel(const AppendParams p) {
+    pdl_wait_and_release();
     constexpr int EPL = D / 32;
     const int u = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -88,6 +89,7 @@ struct MetaParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) update_meta_kernel(const MetaParams p) {
+    pdl_wait_and_release();
     constexpr int EPL = D / 32;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -190,6 +192,7 @@ __global__ void __launch_bounds__(ScoreCfg<D, G>::THREADS, 1)
     int64_t *sch = reinterpret_cast<int64_t *>(empty + C::NSTAGE);  // t_begin, t_end, off_b, b
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sch + 4);
 
+    pdl_wait_and_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hq = p.Hkv * G;
     TileRule rule;
@@ -404,6 +407,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const TopkPara
     __shared__ int hist[256];
     __shared__ int sh_digit, sh_rem;
     __shared__ int wsum[2][kTopkThreads / 32];
+    pdl_wait_and_release();
     const int kv = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t unit = (int64_t)b * p.Hkv + kv;
@@ -515,8 +519,9 @@ int launch_append_t(const gqaq_dims *d, __half *kc, __half *vc, __half *meta, co
     p.B = d->batch; p.Hkv = d->num_kv_heads; p.Lmax = d->max_len; p.S = d->page_size;
     p.Pmax = (d->max_len + d->page_size - 1) / d->page_size;
     const int units = d->batch * d->num_kv_heads;
-    append_kv_kernel<D><<<(units + 3) / 4, 128, 0, ctx.stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
+    return launch_kernel(append_kv_kernel<D>, dim3((units + 3) / 4), dim3(128), 0, ctx, 0, p) == cudaSuccess
+               ? GQAQ_OK
+               : GQAQ_ERR_CUDA;
 }
 
 template <int D>
@@ -531,8 +536,9 @@ int launch_meta_t(const gqaq_dims *d, const __half *kc, const int *vl, __half *m
     if (warps == 0) return GQAQ_OK;
     const int64_t blocks = (warps + 7) / 8;
     if (blocks > 0x7fffffff) return GQAQ_ERR_UNSUPPORTED;
-    update_meta_kernel<D><<<(unsigned)blocks, 256, 0, ctx.stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
+    return launch_kernel(update_meta_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, ctx, 0, p) == cudaSuccess
+               ? GQAQ_OK
+               : GQAQ_ERR_CUDA;
 }
 
 template <int D, int G>
@@ -560,8 +566,9 @@ int launch_score_t(const gqaq_dims *d, const __half *q, const __half *meta, cons
     p.q = q; p.valid_len = vl; p.scores = scores; p.status = ctx.status;
     p.B = d->batch; p.Hkv = d->num_kv_heads; p.Lmax = d->max_len; p.Pmax = Pmax; p.S = d->page_size;
     p.timeout_ns = ctx.timeout_ns;
-    kern<<<grid, C::THREADS, C::SMEM, ctx.stream>>>(mmap, p);
-    return cudaGetLastError() == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
+    return launch_kernel(kern, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, mmap, p) == cudaSuccess
+               ? GQAQ_OK
+               : GQAQ_ERR_CUDA;
 }
 
 template <int D>
@@ -621,8 +628,10 @@ int launch_topk_pages(const gqaq_dims *d, const float *scores, const int *vl, in
     p.scores = scores; p.valid_len = vl; p.page_idx = page_idx; p.status = ctx.status;
     p.B = d->batch; p.Hkv = d->num_kv_heads; p.Lmax = d->max_len; p.Pmax = Pmax; p.S = d->page_size;
     p.k = k;
-    topk_pages_kernel<<<dim3(d->num_kv_heads, d->batch), kTopkThreads, smem, ctx.stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
+    return launch_kernel(topk_pages_kernel, dim3(d->num_kv_heads, d->batch), dim3(kTopkThreads), smem, ctx, 0, p) ==
+                   cudaSuccess
+               ? GQAQ_OK
+               : GQAQ_ERR_CUDA;
 }
 
 }  // namespace gqaq

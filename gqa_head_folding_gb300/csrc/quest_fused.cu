@@ -102,10 +102,16 @@ struct FusedCfg : TileCfg<D, G> {
     static constexpr int QT_BYTES = G * 2 * D * 2;  // [G][2D] fp16 [q_neg | q_pos]
     static constexpr int QREGION = (QT_BYTES > T::QBYTES) ? QT_BYTES : T::QBYTES;
     static constexpr int CSTATE = G * (D + 2) * 4;
-    static constexpr int MISC = 2048;               // hist x2, totals, tile info, barriers, counters
+    // misc region, in 4-byte words: hist [0,512), totals [512,768), tile info
+    // [768,800), counts [800,808), scan scratch [808,832), scalars [832,848),
+    // then the full/empty mbarriers (8-byte aligned) at word 848.
+    static constexpr int MISC_BARRIER_WORD = 848;
+    static constexpr int MISC = MISC_BARRIER_WORD * 4 + 2 * 3 * 8;
     static constexpr int FIXED = KEYMERGE + QREGION + T::PBYTES + KSEL_MAX * 4 + CSTATE + MISC + 1024;
     static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
     static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
+    static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
+    static_assert(NSTAGE * 8 <= 32, "tile info slots");
     static constexpr int NCHQ = D / 16;             // 16-byte chunks per record quarter
     static constexpr bool QTREG = (G * D <= 512);
     static constexpr int GQT = QTREG ? G : 4;
@@ -149,8 +155,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     int *tinfo = misc + 768;              // [NSTAGE][8] valid tokens per page of a stage
     int *cnt = misc + 800;                // [2] this CTA's (> kth, == kth) counts
     int *wsum = misc + 808;               // [2][9] block-scan scratch
-    int *sh = misc + 832;                 // [0] digit, [1] remaining, [2] abort
-    uint64_t *full = reinterpret_cast<uint64_t *>(misc + 848);
+    int *sh = misc + 832;                 // [0] bin, [1] remaining, [2] abort, [3] done, [4..5] key range, [6..7] this CTA's key range
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc + C::MISC_BARRIER_WORD);
     uint64_t *empty = full + C::NSTAGE;
     volatile int *abort_flag = &sh[2];
 
@@ -163,6 +169,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     const int units = p.B * p.Hkv;
     const bool producer = (warp == C::NCW);
 
+    pdl_wait_and_release();
     if (tid == 0) {
         sh[2] = 0;
         for (int s = 0; s < C::NSTAGE; ++s) {
@@ -193,6 +200,10 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
 
         if (MODE == FUSED_FULL) {
             // ================= 1. append + page scores =================
+            // P <= KEYS_MAX: all keys gather in CTA 0, which selects alone (two
+            // cluster barriers per unit). Otherwise each CTA keeps its own keys and
+            // the radix passes sum histograms over the cluster.
+            const bool gather = P <= C::KEYS_MAX;
             const int pr0 = (int)(((int64_t)crank * P) / nct);
             const int pr1 = (int)(((int64_t)(crank + 1) * P) / nct);
             const int ntile = (pr1 - pr0 + C::MT - 1) / C::MT;
@@ -336,7 +347,10 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         }
                         const int page = first + jp;
                         if (qq == 0 && page < pr1) {
-                            keys[page - pr0] = score_key(best);
+                            if (gather)  // every key of the unit goes to CTA 0
+                                st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), score_key(best));
+                            else
+                                keys[page - pr0] = score_key(best);
                             if (p.scores != nullptr) p.scores[(int64_t)u * p.Pmax + page] = best;
                         }
                     }
@@ -344,36 +358,94 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
                 }
             }
-            __syncthreads();
+            if (gather)
+                cluster_sync_all();  // CTA 0 holds every key of the unit
+            else
+                __syncthreads();
 
-            // ================= 2. cluster top-K threshold =================
-            const int nloc = pr1 - pr0;
-            uint32_t kth = 0;
+            // ================= 2. top-K threshold (adaptive range radix) =================
+            // The K-th largest key is located by narrowing a key range [lo, hi]:
+            // each pass bins the keys inside it by (key - lo) >> shift into at most
+            // 256 bins and keeps the bin holding the K-th key. Starting from the
+            // keys' own [min, max] spreads them over the bins (few shared-memory
+            // atomics collide), and the loop ends once that bin is wholly selected
+            // or holds one key value. Selected: keys above hi, plus the first
+            // `need_eq` pages (lowest index) with lo <= key <= hi.
+            const bool selecting = gather ? (crank == 0) : true;   // uniform per CTA
+            const int nk = gather ? P : pr1 - pr0;
+            const int pbase = gather ? 0 : pr0;
+            uint32_t lo = 0, hi = 0xffffffffu;
             int need_eq = 0;
-            if (P > p.kpages) {
-                uint32_t prefix = 0, mask = 0;
+            if (P > p.kpages && selecting) {
+                // ---- key range: block min/max (then over the cluster) ----
+                uint32_t kmin = 0xffffffffu, kmax = 0u;
+                for (int i = tid; i < nk; i += C::THREADS) {
+                    const uint32_t key = keys[i];
+                    kmin = key < kmin ? key : kmin;
+                    kmax = key > kmax ? key : kmax;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    kmin = min(kmin, (uint32_t)__shfl_xor_sync(0xffffffffu, kmin, o));
+                    kmax = max(kmax, (uint32_t)__shfl_xor_sync(0xffffffffu, kmax, o));
+                }
+                if (lane == 0) { wsum[warp] = (int)kmin; wsum[9 + warp] = (int)kmax; }
+                __syncthreads();
+                if (tid == 0) {
+                    uint32_t a = 0xffffffffu, bmax = 0u;
+                    for (int w = 0; w < C::NCW + 1; ++w) {
+                        a = min(a, (uint32_t)wsum[w]);
+                        bmax = max(bmax, (uint32_t)wsum[9 + w]);
+                    }
+                    sh[6] = (int)a;  // this CTA's key range, read by the cluster below
+                    sh[7] = (int)bmax;
+                }
+                if (!gather) {
+                    cluster_sync_all();
+                    if (tid == 0) {
+                        uint32_t a = 0xffffffffu, bmax = 0u;
+                        for (uint32_t r = 0; r < nct; ++r) {
+                            a = min(a, ld_dsmem_u32(dsmem_map(smem_u32(&sh[6]), r)));
+                            bmax = max(bmax, ld_dsmem_u32(dsmem_map(smem_u32(&sh[7]), r)));
+                        }
+                        sh[4] = (int)a;
+                        sh[5] = (int)bmax;
+                    }
+                } else if (tid == 0) {
+                    sh[4] = sh[6];
+                    sh[5] = sh[7];
+                }
+                __syncthreads();
+                lo = (uint32_t)sh[4];
+                hi = (uint32_t)sh[5];
                 int rem = p.kpages;
-                for (int pass = 0; pass < 4; ++pass) {
-                    const int shift = 24 - 8 * pass;
+                for (int pass = 0; pass < 6 && lo < hi; ++pass) {
+                    const uint32_t span = hi - lo;  // < 2^32
+                    const int bits = 32 - __clz(span);
+                    const int shift = bits > 8 ? bits - 8 : 0;
                     int *hb = hist + (pass & 1) * 256;
                     for (int i = tid; i < 256; i += C::THREADS) hb[i] = 0;
                     __syncthreads();
-                    for (int i = tid; i < nloc; i += C::THREADS) {
+                    for (int i = tid; i < nk; i += C::THREADS) {
                         const uint32_t key = keys[i];
-                        if ((key & mask) == prefix) atomicAdd(&hb[(key >> shift) & 255u], 1);
+                        if (key >= lo && key <= hi) atomicAdd(&hb[(key - lo) >> shift], 1);
                     }
-                    cluster_sync_all();
-                    for (int i = tid; i < 256; i += C::THREADS) {
-                        int tot = 0;
-                        for (uint32_t r = 0; r < nct; ++r) tot += (int)ld_dsmem_u32(dsmem_map(smem_u32(hb + i), r));
-                        tots[i] = tot;
+                    const int *src = hb;
+                    if (!gather) {
+                        cluster_sync_all();
+                        for (int i = tid; i < 256; i += C::THREADS) {
+                            int tot = 0;
+                            for (uint32_t r = 0; r < nct; ++r) tot += (int)ld_dsmem_u32(dsmem_map(smem_u32(hb + i), r));
+                            tots[i] = tot;
+                        }
+                        src = tots;
                     }
                     __syncthreads();
                     if (warp == 0) {
                         int c[8], sum = 0;
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            c[e] = tots[255 - 8 * lane - e];
+                            c[e] = src[255 - 8 * lane - e];
                             sum += c[e];
                         }
                         int incl = sum;
@@ -390,6 +462,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                                 if (cum + c[e] >= rem) {
                                     sh[0] = 255 - 8 * lane - e;
                                     sh[1] = rem - cum;
+                                    sh[3] = (c[e] == rem - cum) ? 1 : 0;
                                     break;
                                 }
                                 cum += c[e];
@@ -397,24 +470,29 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         }
                     }
                     __syncthreads();
-                    prefix |= (uint32_t)sh[0] << shift;
-                    mask |= 255u << shift;
+                    const uint32_t bsel = (uint32_t)sh[0];
+                    const uint32_t nlo = lo + (bsel << shift);
+                    const uint32_t top = (bsel << shift) + ((1u << shift) - 1u);  // <= span
+                    hi = lo + (top < span ? top : span);
+                    lo = nlo;
                     rem = sh[1];
+                    const bool done = sh[3] != 0;
                     __syncthreads();
+                    if (done) break;
                 }
-                kth = prefix;
                 need_eq = rem;
             }
 
-            // ================= 3. compaction into the page list =================
-            if (P > p.kpages) {
-                const int chunk = (nloc + C::THREADS - 1) / C::THREADS;
-                const int c0 = tid * chunk < nloc ? tid * chunk : nloc;
-                const int c1 = c0 + chunk < nloc ? c0 + chunk : nloc;
+            // ================= 3. compaction into the ascending page list =================
+            if (P > p.kpages && selecting) {
+                const int chunk = (nk + C::THREADS - 1) / C::THREADS;
+                const int c0 = tid * chunk < nk ? tid * chunk : nk;
+                const int c1 = c0 + chunk < nk ? c0 + chunk : nk;
                 int ngt = 0, neq = 0;
                 for (int i = c0; i < c1; ++i) {
-                    ngt += keys[i] > kth;
-                    neq += keys[i] == kth;
+                    const uint32_t key = keys[i];
+                    ngt += key > hi;
+                    neq += key >= lo && key <= hi;
                 }
                 int ig = ngt, ie = neq;
 #pragma unroll
@@ -431,21 +509,24 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     tg += wsum[w];
                     te += wsum[9 + w];
                 }
-                if (tid == 0) { cnt[0] = tg; cnt[1] = te; }
-                cluster_sync_all();
                 int gt_before = 0, eq_before = 0;
-                for (uint32_t r = 0; r < crank; ++r) {
-                    gt_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[0]), r));
-                    eq_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[1]), r));
+                if (!gather) {
+                    if (tid == 0) { cnt[0] = tg; cnt[1] = te; }
+                    cluster_sync_all();
+                    for (uint32_t r = 0; r < crank; ++r) {
+                        gt_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[0]), r));
+                        eq_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[1]), r));
+                    }
                 }
-                int eqr = eq_before + be + ie - neq;             // global rank among equal keys
+                int eqr = eq_before + be + ie - neq;             // rank among equal keys
                 int pos = gt_before + bg + ig - ngt + (eqr < need_eq ? eqr : need_eq);
                 for (int i = c0; i < c1; ++i) {
                     const uint32_t key = keys[i];
-                    const bool take = key > kth || (key == kth && eqr < need_eq);
-                    eqr += key == kth;
+                    const bool inr = key >= lo && key <= hi;
+                    const bool take = key > hi || (inr && eqr < need_eq);
+                    eqr += inr;
                     if (take) {
-                        const int page = pr0 + i;
+                        const int page = pbase + i;
                         if (pos < p.kpages && pos < C::KSEL_MAX) {
                             for (uint32_t r = 0; r < nct; ++r) st_dsmem_u32(dsmem_map(smem_u32(&list[pos]), r), (uint32_t)page);
                             if (p.page_idx != nullptr) p.page_idx[(int64_t)u * p.kpages + pos] = page;
@@ -453,7 +534,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         ++pos;
                     }
                 }
-            } else {
+            } else if (P <= p.kpages) {
                 for (int i = tid; i < P && i < C::KSEL_MAX; i += C::THREADS) list[i] = i;
                 if (p.page_idx != nullptr && crank == 0)
                     for (int i = tid; i < P; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = i;
@@ -685,19 +766,8 @@ int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_ns = ctx.timeout_ns;
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nclusters * best_c, 1, 1);
-    cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = best_c;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, quest_fused_kernel<D, G, MODE>, mmap, kmap, vmap, p) != cudaSuccess)
+    if (launch_kernel(quest_fused_kernel<D, G, MODE>, dim3(nclusters * best_c), dim3(C::THREADS), C::SMEM, ctx, best_c,
+                      mmap, kmap, vmap, p) != cudaSuccess)
         return GQAQ_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
 }

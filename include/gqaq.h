@@ -209,8 +209,11 @@ enum {
     GQAQ_OPT_TEST_STALL = 3,      /* nonzero: the attention kernels' producer issues
                                      no copy, so every consumer wait runs out
                                      (exercises the timeout path; outputs undefined) */
-    GQAQ_OPT_CLUSTER_SIZE = 4     /* CTAs per cluster of the fused Quest kernel (1, 2,
+    GQAQ_OPT_CLUSTER_SIZE = 4,    /* CTAs per cluster of the fused Quest kernel (1, 2,
                                      4 or 8); 0 = chosen from the SM count and shape */
+    GQAQ_OPT_PDL = 5              /* nonzero (default): launch with programmatic stream
+                                     serialization, so a kernel's launch overlaps the
+                                     end of the previous one in the stream */
 };
 GQAQ_API int gqaq_set_option(int option, int64_t value);
 
