@@ -67,6 +67,27 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+// Arrive (release, cluster scope) on the mbarrier at `local_addr` in CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t local_addr, uint32_t rank) {
+    const uint32_t ra = dsmem_map(local_addr, rank);
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+// Bounded wait (acquire, cluster scope) for the phase with parity `parity`.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(20000u)
+            : "memory");
+        if (ok) return true;
+        if (global_timer_ns() - t0 >= timeout_ns) return false;
+    }
+}
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -106,11 +127,13 @@ struct FusedCfg : TileCfg<D, G> {
     // [768,800), counts [800,808), scan scratch [808,832), scalars [832,848),
     // then the full/empty mbarriers (8-byte aligned) at word 848.
     static constexpr int MISC_BARRIER_WORD = 848;
-    static constexpr int MISC = MISC_BARRIER_WORD * 4 + 2 * 3 * 8;
+    static constexpr int MISC = MISC_BARRIER_WORD * 4 + (2 * 3 + 1) * 8;  // full, empty, list
     static constexpr int FIXED = KEYMERGE + QREGION + T::PBYTES + KSEL_MAX * 4 + CSTATE + MISC + 1024;
     static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
     static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
-    static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
+    static_assert(MISC >= MISC_BARRIER_WORD * 4 + (2 * NSTAGE + 1) * 8, "misc region holds the mbarriers");
+    static constexpr int KPT = 16;                  // keys per thread in the gathered selection
+    static_assert(KPT * THREADS >= KEYS_MAX, "gathered keys fit in registers");
     static_assert(NSTAGE * 8 <= 32, "tile info slots");
     static constexpr int NCHQ = D / 16;             // 16-byte chunks per record quarter
     static constexpr bool QTREG = (G * D <= 512);
@@ -158,6 +181,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     int *sh = misc + 832;                 // [0] bin, [1] remaining, [2] abort, [3] done, [4..5] key range, [6..7] this CTA's key range
     uint64_t *full = reinterpret_cast<uint64_t *>(misc + C::MISC_BARRIER_WORD);
     uint64_t *empty = full + C::NSTAGE;
+    uint64_t *list_bar = empty + C::NSTAGE;  // CTA 0 -> every CTA: "your page list is ready"
     volatile int *abort_flag = &sh[2];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -176,6 +200,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), C::NCW);
         }
+        mbar_init(smem_u32(list_bar), 1);
         fence_mbar_init();
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
@@ -188,6 +213,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     WarpAttn<D, G> wa;
     wa.init(warp, lane, smem_u32(pbuf));
     int it = 0;  // position in the stage ring (same sequence in producer and consumers)
+    uint32_t lb = 0;  // completed phases of list_bar
 
     for (int u = cid; u < units; u += ncl) {
         const int b = u / p.Hkv, kv = u - (u / p.Hkv) * p.Hkv;
@@ -200,8 +226,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
 
         if (MODE == FUSED_FULL) {
             // ================= 1. append + page scores =================
-            // P <= KEYS_MAX: all keys gather in CTA 0, which selects alone (two
-            // cluster barriers per unit). Otherwise each CTA keeps its own keys and
+            // P <= KEYS_MAX: CTA 0 gathers every key, selects alone from registers
+            // and hands each CTA its share of the page list (one cluster barrier and
+            // one remote mbarrier arrival). Otherwise each CTA keeps its own keys and
             // the radix passes sum histograms over the cluster.
             const bool gather = P <= C::KEYS_MAX;
             const int pr0 = (int)(((int64_t)crank * P) / nct);
@@ -347,7 +374,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         }
                         const int page = first + jp;
                         if (qq == 0 && page < pr1) {
-                            if (gather)  // every key of the unit goes to CTA 0
+                            if (gather)  // CTA 0 receives every key of the unit
                                 st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), score_key(best));
                             else
                                 keys[page - pr0] = score_key(best);
@@ -363,185 +390,346 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             else
                 __syncthreads();
 
-            // ================= 2. top-K threshold (adaptive range radix) =================
-            // The K-th largest key is located by narrowing a key range [lo, hi]:
-            // each pass bins the keys inside it by (key - lo) >> shift into at most
-            // 256 bins and keeps the bin holding the K-th key. Starting from the
-            // keys' own [min, max] spreads them over the bins (few shared-memory
-            // atomics collide), and the loop ends once that bin is wholly selected
-            // or holds one key value. Selected: keys above hi, plus the first
-            // `need_eq` pages (lowest index) with lo <= key <= hi.
-            const bool selecting = gather ? (crank == 0) : true;   // uniform per CTA
-            const int nk = gather ? P : pr1 - pr0;
-            const int pbase = gather ? 0 : pr0;
-            uint32_t lo = 0, hi = 0xffffffffu;
-            int need_eq = 0;
-            if (P > p.kpages && selecting) {
-                // ---- key range: block min/max (then over the cluster) ----
-                uint32_t kmin = 0xffffffffu, kmax = 0u;
-                for (int i = tid; i < nk; i += C::THREADS) {
-                    const uint32_t key = keys[i];
-                    kmin = key < kmin ? key : kmin;
-                    kmax = key > kmax ? key : kmax;
-                }
+            if (gather) {
+                // ============ 2-3. CTA 0: exact top-K from register-held keys ============
+                // Thread t holds the contiguous run of keys [t*chunk, t*chunk + cnt).
+                // The K-th largest key is located by narrowing a key range [lo, hi]:
+                // each pass bins the keys inside it by (key - lo) >> shift into at most
+                // 256 bins and keeps the bin holding the K-th key; starting from the
+                // keys' own [min, max] spreads them over the bins, and the loop ends
+                // once that bin is wholly selected or holds one key value. Selected:
+                // keys above hi plus the first `need_eq` pages (lowest index) with
+                // lo <= key <= hi. Entry `pos` of the ascending page list goes to the
+                // CTA whose share [r*nsel/C, (r+1)*nsel/C) contains it.
+                if (crank == 0) {
+                    const int chunk = (P + C::THREADS - 1) / C::THREADS;
+                    const int c0 = tid * chunk < P ? tid * chunk : P;
+                    const int kc = c0 + chunk < P ? chunk : P - c0;
+                    uint32_t kr[C::KPT];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    kmin = min(kmin, (uint32_t)__shfl_xor_sync(0xffffffffu, kmin, o));
-                    kmax = max(kmax, (uint32_t)__shfl_xor_sync(0xffffffffu, kmax, o));
-                }
-                if (lane == 0) { wsum[warp] = (int)kmin; wsum[9 + warp] = (int)kmax; }
-                __syncthreads();
-                if (tid == 0) {
-                    uint32_t a = 0xffffffffu, bmax = 0u;
-                    for (int w = 0; w < C::NCW + 1; ++w) {
-                        a = min(a, (uint32_t)wsum[w]);
-                        bmax = max(bmax, (uint32_t)wsum[9 + w]);
-                    }
-                    sh[6] = (int)a;  // this CTA's key range, read by the cluster below
-                    sh[7] = (int)bmax;
-                }
-                if (!gather) {
-                    cluster_sync_all();
-                    if (tid == 0) {
-                        uint32_t a = 0xffffffffu, bmax = 0u;
-                        for (uint32_t r = 0; r < nct; ++r) {
-                            a = min(a, ld_dsmem_u32(dsmem_map(smem_u32(&sh[6]), r)));
-                            bmax = max(bmax, ld_dsmem_u32(dsmem_map(smem_u32(&sh[7]), r)));
-                        }
-                        sh[4] = (int)a;
-                        sh[5] = (int)bmax;
-                    }
-                } else if (tid == 0) {
-                    sh[4] = sh[6];
-                    sh[5] = sh[7];
-                }
-                __syncthreads();
-                lo = (uint32_t)sh[4];
-                hi = (uint32_t)sh[5];
-                int rem = p.kpages;
-                for (int pass = 0; pass < 6 && lo < hi; ++pass) {
-                    const uint32_t span = hi - lo;  // < 2^32
-                    const int bits = 32 - __clz(span);
-                    const int shift = bits > 8 ? bits - 8 : 0;
-                    int *hb = hist + (pass & 1) * 256;
-                    for (int i = tid; i < 256; i += C::THREADS) hb[i] = 0;
-                    __syncthreads();
-                    for (int i = tid; i < nk; i += C::THREADS) {
-                        const uint32_t key = keys[i];
-                        if (key >= lo && key <= hi) atomicAdd(&hb[(key - lo) >> shift], 1);
-                    }
-                    const int *src = hb;
-                    if (!gather) {
-                        cluster_sync_all();
-                        for (int i = tid; i < 256; i += C::THREADS) {
-                            int tot = 0;
-                            for (uint32_t r = 0; r < nct; ++r) tot += (int)ld_dsmem_u32(dsmem_map(smem_u32(hb + i), r));
-                            tots[i] = tot;
-                        }
-                        src = tots;
-                    }
-                    __syncthreads();
-                    if (warp == 0) {
-                        int c[8], sum = 0;
+                    for (int e = 0; e < C::KPT; ++e) kr[e] = e < kc ? keys[c0 + e] : 0u;
+                    uint32_t lo = 0, hi = 0xffffffffu;
+                    int need_eq = P;
+                    if (P > p.kpages) {
+                        uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            c[e] = src[255 - 8 * lane - e];
-                            sum += c[e];
-                        }
-                        int incl = sum;
+                        for (int e = 0; e < C::KPT; ++e)
+                            if (e < kc) {
+                                kmin = kr[e] < kmin ? kr[e] : kmin;
+                                kmax = kr[e] > kmax ? kr[e] : kmax;
+                            }
 #pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += y;
+                        for (int o = 16; o > 0; o >>= 1) {
+                            kmin = min(kmin, (uint32_t)__shfl_xor_sync(0xffffffffu, kmin, o));
+                            kmax = max(kmax, (uint32_t)__shfl_xor_sync(0xffffffffu, kmax, o));
                         }
-                        const int excl = incl - sum;
-                        if (excl < rem && rem <= incl) {
-                            int cum = excl;
+                        if (lane == 0) { wsum[warp] = (int)kmin; wsum[9 + warp] = (int)kmax; }
+                        __syncthreads();
+                        if (tid == 0) {
+                            uint32_t a = 0xffffffffu, bmax = 0u;
+                            for (int w = 0; w < C::NCW + 1; ++w) {
+                                a = min(a, (uint32_t)wsum[w]);
+                                bmax = max(bmax, (uint32_t)wsum[9 + w]);
+                            }
+                            sh[4] = (int)a;
+                            sh[5] = (int)bmax;
+                        }
+                        __syncthreads();
+                        lo = (uint32_t)sh[4];
+                        hi = (uint32_t)sh[5];
+                        int rem = p.kpages;
+                        for (int pass = 0; pass < 6 && lo < hi; ++pass) {
+                            const uint32_t span = hi - lo;
+                            const int bits = 32 - __clz(span);
+                            const int shift = bits > 8 ? bits - 8 : 0;
+                            int *hb = hist + (pass & 1) * 256;
+                            for (int i = tid; i < 256; i += C::THREADS) hb[i] = 0;
+                            __syncthreads();
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                if (cum + c[e] >= rem) {
-                                    sh[0] = 255 - 8 * lane - e;
-                                    sh[1] = rem - cum;
-                                    sh[3] = (c[e] == rem - cum) ? 1 : 0;
-                                    break;
+                            for (int e = 0; e < C::KPT; ++e)
+                                if (e < kc && kr[e] >= lo && kr[e] <= hi) atomicAdd(&hb[(kr[e] - lo) >> shift], 1);
+                            __syncthreads();
+                            if (warp == 0) {
+                                int c[8], sum = 0;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    c[e] = hb[255 - 8 * lane - e];
+                                    sum += c[e];
                                 }
-                                cum += c[e];
+                                int incl = sum;
+#pragma unroll
+                                for (int o = 1; o < 32; o <<= 1) {
+                                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                                    if (lane >= o) incl += y;
+                                }
+                                const int excl = incl - sum;
+                                if (excl < rem && rem <= incl) {
+                                    int cum = excl;
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        if (cum + c[e] >= rem) {
+                                            sh[0] = 255 - 8 * lane - e;
+                                            sh[1] = rem - cum;
+                                            sh[3] = (c[e] == rem - cum) ? 1 : 0;
+                                            break;
+                                        }
+                                        cum += c[e];
+                                    }
+                                }
+                            }
+                            __syncthreads();
+                            const uint32_t bsel = (uint32_t)sh[0];
+                            const uint32_t nlo = lo + (bsel << shift);
+                            const uint32_t top = (bsel << shift) + ((1u << shift) - 1u);
+                            hi = lo + (top < span ? top : span);
+                            lo = nlo;
+                            rem = sh[1];
+                            if (sh[3] != 0) break;  // the next pass writes other slots first
+                        }
+                        need_eq = rem;
+                    }
+                    // ---- compaction: positions from a block scan of (above, in range) ----
+                    int ngt = 0, neq = 0;
+#pragma unroll
+                    for (int e = 0; e < C::KPT; ++e)
+                        if (e < kc) {
+                            ngt += kr[e] > hi;
+                            neq += kr[e] >= lo && kr[e] <= hi;
+                        }
+                    int ig = ngt, ie = neq;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int yg = __shfl_up_sync(0xffffffffu, ig, o);
+                        const int ye = __shfl_up_sync(0xffffffffu, ie, o);
+                        if (lane >= o) { ig += yg; ie += ye; }
+                    }
+                    __syncthreads();  // wsum is reused below
+                    if (lane == 31) { wsum[warp] = ig; wsum[9 + warp] = ie; }
+                    __syncthreads();
+                    int bg = 0, be = 0;
+                    for (int w = 0; w < warp; ++w) { bg += wsum[w]; be += wsum[9 + w]; }
+                    int eqr = be + ie - neq;
+                    int pos = bg + ig - ngt + (eqr < need_eq ? eqr : need_eq);
+                    int *prow = p.page_idx != nullptr ? p.page_idx + (int64_t)u * p.kpages : nullptr;
+#pragma unroll
+                    for (int e = 0; e < C::KPT; ++e) {
+                        if (e < kc) {
+                            const bool inr = kr[e] >= lo && kr[e] <= hi;
+                            const bool take = kr[e] > hi || (inr && eqr < need_eq);
+                            eqr += inr;
+                            if (take) {
+                                if (pos < nsel && pos < C::KSEL_MAX) {
+                                    const uint32_t owner = (uint32_t)((((int64_t)pos + 1) * nct - 1) / nsel);
+                                    st_dsmem_u32(dsmem_map(smem_u32(&list[pos]), owner), (uint32_t)(c0 + e));
+                                    if (prow != nullptr) prow[pos] = c0 + e;
+                                }
+                                ++pos;
                             }
                         }
                     }
-                    __syncthreads();
-                    const uint32_t bsel = (uint32_t)sh[0];
-                    const uint32_t nlo = lo + (bsel << shift);
-                    const uint32_t top = (bsel << shift) + ((1u << shift) - 1u);  // <= span
-                    hi = lo + (top < span ? top : span);
-                    lo = nlo;
-                    rem = sh[1];
-                    const bool done = sh[3] != 0;
-                    __syncthreads();
-                    if (done) break;
+                    if (prow != nullptr)
+                        for (int i = nsel + tid; i < p.kpages; i += C::THREADS) prow[i] = -1;
+                    __syncthreads();  // every list entry of this unit is stored
+                    if (tid == 0) {
+                        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                        for (uint32_t r = 0; r < nct; ++r) mbar_arrive_remote(smem_u32(list_bar), r);
+                    }
                 }
-                need_eq = rem;
-            }
-
-            // ================= 3. compaction into the ascending page list =================
-            if (P > p.kpages && selecting) {
-                const int chunk = (nk + C::THREADS - 1) / C::THREADS;
-                const int c0 = tid * chunk < nk ? tid * chunk : nk;
-                const int c1 = c0 + chunk < nk ? c0 + chunk : nk;
-                int ngt = 0, neq = 0;
-                for (int i = c0; i < c1; ++i) {
-                    const uint32_t key = keys[i];
-                    ngt += key > hi;
-                    neq += key >= lo && key <= hi;
-                }
-                int ig = ngt, ie = neq;
+                // every CTA: wait for its share of the list
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_cluster(smem_u32(list_bar), lb & 1u, p.timeout_ns);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok && lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
+                ++lb;
+            } else {
+                // ================= 2. top-K threshold (adaptive range radix) =================
+                // The K-th largest key is located by narrowing a key range [lo, hi]:
+                // each pass bins the keys inside it by (key - lo) >> shift into at most
+                // 256 bins and keeps the bin holding the K-th key. Starting from the
+                // keys' own [min, max] spreads them over the bins (few shared-memory
+                // atomics collide), and the loop ends once that bin is wholly selected
+                // or holds one key value. Selected: keys above hi, plus the first
+                // `need_eq` pages (lowest index) with lo <= key <= hi.
+                const bool selecting = true;
+                const int nk = gather ? P : pr1 - pr0;
+                const int pbase = gather ? 0 : pr0;
+                const int e0s = (int)(((int64_t)crank * nsel) / nct);       // this CTA's share of the list
+                const int e1s = (int)(((int64_t)(crank + 1) * nsel) / nct);
+                uint32_t lo = 0, hi = 0xffffffffu;
+                int need_eq = 0;
+                if (P > p.kpages && selecting) {
+                    // ---- key range: block min/max (then over the cluster) ----
+                    uint32_t kmin = 0xffffffffu, kmax = 0u;
+                    for (int i = tid; i < nk; i += C::THREADS) {
+                        const uint32_t key = keys[i];
+                        kmin = key < kmin ? key : kmin;
+                        kmax = key > kmax ? key : kmax;
+                    }
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int yg = __shfl_up_sync(0xffffffffu, ig, o);
-                    const int ye = __shfl_up_sync(0xffffffffu, ie, o);
-                    if (lane >= o) { ig += yg; ie += ye; }
-                }
-                if (lane == 31) { wsum[warp] = ig; wsum[9 + warp] = ie; }
-                __syncthreads();
-                int bg = 0, be = 0, tg = 0, te = 0;
-                for (int w = 0; w < C::NCW + 1; ++w) {
-                    if (w < warp) { bg += wsum[w]; be += wsum[9 + w]; }
-                    tg += wsum[w];
-                    te += wsum[9 + w];
-                }
-                int gt_before = 0, eq_before = 0;
-                if (!gather) {
-                    if (tid == 0) { cnt[0] = tg; cnt[1] = te; }
-                    cluster_sync_all();
-                    for (uint32_t r = 0; r < crank; ++r) {
-                        gt_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[0]), r));
-                        eq_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[1]), r));
+                    for (int o = 16; o > 0; o >>= 1) {
+                        kmin = min(kmin, (uint32_t)__shfl_xor_sync(0xffffffffu, kmin, o));
+                        kmax = max(kmax, (uint32_t)__shfl_xor_sync(0xffffffffu, kmax, o));
                     }
-                }
-                int eqr = eq_before + be + ie - neq;             // rank among equal keys
-                int pos = gt_before + bg + ig - ngt + (eqr < need_eq ? eqr : need_eq);
-                for (int i = c0; i < c1; ++i) {
-                    const uint32_t key = keys[i];
-                    const bool inr = key >= lo && key <= hi;
-                    const bool take = key > hi || (inr && eqr < need_eq);
-                    eqr += inr;
-                    if (take) {
-                        const int page = pbase + i;
-                        if (pos < p.kpages && pos < C::KSEL_MAX) {
-                            for (uint32_t r = 0; r < nct; ++r) st_dsmem_u32(dsmem_map(smem_u32(&list[pos]), r), (uint32_t)page);
-                            if (p.page_idx != nullptr) p.page_idx[(int64_t)u * p.kpages + pos] = page;
+                    if (lane == 0) { wsum[warp] = (int)kmin; wsum[9 + warp] = (int)kmax; }
+                    __syncthreads();
+                    if (tid == 0) {
+                        uint32_t a = 0xffffffffu, bmax = 0u;
+                        for (int w = 0; w < C::NCW + 1; ++w) {
+                            a = min(a, (uint32_t)wsum[w]);
+                            bmax = max(bmax, (uint32_t)wsum[9 + w]);
                         }
-                        ++pos;
+                        sh[6] = (int)a;  // this CTA's key range, read by the cluster below
+                        sh[7] = (int)bmax;
                     }
+                    if (!gather) {
+                        cluster_sync_all();
+                        if (tid == 0) {
+                            uint32_t a = 0xffffffffu, bmax = 0u;
+                            for (uint32_t r = 0; r < nct; ++r) {
+                                a = min(a, ld_dsmem_u32(dsmem_map(smem_u32(&sh[6]), r)));
+                                bmax = max(bmax, ld_dsmem_u32(dsmem_map(smem_u32(&sh[7]), r)));
+                            }
+                            sh[4] = (int)a;
+                            sh[5] = (int)bmax;
+                        }
+                    } else if (tid == 0) {
+                        sh[4] = sh[6];
+                        sh[5] = sh[7];
+                    }
+                    __syncthreads();
+                    lo = (uint32_t)sh[4];
+                    hi = (uint32_t)sh[5];
+                    int rem = p.kpages;
+                    for (int pass = 0; pass < 6 && lo < hi; ++pass) {
+                        const uint32_t span = hi - lo;  // < 2^32
+                        const int bits = 32 - __clz(span);
+                        const int shift = bits > 8 ? bits - 8 : 0;
+                        int *hb = hist + (pass & 1) * 256;
+                        for (int i = tid; i < 256; i += C::THREADS) hb[i] = 0;
+                        __syncthreads();
+                        for (int i = tid; i < nk; i += C::THREADS) {
+                            const uint32_t key = keys[i];
+                            if (key >= lo && key <= hi) atomicAdd(&hb[(key - lo) >> shift], 1);
+                        }
+                        const int *src = hb;
+                        if (!gather) {
+                            cluster_sync_all();
+                            for (int i = tid; i < 256; i += C::THREADS) {
+                                int tot = 0;
+                                for (uint32_t r = 0; r < nct; ++r) tot += (int)ld_dsmem_u32(dsmem_map(smem_u32(hb + i), r));
+                                tots[i] = tot;
+                            }
+                            src = tots;
+                        }
+                        __syncthreads();
+                        if (warp == 0) {
+                            int c[8], sum = 0;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                c[e] = src[255 - 8 * lane - e];
+                                sum += c[e];
+                            }
+                            int incl = sum;
+#pragma unroll
+                            for (int o = 1; o < 32; o <<= 1) {
+                                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                                if (lane >= o) incl += y;
+                            }
+                            const int excl = incl - sum;
+                            if (excl < rem && rem <= incl) {
+                                int cum = excl;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    if (cum + c[e] >= rem) {
+                                        sh[0] = 255 - 8 * lane - e;
+                                        sh[1] = rem - cum;
+                                        sh[3] = (c[e] == rem - cum) ? 1 : 0;
+                                        break;
+                                    }
+                                    cum += c[e];
+                                }
+                            }
+                        }
+                        __syncthreads();
+                        const uint32_t bsel = (uint32_t)sh[0];
+                        const uint32_t nlo = lo + (bsel << shift);
+                        const uint32_t top = (bsel << shift) + ((1u << shift) - 1u);  // <= span
+                        hi = lo + (top < span ? top : span);
+                        lo = nlo;
+                        rem = sh[1];
+                        const bool done = sh[3] != 0;
+                        __syncthreads();
+                        if (done) break;
+                    }
+                    need_eq = rem;
                 }
-            } else if (P <= p.kpages) {
-                for (int i = tid; i < P && i < C::KSEL_MAX; i += C::THREADS) list[i] = i;
+
+                // ================= 3. compaction into the ascending page list =================
+                if (P > p.kpages && selecting) {
+                    const int chunk = (nk + C::THREADS - 1) / C::THREADS;
+                    const int c0 = tid * chunk < nk ? tid * chunk : nk;
+                    const int c1 = c0 + chunk < nk ? c0 + chunk : nk;
+                    int ngt = 0, neq = 0;
+                    for (int i = c0; i < c1; ++i) {
+                        const uint32_t key = keys[i];
+                        ngt += key > hi;
+                        neq += key >= lo && key <= hi;
+                    }
+                    int ig = ngt, ie = neq;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int yg = __shfl_up_sync(0xffffffffu, ig, o);
+                        const int ye = __shfl_up_sync(0xffffffffu, ie, o);
+                        if (lane >= o) { ig += yg; ie += ye; }
+                    }
+                    if (lane == 31) { wsum[warp] = ig; wsum[9 + warp] = ie; }
+                    __syncthreads();
+                    int bg = 0, be = 0, tg = 0, te = 0;
+                    for (int w = 0; w < C::NCW + 1; ++w) {
+                        if (w < warp) { bg += wsum[w]; be += wsum[9 + w]; }
+                        tg += wsum[w];
+                        te += wsum[9 + w];
+                    }
+                    int gt_before = 0, eq_before = 0;
+                    if (!gather) {
+                        if (tid == 0) { cnt[0] = tg; cnt[1] = te; }
+                        cluster_sync_all();
+                        for (uint32_t r = 0; r < crank; ++r) {
+                            gt_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[0]), r));
+                            eq_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[1]), r));
+                        }
+                    }
+                    int eqr = eq_before + be + ie - neq;             // rank among equal keys
+                    int pos = gt_before + bg + ig - ngt + (eqr < need_eq ? eqr : need_eq);
+                    for (int i = c0; i < c1; ++i) {
+                        const uint32_t key = keys[i];
+                        const bool inr = key >= lo && key <= hi;
+                        const bool take = key > hi || (inr && eqr < need_eq);
+                        eqr += inr;
+                        if (take) {
+                            const int page = pbase + i;
+                            if (pos < p.kpages && pos < C::KSEL_MAX) {
+                                if (!gather) {
+                                    for (uint32_t r = 0; r < nct; ++r)
+                                        st_dsmem_u32(dsmem_map(smem_u32(&list[pos]), r), (uint32_t)page);
+                                    if (p.page_idx != nullptr) p.page_idx[(int64_t)u * p.kpages + pos] = page;
+                                } else {
+                                    if (pos >= e0s && pos < e1s) list[pos] = page;  // this CTA's share
+                                    if (p.page_idx != nullptr && crank == 0) p.page_idx[(int64_t)u * p.kpages + pos] = page;
+                                }
+                            }
+                            ++pos;
+                        }
+                    }
+                } else if (P <= p.kpages) {
+                    for (int i = tid; i < P && i < C::KSEL_MAX; i += C::THREADS) list[i] = i;
+                    if (p.page_idx != nullptr && crank == 0)
+                        for (int i = tid; i < P; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = i;
+                }
                 if (p.page_idx != nullptr && crank == 0)
-                    for (int i = tid; i < P; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = i;
+                    for (int i = nsel + tid; i < p.kpages; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = -1;
+                cluster_sync_all();  // remote list entries are complete
             }
-            if (p.page_idx != nullptr && crank == 0)
-                for (int i = nsel + tid; i < p.kpages; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = -1;
-            cluster_sync_all();  // the page list is complete in every CTA
         }
 
         // ================= 4. attention over this CTA's share of the pages =================
