@@ -159,7 +159,9 @@ def workspace_bytes(dims: Dims, max_selected_pages: int = 0) -> int:
 
 
 def alloc_workspace(dims: Dims, device) -> torch.Tensor:
-    return torch.empty(workspace_bytes(dims), dtype=torch.uint8, device=device)
+    """Workspace for gqa_decode_attn / quest_sparse_attn. Zero-filled once, as
+    the library asks; every call leaves its counters at zero again."""
+    return torch.zeros(workspace_bytes(dims), dtype=torch.uint8, device=device)
 
 
 def num_pages(max_len: int, page_size: int = PAGE_SIZE) -> int:

@@ -12,7 +12,7 @@
 // reads only the K/V rows of the selected pages. It is the same kernel with
 // the tile rows taken from a page list instead of a contiguous range.
 //
-// Kernel shape (one persistent CTA per resident slot):
+// Kernel shape (one persistent CTA per resident slot, one launch per call):
 //  - work tiles: 128 consecutive tokens (dense) or 8 selected pages of 16
 //    tokens (sparse) of one (sequence, KV head) unit. The tiles of all units
 //    are split into equal contiguous ranges, one per CTA (balanced split).
@@ -24,8 +24,10 @@
 //    output channels of all G rows.
 //  - at the end of each unit segment the 8 warp states merge in shared
 //    memory. A segment that covers its whole unit writes the fp16 output. A
-//    segment cut by the range boundary writes an fp32 partial (m, l, acc),
-//    which attn_combine_kernel merges.
+//    segment cut by a range boundary writes an fp32 partial (m, l, acc) and
+//    bumps the unit's arrival counter; the CTA that brings the counter to the
+//    unit's number of parts merges all of them (log-sum-exp) and writes the
+//    output, then sets the counter back to zero for the next call.
 #include <math.h>
 
 #include "attn_tile.cuh"
@@ -49,7 +51,8 @@ struct AttnParams {
     const int *valid_len;
     const int *page_idx;
     __half *out;
-    float *part;     // [grid][2][G][D+2]
+    float *part;      // [grid][2][G][D+2]: fp32 (m, l, acc) of split segments
+    unsigned *count;  // [B*Hkv]: arrivals at split units; zero between calls
     int *status;
     int B, Hkv, Lmax, kpages, S;
     float scale_log2;
@@ -57,10 +60,23 @@ struct AttnParams {
     int test_stall;
 };
 
+// A unit segment of this CTA that was cut by a range boundary (at most the
+// first and the last segment of a range).
+struct Split {
+    int64_t off;  // tile offset of the unit
+    int tiles_b, unit, slot, last;
+    __half *out;
+};
+
 struct Sched {
-    int64_t t_begin, t_end, off_b;
-    int b;
+    int64_t T;         // tiles of all units
+    int64_t t_begin, t_end;
+    int64_t unit_off;  // tile offset of the first unit in range
+    int b, kv, local, tiles_b, len;
+    int grid;          // CTAs with work: min(gridDim.x, T)
     int abort;
+    int nsplit;
+    Split split[2];
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -69,50 +85,144 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
 // Walk over the unit segments of one CTA's tile range.
 struct Walk {
-    int b, kv, local, tiles_b;
+    int b, kv, local, tiles_b, len;
+    int64_t off;  // tile offset of unit (b, kv) in the global tile order
     int64_t remaining;
     bool first;
-    __device__ __forceinline__ void init(const Sched &s, const int *valid_len, int Hkv,
-                                         const TileRule &rule) {
+    __device__ __forceinline__ void init(const Sched &s) {
         b = s.b;
-        tiles_b = rule.tiles(valid_len[b]);
-        const int64_t rel = s.t_begin - s.off_b;
-        kv = (int)(rel / tiles_b);
-        local = (int)(rel % tiles_b);
+        kv = s.kv;
+        local = s.local;
+        tiles_b = s.tiles_b;
+        len = s.len;
+        off = s.unit_off;
         remaining = s.t_end - s.t_begin;
         first = true;
-        (void)Hkv;
     }
     __device__ __forceinline__ int seg_len() const {
         const int64_t r = tiles_b - local;
         return (int)(r < remaining ? r : remaining);
     }
     // Move past a segment of n tiles; returns false when the range is done.
-    __device__ __forceinline__ bool next(int n, const int *valid_len, int B, int Hkv,
-                                         const TileRule &rule) {
+    __device__ __forceinline__ bool next(int n, const int *valid_len, int B, int Hkv, const TileRule &rule) {
         remaining -= n;
         first = false;
         if (remaining <= 0) return false;
         local = 0;
+        off += tiles_b;
         if (++kv == Hkv) {
             kv = 0;
             do {
-                ++b;
-                tiles_b = (b < B) ? rule.tiles(valid_len[b]) : 1;
-            } while (b < B && tiles_b == 0);
-            if (b >= B) return false;
+                if (++b >= B) return false;
+                const int raw = valid_len[b];
+                len = clamp_len(raw, rule.lmax);
+                tiles_b = rule.tiles(raw);
+            } while (tiles_b == 0);
         }
         return true;
     }
 };
+
+// Log-sum-exp merge of the n_parts partials of one split unit, run by the 256
+// consumer threads of the CTA that arrived last:
+//   out_g = sum_c 2^(m_c - m*) acc_c / sum_c 2^(m_c - m*) l_c,  m* = max_c m_c.
+// The partials of CTAs c_lo .. c_lo + n_parts - 1 sit in slot 0, except the
+// first CTA's, whose slot is slot_lo. Other CTAs wrote them, so they are read
+// from L2 (ld.global.cg), never from a possibly stale L1 line.
+template <int D, int G>
+__device__ __forceinline__ void merge_parts(const float *part, float *wbuf, int64_t c_lo, int n_parts,
+                                            int slot_lo, __half *outg, int warp, int lane, int tid, int nthreads) {
+    constexpr int W = G * (D + 2);
+    constexpr int FEW = 8;
+    if (n_parts <= FEW) {
+        // Few parts: every thread loads (m, l, acc) of its elements from all
+        // parts at once and merges them itself (one round trip to L2).
+        for (int idx = tid; idx < G * D; idx += nthreads) {
+            const int g = idx / D, d = idx - (idx / D) * D;
+            float2 ml[FEW];
+            float a[FEW];
+#pragma unroll
+            for (int j = 0; j < FEW; ++j) {
+                if (j < n_parts) {
+                    const float *ps = part + ((c_lo + j) * 2 + (j == 0 ? slot_lo : 0)) * W + g * (D + 2);
+                    ml[j] = __ldcg(reinterpret_cast<const float2 *>(ps));
+                    a[j] = __ldcg(ps + 2 + d);
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < FEW; ++j)
+                if (j < n_parts) mx = fmaxf(mx, ml[j].x);
+            float L = 0.f, acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < FEW; ++j) {
+                if (j < n_parts && ml[j].x != -INFINITY) {
+                    const float f = fast_exp2(ml[j].x - mx);
+                    L += f * ml[j].y;
+                    acc += f * a[j];
+                }
+            }
+            outg[idx] = __float2half_rn(L > 0.f ? acc / L : 0.f);
+        }
+        return;
+    }
+    if (warp < G) {
+        // Warp g: running (max, sum) over its lanes' parts, then a warp merge.
+        float mx = -INFINITY, l = 0.f;
+        for (int j = lane; j < n_parts; j += 32) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+                part + ((c_lo + j) * 2 + (j == 0 ? slot_lo : 0)) * W + warp * (D + 2)));
+            if (ml.x > mx) {
+                l = (mx == -INFINITY) ? ml.y : l * fast_exp2(mx - ml.x) + ml.y;
+                mx = ml.x;
+            } else if (ml.x != -INFINITY) {
+                l += ml.y * fast_exp2(ml.x - mx);
+            }
+            wbuf[j * G + warp] = ml.x;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, mx, o);
+            const float lo = __shfl_xor_sync(0xffffffffu, l, o);
+            const float mn = fmaxf(mx, mo);
+            l = (mn == -INFINITY) ? 0.f
+                                  : (mx == -INFINITY ? 0.f : l * fast_exp2(mx - mn)) +
+                                        (mo == -INFINITY ? 0.f : lo * fast_exp2(mo - mn));
+            mx = mn;
+        }
+        __syncwarp();
+        for (int j = lane; j < n_parts; j += 32) {
+            const float m = wbuf[j * G + warp];
+            wbuf[j * G + warp] = (m == -INFINITY) ? 0.f : fast_exp2(m - mx);
+        }
+        if (lane == 0) wbuf[n_parts * G + warp] = l;
+    }
+    named_bar_sync(1, nthreads);
+    for (int idx = tid; idx < G * D; idx += nthreads) {
+        const int g = idx / D, d = idx - (idx / D) * D;
+        const float *pe = part + g * (D + 2) + 2 + d;
+        float acc = wbuf[g] * __ldcg(pe + (c_lo * 2 + slot_lo) * W);
+#pragma unroll 16
+        for (int j = 1; j < n_parts; ++j) acc += wbuf[j * G + g] * __ldcg(pe + (c_lo + j) * 2 * W);
+        const float L = wbuf[n_parts * G + g];
+        outg[idx] = __float2half_rn(L > 0.f ? acc / L : 0.f);
+    }
+}
 
 template <int D, int G, bool SPARSE>
 __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLOCKS)
     attn_partial_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
     using C = AttnCfg<D, G>;
+    constexpr int NCT = C::NCW * 32;  // consumer threads
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -129,6 +239,16 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     const int lane = threadIdx.x & 31;
     const int Hq = p.Hkv * G;
 
+    // Nothing above the dependency wait reads what an earlier kernel writes.
+    if (warp == C::NCW && lane == 0) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), C::NCW);
+        }
+        fence_mbar_init();
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
     pdl_wait_and_release();
     TileRule rule;
     rule.sparse = SPARSE ? 1 : 0;
@@ -139,28 +259,52 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     rule.pages_per_tile = C::NCW;
 
     if (warp == C::NCW) {
+        // Balanced split of the T tiles over min(gridDim.x, T) CTAs, so that
+        // every working CTA owns at least one tile.
         int64_t T, off_b;
         int b;
-        locate_tile(p.valid_len, p.B, p.Hkv, rule, 0, T, b, off_b);  // T
-        const int64_t tb = tile_begin(blockIdx.x, T, gridDim.x);
-        const int64_t te = tile_begin(blockIdx.x + 1, T, gridDim.x);
-        if (tb < te) locate_tile(p.valid_len, p.B, p.Hkv, rule, tb, T, b, off_b);
+        locate_tile(p.valid_len, p.B, p.Hkv, rule, 0, T, b, off_b);
+        const int gp = (T < (int64_t)gridDim.x) ? (int)T : (int)gridDim.x;
+        int64_t tb = 0, te = 0;
+        if ((int)blockIdx.x < gp) {
+            tb = tile_begin(blockIdx.x, T, gp);
+            te = tile_begin(blockIdx.x + 1, T, gp);
+        }
+        if (tb < te && tb != 0) locate_tile(p.valid_len, p.B, p.Hkv, rule, tb, T, b, off_b);
         if (lane == 0) {
+            sched->T = T;
+            sched->grid = gp;
             sched->t_begin = tb;
             sched->t_end = te;
-            sched->off_b = off_b;
-            sched->b = b;
             sched->abort = 0;
-            for (int s = 0; s < C::NSTAGE; ++s) {
-                mbar_init(smem_u32(&full[s]), 1);
-                mbar_init(smem_u32(&empty[s]), C::NCW);
+            sched->nsplit = 0;
+            if (tb < te) {
+                const int raw = p.valid_len[b];
+                const int tiles_b = rule.tiles(raw);
+                const int rel = (int)(tb - off_b);  // < Hkv * tiles_b
+                sched->b = b;
+                sched->kv = rel / tiles_b;
+                sched->local = rel - (rel / tiles_b) * tiles_b;
+                sched->tiles_b = tiles_b;
+                sched->len = clamp_len(raw, p.Lmax);
+                sched->unit_off = off_b + (int64_t)(rel / tiles_b) * tiles_b;
             }
-            fence_mbar_init();
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
         }
     }
     __syncthreads();
+
+    if (warp < C::NCW) {
+        // Sequences with no valid token: defined as a zero output. Lengths
+        // outside [1, Lmax] raise GQAQ_DEV_BAD_LEN. CTA b % gridDim.x checks b.
+        for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+            const int raw = p.valid_len[b];
+            if (threadIdx.x == 0 && (raw < 1 || raw > p.Lmax)) raise_flag(p.status, GQAQ_DEV_BAD_LEN);
+            if (rule.tiles(raw) == 0) {
+                __half *ob = p.out + (int64_t)b * Hq * D;
+                for (int e = threadIdx.x; e < Hq * D; e += NCT) ob[e] = __float2half_rn(0.f);
+            }
+        }
+    }
     if (sched->t_begin >= sched->t_end) return;
 
     if (warp == C::NCW) {
@@ -170,15 +314,14 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
         if (p.test_stall) return;  // issue nothing: every consumer wait runs out
         const uint64_t pol = l2_policy_evict_first();
         Walk w;
-        w.init(*sched, p.valid_len, p.Hkv, rule);
+        w.init(*sched);
         int i = 0;
         bool failed = false;
         do {
             const int n = w.seg_len();
             const int unit = w.b * p.Hkv + w.kv;
             const int row0 = unit * p.Lmax;
-            const int len = clamp_len(p.valid_len[w.b], p.Lmax);
-            const int P = (len + p.S - 1) / p.S;
+            const int P = (w.len + p.S - 1) / p.S;
             const int nsel = P < p.kpages ? P : p.kpages;
             for (int t = 0; t < n; ++t, ++i) {
                 const int s = i % C::NSTAGE;
@@ -245,30 +388,31 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     }
 
     // ----------------------------------------------------------------------
-    // Consumer warps
+    // Consumer warps. After a timeout they still walk every segment and keep
+    // the arrival counters in step, so the workspace stays reusable.
     // ----------------------------------------------------------------------
     const int tid = threadIdx.x;  // 0..255 among consumers
     WarpAttn<D, G> wa;
     wa.init(warp, lane, smem_u32(pbuf));
 
     Walk w;
-    w.init(*sched, p.valid_len, p.Hkv, rule);
+    w.init(*sched);
     int i = 0;
     do {
         const int n = w.seg_len();
         const bool complete = (w.local == 0 && n == w.tiles_b);
         const int slot = w.first ? 0 : 1;
         const int unit = w.b * p.Hkv + w.kv;
-        const int len = clamp_len(p.valid_len[w.b], p.Lmax);
+        const int len = w.len;
         const int P = (len + p.S - 1) / p.S;
         const int nsel = P < p.kpages ? P : p.kpages;
         const __half *qg = p.q + ((int64_t)w.b * Hq + (int64_t)w.kv * G) * D;
         if (C::QREG) {
             wa.load_q(qg);
         } else {
-            for (int e = tid; e < G * D / 8; e += C::NCW * 32)
+            for (int e = tid; e < G * D / 8; e += NCT)
                 reinterpret_cast<uint4 *>(q_s)[e] = reinterpret_cast<const uint4 *>(qg)[e];
-            named_bar_sync(1, C::NCW * 32);
+            named_bar_sync(1, NCT);
         }
         wa.reset();
 
@@ -309,14 +453,14 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
 
         // ---- merge the 8 warp states of this segment ----
         wa.store_state(merge);
-        named_bar_sync(1, C::NCW * 32);
-        for (int idx = tid; idx < G * D; idx += C::NCW * 32) {
+        named_bar_sync(1, NCT);
+        __half *outg = p.out + ((int64_t)w.b * Hq + (int64_t)w.kv * G) * D;
+        for (int idx = tid; idx < G * D; idx += NCT) {
             const int g = idx / D, d = idx - (idx / D) * D;
             float mst, ls, as;
             merge_warps<D, G>(merge, g, d, mst, ls, as);
             if (complete) {
-                p.out[((int64_t)w.b * Hq + (int64_t)w.kv * G + g) * D + d] =
-                    __float2half_rn(ls > 0.f ? as / ls : 0.f);
+                outg[idx] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
             } else {
                 float *ps = p.part + (((int64_t)blockIdx.x * 2 + slot) * G + g) * (D + 2);
                 ps[2 + d] = as;
@@ -326,92 +470,43 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
                 }
             }
         }
-        named_bar_sync(1, C::NCW * 32);
+        named_bar_sync(1, NCT);
+        if (!complete && tid == 0) {
+            // Arrive at the split unit. The barrier above orders every
+            // consumer's partial stores before this release; the unit's last
+            // arrival acquires all of them. It has c_hi - c_lo + 1 parts
+            // (CTAs c_lo..c_hi, all ranges non-empty). Merging waits for the
+            // end of the range.
+            Split &sp = sched->split[sched->nsplit++];
+            sp.off = w.off;
+            sp.tiles_b = w.tiles_b;
+            sp.unit = unit;
+            sp.slot = slot;
+            sp.out = outg;
+            const int64_t T = sched->T;
+            const int gp = sched->grid;
+            const int64_t c_lo = tile_owner(w.off, T, gp);
+            const int n_parts = (int)(tile_owner(w.off + w.tiles_b - 1, T, gp) - c_lo) + 1;
+            const unsigned old = atomic_add_acq_rel_gpu(&p.count[unit], 1u);
+            sp.last = (old + 1u == (unsigned)n_parts);
+            if (sp.last) p.count[unit] = 0u;
+        }
     } while (w.next(w.seg_len(), p.valid_len, p.B, p.Hkv, rule));
-}
 
-// ---------------------------------------------------------------------------
-// Log-sum-exp combine of the partials of units that were split across CTAs:
-//   out_g = sum_c 2^(m_c - m*) acc_c / sum_c 2^(m_c - m*) l_c,  m* = max_c m_c.
-// One CTA per (KV head, sequence).
-// ---------------------------------------------------------------------------
-struct CombineParams {
-    const int *valid_len;
-    const float *part;
-    __half *out;
-    int *status;
-    int B, Hkv, Lmax, kpages, S;
-    int sparse, tile_tokens, pages_per_tile;
-    int grid;  // grid of the partial kernel
-};
-
-template <int D, int G>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
-    pdl_wait_and_release();
-    const int kv = blockIdx.x, b = blockIdx.y;
-    TileRule rule;
-    rule.sparse = p.sparse;
-    rule.lmax = p.Lmax;
-    rule.page_size = p.S;
-    rule.kpages = p.kpages;
-    rule.tile_tokens = p.tile_tokens;
-    rule.pages_per_tile = p.pages_per_tile;
-
-    __shared__ long long red_tot[4], red_before[4];
-    long long tot = 0, before = 0;
-    for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
-        const long long n = (long long)p.Hkv * rule.tiles(p.valid_len[bb]);
-        tot += n;
-        if (bb < b) before += n;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        before += __shfl_xor_sync(0xffffffffu, before, o);
-    }
-    if ((threadIdx.x & 31) == 0) {
-        red_tot[threadIdx.x >> 5] = tot;
-        red_before[threadIdx.x >> 5] = before;
-    }
-    __syncthreads();
-    const int64_t T = red_tot[0] + red_tot[1] + red_tot[2] + red_tot[3];
-    const int64_t off_b = red_before[0] + red_before[1] + red_before[2] + red_before[3];
-
-    const int raw = p.valid_len[b];
-    if (threadIdx.x == 0 && kv == 0 && (raw < 1 || raw > p.Lmax)) raise_flag(p.status, GQAQ_DEV_BAD_LEN);
-    const int tiles_b = rule.tiles(raw);
-    const int Hq = p.Hkv * G;
-    __half *outg = p.out + ((int64_t)b * Hq + (int64_t)kv * G) * D;
-    if (tiles_b == 0) {  // no valid token: defined as a zero output
-        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) outg[idx] = __float2half_rn(0.f);
-        return;
-    }
-    const int64_t o = off_b + (int64_t)kv * tiles_b;
-    const int64_t grid = p.grid;
-    const int64_t c_lo = tile_owner(o, T, grid);
-    const int64_t c_hi = tile_owner(o + tiles_b - 1, T, grid);
-    if (c_lo == c_hi) return;  // written directly by the partial kernel
-    const int slot_lo = (tile_begin(c_lo, T, grid) == o) ? 0 : 1;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int g = idx / D, d = idx - (idx / D) * D;
-        float mst = -INFINITY;
-        for (int64_t c = c_lo; c <= c_hi; ++c) {
-            if (tile_begin(c, T, grid) == tile_begin(c + 1, T, grid)) continue;
-            const int slot = (c == c_lo) ? slot_lo : 0;
-            mst = fmaxf(mst, p.part[((c * 2 + slot) * G + g) * (D + 2)]);
-        }
-        float ls = 0.f, as = 0.f;
-        for (int64_t c = c_lo; c <= c_hi; ++c) {
-            if (tile_begin(c, T, grid) == tile_begin(c + 1, T, grid)) continue;
-            const int slot = (c == c_lo) ? slot_lo : 0;
-            const float *ps = p.part + ((c * 2 + slot) * G + g) * (D + 2);
-            if (ps[0] != -INFINITY) {
-                const float f = fast_exp2(ps[0] - mst);
-                ls += f * ps[1];
-                as += f * ps[2 + d];
-            }
-        }
-        outg[idx] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
+    // ---- merge the split units this CTA arrived at last ----
+    named_bar_sync(1, NCT);  // thread 0's arrivals are recorded
+    const int nsplit = sched->nsplit;
+    if (nsplit == 0) return;
+    const int64_t T = sched->T;
+    const int gp = sched->grid;
+    for (int k = 0; k < nsplit; ++k) {
+        const Split &sp = sched->split[k];
+        if (!sp.last) continue;
+        const int64_t c_lo = tile_owner(sp.off, T, gp);
+        const int n_parts = (int)(tile_owner(sp.off + sp.tiles_b - 1, T, gp) - c_lo) + 1;
+        const int slot_lo = (tile_begin(c_lo, T, gp) == sp.off) ? 0 : 1;
+        merge_parts<D, G>(p.part, merge, c_lo, n_parts, slot_lo, sp.out, warp, lane, tid, NCT);
+        named_bar_sync(1, NCT);
     }
 }
 
@@ -438,7 +533,15 @@ int grid_for(const LaunchCtx &ctx) {
     }
     int grid = occ[ctx.device] * ctx.num_sms;
     if (ctx.max_ctas > 0 && ctx.max_ctas < grid) grid = ctx.max_ctas;
+    // The merge keeps (parts + 1) * G weights in the merge buffer.
+    if (grid > C::NCW * (D + 2) - 1) grid = C::NCW * (D + 2) - 1;
     return grid;
+}
+
+// Workspace: [B*Hkv] u32 arrival counters (256-byte padded), then the
+// partials [grid][2][G][D+2] fp32.
+inline size_t count_bytes(const gqaq_dims &dm) {
+    return ((size_t)dm.batch * dm.num_kv_heads * sizeof(unsigned) + 255) & ~(size_t)255;
 }
 
 template <int D, int G, bool SPARSE>
@@ -447,7 +550,8 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     const gqaq_dims &dm = *a.dims;
     const int grid = grid_for<D, G, SPARSE>(ctx);
     if (grid < 1) return GQAQ_ERR_CUDA;
-    const size_t need = (size_t)grid * 2 * G * (D + 2) * sizeof(float);
+    const size_t cbytes = count_bytes(dm);
+    const size_t need = cbytes + (size_t)grid * 2 * G * (D + 2) * sizeof(float);
     if (a.workspace == nullptr || a.workspace_bytes < need) return GQAQ_ERR_WORKSPACE;
 
     const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
@@ -461,7 +565,8 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     p.valid_len = a.valid_len;
     p.page_idx = a.page_idx;
     p.out = a.out;
-    p.part = reinterpret_cast<float *>(a.workspace);
+    p.count = reinterpret_cast<unsigned *>(a.workspace);
+    p.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + cbytes);
     p.status = ctx.status;
     p.B = dm.batch;
     p.Hkv = dm.num_kv_heads;
@@ -473,24 +578,6 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     p.test_stall = ctx.test_stall;
     if (launch_kernel(attn_partial_kernel<D, G, SPARSE>, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, kmap, vmap,
                       p) != cudaSuccess)
-        return GQAQ_ERR_CUDA;
-
-    CombineParams cp;
-    cp.valid_len = a.valid_len;
-    cp.part = p.part;
-    cp.out = a.out;
-    cp.status = ctx.status;
-    cp.B = dm.batch;
-    cp.Hkv = dm.num_kv_heads;
-    cp.Lmax = dm.max_len;
-    cp.kpages = p.kpages;
-    cp.S = p.S;
-    cp.sparse = SPARSE ? 1 : 0;
-    cp.tile_tokens = C::TILE;
-    cp.pages_per_tile = C::NCW;
-    cp.grid = grid;
-    if (launch_kernel(attn_combine_kernel<D, G>, dim3(dm.num_kv_heads, dm.batch), dim3(128), 0, ctx, 0, cp) !=
-        cudaSuccess)
         return GQAQ_ERR_CUDA;
     return GQAQ_OK;
 }
@@ -512,21 +599,21 @@ int dispatch_g(const AttnArgs &a, const LaunchCtx &ctx, int G) {
 }
 
 template <int D, int G>
-size_t ws_t(const LaunchCtx &ctx) {
+size_t ws_t(const gqaq_dims &dm, const LaunchCtx &ctx) {
     const int g0 = grid_for<D, G, false>(ctx);
     const int g1 = grid_for<D, G, true>(ctx);
     if (g0 < 1 || g1 < 1) return 0;
     const int grid = g0 > g1 ? g0 : g1;
-    return (size_t)grid * 2 * G * (D + 2) * sizeof(float);
+    return count_bytes(dm) + (size_t)grid * 2 * G * (D + 2) * sizeof(float);
 }
 
 template <int D>
-size_t ws_g(const LaunchCtx &ctx, int G) {
+size_t ws_g(const gqaq_dims &dm, const LaunchCtx &ctx, int G) {
     switch (G) {
-        case 1: return ws_t<D, 1>(ctx);
-        case 2: return ws_t<D, 2>(ctx);
-        case 4: return ws_t<D, 4>(ctx);
-        case 8: return ws_t<D, 8>(ctx);
+        case 1: return ws_t<D, 1>(dm, ctx);
+        case 2: return ws_t<D, 2>(dm, ctx);
+        case 4: return ws_t<D, 4>(dm, ctx);
+        case 8: return ws_t<D, 8>(dm, ctx);
         default: return 0;
     }
 }
@@ -545,8 +632,8 @@ int launch_attention(const AttnArgs &a, const LaunchCtx &ctx) {
 size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx) {
     const int G = dims->num_q_heads / dims->num_kv_heads;
     switch (dims->head_dim) {
-        case 64: return ws_g<64>(ctx, G);
-        case 128: return ws_g<128>(ctx, G);
+        case 64: return ws_g<64>(*dims, ctx, G);
+        case 128: return ws_g<128>(*dims, ctx, G);
         default: return 0;
     }
 }

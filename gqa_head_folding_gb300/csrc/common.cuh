@@ -172,6 +172,15 @@ __device__ __forceinline__ void pdl_wait_and_release() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Atomic add at gpu scope with acquire-release semantics: it publishes the
+// writes that happen before it (including other threads' writes ordered by a
+// CTA barrier) and makes visible the writes released by earlier adds.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *ptr, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void raise_flag(int *status, int flag) {
     if (status != nullptr) atomicOr(status, flag);
 }

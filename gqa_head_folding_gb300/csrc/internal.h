@@ -18,7 +18,8 @@ namespace gqaq {
 bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                           uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
-// Dense (page_idx == nullptr) or sparse split-context attention + combine.
+// Dense (page_idx == nullptr) or sparse split-context attention, one launch:
+// split units are merged in-kernel by the CTA that finishes them last.
 struct AttnArgs {
     const gqaq_dims *dims;
     const __half *q;

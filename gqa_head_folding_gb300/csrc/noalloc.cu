@@ -51,10 +51,11 @@ int static_scratch(void **out) {
 }  // namespace gqaq
 
 // Same computation, arguments and results as gqa_decode_attn, without the
-// workspace arguments. Nothing in the scratch needs to start at zero: every
-// partial the combine step reads was written earlier in the same call. Calls
-// that overlap on the GPU (on different streams, or from different host
-// threads without ordering) share the one array and race.
+// workspace arguments. The workspace's arrival counters must start at zero:
+// a __device__ array is zero-filled when the module loads, and every call
+// leaves the counters at zero again. Calls that overlap on the GPU (on
+// different streams, or from different host threads without ordering) share
+// the one array and race.
 extern "C" GQAQ_API int gqa_decode_attn_noalloc(const gqaq_dims *dims, const gqaq_half *q,
                                                 const gqaq_half *k_cache, const gqaq_half *v_cache,
                                                 const int32_t *valid_len, float scale, gqaq_half *out,

@@ -101,11 +101,7 @@ class DecodeStack:
     @staticmethod
     def kernels_per_call(name: str, k_pages: Optional[int]) -> int:
         """Kernel launches behind one call of a family."""
-        if name == "dense":
-            return 2                       # split-context partials + combine
-        if name == "sparse":
-            return 1 if k_pages is not None and k_pages <= 1024 else 2
-        return 1
+        return 1                           # split units are merged inside the attention kernel
 
     def launches_per_step(self, layers: List[Layer]) -> int:
         return sum(len(v) * self.kernels_per_call(k, self.k_pages) for k, v in self.families(layers).items())

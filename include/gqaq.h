@@ -95,7 +95,13 @@ typedef struct {
  * current device for these dims (enough for both). The library sizes its
  * grid from the SM count, so the figure depends on the device.
  * `max_selected_pages` is accepted for future use and is not needed today.
- * Returns 0 when the dims are invalid or unsupported. */
+ * Returns 0 when the dims are invalid or unsupported.
+ * The workspace holds one arrival counter per (sequence, KV head) followed by
+ * the fp32 partials of context splits. The counters must be zero when the
+ * workspace is first used: zero-fill it once (cudaMemsetAsync) after
+ * allocating it. Every call, including one whose waits time out, leaves the
+ * counters at zero again, so the workspace can be reused by any later call
+ * (of any dims that fit) without clearing. */
 GQAQ_API size_t gqaq_workspace_bytes(const gqaq_dims *dims, int max_selected_pages);
 
 /* [OPT] section 3: dense decode attention with the query heads folded.
@@ -106,8 +112,11 @@ GQAQ_API size_t gqaq_workspace_bytes(const gqaq_dims *dims, int max_selected_pag
  * additive context mask. fp32 accumulation; out is rounded to fp16 once
  * (round to nearest even). The context is split across the GPU's SMs, and
  * the split partials are combined by log-sum-exp.
- * workspace: >= gqaq_workspace_bytes(dims, 0) bytes of device scratch. Its
- * contents on entry do not matter. Two calls that overlap must not share it. */
+ * The CTA that finishes a split (sequence, KV head) last merges its partials,
+ * so one kernel launch does the whole call.
+ * workspace: >= gqaq_workspace_bytes(dims, 0) bytes of device memory, zero
+ * filled before its first use (see gqaq_workspace_bytes). Two calls that
+ * overlap on the GPU must not share it. */
 GQAQ_API int gqa_decode_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
                     const gqaq_half *v_cache, const int32_t *valid_len, float scale,
                     gqaq_half *out, void *workspace, size_t workspace_bytes, void *stream);
@@ -192,8 +201,9 @@ GQAQ_API int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_h
  * GB300, for example (gqaq_workspace_bytes reports the need).
  * The first call on each device looks up the array's device address with that
  * device current. Make that first call before any stream capture.
- * All calls share the one array. Nothing in it needs to start at zero, but
- * calls that overlap on the GPU race on it. It allocates nothing. */
+ * All calls share the one array. It is zero-filled when the library loads,
+ * as the workspace contract asks, and every call leaves it so. Calls that
+ * overlap on the GPU race on it. It allocates nothing. */
 GQAQ_API int gqa_decode_attn_noalloc(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
                                      const gqaq_half *v_cache, const int32_t *valid_len, float scale,
                                      gqaq_half *out, void *stream);

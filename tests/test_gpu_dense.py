@@ -3,8 +3,9 @@ oracle's explicit-repeat_kv attention, element by element.
 
 Covers D in {64, 128}, G in {1, 2, 4, 8}, ragged and tiny valid lengths, an
 allocated length that is not a multiple of the tile, persistent grids forced
-small (so units split across CTAs and go through the log-sum-exp combine)
-and the first workload at its full size.
+small (so units split across CTAs and go through the in-kernel log-sum-exp
+merge), one unit split over the whole grid, one workspace reused across
+shapes, and the first workload at its full size.
 """
 import math
 
@@ -52,6 +53,39 @@ def test_dense_group_sizes(D, G):
 def test_dense_split_and_combine(max_ctas):
     # ragged lengths and a tail tile; small grids force units across CTAs
     run_case(3, 32, 8, 64, 1000, [1000, 129, 1], seed=11, max_ctas=max_ctas)
+
+
+def test_dense_one_unit_split_over_the_whole_grid():
+    # batch 1, one KV head: every CTA of the default grid holds a part of it
+    run_case(1, 4, 1, 64, 16 * 2048, [16 * 2048 - 5], seed=21)
+    run_case(1, 8, 1, 128, 16 * 1024, [16 * 1024], seed=22)
+
+
+def test_dense_workspace_reused_across_shapes_and_grids():
+    # one zero-filled workspace serves calls of different dims and grids; each
+    # call leaves its arrival counters at zero for the next
+    cases = [(4, 32, 8, 128, 2048, [2048, 700, 1, 1500], 0), (1, 8, 2, 64, 900, [899], 3),
+             (3, 16, 8, 128, 512, [0, 300, 512], 7), (2, 32, 8, 64, 1200, [1200, 45], 0),
+             (4, 32, 8, 128, 2048, [5, 2048, 2000, 128], 13)]
+    need = max(g.workspace_bytes(g.make_dims(B, Hq, Hkv, D, Lmax)) for (B, Hq, Hkv, D, Lmax, _, _) in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for i, (B, Hq, Hkv, D, Lmax, valid, max_ctas) in enumerate(cases):
+        w = workloads.Workload(0, "case", batch=B, num_layers=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                               head_dim=D, max_len=Lmax)
+        x = workloads.make_layer(w, 0, device="cpu", seed=100 + i)
+        g.set_option(g.GQAQ_OPT_MAX_CTAS, max_ctas)
+        scale = 1.0 / math.sqrt(D)
+        out = g.gqa_decode_attn(x["q"].to(DEV), x["k_cache"].to(DEV), x["v_cache"].to(DEV),
+                                torch.tensor(valid, dtype=torch.int32, device=DEV), scale, workspace=ws)
+        torch.cuda.synchronize()
+        flags = g.device_status()
+        assert flags in (0, g.GQAQ_DEV_BAD_LEN) and (flags == 0) == (min(valid) >= 1)
+        assert int(ws[:256].count_nonzero()) == 0
+        keep = [b for b in range(B) if valid[b] >= 1]
+        assert all(bool((out[b] == 0).all()) for b in range(B) if valid[b] < 1)   # no valid token -> zeros
+        ref = oracle.attn_repeat_kv(x["q"].numpy()[keep], x["k_cache"].numpy()[keep], x["v_cache"].numpy()[keep],
+                                    [valid[b] for b in keep], scale)
+        assert_attn_close(out[keep], ref)
 
 
 @pytest.mark.parametrize("valid", [[1], [15], [16], [17], [127], [128], [129], [300]])

@@ -248,17 +248,22 @@ def test_wait_timeout_is_reported_and_context_survives():
                            max_len=512)
     x = workloads.make_layer(w, 0, device=DEV, seed=3)
     args = (x["q"], x["k_cache"], x["v_cache"], x["valid_len"])
+    ws = g.alloc_workspace(g.dims_of(x["q"], x["k_cache"]), DEV)
     g.device_status(reset=True)
     try:
         g.set_option(g.GQAQ_OPT_WAIT_TIMEOUT_NS, 1_000_000)
         g.set_option(g.GQAQ_OPT_TEST_STALL, 1)
-        g.gqa_decode_attn(*args, 0.1)
+        g.set_option(g.GQAQ_OPT_MAX_CTAS, 5)         # every unit split: counters in use
+        g.gqa_decode_attn(*args, 0.1, workspace=ws)
         flags = g.device_status(reset=True)
     finally:
         g.set_option(g.GQAQ_OPT_TEST_STALL, 0)
         g.set_option(g.GQAQ_OPT_WAIT_TIMEOUT_NS, 2_000_000_000)
+        g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
     assert flags & g.GQAQ_DEV_TIMEOUT
-    out = g.gqa_decode_attn(*args, 0.1)          # the context is still usable
+    torch.cuda.synchronize()
+    assert int(ws[:256].count_nonzero()) == 0      # arrival counters back at zero
+    out = g.gqa_decode_attn(*args, 0.1, workspace=ws)   # the context and the workspace are still usable
     ref = oracle.attn_repeat_kv(x["q"].cpu().numpy(), x["k_cache"].cpu().numpy(), x["v_cache"].cpu().numpy(),
                                 x["valid_len"].cpu().numpy(), 0.1)
     assert_attn_close(out, ref)
