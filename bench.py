@@ -208,11 +208,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Workload state on the device
 # ---------------------------------------------------------------------------
-def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True):
+def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True,
+                quest_kernel: str = "cluster"):
     import gqa_head_folding_gb300 as g
     from gqa_head_folding_gb300.decode import DecodeStack, Layer
     stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
-                        w.dense_layers, device, w.page_size, fused=fused)
+                        w.dense_layers, device, w.page_size, fused=fused, quest_kernel=quest_kernel)
     layers, lens = [], []
     for layer in range(w.num_layers):
         x = workloads.make_layer(w, layer, device=device,
@@ -352,7 +353,8 @@ def workload_from_args(args) -> workloads.Workload:
     return w
 
 
-def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool = True) -> dict:
+def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool = True,
+              quest_kernel: str = "cluster") -> dict:
     return {"workload": f"{w.name} (config {w.id})", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
             "layers": w.num_layers, "dense_layers": w.num_layers if w.k_pages is None else w.dense_layers,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
@@ -360,7 +362,8 @@ def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool =
             "page_size": w.page_size, "k_pages": w.k_pages,
             "token_budget": None if w.k_pages is None else w.k_pages * w.page_size,
             "append": w.append, "planted_pages_per_head": w.n_plant, "parallelism": f"replicas x{world}",
-            "quest_path": "fused (quest_decode_attn)" if fused else "step-by-step calls",
+            "quest_path": (f"fused (quest_decode_attn, {'GPU-wide work queue' if quest_kernel == 'queue' else 'cluster per unit'})"
+                           if fused else "step-by-step calls"),
             "launch": "programmatic dependent launch" if pdl else "plain stream order",
             "l2": "per-step working set > 4x L2; no flush"}
 
@@ -409,7 +412,8 @@ def run_ours(args, rank, world, local):
     w = workload_from_args(args)
     g.lib()
     g.set_option(g.GQAQ_OPT_PDL, 0 if args.no_pdl else 1)
-    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused)
+    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused,
+                                      quest_kernel=args.quest_kernel)
     sb = step_bytes(w, lens, fused=not args.unfused)
     step = lambda: stack.step(layers)  # noqa: E731
     graph = capture(step, device)
@@ -496,7 +500,8 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16 in/out, f32 accumulate",
-        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl),
+        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl,
+                                                                                       quest_kernel=args.quest_kernel),
         "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
         "achieved_frac_of_peak": round(sb["total"] / s_per_step / 1e9 / peaks["hbm_gbs"], 4),
         "bytes_per_step": total_bytes,
@@ -528,6 +533,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="run Quest layers as the step-by-step calls")
+    ap.add_argument("--quest-kernel", choices=("queue", "cluster"), default="cluster",
+                    help="fused Quest kernel: one cluster per unit (default) or the GPU-wide work queue")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()

@@ -83,7 +83,7 @@ def lib():
         L.quest_sparse_attn.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp,
                                         ctypes.c_size_t, vp]
         L.quest_decode_attn.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp,
-                                        vp]
+                                        vp, ctypes.c_size_t, vp]
         L.gqa_decode_attn_noalloc.argtypes = [dp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
         L.gqaq_status_string.argtypes = [i32]
         L.gqaq_status_string.restype = ctypes.c_char_p
@@ -158,10 +158,17 @@ def workspace_bytes(dims: Dims, max_selected_pages: int = 0) -> int:
     return int(n)
 
 
-def alloc_workspace(dims: Dims, device) -> torch.Tensor:
-    """Workspace for gqa_decode_attn / quest_sparse_attn. Zero-filled once, as
-    the library asks; every call leaves its counters at zero again."""
-    return torch.zeros(workspace_bytes(dims), dtype=torch.uint8, device=device)
+def alloc_workspace(dims: Dims, device, max_selected_pages: int = 0) -> torch.Tensor:
+    """Workspace for gqa_decode_attn / quest_sparse_attn, and with
+    max_selected_pages = k also for quest_decode_attn's work-queue kernel.
+    Zero-filled once, as the library asks; every call leaves its counters at
+    zero again."""
+    return torch.zeros(workspace_bytes(dims, max_selected_pages), dtype=torch.uint8, device=device)
+
+
+def workspace_zero_bytes(dims: Dims) -> int:
+    """Leading bytes of a workspace that hold counters and flags (zero between calls)."""
+    return (256 + 12 * dims.batch * dims.num_kv_heads + 255) // 256 * 256
 
 
 def num_pages(max_len: int, page_size: int = PAGE_SIZE) -> int:
@@ -190,10 +197,12 @@ def gqa_decode_attn(q, k_cache, v_cache, valid_len, scale: float, out=None, work
 
 
 def quest_decode_attn(q, k_cache, v_cache, meta, valid_len, k: int, scale: float, k_new=None, v_new=None,
-                      pos=None, out=None, scores=None, page_idx=None, page_size: int = PAGE_SIZE):
+                      pos=None, out=None, scores=None, page_idx=None, page_size: int = PAGE_SIZE,
+                      workspace=None):
     """Fused Quest step in one launch: optional append (k_new, v_new at pos),
     page scores, top-k pages and attention over them. scores/page_idx are
-    optional outputs."""
+    optional outputs. With a workspace (alloc_workspace(dims, device, k)) the
+    step runs as one GPU-wide work queue; without, one cluster per unit."""
     _need(q, "q", torch.float16, 3)
     _need(k_cache, "k_cache", torch.float16, 4)
     _need(v_cache, "v_cache", torch.float16, 4)
@@ -214,7 +223,7 @@ def quest_decode_attn(q, k_cache, v_cache, meta, valid_len, k: int, scale: float
     _check("quest_decode_attn", lib().quest_decode_attn(
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(k_new), _ptr(v_new),
         _ptr(pos), _ptr(valid_len), int(k), float(scale), _ptr(out), _ptr(scores), _ptr(page_idx),
-        _stream(q)))
+        _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(q)))
     return out
 
 

@@ -181,11 +181,16 @@ int gqaq_device_status(int *flags, int reset) {
 }
 
 size_t gqaq_workspace_bytes(const gqaq_dims *dims, int max_selected_pages) {
-    (void)max_selected_pages;
     if (check_dims(dims, false) != GQAQ_OK) return 0;
     LaunchCtx ctx;
     if (make_ctx(&ctx, nullptr) != GQAQ_OK) return 0;
-    return attention_workspace_bytes(dims, ctx);
+    size_t need = attention_workspace_bytes(dims, ctx);
+    if (need == 0) return 0;
+    if (max_selected_pages > 0 && dims->page_size == 16) {
+        const size_t qs = quest_stream_workspace_bytes(dims, max_selected_pages, ctx);
+        if (qs > need) need = qs;
+    }
+    return need;
 }
 
 int gqa_decode_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *k_cache,
@@ -321,7 +326,7 @@ int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half
 int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_cache, gqaq_half *v_cache,
                       gqaq_half *meta, const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos,
                       const int32_t *valid_len, int k, float scale, gqaq_half *out, float *scores,
-                      int32_t *page_idx, void *stream) {
+                      int32_t *page_idx, void *workspace, size_t workspace_bytes, void *stream) {
     int rc = check_dims(dims, true);
     if (rc != GQAQ_OK) return rc;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(meta) ||
@@ -331,7 +336,7 @@ int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_ca
     if ((scores != nullptr && !aligned16(scores)) || (page_idx != nullptr && !aligned16(page_idx)))
         return GQAQ_ERR_INVALID_ARG;
     if (k < 1 || k > 65536) return GQAQ_ERR_INVALID_ARG;
-    if (k > kFusedMaxPages) return GQAQ_ERR_UNSUPPORTED;
+    if (workspace != nullptr && !aligned16(workspace)) return GQAQ_ERR_WORKSPACE;
     if (!isfinite(scale)) return GQAQ_ERR_INVALID_ARG;
     const int64_t pmax = (dims->max_len + dims->page_size - 1) / dims->page_size;
     if ((int64_t)dims->batch * dims->num_kv_heads * pmax > (int64_t)INT32_MAX - 1024) return GQAQ_ERR_UNSUPPORTED;
@@ -353,6 +358,13 @@ int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_ca
     f.kpages = k;
     f.scale = scale;
     f.out = reinterpret_cast<__half *>(out);
+    f.workspace = workspace;
+    f.workspace_bytes = workspace_bytes;
+    if (workspace != nullptr) {
+        // The work-queue kernel, when the shape is in its range.
+        if (quest_stream_workspace_bytes(dims, k, ctx) > 0) return launch_quest_stream(f, ctx);
+    }
+    if (k > kFusedMaxPages) return GQAQ_ERR_UNSUPPORTED;
     return launch_quest_fused(f, ctx);
 }
 

@@ -538,11 +538,9 @@ int grid_for(const LaunchCtx &ctx) {
     return grid;
 }
 
-// Workspace: [B*Hkv] u32 arrival counters (256-byte padded), then the
-// partials [grid][2][G][D+2] fp32.
-inline size_t count_bytes(const gqaq_dims &dm) {
-    return ((size_t)dm.batch * dm.num_kv_heads * sizeof(unsigned) + 255) & ~(size_t)255;
-}
+// Workspace: the zero region (arrival counters [B*Hkv] u32 at kWsCounters),
+// then the partials [grid][2][G][D+2] fp32.
+inline size_t count_bytes(const gqaq_dims &dm) { return workspace_zero_bytes(dm); }
 
 template <int D, int G, bool SPARSE>
 int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
@@ -565,7 +563,7 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     p.valid_len = a.valid_len;
     p.page_idx = a.page_idx;
     p.out = a.out;
-    p.count = reinterpret_cast<unsigned *>(a.workspace);
+    p.count = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(a.workspace) + kWsCounters);
     p.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + cbytes);
     p.status = ctx.status;
     p.B = dm.batch;

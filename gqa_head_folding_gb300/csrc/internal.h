@@ -39,6 +39,17 @@ size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx);
 // Fused Quest step (quest_fused.cu). meta == nullptr selects attention over a
 // given page list (page_idx is then an input); otherwise append (pos may be
 // null), score, select and attend, with scores/page_idx optional outputs.
+// Workspace layout shared by the kernels that take one. A zero region comes
+// first: the work ticket at kWsTicket and three words per (sequence, KV head)
+// from kWsCounters (arrival counters and flags). It is zero between calls;
+// every call leaves it so. Scratch follows from workspace_zero_bytes(dims).
+constexpr size_t kWsTicket = 0;
+constexpr size_t kWsCounters = 256;
+inline size_t workspace_zero_bytes(const gqaq_dims &dm) {
+    const size_t units = (size_t)dm.batch * dm.num_kv_heads;
+    return (kWsCounters + 3 * units * sizeof(unsigned) + 255) & ~(size_t)255;
+}
+
 struct FusedArgs {
     const gqaq_dims *dims;
     const __half *q;
@@ -54,8 +65,14 @@ struct FusedArgs {
     int kpages;
     float scale;
     __half *out;
+    void *workspace;  // work-queue kernel only
+    size_t workspace_bytes;
 };
 int launch_quest_fused(const FusedArgs &a, const LaunchCtx &ctx);
+// The same step as one work queue over the whole GPU (needs the workspace).
+int launch_quest_stream(const FusedArgs &a, const LaunchCtx &ctx);
+// Workspace launch_quest_stream needs; 0 when the shape is outside its range.
+size_t quest_stream_workspace_bytes(const gqaq_dims *dims, int kpages, const LaunchCtx &ctx);
 constexpr int kFusedMaxPages = 1024;
 
 // Quest kernels.

@@ -31,6 +31,7 @@
 
 #include "attn_tile.cuh"
 #include "internal.h"
+#include "quest_tile.cuh"
 
 namespace gqaq {
 
@@ -90,21 +91,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t score_key(float f) {
-    uint32_t x = __float_as_uint(f);
-    if (x == 0x80000000u) x = 0u;  // -0 ranks with +0
-    return (x & 0x80000000u) ? ~x : (x | 0x80000000u);
-}
-__device__ __forceinline__ uint32_t hmin0_bits(uint32_t x) {
-    __half2 h = *reinterpret_cast<__half2 *>(&x);
-    __half2 r = __hmin2(h, __float2half2_rn(0.f));
-    return *reinterpret_cast<uint32_t *>(&r);
-}
-__device__ __forceinline__ uint32_t hmax0_bits(uint32_t x) {
-    __half2 h = *reinterpret_cast<__half2 *>(&x);
-    __half2 r = __hmax2(h, __float2half2_rn(0.f));
-    return *reinterpret_cast<uint32_t *>(&r);
 }
 
 enum { FUSED_FULL = 0, FUSED_ATTEND = 1 };

@@ -9,8 +9,11 @@ carries a new token, every layer first appends it (``quest_append_kv``), so
 each layer's page metadata stays current whatever path reads it.
 
 By default a Quest layer is one fused launch (``quest_decode_attn``: append,
-score, top-K and sparse attention in one thread-block-cluster kernel). With
-``fused=False`` the same layer runs as the four step-by-step calls.
+score, top-K and sparse attention in one kernel). With ``quest_kernel=
+"cluster"`` (default) that kernel runs one thread-block cluster per
+(sequence, KV head) and needs no workspace; ``"queue"`` runs the GPU-wide
+work queue on the stack's workspace. With ``fused=False`` the same layer runs as the four
+step-by-step calls.
 
 This module only sequences library calls and owns the scratch buffers they
 share. Every arithmetic step runs in the CUDA kernels.
@@ -44,15 +47,20 @@ class Layer:
 
 class DecodeStack:
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_len: int,
-                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True):
+                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True,
+                 quest_kernel: str = "cluster"):
+        if quest_kernel not in ("queue", "cluster"):
+            raise ValueError(f"quest_kernel must be 'queue' or 'cluster', not {quest_kernel!r}")
         self.fused = fused
+        self.quest_kernel = quest_kernel
         self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
         self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
         self.k_pages, self.dense_layers = k_pages, dense_layers
         self.scale = 1.0 / math.sqrt(head_dim)
         self.device = torch.device(device)
         dims = make_dims(batch, num_q_heads, num_kv_heads, head_dim, max_len, page_size)
-        self.workspace = alloc_workspace(dims, self.device)
+        self.workspace = alloc_workspace(dims, self.device, k_pages or 0)
+        self.quest_workspace = self.workspace if quest_kernel == "queue" else None
         pmax = num_pages(max_len, page_size)
         self.scores = torch.empty(batch, num_kv_heads, pmax, dtype=torch.float32, device=self.device)
         self.page_idx = (torch.empty(batch, num_kv_heads, k_pages, dtype=torch.int32, device=self.device)
@@ -87,7 +95,8 @@ class DecodeStack:
             elif self.fused:
                 add("quest", lambda L=L: quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len,
                                                            self.k_pages, self.scale, k_new=L.k_new, v_new=L.v_new,
-                                                           pos=L.pos, out=L.out, page_size=self.page_size))
+                                                           pos=L.pos, out=L.out, page_size=self.page_size,
+                                                           workspace=self.quest_workspace))
             else:
                 add("score", lambda L=L: quest_score_pages(L.q, L.meta, L.valid_len, self.max_len,
                                                            scores=self.scores, page_size=self.page_size))
@@ -116,7 +125,8 @@ class DecodeStack:
                                 workspace=self.workspace)
             elif self.fused:
                 quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages, self.scale,
-                                  k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out, page_size=self.page_size)
+                                  k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out, page_size=self.page_size,
+                                  workspace=self.quest_workspace)
             else:
                 quest_score_pages(L.q, L.meta, L.valid_len, self.max_len, scores=self.scores,
                                   page_size=self.page_size)

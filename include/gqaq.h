@@ -94,14 +94,16 @@ typedef struct {
 /* Bytes of workspace that gqa_decode_attn and quest_sparse_attn need on the
  * current device for these dims (enough for both). The library sizes its
  * grid from the SM count, so the figure depends on the device.
- * `max_selected_pages` is accepted for future use and is not needed today.
+ * With max_selected_pages = k > 0 (and S = 16) the figure also covers
+ * quest_decode_attn's work-queue kernel for that k.
  * Returns 0 when the dims are invalid or unsupported.
- * The workspace holds one arrival counter per (sequence, KV head) followed by
- * the fp32 partials of context splits. The counters must be zero when the
- * workspace is first used: zero-fill it once (cudaMemsetAsync) after
- * allocating it. Every call, including one whose waits time out, leaves the
- * counters at zero again, so the workspace can be reused by any later call
- * (of any dims that fit) without clearing. */
+ * The workspace starts with counters and flags (a ticket word, three words
+ * per (sequence, KV head)) followed by scratch (fp32 partials, page keys and
+ * lists). The counters must be zero when the workspace is first used:
+ * zero-fill it once (cudaMemsetAsync) after allocating it. Every call leaves
+ * them at zero again, so the workspace can be reused by any later call (of
+ * any dims that fit) without clearing; gqa_decode_attn and quest_sparse_attn
+ * do so even when their waits time out. */
 GQAQ_API size_t gqaq_workspace_bytes(const gqaq_dims *dims, int max_selected_pages);
 
 /* [OPT] section 3: dense decode attention with the query heads folded.
@@ -173,18 +175,25 @@ GQAQ_API int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const 
  * quest_append_kv, quest_score_pages, quest_topk_pages and quest_sparse_attn
  * do: when pos is not NULL, append k_new/v_new at row pos[b] and update that
  * page's min/max; score every valid page; select the k best pages (ties to
- * the lower index); attend over only their tokens ([QUEST] flowchart). One
- * thread-block cluster handles one (sequence, KV head) at a time: its CTAs
- * split the pages, agree on the K-th score through distributed shared memory,
- * split the selected pages and merge their softmax states there. So the
- * call needs no workspace. scores ([B][Hkv][Pmax] fp32) and page_idx
- * ([B][Hkv][k] int32, ascending, -1 padded) are optional outputs (NULL to
- * skip). Requires 1 <= k <= 1024 (GQAQ_ERR_UNSUPPORTED above), S = 16. */
+ * the lower index); attend over only their tokens ([QUEST] flowchart).
+ * scores ([B][Hkv][Pmax] fp32) and page_idx ([B][Hkv][k] int32, ascending,
+ * -1 padded) are optional outputs (NULL to skip). S = 16, 1 <= k <= 65536.
+ * With a workspace (>= gqaq_workspace_bytes(dims, k) bytes, zero-filled
+ * before its first use, see gqaq_workspace_bytes) the step runs as one work
+ * queue over the whole GPU: page-scoring and attention pieces of every
+ * (sequence, KV head) are taken from a ticket counter; the last scorer of a
+ * (sequence, KV head) selects its pages, the last attention piece merges its
+ * softmax states. That covers Pmax <= 8192 pages. Otherwise, and with
+ * workspace NULL, one thread-block cluster handles one (sequence, KV head)
+ * at a time and needs no workspace; it requires k <= 1024
+ * (GQAQ_ERR_UNSUPPORTED above). Two calls that overlap on the GPU must not
+ * share a workspace. After a call whose waits timed out (GQAQ_DEV_TIMEOUT),
+ * zero the workspace again before reusing it. */
 GQAQ_API int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_cache,
                                gqaq_half *v_cache, gqaq_half *meta, const gqaq_half *k_new,
                                const gqaq_half *v_new, const int32_t *pos, const int32_t *valid_len,
                                int k, float scale, gqaq_half *out, float *scores, int32_t *page_idx,
-                               void *stream);
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* gqa_decode_attn for callers that cannot allocate device memory. The source
  * pages have no counterpart to this call. A plugin or custom operator inside a

@@ -1,10 +1,16 @@
 """GPU parity of quest_decode_attn, the fused Quest step (append, page scores,
-top-K, sparse attention in one cluster kernel), against the fp64 oracle.
+top-K, sparse attention in one launch), against the fp64 oracle, for both of
+its kernels.
 
-Cluster sizes 1, 2, 4 and 8 are forced so the cross-CTA paths (radix
-threshold from summed histograms, page-list compaction, log-sum-exp merge
-through distributed shared memory) all run, including CTAs whose page range
-or page share is empty.
+Cluster kernel (no workspace): cluster sizes 1, 2, 4 and 8 are forced so the
+cross-CTA paths (radix threshold from summed histograms, page-list
+compaction, log-sum-exp merge through distributed shared memory) all run,
+including CTAs whose page range or page share is empty.
+
+Work-queue kernel (with a workspace): grids are forced down to 1..7 CTAs so
+one CTA holds many items, waits for page lists that its own ring has still
+to select, and merges partials that other CTAs wrote; the workspace's
+counters and flags must be back at zero after every call.
 """
 import math
 
@@ -29,9 +35,20 @@ def _reset_options():
     g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
 
 
+def zero_region_clear(ws, B, Hkv):
+    torch.cuda.synchronize()
+    return int(ws[:g.workspace_zero_bytes(g.make_dims(B, Hkv, Hkv, 64, 16))].count_nonzero()) == 0
+
+
 def run_fused(D, G, K, csize, B=3, Hkv=2, Lmax=16 * 45 + 3, valid=(16 * 45 + 3, 16 * 23 + 7, 20), seed=0,
-              append=True):
+              append=True, queue_ctas=None):
+    """csize: forced cluster size (cluster kernel). queue_ctas: when not None,
+    run the work-queue kernel on that many CTAs (0 = the full grid)."""
     g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, csize)
+    ws = None
+    if queue_ctas is not None:
+        g.set_option(g.GQAQ_OPT_MAX_CTAS, queue_ctas)
+        ws = g.alloc_workspace(g.make_dims(B, G * Hkv, Hkv, D, Lmax), DEV, K)
     w = workloads.Workload(0, "fused", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
                            head_dim=D, max_len=Lmax, k_pages=K, n_plant=3, append=True)
     x = workloads.make_layer(w, 0, device="cpu", seed=seed)
@@ -45,9 +62,12 @@ def run_fused(D, G, K, csize, B=3, Hkv=2, Lmax=16 * 45 + 3, valid=(16 * 45 + 3, 
     idx = torch.full((B, Hkv, K), -7, dtype=torch.int32, device=DEV)
     scale = 1.0 / math.sqrt(D)
     kw = dict(k_new=x["k_new"].to(DEV), v_new=x["v_new"].to(DEV), pos=pos.to(DEV)) if append else {}
-    out = g.quest_decode_attn(x["q"].to(DEV), kd, vd, meta, vld, K, scale, scores=scores, page_idx=idx, **kw)
+    out = g.quest_decode_attn(x["q"].to(DEV), kd, vd, meta, vld, K, scale, scores=scores, page_idx=idx,
+                              workspace=ws, **kw)
     torch.cuda.synchronize()
     assert g.device_status() == 0
+    if ws is not None:
+        assert zero_region_clear(ws, B, Hkv)
 
     kc = x["k_cache"].numpy().copy(); vc = x["v_cache"].numpy().copy()
     if append:
@@ -81,6 +101,126 @@ def test_fused_matches_oracle(D, G, K, csize):
 @pytest.mark.parametrize("csize", [1, 4])
 def test_fused_without_append(csize):
     run_fused(128, 4, 9, csize, append=False, seed=77)
+
+
+@pytest.mark.parametrize("D,G,K,ctas", [
+    (128, 4, 8, 0), (128, 1, 16, 1), (128, 4, 16, 2), (64, 4, 5, 2), (64, 2, 40, 0), (128, 8, 3, 3),
+    (64, 8, 7, 5), (64, 1, 12, 1), (128, 2, 30, 7), (128, 1, 200, 4),
+])
+def test_queue_kernel_matches_oracle(D, G, K, ctas):
+    run_fused(D, G, K, 0, seed=D + 10 * G + K + ctas, queue_ctas=ctas)
+
+
+@pytest.mark.parametrize("ctas", [0, 1])
+def test_queue_kernel_without_append(ctas):
+    run_fused(128, 4, 9, 0, append=False, seed=78, queue_ctas=ctas)
+
+
+@pytest.mark.parametrize("ctas", [0, 3])
+def test_queue_kernel_long_ragged_batch(ctas):
+    # more metadata tiles per sequence than one score item holds, ragged lengths
+    run_fused(128, 2, 24, 0, B=4, Hkv=3, Lmax=16 * 700 + 9, valid=(16 * 700 + 9, 16 * 301, 130, 16 * 129 + 1),
+              seed=91, queue_ctas=ctas)
+
+
+def test_queue_kernel_more_than_1024_pages():
+    # k beyond the cluster kernel's limit
+    run_fused(64, 4, 1100, 0, B=1, Hkv=2, Lmax=16 * 1500, valid=(16 * 1500 - 3,), seed=5, queue_ctas=0)
+
+
+def test_queue_kernel_empty_sequence_gives_zeros():
+    B, Hkv, D, G, Lmax, K = 3, 2, 128, 4, 16 * 40, 6
+    w = workloads.Workload(0, "fused", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax)
+    x = workloads.make_layer(w, 0, device=DEV, seed=12)
+    vl = torch.tensor([16 * 40, 0, 77], dtype=torch.int32, device=DEV)
+    meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+    g.quest_update_meta(x["k_cache"], vl, meta)
+    ws = g.alloc_workspace(g.make_dims(B, G * Hkv, Hkv, D, Lmax), DEV, K)
+    g.device_status(reset=True)
+    out = g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, vl, K, 0.09, workspace=ws)
+    assert g.device_status(reset=True) & g.GQAQ_DEV_BAD_LEN
+    assert zero_region_clear(ws, B, Hkv)
+    assert bool((out[1] == 0).all())
+    keep = [0, 2]
+    idx = torch.empty(B, Hkv, K, dtype=torch.int32, device=DEV)
+    out2 = g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, vl, K, 0.09, page_idx=idx, workspace=ws)
+    assert torch.equal(out, out2)
+    vk = vl.cpu().numpy()[keep]
+    sel = idx.cpu().numpy()[keep]
+    q = x["q"].cpu().numpy()[keep]; kc = x["k_cache"].cpu().numpy()[keep]; vc = x["v_cache"].cpu().numpy()[keep]
+    ref_scores = oracle.page_scores(q, oracle.page_minmax(kc, vk, S), vk, S)
+    check_topk(sel, ref_scores, vk, S, K)
+    assert_attn_close(out[keep], oracle.sparse_attn(q, kc, vc, vk, sel, S, 0.09))
+
+
+def test_queue_kernel_repeatable_and_graph_capturable():
+    w = workloads.WORKLOADS[4].with_(batch=3, max_len=16 * 300)
+    x = workloads.make_layer(w, 0, device=DEV)
+    B, Hkv, Lmax, D = x["k_cache"].shape
+    meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+    g.quest_update_meta(x["k_cache"], x["valid_len"] - 1, meta)
+    out = torch.empty_like(x["q"])
+    idx = torch.empty(B, Hkv, 64, dtype=torch.int32, device=DEV)
+    ws = g.alloc_workspace(g.dims_of(x["q"], x["k_cache"]), DEV, 64)
+
+    def step():
+        g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], 64, 0.088,
+                            k_new=x["k_new"], v_new=x["v_new"], pos=x["pos"], out=out, page_idx=idx, workspace=ws)
+
+    step()
+    first_out, first_idx = out.clone(), idx.clone()
+    for _ in range(3):
+        step()                                          # re-appending the same token is idempotent
+        assert torch.equal(out, first_out) and torch.equal(idx, first_idx)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_(); idx.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, first_out) and torch.equal(idx, first_idx)
+    assert zero_region_clear(ws, B, Hkv)
+    # the cluster kernel (no workspace) selects the same pages
+    idx2 = torch.empty_like(idx)
+    g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], 64, 0.088, page_idx=idx2)
+    assert torch.equal(idx2, first_idx)
+
+
+def test_queue_kernel_timeout_is_reported_and_context_survives():
+    # the producers issue nothing, so every consumer wait runs out after 1 ms
+    B, Hkv, D, G, Lmax, K = 2, 2, 128, 2, 16 * 64, 8
+    w = workloads.Workload(0, "fused", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax)
+    x = workloads.make_layer(w, 0, device=DEV, seed=4)
+    meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+    g.quest_update_meta(x["k_cache"], x["valid_len"], meta)
+    ws = g.alloc_workspace(g.make_dims(B, G * Hkv, Hkv, D, Lmax), DEV, K)
+    args = (x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], K, 0.1)
+    g.device_status(reset=True)
+    try:
+        g.set_option(g.GQAQ_OPT_WAIT_TIMEOUT_NS, 1_000_000)
+        g.set_option(g.GQAQ_OPT_TEST_STALL, 1)
+        g.quest_decode_attn(*args, workspace=ws)
+        flags = g.device_status(reset=True)
+    finally:
+        g.set_option(g.GQAQ_OPT_TEST_STALL, 0)
+        g.set_option(g.GQAQ_OPT_WAIT_TIMEOUT_NS, 2_000_000_000)
+    assert flags & g.GQAQ_DEV_TIMEOUT
+    ws.zero_()                                           # the documented reset after a timeout
+    idx = torch.empty(B, Hkv, K, dtype=torch.int32, device=DEV)
+    out = g.quest_decode_attn(*args, page_idx=idx, workspace=ws)
+    assert g.device_status(reset=True) == 0
+    vl = x["valid_len"].cpu().numpy()
+    q, kc, vc = x["q"].cpu().numpy(), x["k_cache"].cpu().numpy(), x["v_cache"].cpu().numpy()
+    sel = idx.cpu().numpy()
+    check_topk(sel, oracle.page_scores(q, oracle.page_minmax(kc, vl, S), vl, S), vl, S, K)
+    assert_attn_close(out, oracle.sparse_attn(q, kc, vc, vl, sel, S, 0.1))
 
 
 @pytest.mark.parametrize("csize", [2, 8])
@@ -147,6 +287,6 @@ def test_sparse_call_above_the_fused_page_limit():
     ref = oracle.sparse_attn(x["q"].cpu().numpy(), x["k_cache"].cpu().numpy(), x["v_cache"].cpu().numpy(),
                              vl.cpu().numpy(), sel, S, 0.125)
     assert_attn_close(out, ref)
-    with pytest.raises(g.GqaqError):
+    with pytest.raises(g.GqaqError):              # the cluster kernel stops at 1024 pages
         meta = g.new_meta(B, Hkv, Lmax, D, DEV)
         g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, vl, K, 0.125)
