@@ -208,12 +208,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Workload state on the device
 # ---------------------------------------------------------------------------
-def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True,
-                quest_kernel: str = "cluster"):
+def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True):
     import gqa_head_folding_gb300 as g
     from gqa_head_folding_gb300.decode import DecodeStack, Layer
     stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
-                        w.dense_layers, device, w.page_size, fused=fused, quest_kernel=quest_kernel)
+                        w.dense_layers, device, w.page_size, fused=fused)
     layers, lens = [], []
     for layer in range(w.num_layers):
         x = workloads.make_layer(w, layer, device=device,
@@ -412,8 +411,9 @@ def run_ours(args, rank, world, local):
     w = workload_from_args(args)
     g.lib()
     g.set_option(g.GQAQ_OPT_PDL, 0 if args.no_pdl else 1)
-    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused,
-                                      quest_kernel=args.quest_kernel)
+    if args.quest_kernel == "queue":
+        g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 2)
+    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused)
     sb = step_bytes(w, lens, fused=not args.unfused)
     step = lambda: stack.step(layers)  # noqa: E731
     graph = capture(step, device)

@@ -39,6 +39,7 @@ GQAQ_OPT_WAIT_TIMEOUT_NS = 2
 GQAQ_OPT_TEST_STALL = 3
 GQAQ_OPT_CLUSTER_SIZE = 4
 GQAQ_OPT_PDL = 5
+GQAQ_OPT_QUEST_KERNEL = 6
 
 PAGE_SIZE = 16
 

@@ -24,6 +24,7 @@ std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cluster_size{0};
 std::atomic<int64_t> g_opt_pdl{1};
+std::atomic<int64_t> g_opt_quest_kernel{0};
 
 struct DeviceState {
     bool ready = false;
@@ -72,6 +73,7 @@ int make_ctx(LaunchCtx *ctx, void *stream) {
     ctx->test_stall = (int)g_opt_test_stall.load();
     ctx->cluster_size = (int)g_opt_cluster_size.load();
     ctx->pdl = (int)g_opt_pdl.load();
+    ctx->quest_kernel = (int)g_opt_quest_kernel.load();
     ctx->status = s->status;
     return GQAQ_OK;
 }
@@ -153,6 +155,10 @@ int gqaq_set_option(int option, int64_t value) {
             return GQAQ_OK;
         case GQAQ_OPT_PDL:
             g_opt_pdl.store(value != 0 ? 1 : 0);
+            return GQAQ_OK;
+        case GQAQ_OPT_QUEST_KERNEL:
+            if (value < 0 || value > 2) return GQAQ_ERR_INVALID_ARG;
+            g_opt_quest_kernel.store(value);
             return GQAQ_OK;
         case GQAQ_OPT_CLUSTER_SIZE:
             if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return GQAQ_ERR_INVALID_ARG;
@@ -360,11 +366,15 @@ int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_ca
     f.out = reinterpret_cast<__half *>(out);
     f.workspace = workspace;
     f.workspace_bytes = workspace_bytes;
-    if (workspace != nullptr) {
-        // The work-queue kernel, when the shape is in its range.
-        if (quest_stream_workspace_bytes(dims, k, ctx) > 0) return launch_quest_stream(f, ctx);
+    // The cluster kernel when it covers the shape (the faster one at every
+    // measured shape); the work-queue kernel for larger k, or when forced.
+    const bool queue_ok = workspace != nullptr && quest_stream_workspace_bytes(dims, k, ctx) > 0;
+    const bool cluster_ok = k <= kFusedMaxPages;
+    if (ctx.quest_kernel == 2 || (ctx.quest_kernel == 0 && !cluster_ok)) {
+        if (!queue_ok) return workspace == nullptr ? GQAQ_ERR_WORKSPACE : GQAQ_ERR_UNSUPPORTED;
+        return launch_quest_stream(f, ctx);
     }
-    if (k > kFusedMaxPages) return GQAQ_ERR_UNSUPPORTED;
+    if (!cluster_ok) return GQAQ_ERR_UNSUPPORTED;
     return launch_quest_fused(f, ctx);
 }
 

@@ -26,6 +26,7 @@ struct LaunchCtx {
     int test_stall;        // attention producer issues nothing (timeout test)
     int cluster_size;      // fused Quest kernel: forced CTAs per cluster, 0 = automatic
     int pdl;               // launch with programmatic stream serialization
+    int quest_kernel;      // fused Quest kernel: 0 automatic, 1 cluster, 2 work queue
     int *status;           // device status word
 };
 

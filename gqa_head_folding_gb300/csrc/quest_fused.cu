@@ -68,29 +68,18 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-// Arrive (release, cluster scope) on the mbarrier at `local_addr` in CTA `rank`.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t local_addr, uint32_t rank) {
-    const uint32_t ra = dsmem_map(local_addr, rank);
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
-}
-// Bounded wait (acquire, cluster scope) for the phase with parity `parity`.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity), "r"(20000u)
-            : "memory");
-        if (ok) return true;
-        if (global_timer_ns() - t0 >= timeout_ns) return false;
-    }
-}
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Unsigned min / max into a shared word of CTA `rank` of this cluster.
+__device__ __forceinline__ void red_dsmem_min_u32(uint32_t local_addr, uint32_t rank, uint32_t v) {
+    asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(dsmem_map(local_addr, rank)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_dsmem_max_u32(uint32_t local_addr, uint32_t rank, uint32_t v) {
+    asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(dsmem_map(local_addr, rank)), "r"(v) : "memory");
 }
 
 enum { FUSED_FULL = 0, FUSED_ATTEND = 1 };
@@ -113,11 +102,11 @@ struct FusedCfg : TileCfg<D, G> {
     // [768,800), counts [800,808), scan scratch [808,832), scalars [832,848),
     // then the full/empty mbarriers (8-byte aligned) at word 848.
     static constexpr int MISC_BARRIER_WORD = 848;
-    static constexpr int MISC = MISC_BARRIER_WORD * 4 + (2 * 3 + 1) * 8;  // full, empty, list
+    static constexpr int MISC = MISC_BARRIER_WORD * 4 + 2 * 3 * 8;  // full, empty
     static constexpr int FIXED = KEYMERGE + QREGION + T::PBYTES + KSEL_MAX * 4 + CSTATE + MISC + 1024;
     static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
     static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
-    static_assert(MISC >= MISC_BARRIER_WORD * 4 + (2 * NSTAGE + 1) * 8, "misc region holds the mbarriers");
+    static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
     static constexpr int KPT = 16;                  // keys per thread in the gathered selection
     static_assert(KPT * THREADS >= KEYS_MAX, "gathered keys fit in registers");
     static_assert(NSTAGE * 8 <= 32, "tile info slots");
@@ -164,10 +153,10 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     int *tinfo = misc + 768;              // [NSTAGE][8] valid tokens per page of a stage
     int *cnt = misc + 800;                // [2] this CTA's (> kth, == kth) counts
     int *wsum = misc + 808;               // [2][9] block-scan scratch
-    int *sh = misc + 832;                 // [0] bin, [1] remaining, [2] abort, [3] done, [4..5] key range, [6..7] this CTA's key range
+    int *sh = misc + 832;                 // [0] bin, [1] remaining, [2] abort, [3] done, [4..5] key range,
+                                          // [6..7] this CTA's key range, [8..9] CTA 0: the unit's key range
     uint64_t *full = reinterpret_cast<uint64_t *>(misc + C::MISC_BARRIER_WORD);
     uint64_t *empty = full + C::NSTAGE;
-    uint64_t *list_bar = empty + C::NSTAGE;  // CTA 0 -> every CTA: "your page list is ready"
     volatile int *abort_flag = &sh[2];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -179,19 +168,20 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     const int units = p.B * p.Hkv;
     const bool producer = (warp == C::NCW);
 
-    pdl_wait_and_release();
-    if (tid == 0) {
+    if (tid == 0) {  // nothing here reads what an earlier kernel writes
         sh[2] = 0;
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), C::NCW);
         }
-        mbar_init(smem_u32(list_bar), 1);
+        sh[8] = (int)0xffffffffu;  // key range of the gathered unit (min, max)
+        sh[9] = 0;
         fence_mbar_init();
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
         if (MODE == FUSED_FULL) prefetch_tensormap(&mmap);
     }
+    pdl_wait_and_release();
     __syncthreads();
     cluster_sync_all();  // every CTA of the cluster is running before any remote access
 
@@ -199,7 +189,6 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     WarpAttn<D, G> wa;
     wa.init(warp, lane, smem_u32(pbuf));
     int it = 0;  // position in the stage ring (same sequence in producer and consumers)
-    uint32_t lb = 0;  // completed phases of list_bar
 
     for (int u = cid; u < units; u += ncl) {
         const int b = u / p.Hkv, kv = u - (u / p.Hkv) * p.Hkv;
@@ -212,50 +201,59 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
 
         if (MODE == FUSED_FULL) {
             // ================= 1. append + page scores =================
-            // P <= KEYS_MAX: CTA 0 gathers every key, selects alone from registers
-            // and hands each CTA its share of the page list (one cluster barrier and
-            // one remote mbarrier arrival). Otherwise each CTA keeps its own keys and
-            // the radix passes sum histograms over the cluster.
+            // P <= KEYS_MAX: CTA 0 gathers every key (and their range), selects
+            // alone from registers and writes each CTA its share of the page list
+            // (two cluster barriers in all). Otherwise each CTA keeps its own keys
+            // and the radix passes sum histograms over the cluster.
             const bool gather = P <= C::KEYS_MAX;
             const int pr0 = (int)(((int64_t)crank * P) / nct);
             const int pr1 = (int)(((int64_t)(crank + 1) * P) / nct);
             const int ntile = (pr1 - pr0 + C::MT - 1) / C::MT;
             if (producer) {
+                // The appended token's page is written just before the metadata
+                // tile that holds it is loaded (usually the last tile of the last
+                // CTA), so the other tiles stream meanwhile.
+                int papp = -1;  // page of the appended token when this CTA writes it
                 if (p.pos != nullptr) {
                     const int pos = p.pos[b];
-                    const int papp = pos / p.S;
-                    const bool mine = (papp >= pr0 && papp < pr1) || (crank == nct - 1 && papp >= pr1);
                     if (pos < 0 || pos >= p.Lmax) {
                         if (lane == 0 && crank == 0) raise_flag(p.status, GQAQ_DEV_BAD_POS);
-                    } else if (mine) {
-                        constexpr int EPL = D / 32;
-                        const int64_t row = (int64_t)u * p.Lmax + pos;
-                        __half *mrow = p.meta + ((int64_t)u * p.Pmax + papp) * 2 * D;
-                        const bool fresh = (pos % p.S) == 0;
-#pragma unroll
-                        for (int e = 0; e < EPL; ++e) {
-                            const int c = lane * EPL + e;
-                            const __half kn = p.k_new[(int64_t)u * D + c];
-                            p.k_cache[row * D + c] = kn;
-                            p.v_cache[row * D + c] = p.v_new[(int64_t)u * D + c];
-                            __half mn = kn, mx = kn;
-                            if (!fresh) {
-                                const __half om = mrow[c], oM = mrow[D + c];
-                                const float kf = __half2float(kn);
-                                mn = (kf < __half2float(om)) ? kn : om;
-                                mx = (kf > __half2float(oM)) ? kn : oM;
-                            }
-                            mrow[c] = mn;
-                            mrow[D + c] = mx;
-                        }
-                        fence_proxy_async_global();  // the TMA reads below see these rows
+                    } else {
+                        const int pg = pos / p.S;
+                        if ((pg >= pr0 && pg < pr1) || (crank == nct - 1 && pg >= pr1)) papp = pg;
                     }
+                }
+                auto append = [&]() {
+                    constexpr int EPL = D / 32;
+                    const int pos = p.pos[b];
+                    const int64_t row = (int64_t)u * p.Lmax + pos;
+                    __half *mrow = p.meta + ((int64_t)u * p.Pmax + papp) * 2 * D;
+                    const bool fresh = (pos % p.S) == 0;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) {
+                        const int c = lane * EPL + e;
+                        const __half kn = p.k_new[(int64_t)u * D + c];
+                        p.k_cache[row * D + c] = kn;
+                        p.v_cache[row * D + c] = p.v_new[(int64_t)u * D + c];
+                        __half mn = kn, mx = kn;
+                        if (!fresh) {
+                            const __half om = mrow[c], oM = mrow[D + c];
+                            const float kf = __half2float(kn);
+                            mn = (kf < __half2float(om)) ? kn : om;
+                            mx = (kf > __half2float(oM)) ? kn : oM;
+                        }
+                        mrow[c] = mn;
+                        mrow[D + c] = mx;
+                    }
+                    fence_proxy_async_global();  // the TMA reads below see these rows
                     __syncwarp();
                     fence_proxy_async_global();
-                }
+                };
+                const int tapp = (papp >= pr0 && papp < pr1) ? (papp - pr0) / C::MT : -1;
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % C::NSTAGE;
                     const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
+                    if (t == tapp) append();
                     if (it >= C::NSTAGE) {
                         bool ok = (*abort_flag == 0);
                         if (ok && lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.timeout_ns, abort_flag);
@@ -275,6 +273,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                     __syncwarp();
                 }
+                if (papp >= 0 && tapp < 0) append();  // a page past the valid ones: no tile reads it here
             } else {
                 // consumer warps: lane = 8*quarter + page; 16 pages per warp per tile
                 const int jp = lane & 7, qq = lane >> 3;
@@ -302,6 +301,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                     named_bar_sync(1, C::NCW * 32);
                 }
+                uint32_t kmin_l = 0xffffffffu, kmax_l = 0u;  // range of the keys this thread stores
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % C::NSTAGE;
                     const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
@@ -360,15 +360,30 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         }
                         const int page = first + jp;
                         if (qq == 0 && page < pr1) {
-                            if (gather)  // CTA 0 receives every key of the unit
-                                st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), score_key(best));
-                            else
-                                keys[page - pr0] = score_key(best);
+                            const uint32_t key = score_key(best);
+                            if (gather) {  // CTA 0 receives every key of the unit
+                                st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), key);
+                                kmin_l = key < kmin_l ? key : kmin_l;
+                                kmax_l = key > kmax_l ? key : kmax_l;
+                            } else {
+                                keys[page - pr0] = key;
+                            }
                             if (p.scores != nullptr) p.scores[(int64_t)u * p.Pmax + page] = best;
                         }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+                }
+                if (gather) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        kmin_l = min(kmin_l, (uint32_t)__shfl_xor_sync(0xffffffffu, kmin_l, o));
+                        kmax_l = max(kmax_l, (uint32_t)__shfl_xor_sync(0xffffffffu, kmax_l, o));
+                    }
+                    if (lane == 0) {
+                        red_dsmem_min_u32(smem_u32(&sh[8]), 0, kmin_l);
+                        red_dsmem_max_u32(smem_u32(&sh[9]), 0, kmax_l);
+                    }
                 }
             }
             if (gather)
@@ -379,15 +394,19 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             if (gather) {
                 // ============ 2-3. CTA 0: exact top-K from register-held keys ============
                 // Thread t holds the contiguous run of keys [t*chunk, t*chunk + cnt).
-                // The K-th largest key is located by narrowing a key range [lo, hi]:
-                // each pass bins the keys inside it by (key - lo) >> shift into at most
-                // 256 bins and keeps the bin holding the K-th key; starting from the
-                // keys' own [min, max] spreads them over the bins, and the loop ends
-                // once that bin is wholly selected or holds one key value. Selected:
-                // keys above hi plus the first `need_eq` pages (lowest index) with
-                // lo <= key <= hi. Entry `pos` of the ascending page list goes to the
-                // CTA whose share [r*nsel/C, (r+1)*nsel/C) contains it.
+                // The K-th largest key is located by narrowing a key range [lo, hi],
+                // starting from the unit's key range that the scoring reduced into
+                // CTA 0: each pass bins the keys inside it by (key - lo) >> shift into
+                // at most 2048 bins (histogram in the idle stage ring) and keeps the
+                // bin holding the K-th key, until that bin is wholly selected or
+                // holds one key value (one pass, usually). Selected: keys above hi
+                // plus the first `need_eq` pages (lowest index) with lo <= key <= hi.
+                // Entry `pos` of the ascending page list goes to the CTA whose share
+                // [r*nsel/C, (r+1)*nsel/C) contains it.
                 if (crank == 0) {
+                    constexpr int NBIN = 2048;
+                    static_assert(NBIN * 4 <= C::STAGE, "the histogram fits in one ring stage");
+                    int *hb = reinterpret_cast<int *>(ring);
                     const int chunk = (P + C::THREADS - 1) / C::THREADS;
                     const int c0 = tid * chunk < P ? tid * chunk : P;
                     const int kc = c0 + chunk < P ? chunk : P - c0;
@@ -397,69 +416,52 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     uint32_t lo = 0, hi = 0xffffffffu;
                     int need_eq = P;
                     if (P > p.kpages) {
-                        uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-                        for (int e = 0; e < C::KPT; ++e)
-                            if (e < kc) {
-                                kmin = kr[e] < kmin ? kr[e] : kmin;
-                                kmax = kr[e] > kmax ? kr[e] : kmax;
-                            }
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            kmin = min(kmin, (uint32_t)__shfl_xor_sync(0xffffffffu, kmin, o));
-                            kmax = max(kmax, (uint32_t)__shfl_xor_sync(0xffffffffu, kmax, o));
-                        }
-                        if (lane == 0) { wsum[warp] = (int)kmin; wsum[9 + warp] = (int)kmax; }
-                        __syncthreads();
-                        if (tid == 0) {
-                            uint32_t a = 0xffffffffu, bmax = 0u;
-                            for (int w = 0; w < C::NCW + 1; ++w) {
-                                a = min(a, (uint32_t)wsum[w]);
-                                bmax = max(bmax, (uint32_t)wsum[9 + w]);
-                            }
-                            sh[4] = (int)a;
-                            sh[5] = (int)bmax;
-                        }
-                        __syncthreads();
-                        lo = (uint32_t)sh[4];
-                        hi = (uint32_t)sh[5];
+                        lo = (uint32_t)sh[8];
+                        hi = (uint32_t)sh[9];
                         int rem = p.kpages;
-                        for (int pass = 0; pass < 6 && lo < hi; ++pass) {
+                        for (int pass = 0; pass < 4 && lo < hi; ++pass) {
                             const uint32_t span = hi - lo;
                             const int bits = 32 - __clz(span);
-                            const int shift = bits > 8 ? bits - 8 : 0;
-                            int *hb = hist + (pass & 1) * 256;
-                            for (int i = tid; i < 256; i += C::THREADS) hb[i] = 0;
+                            const int shift = bits > 11 ? bits - 11 : 0;
+                            for (int i = tid; i < NBIN; i += C::THREADS) hb[i] = 0;
                             __syncthreads();
 #pragma unroll
                             for (int e = 0; e < C::KPT; ++e)
                                 if (e < kc && kr[e] >= lo && kr[e] <= hi) atomicAdd(&hb[(kr[e] - lo) >> shift], 1);
                             __syncthreads();
-                            if (warp == 0) {
-                                int c[8], sum = 0;
+                            // block scan from the top bin down: consumer thread t owns the
+                            // 8 bins 2047-8t .. 2040-8t
+                            int cc[8], sum = 0;
+                            if (tid < C::NCW * 32) {
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
-                                    c[e] = hb[255 - 8 * lane - e];
-                                    sum += c[e];
+                                    cc[e] = hb[NBIN - 1 - 8 * tid - e];
+                                    sum += cc[e];
                                 }
-                                int incl = sum;
+                            }
+                            int incl = sum;
 #pragma unroll
-                                for (int o = 1; o < 32; o <<= 1) {
-                                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                                    if (lane >= o) incl += y;
-                                }
-                                const int excl = incl - sum;
-                                if (excl < rem && rem <= incl) {
+                            for (int o = 1; o < 32; o <<= 1) {
+                                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                                if (lane >= o) incl += y;
+                            }
+                            if (lane == 31 && tid < C::NCW * 32) wsum[warp] = incl;
+                            __syncthreads();
+                            if (tid < C::NCW * 32) {
+                                int before = 0;
+                                for (int w = 0; w < warp; ++w) before += wsum[w];
+                                const int excl = before + incl - sum;
+                                if (excl < rem && rem <= excl + sum) {
                                     int cum = excl;
 #pragma unroll
                                     for (int e = 0; e < 8; ++e) {
-                                        if (cum + c[e] >= rem) {
-                                            sh[0] = 255 - 8 * lane - e;
+                                        if (cum + cc[e] >= rem) {
+                                            sh[0] = NBIN - 1 - 8 * tid - e;
                                             sh[1] = rem - cum;
-                                            sh[3] = (c[e] == rem - cum) ? 1 : 0;
+                                            sh[3] = (cc[e] == rem - cum) ? 1 : 0;
                                             break;
                                         }
-                                        cum += c[e];
+                                        cum += cc[e];
                                     }
                                 }
                             }
@@ -470,9 +472,15 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                             hi = lo + (top < span ? top : span);
                             lo = nlo;
                             rem = sh[1];
-                            if (sh[3] != 0) break;  // the next pass writes other slots first
+                            const bool done = sh[3] != 0;
+                            __syncthreads();  // sh and the histogram are rewritten next
+                            if (done) break;
                         }
                         need_eq = rem;
+                    }
+                    if (tid == 0) {  // reset the key range for the next unit
+                        sh[8] = (int)0xffffffffu;
+                        sh[9] = 0;
                     }
                     // ---- compaction: positions from a block scan of (above, in range) ----
                     int ngt = 0, neq = 0;
@@ -515,18 +523,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                     if (prow != nullptr)
                         for (int i = nsel + tid; i < p.kpages; i += C::THREADS) prow[i] = -1;
-                    __syncthreads();  // every list entry of this unit is stored
-                    if (tid == 0) {
-                        asm volatile("fence.acq_rel.cluster;" ::: "memory");
-                        for (uint32_t r = 0; r < nct; ++r) mbar_arrive_remote(smem_u32(list_bar), r);
-                    }
+                    fence_proxy_async_smem();  // the histogram's stage is TMA-written again later
                 }
-                // every CTA: wait for its share of the list
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_cluster(smem_u32(list_bar), lb & 1u, p.timeout_ns);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok && lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
-                ++lb;
+                cluster_sync_all();  // every CTA's share of the page list is in its shared memory
             } else {
                 // ================= 2. top-K threshold (adaptive range radix) =================
                 // The K-th largest key is located by narrowing a key range [lo, hi]:

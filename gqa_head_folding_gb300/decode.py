@@ -9,11 +9,9 @@ carries a new token, every layer first appends it (``quest_append_kv``), so
 each layer's page metadata stays current whatever path reads it.
 
 By default a Quest layer is one fused launch (``quest_decode_attn``: append,
-score, top-K and sparse attention in one kernel). With ``quest_kernel=
-"cluster"`` (default) that kernel runs one thread-block cluster per
-(sequence, KV head) and needs no workspace; ``"queue"`` runs the GPU-wide
-work queue on the stack's workspace. With ``fused=False`` the same layer runs as the four
-step-by-step calls.
+score, top-K and sparse attention in one kernel); the library picks its
+kernel (GQAQ_OPT_QUEST_KERNEL), and the stack's workspace covers both. With
+``fused=False`` the same layer runs as the four step-by-step calls.
 
 This module only sequences library calls and owns the scratch buffers they
 share. Every arithmetic step runs in the CUDA kernels.
@@ -47,12 +45,8 @@ class Layer:
 
 class DecodeStack:
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_len: int,
-                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True,
-                 quest_kernel: str = "cluster"):
-        if quest_kernel not in ("queue", "cluster"):
-            raise ValueError(f"quest_kernel must be 'queue' or 'cluster', not {quest_kernel!r}")
+                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True):
         self.fused = fused
-        self.quest_kernel = quest_kernel
         self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
         self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
         self.k_pages, self.dense_layers = k_pages, dense_layers
@@ -60,7 +54,6 @@ class DecodeStack:
         self.device = torch.device(device)
         dims = make_dims(batch, num_q_heads, num_kv_heads, head_dim, max_len, page_size)
         self.workspace = alloc_workspace(dims, self.device, k_pages or 0)
-        self.quest_workspace = self.workspace if quest_kernel == "queue" else None
         pmax = num_pages(max_len, page_size)
         self.scores = torch.empty(batch, num_kv_heads, pmax, dtype=torch.float32, device=self.device)
         self.page_idx = (torch.empty(batch, num_kv_heads, k_pages, dtype=torch.int32, device=self.device)
@@ -96,7 +89,7 @@ class DecodeStack:
                 add("quest", lambda L=L: quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len,
                                                            self.k_pages, self.scale, k_new=L.k_new, v_new=L.v_new,
                                                            pos=L.pos, out=L.out, page_size=self.page_size,
-                                                           workspace=self.quest_workspace))
+                                                           workspace=self.workspace))
             else:
                 add("score", lambda L=L: quest_score_pages(L.q, L.meta, L.valid_len, self.max_len,
                                                            scores=self.scores, page_size=self.page_size))
@@ -126,7 +119,7 @@ class DecodeStack:
             elif self.fused:
                 quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages, self.scale,
                                   k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out, page_size=self.page_size,
-                                  workspace=self.quest_workspace)
+                                  workspace=self.workspace)
             else:
                 quest_score_pages(L.q, L.meta, L.valid_len, self.max_len, scores=self.scores,
                                   page_size=self.page_size)

@@ -179,16 +179,18 @@ GQAQ_API int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const 
  * scores ([B][Hkv][Pmax] fp32) and page_idx ([B][Hkv][k] int32, ascending,
  * -1 padded) are optional outputs (NULL to skip). S = 16, 1 <= k <= 65536.
  * With a workspace (>= gqaq_workspace_bytes(dims, k) bytes, zero-filled
- * before its first use, see gqaq_workspace_bytes) the step runs as one work
- * queue over the whole GPU: page-scoring and attention pieces of every
+ * before its first use, see gqaq_workspace_bytes) the step can run as one
+ * work queue over the whole GPU: page-scoring and attention pieces of every
  * (sequence, KV head) are taken from a ticket counter; the last scorer of a
  * (sequence, KV head) selects its pages, the last attention piece merges its
- * softmax states. That covers Pmax <= 8192 pages. Otherwise, and with
- * workspace NULL, one thread-block cluster handles one (sequence, KV head)
- * at a time and needs no workspace; it requires k <= 1024
- * (GQAQ_ERR_UNSUPPORTED above). Two calls that overlap on the GPU must not
- * share a workspace. After a call whose waits timed out (GQAQ_DEV_TIMEOUT),
- * zero the workspace again before reusing it. */
+ * softmax states. That covers Pmax <= 8192 pages. The other kernel hands one
+ * (sequence, KV head) at a time to one thread-block cluster, whose CTAs meet
+ * in distributed shared memory; it needs no workspace and requires k <= 1024.
+ * By default (GQAQ_OPT_QUEST_KERNEL) the cluster kernel runs whenever
+ * k <= 1024, and the work queue above that (GQAQ_ERR_WORKSPACE without a
+ * workspace). Two calls that overlap on the GPU must not share a workspace.
+ * After a call whose waits timed out (GQAQ_DEV_TIMEOUT), zero the workspace
+ * again before reusing it. */
 GQAQ_API int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_cache,
                                gqaq_half *v_cache, gqaq_half *meta, const gqaq_half *k_new,
                                const gqaq_half *v_new, const int32_t *pos, const int32_t *valid_len,
@@ -230,9 +232,13 @@ enum {
                                      (exercises the timeout path; outputs undefined) */
     GQAQ_OPT_CLUSTER_SIZE = 4,    /* CTAs per cluster of the fused Quest kernel (1, 2,
                                      4 or 8); 0 = chosen from the SM count and shape */
-    GQAQ_OPT_PDL = 5              /* nonzero (default): launch with programmatic stream
+    GQAQ_OPT_PDL = 5,             /* nonzero (default): launch with programmatic stream
                                      serialization, so a kernel's launch overlaps the
                                      end of the previous one in the stream */
+    GQAQ_OPT_QUEST_KERNEL = 6     /* quest_decode_attn's kernel: 0 (default) = the
+                                     cluster kernel when k <= 1024, else the work-queue
+                                     kernel; 1 = cluster kernel; 2 = work-queue kernel
+                                     (needs the workspace) */
 };
 GQAQ_API int gqaq_set_option(int option, int64_t value);
 

@@ -100,12 +100,32 @@ def test_quest_calls_reject_bad_arguments(L):
                                None) == g.GQAQ_ERR_WORKSPACE
 
 
+def test_fused_quest_step_rejects_bad_arguments(L):
+    d = g.make_dims(1, 8, 2, 128, 4096)
+    args = [ctypes.byref(d)] + [FAKE] * 8
+    tail = [0.1, FAKE, None, None]
+    assert L.quest_decode_attn(*args, 0, *tail, None, 0, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.quest_decode_attn(*args, 70000, *tail, None, 0, None) == g.GQAQ_ERR_INVALID_ARG
+    odd = ctypes.c_void_p(FAKE.value + 4)
+    assert L.quest_decode_attn(*args, 8, *tail, odd, 1 << 20, None) == g.GQAQ_ERR_WORKSPACE
+
+
 def test_options(L):
     assert L.gqaq_set_option(g.GQAQ_OPT_MAX_CTAS, -1) == g.GQAQ_ERR_INVALID_ARG
     assert L.gqaq_set_option(12345, 0) == g.GQAQ_ERR_INVALID_ARG
     assert L.gqaq_set_option(g.GQAQ_OPT_MAX_CTAS, 0) == g.GQAQ_OK
     assert L.gqaq_set_option(g.GQAQ_OPT_WAIT_TIMEOUT_NS, 2_000_000_000) == g.GQAQ_OK
     assert L.gqaq_set_option(g.GQAQ_OPT_TEST_STALL, 0) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_CLUSTER_SIZE, 3) == g.GQAQ_ERR_INVALID_ARG
+    for v in (0, 1, 2, 4, 8):
+        assert L.gqaq_set_option(g.GQAQ_OPT_CLUSTER_SIZE, v) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_CLUSTER_SIZE, 0) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_PDL, 0) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_PDL, 1) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_KERNEL, 3) == g.GQAQ_ERR_INVALID_ARG
+    assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_KERNEL, -1) == g.GQAQ_ERR_INVALID_ARG
+    for v in (2, 1, 0):
+        assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_KERNEL, v) == g.GQAQ_OK
 
 
 def test_binding_refuses_cpu_tensors():

@@ -1,6 +1,6 @@
 """Parity at the workloads' full sizes, in the launch configuration the bench
-times (default grid, fused Quest layers on the work-queue kernel; the
-cluster kernel once, at the Llama-2 shape).
+times (default grid and kernel choice, fused Quest layers with the decode
+stack's workspace; the work-queue kernel once, at the Llama-2 shape).
 
 The GPU runs every (sequence, KV head) unit; the fp64 oracle checks sampled
 units one by one: page metadata bit-exact, the selected page set against the
@@ -36,7 +36,7 @@ def sample_units(B, Hkv, n, seed=0):
     return [units[i] for i in sorted(pick)]
 
 
-def check_quest_layer(w, seed_layer=2, n_units=3, kernel="queue"):
+def check_quest_layer(w, seed_layer=2, n_units=3, kernel="auto"):
     x = workloads.make_layer(w, seed_layer, device=DEV)
     B, Hkv, Lmax, D = x["k_cache"].shape
     G, S, K = w.group, w.page_size, w.k_pages
@@ -44,13 +44,16 @@ def check_quest_layer(w, seed_layer=2, n_units=3, kernel="queue"):
     g.quest_update_meta(x["k_cache"], x["valid_len"] - 1, meta)
     idx = torch.empty(B, Hkv, K, dtype=torch.int32, device=DEV)
     scale = 1.0 / math.sqrt(D)
-    ws = g.alloc_workspace(g.dims_of(x["q"], x["k_cache"]), DEV, K) if kernel == "queue" else None
-    out = g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], K, scale,
-                              k_new=x["k_new"], v_new=x["v_new"], pos=x["pos"], page_idx=idx, workspace=ws)
+    ws = g.alloc_workspace(g.dims_of(x["q"], x["k_cache"]), DEV, K)
+    g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 2 if kernel == "queue" else 0)
+    try:
+        out = g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], K, scale,
+                                  k_new=x["k_new"], v_new=x["v_new"], pos=x["pos"], page_idx=idx, workspace=ws)
+    finally:
+        g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 0)
     torch.cuda.synchronize()
     assert g.device_status() == 0
-    if ws is not None:
-        assert int(ws[:g.workspace_zero_bytes(g.dims_of(x["q"], x["k_cache"]))].count_nonzero()) == 0
+    assert int(ws[:g.workspace_zero_bytes(g.dims_of(x["q"], x["k_cache"]))].count_nonzero()) == 0
     vl = x["valid_len"].cpu().numpy()
     for (b, kv) in sample_units(B, Hkv, n_units, seed=D + K):
         q, k, v = unit_arrays(x, b, kv, G)          # caches already hold the appended token
@@ -86,7 +89,7 @@ def test_llama2_7b_quest_stack_layers():
     w = workloads.WORKLOADS[3]
     check_dense_layer(w, layer=0)
     check_quest_layer(w, seed_layer=2)
-    check_quest_layer(w, seed_layer=3, n_units=2, kernel="cluster")
+    check_quest_layer(w, seed_layer=3, n_units=2, kernel="queue")
 
 
 def test_exaone_dense_batch_32():

@@ -33,6 +33,11 @@ def _reset_options():
     yield
     g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, 0)
     g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
+    g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 0)
+
+
+def use_queue_kernel():
+    g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 2)
 
 
 def zero_region_clear(ws, B, Hkv):
@@ -47,6 +52,7 @@ def run_fused(D, G, K, csize, B=3, Hkv=2, Lmax=16 * 45 + 3, valid=(16 * 45 + 3, 
     g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, csize)
     ws = None
     if queue_ctas is not None:
+        use_queue_kernel()
         g.set_option(g.GQAQ_OPT_MAX_CTAS, queue_ctas)
         ws = g.alloc_workspace(g.make_dims(B, G * Hkv, Hkv, D, Lmax), DEV, K)
     w = workloads.Workload(0, "fused", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
@@ -128,12 +134,38 @@ def test_queue_kernel_more_than_1024_pages():
     run_fused(64, 4, 1100, 0, B=1, Hkv=2, Lmax=16 * 1500, valid=(16 * 1500 - 3,), seed=5, queue_ctas=0)
 
 
+def test_default_kernel_choice_by_k():
+    # automatic choice: k <= 1024 needs no workspace (cluster kernel); k > 1024
+    # takes the work queue and so a workspace
+    B, Hkv, D, G, Lmax = 1, 2, 64, 4, 16 * 1300
+    w = workloads.Workload(0, "big-k", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax)
+    x = workloads.make_layer(w, 0, device=DEV, seed=8)
+    meta = g.new_meta(B, Hkv, Lmax, D, DEV)
+    g.quest_update_meta(x["k_cache"], x["valid_len"], meta)
+    args = (x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"])
+    g.quest_decode_attn(*args, 1024, 0.1)
+    with pytest.raises(g.GqaqError):
+        g.quest_decode_attn(*args, 1025, 0.1)
+    ws = g.alloc_workspace(g.dims_of(x["q"], x["k_cache"]), DEV, 1025)
+    idx = torch.empty(B, Hkv, 1025, dtype=torch.int32, device=DEV)
+    out = g.quest_decode_attn(*args, 1025, 0.1, page_idx=idx, workspace=ws)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    vl = x["valid_len"].cpu().numpy()
+    q, kc, vc = x["q"].cpu().numpy(), x["k_cache"].cpu().numpy(), x["v_cache"].cpu().numpy()
+    sel = idx.cpu().numpy()
+    check_topk(sel, oracle.page_scores(q, oracle.page_minmax(kc, vl, S), vl, S), vl, S, 1025)
+    assert_attn_close(out, oracle.sparse_attn(q, kc, vc, vl, sel, S, 0.1))
+
+
 def test_queue_kernel_empty_sequence_gives_zeros():
     B, Hkv, D, G, Lmax, K = 3, 2, 128, 4, 16 * 40, 6
     w = workloads.Workload(0, "fused", batch=B, num_layers=1, num_q_heads=G * Hkv, num_kv_heads=Hkv,
                            head_dim=D, max_len=Lmax)
     x = workloads.make_layer(w, 0, device=DEV, seed=12)
     vl = torch.tensor([16 * 40, 0, 77], dtype=torch.int32, device=DEV)
+    use_queue_kernel()
     meta = g.new_meta(B, Hkv, Lmax, D, DEV)
     g.quest_update_meta(x["k_cache"], vl, meta)
     ws = g.alloc_workspace(g.make_dims(B, G * Hkv, Hkv, D, Lmax), DEV, K)
@@ -163,6 +195,7 @@ def test_queue_kernel_repeatable_and_graph_capturable():
     out = torch.empty_like(x["q"])
     idx = torch.empty(B, Hkv, 64, dtype=torch.int32, device=DEV)
     ws = g.alloc_workspace(g.dims_of(x["q"], x["k_cache"]), DEV, 64)
+    use_queue_kernel()
 
     def step():
         g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], 64, 0.088,
@@ -187,6 +220,7 @@ def test_queue_kernel_repeatable_and_graph_capturable():
         assert torch.equal(out, first_out) and torch.equal(idx, first_idx)
     assert zero_region_clear(ws, B, Hkv)
     # the cluster kernel (no workspace) selects the same pages
+    g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 0)
     idx2 = torch.empty_like(idx)
     g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], 64, 0.088, page_idx=idx2)
     assert torch.equal(idx2, first_idx)
@@ -202,6 +236,7 @@ def test_queue_kernel_timeout_is_reported_and_context_survives():
     g.quest_update_meta(x["k_cache"], x["valid_len"], meta)
     ws = g.alloc_workspace(g.make_dims(B, G * Hkv, Hkv, D, Lmax), DEV, K)
     args = (x["q"], x["k_cache"], x["v_cache"], meta, x["valid_len"], K, 0.1)
+    use_queue_kernel()
     g.device_status(reset=True)
     try:
         g.set_option(g.GQAQ_OPT_WAIT_TIMEOUT_NS, 1_000_000)
