@@ -120,6 +120,18 @@ bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_kpage(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    if (cols % 64 != 0 || !encode_tensor_map_2d(map, base, rows, cols, 64, box_rows, true)) return false;  // loads g_encode
+    const cuuint64_t dims[3] = {64, cols / 64, rows};
+    const cuuint64_t strides[2] = {128, cols * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(cols / 64), box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace gqaq
 
 using namespace gqaq;

@@ -353,9 +353,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
                         const int pj = __shfl_sync(0xffffffffu, page, j);
                         if (lane == 0 && ((m >> j) & 1u)) {
                             const int y = row0 + pj * p.S;
-#pragma unroll
-                            for (int kh = 0; kh < C::KH; ++kh)
-                                tma_load_2d(kdst + kh * C::KBLK + j * C::SUB * 128, &kmap, 64 * kh, y, fb, pol);
+                            tma_load_3d(kdst + j * C::SUB * D * 2, &kmap, 0, 0, y, fb, pol);  // page-major K
                             tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
                         }
                     }
@@ -392,7 +390,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     // the arrival counters in step, so the workspace stays reusable.
     // ----------------------------------------------------------------------
     const int tid = threadIdx.x;  // 0..255 among consumers
-    WarpAttn<D, G> wa;
+    WarpAttn<D, G, SPARSE> wa;  // sparse stages hold K page-major
     wa.init(warp, lane, smem_u32(pbuf));
 
     Walk w;
@@ -555,7 +553,9 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
     const uint32_t box_rows = SPARSE ? (uint32_t)C::SUB : (uint32_t)C::TILE;
     CUtensorMap kmap, vmap;
-    if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true)) return GQAQ_ERR_CUDA;
+    if (SPARSE ? !encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, box_rows)
+               : !encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true))
+        return GQAQ_ERR_CUDA;
     if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, box_rows, false)) return GQAQ_ERR_CUDA;
 
     AttnParams p;

@@ -56,7 +56,11 @@ struct TileCfg {
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
 };
 
-template <int D, int G>
+// K layout in a stage: KPAGE = false: KH column blocks of TILE rows x 128 B
+// ([kh][row]); KPAGE = true: row after row, each row's KH 128-byte blocks
+// side by side ([row][kh]), as one 3-D TMA box per page writes them. Both
+// are 128-byte swizzled: 16-byte chunk c of 128-byte line L sits at c ^ (L & 7).
+template <int D, int G, bool KPAGE = false>
 struct WarpAttn {
     using C = TileCfg<D, G>;
     int lane, part, jt, cw;
@@ -71,8 +75,14 @@ struct WarpAttn {
         part = lane >> 3;
         jt = lane & 7;
         const int c0 = part * C::DQ;
-        krow_off = (uint32_t)((c0 / 64) * C::KBLK + (cw * C::SUB + jt) * 128);
-        kx0 = (uint32_t)(((c0 % 64) / 8) ^ jt);  // rows jt and jt+8 share (row & 7)
+        if (KPAGE) {
+            const int line = (cw * C::SUB + jt) * C::KH + c0 / 64;
+            krow_off = (uint32_t)(line * 128);
+            kx0 = (uint32_t)(((c0 % 64) / 8) ^ (line & 7));  // rows jt and jt+8: same (line & 7)
+        } else {
+            krow_off = (uint32_t)((c0 / 64) * C::KBLK + (cw * C::SUB + jt) * 128);
+            kx0 = (uint32_t)(((c0 % 64) / 8) ^ jt);  // rows jt and jt+8 share (row & 7)
+        }
         pbw = pbuf_base + (uint32_t)(cw * C::SUB * G * 4);
     }
     // Row of the query group whose softmax this lane owns (i < HPL).
@@ -153,7 +163,7 @@ struct WarpAttn {
                 float a0[C::GQ], a1[C::GQ];
 #pragma unroll
                 for (int g = 0; g < C::GQ; ++g) a0[g] = a1[g] = 0.f;
-                const uint32_t kro = kbase + krow_off + (uint32_t)(u * C::TPP * 128);
+                const uint32_t kro = kbase + krow_off + (uint32_t)(u * C::TPP * (KPAGE ? C::KH : 1) * 128);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
                     const uint4 kc = lds128(kro + ((kx0 ^ (uint32_t)c) << 4));

@@ -17,6 +17,10 @@ namespace gqaq {
 // box_cols x box_rows, 128-byte swizzle or none. Returns false on failure.
 bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                           uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+// K rows as a 3-D map [rows][cols/64][64], box [box_rows][cols/64][64] with
+// 128-byte swizzle: one TMA load brings box_rows whole rows (all their
+// 128-byte column blocks, interleaved row by row). cols: a multiple of 64.
+bool encode_tensor_map_kpage(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 // Dense (page_idx == nullptr) or sparse split-context attention, one launch:
 // split units are merged in-kernel by the CTA that finishes them last.

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     cluster_sync_all();  // every CTA of the cluster is running before any remote access
 
     const uint64_t pol = l2_policy_evict_first();
-    WarpAttn<D, G> wa;
+    WarpAttn<D, G, true> wa;  // K stages in page-major layout
     wa.init(warp, lane, smem_u32(pbuf));
     int it = 0;  // position in the stage ring (same sequence in producer and consumers)
 
@@ -756,9 +756,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     const int pj = __shfl_sync(0xffffffffu, page, j);
                     if (lane == 0 && ((m >> j) & 1u)) {
                         const int y = u * p.Lmax + pj * p.S;
-#pragma unroll
-                        for (int kh = 0; kh < C::KH; ++kh)
-                            tma_load_2d(kdst + kh * C::KBLK + j * C::SUB * 128, &kmap, 64 * kh, y, fb, pol);
+                        tma_load_3d(kdst + j * C::SUB * D * 2, &kmap, 0, 0, y, fb, pol);  // page-major K
                         tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
                     }
                 }
@@ -914,7 +912,7 @@ int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
     } else {
         memset(&mmap, 0, sizeof(mmap));
     }
-    if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, C::SUB, true)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, C::SUB)) return GQAQ_ERR_CUDA;
     if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, C::SUB, false)) return GQAQ_ERR_CUDA;
 
     FusedParams p;

@@ -490,9 +490,7 @@ __global__ void __launch_bounds__(StreamCfg<D, G>::THREADS, StreamCfg<D, G>::MIN
                             const int pj = __shfl_sync(0xffffffffu, page, j);
                             if (lane == 0 && ((m >> j) & 1u)) {
                                 const int y = u * p.Lmax + pj * p.S;
-#pragma unroll
-                                for (int kh = 0; kh < C::KH; ++kh)
-                                    tma_load_2d(kdst + kh * C::KBLK + j * C::SUB * 128, &kmap, 64 * kh, y, fb, pol);
+                                tma_load_3d(kdst + j * C::SUB * D * 2, &kmap, 0, 0, y, fb, pol);  // page-major K
                                 tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
                             }
                         }
@@ -611,7 +609,7 @@ __global__ void __launch_bounds__(StreamCfg<D, G>::THREADS, StreamCfg<D, G>::MIN
             named_bar_sync(1, NCT);  // every key of the item is stored; qt_s may change
             if (tid == 0) st_release_cta_smem(done_ctr, ++ndone);
         } else if (kind == ST_ATTEND) {
-            WarpAttn<D, G> wa;
+            WarpAttn<D, G, true> wa;  // K stages in page-major layout
             wa.init(warp, lane, smem_u32(pbuf));
             if (C::QREG) {
                 wa.load_q(qg);
@@ -898,7 +896,7 @@ int stream_t(const FusedArgs &a, const LaunchCtx &ctx, size_t *need_out) {
     const uint64_t mrows = (uint64_t)U * Pmax;
     CUtensorMap mmap, kmap, vmap;
     if (!encode_tensor_map_2d(&mmap, a.meta, mrows, 2 * D, 64, C::MT, true)) return GQAQ_ERR_CUDA;
-    if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, C::SUB, true)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, C::SUB)) return GQAQ_ERR_CUDA;
     if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, C::SUB, false)) return GQAQ_ERR_CUDA;
 
     uint8_t *ws = reinterpret_cast<uint8_t *>(a.workspace);
