@@ -46,6 +46,8 @@ struct AttnCfg : TileCfg<D, G> {
     static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
 };
 
+constexpr int kMinTilesPerCta = 4;
+
 struct AttnParams {
     const __half *q;
     const int *valid_len;
@@ -132,16 +134,16 @@ struct Walk {
 };
 
 // Log-sum-exp merge of the n_parts partials of one split unit, run by the 256
-// consumer threads of the CTA that arrived last:
+// consumer threads of the CTA that arrived last (up to FEW parts: one round
+// trip to L2 per thread; more: weights first, then the weighted sums):
 //   out_g = sum_c 2^(m_c - m*) acc_c / sum_c 2^(m_c - m*) l_c,  m* = max_c m_c.
 // The partials of CTAs c_lo .. c_lo + n_parts - 1 sit in slot 0, except the
 // first CTA's, whose slot is slot_lo. Other CTAs wrote them, so they are read
 // from L2 (ld.global.cg), never from a possibly stale L1 line.
-template <int D, int G>
+template <int D, int G, int FEW>
 __device__ __forceinline__ void merge_parts(const float *part, float *wbuf, int64_t c_lo, int n_parts,
                                             int slot_lo, __half *outg, int warp, int lane, int tid, int nthreads) {
     constexpr int W = G * (D + 2);
-    constexpr int FEW = 8;
     if (n_parts <= FEW) {
         // Few parts: every thread loads (m, l, acc) of its elements from all
         // parts at once and merges them itself (one round trip to L2).
@@ -259,12 +261,15 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     rule.pages_per_tile = C::NCW;
 
     if (warp == C::NCW) {
-        // Balanced split of the T tiles over min(gridDim.x, T) CTAs, so that
-        // every working CTA owns at least one tile.
+        // Balanced split of the T tiles over min(gridDim.x, ceil(T / 4)) CTAs:
+        // every working CTA owns at least one tile, and a small problem keeps
+        // about four per CTA (a short pipeline and few parts per split unit
+        // are cheaper than one tile per CTA).
         int64_t T, off_b;
         int b;
         locate_tile(p.valid_len, p.B, p.Hkv, rule, 0, T, b, off_b);
-        const int gp = (T < (int64_t)gridDim.x) ? (int)T : (int)gridDim.x;
+        const int64_t want = (T + kMinTilesPerCta - 1) / kMinTilesPerCta;
+        const int gp = (want < (int64_t)gridDim.x) ? (int)(want > 0 ? want : 1) : (int)gridDim.x;
         int64_t tb = 0, te = 0;
         if ((int)blockIdx.x < gp) {
             tb = tile_begin(blockIdx.x, T, gp);
@@ -503,7 +508,9 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
         const int64_t c_lo = tile_owner(sp.off, T, gp);
         const int n_parts = (int)(tile_owner(sp.off + sp.tiles_b - 1, T, gp) - c_lo) + 1;
         const int slot_lo = (tile_begin(c_lo, T, gp) == sp.off) ? 0 : 1;
-        merge_parts<D, G>(p.part, merge, c_lo, n_parts, slot_lo, sp.out, warp, lane, tid, NCT);
+        // up to FEW parts in one round trip (fewer where two CTAs share an SM's registers)
+        merge_parts<D, G, (C::MIN_BLOCKS == 2 ? 8 : 16)>(p.part, merge, c_lo, n_parts, slot_lo, sp.out, warp, lane,
+                                                          tid, NCT);
         named_bar_sync(1, NCT);
     }
 }
@@ -544,8 +551,18 @@ template <int D, int G, bool SPARSE>
 int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     using C = AttnCfg<D, G>;
     const gqaq_dims &dm = *a.dims;
-    const int grid = grid_for<D, G, SPARSE>(ctx);
+    int grid = grid_for<D, G, SPARSE>(ctx);
     if (grid < 1) return GQAQ_ERR_CUDA;
+    {
+        // Launch no more CTAs than the shape's largest tile count can keep at
+        // kMinTilesPerCta tiles each (the kernel applies the same rule to the
+        // actual count).
+        const int64_t tiles_unit = SPARSE ? ((int64_t)a.kpages + C::NCW - 1) / C::NCW
+                                          : ((int64_t)dm.max_len + C::TILE - 1) / C::TILE;
+        const int64_t tmax = (int64_t)dm.batch * dm.num_kv_heads * tiles_unit;
+        const int64_t want = (tmax + kMinTilesPerCta - 1) / kMinTilesPerCta;
+        if (want < grid) grid = (int)(want > 0 ? want : 1);
+    }
     const size_t cbytes = count_bytes(dm);
     const size_t need = cbytes + (size_t)grid * 2 * G * (D + 2) * sizeof(float);
     if (a.workspace == nullptr || a.workspace_bytes < need) return GQAQ_ERR_WORKSPACE;
