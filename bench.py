@@ -355,6 +355,12 @@ def workload_from_args(args) -> workloads.Workload:
         w = w.with_(k_pages=args.k_pages)
     if args.layers:
         w = w.with_(num_layers=args.layers)
+    if args.page_size:
+        w = w.with_(page_size=args.page_size)
+    if args.budget:
+        if w.k_pages is None:
+            raise SystemExit("--budget applies to Quest workloads")
+        w = w.with_(k_pages=max(1, args.budget // w.page_size))
     return w
 
 
@@ -535,6 +541,10 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--k-pages", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--page-size", type=int, default=0, choices=(0, 8, 16, 32, 64),
+                    help="Quest page size S (tokens); 0 = the workload's (16)")
+    ap.add_argument("--budget", type=int, default=0,
+                    help="Quest token budget; sets k_pages = budget / S (page-size sweep at a fixed budget)")
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed replays before timing")
     ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

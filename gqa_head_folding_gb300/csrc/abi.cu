@@ -90,7 +90,8 @@ int check_dims(const gqaq_dims *d, bool quest) {
     const int G = d->num_q_heads / d->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return GQAQ_ERR_UNSUPPORTED;
     if (d->head_dim != 64 && d->head_dim != 128) return GQAQ_ERR_UNSUPPORTED;
-    if (quest && d->page_size != 16) return GQAQ_ERR_UNSUPPORTED;
+    if (quest && d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
+        return GQAQ_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)d->batch * d->num_kv_heads * d->max_len;
     if (rows > (int64_t)INT32_MAX - 1024) return GQAQ_ERR_UNSUPPORTED;
     return GQAQ_OK;
@@ -204,7 +205,7 @@ size_t gqaq_workspace_bytes(const gqaq_dims *dims, int max_selected_pages) {
     if (make_ctx(&ctx, nullptr) != GQAQ_OK) return 0;
     size_t need = attention_workspace_bytes(dims, ctx);
     if (need == 0) return 0;
-    if (max_selected_pages > 0 && dims->page_size == 16) {
+    if (max_selected_pages > 0 && check_dims(dims, true) == GQAQ_OK) {
         const size_t qs = quest_stream_workspace_bytes(dims, max_selected_pages, ctx);
         if (qs > need) need = qs;
     }

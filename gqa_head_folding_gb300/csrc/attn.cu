@@ -13,8 +13,8 @@
 // the tile rows taken from a page list instead of a contiguous range.
 //
 // Kernel shape (one persistent CTA per resident slot, one launch per call):
-//  - work tiles: 128 consecutive tokens (dense) or 8 selected pages of 16
-//    tokens (sparse) of one (sequence, KV head) unit. The tiles of all units
+//  - work tiles: 128 consecutive tokens (dense) or 128 / max(S, 16) selected
+//    pages of S tokens (sparse) of one (sequence, KV head) unit. The tiles of all units
 //    are split into equal contiguous ranges, one per CTA (balanced split).
 //  - warp 8 (producer): TMA 2-D tile loads of K (128-byte swizzled) and V
 //    into a 2-3 stage shared-memory ring, with mbarrier completion.
@@ -258,7 +258,9 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     rule.page_size = p.S;
     rule.kpages = p.kpages;
     rule.tile_tokens = C::TILE;
-    rule.pages_per_tile = C::NCW;
+    PageSlots slots;
+    slots.init(p.S);
+    rule.pages_per_tile = slots.ppt;
 
     if (warp == C::NCW) {
         // Balanced split of the T tiles over min(gridDim.x, ceil(T / 4)) CTAs:
@@ -345,21 +347,22 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
                 const uint32_t fb = smem_u32(&full[s]);
                 const int local = w.local + t;
                 if (SPARSE) {
-                    const int e = local * C::NCW + lane;
+                    const int e = local * slots.ppt + lane;
+                    const bool mine = lane < slots.ppt && e < nsel;
                     int page = -1;
-                    if (lane < C::NCW && e < nsel) page = p.page_idx[(int64_t)unit * p.kpages + e];
-                    const bool ok = lane < C::NCW && e < nsel && page >= 0 && page < P;
-                    if (lane < C::NCW && e < nsel && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
+                    if (mine) page = p.page_idx[(int64_t)unit * p.kpages + e];
+                    const bool ok = mine && page >= 0 && page < P;
+                    if (mine && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
                     const unsigned m = __ballot_sync(0xffffffffu, ok);
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(C::SUB * D * 2 * 2));
+                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(p.S * D * 2 * 2));
 #pragma unroll
-                    for (int j = 0; j < C::NCW; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const int pj = __shfl_sync(0xffffffffu, page, j);
                         if (lane == 0 && ((m >> j) & 1u)) {
                             const int y = row0 + pj * p.S;
-                            tma_load_3d(kdst + j * C::SUB * D * 2, &kmap, 0, 0, y, fb, pol);  // page-major K
-                            tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
+                            const uint32_t off = (uint32_t)(j * slots.slot * D * 2);
+                            tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K
+                            tma_load_2d(vdst + off, &vmap, 0, y, fb, pol);
                         }
                     }
                 } else {
@@ -434,13 +437,10 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
             const int local = w.local + t;
             int nvalid = 0;
             if (SPARSE) {
-                const int e = local * C::NCW + warp;
+                const int e = local * slots.ppt + slots.warp_page(warp);
                 if (e < nsel) {
                     const int page = p.page_idx[(int64_t)unit * p.kpages + e];
-                    if (page >= 0 && page < P) {
-                        const int rem = len - page * p.S;
-                        nvalid = rem < C::SUB ? rem : C::SUB;
-                    }
+                    if (page >= 0 && page < P) nvalid = slots.warp_rows(warp, page, len);
                 }
             } else {
                 const int rem = len - (local * C::TILE + warp * C::SUB);
@@ -557,7 +557,8 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
         // Launch no more CTAs than the shape's largest tile count can keep at
         // kMinTilesPerCta tiles each (the kernel applies the same rule to the
         // actual count).
-        const int64_t tiles_unit = SPARSE ? ((int64_t)a.kpages + C::NCW - 1) / C::NCW
+        const int ppt = C::TILE / (dm.page_size > C::SUB ? dm.page_size : C::SUB);  // pages per sparse tile
+        const int64_t tiles_unit = SPARSE ? ((int64_t)a.kpages + ppt - 1) / ppt
                                           : ((int64_t)dm.max_len + C::TILE - 1) / C::TILE;
         const int64_t tmax = (int64_t)dm.batch * dm.num_kv_heads * tiles_unit;
         const int64_t want = (tmax + kMinTilesPerCta - 1) / kMinTilesPerCta;
@@ -568,7 +569,7 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     if (a.workspace == nullptr || a.workspace_bytes < need) return GQAQ_ERR_WORKSPACE;
 
     const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
-    const uint32_t box_rows = SPARSE ? (uint32_t)C::SUB : (uint32_t)C::TILE;
+    const uint32_t box_rows = SPARSE ? (uint32_t)dm.page_size : (uint32_t)C::TILE;
     CUtensorMap kmap, vmap;
     if (SPARSE ? !encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, box_rows)
                : !encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true))

@@ -290,6 +290,29 @@ struct WarpAttn {
 
 // Merge the 8 warp states of a CTA, element (g, d) of the G x D block:
 // m* = max_w m_w, l* = sum_w 2^(m_w - m*) l_w, a* = sum_w 2^(m_w - m*) acc_w.
+// Pages gathered into a 128-row stage, page size S in {8, 16, 32, 64}. Each
+// page takes a slot of max(S, 16) rows (one TMA box of S rows at the slot's
+// start), so a stage holds 128 / max(S, 16) pages. Consumer warp w owns rows
+// 16w .. 16w+15: they lie in page (16w) / slot, from row (16w) % slot, and
+// its valid rows are a prefix (only a sequence's last page can be partial).
+struct PageSlots {
+    int S, slot, ppt;
+    __device__ __forceinline__ void init(int page_size) {
+        S = page_size;
+        slot = page_size > 16 ? page_size : 16;
+        ppt = 128 / slot;
+    }
+    __device__ __forceinline__ int warp_page(int w) const { return (16 * w) / slot; }
+    // Valid rows of warp w when its page `page` (a valid page) of a sequence of
+    // `len` tokens is loaded.
+    __device__ __forceinline__ int warp_rows(int w, int page, int len) const {
+        int rows = len - page * S;
+        rows = rows < S ? rows : S;
+        const int r = rows - (16 * w) % slot;
+        return r < 0 ? 0 : (r < 16 ? r : 16);
+    }
+};
+
 template <int D, int G>
 __device__ __forceinline__ void merge_warps(const float *merge, int g, int d, float &mst, float &ls, float &as) {
     constexpr int NCW = TileCfg<D, G>::NCW;

@@ -720,7 +720,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
         // ================= 4. attention over this CTA's share of the pages =================
         const int e0 = (int)(((int64_t)crank * nsel) / nct);
         const int e1 = (int)(((int64_t)(crank + 1) * nsel) / nct);
-        const int ntile4 = (e1 - e0 + C::NCW - 1) / C::NCW;
+        PageSlots slots;
+        slots.init(p.S);
+        const int ntile4 = (e1 - e0 + slots.ppt - 1) / slots.ppt;
         if (producer) {
             for (int t = 0; t < ntile4; ++t, ++it) {
                 const int s = it % C::NSTAGE;
@@ -735,29 +737,31 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                 }
                 if (*abort_flag) continue;
-                const int e = e0 + t * C::NCW + lane;
+                const int e = e0 + t * slots.ppt + lane;
+                const bool in = lane < slots.ppt && e < e1;
                 int page = -1;
-                if (lane < C::NCW && e < e1)
-                    page = (MODE == FUSED_FULL) ? list[e] : p.page_idx[(int64_t)u * p.kpages + e];
-                const bool ok = lane < C::NCW && e < e1 && page >= 0 && page < P;
-                if (MODE == FUSED_ATTEND && lane < C::NCW && e < e1 && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
-                if (lane < C::NCW) {
-                    const int rem = ok ? len - page * p.S : 0;
-                    tinfo[s * 8 + lane] = rem < C::SUB ? rem : C::SUB;
-                }
+                if (in) page = (MODE == FUSED_FULL) ? list[e] : p.page_idx[(int64_t)u * p.kpages + e];
+                const bool ok = in && page >= 0 && page < P;
+                if (MODE == FUSED_ATTEND && in && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
                 const unsigned m = __ballot_sync(0xffffffffu, ok);
+                {  // valid rows of consumer warp (lane & 7)
+                    const int j = slots.warp_page(lane & 7);
+                    const int pw = __shfl_sync(0xffffffffu, page, j);
+                    if (lane < 8) tinfo[s * 8 + lane] = ((m >> j) & 1u) ? slots.warp_rows(lane, pw, len) : 0;
+                }
                 __syncwarp();
                 const uint32_t kdst = smem_u32(ring + s * C::STAGE);
                 const uint32_t vdst = kdst + C::KBYTES;
                 const uint32_t fb = smem_u32(&full[s]);
-                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(C::SUB * D * 2 * 2));
+                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(p.S * D * 2 * 2));
 #pragma unroll
-                for (int j = 0; j < C::NCW; ++j) {
+                for (int j = 0; j < 8; ++j) {
                     const int pj = __shfl_sync(0xffffffffu, page, j);
                     if (lane == 0 && ((m >> j) & 1u)) {
                         const int y = u * p.Lmax + pj * p.S;
-                        tma_load_3d(kdst + j * C::SUB * D * 2, &kmap, 0, 0, y, fb, pol);  // page-major K
-                        tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
+                        const uint32_t off = (uint32_t)(j * slots.slot * D * 2);
+                        tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K
+                        tma_load_2d(vdst + off, &vmap, 0, y, fb, pol);
                     }
                 }
                 __syncwarp();
@@ -912,8 +916,8 @@ int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
     } else {
         memset(&mmap, 0, sizeof(mmap));
     }
-    if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, C::SUB)) return GQAQ_ERR_CUDA;
-    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, C::SUB, false)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, (uint32_t)dm.page_size)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, (uint32_t)dm.page_size, false)) return GQAQ_ERR_CUDA;
 
     FusedParams p;
     p.q = a.q;

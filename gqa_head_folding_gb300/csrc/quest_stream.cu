@@ -124,7 +124,7 @@ struct StreamParams {
     int B, Hkv, Lmax, Pmax, S, kpages;
     int ma;       // metadata tiles per score item
     int n_s;      // score items per unit
-    int ppi;      // list entries per attend item (multiple of 8)
+    int ppi;      // list entries per attend item (a multiple of 8, so of the pages per stage)
     int n_a;      // attend items per unit
     int n_items;  // U * (n_s + n_a)
     float scale_log2;
@@ -457,21 +457,26 @@ __global__ void __launch_bounds__(StreamCfg<D, G>::THREADS, StreamCfg<D, G>::MIN
                     }
                     __syncwarp();  // the list loads below follow lane 0's acquire
                     ok = __shfl_sync(0xffffffffu, ok, 0);
-                    const int nt = (ne + 7) / 8;
+                    PageSlots slots;
+                    slots.init(p.S);
+                    const int nt = (ne + slots.ppt - 1) / slots.ppt;
                     for (int t = 0; t < nt && ok; ++t) {
                         int s = 0;
                         if (lane == 0) ok = slot_wait(s);
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         s = __shfl_sync(0xffffffffu, s, 0);
                         if (!ok) break;
-                        const int e = e_lo + t * 8 + lane;
+                        const int e = e_lo + t * slots.ppt + lane;
+                        const bool in = lane < slots.ppt && e < e_lo + ne;
                         int page = -1;
-                        if (lane < 8 && e < e_lo + ne) page = __ldcg(p.list + (int64_t)u * p.kpages + e);
-                        const bool okp = lane < 8 && e < e_lo + ne && page >= 0 && page < P;
+                        if (in) page = __ldcg(p.list + (int64_t)u * p.kpages + e);
+                        const bool okp = in && page >= 0 && page < P;
+                        const unsigned m = __ballot_sync(0xffffffffu, okp);
                         int *ti = tinfo + s * C::TI;
-                        if (lane < 8) {
-                            const int rem = okp ? len - page * p.S : 0;
-                            ti[4 + lane] = rem < C::SUB ? rem : C::SUB;
+                        {  // valid rows of consumer warp (lane & 7)
+                            const int j = slots.warp_page(lane & 7);
+                            const int pw = __shfl_sync(0xffffffffu, page, j);
+                            if (lane < 8) ti[4 + lane] = ((m >> j) & 1u) ? slots.warp_rows(lane, pw, len) : 0;
                         }
                         if (lane == 0) {
                             ti[0] = ST_ATTEND;
@@ -479,19 +484,19 @@ __global__ void __launch_bounds__(StreamCfg<D, G>::THREADS, StreamCfg<D, G>::MIN
                             ti[2] = (t == 0 ? F_FIRST : 0) | (t == nt - 1 ? F_LAST : 0);
                             ti[3] = idx;
                         }
-                        const unsigned m = __ballot_sync(0xffffffffu, okp);
                         __syncwarp();
                         const uint32_t kdst = smem_u32(ring + s * C::STAGE);
                         const uint32_t vdst = kdst + C::KBYTES;
                         const uint32_t fb = smem_u32(&full[s]);
-                        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(C::SUB * D * 2 * 2));
+                        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(p.S * D * 2 * 2));
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const int pj = __shfl_sync(0xffffffffu, page, j);
                             if (lane == 0 && ((m >> j) & 1u)) {
                                 const int y = u * p.Lmax + pj * p.S;
-                                tma_load_3d(kdst + j * C::SUB * D * 2, &kmap, 0, 0, y, fb, pol);  // page-major K
-                                tma_load_2d(vdst + j * C::SUB * D * 2, &vmap, 0, y, fb, pol);
+                                const uint32_t off = (uint32_t)(j * slots.slot * D * 2);
+                                tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K
+                                tma_load_2d(vdst + off, &vmap, 0, y, fb, pol);
                             }
                         }
                         if (lane == 0) ++it;
@@ -896,8 +901,8 @@ int stream_t(const FusedArgs &a, const LaunchCtx &ctx, size_t *need_out) {
     const uint64_t mrows = (uint64_t)U * Pmax;
     CUtensorMap mmap, kmap, vmap;
     if (!encode_tensor_map_2d(&mmap, a.meta, mrows, 2 * D, 64, C::MT, true)) return GQAQ_ERR_CUDA;
-    if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, C::SUB)) return GQAQ_ERR_CUDA;
-    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, C::SUB, false)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, (uint32_t)dm.page_size)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, (uint32_t)dm.page_size, false)) return GQAQ_ERR_CUDA;
 
     uint8_t *ws = reinterpret_cast<uint8_t *>(a.workspace);
     StreamParams p;

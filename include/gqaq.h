@@ -36,7 +36,8 @@
  *      scores           [B][Hkv][Pmax] fp32
  *      page_idx         [B][Hkv][k] int32 (ascending, -1 padded)
  *      valid_len, pos   [B] int32
- *  - Supported: D in {64, 128}; G in {1, 2, 4, 8}; S = 16 for the Quest calls;
+ *  - Supported: D in {64, 128}; G in {1, 2, 4, 8}; S in {8, 16, 32, 64} for the
+ *    Quest calls (the Quest review's page-size trade-off);
  *    B*Hkv*Lmax < 2^31. Other shapes return GQAQ_ERR_UNSUPPORTED.
  *  - Values that live on the device are checked there. This covers valid_len
  *    outside [1, Lmax], page indices outside [0, ceil(valid_len/S)) and pos
@@ -88,13 +89,13 @@ typedef struct {
     int num_kv_heads; /* Hkv >= 1 */
     int head_dim;     /* D: 64 or 128 */
     int max_len;      /* Lmax >= 1: allocated rows per (sequence, KV head) */
-    int page_size;    /* S: 16 (Quest calls); ignored by gqa_decode_attn */
+    int page_size;    /* S: 8, 16, 32 or 64 (Quest calls); ignored by gqa_decode_attn */
 } gqaq_dims;
 
 /* Bytes of workspace that gqa_decode_attn and quest_sparse_attn need on the
  * current device for these dims (enough for both). The library sizes its
  * grid from the SM count, so the figure depends on the device.
- * With max_selected_pages = k > 0 (and S = 16) the figure also covers
+ * With max_selected_pages = k > 0 (and a supported S) the figure also covers
  * quest_decode_attn's work-queue kernel for that k.
  * Returns 0 when the dims are invalid or unsupported.
  * The workspace starts with counters and flags (a ticket word, three words
@@ -177,7 +178,7 @@ GQAQ_API int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const 
  * page's min/max; score every valid page; select the k best pages (ties to
  * the lower index); attend over only their tokens ([QUEST] flowchart).
  * scores ([B][Hkv][Pmax] fp32) and page_idx ([B][Hkv][k] int32, ascending,
- * -1 padded) are optional outputs (NULL to skip). S = 16, 1 <= k <= 65536.
+ * -1 padded) are optional outputs (NULL to skip). 1 <= k <= 65536.
  * With a workspace (>= gqaq_workspace_bytes(dims, k) bytes, zero-filled
  * before its first use, see gqaq_workspace_bytes) the step can run as one
  * work queue over the whole GPU: page-scoring and attention pieces of every

@@ -87,8 +87,10 @@ def test_decode_reports_unsupported_shapes(L):
 def test_quest_calls_reject_bad_arguments(L):
     d = dims(head_dim=128)
     assert L.quest_append_kv(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == g.GQAQ_ERR_INVALID_ARG
-    assert L.quest_append_kv(ctypes.byref(dims(page_size=8)), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == \
-        g.GQAQ_ERR_UNSUPPORTED
+    for bad_s in (0, 4, 12, 24, 128):               # page sizes 8, 16, 32 and 64 are supported
+        expect = g.GQAQ_ERR_INVALID_ARG if bad_s < 1 else g.GQAQ_ERR_UNSUPPORTED
+        assert L.quest_append_kv(ctypes.byref(dims(page_size=bad_s)), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 None) == expect
     assert L.quest_update_meta(ctypes.byref(d), FAKE, FAKE, FAKE, 3, 2, None) == g.GQAQ_ERR_INVALID_ARG
     assert L.quest_update_meta(ctypes.byref(d), FAKE, FAKE, FAKE, 0, 257, None) == g.GQAQ_ERR_INVALID_ARG
     assert L.quest_score_pages(ctypes.byref(d), FAKE, MISALIGNED, FAKE, FAKE, None) == g.GQAQ_ERR_INVALID_ARG
