@@ -44,13 +44,14 @@ UNIT = "us/step"
 # value vector; dense reads 2ML per KV head, Quest reads ~2ML/S of metadata
 # plus 2MKS of selected keys and values.
 # ---------------------------------------------------------------------------
-def kv_vector_bytes(head_dim: int) -> int:
-    return 2 * head_dim
+def kv_vector_bytes(head_dim: int, kv: str = "f16") -> int:
+    """M: bytes of one cached key or value vector (fp16, or 8-bit E4M3 codes)."""
+    return head_dim * (1 if kv == "e4m3" else 2)
 
 
-def dense_unit_bytes(head_dim: int, length: int) -> int:
+def dense_unit_bytes(head_dim: int, length: int, kv: str = "f16") -> int:
     """Keys and values of one (sequence, KV head): 2 M L."""
-    return 2 * kv_vector_bytes(head_dim) * length
+    return 2 * kv_vector_bytes(head_dim, kv) * length
 
 
 def meta_unit_bytes(head_dim: int, length: int, page_size: int) -> int:
@@ -64,7 +65,7 @@ def selected_unit_bytes(head_dim: int, length: int, page_size: int, k_pages: int
     return 2 * kv_vector_bytes(head_dim) * page_size * min(k_pages, pages)
 
 
-def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True) -> dict:
+def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True, kv: str = "f16") -> dict:
     """Algorithmic bytes of one step, by call family (per-step totals).
 
     Families follow the calls a step makes: "dense" (dense layers), "append"
@@ -81,6 +82,8 @@ def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True) -> dic
 
     qo = 2 * G * M                                   # q read + out write per unit
     app_unit = 2 * M + 2 * M + 4 * M                 # new k,v read, row write, page min/max read+write
+    if kv == "e4m3":                                 # new k,v read (fp16), 8-bit rows written, no metadata
+        app_unit = 2 * M + 2 * kv_vector_bytes(D, kv)
     for layer, lens in enumerate(lens_per_layer):
         dense = w.layer_is_dense(layer)
         if w.append and (dense or not fused):
@@ -89,7 +92,7 @@ def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True) -> dic
         if dense:
             count("dense")
             for L in lens:
-                add("dense", w.num_kv_heads * (dense_unit_bytes(D, L) + qo))
+                add("dense", w.num_kv_heads * (dense_unit_bytes(D, L, kv) + qo))
         elif fused:
             count("quest")
             for L in lens:
@@ -107,11 +110,11 @@ def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True) -> dic
     return {"bytes": fam, "launches": launches, "total": sum(fam.values())}
 
 
-def roofline_unit_bytes(w: workloads.Workload, family: str, lens) -> int:
+def roofline_unit_bytes(w: workloads.Workload, family: str, lens, kv: str = "f16") -> int:
     """Per-launch bytes of the per-unit figures (K/V, metadata, selected K/V)."""
     D, S = w.head_dim, w.page_size
     if family == "dense":
-        return sum(w.num_kv_heads * dense_unit_bytes(D, L) for L in lens)
+        return sum(w.num_kv_heads * dense_unit_bytes(D, L, kv) for L in lens)
     if family == "score":
         return sum(w.num_kv_heads * meta_unit_bytes(D, L, S) for L in lens)
     if family == "sparse":
@@ -208,18 +211,29 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Workload state on the device
 # ---------------------------------------------------------------------------
-def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True):
+def e4m3_cache(x: torch.Tensor):
+    """Input preparation for the 8-bit cache: per-tensor scale amax / 448 and
+    the E4M3 codes of x / scale (torch's float8 conversion, outside the step)."""
+    scale = max(float(x.abs().max()), 1e-6) / 448.0
+    return (x.float() * (1.0 / scale)).to(torch.float8_e4m3fn).view(torch.uint8), scale
+
+
+def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True, kv: str = "f16"):
     import gqa_head_folding_gb300 as g
     from gqa_head_folding_gb300.decode import DecodeStack, Layer
     stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
-                        w.dense_layers, device, w.page_size, fused=fused)
+                        w.dense_layers, device, w.page_size, fused=fused, kv=kv, num_layers=w.num_layers)
     layers, lens = [], []
     for layer in range(w.num_layers):
         x = workloads.make_layer(w, layer, device=device,
                                  seed=workloads.layer_seed(w, layer) + seed_offset if seed_offset else None)
         L = Layer(q=x["q"], k_cache=x["k_cache"], v_cache=x["v_cache"], valid_len=x["valid_len"],
                   out=torch.empty_like(x["q"]))
-        if w.append or not w.layer_is_dense(layer):
+        if kv == "e4m3":
+            L.k_cache, L.k_scale = e4m3_cache(x["k_cache"])
+            L.v_cache, L.v_scale = e4m3_cache(x["v_cache"])
+            del x["k_cache"], x["v_cache"]
+        elif w.append or not w.layer_is_dense(layer):
             L.meta = stack.new_meta()
             prefill = x["valid_len"] - 1 if w.append else x["valid_len"]
             g.quest_update_meta(L.k_cache, prefill, L.meta, page_size=w.page_size)
@@ -234,7 +248,8 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from one ncu
 # capture of the kernel as it stands, keyed by (workload id, batch, family). A kernel
 # change makes its entry stale: it is then removed until the capture is taken again.
-NCU_TRAFFIC = {(3, 1, "quest"): 67_802_624, (3, 1, "dense"): 539_928_576, (2, 32, "dense"): 180_061_184}
+NCU_TRAFFIC = {(3, 1, "quest", "f16"): 67_802_624, (3, 1, "dense", "f16"): 539_928_576,
+               (2, 32, "dense", "f16"): 180_061_184}
 
 
 def capture(fn, device):
@@ -279,13 +294,14 @@ def family_timings(stack, layers, w, device, reps: int) -> dict:
 # ---------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle on a bounded sample, scaled to one step
 # ---------------------------------------------------------------------------
-def oracle_step_seconds(w: workloads.Workload, layers, lens, budget_s: float = 15.0) -> dict:
+def oracle_step_seconds(w: workloads.Workload, layers, lens, budget_s: float = 15.0, kv: str = "f16") -> dict:
     """Time the oracle per (sequence, KV head) unit on sampled units of one
     dense and one Quest layer, and scale by the units of a whole step."""
     import numpy as np
 
     import oracle
     S, G = w.page_size, w.group
+    kv_dtype = kv
     scale = 1.0 / math.sqrt(w.head_dim)
 
     def unit_arrays(L, b, kv):
@@ -297,7 +313,10 @@ def oracle_step_seconds(w: workloads.Workload, layers, lens, budget_s: float = 1
     def dense_unit(L, b, kv, length):
         q, k, v = unit_arrays(L, b, kv)
         t0 = time.perf_counter()
-        oracle.attn_repeat_kv(q, k, v, [length], scale)
+        if kv_dtype == "e4m3":
+            oracle.attn_e4m3(q, k, v, L.k_scale, L.v_scale, [length], scale)
+        else:
+            oracle.attn_repeat_kv(q, k, v, [length], scale)
         return time.perf_counter() - t0
 
     def quest_unit(L, b, kv, length):
@@ -365,7 +384,7 @@ def workload_from_args(args) -> workloads.Workload:
 
 
 def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool = True,
-              quest_kernel: str = "cluster") -> dict:
+              quest_kernel: str = "cluster", kv: str = "f16") -> dict:
     return {"workload": f"{w.name} (config {w.id})", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
             "layers": w.num_layers, "dense_layers": w.num_layers if w.k_pages is None else w.dense_layers,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
@@ -376,6 +395,7 @@ def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool =
             "quest_path": (f"fused (quest_decode_attn, {'GPU-wide work queue' if quest_kernel == 'queue' else 'cluster per unit'})"
                            if fused else "step-by-step calls"),
             "launch": "programmatic dependent launch" if pdl else "plain stream order",
+            "kv_cache": "e4m3 codes, per-tensor fp32 scales" if kv == "e4m3" else "f16",
             "l2": "per-step working set > 4x L2; no flush"}
 
 
@@ -389,18 +409,18 @@ def run_reference(args, rank, world):
         print(json.dumps({"impl": "reference", "unavailable": "inputs are drawn on the GPU; no CUDA device"}))
         return
     import gqa_head_folding_gb300 as g  # noqa: F401  (prefill metadata on the device)
-    stack, layers, lens = build_state(w, device)
+    stack, layers, lens = build_state(w, device, kv=args.kv)
     per_step = []
     for i in range(args.warmup + args.steps):
-        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget)
+        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget, kv=args.kv)
         if i >= args.warmup:
             per_step.append(r["seconds_per_step"])
     value = statistics.mean(per_step) * 1e6
-    sb = step_bytes(w, lens)
+    sb = step_bytes(w, lens, kv=args.kv)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, 1),
+            "config": config_of(w, 1, kv=args.kv),
             "achieved_gbs": sb["total"] / (value / 1e6) / 1e9,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": r["sample"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -425,8 +445,8 @@ def run_ours(args, rank, world, local):
     g.set_option(g.GQAQ_OPT_PDL, 0 if args.no_pdl else 1)
     if args.quest_kernel == "queue":
         g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 2)
-    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused)
-    sb = step_bytes(w, lens, fused=not args.unfused)
+    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused, kv=args.kv)
+    sb = step_bytes(w, lens, fused=not args.unfused, kv=args.kv)
     step = lambda: stack.step(layers)  # noqa: E731
     graph = capture(step, device)
 
@@ -467,13 +487,13 @@ def run_ours(args, rank, world, local):
     if dominant in ("dense", "score", "sparse", "quest"):
         layer_of = next(i for i in range(w.num_layers)
                         if (stack.is_dense(i) if dominant == "dense" else not stack.is_dense(i)))
-        per_launch = roofline_unit_bytes(w, dominant, lens[layer_of])
+        per_launch = roofline_unit_bytes(w, dominant, lens[layer_of], kv=args.kv)
         achieved = per_launch / fam[dominant]["s_per_launch"] / 1e9
         roof = {"bound": "hbm", "kernel": {"dense": "gqa_decode_attn", "score": "quest_score_pages",
                                            "sparse": "quest_sparse_attn", "quest": "quest_decode_attn"}[dominant],
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                "traffic": NCU_TRAFFIC.get((w.id, w.batch, dominant)), "bytes_per_launch": per_launch,
+                "traffic": NCU_TRAFFIC.get((w.id, w.batch, dominant, args.kv)), "bytes_per_launch": per_launch,
                 "us_per_launch": round(fam[dominant]["s_per_launch"] * 1e6, 2)}
 
     # end to end through the public API: host inputs in, host outputs out
@@ -503,7 +523,7 @@ def run_ours(args, rank, world, local):
         return
     cpu = None
     if not args.no_cpu_baseline:
-        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget)
+        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget, kv=args.kv)
         cpu = {"value": r["seconds_per_step"] * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": r["sample"]}
     launches = stack.launches_per_step(layers)
@@ -511,9 +531,10 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16 in/out, f32 accumulate",
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 in/out, " + ("e4m3 KV cache, " if args.kv == "e4m3" else "") + "f32 accumulate",
         "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl,
-                                                                                       quest_kernel=args.quest_kernel),
+                                                                                       quest_kernel=args.quest_kernel, kv=args.kv),
         "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
         "achieved_frac_of_peak": round(sb["total"] / s_per_step / 1e9 / peaks["hbm_gbs"], 4),
         "bytes_per_step": total_bytes,
@@ -552,7 +573,13 @@ def main(argv=None):
     ap.add_argument("--quest-kernel", choices=("queue", "cluster"), default="cluster",
                     help="fused Quest kernel: one cluster per unit (default) or the GPU-wide work queue")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
+    ap.add_argument("--kv", choices=("f16", "e4m3"), default="f16",
+                    help="KV-cache format; e4m3 (8-bit codes, per-tensor scales) runs all-dense stacks only")
     args = ap.parse_args(argv)
+    if args.kv == "e4m3":
+        w = workload_from_args(args)
+        if any(not w.layer_is_dense(i) for i in range(w.num_layers)):
+            raise SystemExit("--kv e4m3 needs a stack of dense layers only (e.g. --workload 2, or --layers 2)")
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

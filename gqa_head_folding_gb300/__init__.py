@@ -9,7 +9,9 @@ missing, the import still succeeds but every call raises: there is no CPU
 fallback.
 
 Function names follow the C ABI: gqa_decode_attn, quest_append_kv,
-quest_update_meta, quest_score_pages, quest_topk_pages, quest_sparse_attn.
+quest_update_meta, quest_score_pages, quest_topk_pages, quest_sparse_attn,
+quest_decode_attn, and the 8-bit cache pair gqa_decode_attn_e4m3 /
+kv_append_e4m3.
 """
 from __future__ import annotations
 
@@ -59,7 +61,7 @@ class Dims(ctypes.Structure):
 # Exported symbols, in the order include/gqaq.h declares them.
 EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_update_meta",
            "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "quest_decode_attn",
-           "gqa_decode_attn_noalloc",
+           "gqa_decode_attn_noalloc", "gqa_decode_attn_e4m3", "kv_append_e4m3",
            "gqaq_status_string", "gqaq_set_option", "gqaq_device_status", "gqaq_version")
 
 _lib = None
@@ -86,6 +88,9 @@ def lib():
         L.quest_decode_attn.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp,
                                         vp, ctypes.c_size_t, vp]
         L.gqa_decode_attn_noalloc.argtypes = [dp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
+        f32 = ctypes.c_float
+        L.gqa_decode_attn_e4m3.argtypes = [dp, vp, vp, vp, f32, f32, vp, f32, vp, vp, ctypes.c_size_t, vp]
+        L.kv_append_e4m3.argtypes = [dp, vp, vp, vp, vp, vp, f32, f32, vp]
         L.gqaq_status_string.argtypes = [i32]
         L.gqaq_status_string.restype = ctypes.c_char_p
         L.gqaq_set_option.argtypes = [i32, ctypes.c_int64]
@@ -242,6 +247,41 @@ def gqa_decode_attn_noalloc(q, k_cache, v_cache, valid_len, scale: float, out):
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(valid_len), float(scale),
         _ptr(out), _stream(q)))
     return out
+
+
+def gqa_decode_attn_e4m3(q, k_cache, v_cache, k_scale: float, v_scale: float, valid_len, scale: float,
+                         out=None, workspace=None):
+    """Dense folded-GQA decode attention over an E4M3 cache: k_cache / v_cache
+    [B,Hkv,Lmax,D] uint8 codes, dequantized as code value * k_scale (v_scale)."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    d = dims_of(q, k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 3)
+    if workspace is None:
+        workspace = alloc_workspace(d, q.device)
+    _check("gqa_decode_attn_e4m3", lib().gqa_decode_attn_e4m3(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale), _ptr(valid_len),
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(q)))
+    return out
+
+
+def kv_append_e4m3(k_cache, v_cache, k_new, v_new, pos, k_inv_scale: float, v_inv_scale: float):
+    """Quantize k_new/v_new [B,Hkv,D] fp16 to E4M3 (x * inv_scale, nearest-even,
+    saturating) and write the codes at row pos[b] of the uint8 caches."""
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(k_new, "k_new", torch.float16, 3)
+    _need(v_new, "v_new", torch.float16, 3)
+    _need(pos, "pos", torch.int32, 1)
+    B, Hkv, Lmax, D = k_cache.shape
+    d = make_dims(B, Hkv, Hkv, D, Lmax)
+    _check("kv_append_e4m3", lib().kv_append_e4m3(
+        ctypes.byref(d), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos), float(k_inv_scale),
+        float(v_inv_scale), _stream(k_cache)))
 
 
 def quest_append_kv(k_cache, v_cache, meta, k_new, v_new, pos, page_size: int = PAGE_SIZE):

@@ -121,6 +121,22 @@ bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                          int swizzle_bytes) {
+    if (!encode_tensor_map_2d(map, base, rows, cols, cols, box_rows, false)) return false;  // loads g_encode
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {(cuuint32_t)cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_tensor_map_kpage(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     if (cols % 64 != 0 || !encode_tensor_map_2d(map, base, rows, cols, 64, box_rows, true)) return false;  // loads g_encode
     const cuuint64_t dims[3] = {64, cols / 64, rows};
@@ -225,7 +241,7 @@ int gqa_decode_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half *
     LaunchCtx ctx;
     rc = make_ctx(&ctx, stream);
     if (rc != GQAQ_OK) return rc;
-    AttnArgs a;
+    AttnArgs a = {};
     a.dims = dims;
     a.q = reinterpret_cast<const __half *>(q);
     a.k_cache = reinterpret_cast<const __half *>(k_cache);
@@ -327,7 +343,7 @@ int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half
         f.out = reinterpret_cast<__half *>(out);
         return launch_quest_fused(f, ctx);
     }
-    AttnArgs a;
+    AttnArgs a = {};
     a.dims = dims;
     a.q = reinterpret_cast<const __half *>(q);
     a.k_cache = reinterpret_cast<const __half *>(k_cache);
@@ -340,6 +356,50 @@ int quest_sparse_attn(const gqaq_dims *dims, const gqaq_half *q, const gqaq_half
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     return launch_attention(a, ctx);
+}
+
+int gqa_decode_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                         float k_scale, float v_scale, const int32_t *valid_len, float scale, gqaq_half *out,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_dims(dims, false);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(valid_len))
+        return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !isfinite(k_scale) || !isfinite(v_scale)) return GQAQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace)) return GQAQ_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    AttnArgs a = {};
+    a.dims = dims;
+    a.q = reinterpret_cast<const __half *>(q);
+    a.k_cache = reinterpret_cast<const __half *>(k_cache);  // byte rows; typed as the kernels take it
+    a.v_cache = reinterpret_cast<const __half *>(v_cache);
+    a.valid_len = valid_len;
+    a.page_idx = nullptr;
+    a.kpages = 0;
+    a.scale = scale;
+    a.kv8 = true;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.out = reinterpret_cast<__half *>(out);
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launch_attention(a, ctx);
+}
+
+int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_cache, const gqaq_half *k_new,
+                   const gqaq_half *v_new, const int32_t *pos, float k_inv_scale, float v_inv_scale, void *stream) {
+    int rc = check_dims(dims, false);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(pos))
+        return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(k_inv_scale) || !isfinite(v_inv_scale)) return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_append_e4m3(dims, k_cache, v_cache, reinterpret_cast<const __half *>(k_new),
+                              reinterpret_cast<const __half *>(v_new), pos, k_inv_scale, v_inv_scale, ctx);
 }
 
 int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_cache, gqaq_half *v_cache,

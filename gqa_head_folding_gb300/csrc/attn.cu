@@ -35,15 +35,25 @@
 
 namespace gqaq {
 
-template <int D, int G>
+// KV8: the E4M3 cache variant (one byte per channel): half the stage bytes,
+// so up to six stages (192 KB of copies in flight per SM).
+template <int D, int G, bool KV8 = false>
 struct AttnCfg : TileCfg<D, G> {
     using T = TileCfg<D, G>;
     static constexpr int THREADS = (T::NCW + 1) * 32;
     static constexpr int MISC = 256;
     static constexpr int FIXED = T::QBYTES + T::MERGE + T::PBYTES + MISC;
-    static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2;
-    static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
+    static constexpr int KBYTES = KV8 ? T::TILE * D : T::KBYTES;
+    static constexpr int STAGE = KV8 ? 2 * T::TILE * D : T::STAGE;
+    // 8-bit tiles: the deepest ring of at most six stages that fits (two CTAs
+    // per SM at D = 64, one at D = 128).
+    static constexpr int LIMIT8 = (D == 64 ? 112 : 225) * 1024 - FIXED - 1024;
+    static constexpr int NSTAGE8 = LIMIT8 / STAGE < 6 ? LIMIT8 / STAGE : 6;
+    static constexpr int NSTAGE = KV8 ? NSTAGE8 : ((3 * STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2);
+    static constexpr int SMEM = 1024 + NSTAGE * STAGE + FIXED;
     static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
+    static_assert(NSTAGE >= 2, "at least a double-buffered ring");
+    static_assert(2 * NSTAGE * 8 + 128 <= MISC, "mbarriers and schedule fit the misc region");
 };
 
 constexpr int kMinTilesPerCta = 4;
@@ -57,7 +67,8 @@ struct AttnParams {
     unsigned *count;  // [B*Hkv]: arrivals at split units; zero between calls
     int *status;
     int B, Hkv, Lmax, kpages, S;
-    float scale_log2;
+    float scale_log2;  // includes the K scale of an E4M3 cache
+    float v_scale;     // E4M3 cache: V scale (1 otherwise)
     uint64_t timeout_ns;
     int test_stall;
 };
@@ -219,11 +230,12 @@ __device__ __forceinline__ void merge_parts(const float *part, float *wbuf, int6
     }
 }
 
-template <int D, int G, bool SPARSE>
-__global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLOCKS)
+template <int D, int G, bool SPARSE, bool KV8 = false>
+__global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8>::MIN_BLOCKS)
     attn_partial_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
-    using C = AttnCfg<D, G>;
+    using C = AttnCfg<D, G, KV8>;
+    static_assert(!(SPARSE && KV8), "the E4M3 variant is dense");
     constexpr int NCT = C::NCW * 32;  // consumer threads
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -369,9 +381,13 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
                     if (lane == 0) {
                         mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
                         const int y = row0 + local * C::TILE;
+                        if (KV8) {
+                            tma_load_2d(kdst, &kmap, 0, y, fb, pol);
+                        } else {
 #pragma unroll
-                        for (int kh = 0; kh < C::KH; ++kh)
-                            tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
+                            for (int kh = 0; kh < C::KH; ++kh)
+                                tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
+                        }
                         tma_load_2d(vdst, &vmap, 0, y, fb, pol);
                     }
                 }
@@ -398,7 +414,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
     // the arrival counters in step, so the workspace stays reusable.
     // ----------------------------------------------------------------------
     const int tid = threadIdx.x;  // 0..255 among consumers
-    WarpAttn<D, G, SPARSE> wa;  // sparse stages hold K page-major
+    WarpAttn<D, G, SPARSE, KV8> wa;  // sparse stages hold K page-major
     wa.init(warp, lane, smem_u32(pbuf));
 
     Walk w;
@@ -462,6 +478,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G>::THREADS, AttnCfg<D, G>::MIN_BLO
             const int g = idx / D, d = idx - (idx / D) * D;
             float mst, ls, as;
             merge_warps<D, G>(merge, g, d, mst, ls, as);
+            if (KV8) as *= p.v_scale;
             if (complete) {
                 outg[idx] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
             } else {
@@ -522,13 +539,13 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-template <int D, int G, bool SPARSE>
+template <int D, int G, bool SPARSE, bool KV8 = false>
 int grid_for(const LaunchCtx &ctx) {
-    using C = AttnCfg<D, G>;
+    using C = AttnCfg<D, G, KV8>;
     static int occ[kMaxDevices] = {0};
     if (ctx.device < 0 || ctx.device >= kMaxDevices) return -1;
     if (occ[ctx.device] == 0) {
-        auto kern = attn_partial_kernel<D, G, SPARSE>;
+        auto kern = attn_partial_kernel<D, G, SPARSE, KV8>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return -1;
         int n = 0;
@@ -547,11 +564,11 @@ int grid_for(const LaunchCtx &ctx) {
 // then the partials [grid][2][G][D+2] fp32.
 inline size_t count_bytes(const gqaq_dims &dm) { return workspace_zero_bytes(dm); }
 
-template <int D, int G, bool SPARSE>
+template <int D, int G, bool SPARSE, bool KV8 = false>
 int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
-    using C = AttnCfg<D, G>;
+    using C = AttnCfg<D, G, KV8>;
     const gqaq_dims &dm = *a.dims;
-    int grid = grid_for<D, G, SPARSE>(ctx);
+    int grid = grid_for<D, G, SPARSE, KV8>(ctx);
     if (grid < 1) return GQAQ_ERR_CUDA;
     {
         // Launch no more CTAs than the shape's largest tile count can keep at
@@ -571,10 +588,15 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
     const uint32_t box_rows = SPARSE ? (uint32_t)dm.page_size : (uint32_t)C::TILE;
     CUtensorMap kmap, vmap;
-    if (SPARSE ? !encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, box_rows)
-               : !encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true))
-        return GQAQ_ERR_CUDA;
-    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, box_rows, false)) return GQAQ_ERR_CUDA;
+    if (KV8) {  // byte rows: D = 128 rows 128-byte swizzled, D = 64 rows 64-byte swizzled
+        if (!encode_tensor_map_u8(&kmap, a.k_cache, rows, D, box_rows, D == 128 ? 128 : 64)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_u8(&vmap, a.v_cache, rows, D, box_rows, 0)) return GQAQ_ERR_CUDA;
+    } else {
+        if (SPARSE ? !encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, box_rows)
+                   : !encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true))
+            return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, box_rows, false)) return GQAQ_ERR_CUDA;
+    }
 
     AttnParams p;
     p.q = a.q;
@@ -589,17 +611,19 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     p.Lmax = dm.max_len;
     p.kpages = SPARSE ? a.kpages : 1;
     p.S = SPARSE ? dm.page_size : 16;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.scale_log2 = a.scale * (KV8 ? a.k_scale : 1.f) * 1.4426950408889634f;
+    p.v_scale = KV8 ? a.v_scale : 1.f;
     p.timeout_ns = ctx.timeout_ns;
     p.test_stall = ctx.test_stall;
-    if (launch_kernel(attn_partial_kernel<D, G, SPARSE>, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, kmap, vmap,
-                      p) != cudaSuccess)
+    if (launch_kernel(attn_partial_kernel<D, G, SPARSE, KV8>, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, kmap,
+                      vmap, p) != cudaSuccess)
         return GQAQ_ERR_CUDA;
     return GQAQ_OK;
 }
 
 template <int D, int G>
 int dispatch_sparse(const AttnArgs &a, const LaunchCtx &ctx) {
+    if (a.kv8) return a.page_idx ? GQAQ_ERR_UNSUPPORTED : launch_t<D, G, false, true>(a, ctx);
     return a.page_idx ? launch_t<D, G, true>(a, ctx) : launch_t<D, G, false>(a, ctx);
 }
 
@@ -618,8 +642,10 @@ template <int D, int G>
 size_t ws_t(const gqaq_dims &dm, const LaunchCtx &ctx) {
     const int g0 = grid_for<D, G, false>(ctx);
     const int g1 = grid_for<D, G, true>(ctx);
-    if (g0 < 1 || g1 < 1) return 0;
-    const int grid = g0 > g1 ? g0 : g1;
+    const int g2 = grid_for<D, G, false, true>(ctx);
+    if (g0 < 1 || g1 < 1 || g2 < 1) return 0;
+    int grid = g0 > g1 ? g0 : g1;
+    grid = grid > g2 ? grid : g2;
     return count_bytes(dm) + (size_t)grid * 2 * G * (D + 2) * sizeof(float);
 }
 

@@ -56,13 +56,28 @@ struct TileCfg {
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
 };
 
+// Two E4M3 codes (low byte = first element) -> fp16x2 (low half = first).
+// Every E4M3 value is exactly representable in fp16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(two));
+    return r;
+}
+
 // K layout in a stage: KPAGE = false: KH column blocks of TILE rows x 128 B
 // ([kh][row]); KPAGE = true: row after row, each row's KH 128-byte blocks
 // side by side ([row][kh]), as one 3-D TMA box per page writes them. Both
 // are 128-byte swizzled: 16-byte chunk c of 128-byte line L sits at c ^ (L & 7).
-template <int D, int G, bool KPAGE = false>
+// KV8 = true: K and V hold E4M3 codes, one byte per channel. K rows are D
+// bytes: D = 128 rows are 128-byte swizzled like above (chunk c of row r at
+// c ^ (r & 7)); D = 64 rows are 64-byte swizzled (chunk c of row r at
+// c ^ ((r >> 1) & 3)). V rows are D bytes, not swizzled. Products of the fp16
+// q with the decoded codes are exact; the caller folds the per-tensor K scale
+// into scale_log2 and multiplies the output by the V scale.
+template <int D, int G, bool KPAGE = false, bool KV8 = false>
 struct WarpAttn {
     using C = TileCfg<D, G>;
+    static_assert(!(KPAGE && KV8), "8-bit K is dense-only");
     int lane, part, jt, cw;
     uint32_t krow_off, kx0, pbw;
     uint4 qr[C::GQ][C::NCH];
@@ -75,7 +90,11 @@ struct WarpAttn {
         part = lane >> 3;
         jt = lane & 7;
         const int c0 = part * C::DQ;
-        if (KPAGE) {
+        if (KV8) {
+            const int row = cw * C::SUB + jt;
+            krow_off = (uint32_t)(row * D);
+            kx0 = (D == 128) ? (uint32_t)((2 * part) ^ jt) : (uint32_t)(part ^ ((jt >> 1) & 3));
+        } else if (KPAGE) {
             const int line = (cw * C::SUB + jt) * C::KH + c0 / 64;
             krow_off = (uint32_t)(line * 128);
             kx0 = (uint32_t)(((c0 % 64) / 8) ^ (line & 7));  // rows jt and jt+8: same (line & 7)
@@ -163,10 +182,20 @@ struct WarpAttn {
                 float a0[C::GQ], a1[C::GQ];
 #pragma unroll
                 for (int g = 0; g < C::GQ; ++g) a0[g] = a1[g] = 0.f;
-                const uint32_t kro = kbase + krow_off + (uint32_t)(u * C::TPP * (KPAGE ? C::KH : 1) * 128);
+                const uint32_t kro = KV8 ? kbase + krow_off + (uint32_t)(u * C::TPP * D)
+                                         : kbase + krow_off + (uint32_t)(u * C::TPP * (KPAGE ? C::KH : 1) * 128);
+                uint4 k8 = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
-                    const uint4 kc = lds128(kro + ((kx0 ^ (uint32_t)c) << 4));
+                    uint4 kc;
+                    if (KV8) {  // one 16-byte chunk of codes feeds two fp16 chunks of q
+                        if ((c & 1) == 0) k8 = lds128(kro + ((kx0 ^ (uint32_t)(c >> 1)) << 4));
+                        const uint32_t lo = (c & 1) ? k8.z : k8.x, hi = (c & 1) ? k8.w : k8.y;
+                        kc = make_uint4(e4m3x2_to_f16x2(lo & 0xffffu), e4m3x2_to_f16x2(lo >> 16),
+                                        e4m3x2_to_f16x2(hi & 0xffffu), e4m3x2_to_f16x2(hi >> 16));
+                    } else {
+                        kc = lds128(kro + ((kx0 ^ (uint32_t)c) << 4));
+                    }
 #pragma unroll
                     for (int g = 0; g < C::GQ; ++g) {
                         a0[g] = fma_h_lo(qr[g][c].x, kc.x, a0[g]);
@@ -226,12 +255,30 @@ struct WarpAttn {
         __syncwarp();
         // ---- 5. acc += p @ V, two tokens per packed FMA ----
         const int npairs = (nvalid + 1) >> 1;
-        const uint32_t vrow = vbase + (uint32_t)(cw * C::SUB * D * 2 + lane * C::DPL * 2);
+        const uint32_t vrow = KV8 ? vbase + (uint32_t)(cw * C::SUB * D + lane * C::DPL)
+                                  : vbase + (uint32_t)(cw * C::SUB * D * 2 + lane * C::DPL * 2);
 #pragma unroll 1
         for (int jp = 0; jp < npairs; ++jp) {
             const bool has1 = 2 * jp + 1 < nvalid;
             float v0[C::DPL], v1[C::DPL];
-            if constexpr (D == 128) {
+            if constexpr (KV8 && D == 128) {  // 4 codes per lane per row
+                const uint32_t r0 = lds32(vrow + (uint32_t)(2 * jp * D));
+                const uint32_t r1 = has1 ? lds32(vrow + (uint32_t)((2 * jp + 1) * D)) : 0u;
+                const float2 a0 = half2_bits_to_float2(e4m3x2_to_f16x2(r0 & 0xffffu));
+                const float2 a1 = half2_bits_to_float2(e4m3x2_to_f16x2(r0 >> 16));
+                const float2 b0 = half2_bits_to_float2(e4m3x2_to_f16x2(r1 & 0xffffu));
+                const float2 b1 = half2_bits_to_float2(e4m3x2_to_f16x2(r1 >> 16));
+                v0[0] = a0.x; v0[1] = a0.y; v0[C::DPL > 2 ? 2 : 0] = a1.x; v0[C::DPL > 3 ? 3 : 0] = a1.y;
+                v1[0] = b0.x; v1[1] = b0.y; v1[C::DPL > 2 ? 2 : 0] = b1.x; v1[C::DPL > 3 ? 3 : 0] = b1.y;
+            } else if constexpr (KV8) {  // D = 64: 2 codes per lane per row
+                uint32_t r0, r1 = 0u;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(r0) : "r"(vrow + (uint32_t)(2 * jp * D)));
+                if (has1) asm volatile("ld.shared.u16 %0, [%1];" : "=r"(r1) : "r"(vrow + (uint32_t)((2 * jp + 1) * D)));
+                const float2 a = half2_bits_to_float2(e4m3x2_to_f16x2(r0));
+                const float2 b = half2_bits_to_float2(e4m3x2_to_f16x2(r1));
+                v0[0] = a.x; v0[C::DPL > 1 ? 1 : 0] = a.y;
+                v1[0] = b.x; v1[C::DPL > 1 ? 1 : 0] = b.y;
+            } else if constexpr (D == 128) {
                 const uint2 r0 = lds64(vrow + (uint32_t)(2 * jp * D * 2));
                 uint2 r1 = lds64(vrow + (uint32_t)((2 * jp + 1) * D * 2));
                 if (!has1) r1 = make_uint2(0u, 0u);

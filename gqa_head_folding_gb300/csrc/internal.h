@@ -21,6 +21,9 @@ bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uin
 // 128-byte swizzle: one TMA load brings box_rows whole rows (all their
 // 128-byte column blocks, interleaved row by row). cols: a multiple of 64.
 bool encode_tensor_map_kpage(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// Byte matrix [rows][cols] (E4M3 codes), box [box_rows][cols], swizzle 0, 64 or 128 bytes.
+bool encode_tensor_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                          int swizzle_bytes);
 
 // Dense (page_idx == nullptr) or sparse split-context attention, one launch:
 // split units are merged in-kernel by the CTA that finishes them last.
@@ -33,11 +36,17 @@ struct AttnArgs {
     const int *page_idx;  // sparse only
     int kpages;           // sparse only
     float scale;
+    bool kv8;             // caches hold E4M3 codes (dense only)
+    float k_scale, v_scale;  // E4M3: value = code * scale
     __half *out;
     void *workspace;
     size_t workspace_bytes;
 };
 int launch_attention(const AttnArgs &a, const LaunchCtx &ctx);
+// E4M3 cache append (kv_e4m3.cu).
+int launch_append_e4m3(const gqaq_dims *d, uint8_t *k_cache, uint8_t *v_cache, const __half *k_new,
+                       const __half *v_new, const int *pos, float k_inv_scale, float v_inv_scale,
+                       const LaunchCtx &ctx);
 size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx);
 
 // Fused Quest step (quest_fused.cu). meta == nullptr selects attention over a

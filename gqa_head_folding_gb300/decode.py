@@ -8,6 +8,12 @@ pick the top ``k_pages``, and attend over those pages only. When a step
 carries a new token, every layer first appends it (``quest_append_kv``), so
 each layer's page metadata stays current whatever path reads it.
 
+With ``kv="e4m3"`` the caches hold 8-bit E4M3 codes with one fp32 scale per
+tensor (``Layer.k_scale`` / ``v_scale``): appends quantize
+(``kv_append_e4m3``) and dense layers read them through
+``gqa_decode_attn_e4m3``. The Quest kernels take fp16 caches only, so an
+8-bit stack must be all dense.
+
 By default a Quest layer is one fused launch (``quest_decode_attn``: append,
 score, top-K and sparse attention in one kernel); the library picks its
 kernel (GQAQ_OPT_QUEST_KERNEL), and the stack's workspace covers both. With
@@ -24,16 +30,16 @@ from typing import List, Optional
 
 import torch
 
-from . import (alloc_workspace, gqa_decode_attn, make_dims, new_meta, num_pages, quest_append_kv,
-               quest_decode_attn, quest_score_pages, quest_sparse_attn, quest_topk_pages,
-               quest_update_meta)
+from . import (alloc_workspace, gqa_decode_attn, gqa_decode_attn_e4m3, kv_append_e4m3, make_dims, new_meta,
+               num_pages, quest_append_kv, quest_decode_attn, quest_score_pages, quest_sparse_attn,
+               quest_topk_pages, quest_update_meta)
 
 
 @dataclasses.dataclass
 class Layer:
     """Device tensors of one attention layer for one step."""
     q: torch.Tensor                       # [B,Hq,D] fp16
-    k_cache: torch.Tensor                 # [B,Hkv,Lmax,D] fp16
+    k_cache: torch.Tensor                 # [B,Hkv,Lmax,D] fp16 (uint8 E4M3 codes with kv="e4m3")
     v_cache: torch.Tensor
     valid_len: torch.Tensor               # [B] int32 (tokens attended after the append)
     out: torch.Tensor                     # [B,Hq,D] fp16
@@ -41,12 +47,19 @@ class Layer:
     k_new: Optional[torch.Tensor] = None  # [B,Hkv,D] fp16
     v_new: Optional[torch.Tensor] = None
     pos: Optional[torch.Tensor] = None    # [B] int32 row the new token goes to
+    k_scale: float = 1.0                  # E4M3 caches: value = code value * scale
+    v_scale: float = 1.0
 
 
 class DecodeStack:
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_len: int,
-                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True):
-        self.fused = fused
+                 k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True,
+                 kv: str = "f16", num_layers: Optional[int] = None):
+        if kv not in ("f16", "e4m3"):
+            raise ValueError(f"kv must be 'f16' or 'e4m3', got {kv!r}")
+        if kv == "e4m3" and k_pages is not None and (num_layers is None or num_layers > dense_layers):
+            raise ValueError("an E4M3 cache runs dense layers only (the Quest kernels read fp16 caches)")
+        self.fused, self.kv = fused, kv
         self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
         self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
         self.k_pages, self.dense_layers = k_pages, dense_layers
@@ -70,6 +83,20 @@ class DecodeStack:
         """Metadata of the pages already in the cache (after a prefill)."""
         quest_update_meta(layer.k_cache, valid_len, layer.meta, page_size=self.page_size)
 
+    def append(self, L: Layer):
+        if self.kv == "e4m3":
+            kv_append_e4m3(L.k_cache, L.v_cache, L.k_new, L.v_new, L.pos, 1.0 / L.k_scale, 1.0 / L.v_scale)
+        else:
+            quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos, self.page_size)
+
+    def dense(self, L: Layer):
+        if self.kv == "e4m3":
+            gqa_decode_attn_e4m3(L.q, L.k_cache, L.v_cache, L.k_scale, L.v_scale, L.valid_len, self.scale,
+                                 out=L.out, workspace=self.workspace)
+        else:
+            gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale, out=L.out,
+                            workspace=self.workspace)
+
     def families(self, layers: List[Layer]):
         """The library calls of one step, grouped by kind: name -> list of thunks."""
         fam = {}
@@ -80,11 +107,9 @@ class DecodeStack:
         for i, L in enumerate(layers):
             dense = self.is_dense(i)
             if L.k_new is not None and (dense or not self.fused):
-                add("append", lambda L=L: quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos,
-                                                          self.page_size))
+                add("append", lambda L=L: self.append(L))
             if dense:
-                add("dense", lambda L=L: gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale,
-                                                         out=L.out, workspace=self.workspace))
+                add("dense", lambda L=L: self.dense(L))
             elif self.fused:
                 add("quest", lambda L=L: quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len,
                                                            self.k_pages, self.scale, k_new=L.k_new, v_new=L.v_new,
@@ -112,10 +137,9 @@ class DecodeStack:
         for i, L in enumerate(layers):
             dense = self.is_dense(i)
             if L.k_new is not None and (dense or not self.fused):
-                quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos, self.page_size)
+                self.append(L)
             if dense:
-                gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale, out=L.out,
-                                workspace=self.workspace)
+                self.dense(L)
             elif self.fused:
                 quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages, self.scale,
                                   k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out, page_size=self.page_size,

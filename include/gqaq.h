@@ -221,6 +221,31 @@ GQAQ_API int gqa_decode_attn_noalloc(const gqaq_dims *dims, const gqaq_half *q, 
                                      gqaq_half *out, void *stream);
 
 /* Human-readable name of a gqaq_status value (static string). */
+/* The 8-bit KV-cache variant ([QUEST] names lower-precision KV caches, after
+ * the cache update path, as the next step; the pages fix no format, so this
+ * is the plainest one). k_cache / v_cache are [B][Hkv][Lmax][D] bytes of
+ * E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, largest finite 448) with one fp32 scale per tensor: a key
+ * channel's value is k_scale * value(code), likewise for values.
+ *
+ * gqa_decode_attn over such a cache: [OPT] section 3's folded dense attention
+ * with the keys and values dequantized on load (exactly, to fp16, then fp32
+ * accumulation). Same arguments, layouts, workspace (and its zero-fill rule)
+ * and results as gqa_decode_attn otherwise. D in {64, 128}. */
+GQAQ_API int gqa_decode_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_cache,
+                                  const uint8_t *v_cache, float k_scale, float v_scale,
+                                  const int32_t *valid_len, float scale, gqaq_half *out, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* Append one token per (sequence, KV head) to an E4M3 cache: row pos[b] of
+ * k_cache[b][kv] becomes the codes of k_new[b][kv] ([B][Hkv][D] fp16), each
+ * RNE-satfinite(fp32(k) * k_inv_scale): the nearest E4M3 value, ties to the
+ * even code, magnitudes beyond 448 saturated; likewise v with v_inv_scale.
+ * pos[b] outside [0, Lmax) is skipped and raises GQAQ_DEV_BAD_POS. */
+GQAQ_API int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_cache, const gqaq_half *k_new,
+                            const gqaq_half *v_new, const int32_t *pos, float k_inv_scale, float v_inv_scale,
+                            void *stream);
+
 GQAQ_API const char *gqaq_status_string(int status);
 
 /* Library options (process-wide, read at launch time). */

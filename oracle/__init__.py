@@ -56,6 +56,11 @@ def _load():
         lib.oracle_f16_to_f64.restype = dbl
         lib.oracle_f16_array_to_f64.argtypes = [_up, _dp, i64]
         lib.oracle_f16_array_to_f64.restype = None
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_e4m3_array_to_f64.argtypes = [u8p, _dp, i64]
+        lib.oracle_e4m3_array_to_f64.restype = None
+        lib.oracle_f32_array_to_e4m3.argtypes = [ctypes.POINTER(ctypes.c_float), u8p, i64]
+        lib.oracle_f32_array_to_e4m3.restype = None
         for name in ("oracle_attn_repeat_kv", "oracle_attn_folded"):
             fn = getattr(lib, name)
             fn.argtypes = [i32, i32, i32, i64, i64, _dp, _dp, _dp, dbl, _dp]
@@ -101,6 +106,26 @@ def f16_to_f64(a) -> np.ndarray:
     return out
 
 
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Decode E4M3 codes (uint8) to float64 (the fp8 KV-cache variant)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_array_to_f64(c.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), _dptr(out), c.size)
+    return out
+
+
+def quantize_e4m3(x, inv_scale: float) -> np.ndarray:
+    """E4M3 codes of fp16 values x: round(fp32(x) * fp32(inv_scale)) to the
+    nearest E4M3 value (ties to even), magnitudes above 448 saturated. The
+    product is taken in fp32, as the GPU takes it, so both sides round the
+    same value."""
+    y = np.ascontiguousarray(_as_f64(x).astype(np.float32) * np.float32(inv_scale), dtype=np.float32)
+    out = np.empty(y.shape, dtype=np.uint8)
+    _load().oracle_f32_array_to_e4m3(y.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                     out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), y.size)
+    return out
+
+
 def _as_f64(a) -> np.ndarray:
     a = np.asarray(a)
     if a.dtype == np.float16:
@@ -132,6 +157,14 @@ def attn_repeat_kv(q, k, v, valid_len, scale):
     q [B,Hq,D], k/v [B,Hkv,Lmax,D] (fp16 or fp64), valid_len [B] -> [B,Hq,D] fp64.
     """
     return _attn("oracle_attn_repeat_kv", q, k, v, valid_len, scale)
+
+
+def attn_e4m3(q, k_codes, v_codes, k_scale: float, v_scale: float, valid_len, scale):
+    """fp64 decode attention over an E4M3 KV cache: keys and values are the
+    decoded codes times their per-tensor scales; then as attn_repeat_kv."""
+    k = e4m3_to_f64(k_codes) * float(k_scale)
+    v = e4m3_to_f64(v_codes) * float(v_scale)
+    return attn_repeat_kv(q, k, v, valid_len, scale)
 
 
 def attn_folded(q, k, v, valid_len, scale):

@@ -53,6 +53,50 @@ double oracle_f16_to_f64(uint16_t h)
     return sign ? -v : v;
 }
 
+/* 8-bit floating point E4M3 (the fp8 KV-cache variant): 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; no infinities, and the codes
+ * S.1111.111 are NaN. Normal codes are (8 + m) * 2^(e - 10), subnormal ones
+ * (e = 0) m * 2^-9; the largest finite magnitude is 448. */
+double oracle_e4m3_to_f64(uint8_t code)
+{
+    const int sgn = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = (e == 0) ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return sgn ? -v : v;
+}
+
+/* fp32 value -> E4M3 code: the nearest of the 127 non-negative finite
+ * magnitudes (ties to the even code, i.e. the even mantissa), sign kept;
+ * magnitudes above 448 saturate to 448 ("satfinite"); NaN -> 0x7F. */
+uint8_t oracle_f32_to_e4m3(float y)
+{
+    if (isnan(y)) return 0x7F;
+    const int sgn = signbit(y) ? 1 : 0;
+    const double a = fabs((double)y);
+    int best = 0x7E;
+    if (a <= 448.0) {
+        double best_err = INFINITY;
+        for (int c = 0; c <= 0x7E; ++c) {
+            const double err = fabs(a - oracle_e4m3_to_f64((uint8_t)c));
+            if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) != 0)) {
+                best_err = err;
+                best = c;
+            }
+        }
+    }
+    return (uint8_t)((sgn << 7) | best);
+}
+
+void oracle_e4m3_array_to_f64(const uint8_t *src, double *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = oracle_e4m3_to_f64(src[i]);
+}
+
+void oracle_f32_array_to_e4m3(const float *src, uint8_t *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = oracle_f32_to_e4m3(src[i]);
+}
+
 void oracle_f16_array_to_f64(const uint16_t *src, double *dst, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)

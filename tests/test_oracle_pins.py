@@ -279,3 +279,79 @@ def test_repeat_kv_storage_and_byte_counts(golden_dir):
     q = torch.zeros(*g["q_decode_shape"], dtype=torch.float16)
     assert q.numel() * 2 == g["q_decode_bytes"]
     assert q.reshape(1, 8, 4, 64).data_ptr() == q.data_ptr()              # the fold is a view
+
+
+# ---------------------------------------------------------------------------
+# E4M3 (the 8-bit KV-cache variant): decoding, quantization, attention
+# ---------------------------------------------------------------------------
+def test_e4m3_decoder_all_codes_against_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF]                 # the only NaNs: S.1111.111
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_e4m3_decoder_closed_forms():
+    v = oracle.e4m3_to_f64(np.array([0x38, 0x7E, 0x08, 0x07, 0x01, 0x80, 0xB8, 0x3C], dtype=np.uint8))
+    # 1.0 = 2^(7-7); 448 = 1.75 * 2^8; 2^-6 smallest normal; 7 * 2^-9 largest subnormal
+    assert list(v[:5]) == [1.0, 448.0, 2.0 ** -6, 7 * 2.0 ** -9, 2.0 ** -9]
+    assert v[5] == 0.0 and np.signbit(v[5])                           # negative zero
+    assert v[6] == -1.0 and v[7] == 1.5
+    pos = oracle.e4m3_to_f64(np.arange(0, 127, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)                                   # codes 0..126 increase
+
+
+def test_e4m3_quantize_against_torch_in_range():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(200_000) * 60).astype(np.float16)
+    x = x[np.abs(x.astype(np.float64)) * 1.5 < 448]
+    codes = oracle.quantize_e4m3(x, 1.5)
+    ref = (torch.from_numpy(x).float() * 1.5).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+
+
+def test_e4m3_quantize_ties_and_saturation():
+    x = np.array([1.0, 1.0625, 1.1875, 448, 470, 1000, -1000, 2.0 ** -10, 1.5 * 2.0 ** -9, 0.0, -0.0],
+                 dtype=np.float16)
+    codes = oracle.quantize_e4m3(x, 1.0)
+    # 1.0625 halfway between 1.0 (56) and 1.125 (57) -> even 56; 1.1875 between 57 and 58 -> 58;
+    # above 448 saturates to 448 (126 / 254); 2^-10 halfway between 0 and 2^-9 -> 0;
+    # 1.5 * 2^-9 halfway between codes 1 and 2 -> 2; signed zeros keep their sign bit
+    assert list(codes) == [56, 56, 58, 126, 126, 126, 254, 0, 2, 0, 128]
+
+
+def test_e4m3_quantize_then_decode_is_nearest():
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal(5000) * 40).astype(np.float16)
+    codes = oracle.quantize_e4m3(x, 2.0)
+    grid = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    grid = grid[np.isfinite(grid)]
+    y = x.astype(np.float64) * 2.0
+    err = np.abs(oracle.e4m3_to_f64(codes) - np.clip(y, -448, 448))
+    best = np.min(np.abs(grid[None, :] - np.clip(y, -448, 448)[:, None]), axis=1)
+    assert np.array_equal(err, best)
+
+
+def test_attn_e4m3_matches_sdpa_on_torch_dequantized_cache():
+    rng = np.random.default_rng(13)
+    B, Hkv, G, D, Lmax = 2, 2, 4, 64, 40
+    q = rand_f16(B, Hkv * G, D, rng=rng)
+    kc = rng.integers(0, 256, size=(B, Hkv, Lmax, D), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x38                                    # no NaN codes in a cache
+    vc = rng.integers(0, 256, size=(B, Hkv, Lmax, D), dtype=np.uint8)
+    vc[(vc & 0x7F) == 0x7F] = 0x30
+    vl = [Lmax, 17]
+    ks, vs, scale = 0.01, 0.02, 0.125
+    got = oracle.attn_e4m3(q, kc, vc, ks, vs, vl, scale)
+    k = torch.from_numpy(kc).view(torch.float8_e4m3fn).to(torch.float64) * ks
+    v = torch.from_numpy(vc).view(torch.float8_e4m3fn).to(torch.float64) * vs
+    qt = torch.from_numpy(q.astype(np.float64))
+    for b in range(B):
+        L = vl[b]
+        kk = k[b, :, :L].repeat_interleave(G, dim=0)
+        vv = v[b, :, :L].repeat_interleave(G, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt[b][:, None, :], kk, vv, scale=scale)[:, 0]
+        assert np.allclose(got[b], ref.numpy(), rtol=0, atol=1e-12)
