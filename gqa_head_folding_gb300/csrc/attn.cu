@@ -16,12 +16,13 @@
 //  - work tiles: 128 consecutive tokens (dense) or 128 / max(S, 16) selected
 //    pages of S tokens (sparse) of one (sequence, KV head) unit. The tiles of all units
 //    are split into equal contiguous ranges, one per CTA (balanced split).
-//  - warp 8 (producer): TMA 2-D tile loads of K (128-byte swizzled) and V
-//    into a 2-3 stage shared-memory ring, with mbarrier completion.
-//  - warps 0-7 (consumers): warp w owns 16 tokens of each tile. Two lanes share
-//    a token for q.k (each covers D/2 channels with fp16 x fp16 -> fp32
-//    FMAs), then online softmax in the log2 domain. For p @ V, lane l owns D/32
-//    output channels of all G rows.
+//  - warp 8 (producer): TMA tile loads of K and V (both 128-byte swizzled;
+//    the E4M3 cache's byte rows 64- or 128-byte swizzled) into a shared-memory
+//    ring of 2-6 stages, with mbarrier completion.
+//  - warps 0-7 (consumers): warp w owns 16 tokens of each tile and runs both
+//    products on the tensor cores (MmaAttn: S^T = K Q^T and O^T += V^T P^T
+//    with mma.sync m16n8k16, the G folded rows on the N = 8 side), with the
+//    online softmax in the log2 domain on the S^T fragments.
 //  - at the end of each unit segment the 8 warp states merge in shared
 //    memory. A segment that covers its whole unit writes the fp16 output. A
 //    segment cut by a range boundary writes an fp32 partial (m, l, acc) and
@@ -30,7 +31,7 @@
 //    output, then sets the counter back to zero for the next call.
 #include <math.h>
 
-#include "attn_tile.cuh"
+#include "attn_mma.cuh"
 #include "internal.h"
 
 namespace gqaq {
@@ -373,8 +374,8 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8
                         if (lane == 0 && ((m >> j) & 1u)) {
                             const int y = row0 + pj * p.S;
                             const uint32_t off = (uint32_t)(j * slots.slot * D * 2);
-                            tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K
-                            tma_load_2d(vdst + off, &vmap, 0, y, fb, pol);
+                            tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K and V
+                            tma_load_3d(vdst + off, &vmap, 0, 0, y, fb, pol);
                         }
                     }
                 } else {
@@ -383,12 +384,14 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8
                         const int y = row0 + local * C::TILE;
                         if (KV8) {
                             tma_load_2d(kdst, &kmap, 0, y, fb, pol);
+                            tma_load_2d(vdst, &vmap, 0, y, fb, pol);
                         } else {
 #pragma unroll
-                            for (int kh = 0; kh < C::KH; ++kh)
+                            for (int kh = 0; kh < C::KH; ++kh) {
                                 tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
+                                tma_load_2d(vdst + kh * C::KBLK, &vmap, 64 * kh, y, fb, pol);
+                            }
                         }
-                        tma_load_2d(vdst, &vmap, 0, y, fb, pol);
                     }
                 }
             }
@@ -414,7 +417,8 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8
     // the arrival counters in step, so the workspace stays reusable.
     // ----------------------------------------------------------------------
     const int tid = threadIdx.x;  // 0..255 among consumers
-    WarpAttn<D, G, SPARSE, KV8> wa;  // sparse stages hold K page-major
+    using WA = MmaAttn<D, G, SPARSE, KV8>;  // sparse stages hold K and V page-major
+    WA wa;
     wa.init(warp, lane, smem_u32(pbuf));
 
     Walk w;
@@ -429,7 +433,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8
         const int P = (len + p.S - 1) / p.S;
         const int nsel = P < p.kpages ? P : p.kpages;
         const __half *qg = p.q + ((int64_t)w.b * Hq + (int64_t)w.kv * G) * D;
-        if (C::QREG) {
+        if (WA::QREG) {
             wa.load_q(qg);
         } else {
             for (int e = tid; e < G * D / 8; e += NCT)
@@ -588,14 +592,16 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
     const uint32_t box_rows = SPARSE ? (uint32_t)dm.page_size : (uint32_t)C::TILE;
     CUtensorMap kmap, vmap;
+    // K and V stages share one layout (the tile reads both through it).
     if (KV8) {  // byte rows: D = 128 rows 128-byte swizzled, D = 64 rows 64-byte swizzled
         if (!encode_tensor_map_u8(&kmap, a.k_cache, rows, D, box_rows, D == 128 ? 128 : 64)) return GQAQ_ERR_CUDA;
-        if (!encode_tensor_map_u8(&vmap, a.v_cache, rows, D, box_rows, 0)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_u8(&vmap, a.v_cache, rows, D, box_rows, D == 128 ? 128 : 64)) return GQAQ_ERR_CUDA;
+    } else if (SPARSE) {
+        if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, box_rows)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_kpage(&vmap, a.v_cache, rows, D, box_rows)) return GQAQ_ERR_CUDA;
     } else {
-        if (SPARSE ? !encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, box_rows)
-                   : !encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true))
-            return GQAQ_ERR_CUDA;
-        if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, box_rows, false)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, 64, box_rows, true)) return GQAQ_ERR_CUDA;
     }
 
     AttnParams p;

@@ -1,0 +1,301 @@
+// attn_mma.cuh -- one consumer warp's share of a decode-attention tile on the
+// tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation).
+//
+// "Core ML Decode Optimization ...", section 3 ("Fold Q Instead of Expanding
+// KV"): the G query rows of one KV head form a [G, D] block that meets every
+// K and V row once. With G <= 8 that block is the N = 8 side of the MMA, and
+// the 16 tokens a warp owns are the M = 16 side, so both products of a tile
+// are tensor-core contractions with no copy of K or V:
+//   S^T [16 tokens x 8 rows] = K [16 x D] . Q^T [D x 8]          (D/16 MMAs)
+//   O^T [D x 8 rows]        += V^T [D x 16 tokens] . P^T [16 x 8] (D/16 MMAs)
+// Softmax runs in the log2 domain on the S^T fragments (each lane holds two
+// query columns of two tokens), P is rounded to fp16 once and turned into the
+// B operand of the second product with movmatrix.trans. Rows G..7 of the N
+// side are zero queries whose results are never stored.
+//
+// fp16 caches: K and V stages share one layout, KH column blocks of 128-byte
+// lines, 128-byte swizzled (dense: [kh][row] blocks of TILE lines; KPAGE:
+// [row][kh], as the page-major 3-D box writes them). ldmatrix brings K
+// fragments and, transposed, V^T fragments.
+// E4M3 caches (KV8): rows of D bytes, swizzled by 128 bytes (D = 128) or 64
+// bytes (D = 64). A lane reads its K bytes as whole 16-byte chunks and
+// decodes them into fragments; the channel order inside the contraction is
+// permuted to match (q uses the same permutation, so q.k is unchanged). V^T
+// fragments pair two tokens' codes with a byte permute before decoding.
+#pragma once
+
+#include "attn_tile.cuh"
+
+namespace gqaq {
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t r;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// d += a (16x16, row) . b (16x8, col), fp16 in, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> fp16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t y, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(y), "r"(sel));
+    return r;
+}
+
+template <int D, int G, bool KPAGE = false, bool KV8 = false>
+struct MmaAttn {
+    using C = TileCfg<D, G>;
+    static_assert(!(KPAGE && KV8), "8-bit stages are dense-only");
+    static constexpr bool QREG = true;   // q fragments live in registers
+    static constexpr int KS = D / 16;    // k-steps of q.k, m-blocks of p @ V
+    int lane, cw, r, c;                  // r = lane / 4 (token / channel row), c = lane % 4 (column pair)
+    uint32_t qb[KS][2];                  // B fragments of Q^T
+    float m[2], l[2];                    // columns 2c, 2c+1: running max (log2 domain), partial sum
+    float o[KS][4];                      // O^T fragments
+
+    // ---- shared-memory addressing ----
+    // fp16 stage: byte address of the 16-byte chunk (row, ch8) (8 channels).
+    __device__ __forceinline__ static uint32_t chunk16(uint32_t base, int row, int ch8) {
+        const int kh = ch8 >> 3, cc = ch8 & 7;
+        if (KPAGE) {
+            const int line = row * C::KH + kh;
+            return base + (uint32_t)(line * 128 + ((cc ^ (line & 7)) << 4));
+        }
+        return base + (uint32_t)(kh * C::KBLK + row * 128 + ((cc ^ (row & 7)) << 4));
+    }
+    // E4M3 stage: byte address of logical byte `byte` (a multiple of 8) of row `row`.
+    __device__ __forceinline__ static uint32_t byte8(uint32_t base, int row, int byte) {
+        if (D == 128) return base + (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15));
+        return base + (uint32_t)(row * 64 + ((((byte >> 4) ^ ((row >> 1) & 3))) << 4) + (byte & 15));
+    }
+
+    __device__ __forceinline__ void init(int warp, int lane_, uint32_t /*pbuf_base*/) {
+        lane = lane_;
+        cw = warp;
+        r = lane >> 2;
+        c = lane & 3;
+    }
+
+    __device__ __forceinline__ void reset() {
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+
+    // B fragments of Q^T for the unit's [G][D] block (row n = r; rows >= G are zero).
+    // fp16 stages: k-step j covers channels 16j .. 16j+15 in natural order.
+    // E4M3 stages: k-step j of column pair c covers channels (D/4) c + 4j .. +3.
+    __device__ __forceinline__ void load_q(const __half *qg) {
+        const bool live = r < G;
+        const __half *qrow = qg + (live ? r : 0) * D;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+            if (KV8) {
+                const uint2 x = live ? *reinterpret_cast<const uint2 *>(qrow + (D / 4) * c + 4 * j) : make_uint2(0u, 0u);
+                qb[j][0] = x.x;
+                qb[j][1] = x.y;
+            } else {
+                qb[j][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * j + 2 * c) : 0u;
+                qb[j][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * j + 8 + 2 * c) : 0u;
+            }
+        }
+    }
+
+    // One 16-token sub-tile. kbase/vbase: shared addresses of the stage's K and
+    // V; nvalid: valid tokens (a prefix) of this warp's 16 rows, 1..16.
+    __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, float scale_log2,
+                                         const __half * /*q_s*/) {
+        const int row0 = cw * C::SUB;
+        // ---- 1. S^T = K . Q^T ----
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        if (KV8) {
+            constexpr int BPL = D / 4;  // bytes of a row this lane decodes
+            uint4 ka[BPL / 16], kb[BPL / 16];
+#pragma unroll
+            for (int h = 0; h < BPL / 16; ++h) {
+                ka[h] = lds128(byte8(kbase, row0 + r, BPL * c + 16 * h));
+                kb[h] = lds128(byte8(kbase, row0 + r + 8, BPL * c + 16 * h));
+            }
+#pragma unroll
+            for (int j = 0; j < KS; ++j) {
+                const uint4 &xa = ka[j >> 2], &xb = kb[j >> 2];
+                const uint32_t wa = (j & 3) == 0 ? xa.x : (j & 3) == 1 ? xa.y : (j & 3) == 2 ? xa.z : xa.w;
+                const uint32_t wb = (j & 3) == 0 ? xb.x : (j & 3) == 1 ? xb.y : (j & 3) == 2 ? xb.z : xb.w;
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(wa & 0xffffu);
+                a[1] = e4m3x2_to_f16x2(wb & 0xffffu);
+                a[2] = e4m3x2_to_f16x2(wa >> 16);
+                a[3] = e4m3x2_to_f16x2(wb >> 16);
+                mma_16816(s, a, qb[j][0], qb[j][1]);
+            }
+        } else {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int krow = row0 + (mi & 1) * 8 + rr;
+#pragma unroll
+            for (int j = 0; j < KS; ++j) {
+                uint32_t a[4];
+                ldsm_x4(chunk16(kbase, krow, 2 * j + (mi >> 1)), a);
+                mma_16816(s, a, qb[j][0], qb[j][1]);
+            }
+        }
+        // ---- 2. online softmax per query column (log2 domain) ----
+        // s[0], s[1]: token r, columns 2c, 2c+1; s[2], s[3]: token r + 8.
+        const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+        float x[4];
+        x[0] = v0 ? s[0] * scale_log2 : -INFINITY;
+        x[1] = v0 ? s[1] * scale_log2 : -INFINITY;
+        x[2] = v1 ? s[2] * scale_log2 : -INFINITY;
+        x[3] = v1 ? s[3] * scale_log2 : -INFINITY;
+        float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o_));
+            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o_));
+        }
+        const float mn0 = fmaxf(m[0], t0), mn1 = fmaxf(m[1], t1);  // token 0 is valid: finite
+        const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
+        m[0] = mn0;
+        m[1] = mn1;
+        const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
+        const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
+        l[0] = l[0] * al0 + (p0 + p2);
+        l[1] = l[1] * al1 + (p1 + p3);
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                o[i][0] *= al0;
+                o[i][1] *= al1;
+                o[i][2] *= al0;
+                o[i][3] *= al1;
+            }
+        }
+        // ---- 3. P^T as the B operand: fp16, transposed 8x8 halves ----
+        const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // tokens 2c, 2c+1 of column r
+        const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // tokens 8+2c, 8+2c+1
+        // Rows past nvalid may hold anything (even NaN codes): their V^T
+        // entries are zeroed, since 0 * NaN would poison the sum.
+        const bool partial = nvalid < C::SUB;  // warp-uniform
+        const uint32_t mk0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t mk1 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
+        // ---- 4. O^T += V^T . P^T ----
+        if (KV8) {
+            constexpr int BPL = D / 8;  // bytes of a token row this lane reads (channels BPL r ..)
+            uint32_t w[4][BPL / 4];     // tokens 2c, 2c+1, 2c+8, 2c+9
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int row = row0 + 2 * c + (t & 1) + (t >> 1) * 8;
+                if constexpr (BPL == 16) {
+                    const uint4 v = lds128(byte8(vbase, row, BPL * r));
+                    w[t][0] = v.x;
+                    w[t][1] = v.y;
+                    w[t][2 % (BPL / 4)] = v.z;
+                    w[t][3 % (BPL / 4)] = v.w;
+                } else {
+                    const uint2 v = lds64(byte8(vbase, row, BPL * r));
+                    w[t][0] = v.x;
+                    w[t][1 % (BPL / 4)] = v.y;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                // m-block i: row r <-> channel BPL r + 2i, row r + 8 <-> BPL r + 2i + 1
+                const int wd = i >> 1;
+                const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                const uint32_t lo = byte_perm(w[0][wd], w[1][wd], sel);  // tokens 2c, 2c+1
+                const uint32_t hi = byte_perm(w[2][wd], w[3][wd], sel);  // tokens 2c+8, 2c+9
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(lo & 0xffffu);
+                a[1] = e4m3x2_to_f16x2(lo >> 16);
+                a[2] = e4m3x2_to_f16x2(hi & 0xffffu);
+                a[3] = e4m3x2_to_f16x2(hi >> 16);
+                if (partial) mask_tokens(a, mk0, mk1);
+                mma_16816(o[i], a, pb0, pb1);
+            }
+        } else {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int vrow = row0 + (mi >> 1) * 8 + rr;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                uint32_t a[4];
+                ldsm_x4_trans(chunk16(vbase, vrow, 2 * i + (mi & 1)), a);
+                if (partial) mask_tokens(a, mk0, mk1);
+                mma_16816(o[i], a, pb0, pb1);
+            }
+        }
+    }
+
+    // V^T fragment: reg 0, 1 hold tokens 2c, 2c+1; reg 2, 3 tokens 2c+8, 2c+9.
+    static __device__ __forceinline__ void mask_tokens(uint32_t (&a)[4], uint32_t mk0, uint32_t mk1) {
+        a[0] &= mk0;
+        a[1] &= mk0;
+        a[2] &= mk1;
+        a[3] &= mk1;
+    }
+
+    // Output channel of O^T fragment element (m-block i, upper half h).
+    __device__ __forceinline__ int out_channel(int i, int h) const {
+        if (KV8) return (D / 8) * r + 2 * i + h;
+        return 16 * i + r + 8 * h;
+    }
+
+    // Write this warp's state to its slot of the merge buffer [NCW][G][D+2]:
+    // (m, l, acc[D]) per row; l is summed over the 8 token rows first.
+    __device__ __forceinline__ void store_state(float *merge) {
+        float *mw = merge + cw * G * (D + 2);
+        float ls0 = l[0], ls1 = l[1];
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+            ls0 += __shfl_xor_sync(0xffffffffu, ls0, o_);
+            ls1 += __shfl_xor_sync(0xffffffffu, ls1, o_);
+        }
+        const int q0 = 2 * c, q1 = 2 * c + 1;
+        if (r == 0) {
+            if (q0 < G) {
+                mw[q0 * (D + 2)] = m[0];
+                mw[q0 * (D + 2) + 1] = ls0;
+            }
+            if (q1 < G) {
+                mw[q1 * (D + 2)] = m[1];
+                mw[q1 * (D + 2) + 1] = ls1;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ch = out_channel(i, h);
+                if (q0 < G) mw[q0 * (D + 2) + 2 + ch] = o[i][2 * h];
+                if (q1 < G) mw[q1 * (D + 2) + 2 + ch] = o[i][2 * h + 1];
+            }
+        }
+    }
+};
+
+}  // namespace gqaq
