@@ -65,6 +65,8 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [i32, i32, i32, i64, i64, _dp, _dp, _dp, dbl, _dp]
             fn.restype = i32
+        lib.oracle_prefill_repeat_kv.argtypes = [i32, i32, i32, i64, i32, i64, _dp, _dp, _dp, dbl, _dp]
+        lib.oracle_prefill_repeat_kv.restype = i32
         lib.oracle_page_minmax.argtypes = [i32, i32, i64, i64, i32, _dp, _dp]
         lib.oracle_page_minmax.restype = i32
         lib.oracle_page_scores.argtypes = [i32, i32, i32, i64, i64, _dp, _dp, _dp]
@@ -165,6 +167,28 @@ def attn_e4m3(q, k_codes, v_codes, k_scale: float, v_scale: float, valid_len, sc
     k = e4m3_to_f64(k_codes) * float(k_scale)
     v = e4m3_to_f64(v_codes) * float(v_scale)
     return attn_repeat_kv(q, k, v, valid_len, scale)
+
+
+def prefill_attn(q, k, v, start, scale):
+    """fp64 causal attention of a chunk of q_len new tokens per sequence
+    ("Prefill Needs Separate Design": the group axis merged into the sequence
+    axis, each row with its own mask), explicit repeat_kv.
+
+    q [B,Hq,q_len,D]; k/v [B,Hkv,Lmax,D] already holding the chunk at rows
+    start[b] .. start[b]+q_len-1; token t attends to rows 0 .. start[b]+t.
+    Returns [B,Hq,q_len,D] fp64."""
+    q = np.asarray(q); k = np.asarray(k); v = np.asarray(v)
+    B, Hq, q_len, D = q.shape
+    _, Hkv, Lmax, _ = k.shape
+    out = np.empty((B, Hq, q_len, D), dtype=np.float64)
+    lib = _load()
+    for b in range(B):
+        qb, kb, vb = _as_f64(q[b]), _as_f64(k[b]), _as_f64(v[b])
+        ob = np.empty((Hq, q_len, D), dtype=np.float64)
+        _check(lib.oracle_prefill_repeat_kv(Hq, Hkv, D, Lmax, q_len, int(start[b]), _dptr(qb), _dptr(kb), _dptr(vb),
+                                            float(scale), _dptr(ob)), "oracle_prefill_repeat_kv")
+        out[b] = ob
+    return out
 
 
 def attn_folded(q, k, v, valid_len, scale):

@@ -164,6 +164,42 @@ int oracle_attn_repeat_kv(int hq, int hkv, int d, int64_t lmax, int64_t l,
 }
 
 /* ------------------------------------------------------------------------ */
+/* [OPT] "Prefill Needs Separate Design": with q_len > 1 new tokens the      */
+/* group axis is merged into the sequence axis, and each row keeps its own   */
+/* causal mask.  Plain definition, explicit repeat_kv: the chunk's tokens    */
+/* sit at cache rows start .. start+q_len-1, and token t of query head h     */
+/* attends to cache rows 0 .. start+t of KV head h / G.                      */
+/*   q, out [Hq][q_len][D];  k, v [Hkv][Lmax][D]                             */
+/* ------------------------------------------------------------------------ */
+int oracle_prefill_repeat_kv(int hq, int hkv, int d, int64_t lmax, int q_len, int64_t start,
+                             const double *q, const double *k, const double *v,
+                             double scale, double *out)
+{
+    if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || q_len <= 0 || start < 0 || start + q_len > lmax)
+        return -1;
+    int group = hq / hkv;
+    int64_t l = start + q_len;
+    double *krep = (double *)malloc(sizeof(double) * (size_t)(l * d));
+    double *vrep = (double *)malloc(sizeof(double) * (size_t)(l * d));
+    double *s = (double *)malloc(sizeof(double) * (size_t)l);
+    if (!krep || !vrep || !s) {
+        free(krep); free(vrep); free(s);
+        return -1;
+    }
+    for (int h = 0; h < hq; ++h) {
+        int kv = h / group;                 /* repeat_kv order: h = G*kv + g */
+        memcpy(krep, k + (int64_t)kv * lmax * d, sizeof(double) * (size_t)(l * d));
+        memcpy(vrep, v + (int64_t)kv * lmax * d, sizeof(double) * (size_t)(l * d));
+        for (int t = 0; t < q_len; ++t) {
+            const int64_t off = ((int64_t)h * q_len + t) * d;
+            attend_rows(d, start + t + 1, q + off, krep, vrep, scale, s, out + off);
+        }
+    }
+    free(krep); free(vrep); free(s);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* [OPT] section 3: the folded form.  Q [Hq][D] is read as [Hkv][G][D]       */
 /* (a reshape, no copy) and each KV head is read in place for its G rows.    */
 /* Same arithmetic per row as the repeat_kv form, so the two agree bit for   */

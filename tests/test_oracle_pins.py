@@ -355,3 +355,60 @@ def test_attn_e4m3_matches_sdpa_on_torch_dequantized_cache():
         vv = v[b, :, :L].repeat_interleave(G, dim=0)
         ref = torch.nn.functional.scaled_dot_product_attention(qt[b][:, None, :], kk, vv, scale=scale)[:, 0]
         assert np.allclose(got[b], ref.numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Prefill (q_len > 1): causal attention of a chunk, group axis merged into rows
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("G,q_len,start", [(1, 5, 0), (4, 7, 0), (2, 9, 13), (8, 3, 30)])
+def test_prefill_matches_sdpa_causal(G, q_len, start):
+    rng = np.random.default_rng(G * 100 + q_len)
+    B, Hkv, D, Lmax = 2, 2, 32, 48
+    q = rand_f16(B, Hkv * G, q_len, D, rng=rng)
+    k = rand_f16(B, Hkv, Lmax, D, rng=rng)
+    v = rand_f16(B, Hkv, Lmax, D, rng=rng)
+    st = [start, max(0, start - 3)]
+    got = oracle.prefill_attn(q, k, v, st, 0.2)
+    for b in range(B):
+        L = st[b] + q_len
+        kk = torch.from_numpy(k[b, :, :L].astype(np.float64)).repeat_interleave(G, dim=0)
+        vv = torch.from_numpy(v[b, :, :L].astype(np.float64)).repeat_interleave(G, dim=0)
+        # row t sees cache rows <= start + t: a bottom-right-aligned causal mask
+        mask = torch.arange(L)[None, :] <= (st[b] + torch.arange(q_len))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[b].astype(np.float64)), kk, vv, attn_mask=mask, scale=0.2)
+        assert np.allclose(got[b], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_from_zero_equals_is_causal():
+    rng = np.random.default_rng(5)
+    G, q_len, D = 4, 12, 16
+    q = rand_f16(1, 2 * G, q_len, D, rng=rng)
+    k = rand_f16(1, 2, q_len, D, rng=rng)
+    v = rand_f16(1, 2, q_len, D, rng=rng)
+    got = oracle.prefill_attn(q, k, v, [0], 0.25)[0]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q[0].astype(np.float64)),
+        torch.from_numpy(k[0].astype(np.float64)).repeat_interleave(G, dim=0),
+        torch.from_numpy(v[0].astype(np.float64)).repeat_interleave(G, dim=0), is_causal=True, scale=0.25)
+    assert np.allclose(got, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_one_token_is_decode():
+    rng = np.random.default_rng(6)
+    q = rand_f16(2, 8, 1, 64, rng=rng)
+    k = rand_f16(2, 2, 30, 64, rng=rng)
+    v = rand_f16(2, 2, 30, 64, rng=rng)
+    st = [29, 11]
+    got = oracle.prefill_attn(q, k, v, st, 0.125)[:, :, 0]
+    ref = oracle.attn_repeat_kv(q[:, :, 0], k, v, [s + 1 for s in st], 0.125)
+    assert np.array_equal(got, ref)
+
+
+def test_prefill_first_row_sees_one_token():
+    rng = np.random.default_rng(7)
+    q = rand_f16(1, 2, 4, 16, rng=rng)
+    k = rand_f16(1, 1, 4, 16, rng=rng)
+    v = rand_f16(1, 1, 4, 16, rng=rng)
+    got = oracle.prefill_attn(q, k, v, [0], 0.5)
+    assert np.array_equal(got[0, :, 0], np.repeat(v[0, :, 0].astype(np.float64), 2, axis=0))
