@@ -42,6 +42,7 @@ GQAQ_OPT_TEST_STALL = 3
 GQAQ_OPT_CLUSTER_SIZE = 4
 GQAQ_OPT_PDL = 5
 GQAQ_OPT_QUEST_KERNEL = 6
+GQAQ_OPT_PREFILL_SPLITS = 7
 
 PAGE_SIZE = 16
 
@@ -62,6 +63,7 @@ class Dims(ctypes.Structure):
 EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_update_meta",
            "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "quest_decode_attn",
            "gqa_decode_attn_noalloc", "gqa_decode_attn_e4m3", "kv_append_e4m3",
+           "gqaq_prefill_workspace_bytes", "gqa_prefill_attn",
            "gqaq_status_string", "gqaq_set_option", "gqaq_device_status", "gqaq_version")
 
 _lib = None
@@ -91,13 +93,16 @@ def lib():
         f32 = ctypes.c_float
         L.gqa_decode_attn_e4m3.argtypes = [dp, vp, vp, vp, f32, f32, vp, f32, vp, vp, ctypes.c_size_t, vp]
         L.kv_append_e4m3.argtypes = [dp, vp, vp, vp, vp, vp, f32, f32, vp]
+        L.gqaq_prefill_workspace_bytes.argtypes = [dp, i32]
+        L.gqaq_prefill_workspace_bytes.restype = ctypes.c_size_t
+        L.gqa_prefill_attn.argtypes = [dp, i32, vp, vp, vp, vp, f32, vp, vp, ctypes.c_size_t, vp]
         L.gqaq_status_string.argtypes = [i32]
         L.gqaq_status_string.restype = ctypes.c_char_p
         L.gqaq_set_option.argtypes = [i32, ctypes.c_int64]
         L.gqaq_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
         L.gqaq_version.argtypes = []
         for name in EXPORTS:
-            if name not in ("gqaq_workspace_bytes", "gqaq_status_string"):
+            if name not in ("gqaq_workspace_bytes", "gqaq_status_string", "gqaq_prefill_workspace_bytes"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -282,6 +287,41 @@ def kv_append_e4m3(k_cache, v_cache, k_new, v_new, pos, k_inv_scale: float, v_in
     _check("kv_append_e4m3", lib().kv_append_e4m3(
         ctypes.byref(d), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos), float(k_inv_scale),
         float(v_inv_scale), _stream(k_cache)))
+
+
+def prefill_workspace_bytes(dims: Dims, q_len: int) -> int:
+    n = lib().gqaq_prefill_workspace_bytes(ctypes.byref(dims), int(q_len))
+    if n == 0:
+        raise GqaqError("gqaq_prefill_workspace_bytes", GQAQ_ERR_UNSUPPORTED, "dims rejected")
+    return int(n)
+
+
+def alloc_prefill_workspace(dims: Dims, q_len: int, device) -> torch.Tensor:
+    """Zero-filled workspace for gqa_prefill_attn (its counters stay zero between calls)."""
+    return torch.zeros(prefill_workspace_bytes(dims, q_len), dtype=torch.uint8, device=device)
+
+
+def gqa_prefill_attn(q, k_cache, v_cache, start, scale: float, out=None, workspace=None):
+    """Causal attention of a chunk: q [B,Hq,q_len,D], caches [B,Hkv,Lmax,D]
+    holding the chunk at rows start[b] .. start[b]+q_len-1; token t attends to
+    rows 0 .. start[b]+t. The G heads and q_len tokens of a KV head are one
+    folded row block."""
+    _need(q, "q", torch.float16, 4)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(start, "start", torch.int32, 1)
+    B, Hq, q_len, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    d = make_dims(B, Hq, Hkv, D, Lmax)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 4)
+    if workspace is None:
+        workspace = alloc_prefill_workspace(d, q_len, q.device)
+    _check("gqa_prefill_attn", lib().gqa_prefill_attn(
+        ctypes.byref(d), int(q_len), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(start), float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(q)))
+    return out
 
 
 def quest_append_kv(k_cache, v_cache, meta, k_new, v_new, pos, page_size: int = PAGE_SIZE):

@@ -25,6 +25,7 @@ std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cluster_size{0};
 std::atomic<int64_t> g_opt_pdl{1};
 std::atomic<int64_t> g_opt_quest_kernel{0};
+std::atomic<int64_t> g_opt_prefill_splits{0};
 
 struct DeviceState {
     bool ready = false;
@@ -74,6 +75,7 @@ int make_ctx(LaunchCtx *ctx, void *stream) {
     ctx->cluster_size = (int)g_opt_cluster_size.load();
     ctx->pdl = (int)g_opt_pdl.load();
     ctx->quest_kernel = (int)g_opt_quest_kernel.load();
+    ctx->prefill_splits = (int)g_opt_prefill_splits.load();
     ctx->status = s->status;
     return GQAQ_OK;
 }
@@ -188,6 +190,10 @@ int gqaq_set_option(int option, int64_t value) {
         case GQAQ_OPT_QUEST_KERNEL:
             if (value < 0 || value > 2) return GQAQ_ERR_INVALID_ARG;
             g_opt_quest_kernel.store(value);
+            return GQAQ_OK;
+        case GQAQ_OPT_PREFILL_SPLITS:
+            if (value < 0 || value > kPrefillMaxSplits) return GQAQ_ERR_INVALID_ARG;
+            g_opt_prefill_splits.store(value);
             return GQAQ_OK;
         case GQAQ_OPT_CLUSTER_SIZE:
             if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return GQAQ_ERR_INVALID_ARG;
@@ -400,6 +406,50 @@ int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_cache, co
     if (rc != GQAQ_OK) return rc;
     return launch_append_e4m3(dims, k_cache, v_cache, reinterpret_cast<const __half *>(k_new),
                               reinterpret_cast<const __half *>(v_new), pos, k_inv_scale, v_inv_scale, ctx);
+}
+
+namespace {
+int check_prefill(const gqaq_dims *dims, int q_len) {
+    const int rc = check_dims(dims, false);
+    if (rc != GQAQ_OK) return rc;
+    if (q_len < 1 || q_len > dims->max_len) return GQAQ_ERR_INVALID_ARG;
+    const int64_t qrows = (int64_t)dims->batch * dims->num_q_heads * q_len;
+    if (qrows > (int64_t)INT32_MAX / 128) return GQAQ_ERR_UNSUPPORTED;
+    return GQAQ_OK;
+}
+}  // namespace
+
+size_t gqaq_prefill_workspace_bytes(const gqaq_dims *dims, int q_len) {
+    if (check_prefill(dims, q_len) != GQAQ_OK) return 0;
+    LaunchCtx ctx;
+    if (make_ctx(&ctx, nullptr) != GQAQ_OK) return 0;
+    return prefill_workspace_bytes(dims, q_len, ctx);
+}
+
+int gqa_prefill_attn(const gqaq_dims *dims, int q_len, const gqaq_half *q, const gqaq_half *k_cache,
+                     const gqaq_half *v_cache, const int32_t *start, float scale, gqaq_half *out, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    int rc = check_prefill(dims, q_len);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(start))
+        return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return GQAQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace)) return GQAQ_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    PrefillArgs a;
+    a.dims = dims;
+    a.q_len = q_len;
+    a.q = reinterpret_cast<const __half *>(q);
+    a.k_cache = reinterpret_cast<const __half *>(k_cache);
+    a.v_cache = reinterpret_cast<const __half *>(v_cache);
+    a.start = start;
+    a.scale = scale;
+    a.out = reinterpret_cast<__half *>(out);
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launch_prefill(a, ctx);
 }
 
 int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_half *k_cache, gqaq_half *v_cache,

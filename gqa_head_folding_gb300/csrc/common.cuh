@@ -27,6 +27,7 @@ struct LaunchCtx {
     int cluster_size;      // fused Quest kernel: forced CTAs per cluster, 0 = automatic
     int pdl;               // launch with programmatic stream serialization
     int quest_kernel;      // fused Quest kernel: 0 automatic, 1 cluster, 2 work queue
+    int prefill_splits;    // prefill context splits per item: 0 automatic, n forced
     int *status;           // device status word
 };
 

@@ -49,6 +49,28 @@ int launch_append_e4m3(const gqaq_dims *d, uint8_t *k_cache, uint8_t *v_cache, c
                        const LaunchCtx &ctx);
 size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx);
 
+// Causal chunk attention (prefill.cu): q_len new tokens per sequence, the
+// group axis merged into the row axis. Work items are (sequence, KV head,
+// block of 128 merged rows); each is split into up to kPrefillMaxSplits
+// context slices merged in-kernel. Workspace: arrival counters [items] u32
+// (zero region, 256-byte rounded), then fp32 partials when split.
+constexpr int kPrefillMaxSplits = 32;
+struct PrefillArgs {
+    const gqaq_dims *dims;
+    int q_len;
+    const __half *q;        // [B][Hq][q_len][D]
+    const __half *k_cache;  // [B][Hkv][Lmax][D]
+    const __half *v_cache;
+    const int *start;       // [B]: cache row of the chunk's first token
+    float scale;
+    __half *out;            // [B][Hq][q_len][D]
+    void *workspace;
+    size_t workspace_bytes;
+};
+int64_t prefill_items(const gqaq_dims &dm, int q_len);
+int launch_prefill(const PrefillArgs &a, const LaunchCtx &ctx);
+size_t prefill_workspace_bytes(const gqaq_dims *dims, int q_len, const LaunchCtx &ctx);
+
 // Fused Quest step (quest_fused.cu). meta == nullptr selects attention over a
 // given page list (page_idx is then an input); otherwise append (pos may be
 // null), score, select and attend, with scores/page_idx optional outputs.

@@ -246,6 +246,30 @@ GQAQ_API int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_
                             const gqaq_half *v_new, const int32_t *pos, float k_inv_scale, float v_inv_scale,
                             void *stream);
 
+/* Prefill: causal attention of a chunk of q_len new tokens per sequence
+ * ([OPT] "Prefill Needs Separate Design": for q_len > 1 the group axis is
+ * merged into the sequence axis, so the G query heads of KV head kv and the
+ * q_len tokens form one [G * q_len][D] row block, g outer, and every row
+ * keeps its own causal mask).
+ *   q, out     [B][Hq][q_len][D] fp16 (q_len rows per query head)
+ *   k_cache, v_cache [B][Hkv][Lmax][D] fp16, already holding the chunk's keys
+ *              and values at rows start[b] .. start[b]+q_len-1
+ *   start      [B] int32, device: 0 <= start[b] <= Lmax - q_len
+ * Token t of query head h of sequence b attends to rows 0 .. start[b]+t of
+ * KV head h / G: out = softmax(scale q k^T) v over them, fp32 accumulation,
+ * one rounding to fp16. With q_len = 1 and start = valid_len - 1 this is
+ * gqa_decode_attn. A start outside its range raises GQAQ_DEV_BAD_POS and
+ * gives that sequence a zero output. 1 <= q_len <= Lmax; D in {64, 128};
+ * G in {1, 2, 4, 8}; page_size is ignored.
+ * workspace: at least gqaq_prefill_workspace_bytes(dims, q_len) bytes, zero
+ * filled once before first use; every call leaves its counters at zero. The
+ * size depends on the SM count and GQAQ_OPT_PREFILL_SPLITS, so query it
+ * again after changing that option. */
+GQAQ_API size_t gqaq_prefill_workspace_bytes(const gqaq_dims *dims, int q_len);
+GQAQ_API int gqa_prefill_attn(const gqaq_dims *dims, int q_len, const gqaq_half *q, const gqaq_half *k_cache,
+                              const gqaq_half *v_cache, const int32_t *start, float scale, gqaq_half *out,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
 GQAQ_API const char *gqaq_status_string(int status);
 
 /* Library options (process-wide, read at launch time). */
@@ -261,10 +285,13 @@ enum {
     GQAQ_OPT_PDL = 5,             /* nonzero (default): launch with programmatic stream
                                      serialization, so a kernel's launch overlaps the
                                      end of the previous one in the stream */
-    GQAQ_OPT_QUEST_KERNEL = 6     /* quest_decode_attn's kernel: 0 (default) = the
+    GQAQ_OPT_QUEST_KERNEL = 6,    /* quest_decode_attn's kernel: 0 (default) = the
                                      cluster kernel when k <= 1024, else the work-queue
                                      kernel; 1 = cluster kernel; 2 = work-queue kernel
                                      (needs the workspace) */
+    GQAQ_OPT_PREFILL_SPLITS = 7   /* context splits per gqa_prefill_attn work item:
+                                     0 (default) = enough CTAs for one wave; 1..32
+                                     forced (larger splits may be empty) */
 };
 GQAQ_API int gqaq_set_option(int option, int64_t value);
 

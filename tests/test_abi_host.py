@@ -112,6 +112,43 @@ def test_fused_quest_step_rejects_bad_arguments(L):
     assert L.quest_decode_attn(*args, 8, *tail, odd, 1 << 20, None) == g.GQAQ_ERR_WORKSPACE
 
 
+def test_e4m3_calls_reject_bad_arguments(L):
+    d = dims()
+    f = ctypes.c_float
+    assert L.gqa_decode_attn_e4m3(ctypes.byref(d), FAKE, FAKE, FAKE, f(1.0), f(1.0), FAKE, f(0.1), FAKE, None, 0,
+                                  None) == g.GQAQ_ERR_WORKSPACE
+    assert L.gqa_decode_attn_e4m3(ctypes.byref(d), FAKE, MISALIGNED, FAKE, f(1.0), f(1.0), FAKE, f(0.1), FAKE, FAKE,
+                                  1 << 20, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.gqa_decode_attn_e4m3(ctypes.byref(d), FAKE, FAKE, FAKE, f(float("inf")), f(1.0), FAKE, f(0.1), FAKE,
+                                  FAKE, 1 << 20, None) == g.GQAQ_ERR_INVALID_ARG
+    assert L.gqa_decode_attn_e4m3(ctypes.byref(dims(head_dim=96)), FAKE, FAKE, FAKE, f(1.0), f(1.0), FAKE, f(0.1),
+                                  FAKE, FAKE, 1 << 20, None) == g.GQAQ_ERR_UNSUPPORTED
+    assert L.kv_append_e4m3(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, None, f(1.0), f(1.0), None) == \
+        g.GQAQ_ERR_INVALID_ARG
+    assert L.kv_append_e4m3(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, f(float("nan")), f(1.0), None) == \
+        g.GQAQ_ERR_INVALID_ARG
+
+
+def test_prefill_rejects_bad_arguments(L):
+    d = dims(max_len=256)
+    f = ctypes.c_float
+
+    def call(dd=d, q_len=16, q=FAKE, k=FAKE, start=FAKE, scale=0.1, ws=FAKE):
+        return L.gqa_prefill_attn(None if dd is None else ctypes.byref(dd), q_len, q, k, FAKE, start, f(scale), FAKE,
+                                  ws, 1 << 20, None)
+    assert call(dd=None) == g.GQAQ_ERR_INVALID_ARG
+    assert call(q_len=0) == g.GQAQ_ERR_INVALID_ARG
+    assert call(q_len=257) == g.GQAQ_ERR_INVALID_ARG                  # longer than the cache
+    assert call(q=None) == g.GQAQ_ERR_INVALID_ARG
+    assert call(k=MISALIGNED) == g.GQAQ_ERR_INVALID_ARG
+    assert call(start=None) == g.GQAQ_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == g.GQAQ_ERR_INVALID_ARG
+    assert call(ws=None) == g.GQAQ_ERR_WORKSPACE
+    assert call(dd=dims(head_dim=96, max_len=256)) == g.GQAQ_ERR_UNSUPPORTED
+    assert call(dd=dims(num_q_heads=24, num_kv_heads=8, max_len=256)) == g.GQAQ_ERR_UNSUPPORTED
+    assert L.gqaq_prefill_workspace_bytes(ctypes.byref(d), 0) == 0
+
+
 def test_options(L):
     assert L.gqaq_set_option(g.GQAQ_OPT_MAX_CTAS, -1) == g.GQAQ_ERR_INVALID_ARG
     assert L.gqaq_set_option(12345, 0) == g.GQAQ_ERR_INVALID_ARG
@@ -128,6 +165,10 @@ def test_options(L):
     assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_KERNEL, -1) == g.GQAQ_ERR_INVALID_ARG
     for v in (2, 1, 0):
         assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_KERNEL, v) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_SPLITS, -1) == g.GQAQ_ERR_INVALID_ARG
+    assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_SPLITS, 33) == g.GQAQ_ERR_INVALID_ARG
+    for v in (5, 32, 0):
+        assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_SPLITS, v) == g.GQAQ_OK
 
 
 def test_binding_refuses_cpu_tensors():
