@@ -431,8 +431,135 @@ def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "tensor_tflops": float(d.get("bf16_tflops_sustained", 1700.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "tensor_tflops": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Prefill mode: a chunk of q_len new tokens per sequence and layer
+# ---------------------------------------------------------------------------
+PREFILL_METRIC = "prefill-attn us/step (causal chunk of q_len tokens per sequence per layer) and TFLOP/s vs tensor peak"
+
+
+def prefill_flops(w: workloads.Workload, starts, q_len: int) -> int:
+    """q.k and p.V multiply-adds of one layer: 2 x 2 D flops per (row, attended token)."""
+    return sum(4 * w.head_dim * w.num_q_heads * (q_len * s + q_len * (q_len + 1) // 2) for s in starts)
+
+
+def prefill_bytes(w: workloads.Workload, starts, q_len: int) -> int:
+    """K and V rows read once per KV head (2 M per token), plus q in and out."""
+    M = kv_vector_bytes(w.head_dim)
+    return sum(w.num_kv_heads * 2 * M * (s + q_len) + 2 * w.num_q_heads * q_len * M for s in starts)
+
+
+def run_prefill(args, rank, world, local):
+    import gqa_head_folding_gb300 as g
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    w = workload_from_args(args)
+    Q = int(args.prefill)
+    g.lib()
+    g.set_option(g.GQAQ_OPT_PDL, 0 if args.no_pdl else 1)
+    layers = []
+    for layer in range(w.num_layers):
+        x = workloads.make_prefill_layer(w, layer, Q, device=device,
+                                         seed=workloads.layer_seed(w, layer) + rank_seed(rank) if rank else None)
+        x["out"] = torch.empty_like(x["q"])
+        layers.append(x)
+    starts = [[int(v) for v in x["start"].cpu()] for x in layers]
+    dims = g.make_dims(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len)
+    ws = g.alloc_prefill_workspace(dims, Q, device)
+    scale = 1.0 / math.sqrt(w.head_dim)
+
+    def step():
+        for x in layers:
+            g.gqa_prefill_attn(x["q"], x["k_cache"], x["v_cache"], x["start"], scale, out=x["out"], workspace=ws)
+
+    graph = capture(step, device)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        graph.replay()
+        torch.cuda.synchronize(device)
+    st = torch.cuda.current_stream(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    ev0.record(st)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(st)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    clocks = sampler.stop()
+    s_per_step = max_over_ranks(ev0.elapsed_time(ev1) / 1e3 / args.steps, dist, device)
+    assert g.device_status() == 0, "prefill raised a device status flag"
+
+    # end to end: q in from pinned host memory, out back, every step
+    h_q = [torch.empty(x["q"].shape, dtype=x["q"].dtype, pin_memory=True).copy_(x["q"].cpu()) for x in layers]
+    h_o = [torch.empty(x["out"].shape, dtype=x["out"].dtype, pin_memory=True) for x in layers]
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for x, hq in zip(layers, h_q):
+            x["q"].copy_(hq, non_blocking=True)
+        graph.replay()
+        for x, ho in zip(layers, h_o):
+            ho.copy_(x["out"], non_blocking=True)
+        torch.cuda.synchronize(device)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dist, device)
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    flops = sum(prefill_flops(w, s, Q) for s in starts)
+    per_launch_flops = prefill_flops(w, starts[0], Q)
+    achieved = flops / s_per_step / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        import numpy as np
+
+        import oracle
+        x = layers[0]
+        t0 = time.perf_counter()
+        oracle.prefill_attn(x["q"][:1, :w.group].cpu().numpy(), x["k_cache"][:1, :1].cpu().numpy(),
+                            x["v_cache"][:1, :1].cpu().numpy(), starts[0][:1], scale)
+        unit_s = time.perf_counter() - t0
+        unit_flops = prefill_flops(w.with_(num_q_heads=w.group, num_kv_heads=1), starts[0][:1], Q)
+        est = unit_s * flops / max(1, unit_flops)
+        cpu = {"value": round(est * 1e6, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"fp64 oracle on one (sequence, KV head) unit of layer 0 ({w.group} query heads x {Q} "
+                         f"tokens), scaled by flops to the whole step"}
+        del np
+    line = {
+        "metric": PREFILL_METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 in/out, f32 accumulate",
+        "data": "synthetic (seeded N(0,1) fp16 q and caches)",
+        "config": dict(config_of(w, world, pdl=not args.no_pdl), q_len=Q,
+                       chunk="last q_len tokens of each sequence's valid length"),
+        "achieved_tflops": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": "gqa_prefill_attn", "achieved": round(achieved, 1),
+                     "peak": peaks["tensor_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["tensor_tflops"], 4),
+                     "peak_source": peaks["source"] + " (bf16 sustained; fp16 has the same nominal rate)",
+                     "traffic": None, "flops_per_launch": per_launch_flops,
+                     "us_per_launch": round(s_per_step / w.num_layers * 1e6, 2)},
+        "achieved_gbs": round(sum(prefill_bytes(w, s, Q) for s in starts) / s_per_step / 1e9, 1),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_s * 1e6, 2), "unit": UNIT,
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_q),
+                "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in h_o)},
+        "gpu_launches": w.num_layers * args.steps, "gpu_launches_per_step": w.num_layers,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
 
 
 def run_ours(args, rank, world, local):
@@ -573,6 +700,8 @@ def main(argv=None):
     ap.add_argument("--quest-kernel", choices=("queue", "cluster"), default="cluster",
                     help="fused Quest kernel: one cluster per unit (default) or the GPU-wide work queue")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="time gqa_prefill_attn on a chunk of this many tokens per sequence and layer instead")
     ap.add_argument("--kv", choices=("f16", "e4m3"), default="f16",
                     help="KV-cache format; e4m3 (8-bit codes, per-tensor scales) runs all-dense stacks only")
     args = ap.parse_args(argv)
@@ -581,7 +710,9 @@ def main(argv=None):
         if any(not w.layer_is_dense(i) for i in range(w.num_layers)):
             raise SystemExit("--kv e4m3 needs a stack of dense layers only (e.g. --workload 2, or --layers 2)")
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.prefill and args.impl == "ours":
+        run_prefill(args, rank, world, local)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

@@ -149,6 +149,18 @@ def make_layer(w: Workload, layer: int = 0, device="cpu", seed: Optional[int] = 
     return out
 
 
+def make_prefill_layer(w: Workload, layer: int, q_len: int, device="cpu", seed: Optional[int] = None):
+    """One layer's inputs for a prefill chunk: the workload's caches, a chunk
+    of q_len query tokens per head, q [B,Hq,q_len,D] ~ N(0,1) fp16, and start
+    [B] int32 = valid_len - q_len (the chunk is the last q_len valid tokens,
+    already in the cache). The decode-only planted pages are not drawn."""
+    x = make_layer(w.with_(n_plant=0, append=False), layer, device=device, seed=seed)
+    g = torch.Generator(device=torch.device(device)).manual_seed(layer_seed(w, layer, salt=2) if seed is None else seed + 1)
+    q = torch.randn(w.batch, w.num_q_heads, q_len, w.head_dim, generator=g, device=device).to(torch.float16)
+    start = (x["valid_len"] - q_len).clamp(min=0).to(torch.int32)
+    return {"q": q, "k_cache": x["k_cache"], "v_cache": x["v_cache"], "start": start}
+
+
 def small(w: Workload, **overrides) -> Workload:
     """A reduced copy of a workload with the same structure (for oracle-sized tests)."""
     return w.with_(**overrides)
