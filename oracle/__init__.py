@@ -65,6 +65,11 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [i32, i32, i32, i64, i64, _dp, _dp, _dp, dbl, _dp]
             fn.restype = i32
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_int4_quantize_rows.argtypes = [fp, i64, i32, u8p, fp]
+        lib.oracle_int4_quantize_rows.restype = None
+        lib.oracle_int4_dequantize_rows.argtypes = [u8p, fp, i64, i32, _dp]
+        lib.oracle_int4_dequantize_rows.restype = None
         lib.oracle_prefill_repeat_kv.argtypes = [i32, i32, i32, i64, i32, i64, _dp, _dp, _dp, dbl, _dp]
         lib.oracle_prefill_repeat_kv.restype = i32
         lib.oracle_page_minmax.argtypes = [i32, i32, i64, i64, i32, _dp, _dp]
@@ -126,6 +131,38 @@ def quantize_e4m3(x, inv_scale: float) -> np.ndarray:
     _load().oracle_f32_array_to_e4m3(y.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
                                      out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), y.size)
     return out
+
+
+def quantize_int4(x):
+    """4-bit KV rows: x [..., D] (fp16 or fp32) -> (codes [..., D/2] uint8, scales [...] fp32).
+    Symmetric INT4 per row: scale = amax / 7, q = clamp(rne(x / scale), -7, 7),
+    nibble q + 8 (channel 2i in the low nibble of byte i); fp32 arithmetic."""
+    y = np.ascontiguousarray(_as_f64(x).astype(np.float32))
+    D = y.shape[-1]
+    rows = y.size // D
+    codes = np.empty(y.shape[:-1] + (D // 2,), dtype=np.uint8)
+    scales = np.empty(y.shape[:-1], dtype=np.float32)
+    fp = ctypes.POINTER(ctypes.c_float)
+    _load().oracle_int4_quantize_rows(y.ctypes.data_as(fp), rows, D,
+                                      codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), scales.ctypes.data_as(fp))
+    return codes, scales
+
+
+def dequantize_int4(codes, scales) -> np.ndarray:
+    """(codes [..., D/2], scales [...]) -> values (nibble - 8) * scale, float64 [..., D]."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    sc = np.ascontiguousarray(np.asarray(scales, dtype=np.float32))
+    D = c.shape[-1] * 2
+    out = np.empty(c.shape[:-1] + (D,), dtype=np.float64)
+    fp = ctypes.POINTER(ctypes.c_float)
+    _load().oracle_int4_dequantize_rows(c.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), sc.ctypes.data_as(fp),
+                                        sc.size, D, _dptr(out))
+    return out
+
+
+def attn_int4(q, k_codes, k_scales, v_codes, v_scales, valid_len, scale):
+    """fp64 decode attention over a 4-bit KV cache: dequantize, then attn_repeat_kv."""
+    return attn_repeat_kv(q, dequantize_int4(k_codes, k_scales), dequantize_int4(v_codes, v_scales), valid_len, scale)
 
 
 def _as_f64(a) -> np.ndarray:

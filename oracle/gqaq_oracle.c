@@ -97,6 +97,53 @@ void oracle_f32_array_to_e4m3(const float *src, uint8_t *dst, int64_t n)
     for (int64_t i = 0; i < n; ++i) dst[i] = oracle_f32_to_e4m3(src[i]);
 }
 
+/* ------------------------------------------------------------------------ */
+/* 4-bit KV cache (reading of [QUEST]'s "next steps"): symmetric INT4 with  */
+/* one fp32 scale per (token, head) row of D channels.                       */
+/*   scale = amax / 7            (fp32 division; amax = max |x| of the row)  */
+/*   q     = clamp(rne(x / scale), -7, 7)   (fp32 division, ties to even)    */
+/*   code  = q + 8 (a nibble; channel 2i in the low nibble of byte i)        */
+/* A row of zeros gets scale 0 and codes 8.  Value = (code - 8) * scale.     */
+/* float arithmetic throughout, so the two IEEE divisions round the same     */
+/* way as the GPU's.                                                         */
+/* ------------------------------------------------------------------------ */
+void oracle_int4_quantize_rows(const float *x, int64_t rows, int d, uint8_t *codes, float *scales)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * d;
+        float amax = 0.0f;
+        for (int i = 0; i < d; ++i) {
+            float a = fabsf(xr[i]);
+            if (a > amax)
+                amax = a;
+        }
+        float scale = amax / 7.0f;
+        scales[r] = scale;
+        uint8_t *cr = codes + r * (d / 2);
+        for (int i = 0; i < d / 2; ++i)
+            cr[i] = 0;
+        for (int i = 0; i < d; ++i) {
+            int q = 0;
+            if (scale > 0.0f) {
+                float t = rintf(xr[i] / scale);
+                q = t > 7.0f ? 7 : (t < -7.0f ? -7 : (int)t);
+            }
+            uint8_t nib = (uint8_t)(q + 8);
+            cr[i / 2] |= (i & 1) ? (uint8_t)(nib << 4) : nib;
+        }
+    }
+}
+
+void oracle_int4_dequantize_rows(const uint8_t *codes, const float *scales, int64_t rows, int d, double *out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int i = 0; i < d; ++i) {
+            uint8_t byte = codes[r * (d / 2) + i / 2];
+            int nib = (i & 1) ? (byte >> 4) : (byte & 15);
+            out[r * d + i] = (double)(nib - 8) * (double)scales[r];
+        }
+}
+
 void oracle_f16_array_to_f64(const uint16_t *src, double *dst, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)

@@ -412,3 +412,72 @@ def test_prefill_first_row_sees_one_token():
     v = rand_f16(1, 1, 4, 16, rng=rng)
     got = oracle.prefill_attn(q, k, v, [0], 0.5)
     assert np.array_equal(got[0, :, 0], np.repeat(v[0, :, 0].astype(np.float64), 2, axis=0))
+
+
+# ---------------------------------------------------------------------------
+# INT4 (the 4-bit KV-cache variant): per-row symmetric quantization
+# ---------------------------------------------------------------------------
+def _nibbles(codes):
+    c = np.asarray(codes)
+    return np.stack([c & 15, c >> 4], axis=-1).reshape(c.shape[:-1] + (c.shape[-1] * 2,)).astype(np.int64)
+
+
+def test_int4_codes_are_the_nearest_grid_point():
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((300, 64)) * rng.uniform(0.01, 30, size=(300, 1))).astype(np.float16)
+    codes, scales = oracle.quantize_int4(x)
+    xf = x.astype(np.float32)
+    amax = np.abs(xf).max(axis=1)
+    assert np.array_equal(scales, amax / np.float32(7.0))
+    q = _nibbles(codes) - 8
+    assert q.min() >= -7 and q.max() <= 7
+    # brute force over the 15 levels, in the same fp32 units x / scale
+    t = xf / scales[:, None]
+    grid = np.arange(-7, 8)
+    dist = np.abs(t[:, :, None] - grid[None, None, :])
+    best = dist.min(axis=2)
+    assert np.all(np.abs(t - q) == best)
+    # the row maximum lands on +-7
+    arg = np.abs(xf).argmax(axis=1)
+    assert np.all(np.abs(q[np.arange(300), arg]) == 7)
+
+
+def test_int4_ties_zero_rows_and_packing():
+    x = np.zeros((3, 8), dtype=np.float32)
+    x[0] = [7, 2.5, -2.5, 3.5, 0.5, -0.5, 1.5, -7]        # scale 1: ties go to the even level
+    x[1] = [14, 5, -5, 1, 0, 0, 0, 0]                    # scale 2: 2.5 -> 2, -2.5 -> -2, 0.5 -> 0
+    codes, scales = oracle.quantize_int4(x)
+    assert list(scales) == [1.0, 2.0, 0.0]
+    assert list(_nibbles(codes)[0] - 8) == [7, 2, -2, 4, 0, 0, 2, -7]
+    assert list(_nibbles(codes)[1] - 8) == [7, 2, -2, 0, 0, 0, 0, 0]
+    assert list(_nibbles(codes)[2]) == [8] * 8               # an all-zero row: scale 0, level 0
+    # channel 2i in the low nibble of byte i
+    assert codes[0, 0] == ((2 + 8) << 4) | (7 + 8)
+
+
+def test_int4_dequantize_closed_form():
+    rng = np.random.default_rng(22)
+    codes = rng.integers(0, 256, size=(5, 3, 32), dtype=np.uint8)
+    scales = rng.uniform(0.001, 3, size=(5, 3)).astype(np.float32)
+    got = oracle.dequantize_int4(codes, scales)
+    ref = (_nibbles(codes) - 8) * scales[..., None].astype(np.float64)
+    assert np.array_equal(got, ref)
+
+
+def test_attn_int4_matches_sdpa_on_dequantized_cache():
+    rng = np.random.default_rng(23)
+    B, Hkv, G, D, Lmax = 2, 2, 4, 64, 40
+    q = rand_f16(B, Hkv * G, D, rng=rng)
+    kc, ks = oracle.quantize_int4(rand_f16(B, Hkv, Lmax, D, rng=rng))
+    vc, vs = oracle.quantize_int4(rand_f16(B, Hkv, Lmax, D, rng=rng))
+    vl = [Lmax, 9]
+    got = oracle.attn_int4(q, kc, ks, vc, vs, vl, 0.125)
+    k = torch.from_numpy((_nibbles(kc) - 8) * ks[..., None].astype(np.float64))
+    v = torch.from_numpy((_nibbles(vc) - 8) * vs[..., None].astype(np.float64))
+    qt = torch.from_numpy(q.astype(np.float64))
+    for b in range(B):
+        L = vl[b]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qt[b][:, None, :], k[b, :, :L].repeat_interleave(G, dim=0), v[b, :, :L].repeat_interleave(G, dim=0),
+            scale=0.125)[:, 0]
+        assert np.allclose(got[b], ref.numpy(), rtol=0, atol=1e-12)
