@@ -45,7 +45,10 @@ UNIT = "us/step"
 # plus 2MKS of selected keys and values.
 # ---------------------------------------------------------------------------
 def kv_vector_bytes(head_dim: int, kv: str = "f16") -> int:
-    """M: bytes of one cached key or value vector (fp16, or 8-bit E4M3 codes)."""
+    """M: bytes of one cached key or value vector (fp16; 8-bit E4M3 codes; 4-bit
+    levels plus the row's fp32 scale)."""
+    if kv == "int4":
+        return head_dim // 2 + 4
     return head_dim * (1 if kv == "e4m3" else 2)
 
 
@@ -82,7 +85,7 @@ def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True, kv: st
 
     qo = 2 * G * M                                   # q read + out write per unit
     app_unit = 2 * M + 2 * M + 4 * M                 # new k,v read, row write, page min/max read+write
-    if kv == "e4m3":                                 # new k,v read (fp16), 8-bit rows written, no metadata
+    if kv != "f16":                                  # new k,v read (fp16), low-bit rows written, no metadata
         app_unit = 2 * M + 2 * kv_vector_bytes(D, kv)
     for layer, lens in enumerate(lens_per_layer):
         dense = w.layer_is_dense(layer)
@@ -218,6 +221,18 @@ def e4m3_cache(x: torch.Tensor):
     return (x.float() * (1.0 / scale)).to(torch.float8_e4m3fn).view(torch.uint8), scale
 
 
+def int4_cache(x: torch.Tensor):
+    """Input preparation for the 4-bit cache: per-row scale amax / 7 and the
+    levels clamp(round(x / scale), -7, 7) + 8 packed two per byte (torch ops,
+    outside the step)."""
+    xf = x.float()
+    scale = xf.abs().amax(dim=-1) / 7.0
+    lv = torch.where(scale[..., None] > 0, torch.round(xf / scale[..., None].clamp(min=1e-30)), torch.zeros_like(xf))
+    nib = (lv.clamp(-7, 7) + 8).to(torch.uint8)
+    codes = nib[..., 0::2] | (nib[..., 1::2] << 4)
+    return codes.contiguous(), scale.contiguous()
+
+
 def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True, kv: str = "f16"):
     import gqa_head_folding_gb300 as g
     from gqa_head_folding_gb300.decode import DecodeStack, Layer
@@ -232,6 +247,10 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
         if kv == "e4m3":
             L.k_cache, L.k_scale = e4m3_cache(x["k_cache"])
             L.v_cache, L.v_scale = e4m3_cache(x["v_cache"])
+            del x["k_cache"], x["v_cache"]
+        elif kv == "int4":
+            L.k_cache, L.k_scales = int4_cache(x["k_cache"])
+            L.v_cache, L.v_scales = int4_cache(x["v_cache"])
             del x["k_cache"], x["v_cache"]
         elif w.append or not w.layer_is_dense(layer):
             L.meta = stack.new_meta()
@@ -249,7 +268,8 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
 # capture of the kernel as it stands, keyed by (workload id, batch, family). A kernel
 # change makes its entry stale: it is then removed until the capture is taken again.
 NCU_TRAFFIC = {(3, 1, "quest", "f16"): 67_802_624, (3, 1, "dense", "f16"): 539_854_848,
-               (2, 32, "dense", "f16"): 180_059_392, (2, 32, "dense", "e4m3"): 90_711_552}
+               (2, 32, "dense", "f16"): 180_059_392, (2, 32, "dense", "e4m3"): 90_711_552,
+               (2, 32, "dense", "int4"): 49_939_712}
 
 
 def capture(fn, device):
@@ -315,6 +335,9 @@ def oracle_step_seconds(w: workloads.Workload, layers, lens, budget_s: float = 1
         t0 = time.perf_counter()
         if kv_dtype == "e4m3":
             oracle.attn_e4m3(q, k, v, L.k_scale, L.v_scale, [length], scale)
+        elif kv_dtype == "int4":
+            oracle.attn_int4(q, k, L.k_scales[b, kv][None, None].cpu().numpy(), v,
+                             L.v_scales[b, kv][None, None].cpu().numpy(), [length], scale)
         else:
             oracle.attn_repeat_kv(q, k, v, [length], scale)
         return time.perf_counter() - t0
@@ -395,7 +418,8 @@ def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool =
             "quest_path": (f"fused (quest_decode_attn, {'GPU-wide work queue' if quest_kernel == 'queue' else 'cluster per unit'})"
                            if fused else "step-by-step calls"),
             "launch": "programmatic dependent launch" if pdl else "plain stream order",
-            "kv_cache": "e4m3 codes, per-tensor fp32 scales" if kv == "e4m3" else "f16",
+            "kv_cache": {"e4m3": "e4m3 codes, per-tensor fp32 scales",
+                         "int4": "int4 levels, per-token fp32 scales"}.get(kv, "f16"),
             "l2": "per-step working set > 4x L2; no flush"}
 
 
@@ -659,7 +683,8 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 in/out, " + ("e4m3 KV cache, " if args.kv == "e4m3" else "") + "f32 accumulate",
+        "dtype": "f16 in/out, " + ({"e4m3": "e4m3 KV cache, ", "int4": "int4 KV cache, "}.get(args.kv, "")) +
+                 "f32 accumulate",
         "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl,
                                                                                        quest_kernel=args.quest_kernel, kv=args.kv),
         "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
@@ -702,13 +727,14 @@ def main(argv=None):
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
     ap.add_argument("--prefill", type=int, default=0,
                     help="time gqa_prefill_attn on a chunk of this many tokens per sequence and layer instead")
-    ap.add_argument("--kv", choices=("f16", "e4m3"), default="f16",
-                    help="KV-cache format; e4m3 (8-bit codes, per-tensor scales) runs all-dense stacks only")
+    ap.add_argument("--kv", choices=("f16", "e4m3", "int4"), default="f16",
+                    help="KV-cache format; e4m3 (8-bit codes, per-tensor scales) and int4 (4-bit levels, per-token "
+                         "scales) run all-dense stacks only")
     args = ap.parse_args(argv)
-    if args.kv == "e4m3":
+    if args.kv != "f16":
         w = workload_from_args(args)
         if any(not w.layer_is_dense(i) for i in range(w.num_layers)):
-            raise SystemExit("--kv e4m3 needs a stack of dense layers only (e.g. --workload 2, or --layers 2)")
+            raise SystemExit(f"--kv {args.kv} needs a stack of dense layers only (e.g. --workload 2, or --layers 2)")
     rank, world, local = dist_env()
     if args.prefill and args.impl == "ours":
         run_prefill(args, rank, world, local)

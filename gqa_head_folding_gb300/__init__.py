@@ -63,6 +63,7 @@ class Dims(ctypes.Structure):
 EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_update_meta",
            "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "quest_decode_attn",
            "gqa_decode_attn_noalloc", "gqa_decode_attn_e4m3", "kv_append_e4m3",
+           "gqa_decode_attn_int4", "kv_append_int4",
            "gqaq_prefill_workspace_bytes", "gqa_prefill_attn",
            "gqaq_status_string", "gqaq_set_option", "gqaq_device_status", "gqaq_version")
 
@@ -93,6 +94,8 @@ def lib():
         f32 = ctypes.c_float
         L.gqa_decode_attn_e4m3.argtypes = [dp, vp, vp, vp, f32, f32, vp, f32, vp, vp, ctypes.c_size_t, vp]
         L.kv_append_e4m3.argtypes = [dp, vp, vp, vp, vp, vp, f32, f32, vp]
+        L.gqa_decode_attn_int4.argtypes = [dp, vp, vp, vp, vp, vp, vp, f32, vp, vp, ctypes.c_size_t, vp]
+        L.kv_append_int4.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gqaq_prefill_workspace_bytes.argtypes = [dp, i32]
         L.gqaq_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.gqa_prefill_attn.argtypes = [dp, i32, vp, vp, vp, vp, f32, vp, vp, ctypes.c_size_t, vp]
@@ -322,6 +325,49 @@ def gqa_prefill_attn(q, k_cache, v_cache, start, scale: float, out=None, workspa
         ctypes.byref(d), int(q_len), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(start), float(scale), _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(q)))
     return out
+
+
+def gqa_decode_attn_int4(q, k_codes, k_scales, v_codes, v_scales, valid_len, scale: float, out=None,
+                         workspace=None):
+    """Dense folded-GQA decode attention over a 4-bit cache: codes
+    [B,Hkv,Lmax,D/2] uint8 (two levels + 8 per byte, low nibble first), scales
+    [B,Hkv,Lmax] fp32 (value = level * scale). Lmax must be a multiple of 4."""
+    _need(q, "q", torch.float16, 3)
+    for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
+        _need(t, name, torch.uint8, 4)
+    for name, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _need(t, name, torch.float32, 3)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_codes.shape
+    d = make_dims(B, Hq, Hkv, D, Lmax)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 3)
+    if workspace is None:
+        workspace = alloc_workspace(d, q.device)
+    _check("gqa_decode_attn_int4", lib().gqa_decode_attn_int4(
+        ctypes.byref(d), _ptr(q), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(valid_len),
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(q)))
+    return out
+
+
+def kv_append_int4(k_codes, k_scales, v_codes, v_scales, k_new, v_new, pos):
+    """Quantize k_new/v_new [B,Hkv,D] fp16 rows to INT4 (scale = amax / 7 per
+    row) and write codes and scales at row pos[b]."""
+    for name, t in (("k_codes", k_codes), ("v_codes", v_codes)):
+        _need(t, name, torch.uint8, 4)
+    for name, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _need(t, name, torch.float32, 3)
+    _need(k_new, "k_new", torch.float16, 3)
+    _need(v_new, "v_new", torch.float16, 3)
+    _need(pos, "pos", torch.int32, 1)
+    B, Hkv, Lmax, _ = k_codes.shape
+    D = k_new.shape[2]
+    d = make_dims(B, Hkv, Hkv, D, Lmax)
+    _check("kv_append_int4", lib().kv_append_int4(
+        ctypes.byref(d), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(k_new), _ptr(v_new),
+        _ptr(pos), _stream(k_codes)))
 
 
 def quest_append_kv(k_cache, v_cache, meta, k_new, v_new, pos, page_size: int = PAGE_SIZE):

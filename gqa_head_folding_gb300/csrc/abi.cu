@@ -139,6 +139,19 @@ bool encode_tensor_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_f32_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols) {
+    if ((cols * 4) % 16 != 0) return false;
+    if (!encode_tensor_map_2d(map, base, rows, cols * 2, 64, 1, false)) return false;  // loads g_encode
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {box_cols, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_tensor_map_kpage(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     if (cols % 64 != 0 || !encode_tensor_map_2d(map, base, rows, cols, 64, box_rows, true)) return false;  // loads g_encode
     const cuuint64_t dims[3] = {64, cols / 64, rows};
@@ -406,6 +419,50 @@ int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_cache, co
     if (rc != GQAQ_OK) return rc;
     return launch_append_e4m3(dims, k_cache, v_cache, reinterpret_cast<const __half *>(k_new),
                               reinterpret_cast<const __half *>(v_new), pos, k_inv_scale, v_inv_scale, ctx);
+}
+
+int gqa_decode_attn_int4(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_codes, const float *k_scales,
+                         const uint8_t *v_codes, const float *v_scales, const int32_t *valid_len, float scale,
+                         gqaq_half *out, void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_dims(dims, false);
+    if (rc != GQAQ_OK) return rc;
+    if (dims->max_len % 4 != 0) return GQAQ_ERR_UNSUPPORTED;  // scale rows are 16-byte multiples
+    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) ||
+        !aligned16(v_scales) || !aligned16(out) || !aligned16(valid_len))
+        return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return GQAQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace)) return GQAQ_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    AttnArgs a = {};
+    a.dims = dims;
+    a.q = reinterpret_cast<const __half *>(q);
+    a.k_cache = reinterpret_cast<const __half *>(k_codes);  // byte rows; typed as the kernels take it
+    a.v_cache = reinterpret_cast<const __half *>(v_codes);
+    a.valid_len = valid_len;
+    a.scale = scale;
+    a.kv4 = true;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.out = reinterpret_cast<__half *>(out);
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launch_attention(a, ctx);
+}
+
+int kv_append_int4(const gqaq_dims *dims, uint8_t *k_codes, float *k_scales, uint8_t *v_codes, float *v_scales,
+                   const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos, void *stream) {
+    int rc = check_dims(dims, false);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales) ||
+        !aligned16(k_new) || !aligned16(v_new) || !aligned16(pos))
+        return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_append_int4(dims, k_codes, k_scales, v_codes, v_scales, reinterpret_cast<const __half *>(k_new),
+                              reinterpret_cast<const __half *>(v_new), pos, ctx);
 }
 
 namespace {

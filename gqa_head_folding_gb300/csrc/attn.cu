@@ -36,21 +36,23 @@
 
 namespace gqaq {
 
-// KV8: the E4M3 cache variant (one byte per channel): half the stage bytes,
-// so up to six stages (192 KB of copies in flight per SM).
-template <int D, int G, bool KV8 = false>
+// KV: the cache format. 0 = fp16; 1 = E4M3 codes (one byte per channel:
+// half the stage bytes, so up to six stages); 2 = INT4 levels (half a byte
+// per channel) with one fp32 scale per token row (up to eight stages).
+template <int D, int G, int KV = 0>
 struct AttnCfg : TileCfg<D, G> {
     using T = TileCfg<D, G>;
     static constexpr int THREADS = (T::NCW + 1) * 32;
     static constexpr int MISC = 256;
     static constexpr int FIXED = T::QBYTES + T::MERGE + T::PBYTES + MISC;
-    static constexpr int KBYTES = KV8 ? T::TILE * D : T::KBYTES;
-    static constexpr int STAGE = KV8 ? 2 * T::TILE * D : T::STAGE;
+    static constexpr int KBYTES = KV == 1 ? T::TILE * D : KV == 2 ? T::TILE * D / 2 + T::TILE * 4 : T::KBYTES;
+    static constexpr int STAGE = KV != 0 ? 2 * KBYTES : T::STAGE;
     // 8-bit tiles: the deepest ring of at most six stages that fits (two CTAs
     // per SM at D = 64, one at D = 128).
     static constexpr int LIMIT8 = (D == 64 ? 112 : 225) * 1024 - FIXED - 1024;
-    static constexpr int NSTAGE8 = LIMIT8 / STAGE < 6 ? LIMIT8 / STAGE : 6;
-    static constexpr int NSTAGE = KV8 ? NSTAGE8 : ((3 * STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2);
+    static constexpr int MAXST = KV == 2 ? 8 : 6;
+    static constexpr int NSTAGE8 = LIMIT8 / STAGE < MAXST ? LIMIT8 / STAGE : MAXST;
+    static constexpr int NSTAGE = KV != 0 ? NSTAGE8 : ((3 * STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2);
     static constexpr int SMEM = 1024 + NSTAGE * STAGE + FIXED;
     static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
     static_assert(NSTAGE >= 2, "at least a double-buffered ring");
@@ -231,12 +233,15 @@ __device__ __forceinline__ void merge_parts(const float *part, float *wbuf, int6
     }
 }
 
-template <int D, int G, bool SPARSE, bool KV8 = false>
-__global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8>::MIN_BLOCKS)
-    attn_partial_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
-    using C = AttnCfg<D, G, KV8>;
-    static_assert(!(SPARSE && KV8), "the E4M3 variant is dense");
+// ksmap / vsmap: the INT4 variant's per-token scale rows (unused otherwise).
+template <int D, int G, bool SPARSE, int KV = 0>
+__global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>::MIN_BLOCKS)
+    attn_partial_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap ksmap, const __grid_constant__ CUtensorMap vsmap,
+                        const AttnParams p) {
+    using C = AttnCfg<D, G, KV>;
+    constexpr bool KV8 = KV == 1, KV4 = KV == 2;
+    static_assert(!(SPARSE && KV != 0), "the 8-bit and 4-bit variants are dense");
     constexpr int NCT = C::NCW * 32;  // consumer threads
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -263,6 +268,10 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8
         fence_mbar_init();
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
+        if (KV4) {
+            prefetch_tensormap(&ksmap);
+            prefetch_tensormap(&vsmap);
+        }
     }
     pdl_wait_and_release();
     TileRule rule;
@@ -382,7 +391,13 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8
                     if (lane == 0) {
                         mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
                         const int y = row0 + local * C::TILE;
-                        if (KV8) {
+                        if (KV4) {  // codes, then the tile's 128 scales (row = unit, x = first token)
+                            constexpr int CODE4 = C::TILE * D / 2;
+                            tma_load_2d(kdst, &kmap, 0, y, fb, pol);
+                            tma_load_2d(kdst + CODE4, &ksmap, local * C::TILE, unit, fb, pol);
+                            tma_load_2d(vdst, &vmap, 0, y, fb, pol);
+                            tma_load_2d(vdst + CODE4, &vsmap, local * C::TILE, unit, fb, pol);
+                        } else if (KV8) {
                             tma_load_2d(kdst, &kmap, 0, y, fb, pol);
                             tma_load_2d(vdst, &vmap, 0, y, fb, pol);
                         } else {
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV8>::THREADS, AttnCfg<D, G, KV8
     // the arrival counters in step, so the workspace stays reusable.
     // ----------------------------------------------------------------------
     const int tid = threadIdx.x;  // 0..255 among consumers
-    using WA = MmaAttn<D, G, SPARSE, KV8>;  // sparse stages hold K and V page-major
+    using WA = MmaAttn<D, G, SPARSE, KV>;  // sparse stages hold K and V page-major
     WA wa;
     wa.init(warp, lane, smem_u32(pbuf));
 
@@ -543,13 +558,13 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-template <int D, int G, bool SPARSE, bool KV8 = false>
+template <int D, int G, bool SPARSE, int KV = 0>
 int grid_for(const LaunchCtx &ctx) {
-    using C = AttnCfg<D, G, KV8>;
+    using C = AttnCfg<D, G, KV>;
     static int occ[kMaxDevices] = {0};
     if (ctx.device < 0 || ctx.device >= kMaxDevices) return -1;
     if (occ[ctx.device] == 0) {
-        auto kern = attn_partial_kernel<D, G, SPARSE, KV8>;
+        auto kern = attn_partial_kernel<D, G, SPARSE, KV>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return -1;
         int n = 0;
@@ -568,11 +583,12 @@ int grid_for(const LaunchCtx &ctx) {
 // then the partials [grid][2][G][D+2] fp32.
 inline size_t count_bytes(const gqaq_dims &dm) { return workspace_zero_bytes(dm); }
 
-template <int D, int G, bool SPARSE, bool KV8 = false>
+template <int D, int G, bool SPARSE, int KV = 0>
 int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
-    using C = AttnCfg<D, G, KV8>;
+    using C = AttnCfg<D, G, KV>;
+    constexpr bool KV8 = KV == 1, KV4 = KV == 2;
     const gqaq_dims &dm = *a.dims;
-    int grid = grid_for<D, G, SPARSE, KV8>(ctx);
+    int grid = grid_for<D, G, SPARSE, KV>(ctx);
     if (grid < 1) return GQAQ_ERR_CUDA;
     {
         // Launch no more CTAs than the shape's largest tile count can keep at
@@ -591,9 +607,15 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
 
     const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
     const uint32_t box_rows = SPARSE ? (uint32_t)dm.page_size : (uint32_t)C::TILE;
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap, ksmap, vsmap;
     // K and V stages share one layout (the tile reads both through it).
-    if (KV8) {  // byte rows: D = 128 rows 128-byte swizzled, D = 64 rows 64-byte swizzled
+    if (KV4) {  // code rows of D/2 bytes, unswizzled; scale rows [units][Lmax] fp32
+        const uint64_t units = (uint64_t)dm.batch * dm.num_kv_heads;
+        if (!encode_tensor_map_u8(&kmap, a.k_cache, rows, D / 2, box_rows, 0)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_u8(&vmap, a.v_cache, rows, D / 2, box_rows, 0)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_f32_rows(&ksmap, a.k_scales, units, dm.max_len, C::TILE)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_f32_rows(&vsmap, a.v_scales, units, dm.max_len, C::TILE)) return GQAQ_ERR_CUDA;
+    } else if (KV8) {  // byte rows: D = 128 rows 128-byte swizzled, D = 64 rows 64-byte swizzled
         if (!encode_tensor_map_u8(&kmap, a.k_cache, rows, D, box_rows, D == 128 ? 128 : 64)) return GQAQ_ERR_CUDA;
         if (!encode_tensor_map_u8(&vmap, a.v_cache, rows, D, box_rows, D == 128 ? 128 : 64)) return GQAQ_ERR_CUDA;
     } else if (SPARSE) {
@@ -602,6 +624,10 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     } else {
         if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, box_rows, true)) return GQAQ_ERR_CUDA;
         if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, 64, box_rows, true)) return GQAQ_ERR_CUDA;
+    }
+    if (!KV4) {
+        ksmap = kmap;  // placeholders: only the INT4 variant reads scale maps
+        vsmap = vmap;
     }
 
     AttnParams p;
@@ -621,15 +647,16 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     p.v_scale = KV8 ? a.v_scale : 1.f;
     p.timeout_ns = ctx.timeout_ns;
     p.test_stall = ctx.test_stall;
-    if (launch_kernel(attn_partial_kernel<D, G, SPARSE, KV8>, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, kmap,
-                      vmap, p) != cudaSuccess)
+    if (launch_kernel(attn_partial_kernel<D, G, SPARSE, KV>, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, kmap,
+                      vmap, ksmap, vsmap, p) != cudaSuccess)
         return GQAQ_ERR_CUDA;
     return GQAQ_OK;
 }
 
 template <int D, int G>
 int dispatch_sparse(const AttnArgs &a, const LaunchCtx &ctx) {
-    if (a.kv8) return a.page_idx ? GQAQ_ERR_UNSUPPORTED : launch_t<D, G, false, true>(a, ctx);
+    if (a.kv8) return a.page_idx ? GQAQ_ERR_UNSUPPORTED : launch_t<D, G, false, 1>(a, ctx);
+    if (a.kv4) return a.page_idx ? GQAQ_ERR_UNSUPPORTED : launch_t<D, G, false, 2>(a, ctx);
     return a.page_idx ? launch_t<D, G, true>(a, ctx) : launch_t<D, G, false>(a, ctx);
 }
 
@@ -648,10 +675,12 @@ template <int D, int G>
 size_t ws_t(const gqaq_dims &dm, const LaunchCtx &ctx) {
     const int g0 = grid_for<D, G, false>(ctx);
     const int g1 = grid_for<D, G, true>(ctx);
-    const int g2 = grid_for<D, G, false, true>(ctx);
-    if (g0 < 1 || g1 < 1 || g2 < 1) return 0;
+    const int g2 = grid_for<D, G, false, 1>(ctx);
+    const int g3 = grid_for<D, G, false, 2>(ctx);
+    if (g0 < 1 || g1 < 1 || g2 < 1 || g3 < 1) return 0;
     int grid = g0 > g1 ? g0 : g1;
     grid = grid > g2 ? grid : g2;
+    grid = grid > g3 ? grid : g3;
     return count_bytes(dm) + (size_t)grid * 2 * G * (D + 2) * sizeof(float);
 }
 

@@ -22,6 +22,11 @@
 // decodes them into fragments; the channel order inside the contraction is
 // permuted to match (q uses the same permutation, so q.k is unchanged). V^T
 // fragments pair two tokens' codes with a byte permute before decoding.
+// INT4 caches (KV4): rows of D/2 bytes (channel 2i in the low nibble of byte
+// i) plus one fp32 scale per token row. Nibbles decode exactly to fp16 (the
+// 1024 + n bit trick, minus 1032); the K scale multiplies the token's fp32
+// score and the V scale its probability, so both contractions run on the
+// integer levels. The channel order is permuted as for E4M3.
 #pragma once
 
 #include "attn_tile.cuh"
@@ -68,10 +73,20 @@ __device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t y, uint32_t s
     return r;
 }
 
-template <int D, int G, bool KPAGE = false, bool KV8 = false>
+// Four nibbles at bit offsets s and s + 16 of w -> fp16x2 of (nibble - 8), exact.
+__device__ __forceinline__ uint32_t nib2_to_f16x2(uint32_t w, int s) {
+    uint32_t t, r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(w >> s), "r"(0x000F000Fu), "r"(0x64006400u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64086408u));  // - (1024 + 8)
+    return r;
+}
+
+template <int D, int G, bool KPAGE = false, int KV = 0>
 struct MmaAttn {
     using C = TileCfg<D, G>;
-    static_assert(!(KPAGE && KV8), "8-bit stages are dense-only");
+    static constexpr bool KV8 = KV == 1;  // E4M3 codes
+    static constexpr bool KV4 = KV == 2;  // INT4 levels + per-token scales
+    static_assert(!(KPAGE && KV != 0), "8-bit and 4-bit stages are dense-only");
     static constexpr bool QREG = true;   // q fragments live in registers
     static constexpr int KS = D / 16;    // k-steps of q.k, m-blocks of p @ V
     int lane, cw, r, c;                  // r = lane / 4 (token / channel row), c = lane % 4 (column pair)
@@ -89,6 +104,8 @@ struct MmaAttn {
         }
         return base + (uint32_t)(kh * C::KBLK + row * 128 + ((cc ^ (row & 7)) << 4));
     }
+    // INT4 stage: codes [TILE][D/2] unswizzled, then the TILE fp32 scales.
+    static constexpr int CODE4 = C::TILE * D / 2;
     // E4M3 stage: byte address of logical byte `byte` (a multiple of 8) of row `row`.
     __device__ __forceinline__ static uint32_t byte8(uint32_t base, int row, int byte) {
         if (D == 128) return base + (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15));
@@ -112,12 +129,19 @@ struct MmaAttn {
     // B fragments of Q^T for the unit's [G][D] block (row n = r; rows >= G are zero).
     // fp16 stages: k-step j covers channels 16j .. 16j+15 in natural order.
     // E4M3 stages: k-step j of column pair c covers channels (D/4) c + 4j .. +3.
+    // INT4 stages: k-step j of column pair c covers base, base+4 (b0) and
+    // base+1, base+5 (b1), base = (D/4) c + 8 (j/2) + 2 (j%2).
     __device__ __forceinline__ void load_q(const __half *qg) {
         const bool live = r < G;
         const __half *qrow = qg + (live ? r : 0) * D;
+        const uint16_t *qh = reinterpret_cast<const uint16_t *>(qrow);
 #pragma unroll
         for (int j = 0; j < KS; ++j) {
-            if (KV8) {
+            if (KV4) {
+                const int base = (D / 4) * c + 8 * (j >> 1) + 2 * (j & 1);
+                qb[j][0] = live ? ((uint32_t)qh[base] | ((uint32_t)qh[base + 4] << 16)) : 0u;
+                qb[j][1] = live ? ((uint32_t)qh[base + 1] | ((uint32_t)qh[base + 5] << 16)) : 0u;
+            } else if (KV8) {
                 const uint2 x = live ? *reinterpret_cast<const uint2 *>(qrow + (D / 4) * c + 4 * j) : make_uint2(0u, 0u);
                 qb[j][0] = x.x;
                 qb[j][1] = x.y;
@@ -135,7 +159,36 @@ struct MmaAttn {
         const int row0 = cw * C::SUB;
         // ---- 1. S^T = K . Q^T ----
         float s[4] = {0.f, 0.f, 0.f, 0.f};
-        if (KV8) {
+        if constexpr (KV4) {
+            constexpr int NW = D / 32;  // words of a row this lane decodes (D/4 channels)
+            uint32_t wa[NW], wb[NW];
+            const uint32_t ra = kbase + (uint32_t)((row0 + r) * (D / 2) + (D / 8) * c);
+            const uint32_t rb = ra + (uint32_t)(8 * (D / 2));
+            if constexpr (NW == 2) {
+                const uint2 x = lds64(ra), y = lds64(rb);
+                wa[0] = x.x; wa[NW - 1] = x.y; wb[0] = y.x; wb[NW - 1] = y.y;
+            } else {
+                const uint4 x = lds128(ra), y = lds128(rb);
+                wa[0] = x.x; wa[1 % NW] = x.y; wa[2 % NW] = x.z; wa[3 % NW] = x.w;
+                wb[0] = y.x; wb[1 % NW] = y.y; wb[2 % NW] = y.z; wb[3 % NW] = y.w;
+            }
+#pragma unroll
+            for (int j = 0; j < KS; ++j) {
+                const int e = 2 * (j & 1);
+                uint32_t a[4];
+                a[0] = nib2_to_f16x2(wa[j >> 1], 4 * e);
+                a[1] = nib2_to_f16x2(wb[j >> 1], 4 * e);
+                a[2] = nib2_to_f16x2(wa[j >> 1], 4 * e + 4);
+                a[3] = nib2_to_f16x2(wb[j >> 1], 4 * e + 4);
+                mma_16816(s, a, qb[j][0], qb[j][1]);
+            }
+            const float ks0 = __uint_as_float(lds32(kbase + (uint32_t)(CODE4 + (row0 + r) * 4)));
+            const float ks1 = __uint_as_float(lds32(kbase + (uint32_t)(CODE4 + (row0 + r + 8) * 4)));
+            s[0] *= ks0;
+            s[1] *= ks0;
+            s[2] *= ks1;
+            s[3] *= ks1;
+        } else if (KV8) {
             constexpr int BPL = D / 4;  // bytes of a row this lane decodes
             uint4 ka[BPL / 16], kb[BPL / 16];
 #pragma unroll
@@ -197,15 +250,53 @@ struct MmaAttn {
             }
         }
         // ---- 3. P^T as the B operand: fp16, transposed 8x8 halves ----
-        const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // tokens 2c, 2c+1 of column r
-        const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // tokens 8+2c, 8+2c+1
+        float w0 = 1.f, w1 = 1.f;  // INT4: each token's V scale rides on its probability
+        if constexpr (KV4) {
+            const float vs0 = __uint_as_float(lds32(vbase + (uint32_t)(CODE4 + (row0 + r) * 4)));
+            const float vs1 = __uint_as_float(lds32(vbase + (uint32_t)(CODE4 + (row0 + r + 8) * 4)));
+            w0 = v0 ? vs0 : 0.f;  // a row past nvalid may hold any scale bits
+            w1 = v1 ? vs1 : 0.f;
+        }
+        const uint32_t pb0 = movmatrix_trans(pack_half2(p0 * w0, p1 * w0));  // tokens 2c, 2c+1 of column r
+        const uint32_t pb1 = movmatrix_trans(pack_half2(p2 * w1, p3 * w1));  // tokens 8+2c, 8+2c+1
         // Rows past nvalid may hold anything (even NaN codes): their V^T
         // entries are zeroed, since 0 * NaN would poison the sum.
         const bool partial = nvalid < C::SUB;  // warp-uniform
         const uint32_t mk0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
         const uint32_t mk1 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
         // ---- 4. O^T += V^T . P^T ----
-        if (KV8) {
+        if constexpr (KV4) {
+            constexpr int NW = D / 64;  // words of a token row this lane reads (channels (D/8) r ..)
+            uint32_t w[4][NW];          // tokens 2c, 2c+1, 2c+8, 2c+9
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int row = row0 + 2 * c + (t & 1) + (t >> 1) * 8;
+                const uint32_t addr = vbase + (uint32_t)(row * (D / 2) + (D / 16) * r);
+                if constexpr (NW == 2) {
+                    const uint2 v = lds64(addr);
+                    w[t][0] = v.x;
+                    w[t][NW - 1] = v.y;
+                } else {
+                    w[t][0] = lds32(addr);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                // m-block i: row r <-> channel (D/8) r + 2i, row r + 8 <-> (D/8) r + 2i + 1
+                const int wd = i >> 2, k = 2 * (i & 3);            // channel k, k+1 of word wd
+                const uint32_t sel = k < 4 ? 0x5410u : 0x7632u;      // bytes holding channels 0-3 / 4-7
+                const int sh = 4 * (k & 3);
+                const uint32_t lo = byte_perm(w[0][wd], w[1][wd], sel);  // tokens 2c | 2c+1
+                const uint32_t hi = byte_perm(w[2][wd], w[3][wd], sel);  // tokens 2c+8 | 2c+9
+                uint32_t a[4];
+                a[0] = nib2_to_f16x2(lo, sh);
+                a[1] = nib2_to_f16x2(lo, sh + 4);
+                a[2] = nib2_to_f16x2(hi, sh);
+                a[3] = nib2_to_f16x2(hi, sh + 4);
+                if (partial) mask_tokens(a, mk0, mk1);
+                mma_16816(o[i], a, pb0, pb1);
+            }
+        } else if (KV8) {
             constexpr int BPL = D / 8;  // bytes of a token row this lane reads (channels BPL r ..)
             uint32_t w[4][BPL / 4];     // tokens 2c, 2c+1, 2c+8, 2c+9
 #pragma unroll
@@ -261,7 +352,7 @@ struct MmaAttn {
 
     // Output channel of O^T fragment element (m-block i, upper half h).
     __device__ __forceinline__ int out_channel(int i, int h) const {
-        if (KV8) return (D / 8) * r + 2 * i + h;
+        if (KV8 || KV4) return (D / 8) * r + 2 * i + h;
         return 16 * i + r + 8 * h;
     }
 

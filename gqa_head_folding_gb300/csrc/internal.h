@@ -21,6 +21,8 @@ bool encode_tensor_map_2d(CUtensorMap *map, const void *base, uint64_t rows, uin
 // 128-byte swizzle: one TMA load brings box_rows whole rows (all their
 // 128-byte column blocks, interleaved row by row). cols: a multiple of 64.
 bool encode_tensor_map_kpage(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// fp32 matrix [rows][cols] (INT4 scale rows, cols * 4 a multiple of 16), box [1][box_cols].
+bool encode_tensor_map_f32_rows(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols);
 // Byte matrix [rows][cols] (E4M3 codes), box [box_rows][cols], swizzle 0, 64 or 128 bytes.
 bool encode_tensor_map_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                           int swizzle_bytes);
@@ -38,15 +40,19 @@ struct AttnArgs {
     float scale;
     bool kv8;             // caches hold E4M3 codes (dense only)
     float k_scale, v_scale;  // E4M3: value = code * scale
+    bool kv4;             // caches hold INT4 levels (dense only)
+    const float *k_scales, *v_scales;  // INT4: [B*Hkv][Lmax] per-token scales
     __half *out;
     void *workspace;
     size_t workspace_bytes;
 };
 int launch_attention(const AttnArgs &a, const LaunchCtx &ctx);
-// E4M3 cache append (kv_e4m3.cu).
+// E4M3 and INT4 cache appends (kv_lowbit.cu).
 int launch_append_e4m3(const gqaq_dims *d, uint8_t *k_cache, uint8_t *v_cache, const __half *k_new,
                        const __half *v_new, const int *pos, float k_inv_scale, float v_inv_scale,
                        const LaunchCtx &ctx);
+int launch_append_int4(const gqaq_dims *d, uint8_t *k_codes, float *k_scales, uint8_t *v_codes, float *v_scales,
+                       const __half *k_new, const __half *v_new, const int *pos, const LaunchCtx &ctx);
 size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx);
 
 // Causal chunk attention (prefill.cu): q_len new tokens per sequence, the

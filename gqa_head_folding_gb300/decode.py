@@ -11,8 +11,10 @@ each layer's page metadata stays current whatever path reads it.
 With ``kv="e4m3"`` the caches hold 8-bit E4M3 codes with one fp32 scale per
 tensor (``Layer.k_scale`` / ``v_scale``): appends quantize
 (``kv_append_e4m3``) and dense layers read them through
-``gqa_decode_attn_e4m3``. The Quest kernels take fp16 caches only, so an
-8-bit stack must be all dense.
+``gqa_decode_attn_e4m3``. With ``kv="int4"`` they hold 4-bit levels
+``[B,Hkv,Lmax,D/2]`` with one fp32 scale per token row (``Layer.k_scales`` /
+``v_scales``), through ``kv_append_int4`` and ``gqa_decode_attn_int4``. The
+Quest kernels take fp16 caches only, so a low-bit stack must be all dense.
 
 By default a Quest layer is one fused launch (``quest_decode_attn``: append,
 score, top-K and sparse attention in one kernel); the library picks its
@@ -30,9 +32,9 @@ from typing import List, Optional
 
 import torch
 
-from . import (alloc_workspace, gqa_decode_attn, gqa_decode_attn_e4m3, kv_append_e4m3, make_dims, new_meta,
-               num_pages, quest_append_kv, quest_decode_attn, quest_score_pages, quest_sparse_attn,
-               quest_topk_pages, quest_update_meta)
+from . import (alloc_workspace, gqa_decode_attn, gqa_decode_attn_e4m3, gqa_decode_attn_int4, kv_append_e4m3,
+               kv_append_int4, make_dims, new_meta, num_pages, quest_append_kv, quest_decode_attn, quest_score_pages,
+               quest_sparse_attn, quest_topk_pages, quest_update_meta)
 
 
 @dataclasses.dataclass
@@ -49,16 +51,18 @@ class Layer:
     pos: Optional[torch.Tensor] = None    # [B] int32 row the new token goes to
     k_scale: float = 1.0                  # E4M3 caches: value = code value * scale
     v_scale: float = 1.0
+    k_scales: Optional[torch.Tensor] = None  # INT4 caches: [B,Hkv,Lmax] fp32 per-token scales
+    v_scales: Optional[torch.Tensor] = None
 
 
 class DecodeStack:
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_len: int,
                  k_pages: Optional[int], dense_layers: int, device, page_size: int = 16, fused: bool = True,
                  kv: str = "f16", num_layers: Optional[int] = None):
-        if kv not in ("f16", "e4m3"):
-            raise ValueError(f"kv must be 'f16' or 'e4m3', got {kv!r}")
-        if kv == "e4m3" and k_pages is not None and (num_layers is None or num_layers > dense_layers):
-            raise ValueError("an E4M3 cache runs dense layers only (the Quest kernels read fp16 caches)")
+        if kv not in ("f16", "e4m3", "int4"):
+            raise ValueError(f"kv must be 'f16', 'e4m3' or 'int4', got {kv!r}")
+        if kv != "f16" and k_pages is not None and (num_layers is None or num_layers > dense_layers):
+            raise ValueError("a low-bit cache runs dense layers only (the Quest kernels read fp16 caches)")
         self.fused, self.kv = fused, kv
         self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
         self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
@@ -86,12 +90,17 @@ class DecodeStack:
     def append(self, L: Layer):
         if self.kv == "e4m3":
             kv_append_e4m3(L.k_cache, L.v_cache, L.k_new, L.v_new, L.pos, 1.0 / L.k_scale, 1.0 / L.v_scale)
+        elif self.kv == "int4":
+            kv_append_int4(L.k_cache, L.k_scales, L.v_cache, L.v_scales, L.k_new, L.v_new, L.pos)
         else:
             quest_append_kv(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos, self.page_size)
 
     def dense(self, L: Layer):
         if self.kv == "e4m3":
             gqa_decode_attn_e4m3(L.q, L.k_cache, L.v_cache, L.k_scale, L.v_scale, L.valid_len, self.scale,
+                                 out=L.out, workspace=self.workspace)
+        elif self.kv == "int4":
+            gqa_decode_attn_int4(L.q, L.k_cache, L.k_scales, L.v_cache, L.v_scales, L.valid_len, self.scale,
                                  out=L.out, workspace=self.workspace)
         else:
             gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale, out=L.out,

@@ -246,6 +246,32 @@ GQAQ_API int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_
                             const gqaq_half *v_new, const int32_t *pos, float k_inv_scale, float v_inv_scale,
                             void *stream);
 
+/* The 4-bit KV-cache variant (same [QUEST] "next steps"; the plainest
+ * format that keeps both contractions exact on integer levels): symmetric
+ * INT4 with one fp32 scale per (token, KV head) row.
+ *   k_codes, v_codes   [B][Hkv][Lmax][D/2] bytes: channel 2i of a row in the
+ *                      low nibble of byte i, high nibble channel 2i+1; a
+ *                      nibble holds level + 8, level in [-7, 7]
+ *   k_scales, v_scales [B][Hkv][Lmax] fp32; value = level * scale
+ * gqa_decode_attn_int4: [OPT] section 3's folded dense attention over such a
+ * cache (levels exact in fp16; the K scale multiplies each fp32 score, the V
+ * scale each token's probability). Same arguments, workspace and results as
+ * gqa_decode_attn otherwise. Needs max_len % 4 == 0 (scale rows are loaded
+ * as 16-byte multiples), else GQAQ_ERR_UNSUPPORTED. D in {64, 128}. */
+GQAQ_API int gqa_decode_attn_int4(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_codes,
+                                  const float *k_scales, const uint8_t *v_codes, const float *v_scales,
+                                  const int32_t *valid_len, float scale, gqaq_half *out, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* Append one token per (sequence, KV head) to an INT4 cache: for the fp16 row
+ * x = k_new[b][kv] ([B][Hkv][D]), scale = amax|x| / 7 and level =
+ * clamp(rne(x / scale), -7, 7) in fp32 (a zero row: scale 0, levels 0),
+ * written at row pos[b]; likewise v. pos[b] outside [0, Lmax) is skipped and
+ * raises GQAQ_DEV_BAD_POS. */
+GQAQ_API int kv_append_int4(const gqaq_dims *dims, uint8_t *k_codes, float *k_scales, uint8_t *v_codes,
+                            float *v_scales, const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos,
+                            void *stream);
+
 /* Prefill: causal attention of a chunk of q_len new tokens per sequence
  * ([OPT] "Prefill Needs Separate Design": for q_len > 1 the group axis is
  * merged into the sequence axis, so the G query heads of KV head kv and the

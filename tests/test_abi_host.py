@@ -129,6 +129,20 @@ def test_e4m3_calls_reject_bad_arguments(L):
         g.GQAQ_ERR_INVALID_ARG
 
 
+def test_int4_calls_reject_bad_arguments(L):
+    f = ctypes.c_float
+
+    def call(d, ks=FAKE, ws=FAKE):
+        return L.gqa_decode_attn_int4(ctypes.byref(d), FAKE, FAKE, ks, FAKE, FAKE, FAKE, f(0.1), FAKE, ws, 1 << 20,
+                                      None)
+    assert call(dims(max_len=4098)) == g.GQAQ_ERR_UNSUPPORTED      # scale rows need Lmax % 4 == 0
+    assert call(dims(), ks=MISALIGNED) == g.GQAQ_ERR_INVALID_ARG
+    assert call(dims(), ws=None) == g.GQAQ_ERR_WORKSPACE
+    assert call(dims(head_dim=96)) == g.GQAQ_ERR_UNSUPPORTED
+    assert L.kv_append_int4(ctypes.byref(dims()), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == \
+        g.GQAQ_ERR_INVALID_ARG
+
+
 def test_prefill_rejects_bad_arguments(L):
     d = dims(max_len=256)
     f = ctypes.c_float
