@@ -19,10 +19,14 @@
 //  - warp 8 (producer): TMA tile loads of K and V (both 128-byte swizzled;
 //    the E4M3 cache's byte rows 64- or 128-byte swizzled) into a shared-memory
 //    ring of 2-6 stages, with mbarrier completion.
-//  - warps 0-7 (consumers): warp w owns 16 tokens of each tile and runs both
-//    products on the tensor cores (MmaAttn: S^T = K Q^T and O^T += V^T P^T
-//    with mma.sync m16n8k16, the G folded rows on the N = 8 side), with the
-//    online softmax in the log2 domain on the S^T fragments.
+//  - warps 0-7 (consumers): fp16 stages: warp w owns 16 tokens of each
+//    stage. Low-bit stages: warps 0-3 take the even stages, 4-7 the odd ones
+//    (an even ring, so a stage always has the same consumers), and a warp
+//    owns 32 tokens of its stages (two 16-token sub-tiles whose MMA chains
+//    overlap). Either way a warp runs both products on the tensor cores (MmaAttn:
+//    S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16, the G folded rows
+//    on the N = 8 side), with the online softmax in the log2 domain on the
+//    S^T fragments.
 //  - at the end of each unit segment the 8 warp states merge in shared
 //    memory. A segment that covers its whole unit writes the fp16 output. A
 //    segment cut by a range boundary writes an fp32 partial (m, l, acc) and
@@ -47,12 +51,19 @@ struct AttnCfg : TileCfg<D, G> {
     static constexpr int FIXED = T::QBYTES + T::MERGE + T::PBYTES + MISC;
     static constexpr int KBYTES = KV == 1 ? T::TILE * D : KV == 2 ? T::TILE * D / 2 + T::TILE * 4 : T::KBYTES;
     static constexpr int STAGE = KV != 0 ? 2 * KBYTES : T::STAGE;
-    // 8-bit tiles: the deepest ring of at most six stages that fits (two CTAs
-    // per SM at D = 64, one at D = 128).
+    // Low-bit tiles: the deepest even ring of at most six (E4M3) or eight
+    // (INT4) stages that fits (two CTAs per SM at D = 64, one at D = 128: at
+    // D = 128 two CTAs would leave E4M3 a two-stage ring, measured slower).
     static constexpr int LIMIT8 = (D == 64 ? 112 : 225) * 1024 - FIXED - 1024;
     static constexpr int MAXST = KV == 2 ? 8 : 6;
-    static constexpr int NSTAGE8 = LIMIT8 / STAGE < MAXST ? LIMIT8 / STAGE : MAXST;
+    static constexpr int NSTAGE8 = (LIMIT8 / STAGE < MAXST ? LIMIT8 / STAGE : MAXST) & ~1;
     static constexpr int NSTAGE = KV != 0 ? NSTAGE8 : ((3 * STAGE + FIXED + 1024 <= 225 * 1024) ? 3 : 2);
+    // Low-bit variants: warps 0-3 consume the even stages and warps 4-7 the
+    // odd ones, 32 tokens per warp. A stage must then always belong to the
+    // same group (an even ring), or a group that skips one of a stage's phases
+    // could pass its parity wait a phase early.
+    static constexpr bool ALT = KV != 0;
+    static_assert(!ALT || NSTAGE % 2 == 0, "alternating warp groups need an even ring");
     static constexpr int SMEM = 1024 + NSTAGE * STAGE + FIXED;
     static constexpr int MIN_BLOCKS = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
     static_assert(NSTAGE >= 2, "at least a double-buffered ring");
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
     if (warp == C::NCW && lane == 0) {
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), C::NCW);
+            mbar_init(smem_u32(&empty[s]), C::ALT ? C::NCW / 2 : C::NCW);  // the warps that consume a stage
         }
         fence_mbar_init();
         prefetch_tensormap(&kmap);
@@ -458,6 +469,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
         wa.reset();
 
         for (int t = 0; t < n; ++t, ++i) {
+            if (C::ALT && (i & 1) != (warp >> 2)) continue;  // low-bit: warps 0-3 even stages, 4-7 odd
             const int s = i % C::NSTAGE;
             const uint32_t ph = (uint32_t)(i / C::NSTAGE) & 1u;
             bool ok = (*abort_flag == 0);
@@ -469,21 +481,32 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
                     *abort_flag = 1;
                 }
             }
+            // this warp's rows of the stage: NS sub-tiles of 16 (virtual warps vw)
+            constexpr int NS = C::ALT ? 2 : 1;
             const int local = w.local + t;
-            int nvalid = 0;
-            if (SPARSE) {
-                const int e = local * slots.ppt + slots.warp_page(warp);
-                if (e < nsel) {
-                    const int page = p.page_idx[(int64_t)unit * p.kpages + e];
-                    if (page >= 0 && page < P) nvalid = slots.warp_rows(warp, page, len);
+            int nv[NS];
+#pragma unroll
+            for (int h = 0; h < NS; ++h) {
+                nv[h] = 0;
+                const int vw = C::ALT ? 2 * (warp & 3) + h : warp;
+                if (SPARSE) {
+                    const int e = local * slots.ppt + slots.warp_page(vw);
+                    if (e < nsel) {
+                        const int page = p.page_idx[(int64_t)unit * p.kpages + e];
+                        if (page >= 0 && page < P) nv[h] = slots.warp_rows(vw, page, len);
+                    }
+                } else {
+                    const int rem = len - (local * C::TILE + vw * C::SUB);
+                    nv[h] = rem < 0 ? 0 : (rem < C::SUB ? rem : C::SUB);
                 }
-            } else {
-                const int rem = len - (local * C::TILE + warp * C::SUB);
-                nvalid = rem < 0 ? 0 : (rem < C::SUB ? rem : C::SUB);
             }
-            if (ok && nvalid > 0) {
+            int nsum = 0;
+#pragma unroll
+            for (int h = 0; h < NS; ++h) nsum += nv[h];
+            if (ok && nsum > 0) {
                 const uint32_t kbase = smem_u32(stages + s * C::STAGE);
-                wa.tile(kbase, kbase + C::KBYTES, nvalid, p.scale_log2, q_s);
+                wa.template tile_n<NS>(kbase, kbase + C::KBYTES, C::ALT ? 32 * (warp & 3) : 16 * warp, nv,
+                                       p.scale_log2);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));

@@ -152,13 +152,9 @@ struct MmaAttn {
         }
     }
 
-    // One 16-token sub-tile. kbase/vbase: shared addresses of the stage's K and
-    // V; nvalid: valid tokens (a prefix) of this warp's 16 rows, 1..16.
-    __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, float scale_log2,
-                                         const __half * /*q_s*/) {
-        const int row0 = cw * C::SUB;
-        // ---- 1. S^T = K . Q^T ----
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T of the 16 stage rows row0 .. row0+15 (K scales applied for INT4) ----
+    __device__ __forceinline__ void qk(uint32_t kbase, int row0, float (&s)[4]) const {
+        s[0] = s[1] = s[2] = s[3] = 0.f;
         if constexpr (KV4) {
             constexpr int NW = D / 32;  // words of a row this lane decodes (D/4 channels)
             uint32_t wa[NW], wb[NW];
@@ -218,53 +214,14 @@ struct MmaAttn {
                 mma_16816(s, a, qb[j][0], qb[j][1]);
             }
         }
-        // ---- 2. online softmax per query column (log2 domain) ----
-        // s[0], s[1]: token r, columns 2c, 2c+1; s[2], s[3]: token r + 8.
-        const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
-        float x[4];
-        x[0] = v0 ? s[0] * scale_log2 : -INFINITY;
-        x[1] = v0 ? s[1] * scale_log2 : -INFINITY;
-        x[2] = v1 ? s[2] * scale_log2 : -INFINITY;
-        x[3] = v1 ? s[3] * scale_log2 : -INFINITY;
-        float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
-#pragma unroll
-        for (int o_ = 4; o_ < 32; o_ <<= 1) {
-            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o_));
-            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o_));
-        }
-        const float mn0 = fmaxf(m[0], t0), mn1 = fmaxf(m[1], t1);  // token 0 is valid: finite
-        const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
-        m[0] = mn0;
-        m[1] = mn1;
-        const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
-        const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
-        l[0] = l[0] * al0 + (p0 + p2);
-        l[1] = l[1] * al1 + (p1 + p3);
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-            for (int i = 0; i < KS; ++i) {
-                o[i][0] *= al0;
-                o[i][1] *= al1;
-                o[i][2] *= al0;
-                o[i][3] *= al1;
-            }
-        }
-        // ---- 3. P^T as the B operand: fp16, transposed 8x8 halves ----
-        float w0 = 1.f, w1 = 1.f;  // INT4: each token's V scale rides on its probability
-        if constexpr (KV4) {
-            const float vs0 = __uint_as_float(lds32(vbase + (uint32_t)(CODE4 + (row0 + r) * 4)));
-            const float vs1 = __uint_as_float(lds32(vbase + (uint32_t)(CODE4 + (row0 + r + 8) * 4)));
-            w0 = v0 ? vs0 : 0.f;  // a row past nvalid may hold any scale bits
-            w1 = v1 ? vs1 : 0.f;
-        }
-        const uint32_t pb0 = movmatrix_trans(pack_half2(p0 * w0, p1 * w0));  // tokens 2c, 2c+1 of column r
-        const uint32_t pb1 = movmatrix_trans(pack_half2(p2 * w1, p3 * w1));  // tokens 8+2c, 8+2c+1
-        // Rows past nvalid may hold anything (even NaN codes): their V^T
-        // entries are zeroed, since 0 * NaN would poison the sum.
-        const bool partial = nvalid < C::SUB;  // warp-uniform
-        const uint32_t mk0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t mk1 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
-        // ---- 4. O^T += V^T . P^T ----
+    }
+
+    // ---- O^T += V^T . P^T over the 16 stage rows row0 .. row0+15 ----
+    // Rows past the valid prefix may hold anything (even NaN codes): with
+    // `partial` their V^T entries are zeroed by mk0 / mk1, since 0 * NaN
+    // would poison the sum.
+    __device__ __forceinline__ void pv(uint32_t vbase, int row0, uint32_t pb0, uint32_t pb1, bool partial,
+                                       uint32_t mk0, uint32_t mk1) {
         if constexpr (KV4) {
             constexpr int NW = D / 64;  // words of a token row this lane reads (channels (D/8) r ..)
             uint32_t w[4][NW];          // tokens 2c, 2c+1, 2c+8, 2c+9
@@ -339,6 +296,85 @@ struct MmaAttn {
                 if (partial) mask_tokens(a, mk0, mk1);
                 mma_16816(o[i], a, pb0, pb1);
             }
+        }
+    }
+
+    // NS sub-tiles of 16 stage rows each, from row0 (a multiple of 16), with
+    // one online-softmax step over all 16 NS tokens. kbase/vbase: shared
+    // addresses of the stage's K and V; nv[h]: valid tokens (a prefix) of
+    // sub-tile h, 0..16, at least one of them nonzero. The sub-tiles' MMA
+    // chains are independent, so the scheduler overlaps them.
+    template <int NS>
+    __device__ __forceinline__ void tile_n(uint32_t kbase, uint32_t vbase, int row0, const int (&nv)[NS],
+                                           float scale_log2) {
+        // ---- 1. S^T = K . Q^T per sub-tile ----
+        float s[NS][4];
+#pragma unroll
+        for (int h = 0; h < NS; ++h) qk(kbase, row0 + 16 * h, s[h]);
+        // ---- 2. online softmax per query column (log2 domain) ----
+        // s[h][0], s[h][1]: token r of sub-tile h, columns 2c, 2c+1; s[h][2], s[h][3]: token r + 8.
+        bool v0[NS], v1[NS];
+        float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < NS; ++h) {
+            v0[h] = r < nv[h];
+            v1[h] = r + 8 < nv[h];
+            s[h][0] = v0[h] ? s[h][0] * scale_log2 : -INFINITY;
+            s[h][1] = v0[h] ? s[h][1] * scale_log2 : -INFINITY;
+            s[h][2] = v1[h] ? s[h][2] * scale_log2 : -INFINITY;
+            s[h][3] = v1[h] ? s[h][3] * scale_log2 : -INFINITY;
+            t0 = fmaxf(t0, fmaxf(s[h][0], s[h][2]));
+            t1 = fmaxf(t1, fmaxf(s[h][1], s[h][3]));
+        }
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o_));
+            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o_));
+        }
+        const float mn0 = fmaxf(m[0], t0), mn1 = fmaxf(m[1], t1);  // some token is valid: finite
+        const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
+        m[0] = mn0;
+        m[1] = mn1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < NS; ++h) {
+            s[h][0] = fast_exp2(s[h][0] - mn0);
+            s[h][1] = fast_exp2(s[h][1] - mn1);
+            s[h][2] = fast_exp2(s[h][2] - mn0);
+            s[h][3] = fast_exp2(s[h][3] - mn1);
+            ps0 += s[h][0] + s[h][2];
+            ps1 += s[h][1] + s[h][3];
+        }
+        l[0] = l[0] * al0 + ps0;
+        l[1] = l[1] * al1 + ps1;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                o[i][0] *= al0;
+                o[i][1] *= al1;
+                o[i][2] *= al0;
+                o[i][3] *= al1;
+            }
+        }
+        // ---- 3. P^T as the B operand: fp16, transposed 8x8 halves; 4. O^T += V^T . P^T ----
+#pragma unroll
+        for (int h = 0; h < NS; ++h) {
+            if (NS > 1 && nv[h] == 0) continue;  // warp-uniform: nothing valid in this sub-tile
+            const int rh = row0 + 16 * h;
+            float w0 = 1.f, w1 = 1.f;  // INT4: each token's V scale rides on its probability
+            if constexpr (KV4) {
+                const float vs0 = __uint_as_float(lds32(vbase + (uint32_t)(CODE4 + (rh + r) * 4)));
+                const float vs1 = __uint_as_float(lds32(vbase + (uint32_t)(CODE4 + (rh + r + 8) * 4)));
+                w0 = v0[h] ? vs0 : 0.f;  // a row past the prefix may hold any scale bits
+                w1 = v1[h] ? vs1 : 0.f;
+            }
+            const uint32_t pb0 = movmatrix_trans(pack_half2(s[h][0] * w0, s[h][1] * w0));  // tokens 2c, 2c+1
+            const uint32_t pb1 = movmatrix_trans(pack_half2(s[h][2] * w1, s[h][3] * w1));  // tokens 8+2c, 8+2c+1
+            const int n = nv[h];
+            const bool partial = n < C::SUB;  // warp-uniform
+            const uint32_t mk0 = (2 * c < n ? 0x0000ffffu : 0u) | (2 * c + 1 < n ? 0xffff0000u : 0u);
+            const uint32_t mk1 = (2 * c + 8 < n ? 0x0000ffffu : 0u) | (2 * c + 9 < n ? 0xffff0000u : 0u);
+            pv(vbase, rh, pb0, pb1, partial, mk0, mk1);
         }
     }
 
