@@ -43,6 +43,7 @@ GQAQ_OPT_CLUSTER_SIZE = 4
 GQAQ_OPT_PDL = 5
 GQAQ_OPT_QUEST_KERNEL = 6
 GQAQ_OPT_PREFILL_SPLITS = 7
+GQAQ_OPT_PREFILL_KERNEL = 8
 
 PAGE_SIZE = 16
 

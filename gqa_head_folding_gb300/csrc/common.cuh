@@ -28,6 +28,7 @@ struct LaunchCtx {
     int pdl;               // launch with programmatic stream serialization
     int quest_kernel;      // fused Quest kernel: 0 automatic, 1 cluster, 2 work queue
     int prefill_splits;    // prefill context splits per item: 0 automatic, n forced
+    int prefill_kernel;    // prefill kernel: 0 automatic (tensor memory), 1 tensor memory, 2 warp MMA
     int *status;           // device status word
 };
 

@@ -382,22 +382,517 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::MIN_BLO
     }
 }
 
-constexpr int kMaxDevices = 64;
+// ===========================================================================
+// Tensor-memory kernel (tcgen05): the same work items, splits and merge as
+// prefill_kernel, with both products on the 5th-generation tensor cores.
+//  - warp 4 (TMA): the item's Q block once, then K and V tiles of 128 tokens
+//    (128-byte-swizzled 64-column boxes) into a 3-5 stage ring.
+//  - warp 5 (MMA, one thread): S_j = Q K_j^T (M = 128 rows, N = 128 tokens,
+//    K = D; both operands K-major in shared memory) into one of two TMEM S
+//    buffers, and O += P_j V_j (A = P_j from TMEM, B = V_j MN-major in shared
+//    memory, N = 64 per 64-channel block) into the TMEM O block. Issue order
+//    S_0, S_1, PV_0, S_2, PV_1, ...: the S of the next tile overlaps the
+//    softmax of this one, and each S buffer is rewritten only after the PV
+//    that read its P (the tensor core runs one thread's MMAs in order).
+//    Completions arrive on mbarriers through tcgen05.commit.
+//  - warps 0-3 (softmax, one thread per row): read the row's 128 scores from
+//    TMEM, mask the causal limit, keep a lazy reference max (rescaling O in
+//    TMEM only when the row max grows by more than 2^8, so P stays <= 256 in
+//    fp16), write P as fp16 over its S buffer, and at the end read O.
+//  - TMEM (512 columns): S buffers at columns 0 and 128, O at 256.
+// ===========================================================================
+template <int D>
+struct TcCfg {
+    static constexpr int THREADS = 192;
+    static constexpr int RB = 128;                // rows per item (TMEM lanes)
+    static constexpr int TT = 128;                // tokens per stage (N of S)
+    static constexpr int KH = D / 64;
+    static constexpr int KBLK = TT * 128;         // one 64-column block of a K or V tile
+    static constexpr int KBYTES = KH * KBLK;      // = TT * D * 2
+    static constexpr int STAGE = 2 * KBYTES;
+    static constexpr int QBLK = RB * 128;
+    static constexpr int QBYTES = KH * QBLK;
+    static constexpr int NSTAGE = D == 128 ? 3 : 5;
+    static constexpr int MISC = 512;
+    static constexpr int SMEM = 1024 + QBYTES + NSTAGE * STAGE + MISC;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int S_COL = 0, O_COL = 256;
+    static constexpr float RESCALE_LOG2 = 8.f;    // lazy reference: P <= 2^8
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(RB * kPrefillMaxSplits * 4 <= NSTAGE * STAGE, "merge weights fit the idle ring");
+};
+
+// Shared-memory matrix descriptor: 128-byte swizzle, SBO = 1024 (8 rows of
+// 128 B), LBO = lbo (the MN-direction block stride of an MN-major operand;
+// not used by K-major operands whose K slice stays inside one 128-byte row).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, M x N, B K- or MN-major.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, int acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// One warp's bounded wait (lane 0 waits, the warp follows): false on timeout or abort.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const PrefillParams &p,
+                                          volatile int *abort_flag, int lane) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(bar, parity, p.timeout_ns, abort_flag);
+    return __shfl_sync(0xffffffffu, ok, 0);
+}
 
 template <int D>
+__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    using C = TcCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sq = smem;
+    uint8_t *stages = sq + C::QBYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(stages + C::NSTAGE * C::STAGE);
+    uint64_t *empty = full + C::NSTAGE;
+    uint64_t *qbar = empty + C::NSTAGE;
+    uint64_t *s_ready = qbar + 1;   // [2]
+    uint64_t *p_ready = s_ready + 2;  // [2]
+    uint64_t *o_done = p_ready + 2;  // [2]: PV_j completes on o_done[j & 1]
+    uint64_t *drain = o_done + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+    int *last_flag = reinterpret_cast<int *>(tslot + 2);
+    float *wbuf = reinterpret_cast<float *>(stages);  // merge weights, once the ring is idle
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 4 && lane == 0) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(qbar), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&s_ready[b]), 1);
+            mbar_init(smem_u32(&p_ready[b]), 4);  // one arrival per softmax warp
+        }
+        mbar_init(smem_u32(&o_done[0]), 1);
+        mbar_init(smem_u32(&o_done[1]), 1);
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "n"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    pdl_wait_and_release();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+
+    // ---- the work item and this CTA's slice of its context tiles ----
+    const int item = blockIdx.x / p.splits, split = blockIdx.x - (blockIdx.x / p.splits) * p.splits;
+    const int rb = item % p.nrb, unit = item / p.nrb;  // unit = b * Hkv + kv
+    const int b = unit / p.Hkv;
+    const int rho0 = rb * C::RB;
+    const int nrows = (p.R - rho0) < C::RB ? (p.R - rho0) : C::RB;
+    const int st = p.start[b];
+    const bool good = st >= 0 && st <= p.Lmax - p.q_len;
+    if (!good && threadIdx.x == 0 && split == 0 && rb == 0 && unit % p.Hkv == 0) raise_flag(p.status, GQAQ_DEV_BAD_POS);
+    const int t_first = rho0 % p.q_len, t_last = (rho0 + nrows - 1) % p.q_len;
+    const bool wraps = nrows >= p.q_len || t_first > t_last;
+    const int t_max = wraps ? p.q_len - 1 : t_last, t_min = wraps ? 0 : t_first;
+    const int nt = good ? (st + t_max + C::TT) / C::TT : 0;
+    const int j0 = (int)(((int64_t)split * nt) / p.splits), j1 = (int)(((int64_t)(split + 1) * nt) / p.splits);
+    const int n = j1 - j0;
+    const int kv_end = st + p.q_len;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------------
+        // TMA producer
+        // ------------------------------------------------------------------
+        if (lane == 0 && n > 0 && !p.test_stall) {
+            const uint64_t pol = l2_policy_evict_first();
+            mbar_arrive_expect_tx(smem_u32(qbar), (uint32_t)C::QBYTES);
+            const int qrow = unit * p.R + rho0;
+#pragma unroll
+            for (int kh = 0; kh < C::KH; ++kh)
+                tma_load_2d(smem_u32(sq) + kh * C::QBLK, &qmap, 64 * kh, qrow, smem_u32(qbar), pol);
+            int i = 0;
+            bool failed = false;
+            for (; i < n; ++i) {
+                const int s = i % C::NSTAGE;
+                if (i >= C::NSTAGE && !mbar_wait(smem_u32(&empty[s]), ((uint32_t)(i / C::NSTAGE) & 1u) ^ 1u,
+                                                 p.timeout_ns, abort_flag)) {
+                    failed = true;
+                    break;
+                }
+                const uint32_t kdst = smem_u32(stages + s * C::STAGE), vdst = kdst + C::KBYTES;
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
+                const int y = unit * p.Lmax + (j0 + i) * C::TT;
+#pragma unroll
+                for (int kh = 0; kh < C::KH; ++kh) {
+                    tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
+                    tma_load_2d(vdst + kh * C::KBLK, &vmap, 64 * kh, y, fb, pol);
+                }
+            }
+            if (failed) {
+                raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                *abort_flag = 1;
+                const int first = i - C::NSTAGE > 0 ? i - C::NSTAGE : 0;
+                for (int it = first; it < i; ++it)
+                    mbar_wait(smem_u32(&full[it % C::NSTAGE]), (uint32_t)(it / C::NSTAGE) & 1u, p.timeout_ns, nullptr);
+                mbar_wait(smem_u32(qbar), 0u, p.timeout_ns, nullptr);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------------
+        // MMA issuer (one thread)
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            bool fail = false;
+            if (n > 0) {
+                fail = !mbar_wait(smem_u32(qbar), 0u, p.timeout_ns, abort_flag);
+                constexpr uint32_t IDESC_S = umma_idesc(128, C::TT, 0);
+                constexpr uint32_t IDESC_O = umma_idesc(128, 64, 1);
+                for (int idx = 0; idx <= n && !fail; ++idx) {
+                    if (idx < n) {
+                        const int s = idx % C::NSTAGE;
+                        if (!mbar_wait(smem_u32(&full[s]), (uint32_t)(idx / C::NSTAGE) & 1u, p.timeout_ns, abort_flag)) {
+                            fail = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t kst = smem_u32(stages + s * C::STAGE);
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t off = (uint32_t)((ks >> 2) * C::QBLK + (ks & 3) * 32);
+                            const uint32_t koff = (uint32_t)((ks >> 2) * C::KBLK + (ks & 3) * 32);
+                            umma_ss(tbase + C::S_COL + 128u * (idx & 1), umma_desc(smem_u32(sq) + off, 16),
+                                    umma_desc(kst + koff, 16), IDESC_S, ks > 0);
+                        }
+                        umma_commit(smem_u32(&s_ready[idx & 1]));
+                    }
+                    if (idx >= 1) {
+                        const int jj = idx - 1;
+                        if (!mbar_wait(smem_u32(&p_ready[jj & 1]), (uint32_t)(jj >> 1) & 1u, p.timeout_ns, abort_flag)) {
+                            fail = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int s = jj % C::NSTAGE;
+                        const uint32_t vst = smem_u32(stages + s * C::STAGE) + C::KBYTES;
+#pragma unroll
+                        for (int kk = 0; kk < C::TT / 16; ++kk) {
+#pragma unroll
+                            for (int nb = 0; nb < C::KH; ++nb)
+                                umma_ts(tbase + C::O_COL + 64u * nb, tbase + C::S_COL + 128u * (jj & 1) + 8u * kk,
+                                        umma_desc(vst + nb * C::KBLK + kk * 16 * 128, C::KBLK), IDESC_O,
+                                        (jj > 0 || kk > 0) ? 1 : 0);
+                        }
+                        umma_commit(smem_u32(&o_done[jj & 1]));
+                        umma_commit(smem_u32(&empty[s]));
+                    }
+                }
+            }
+            if (fail) {
+                raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every issued MMA completes before TMEM is released
+            if (n > 0) {
+                umma_commit(smem_u32(drain));
+                mbar_wait(smem_u32(drain), 0u, p.timeout_ns, nullptr);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // Softmax and epilogue: thread tid owns row tid of the item (TMEM lane)
+        // ------------------------------------------------------------------
+        const int tid = threadIdx.x;  // 0..127
+        const bool live = tid < nrows;
+        const int lim = st + (rho0 + tid) % p.q_len;
+        const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        // PV_j's completion, on o_done[j & 1]: its previous use (PV_{j-2}) has
+        // completed whenever this is asked (S_{j+1} has, and MMAs complete in
+        // order) and its next (PV_{j+2}) is not issued yet, so the parity wait
+        // is never more than one phase behind.
+        auto wait_pv = [&](int j) {
+            return warp_wait(smem_u32(&o_done[j & 1]), (uint32_t)(j >> 1) & 1u, p, abort_flag, lane);
+        };
+        for (int idx = 0; idx < n; ++idx) {
+            ok = ok && warp_wait(smem_u32(&s_ready[idx & 1]), (uint32_t)(idx >> 1) & 1u, p, abort_flag, lane);
+            if (!ok) {
+                if (lane == 0) {
+                    raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            const int tok0 = (j0 + idx) * C::TT;
+            const bool need_mask = tok0 + C::TT - 1 > st + t_min;  // uniform over the item
+            const uint32_t scol = trow + C::S_COL + 128u * (idx & 1);
+            // pass 1: the row max of this tile (log2 domain)
+            float mx = -INFINITY;
+#pragma unroll
+            for (int ch = 0; ch < C::TT / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(scol + 32u * ch, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float x = __uint_as_float(v[e]) * p.scale_log2;
+                    if (need_mask && tok0 + 32 * ch + e > lim) x = -INFINITY;
+                    mx = fmaxf(mx, x);
+                }
+            }
+            // lazy reference: move it (and rescale l, O) only when the max grows by > 2^8
+            float alpha = 1.f;
+            bool resc = false;
+            if (mx > m_ref + C::RESCALE_LOG2) {
+                alpha = fast_exp2(m_ref - mx);  // 0 when m_ref is -inf
+                m_ref = mx;
+                l *= alpha;
+                resc = idx > 0;
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+                // O holds PV_0 .. PV_{idx-1}: wait for the last of them
+                ok = wait_pv(idx - 1);
+                if (!ok) {
+                    if (lane == 0) {
+                        raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(trow + C::O_COL + 32u * ch, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st32(trow + C::O_COL + 32u * ch, v);
+                }
+                tmem_wait_st();
+            }
+            // pass 2: P = 2^(x - m_ref) as fp16 over the S buffer (pairs, low half = even token)
+            const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+            float ps = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < C::TT / 32; ++ch) {
+                uint32_t v[32], pk[16];
+                tmem_ld32(scol + 32u * ch, v);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float x0 = __uint_as_float(v[e]) * p.scale_log2, x1 = __uint_as_float(v[e + 1]) * p.scale_log2;
+                    if (need_mask) {
+                        x0 = tok0 + 32 * ch + e > lim ? -INFINITY : x0;
+                        x1 = tok0 + 32 * ch + e + 1 > lim ? -INFINITY : x1;
+                    }
+                    const float e0 = fast_exp2(x0 - ref), e1 = fast_exp2(x1 - ref);
+                    ps += e0 + e1;
+                    pk[e >> 1] = pack_half2(e0, e1);
+                }
+                tmem_st16(scol + 16u * ch, pk);
+            }
+            l += ps;
+            tmem_wait_st();
+            if (tok0 + C::TT > kv_end && tok0 + tid >= kv_end) {
+                // rows past the chunk may hold anything: zero them so 0 * NaN cannot reach O
+                uint8_t *vrow = stages + (idx % C::NSTAGE) * C::STAGE + C::KBYTES + tid * 128;
+#pragma unroll
+                for (int kh = 0; kh < C::KH; ++kh)
+#pragma unroll
+                    for (int q16 = 0; q16 < 8; ++q16)
+                        *reinterpret_cast<uint4 *>(vrow + kh * C::KBLK + 16 * q16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // zeroed rows reach the tensor core
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&p_ready[idx & 1]));
+        }
+        // ---- epilogue: O after the last PV ----
+        if (ok && n > 0) {
+            ok = wait_pv(n - 1);  // PV_{n-1} done: every PV is (in-order completion)
+            if (!ok && lane == 0) {
+                raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        tc_fence_after();
+        __half *ob = p.out + ((int64_t)unit * p.R + rho0) * D;
+        float *pml = p.part + (int64_t)blockIdx.x * C::RB * (D + 2);
+        float *pacc = pml + 2 * C::RB;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (p.splits > 1 && live) reinterpret_cast<float2 *>(pml)[tid] = make_float2(m_ref, l);
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t v[32];
+            if (ok && n > 0) {
+                tmem_ld32(trow + C::O_COL + 32u * ch, v);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+            if (!live) continue;
+            if (p.splits == 1) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 h;
+                    h.x = pack_half2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                    h.y = pack_half2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                    h.z = pack_half2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                    h.w = pack_half2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(ob + (int64_t)tid * D + 32 * ch + e) = h;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(pacc + (int64_t)tid * D + 32 * ch + e) =
+                        make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                    __uint_as_float(v[e + 3]));
+            }
+        }
+    }
+
+    // ---- all roles meet: the ring is idle, every MMA has completed ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(C::TMEM_COLS));
+    if (p.splits == 1 || warp >= 4) return;
+
+    // ---- split: arrival, and the last arrival's merge (the 128 softmax threads) ----
+    constexpr int NCT = 128;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        // __syncthreads above orders every thread's partial stores before this
+        // release; the item's last arrival acquires all of them.
+        const unsigned old = atomic_add_acq_rel_gpu(&p.count[item], 1u);
+        const int last = old + 1u == (unsigned)p.splits;
+        if (last) p.count[item] = 0u;
+        *last_flag = last;
+    }
+    named_bar_sync(1, NCT);
+    if (!*last_flag) return;
+    __half *ob = p.out + ((int64_t)unit * p.R + rho0) * D;
+    const float *base = p.part + (int64_t)item * p.splits * C::RB * (D + 2);
+    for (int row = tid; row < nrows; row += NCT) {
+        float mst = -INFINITY;
+        for (int sp = 0; sp < p.splits; ++sp)
+            mst = fmaxf(mst, __ldcg(base + (int64_t)sp * C::RB * (D + 2) + 2 * row));
+        float L = 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(base + (int64_t)sp * C::RB * (D + 2)) + row);
+            const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mst);
+            wbuf[row * kPrefillMaxSplits + sp] = f;
+            L += f * ml.y;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) wbuf[row * kPrefillMaxSplits + sp] *= inv;
+    }
+    named_bar_sync(1, NCT);
+    for (int e = tid; e < nrows * (D / 4); e += NCT) {
+        const int row = e / (D / 4), d4 = e - (e / (D / 4)) * (D / 4);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < p.splits; ++sp) {
+            const float w = wbuf[row * kPrefillMaxSplits + sp];
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(base + (int64_t)sp * C::RB * (D + 2) + 2 * C::RB +
+                                                                     (int64_t)row * D) + d4);
+            a.x += w * x.x;
+            a.y += w * x.y;
+            a.z += w * x.z;
+            a.w += w * x.w;
+        }
+        __half2 *dst = reinterpret_cast<__half2 *>(ob + (int64_t)row * D + 4 * d4);
+        dst[0] = __floats2half2_rn(a.x, a.y);
+        dst[1] = __floats2half2_rn(a.z, a.w);
+    }
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int D, bool TC>
 int blocks_per_sm(const LaunchCtx &ctx) {
-    using C = PrefillCfg<D>;
     static int occ[kMaxDevices] = {0};
     if (ctx.device < 0 || ctx.device >= kMaxDevices) return -1;
     if (occ[ctx.device] == 0) {
-        if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-            cudaSuccess)
-            return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_kernel<D>, C::THREADS, C::SMEM) !=
-                cudaSuccess ||
-            n < 1)
-            return -1;
+        cudaError_t e;
+        if constexpr (TC) {
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::SMEM);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_tc_kernel<D>, TcCfg<D>::THREADS,
+                                                                  TcCfg<D>::SMEM);
+        } else {
+            e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PrefillCfg<D>::SMEM);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_kernel<D>, PrefillCfg<D>::THREADS,
+                                                                  PrefillCfg<D>::SMEM);
+        }
+        if (e != cudaSuccess || n < 1) return -1;
         occ[ctx.device] = n;
     }
     return occ[ctx.device];
@@ -405,45 +900,49 @@ int blocks_per_sm(const LaunchCtx &ctx) {
 
 // Context splits per item: enough CTAs to cover the GPU's resident slots,
 // at least two tiles per split, at most kPrefillMaxSplits (or the forced value).
-template <int D>
+template <int D, bool TC>
 int splits_for(const gqaq_dims &dm, int q_len, const LaunchCtx &ctx) {
-    const int occ = blocks_per_sm<D>(ctx);
+    const int occ = blocks_per_sm<D, TC>(ctx);
     if (occ < 1) return -1;
     const int64_t items = prefill_items(dm, q_len);
     if (ctx.prefill_splits > 0) return ctx.prefill_splits < kPrefillMaxSplits ? ctx.prefill_splits : kPrefillMaxSplits;
     const int64_t slots = (int64_t)occ * ctx.num_sms;
     int64_t s = (slots + items - 1) / items;
-    const int64_t tiles = ((int64_t)dm.max_len + PrefillCfg<D>::TT - 1) / PrefillCfg<D>::TT;
+    const int tt = TC ? TcCfg<D>::TT : PrefillCfg<D>::TT;
+    const int64_t tiles = ((int64_t)dm.max_len + tt - 1) / tt;
     const int64_t cap = tiles / 2 > 1 ? tiles / 2 : 1;
     if (s > cap) s = cap;
     if (s > kPrefillMaxSplits) s = kPrefillMaxSplits;
     return (int)(s < 1 ? 1 : s);
 }
 
+// Workspace for either kernel: the counters, then partials for the larger split.
 template <int D>
 size_t ws_bytes(const gqaq_dims &dm, int q_len, const LaunchCtx &ctx) {
-    const int s = splits_for<D>(dm, q_len, ctx);
-    if (s < 1) return 0;
+    const int s0 = splits_for<D, false>(dm, q_len, ctx), s1 = splits_for<D, true>(dm, q_len, ctx);
+    if (s0 < 1 || s1 < 1) return 0;
+    const int s = s0 > s1 ? s0 : s1;
     const int64_t items = prefill_items(dm, q_len);
     const size_t zero = ((size_t)items * 4 + 255) / 256 * 256;
     return zero + (s > 1 ? (size_t)items * s * PrefillCfg<D>::RB * (D + 2) * sizeof(float) : 0);
 }
 
-template <int D>
+template <int D, bool TC>
 int launch_d(const PrefillArgs &a, const LaunchCtx &ctx) {
     using C = PrefillCfg<D>;
     const gqaq_dims &dm = *a.dims;
-    const int splits = splits_for<D>(dm, a.q_len, ctx);
+    const int splits = splits_for<D, TC>(dm, a.q_len, ctx);
     if (splits < 1) return GQAQ_ERR_CUDA;
     const size_t need = ws_bytes<D>(dm, a.q_len, ctx);
     if (a.workspace == nullptr || a.workspace_bytes < need) return GQAQ_ERR_WORKSPACE;
     const int64_t items = prefill_items(dm, a.q_len);
     if (items * splits > INT32_MAX) return GQAQ_ERR_UNSUPPORTED;
 
+    const int tt = TC ? TcCfg<D>::TT : C::TT;
     const uint64_t rows = (uint64_t)dm.batch * dm.num_kv_heads * dm.max_len;
-    CUtensorMap kmap, vmap;
-    if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, C::TT, true)) return GQAQ_ERR_CUDA;
-    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, 64, C::TT, true)) return GQAQ_ERR_CUDA;
+    CUtensorMap kmap, vmap, qmap;
+    if (!encode_tensor_map_2d(&kmap, a.k_cache, rows, D, 64, tt, true)) return GQAQ_ERR_CUDA;
+    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, 64, tt, true)) return GQAQ_ERR_CUDA;
 
     PrefillParams p;
     p.q = a.q;
@@ -463,10 +962,22 @@ int launch_d(const PrefillArgs &a, const LaunchCtx &ctx) {
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_ns = ctx.timeout_ns;
     p.test_stall = ctx.test_stall;
-    if (launch_kernel(prefill_kernel<D>, dim3((unsigned)(items * splits)), dim3(C::THREADS), C::SMEM, ctx, 0, kmap,
-                      vmap, p) != cudaSuccess)
-        return GQAQ_ERR_CUDA;
-    return GQAQ_OK;
+    cudaError_t e;
+    if constexpr (TC) {
+        const uint64_t qrows = (uint64_t)dm.batch * dm.num_kv_heads * p.R;  // [B][Hq][q_len] rows of D
+        if (!encode_tensor_map_2d(&qmap, a.q, qrows, D, 64, TcCfg<D>::RB, true)) return GQAQ_ERR_CUDA;
+        e = launch_kernel(prefill_tc_kernel<D>, dim3((unsigned)(items * splits)), dim3(TcCfg<D>::THREADS),
+                          TcCfg<D>::SMEM, ctx, 0, qmap, kmap, vmap, p);
+    } else {
+        e = launch_kernel(prefill_kernel<D>, dim3((unsigned)(items * splits)), dim3(C::THREADS), C::SMEM, ctx, 0, kmap,
+                          vmap, p);
+    }
+    return e == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
+}
+
+template <int D>
+int launch_kind(const PrefillArgs &a, const LaunchCtx &ctx) {
+    return ctx.prefill_kernel == 2 ? launch_d<D, false>(a, ctx) : launch_d<D, true>(a, ctx);
 }
 
 }  // namespace
@@ -478,8 +989,8 @@ int64_t prefill_items(const gqaq_dims &dm, int q_len) {
 
 int launch_prefill(const PrefillArgs &a, const LaunchCtx &ctx) {
     switch (a.dims->head_dim) {
-        case 64: return launch_d<64>(a, ctx);
-        case 128: return launch_d<128>(a, ctx);
+        case 64: return launch_kind<64>(a, ctx);
+        case 128: return launch_kind<128>(a, ctx);
         default: return GQAQ_ERR_UNSUPPORTED;
     }
 }

@@ -315,9 +315,12 @@ enum {
                                      cluster kernel when k <= 1024, else the work-queue
                                      kernel; 1 = cluster kernel; 2 = work-queue kernel
                                      (needs the workspace) */
-    GQAQ_OPT_PREFILL_SPLITS = 7   /* context splits per gqa_prefill_attn work item:
+    GQAQ_OPT_PREFILL_SPLITS = 7,  /* context splits per gqa_prefill_attn work item:
                                      0 (default) = enough CTAs for one wave; 1..32
                                      forced (larger splits may be empty) */
+    GQAQ_OPT_PREFILL_KERNEL = 8   /* gqa_prefill_attn's kernel: 0 (default) or 1 = the
+                                     tensor-memory (tcgen05) kernel; 2 = the warp-level
+                                     MMA kernel */
 };
 GQAQ_API int gqaq_set_option(int option, int64_t value);
 

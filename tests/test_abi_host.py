@@ -179,6 +179,9 @@ def test_options(L):
     assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_KERNEL, -1) == g.GQAQ_ERR_INVALID_ARG
     for v in (2, 1, 0):
         assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_KERNEL, v) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_KERNEL, 3) == g.GQAQ_ERR_INVALID_ARG
+    for v in (1, 2, 0):
+        assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_KERNEL, v) == g.GQAQ_OK
     assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_SPLITS, -1) == g.GQAQ_ERR_INVALID_ARG
     assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_SPLITS, 33) == g.GQAQ_ERR_INVALID_ARG
     for v in (5, 32, 0):

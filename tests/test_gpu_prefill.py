@@ -1,7 +1,8 @@
 """GPU parity of gqa_prefill_attn (causal chunk attention with the group axis
 merged into the row axis) against the fp64 oracle, element by element.
 
-Covers D in {64, 128}, G in {1, 2, 4, 8}, chunk lengths from 1 to past one
+Every case runs on both kernels (tcgen05 / tensor memory, the default, and
+warp-level MMA). Covers D in {64, 128}, G in {1, 2, 4, 8}, chunk lengths from 1 to past one
 128-row block (so blocks wrap across query heads), chunks starting at zero
 and deep in the cache, per-sequence starts, forced context splits (including
 more splits than tiles: empty slices), NaN rows past the chunk, a bad start,
@@ -20,6 +21,14 @@ from _util import assert_attn_close
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True, params=["tcgen05", "warp_mma"])
+def kernel(request):
+    """Every case runs on both prefill kernels: tensor memory (default) and warp-level MMA."""
+    g.set_option(g.GQAQ_OPT_PREFILL_KERNEL, 1 if request.param == "tcgen05" else 2)
+    yield request.param
+    g.set_option(g.GQAQ_OPT_PREFILL_KERNEL, 0)
 
 
 @pytest.fixture(autouse=True)
