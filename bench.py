@@ -268,7 +268,8 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
 # capture of the kernel as it stands, keyed by (workload id, batch, family). A kernel
 # change makes its entry stale: it is then removed until the capture is taken again.
 NCU_TRAFFIC = {(3, 1, "quest", "f16"): 67_802_624, (3, 1, "dense", "f16"): 539_854_848,
-               (2, 32, "dense", "f16"): 180_059_392}
+               (2, 32, "dense", "f16"): 180_059_392, (2, 32, "dense", "e4m3"): 90_767_360,
+               (2, 32, "dense", "int4"): 49_910_272}
 
 
 def capture(fn, device):
