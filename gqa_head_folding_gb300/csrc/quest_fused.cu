@@ -20,8 +20,9 @@
 //     summing the C per-CTA histograms through distributed shared memory;
 //  3. each CTA compacts its selected pages (ties to the lower page index)
 //     into the ascending page list, written into every CTA's shared memory;
-//  4. each CTA attends over 1/C of the selected pages (TMA page loads, the
-//     shared warp tile of attn_tile.cuh);
+//  4. each CTA attends over 1/C of the selected pages: each consumer warp
+//     fetches its own rows with cp.async (a TMA page gather is bound by the
+//     TMA unit's per-box time) and runs the tensor-core tile of attn_mma.cuh;
 //  5. the C CTA states (m, l, acc) merge by log-sum-exp through distributed
 //     shared memory, and the fp16 output is written.
 // No workspace, no second launch. ATTEND mode runs only steps 4-5 on a page
@@ -29,7 +30,7 @@
 #include <math.h>
 #include <string.h>
 
-#include "attn_tile.cuh"
+#include "attn_mma.cuh"
 #include "internal.h"
 #include "quest_tile.cuh"
 
@@ -70,6 +71,14 @@ __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -186,7 +195,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     cluster_sync_all();  // every CTA of the cluster is running before any remote access
 
     const uint64_t pol = l2_policy_evict_first();
-    WarpAttn<D, G, true> wa;  // K stages in page-major layout
+    using WA = MmaAttn<D, G, true>;  // tensor-core tile; K and V stages page-major and swizzled
+    WA wa;
     wa.init(warp, lane, smem_u32(pbuf));
     int it = 0;  // position in the stage ring (same sequence in producer and consumers)
 
@@ -723,51 +733,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
         PageSlots slots;
         slots.init(p.S);
         const int ntile4 = (e1 - e0 + slots.ppt - 1) / slots.ppt;
-        if (producer) {
-            for (int t = 0; t < ntile4; ++t, ++it) {
-                const int s = it % C::NSTAGE;
-                const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
-                if (it >= C::NSTAGE) {
-                    bool ok = (*abort_flag == 0);
-                    if (ok && lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.timeout_ns, abort_flag);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) {
-                        if (lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
-                        continue;
-                    }
-                }
-                if (*abort_flag) continue;
-                const int e = e0 + t * slots.ppt + lane;
-                const bool in = lane < slots.ppt && e < e1;
-                int page = -1;
-                if (in) page = (MODE == FUSED_FULL) ? list[e] : p.page_idx[(int64_t)u * p.kpages + e];
-                const bool ok = in && page >= 0 && page < P;
-                if (MODE == FUSED_ATTEND && in && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
-                const unsigned m = __ballot_sync(0xffffffffu, ok);
-                {  // valid rows of consumer warp (lane & 7)
-                    const int j = slots.warp_page(lane & 7);
-                    const int pw = __shfl_sync(0xffffffffu, page, j);
-                    if (lane < 8) tinfo[s * 8 + lane] = ((m >> j) & 1u) ? slots.warp_rows(lane, pw, len) : 0;
-                }
-                __syncwarp();
-                const uint32_t kdst = smem_u32(ring + s * C::STAGE);
-                const uint32_t vdst = kdst + C::KBYTES;
-                const uint32_t fb = smem_u32(&full[s]);
-                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(p.S * D * 2 * 2));
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int pj = __shfl_sync(0xffffffffu, page, j);
-                    if (lane == 0 && ((m >> j) & 1u)) {
-                        const int y = u * p.Lmax + pj * p.S;
-                        const uint32_t off = (uint32_t)(j * slots.slot * D * 2);
-                        tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K
-                        tma_load_2d(vdst + off, &vmap, 0, y, fb, pol);
-                    }
-                }
-                __syncwarp();
-            }
-        } else {
-            if (C::QREG) {
+        if (!producer) {
+            if (WA::QREG) {
                 wa.load_q(qg);
             } else {
                 for (int e = tid; e < G * D / 8; e += C::NCW * 32)
@@ -775,23 +742,58 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 named_bar_sync(1, C::NCW * 32);
             }
             wa.reset();
-            for (int t = 0; t < ntile4; ++t, ++it) {
-                const int s = it % C::NSTAGE;
-                const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
-                bool ok = (*abort_flag == 0);
-                if (ok) {
-                    if (lane == 0) ok = mbar_wait(smem_u32(&full[s]), ph, p.timeout_ns, abort_flag);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok && lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
+            // Each consumer warp fetches its own 16 rows of every tile with
+            // 16-byte cp.async copies into its slice of the idle stage ring, up
+            // to NSTAGE tiles ahead, K and V both page-major and 128-byte swizzled
+            // (the layout the tensor-core tile reads with ldmatrix): a page
+            // gather by TMA is bound by the TMA unit's per-box time, the warps'
+            // loads are not.
+            // One commit group per tile (empty past the end), so
+            // wait_group<NSTAGE - 1> always means "tile t has landed".
+            auto in_share = [&](int t) { return t < ntile4 && e0 + t * slots.ppt + slots.warp_page(warp) < e1; };
+            auto page_of = [&](int t) {
+                if (!in_share(t)) return -1;
+                const int e = e0 + t * slots.ppt + slots.warp_page(warp);
+                return (MODE == FUSED_FULL) ? list[e] : p.page_idx[(int64_t)u * p.kpages + e];
+            };
+            auto fetch = [&](int t) {
+                const int page = page_of(t);
+                if (page >= 0 && page < P) {
+                    const int nv = slots.warp_rows(warp, page, len);
+                    const int64_t tok0 = (int64_t)u * p.Lmax + (int64_t)page * p.S + (16 * warp) % slots.slot;
+                    const uint32_t kb = smem_u32(ring + (t % C::NSTAGE) * C::STAGE), vb = kb + C::KBYTES;
+                    constexpr int CPR = D / 8;  // 16-byte chunks per row
+                    for (int idx = lane; idx < nv * CPR; idx += 32) {
+                        const int i = idx / CPR, c = idx - (idx / CPR) * CPR;
+                        const int row = 16 * warp + i;  // stage row
+                        const int line = row * C::KH + (c >> 3);
+                        cp_async16(kb + (uint32_t)(line * 128 + (((c & 7) ^ (line & 7)) << 4)),
+                                   p.k_cache + (tok0 + i) * D + c * 8);
+                        cp_async16(vb + (uint32_t)(line * 128 + (((c & 7) ^ (line & 7)) << 4)),
+                                   p.v_cache + (tok0 + i) * D + c * 8);
+                    }
                 }
-                const int nv = ok ? tinfo[s * 8 + warp] : 0;
-                if (nv > 0) {
-                    const uint32_t kbase = smem_u32(ring + s * C::STAGE);
-                    wa.tile(kbase, kbase + C::KBYTES, nv, p.scale_log2, qreg_s);
+                cp_async_commit();
+            };
+            for (int t = 0; t < C::NSTAGE; ++t) fetch(t);
+            for (int t = 0; t < ntile4; ++t) {
+                cp_async_wait<C::NSTAGE - 1>();
+                __syncwarp();  // every lane's copies of tile t are visible to the warp
+                const int page = page_of(t);
+                const bool ok = page >= 0 && page < P;
+                if (MODE == FUSED_ATTEND && lane == 0 && in_share(t) && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
+                const int nv = ok ? slots.warp_rows(warp, page, len) : 0;
+                const bool live = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);  // warp-uniform
+                if (nv > 0 && live) {
+                    const uint32_t kbase = smem_u32(ring + (t % C::NSTAGE) * C::STAGE);
+                    const int nvs[1] = {nv};
+                    wa.template tile_n<1>(kbase, kbase + C::KBYTES, 16 * warp, nvs, p.scale_log2);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+                __syncwarp();  // the slice is free before tile t + NSTAGE lands in it
+                fetch(t + C::NSTAGE);
             }
+            cp_async_wait<0>();
+            fence_proxy_async_smem();  // the ring is TMA-written again by the next unit
             // ---- merge the 8 warp states into this CTA's state ----
             wa.store_state(merge);
             named_bar_sync(1, C::NCW * 32);
