@@ -51,6 +51,12 @@ __device__ __forceinline__ uint32_t cluster_ctas() {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
@@ -191,8 +197,24 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
         if (MODE == FUSED_FULL) prefetch_tensormap(&mmap);
     }
     pdl_wait_and_release();
+    // The first unit's length (and appended position) are read before the
+    // barriers, so their latency overlaps them.
+    const int raw_first = (int)(blockIdx.x / cluster_ctas()) < p.B * p.Hkv ? p.valid_len[(blockIdx.x / cluster_ctas()) / p.Hkv] : 1;
+    const int pos_first = (p.pos != nullptr && (int)(blockIdx.x / cluster_ctas()) < p.B * p.Hkv)
+                              ? p.pos[(blockIdx.x / cluster_ctas()) / p.Hkv] : 0;
     __syncthreads();
-    cluster_sync_all();  // every CTA of the cluster is running before any remote access
+    // Every CTA of the cluster must be running before any remote access: the
+    // start barrier is arrived at here and waited on just before a thread's
+    // first remote access or cluster barrier (cluster_ready), so the first
+    // metadata loads and q loads are issued meanwhile.
+    cluster_arrive();  // release: this CTA's initialised barriers and key range
+    bool cl_pending = true;
+    auto cluster_ready = [&]() {
+        if (cl_pending) {
+            cluster_wait();
+            cl_pending = false;
+        }
+    };
 
     const uint64_t pol = l2_policy_evict_first();
     using WA = MmaAttn<D, G, true>;  // tensor-core tile; K and V stages page-major and swizzled
@@ -202,7 +224,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
 
     for (int u = cid; u < units; u += ncl) {
         const int b = u / p.Hkv, kv = u - (u / p.Hkv) * p.Hkv;
-        const int raw = p.valid_len[b];
+        const int raw = (u == cid) ? raw_first : p.valid_len[b];
         if (tid == 0 && crank == 0 && (raw < 1 || raw > p.Lmax)) raise_flag(p.status, GQAQ_DEV_BAD_LEN);
         const int len = clamp_len(raw, p.Lmax);
         const int P = (len + p.S - 1) / p.S;
@@ -225,7 +247,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 // CTA), so the other tiles stream meanwhile.
                 int papp = -1;  // page of the appended token when this CTA writes it
                 if (p.pos != nullptr) {
-                    const int pos = p.pos[b];
+                    const int pos = (u == cid) ? pos_first : p.pos[b];
                     if (pos < 0 || pos >= p.Lmax) {
                         if (lane == 0 && crank == 0) raise_flag(p.status, GQAQ_DEV_BAD_POS);
                     } else {
@@ -312,6 +334,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     named_bar_sync(1, C::NCW * 32);
                 }
                 uint32_t kmin_l = 0xffffffffu, kmax_l = 0u;  // range of the keys this thread stores
+                cluster_ready();  // the key stores below reach CTA 0
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % C::NSTAGE;
                     const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
@@ -396,10 +419,12 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                 }
             }
-            if (gather)
+            if (gather) {
+                cluster_ready();
                 cluster_sync_all();  // CTA 0 holds every key of the unit
-            else
+            } else {
                 __syncthreads();
+            }
 
             if (gather) {
                 // ============ 2-3. CTA 0: exact top-K from register-held keys ============
@@ -535,6 +560,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         for (int i = nsel + tid; i < p.kpages; i += C::THREADS) prow[i] = -1;
                     fence_proxy_async_smem();  // the histogram's stage is TMA-written again later
                 }
+                cluster_ready();
                 cluster_sync_all();  // every CTA's share of the page list is in its shared memory
             } else {
                 // ================= 2. top-K threshold (adaptive range radix) =================
@@ -577,6 +603,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         sh[7] = (int)bmax;
                     }
                     if (!gather) {
+                        cluster_ready();
                         cluster_sync_all();
                         if (tid == 0) {
                             uint32_t a = 0xffffffffu, bmax = 0u;
@@ -608,6 +635,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         }
                         const int *src = hb;
                         if (!gather) {
+                            cluster_ready();
                             cluster_sync_all();
                             for (int i = tid; i < 256; i += C::THREADS) {
                                 int tot = 0;
@@ -688,6 +716,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     int gt_before = 0, eq_before = 0;
                     if (!gather) {
                         if (tid == 0) { cnt[0] = tg; cnt[1] = te; }
+                        cluster_ready();
                         cluster_sync_all();
                         for (uint32_t r = 0; r < crank; ++r) {
                             gt_before += (int)ld_dsmem_u32(dsmem_map(smem_u32(&cnt[0]), r));
@@ -723,6 +752,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 }
                 if (p.page_idx != nullptr && crank == 0)
                     for (int i = nsel + tid; i < p.kpages; i += C::THREADS) p.page_idx[(int64_t)u * p.kpages + i] = -1;
+                cluster_ready();
                 cluster_sync_all();  // remote list entries are complete
             }
         }
@@ -808,6 +838,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 }
             }
         }
+        cluster_ready();
         cluster_sync_all();  // every CTA's state is complete
 
         // ================= 5. log-sum-exp merge across the cluster =================
@@ -833,8 +864,11 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 p.out[((int64_t)b * Hq + (int64_t)kv * G + g) * D + d] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
             }
         }
+        cluster_ready();
         cluster_sync_all();  // before the next unit reuses keys, list and state
     }
+
+    cluster_ready();  // a cluster with no unit still completes the start barrier
 
     // If a wait gave up, let this CTA's copies in flight land before it retires.
     if (producer && lane == 0 && *abort_flag) {
