@@ -385,9 +385,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::MIN_BLO
 // ===========================================================================
 // Tensor-memory kernel (tcgen05): the same work items, splits and merge as
 // prefill_kernel, with both products on the 5th-generation tensor cores.
-//  - warp 4 (TMA): the item's Q block once, then K and V tiles of 128 tokens
+//  - warp 8 (TMA): the item's Q block once, then K and V tiles of 128 tokens
 //    (128-byte-swizzled 64-column boxes) into a 3-5 stage ring.
-//  - warp 5 (MMA, one thread): S_j = Q K_j^T (M = 128 rows, N = 128 tokens,
+//  - warp 9 (MMA, one thread): S_j = Q K_j^T (M = 128 rows, N = 128 tokens,
 //    K = D; both operands K-major in shared memory) into one of two TMEM S
 //    buffers, and O += P_j V_j (A = P_j from TMEM, B = V_j MN-major in shared
 //    memory, N = 64 per 64-channel block) into the TMEM O block. Issue order
@@ -395,15 +395,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::MIN_BLO
 //    softmax of this one, and each S buffer is rewritten only after the PV
 //    that read its P (the tensor core runs one thread's MMAs in order).
 //    Completions arrive on mbarriers through tcgen05.commit.
-//  - warps 0-3 (softmax, one thread per row): read the row's 128 scores from
-//    TMEM, mask the causal limit, keep a lazy reference max (rescaling O in
-//    TMEM only when the row max grows by more than 2^8, so P stays <= 256 in
-//    fp16), write P as fp16 over its S buffer, and at the end read O.
-//  - TMEM (512 columns): S buffers at columns 0 and 128, O at 256.
+//  - warps 0-7 (softmax, two warpgroups taking alternate tiles, one thread
+//    per row): read the row's 128 scores from TMEM, mask the causal limit,
+//    keep a lazy reference max (rescaling the group's O in TMEM only when the
+//    row max grows by more than 2^8, so P stays <= 256 in fp16), write P as
+//    fp16 over the group's S buffer. One group's softmax overlaps the MMAs of
+//    the other's tile. At the end the two (m, l, O) states merge per row.
+//  - TMEM (512 columns): S of group g at column 128 g, O of group g at 256 + D g.
 // ===========================================================================
 template <int D>
 struct TcCfg {
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 320;           // 2 softmax warpgroups, TMA warp, MMA warp
     static constexpr int RB = 128;                // rows per item (TMEM lanes)
     static constexpr int TT = 128;                // tokens per stage (N of S)
     static constexpr int KH = D / 64;
@@ -413,10 +415,10 @@ struct TcCfg {
     static constexpr int QBLK = RB * 128;
     static constexpr int QBYTES = KH * QBLK;
     static constexpr int NSTAGE = D == 128 ? 3 : 5;
-    static constexpr int MISC = 512;
+    static constexpr int MISC = 2048;             // barriers, flags, and group 1's (m, l) per row at +512
     static constexpr int SMEM = 1024 + QBYTES + NSTAGE * STAGE + MISC;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int S_COL = 0, O_COL = 256;
+    static constexpr int S_COL = 0, O_COL = 256;  // S of group g at 128 g, O of group g at 256 + D g
     static constexpr float RESCALE_LOG2 = 8.f;    // lazy reference: P <= 2^8
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(RB * kPrefillMaxSplits * 4 <= NSTAGE * STAGE, "merge weights fit the idle ring");
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     float *wbuf = reinterpret_cast<float *>(stages);  // merge weights, once the ring is idle
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -538,7 +540,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
                      "n"(C::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     const int n = j1 - j0;
     const int kv_end = st + p.q_len;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------------
         // TMA producer
         // ------------------------------------------------------------------
@@ -605,7 +607,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                 mbar_wait(smem_u32(qbar), 0u, p.timeout_ns, nullptr);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------------
         // MMA issuer (one thread)
         // ------------------------------------------------------------------
@@ -646,9 +648,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                         for (int kk = 0; kk < C::TT / 16; ++kk) {
 #pragma unroll
                             for (int nb = 0; nb < C::KH; ++nb)
-                                umma_ts(tbase + C::O_COL + 64u * nb, tbase + C::S_COL + 128u * (jj & 1) + 8u * kk,
+                                umma_ts(tbase + C::O_COL + (uint32_t)(D * (jj & 1)) + 64u * nb,
+                                        tbase + C::S_COL + 128u * (jj & 1) + 8u * kk,
                                         umma_desc(vst + nb * C::KBLK + kk * 16 * 128, C::KBLK), IDESC_O,
-                                        (jj > 0 || kk > 0) ? 1 : 0);
+                                        (jj > 1 || kk > 0) ? 1 : 0);  // each group's first PV starts its O
                         }
                         umma_commit(smem_u32(&o_done[jj & 1]));
                         umma_commit(smem_u32(&empty[s]));
@@ -667,22 +670,28 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------------
-        // Softmax and epilogue: thread tid owns row tid of the item (TMEM lane)
+        // Softmax, two warpgroups: group g (warps 4g .. 4g+3) takes the
+        // tiles idx = g, g + 2, ... with its own S buffer, O block and (m, l);
+        // thread tid owns row tid of the item (its warp's TMEM lane quarter).
+        // A group's O is never written while its softmax runs (its next PV
+        // waits for its P), and S_idx complete implies PV_{idx-2} complete
+        // (issued before it, in-order completion), so rescaling O needs no wait.
         // ------------------------------------------------------------------
-        const int tid = threadIdx.x;  // 0..127
+        const int grp = warp >> 2;
+        const int tid = threadIdx.x & 127;
         const bool live = tid < nrows;
         const int lim = st + (rho0 + tid) % p.q_len;
-        const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
+        const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t ocol = trow + C::O_COL + (uint32_t)(D * grp);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         // PV_j's completion, on o_done[j & 1]: its previous use (PV_{j-2}) has
-        // completed whenever this is asked (S_{j+1} has, and MMAs complete in
-        // order) and its next (PV_{j+2}) is not issued yet, so the parity wait
-        // is never more than one phase behind.
+        // completed whenever this is asked and its next (PV_{j+2}) is not
+        // issued, so the parity wait is never more than one phase behind.
         auto wait_pv = [&](int j) {
             return warp_wait(smem_u32(&o_done[j & 1]), (uint32_t)(j >> 1) & 1u, p, abort_flag, lane);
         };
-        for (int idx = 0; idx < n; ++idx) {
+        for (int idx = grp; idx < n; idx += 2) {
             ok = ok && warp_wait(smem_u32(&s_ready[idx & 1]), (uint32_t)(idx >> 1) & 1u, p, abort_flag, lane);
             if (!ok) {
                 if (lane == 0) {
@@ -715,26 +724,16 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                 alpha = fast_exp2(m_ref - mx);  // 0 when m_ref is -inf
                 m_ref = mx;
                 l *= alpha;
-                resc = idx > 0;
+                resc = idx >= 2;  // this group's O holds earlier tiles
             }
             if (__any_sync(0xffffffffu, resc)) {
-                // O holds PV_0 .. PV_{idx-1}: wait for the last of them
-                ok = wait_pv(idx - 1);
-                if (!ok) {
-                    if (lane == 0) {
-                        raise_flag(p.status, GQAQ_DEV_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t v[32];
-                    tmem_ld32(trow + C::O_COL + 32u * ch, v);
+                    tmem_ld32(ocol + 32u * ch, v);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(trow + C::O_COL + 32u * ch, v);
+                    tmem_st32(ocol + 32u * ch, v);
                 }
                 tmem_wait_st();
             }
@@ -774,46 +773,71 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&p_ready[idx & 1]));
         }
-        // ---- epilogue: O after the last PV ----
-        if (ok && n > 0) {
-            ok = wait_pv(n - 1);  // PV_{n-1} done: every PV is (in-order completion)
+        // ---- epilogue: each group's O after its last PV, then the two merge per row ----
+        const int last = n > grp ? grp + 2 * ((n - 1 - grp) / 2) : -1;  // this group's last tile
+        if (ok && last >= 0) {
+            ok = wait_pv(last);  // every PV of this group is done (in-order completion)
             if (!ok && lane == 0) {
                 raise_flag(p.status, GQAQ_DEV_TIMEOUT);
                 *abort_flag = 1;
             }
         }
-        tc_fence_after();
-        __half *ob = p.out + ((int64_t)unit * p.R + rho0) * D;
-        float *pml = p.part + (int64_t)blockIdx.x * C::RB * (D + 2);
-        float *pacc = pml + 2 * C::RB;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        if (p.splits > 1 && live) reinterpret_cast<float2 *>(pml)[tid] = make_float2(m_ref, l);
+        // Group 1 hands its (m, l) over in shared memory (outside the ring: the
+        // other group's last PV may still read a stage), group 0 reads both O
+        // blocks and merges:
+        // m* = max(m0, m1), w_g = 2^(m_g - m*), out = (w0 O0 + w1 O1) / (w0 l0 + w1 l1).
+        float2 *hand = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(full) + 512);  // misc region
+        if (grp == 1) hand[tid] = make_float2(m_ref, l);
+        tc_fence_before();
+        named_bar_sync(2, 256);  // both softmax groups: group 1's O and (m, l) are final
+        if (grp == 0) {
+            tc_fence_after();
+            const bool have_a = n > 0, have_b = n > 1;
+            const float2 mlb = have_b ? hand[tid] : make_float2(-INFINITY, 0.f);
+            const float mst = fmaxf(m_ref, mlb.x);
+            const float wa = (mst == -INFINITY || m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - mst);
+            const float wb = (mst == -INFINITY || mlb.x == -INFINITY) ? 0.f : fast_exp2(mlb.x - mst);
+            const float L = wa * l + wb * mlb.y;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            __half *ob = p.out + ((int64_t)unit * p.R + rho0) * D;
+            float *pml = p.part + (int64_t)blockIdx.x * C::RB * (D + 2);
+            float *pacc = pml + 2 * C::RB;
+            if (p.splits > 1 && live) reinterpret_cast<float2 *>(pml)[tid] = make_float2(mst, L);
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t v[32], w[32];
+                if (ok && have_a) {
+                    tmem_ld32(trow + C::O_COL + 32u * ch, v);
+                } else {
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t v[32];
-            if (ok && n > 0) {
-                tmem_ld32(trow + C::O_COL + 32u * ch, v);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0u;
-            }
-            if (!live) continue;
-            if (p.splits == 1) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    uint4 h;
-                    h.x = pack_half2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-                    h.y = pack_half2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-                    h.z = pack_half2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-                    h.w = pack_half2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-                    *reinterpret_cast<uint4 *>(ob + (int64_t)tid * D + 32 * ch + e) = h;
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
                 }
-            } else {
+                if (ok && have_b) {
+                    tmem_ld32(trow + C::O_COL + (uint32_t)D + 32u * ch, w);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4 *>(pacc + (int64_t)tid * D + 32 * ch + e) =
-                        make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                    __uint_as_float(v[e + 3]));
+                    for (int e = 0; e < 32; ++e) w[e] = 0u;
+                }
+                if (!live) continue;
+                float o[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = wa * __uint_as_float(v[e]) + wb * __uint_as_float(w[e]);
+                if (p.splits == 1) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 h;
+                        h.x = pack_half2(o[e] * inv, o[e + 1] * inv);
+                        h.y = pack_half2(o[e + 2] * inv, o[e + 3] * inv);
+                        h.z = pack_half2(o[e + 4] * inv, o[e + 5] * inv);
+                        h.w = pack_half2(o[e + 6] * inv, o[e + 7] * inv);
+                        *reinterpret_cast<uint4 *>(ob + (int64_t)tid * D + 32 * ch + e) = h;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(pacc + (int64_t)tid * D + 32 * ch + e) =
+                            make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                }
             }
         }
     }
@@ -821,10 +845,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     // ---- all roles meet: the ring is idle, every MMA has completed ----
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(C::TMEM_COLS));
+    if (warp == 9) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "n"(C::TMEM_COLS));
     if (p.splits == 1 || warp >= 4) return;
 
-    // ---- split: arrival, and the last arrival's merge (the 128 softmax threads) ----
+    // ---- split: arrival, and the last arrival's merge (softmax group 0, 128 threads) ----
     constexpr int NCT = 128;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -898,8 +922,11 @@ int blocks_per_sm(const LaunchCtx &ctx) {
     return occ[ctx.device];
 }
 
-// Context splits per item: enough CTAs to cover the GPU's resident slots,
-// at least two tiles per split, at most kPrefillMaxSplits (or the forced value).
+// Context splits per item (or the forced value): the count s <= min(tiles / 2,
+// kPrefillMaxSplits) that minimises waves x (tiles per split + 2), i.e.
+// ceil(items s / slots) (ceil(tiles / s) + 2), for a context of max_len
+// tokens; the 2 stands for a CTA's fixed cost (prologue, epilogue, merge) in
+// tile times. Ties go to fewer splits (fewer partials to merge).
 template <int D, bool TC>
 int splits_for(const gqaq_dims &dm, int q_len, const LaunchCtx &ctx) {
     const int occ = blocks_per_sm<D, TC>(ctx);
@@ -907,13 +934,19 @@ int splits_for(const gqaq_dims &dm, int q_len, const LaunchCtx &ctx) {
     const int64_t items = prefill_items(dm, q_len);
     if (ctx.prefill_splits > 0) return ctx.prefill_splits < kPrefillMaxSplits ? ctx.prefill_splits : kPrefillMaxSplits;
     const int64_t slots = (int64_t)occ * ctx.num_sms;
-    int64_t s = (slots + items - 1) / items;
     const int tt = TC ? TcCfg<D>::TT : PrefillCfg<D>::TT;
     const int64_t tiles = ((int64_t)dm.max_len + tt - 1) / tt;
-    const int64_t cap = tiles / 2 > 1 ? tiles / 2 : 1;
-    if (s > cap) s = cap;
-    if (s > kPrefillMaxSplits) s = kPrefillMaxSplits;
-    return (int)(s < 1 ? 1 : s);
+    int64_t cap = tiles / 2 > 1 ? tiles / 2 : 1;
+    if (cap > kPrefillMaxSplits) cap = kPrefillMaxSplits;
+    int64_t best = 1, best_cost = -1;
+    for (int64_t s = 1; s <= cap; ++s) {
+        const int64_t cost = ((items * s + slots - 1) / slots) * ((tiles + s - 1) / s + 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return (int)best;
 }
 
 // Workspace for either kernel: the counters, then partials for the larger split.
