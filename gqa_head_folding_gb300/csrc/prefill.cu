@@ -468,6 +468,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 64 consecutive columns of this thread's lane: two x32 loads, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr + 32u));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -704,16 +725,16 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             const int tok0 = (j0 + idx) * C::TT;
             const bool need_mask = tok0 + C::TT - 1 > st + t_min;  // uniform over the item
             const uint32_t scol = trow + C::S_COL + 128u * (idx & 1);
-            // pass 1: the row max of this tile (log2 domain)
+            // pass 1: the row max of this tile (log2 domain), 64 columns per TMEM round trip
             float mx = -INFINITY;
+#pragma unroll 1
+            for (int ch = 0; ch < C::TT / 64; ++ch) {
+                uint32_t v[64];
+                tmem_ld64(scol + 64u * ch, v);
 #pragma unroll
-            for (int ch = 0; ch < C::TT / 32; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(scol + 32u * ch, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
+                for (int e = 0; e < 64; ++e) {
                     float x = __uint_as_float(v[e]) * p.scale_log2;
-                    if (need_mask && tok0 + 32 * ch + e > lim) x = -INFINITY;
+                    if (need_mask && tok0 + 64 * ch + e > lim) x = -INFINITY;
                     mx = fmaxf(mx, x);
                 }
             }
@@ -740,22 +761,22 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             // pass 2: P = 2^(x - m_ref) as fp16 over the S buffer (pairs, low half = even token)
             const float ref = m_ref == -INFINITY ? 0.f : m_ref;
             float ps = 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < C::TT / 64; ++ch) {
+                uint32_t v[64], pk[32];
+                tmem_ld64(scol + 64u * ch, v);
 #pragma unroll
-            for (int ch = 0; ch < C::TT / 32; ++ch) {
-                uint32_t v[32], pk[16];
-                tmem_ld32(scol + 32u * ch, v);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < 64; e += 2) {
                     float x0 = __uint_as_float(v[e]) * p.scale_log2, x1 = __uint_as_float(v[e + 1]) * p.scale_log2;
                     if (need_mask) {
-                        x0 = tok0 + 32 * ch + e > lim ? -INFINITY : x0;
-                        x1 = tok0 + 32 * ch + e + 1 > lim ? -INFINITY : x1;
+                        x0 = tok0 + 64 * ch + e > lim ? -INFINITY : x0;
+                        x1 = tok0 + 64 * ch + e + 1 > lim ? -INFINITY : x1;
                     }
                     const float e0 = fast_exp2(x0 - ref), e1 = fast_exp2(x1 - ref);
                     ps += e0 + e1;
                     pk[e >> 1] = pack_half2(e0, e1);
                 }
-                tmem_st16(scol + 16u * ch, pk);
+                tmem_st32(scol + 32u * ch, pk);  // P of tokens 64 ch .. +63 over S columns 32 ch .. +31
             }
             l += ps;
             tmem_wait_st();
