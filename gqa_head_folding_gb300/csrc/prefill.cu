@@ -500,14 +500,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // One warp's bounded wait (lane 0 waits, the warp follows): false on timeout or abort.
@@ -725,54 +717,60 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             const int tok0 = (j0 + idx) * C::TT;
             const bool need_mask = tok0 + C::TT - 1 > st + t_min;  // uniform over the item
             const uint32_t scol = trow + C::S_COL + 128u * (idx & 1);
-            // pass 1: the row max of this tile (log2 domain), 64 columns per TMEM round trip
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int ch = 0; ch < C::TT / 64; ++ch) {
-                uint32_t v[64];
-                tmem_ld64(scol + 64u * ch, v);
-#pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    float x = __uint_as_float(v[e]) * p.scale_log2;
-                    if (need_mask && tok0 + 64 * ch + e > lim) x = -INFINITY;
-                    mx = fmaxf(mx, x);
-                }
-            }
-            // lazy reference: move it (and rescale l, O) only when the max grows by > 2^8
-            float alpha = 1.f;
-            bool resc = false;
-            if (mx > m_ref + C::RESCALE_LOG2) {
-                alpha = fast_exp2(m_ref - mx);  // 0 when m_ref is -inf
-                m_ref = mx;
-                l *= alpha;
-                resc = idx >= 2;  // this group's O holds earlier tiles
-            }
-            if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t v[32];
-                    tmem_ld32(ocol + 32u * ch, v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(ocol + 32u * ch, v);
-                }
-                tmem_wait_st();
-            }
-            // pass 2: P = 2^(x - m_ref) as fp16 over the S buffer (pairs, low half = even token)
-            const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+            // One pass over the tile, 64 columns per TMEM round trip: the chunk's
+            // max, then P = 2^(x - m_ref) as fp16 over the S buffer (pairs, low half =
+            // even token). The lazy reference m_ref moves only when a chunk's max
+            // exceeds it by more than 2^8 (so P <= 256 fits fp16); then l, this
+            // group's O (when it holds earlier tiles) and the P already written for
+            // this tile are rescaled by alpha = 2^(old - new). That is rare: after
+            // the first chunks the reference rarely moves.
             float ps = 0.f;
 #pragma unroll 1
             for (int ch = 0; ch < C::TT / 64; ++ch) {
                 uint32_t v[64], pk[32];
                 tmem_ld64(scol + 64u * ch, v);
+                float cm = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    float x = __uint_as_float(v[e]) * p.scale_log2;
+                    if (need_mask && tok0 + 64 * ch + e > lim) x = -INFINITY;
+                    v[e] = __float_as_uint(x);
+                    cm = fmaxf(cm, x);
+                }
+                const bool up = cm > m_ref + C::RESCALE_LOG2;
+                if (__any_sync(0xffffffffu, up)) {
+                    const float alpha = up ? fast_exp2(m_ref - cm) : 1.f;  // 0 when m_ref is -inf
+                    if (up) {
+                        m_ref = cm;
+                        l *= alpha;
+                        ps *= alpha;
+                    }
+                    if (__any_sync(0xffffffffu, up && idx >= 2)) {  // this group's O holds earlier tiles
+#pragma unroll 1
+                        for (int oc = 0; oc < D / 32; ++oc) {
+                            uint32_t o[32];
+                            tmem_ld32(ocol + 32u * oc, o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(ocol + 32u * oc, o);
+                        }
+                    }
+                    for (int pc = 0; pc < ch; ++pc) {  // this tile's P written so far
+                        uint32_t q[32];
+                        tmem_ld32(scol + 32u * pc, q);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q[e]));
+                            q[e] = pack_half2(f.x * alpha, f.y * alpha);
+                        }
+                        tmem_st32(scol + 32u * pc, q);
+                    }
+                    tmem_wait_st();
+                }
+                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
-                    float x0 = __uint_as_float(v[e]) * p.scale_log2, x1 = __uint_as_float(v[e + 1]) * p.scale_log2;
-                    if (need_mask) {
-                        x0 = tok0 + 64 * ch + e > lim ? -INFINITY : x0;
-                        x1 = tok0 + 64 * ch + e + 1 > lim ? -INFINITY : x1;
-                    }
-                    const float e0 = fast_exp2(x0 - ref), e1 = fast_exp2(x1 - ref);
+                    const float e0 = fast_exp2(__uint_as_float(v[e]) - ref), e1 = fast_exp2(__uint_as_float(v[e + 1]) - ref);
                     ps += e0 + e1;
                     pk[e >> 1] = pack_half2(e0, e1);
                 }
