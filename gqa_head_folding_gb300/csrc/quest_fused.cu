@@ -16,15 +16,19 @@
 //     fence); every CTA streams the metadata of its 1/C of the pages with TMA
 //     and scores them into shared-memory keys (U as a dot of
 //     [min(q,0); max(q,0)] with [m; M], since m <= M);
-//  2. the cluster finds the K-th largest key with four 8-bit radix passes,
-//     summing the C per-CTA histograms through distributed shared memory;
-//  3. each CTA compacts its selected pages (ties to the lower page index)
-//     into the ascending page list, written into every CTA's shared memory;
+//  2-3. up to 4096 pages, CTA 0 gathers every key (remote stores into its
+//     shared memory), finds the K-th largest with range-narrowing histogram
+//     passes over register-held keys, and writes each CTA its share of the
+//     ascending page list (ties to the lower page index); with more pages,
+//     the cluster runs four 8-bit radix passes, summing the C per-CTA
+//     histograms through distributed shared memory, and each CTA compacts
+//     its own selected pages into every CTA's list;
 //  4. each CTA attends over 1/C of the selected pages: each consumer warp
 //     fetches its own rows with cp.async (a TMA page gather is bound by the
 //     TMA unit's per-box time) and runs the tensor-core tile of attn_mma.cuh;
-//  5. the C CTA states (m, l, acc) merge by log-sum-exp through distributed
-//     shared memory, and the fp16 output is written.
+//  5. each CTA pushes its state (m, l, acc) into the rank that owns each
+//     slice of the output; after one cluster barrier every rank merges its
+//     slice by log-sum-exp from its own shared memory and writes it in fp16.
 // No workspace, no second launch. ATTEND mode runs only steps 4-5 on a page
 // list given in global memory.
 #include <math.h>
@@ -75,6 +79,9 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -112,13 +119,15 @@ struct FusedCfg : TileCfg<D, G> {
     static constexpr int KEYMERGE = (KEYS_MAX * 4 > T::MERGE) ? KEYS_MAX * 4 : T::MERGE;
     static constexpr int QT_BYTES = G * 2 * D * 2;  // [G][2D] fp16 [q_neg | q_pos]
     static constexpr int QREGION = (QT_BYTES > T::QBYTES) ? QT_BYTES : T::QBYTES;
-    static constexpr int CSTATE = G * (D + 2) * 4;
+    // A cluster rank's inbox: for every source rank, (m, l) of the G rows then
+    // the accumulators of the rank's slice of the G*D outputs (<= 8 ranks).
+    static constexpr int INBOX = (G * D + 16 * G + 8) * 4;
     // misc region, in 4-byte words: hist [0,512), totals [512,768), tile info
     // [768,800), counts [800,808), scan scratch [808,832), scalars [832,848),
     // then the full/empty mbarriers (8-byte aligned) at word 848.
     static constexpr int MISC_BARRIER_WORD = 848;
     static constexpr int MISC = MISC_BARRIER_WORD * 4 + 2 * 3 * 8;  // full, empty
-    static constexpr int FIXED = KEYMERGE + QREGION + T::PBYTES + KSEL_MAX * 4 + CSTATE + MISC + 1024;
+    static constexpr int FIXED = KEYMERGE + QREGION + T::PBYTES + KSEL_MAX * 4 + INBOX + MISC + 1024;
     static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
     static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
     static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
@@ -161,8 +170,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     __half *qreg_s = reinterpret_cast<__half *>(fixed + C::KEYMERGE);
     float *pbuf = reinterpret_cast<float *>(fixed + C::KEYMERGE + C::QREGION);
     int *list = reinterpret_cast<int *>(fixed + C::KEYMERGE + C::QREGION + C::PBYTES);
-    float *cstate = reinterpret_cast<float *>(list + C::KSEL_MAX);
-    int *misc = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(cstate) + C::CSTATE);
+    float *inbox = reinterpret_cast<float *>(list + C::KSEL_MAX);
+    int *misc = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(inbox) + C::INBOX);
     int *hist = misc;                     // [2][256]
     int *tots = misc + 512;               // [256]
     int *tinfo = misc + 768;              // [NSTAGE][8] valid tokens per page of a stage
@@ -539,22 +548,27 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     for (int w = 0; w < warp; ++w) { bg += wsum[w]; be += wsum[9 + w]; }
                     int eqr = be + ie - neq;
                     int pos = bg + ig - ngt + (eqr < need_eq ? eqr : need_eq);
-                    int *prow = p.page_idx != nullptr ? p.page_idx + (int64_t)u * p.kpages : nullptr;
+                    // The ascending list is built in the histogram's stage first (a short
+                    // loop body), then spread over the cluster by one strided loop.
+                    int *sel = hb;
 #pragma unroll
                     for (int e = 0; e < C::KPT; ++e) {
                         if (e < kc) {
                             const bool inr = kr[e] >= lo && kr[e] <= hi;
                             const bool take = kr[e] > hi || (inr && eqr < need_eq);
                             eqr += inr;
-                            if (take) {
-                                if (pos < nsel && pos < C::KSEL_MAX) {
-                                    const uint32_t owner = (uint32_t)((((int64_t)pos + 1) * nct - 1) / nsel);
-                                    st_dsmem_u32(dsmem_map(smem_u32(&list[pos]), owner), (uint32_t)(c0 + e));
-                                    if (prow != nullptr) prow[pos] = c0 + e;
-                                }
-                                ++pos;
-                            }
+                            if (take && pos < nsel) sel[pos] = c0 + e;
+                            pos += take;
                         }
+                    }
+                    __syncthreads();
+                    int *prow = p.page_idx != nullptr ? p.page_idx + (int64_t)u * p.kpages : nullptr;
+#pragma unroll 1
+                    for (int i = tid; i < nsel; i += C::THREADS) {
+                        const int pg = sel[i];
+                        const uint32_t owner = (uint32_t)((i + 1) * (int)nct - 1) / (uint32_t)nsel;  // share [r*nsel/C, (r+1)*nsel/C)
+                        st_dsmem_u32(dsmem_map(smem_u32(&list[i]), owner), (uint32_t)pg);
+                        if (prow != nullptr) prow[i] = pg;
                     }
                     if (prow != nullptr)
                         for (int i = nsel + tid; i < p.kpages; i += C::THREADS) prow[i] = -1;
@@ -824,48 +838,59 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             }
             cp_async_wait<0>();
             fence_proxy_async_smem();  // the ring is TMA-written again by the next unit
-            // ---- merge the 8 warp states into this CTA's state ----
+            // ---- merge the 8 warp states; push each rank its slice ----
+            // Output i of the G*D belongs to rank i / per. Every rank gets this
+            // CTA's (m, l) of all G rows and its accumulators of the rank's slice,
+            // in the rank's inbox record for this source, so the merge below reads
+            // only local shared memory and no rank reads another after it.
             wa.store_state(merge);
             named_bar_sync(1, C::NCW * 32);
+            const int per = (G * D + (int)nct - 1) / (int)nct;
+            const uint32_t mine = smem_u32(inbox + (int)crank * (2 * G + per));
             for (int idx = tid; idx < G * D; idx += C::NCW * 32) {
                 const int g = idx / D, d = idx - (idx / D) * D;
                 float mst, ls, as;
                 merge_warps<D, G>(merge, g, d, mst, ls, as);
-                cstate[g * (D + 2) + 2 + d] = as;
-                if (d == 0) {
-                    cstate[g * (D + 2)] = mst;
-                    cstate[g * (D + 2) + 1] = ls;
-                }
+                const int r = idx / per;
+                st_dsmem_f32(dsmem_map(mine + 4u * (uint32_t)(2 * G + idx - r * per), (uint32_t)r), as);
+                if (d == 0)
+                    for (uint32_t q = 0; q < nct; ++q) {
+                        st_dsmem_f32(dsmem_map(mine + 8u * (uint32_t)g, q), mst);
+                        st_dsmem_f32(dsmem_map(mine + 8u * (uint32_t)g + 4u, q), ls);
+                    }
             }
         }
         cluster_ready();
-        cluster_sync_all();  // every CTA's state is complete
+        cluster_sync_all();  // every rank's inbox holds the cluster's states of its slice
 
-        // ================= 5. log-sum-exp merge across the cluster =================
+        // ================= 5. log-sum-exp merge of this rank's slice =================
         {
             const int per = (G * D + (int)nct - 1) / (int)nct;
+            const int rec = 2 * G + per;
             const int i0 = (int)crank * per;
             const int i1 = i0 + per < G * D ? i0 + per : G * D;
             for (int idx = i0 + tid; idx < i1; idx += C::THREADS) {
                 const int g = idx / D, d = idx - (idx / D) * D;
-                const uint32_t mloc = smem_u32(cstate + g * (D + 2));
                 float mst = -INFINITY;
-                for (uint32_t r = 0; r < nct; ++r) mst = fmaxf(mst, ld_dsmem_f32(dsmem_map(mloc, r)));
+                for (uint32_t r = 0; r < nct; ++r) mst = fmaxf(mst, inbox[r * rec + 2 * g]);
                 float ls = 0.f, as = 0.f;
                 for (uint32_t r = 0; r < nct; ++r) {
-                    const uint32_t base = dsmem_map(mloc, r);
-                    const float mr = ld_dsmem_f32(base);
+                    const float mr = inbox[r * rec + 2 * g];
                     if (mr != -INFINITY) {
                         const float f = fast_exp2(mr - mst);
-                        ls += f * ld_dsmem_f32(base + 4);
-                        as += f * ld_dsmem_f32(base + (uint32_t)(8 + 4 * d));
+                        ls += f * inbox[r * rec + 2 * g + 1];
+                        as += f * inbox[r * rec + 2 * G + idx - i0];
                     }
                 }
                 p.out[((int64_t)b * Hq + (int64_t)kv * G + g) * D + d] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
             }
         }
-        cluster_ready();
-        cluster_sync_all();  // before the next unit reuses keys, list and state
+        // Before the next unit reuses keys, list and inbox. After the last unit no
+        // rank touches another's shared memory, so the ranks retire without it.
+        if (u + ncl < units) {
+            cluster_ready();
+            cluster_sync_all();
+        }
     }
 
     cluster_ready();  // a cluster with no unit still completes the start barrier
