@@ -55,8 +55,9 @@ __device__ __forceinline__ uint32_t cluster_ctas() {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// Arrive without release: for a barrier that only says "this CTA is running".
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -96,13 +97,6 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Unsigned min / max into a shared word of CTA `rank` of this cluster.
-__device__ __forceinline__ void red_dsmem_min_u32(uint32_t local_addr, uint32_t rank, uint32_t v) {
-    asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(dsmem_map(local_addr, rank)), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_dsmem_max_u32(uint32_t local_addr, uint32_t rank, uint32_t v) {
-    asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(dsmem_map(local_addr, rank)), "r"(v) : "memory");
-}
 
 enum { FUSED_FULL = 0, FUSED_ATTEND = 1 };
 
@@ -122,7 +116,7 @@ struct FusedCfg : TileCfg<D, G> {
     // A cluster rank's inbox: for every source rank, (m, l) of the G rows then
     // the accumulators of the rank's slice of the G*D outputs (<= 8 ranks).
     static constexpr int INBOX = (G * D + 16 * G + 8) * 4;
-    // misc region, in 4-byte words: hist [0,512), totals [512,768), tile info
+    // misc region, in 4-byte words: hist [0,512), totals [512,768), unused
     // [768,800), counts [800,808), scan scratch [808,832), scalars [832,848),
     // then the full/empty mbarriers (8-byte aligned) at word 848.
     static constexpr int MISC_BARRIER_WORD = 848;
@@ -133,7 +127,6 @@ struct FusedCfg : TileCfg<D, G> {
     static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
     static constexpr int KPT = 16;                  // keys per thread in the gathered selection
     static_assert(KPT * THREADS >= KEYS_MAX, "gathered keys fit in registers");
-    static_assert(NSTAGE * 8 <= 32, "tile info slots");
     static constexpr int NCHQ = D / 16;             // 16-byte chunks per record quarter
     static constexpr bool QTREG = (G * D <= 512);
     static constexpr int GQT = QTREG ? G : 4;
@@ -174,11 +167,10 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     int *misc = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(inbox) + C::INBOX);
     int *hist = misc;                     // [2][256]
     int *tots = misc + 512;               // [256]
-    int *tinfo = misc + 768;              // [NSTAGE][8] valid tokens per page of a stage
     int *cnt = misc + 800;                // [2] this CTA's (> kth, == kth) counts
     int *wsum = misc + 808;               // [2][9] block-scan scratch
     int *sh = misc + 832;                 // [0] bin, [1] remaining, [2] abort, [3] done, [4..5] key range,
-                                          // [6..7] this CTA's key range, [8..9] CTA 0: the unit's key range
+                                          // [6..7] this CTA's key range
     uint64_t *full = reinterpret_cast<uint64_t *>(misc + C::MISC_BARRIER_WORD);
     uint64_t *empty = full + C::NSTAGE;
     volatile int *abort_flag = &sh[2];
@@ -198,8 +190,6 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), C::NCW);
         }
-        sh[8] = (int)0xffffffffu;  // key range of the gathered unit (min, max)
-        sh[9] = 0;
         fence_mbar_init();
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
@@ -216,7 +206,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     // start barrier is arrived at here and waited on just before a thread's
     // first remote access or cluster barrier (cluster_ready), so the first
     // metadata loads and q loads are issued meanwhile.
-    cluster_arrive();  // release: this CTA's initialised barriers and key range
+    // No remote access reads anything written before it, so the arrive is
+    // relaxed (a release arrive costs a cluster-scope fence here).
+    cluster_arrive_relaxed();
     bool cl_pending = true;
     auto cluster_ready = [&]() {
         if (cl_pending) {
@@ -342,7 +334,6 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                     named_bar_sync(1, C::NCW * 32);
                 }
-                uint32_t kmin_l = 0xffffffffu, kmax_l = 0u;  // range of the keys this thread stores
                 cluster_ready();  // the key stores below reach CTA 0
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % C::NSTAGE;
@@ -405,8 +396,6 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                             const uint32_t key = score_key(best);
                             if (gather) {  // CTA 0 receives every key of the unit
                                 st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), key);
-                                kmin_l = key < kmin_l ? key : kmin_l;
-                                kmax_l = key > kmax_l ? key : kmax_l;
                             } else {
                                 keys[page - pr0] = key;
                             }
@@ -415,17 +404,6 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-                }
-                if (gather) {
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        kmin_l = min(kmin_l, (uint32_t)__shfl_xor_sync(0xffffffffu, kmin_l, o));
-                        kmax_l = max(kmax_l, (uint32_t)__shfl_xor_sync(0xffffffffu, kmax_l, o));
-                    }
-                    if (lane == 0) {
-                        red_dsmem_min_u32(smem_u32(&sh[8]), 0, kmin_l);
-                        red_dsmem_max_u32(smem_u32(&sh[9]), 0, kmax_l);
-                    }
                 }
             }
             if (gather) {
@@ -439,10 +417,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 // ============ 2-3. CTA 0: exact top-K from register-held keys ============
                 // Thread t holds the contiguous run of keys [t*chunk, t*chunk + cnt).
                 // The K-th largest key is located by narrowing a key range [lo, hi],
-                // starting from the unit's key range that the scoring reduced into
-                // CTA 0: each pass bins the keys inside it by (key - lo) >> shift into
-                // at most 2048 bins (histogram in the idle stage ring) and keeps the
-                // bin holding the K-th key, until that bin is wholly selected or
+                // starting from the keys' [min, max]: each pass bins the keys inside
+                // it by (key - lo) >> shift into at most 2048 bins (histogram in the
+                // idle stage ring) and keeps the bin holding the K-th key, until that bin is wholly selected or
                 // holds one key value (one pass, usually). Selected: keys above hi
                 // plus the first `need_eq` pages (lowest index) with lo <= key <= hi.
                 // Entry `pos` of the ascending page list goes to the CTA whose share
@@ -460,8 +437,30 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     uint32_t lo = 0, hi = 0xffffffffu;
                     int need_eq = P;
                     if (P > p.kpages) {
-                        lo = (uint32_t)sh[8];
-                        hi = (uint32_t)sh[9];
+                        // the unit's key range: block min / max of the held keys
+                        uint32_t kmn = 0xffffffffu, kmx = 0u;
+#pragma unroll
+                        for (int e = 0; e < C::KPT; ++e)
+                            if (e < kc) {
+                                kmn = kr[e] < kmn ? kr[e] : kmn;
+                                kmx = kr[e] > kmx ? kr[e] : kmx;
+                            }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            kmn = min(kmn, (uint32_t)__shfl_xor_sync(0xffffffffu, kmn, o));
+                            kmx = max(kmx, (uint32_t)__shfl_xor_sync(0xffffffffu, kmx, o));
+                        }
+                        if (lane == 0) {
+                            wsum[warp] = (int)kmn;
+                            wsum[9 + warp] = (int)kmx;
+                        }
+                        __syncthreads();
+                        lo = 0xffffffffu;
+                        hi = 0u;
+                        for (int w = 0; w < C::NCW + 1; ++w) {
+                            lo = min(lo, (uint32_t)wsum[w]);
+                            hi = max(hi, (uint32_t)wsum[9 + w]);
+                        }
                         int rem = p.kpages;
                         for (int pass = 0; pass < 4 && lo < hi; ++pass) {
                             const uint32_t span = hi - lo;
@@ -521,10 +520,6 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                             if (done) break;
                         }
                         need_eq = rem;
-                    }
-                    if (tid == 0) {  // reset the key range for the next unit
-                        sh[8] = (int)0xffffffffu;
-                        sh[9] = 0;
                     }
                     // ---- compaction: positions from a block scan of (above, in range) ----
                     int ngt = 0, neq = 0;
