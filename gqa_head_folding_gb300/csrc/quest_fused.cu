@@ -125,8 +125,6 @@ struct FusedCfg : TileCfg<D, G> {
     static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
     static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
     static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
-    static constexpr int KPT = 16;                  // keys per thread in the gathered selection
-    static_assert(KPT * THREADS >= KEYS_MAX, "gathered keys fit in registers");
     static constexpr int NCHQ = D / 16;             // 16-byte chunks per record quarter
     static constexpr bool QTREG = (G * D <= 512);
     static constexpr int GQT = QTREG ? G : 4;
@@ -178,8 +176,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t crank = cluster_rank();
     const uint32_t nct = cluster_ctas();
-    const int cid = (int)(blockIdx.x / nct);
-    const int ncl = (int)(gridDim.x / nct);
+    const int lgc = __ffs((int)nct) - 1;  // cluster sizes are powers of two: shares by shifts
+    const int cid = (int)(blockIdx.x >> lgc);
+    const int ncl = (int)(gridDim.x >> lgc);
     const int Hq = p.Hkv * G;
     const int units = p.B * p.Hkv;
     const bool producer = (warp == C::NCW);
@@ -198,9 +197,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     pdl_wait_and_release();
     // The first unit's length (and appended position) are read before the
     // barriers, so their latency overlaps them.
-    const int raw_first = (int)(blockIdx.x / cluster_ctas()) < p.B * p.Hkv ? p.valid_len[(blockIdx.x / cluster_ctas()) / p.Hkv] : 1;
-    const int pos_first = (p.pos != nullptr && (int)(blockIdx.x / cluster_ctas()) < p.B * p.Hkv)
-                              ? p.pos[(blockIdx.x / cluster_ctas()) / p.Hkv] : 0;
+    const int raw_first = cid < p.B * p.Hkv ? p.valid_len[cid / p.Hkv] : 1;
+    const int pos_first = (p.pos != nullptr && cid < p.B * p.Hkv) ? p.pos[cid / p.Hkv] : 0;
     __syncthreads();
     // Every CTA of the cluster must be running before any remote access: the
     // start barrier is arrived at here and waited on just before a thread's
@@ -239,8 +237,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             // (two cluster barriers in all). Otherwise each CTA keeps its own keys
             // and the radix passes sum histograms over the cluster.
             const bool gather = P <= C::KEYS_MAX;
-            const int pr0 = (int)(((int64_t)crank * P) / nct);
-            const int pr1 = (int)(((int64_t)(crank + 1) * P) / nct);
+            const int pr0 = (int)(((int64_t)crank * P) >> lgc);
+            const int pr1 = (int)(((int64_t)(crank + 1) * P) >> lgc);
             const int ntile = (pr1 - pr0 + C::MT - 1) / C::MT;
             if (producer) {
                 // The appended token's page is written just before the metadata
@@ -414,37 +412,36 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             }
 
             if (gather) {
-                // ============ 2-3. CTA 0: exact top-K from register-held keys ============
-                // Thread t holds the contiguous run of keys [t*chunk, t*chunk + cnt).
+                // ============ 2-3. CTA 0: exact top-K of the gathered keys ============
+                // Thread t owns the contiguous run of keys [c0, c1) = [t*chunk, ...).
                 // The K-th largest key is located by narrowing a key range [lo, hi],
                 // starting from the keys' [min, max]: each pass bins the keys inside
                 // it by (key - lo) >> shift into at most 2048 bins (histogram in the
-                // idle stage ring) and keeps the bin holding the K-th key, until that bin is wholly selected or
-                // holds one key value (one pass, usually). Selected: keys above hi
-                // plus the first `need_eq` pages (lowest index) with lo <= key <= hi.
-                // Entry `pos` of the ascending page list goes to the CTA whose share
-                // [r*nsel/C, (r+1)*nsel/C) contains it.
+                // idle stage ring) and keeps the bin holding the K-th key, until that
+                // bin is wholly selected or holds one key value (one pass, usually).
+                // Selected: keys above hi plus the first `need_eq` pages (lowest
+                // index) with lo <= key <= hi. Entry `pos` of the ascending page list
+                // goes to the CTA whose share [r*nsel/C, (r+1)*nsel/C) contains it.
+                // This code runs once per unit on one CTA, so its loops are kept
+                // rolled: it is short of instruction-cache hits, not of issue slots.
                 if (crank == 0) {
                     constexpr int NBIN = 2048;
                     static_assert(NBIN * 4 <= C::STAGE, "the histogram fits in one ring stage");
                     int *hb = reinterpret_cast<int *>(ring);
                     const int chunk = (P + C::THREADS - 1) / C::THREADS;
                     const int c0 = tid * chunk < P ? tid * chunk : P;
-                    const int kc = c0 + chunk < P ? chunk : P - c0;
-                    uint32_t kr[C::KPT];
-#pragma unroll
-                    for (int e = 0; e < C::KPT; ++e) kr[e] = e < kc ? keys[c0 + e] : 0u;
+                    const int c1 = c0 + chunk < P ? c0 + chunk : P;
                     uint32_t lo = 0, hi = 0xffffffffu;
                     int need_eq = P;
                     if (P > p.kpages) {
                         // the unit's key range: block min / max of the held keys
                         uint32_t kmn = 0xffffffffu, kmx = 0u;
-#pragma unroll
-                        for (int e = 0; e < C::KPT; ++e)
-                            if (e < kc) {
-                                kmn = kr[e] < kmn ? kr[e] : kmn;
-                                kmx = kr[e] > kmx ? kr[e] : kmx;
-                            }
+#pragma unroll 1
+                        for (int i = c0; i < c1; ++i) {
+                            const uint32_t k = keys[i];
+                            kmn = k < kmn ? k : kmn;
+                            kmx = k > kmx ? k : kmx;
+                        }
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) {
                             kmn = min(kmn, (uint32_t)__shfl_xor_sync(0xffffffffu, kmn, o));
@@ -468,9 +465,11 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                             const int shift = bits > 11 ? bits - 11 : 0;
                             for (int i = tid; i < NBIN; i += C::THREADS) hb[i] = 0;
                             __syncthreads();
-#pragma unroll
-                            for (int e = 0; e < C::KPT; ++e)
-                                if (e < kc && kr[e] >= lo && kr[e] <= hi) atomicAdd(&hb[(kr[e] - lo) >> shift], 1);
+#pragma unroll 1
+                            for (int i = c0; i < c1; ++i) {
+                                const uint32_t k = keys[i];
+                                if (k >= lo && k <= hi) atomicAdd(&hb[(k - lo) >> shift], 1);
+                            }
                             __syncthreads();
                             // block scan from the top bin down: consumer thread t owns the
                             // 8 bins 2047-8t .. 2040-8t
@@ -523,12 +522,12 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                     // ---- compaction: positions from a block scan of (above, in range) ----
                     int ngt = 0, neq = 0;
-#pragma unroll
-                    for (int e = 0; e < C::KPT; ++e)
-                        if (e < kc) {
-                            ngt += kr[e] > hi;
-                            neq += kr[e] >= lo && kr[e] <= hi;
-                        }
+#pragma unroll 1
+                    for (int i = c0; i < c1; ++i) {
+                        const uint32_t k = keys[i];
+                        ngt += k > hi;
+                        neq += k >= lo && k <= hi;
+                    }
                     int ig = ngt, ie = neq;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
@@ -546,15 +545,14 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     // The ascending list is built in the histogram's stage first (a short
                     // loop body), then spread over the cluster by one strided loop.
                     int *sel = hb;
-#pragma unroll
-                    for (int e = 0; e < C::KPT; ++e) {
-                        if (e < kc) {
-                            const bool inr = kr[e] >= lo && kr[e] <= hi;
-                            const bool take = kr[e] > hi || (inr && eqr < need_eq);
-                            eqr += inr;
-                            if (take && pos < nsel) sel[pos] = c0 + e;
-                            pos += take;
-                        }
+#pragma unroll 1
+                    for (int i = c0; i < c1; ++i) {
+                        const uint32_t k = keys[i];
+                        const bool inr = k >= lo && k <= hi;
+                        const bool take = k > hi || (inr && eqr < need_eq);
+                        eqr += inr;
+                        if (take && pos < nsel) sel[pos] = i;
+                        pos += take;
                     }
                     __syncthreads();
                     int *prow = p.page_idx != nullptr ? p.page_idx + (int64_t)u * p.kpages : nullptr;
@@ -583,8 +581,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 const bool selecting = true;
                 const int nk = gather ? P : pr1 - pr0;
                 const int pbase = gather ? 0 : pr0;
-                const int e0s = (int)(((int64_t)crank * nsel) / nct);       // this CTA's share of the list
-                const int e1s = (int)(((int64_t)(crank + 1) * nsel) / nct);
+                const int e0s = (int)(((int64_t)crank * nsel) >> lgc);       // this CTA's share of the list
+                const int e1s = (int)(((int64_t)(crank + 1) * nsel) >> lgc);
                 uint32_t lo = 0, hi = 0xffffffffu;
                 int need_eq = 0;
                 if (P > p.kpages && selecting) {
@@ -767,8 +765,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
         }
 
         // ================= 4. attention over this CTA's share of the pages =================
-        const int e0 = (int)(((int64_t)crank * nsel) / nct);
-        const int e1 = (int)(((int64_t)(crank + 1) * nsel) / nct);
+        const int e0 = (int)(((int64_t)crank * nsel) >> lgc);
+        const int e1 = (int)(((int64_t)(crank + 1) * nsel) >> lgc);
         PageSlots slots;
         slots.init(p.S);
         const int ntile4 = (e1 - e0 + slots.ppt - 1) / slots.ppt;
@@ -840,7 +838,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
             // only local shared memory and no rank reads another after it.
             wa.store_state(merge);
             named_bar_sync(1, C::NCW * 32);
-            const int per = (G * D + (int)nct - 1) / (int)nct;
+            const int per = (G * D + (int)nct - 1) >> lgc;
             const uint32_t mine = smem_u32(inbox + (int)crank * (2 * G + per));
             for (int idx = tid; idx < G * D; idx += C::NCW * 32) {
                 const int g = idx / D, d = idx - (idx / D) * D;
@@ -860,7 +858,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
 
         // ================= 5. log-sum-exp merge of this rank's slice =================
         {
-            const int per = (G * D + (int)nct - 1) / (int)nct;
+            const int per = (G * D + (int)nct - 1) >> lgc;
             const int rec = 2 * G + per;
             const int i0 = (int)crank * per;
             const int i1 = i0 + per < G * D ? i0 + per : G * D;
