@@ -44,6 +44,7 @@ GQAQ_OPT_PDL = 5
 GQAQ_OPT_QUEST_KERNEL = 6
 GQAQ_OPT_PREFILL_SPLITS = 7
 GQAQ_OPT_PREFILL_KERNEL = 8
+GQAQ_OPT_QUEST_EARLY_META = 9
 
 PAGE_SIZE = 16
 

@@ -29,6 +29,7 @@ struct LaunchCtx {
     int quest_kernel;      // fused Quest kernel: 0 automatic, 1 cluster, 2 work queue
     int prefill_splits;    // prefill context splits per item: 0 automatic, n forced
     int prefill_kernel;    // prefill kernel: 0 automatic (tensor memory), 1 tensor memory, 2 warp MMA
+    int quest_early_meta;  // fused Quest kernel: first metadata tiles read before the grid dependency wait
     int *status;           // device status word
 };
 

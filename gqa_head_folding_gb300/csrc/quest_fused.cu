@@ -144,6 +144,7 @@ struct FusedParams {
     int B, Hkv, Lmax, Pmax, S, kpages;
     float scale_log2;
     uint64_t timeout_ns;
+    int early_meta;          // FULL: first metadata tiles of the first unit issued before the grid dependency wait
 };
 
 template <int D, int G, int MODE>
@@ -193,6 +194,42 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
         if (MODE == FUSED_FULL) prefetch_tensormap(&mmap);
+    }
+    // Early metadata (early_meta): the producer issues the first unit's first
+    // ring-full of metadata tiles before the grid dependency wait, so with a
+    // programmatic launch they stream while the previous kernel finishes. The
+    // caller guarantees that kernel writes neither valid_len, pos nor any page
+    // other than those holding rows pos-1 and pos; tiles from the one holding
+    // either on are left to the loop below, after the wait. They are the same
+    // tiles, stages and barrier phases the loop would use, so it skips them.
+    int n_early = 0;
+    if (MODE == FUSED_FULL && p.early_meta) {
+        __syncthreads();  // the ring barriers are initialised
+        if (producer && lane == 0 && cid < units) {
+            const int b0 = cid / p.Hkv;
+            const int P0 = (clamp_len(p.valid_len[b0], p.Lmax) + p.S - 1) / p.S;
+            const int q0 = (int)(((int64_t)crank * P0) >> lgc);
+            const int q1 = (int)(((int64_t)(crank + 1) * P0) >> lgc);
+            int lim = (q1 - q0 + C::MT - 1) / C::MT;
+            lim = lim < C::NSTAGE ? lim : C::NSTAGE;
+            if (p.pos != nullptr) {
+                const int pos0 = p.pos[b0];
+                if (pos0 >= 0) {
+                    const int pa = (pos0 > 0 ? pos0 - 1 : 0) / p.S, pb = pos0 / p.S;  // pages of rows pos-1, pos
+                    if (pa >= q0 && pa < q1) lim = min(lim, (pa - q0) / C::MT);
+                    if (pb >= q0 && pb < q1) lim = min(lim, (pb - q0) / C::MT);
+                }
+            }
+            const uint64_t pol0 = l2_policy_evict_first();
+            for (int t = 0; t < lim; ++t) {
+                const uint32_t fb = smem_u32(&full[t]);
+                mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
+#pragma unroll 1
+                for (int kb = 0; kb < C::NB; ++kb)
+                    tma_load_2d(smem_u32(ring + t * C::STAGE) + kb * C::MBLK, &mmap, 64 * kb, cid * p.Pmax + q0 + t * C::MT, fb, pol0);
+            }
+            n_early = lim;
+        }
     }
     pdl_wait_and_release();
     // The first unit's length (and appended position) are read before the
@@ -294,7 +331,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                             continue;  // keep the ring count in step; issue nothing
                         }
                     }
-                    if (lane == 0 && *abort_flag == 0) {
+                    if (lane == 0 && *abort_flag == 0 && !(u == cid && t < n_early)) {
                         const uint32_t fb = smem_u32(&full[s]);
                         const uint32_t dst = smem_u32(ring + s * C::STAGE);
                         mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
@@ -994,6 +1031,7 @@ int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
     p.kpages = a.kpages;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_ns = ctx.timeout_ns;
+    p.early_meta = ctx.quest_early_meta;
 
     if (launch_kernel(quest_fused_kernel<D, G, MODE>, dim3(nclusters * best_c), dim3(C::THREADS), C::SMEM, ctx, best_c,
                       mmap, kmap, vmap, p) != cudaSuccess)

@@ -318,9 +318,22 @@ enum {
     GQAQ_OPT_PREFILL_SPLITS = 7,  /* context splits per gqa_prefill_attn work item:
                                      0 (default) = enough CTAs for one wave; 1..32
                                      forced (larger splits may be empty) */
-    GQAQ_OPT_PREFILL_KERNEL = 8   /* gqa_prefill_attn's kernel: 0 (default) or 1 = the
+    GQAQ_OPT_PREFILL_KERNEL = 8,  /* gqa_prefill_attn's kernel: 0 (default) or 1 = the
                                      tensor-memory (tcgen05) kernel; 2 = the warp-level
                                      MMA kernel */
+    GQAQ_OPT_QUEST_EARLY_META = 9 /* nonzero: quest_decode_attn's cluster kernel reads
+                                     valid_len, pos and the first metadata tiles of its
+                                     first (sequence, KV head) before it waits for the
+                                     previous kernel in the stream (with GQAQ_OPT_PDL,
+                                     while that kernel is still finishing). Tiles that
+                                     hold rows pos-1 or pos are read after the wait.
+                                     The caller guarantees that the previous kernel
+                                     writes neither valid_len nor pos, nor any other
+                                     page of meta. A decode loop whose previous kernel
+                                     is another layer's attention, or this layer's
+                                     previous step, satisfies it; quest_update_meta or
+                                     a position update right before does not.
+                                     Default 0. */
 };
 GQAQ_API int gqaq_set_option(int option, int64_t value);
 

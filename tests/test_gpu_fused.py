@@ -34,6 +34,7 @@ def _reset_options():
     g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, 0)
     g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
     g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 0)
+    g.set_option(g.GQAQ_OPT_QUEST_EARLY_META, 0)
 
 
 def use_queue_kernel():
@@ -325,3 +326,60 @@ def test_sparse_call_above_the_fused_page_limit():
     with pytest.raises(g.GqaqError):              # the cluster kernel stops at 1024 pages
         meta = g.new_meta(B, Hkv, Lmax, D, DEV)
         g.quest_decode_attn(x["q"], x["k_cache"], x["v_cache"], meta, vl, K, 0.125)
+
+
+@pytest.mark.parametrize("csize,valid0", [(1, (16 * 30 - 1, 16 * 23 + 15, 17)), (4, (16 * 44 - 2, 16 * 8, 33)),
+                                          (8, (16 * 45 + 1, 16 * 16 - 1, 2))])
+def test_fused_early_metadata_decode_loop(csize, valid0):
+    """GQAQ_OPT_QUEST_EARLY_META: two layers, three decode steps, every call
+    launched right behind the other layer's (programmatic launch), as a decode
+    loop does. Steps cross page boundaries (pos % S == 0, the case where the
+    previous step wrote the page before the appended one); each output and
+    page list is checked against the oracle replaying the appends."""
+    g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, csize)
+    g.set_option(g.GQAQ_OPT_QUEST_EARLY_META, 1)
+    B, Hkv, G, D, K = 3, 2, 4, 128, 8
+    Lmax, nsteps, nl = 16 * 45 + 3, 3, 2
+    w = workloads.Workload(0, "fused", batch=B, num_layers=nl, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax, k_pages=K, n_plant=3, append=True)
+    xs = [workloads.make_layer(w, l, device="cpu", seed=50 + csize + l) for l in range(nl)]
+    gen = torch.Generator().manual_seed(90 + csize)
+    knew = torch.randn(nsteps, nl, B, Hkv, D, generator=gen).to(torch.float16)
+    vnew = torch.randn(nsteps, nl, B, Hkv, D, generator=gen).to(torch.float16)
+    vls = [np.array(valid0) + s for s in range(nsteps)]
+    vld = [torch.tensor(v, dtype=torch.int32, device=DEV) for v in vls]       # made before the loop:
+    posd = [torch.tensor(v - 1, dtype=torch.int32, device=DEV) for v in vls]  # no kernel writes them in it
+    kd = [x["k_cache"].to(DEV) for x in xs]
+    vd = [x["v_cache"].to(DEV) for x in xs]
+    qd = [x["q"].to(DEV) for x in xs]
+    metas = [g.new_meta(B, Hkv, Lmax, D, DEV) for _ in range(nl)]
+    for l in range(nl):
+        g.quest_update_meta(kd[l], vld[0] - 1, metas[l])
+    kn, vn = knew.to(DEV), vnew.to(DEV)
+    outs = torch.empty(nsteps, nl, B, G * Hkv, D, dtype=torch.float16, device=DEV)
+    idx = torch.full((nsteps, nl, B, Hkv, K), -7, dtype=torch.int32, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+    torch.cuda.synchronize()
+    for s in range(nsteps):
+        for l in range(nl):
+            g.quest_decode_attn(qd[l], kd[l], vd[l], metas[l], vld[s], K, scale, k_new=kn[s, l], v_new=vn[s, l],
+                                pos=posd[s], out=outs[s, l], page_idx=idx[s, l])
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    for l in range(nl):
+        kc = xs[l]["k_cache"].numpy().copy(); vc = xs[l]["v_cache"].numpy().copy()
+        q = xs[l]["q"].numpy()
+        for s in range(nsteps):
+            vl = vls[s]
+            for b in range(B):
+                kc[b, :, vl[b] - 1] = knew[s, l, b].numpy(); vc[b, :, vl[b] - 1] = vnew[s, l, b].numpy()
+            ref_meta = oracle.page_minmax(kc, vl, S)
+            ref_scores = oracle.page_scores(q, ref_meta, vl, S)
+            sel = idx[s, l].cpu().numpy()
+            check_topk(sel, ref_scores, vl, S, K)
+            assert_attn_close(outs[s, l], oracle.sparse_attn(q, kc, vc, vl, sel, S, scale), f"step {s} layer {l}")
+        assert np.array_equal(kd[l].cpu().numpy(), kc) and np.array_equal(vd[l].cpu().numpy(), vc)
+        got_meta = to64(metas[l])
+        for b in range(B):
+            P = (vls[-1][b] + S - 1) // S
+            assert np.array_equal(got_meta[b, :, :P], ref_meta[b, :, :P]), f"meta layer {l} b={b}"
