@@ -265,11 +265,12 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from one ncu
-# capture of the kernel as it stands, keyed by (workload id, batch, family). A kernel
-# change makes its entry stale: it is then removed until the capture is taken again.
-NCU_TRAFFIC = {(3, 1, "quest", "f16"): 67_678_464, (3, 1, "dense", "f16"): 539_854_848,
-               (2, 32, "dense", "f16"): 180_059_392, (2, 32, "dense", "e4m3"): 90_767_360,
-               (2, 32, "dense", "int4"): 49_910_272}
+# capture of the kernel as it stands, keyed by (workload id, batch, family, KV format,
+# page size). A kernel change makes its entry stale: it is then removed until the capture
+# is taken again.
+NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_692_032, (3, 1, "dense", "f16", 16): 539_840_256,
+               (2, 32, "dense", "f16", 16): 179_752_192, (2, 32, "dense", "e4m3", 16): 90_767_360,
+               (2, 32, "dense", "int4", 16): 49_910_272}
 
 
 def capture(fn, device):
@@ -649,7 +650,7 @@ def run_ours(args, rank, world, local):
                                            "sparse": "quest_sparse_attn", "quest": "quest_decode_attn"}[dominant],
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                "traffic": NCU_TRAFFIC.get((w.id, w.batch, dominant, args.kv)), "bytes_per_launch": per_launch,
+                "traffic": NCU_TRAFFIC.get((w.id, w.batch, dominant, args.kv, w.page_size)), "bytes_per_launch": per_launch,
                 "us_per_launch": round(fam[dominant]["s_per_launch"] * 1e6, 2)}
 
     # end to end through the public API: host inputs in, host outputs out
