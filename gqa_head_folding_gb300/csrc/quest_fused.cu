@@ -111,8 +111,7 @@ struct FusedCfg : TileCfg<D, G> {
     static constexpr int KEYS_MAX = 4096;           // pages one CTA scores per unit
     static constexpr int KSEL_MAX = 1024;           // selected pages per unit
     static constexpr int KEYMERGE = (KEYS_MAX * 4 > T::MERGE) ? KEYS_MAX * 4 : T::MERGE;
-    static constexpr int QT_BYTES = G * 2 * D * 2;  // [G][2D] fp16 [q_neg | q_pos]
-    static constexpr int QREGION = (QT_BYTES > T::QBYTES) ? QT_BYTES : T::QBYTES;
+    static constexpr int QREGION = T::QBYTES;       // q of the attention tile when it is staged
     // A cluster rank's inbox: for every source rank, (m, l) of the G rows then
     // the accumulators of the rank's slice of the G*D outputs (<= 8 ranks).
     static constexpr int INBOX = (G * D + 16 * G + 8) * 4;
@@ -125,10 +124,6 @@ struct FusedCfg : TileCfg<D, G> {
     static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
     static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
     static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
-    static constexpr int NCHQ = D / 16;             // 16-byte chunks per record quarter
-    static constexpr bool QTREG = (G * D <= 512);
-    static constexpr int GQT = QTREG ? G : 4;
-    static constexpr int NPASST = G / GQT;
 };
 
 struct FusedParams {
@@ -343,31 +338,26 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 }
                 if (papp >= 0 && tapp < 0) append();  // a page past the valid ones: no tile reads it here
             } else {
-                // consumer warps: lane = 8*quarter + page; 16 pages per warp per tile
-                const int jp = lane & 7, qq = lane >> 3;
-                const int cq0 = qq * (D / 2);
-                const bool negq = qq < 2;
-                const int qch0 = (qq & 1) * (D / 2);
-                uint4 qt[C::GQT][C::NCHQ];
-                if (C::QTREG) {
+                // consumer warps: each scores 16 pages of every tile on the tensor
+                // cores, S^T[page][g] = [m; M](page) . [min(q_g, 0); max(q_g, 0)], as
+                // one m16n8k16 chain over the 2D-wide record (pages on M, the G query
+                // rows on N, columns past G zero and masked), fp32 accumulation.
+                constexpr int KS = 2 * D / 16;  // k-steps over the [m; M] record
+                uint32_t qb[KS][2];             // B fragments: rows k0, k0+1 (+8) of column lane/4
+                {
+                    const int n = lane >> 2, k0 = 2 * (lane & 3);
 #pragma unroll
-                    for (int g = 0; g < C::GQT; ++g)
+                    for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-                        for (int c = 0; c < C::NCHQ; ++c) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(qg + g * D + qch0 + c * 8);
-                            qt[g][c] = negq ? make_uint4(hmin0_bits(v.x), hmin0_bits(v.y), hmin0_bits(v.z), hmin0_bits(v.w))
-                                            : make_uint4(hmax0_bits(v.x), hmax0_bits(v.y), hmax0_bits(v.z), hmax0_bits(v.w));
+                        for (int h = 0; h < 2; ++h) {
+                            const int c = ks * 16 + k0 + 8 * h;  // record channel: c < D is the min side
+                            uint32_t v = 0u;
+                            if (n < G) {
+                                const uint32_t pr = *reinterpret_cast<const uint32_t *>(qg + n * D + (c < D ? c : c - D));
+                                v = c < D ? hmin0_bits(pr) : hmax0_bits(pr);
+                            }
+                            qb[ks][h] = v;
                         }
-                } else {
-                    for (int e = tid; e < G * D / 8; e += C::NCW * 32) {
-                        const int g = e / (D / 8), c = e % (D / 8);
-                        const uint4 v = *reinterpret_cast<const uint4 *>(qg + g * D + c * 8);
-                        reinterpret_cast<uint4 *>(qreg_s + g * 2 * D)[c] =
-                            make_uint4(hmin0_bits(v.x), hmin0_bits(v.y), hmin0_bits(v.z), hmin0_bits(v.w));
-                        reinterpret_cast<uint4 *>(qreg_s + g * 2 * D + D)[c] =
-                            make_uint4(hmax0_bits(v.x), hmax0_bits(v.y), hmax0_bits(v.z), hmax0_bits(v.w));
-                    }
-                    named_bar_sync(1, C::NCW * 32);
                 }
                 cluster_ready();  // the key stores below reach CTA 0
                 for (int t = 0; t < ntile; ++t, ++it) {
@@ -380,61 +370,39 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         if (!ok && lane == 0) { raise_flag(p.status, GQAQ_DEV_TIMEOUT); *abort_flag = 1; }
                     }
                     const uint32_t sbase = smem_u32(ring + s * C::STAGE);
+                    const int first = pr0 + t * C::MT + warp * 16;  // this warp's 16 pages
+                    if (ok && first < pr1) {                        // warp-uniform
+                        const int arow = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);  // ldmatrix row address
+                        const uint32_t abase = sbase + (uint32_t)(arow * 128);
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int pass = 0; pass < 2; ++pass) {
-                        const int row = warp * 16 + pass * 8 + jp;
-                        const int first = pr0 + t * C::MT + warp * 16 + pass * 8;
-                        if (!ok || first >= pr1) continue;  // warp-uniform
-                        const uint32_t base = sbase + (uint32_t)((cq0 / 64) * C::MBLK + row * 128);
-                        const uint32_t x0 = (uint32_t)(((cq0 % 64) / 8) ^ (row & 7));
-                        float uu[G];
+                        for (int ks = 0; ks < KS; ++ks) {
+                            const uint32_t c16 = (uint32_t)((ks & 3) * 2 + (lane >> 4));
+                            uint32_t af[4];
+                            ldsm_x4(abase + (uint32_t)((ks >> 2) * C::MBLK) + ((c16 ^ (uint32_t)(arow & 7)) << 4), af);
+                            mma_16816(acc, af, qb[ks][0], qb[ks][1]);
+                        }
+                        // C fragment: rows lane/4 and lane/4 + 8, columns 2*(lane%4) + {0, 1}
+                        const int g0 = 2 * (lane & 3);
+                        float b0 = fmaxf(g0 < G ? acc[0] : -INFINITY, g0 + 1 < G ? acc[1] : -INFINITY);
+                        float b1 = fmaxf(g0 < G ? acc[2] : -INFINITY, g0 + 1 < G ? acc[3] : -INFINITY);
+                        b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, 1));
+                        b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, 1));
+                        b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, 2));
+                        b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, 2));
 #pragma unroll
-                        for (int ps = 0; ps < C::NPASST; ++ps) {
-                            if (!C::QTREG) {
-#pragma unroll
-                                for (int g = 0; g < C::GQT; ++g)
-#pragma unroll
-                                    for (int c = 0; c < C::NCHQ; ++c)
-                                        qt[g][c] = lds128(smem_u32(qreg_s + (ps * C::GQT + g) * 2 * D + cq0 + c * 8));
-                            }
-                            float a0[C::GQT], a1[C::GQT];
-#pragma unroll
-                            for (int g = 0; g < C::GQT; ++g) a0[g] = a1[g] = 0.f;
-#pragma unroll
-                            for (int c = 0; c < C::NCHQ; ++c) {
-                                const uint4 mc = lds128(base + ((x0 ^ (uint32_t)c) << 4));
-#pragma unroll
-                                for (int g = 0; g < C::GQT; ++g) {
-                                    a0[g] = fma_h_lo(qt[g][c].x, mc.x, a0[g]);
-                                    a1[g] = fma_h_hi(qt[g][c].x, mc.x, a1[g]);
-                                    a0[g] = fma_h_lo(qt[g][c].y, mc.y, a0[g]);
-                                    a1[g] = fma_h_hi(qt[g][c].y, mc.y, a1[g]);
-                                    a0[g] = fma_h_lo(qt[g][c].z, mc.z, a0[g]);
-                                    a1[g] = fma_h_hi(qt[g][c].z, mc.z, a1[g]);
-                                    a0[g] = fma_h_lo(qt[g][c].w, mc.w, a0[g]);
-                                    a1[g] = fma_h_hi(qt[g][c].w, mc.w, a1[g]);
+                        for (int half = 0; half < 2; ++half) {
+                            const float best = half ? b1 : b0;
+                            const int page = first + (lane >> 2) + 8 * half;
+                            if ((lane & 3) == 0 && page < pr1) {
+                                const uint32_t key = score_key(best);
+                                if (gather) {  // CTA 0 receives every key of the unit
+                                    st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), key);
+                                } else {
+                                    keys[page - pr0] = key;
                                 }
+                                if (p.scores != nullptr) p.scores[(int64_t)u * p.Pmax + page] = best;
                             }
-#pragma unroll
-                            for (int g = 0; g < C::GQT; ++g) uu[ps * C::GQT + g] = a0[g] + a1[g];
-                        }
-                        float best = -INFINITY;
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            float x = uu[g];
-                            x += __shfl_xor_sync(0xffffffffu, x, 8);
-                            x += __shfl_xor_sync(0xffffffffu, x, 16);
-                            best = fmaxf(best, x);
-                        }
-                        const int page = first + jp;
-                        if (qq == 0 && page < pr1) {
-                            const uint32_t key = score_key(best);
-                            if (gather) {  // CTA 0 receives every key of the unit
-                                st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), key);
-                            } else {
-                                keys[page - pr0] = key;
-                            }
-                            if (p.scores != nullptr) p.scores[(int64_t)u * p.Pmax + page] = best;
                         }
                     }
                     __syncwarp();
