@@ -427,8 +427,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 // Selected: keys above hi plus the first `need_eq` pages (lowest
                 // index) with lo <= key <= hi. Entry `pos` of the ascending page list
                 // goes to the CTA whose share [r*nsel/C, (r+1)*nsel/C) contains it.
-                // This code runs once per unit on one CTA, so its loops are kept
-                // rolled: it is short of instruction-cache hits, not of issue slots.
+                // This code runs once per unit on one CTA, so its loops are only
+                // lightly unrolled (four independent loads in flight): it is short of
+                // instruction-cache hits and load latency, not of issue slots.
                 if (crank == 0) {
                     constexpr int NBIN = 2048;
                     static_assert(NBIN * 4 <= C::STAGE, "the histogram fits in one ring stage");
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     if (P > p.kpages) {
                         // the unit's key range: block min / max of the held keys
                         uint32_t kmn = 0xffffffffu, kmx = 0u;
-#pragma unroll 1
+#pragma unroll 4
                         for (int i = c0; i < c1; ++i) {
                             const uint32_t k = keys[i];
                             kmn = k < kmn ? k : kmn;
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                             const int shift = bits > 11 ? bits - 11 : 0;
                             for (int i = tid; i < NBIN; i += C::THREADS) hb[i] = 0;
                             __syncthreads();
-#pragma unroll 1
+#pragma unroll 4
                             for (int i = c0; i < c1; ++i) {
                                 const uint32_t k = keys[i];
                                 if (k >= lo && k <= hi) atomicAdd(&hb[(k - lo) >> shift], 1);
@@ -527,7 +528,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     }
                     // ---- compaction: positions from a block scan of (above, in range) ----
                     int ngt = 0, neq = 0;
-#pragma unroll 1
+#pragma unroll 4
                     for (int i = c0; i < c1; ++i) {
                         const uint32_t k = keys[i];
                         ngt += k > hi;
@@ -550,7 +551,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     // The ascending list is built in the histogram's stage first (a short
                     // loop body), then spread over the cluster by one strided loop.
                     int *sel = hb;
-#pragma unroll 1
+#pragma unroll 4
                     for (int i = c0; i < c1; ++i) {
                         const uint32_t k = keys[i];
                         const bool inr = k >= lo && k <= hi;
