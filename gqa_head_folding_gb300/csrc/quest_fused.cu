@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     int *list = reinterpret_cast<int *>(fixed + C::KEYMERGE + C::QREGION + C::PBYTES);
     float *inbox = reinterpret_cast<float *>(list + C::KSEL_MAX);
     int *misc = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(inbox) + C::INBOX);
-    int *hist = misc;                     // [2][256]
+    int *hist = misc;                     // [2][256] (cluster radix passes)
+    uint32_t *krange = reinterpret_cast<uint32_t *>(misc);  // [2][64] gathered unit: per-warp key min / max
     int *tots = misc + 512;               // [256]
     int *cnt = misc + 800;                // [2] this CTA's (> kth, == kth) counts
     int *wsum = misc + 808;               // [2][9] block-scan scratch
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         }
                 }
                 cluster_ready();  // the key stores below reach CTA 0
+                uint32_t kmn = 0xffffffffu, kmx = 0u;  // range of the keys this lane stores (gather)
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % C::NSTAGE;
                     const uint32_t ph = (uint32_t)(it / C::NSTAGE) & 1u;
@@ -398,6 +400,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                                 const uint32_t key = score_key(best);
                                 if (gather) {  // CTA 0 receives every key of the unit
                                     st_dsmem_u32(dsmem_map(smem_u32(keys + page), 0), key);
+                                    kmn = key < kmn ? key : kmn;
+                                    kmx = key > kmx ? key : kmx;
                                 } else {
                                     keys[page - pr0] = key;
                                 }
@@ -408,10 +412,22 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
                 }
+                if (gather) {  // this warp's key range into CTA 0's slot (every unit, even if empty)
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        kmn = min(kmn, (uint32_t)__shfl_xor_sync(0xffffffffu, kmn, o));
+                        kmx = max(kmx, (uint32_t)__shfl_xor_sync(0xffffffffu, kmx, o));
+                    }
+                    if (lane == 0) {
+                        const int slot = (int)crank * C::NCW + warp;
+                        st_dsmem_u32(dsmem_map(smem_u32(&krange[slot]), 0), kmn);
+                        st_dsmem_u32(dsmem_map(smem_u32(&krange[64 + slot]), 0), kmx);
+                    }
+                }
             }
             if (gather) {
                 cluster_ready();
-                cluster_sync_all();  // CTA 0 holds every key of the unit
+                cluster_sync_all();  // CTA 0 holds every key of the unit and its range
             } else {
                 __syncthreads();
             }
@@ -440,29 +456,18 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     uint32_t lo = 0, hi = 0xffffffffu;
                     int need_eq = P;
                     if (P > p.kpages) {
-                        // the unit's key range: block min / max of the held keys
-                        uint32_t kmn = 0xffffffffu, kmx = 0u;
-#pragma unroll 4
-                        for (int i = c0; i < c1; ++i) {
-                            const uint32_t k = keys[i];
-                            kmn = k < kmn ? k : kmn;
-                            kmx = k > kmx ? k : kmx;
+                        // the unit's key range: the scoring warps' slots, reduced per warp
+                        const int nslot = (int)nct * C::NCW;  // <= 64
+                        lo = 0xffffffffu;
+                        hi = 0u;
+                        for (int i = lane; i < nslot; i += 32) {
+                            lo = min(lo, krange[i]);
+                            hi = max(hi, krange[64 + i]);
                         }
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) {
-                            kmn = min(kmn, (uint32_t)__shfl_xor_sync(0xffffffffu, kmn, o));
-                            kmx = max(kmx, (uint32_t)__shfl_xor_sync(0xffffffffu, kmx, o));
-                        }
-                        if (lane == 0) {
-                            wsum[warp] = (int)kmn;
-                            wsum[9 + warp] = (int)kmx;
-                        }
-                        __syncthreads();
-                        lo = 0xffffffffu;
-                        hi = 0u;
-                        for (int w = 0; w < C::NCW + 1; ++w) {
-                            lo = min(lo, (uint32_t)wsum[w]);
-                            hi = max(hi, (uint32_t)wsum[9 + w]);
+                            lo = min(lo, (uint32_t)__shfl_xor_sync(0xffffffffu, lo, o));
+                            hi = max(hi, (uint32_t)__shfl_xor_sync(0xffffffffu, hi, o));
                         }
                         int rem = p.kpages;
                         for (int pass = 0; pass < 4 && lo < hi; ++pass) {
