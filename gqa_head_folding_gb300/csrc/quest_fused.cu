@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         const int ye = __shfl_up_sync(0xffffffffu, ie, o);
                         if (lane >= o) { ig += yg; ie += ye; }
                     }
-                    __syncthreads();  // wsum is reused below
+                    // (the last pass ended at a barrier after its reads of wsum)
                     if (lane == 31) { wsum[warp] = ig; wsum[9 + warp] = ie; }
                     __syncthreads();
                     int bg = 0, be = 0;
