@@ -729,13 +729,31 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             for (int ch = 0; ch < C::TT / 64; ++ch) {
                 uint32_t v[64], pk[32];
                 tmem_ld64(scol + 64u * ch, v);
-                float cm = -INFINITY;
+                // With a positive scale the max is taken on the raw scores and the
+                // scale folds into the exponent's FFMA; otherwise the scores are
+                // scaled first (mul = 1 below).
+                float cm, mul;
+                if (p.scale_log2 > 0.f) {
+                    if (need_mask) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    float x = __uint_as_float(v[e]) * p.scale_log2;
-                    if (need_mask && tok0 + 64 * ch + e > lim) x = -INFINITY;
-                    v[e] = __float_as_uint(x);
-                    cm = fmaxf(cm, x);
+                        for (int e = 0; e < 64; ++e)
+                            if (tok0 + 64 * ch + e > lim) v[e] = __float_as_uint(-INFINITY);
+                    }
+                    float r = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) r = fmaxf(r, __uint_as_float(v[e]));
+                    cm = r * p.scale_log2;
+                    mul = p.scale_log2;
+                } else {
+                    cm = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) {
+                        float x = __uint_as_float(v[e]) * p.scale_log2;
+                        if (need_mask && tok0 + 64 * ch + e > lim) x = -INFINITY;
+                        v[e] = __float_as_uint(x);
+                        cm = fmaxf(cm, x);
+                    }
+                    mul = 1.f;
                 }
                 const bool up = cm > m_ref + C::RESCALE_LOG2;
                 if (__any_sync(0xffffffffu, up)) {
@@ -767,10 +785,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                     }
                     tmem_wait_st();
                 }
-                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+                const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
-                    const float e0 = fast_exp2(__uint_as_float(v[e]) - ref), e1 = fast_exp2(__uint_as_float(v[e + 1]) - ref);
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(v[e]), mul, nref));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), mul, nref));
                     ps += e0 + e1;
                     pk[e >> 1] = pack_half2(e0, e1);
                 }
