@@ -268,9 +268,11 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
 # capture of the kernel as it stands, keyed by (workload id, batch, family, KV format,
 # page size). A kernel change makes its entry stale: it is then removed until the capture
 # is taken again.
-NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_717_376, (3, 1, "dense", "f16", 16): 539_840_256,
+NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_695_872, (3, 1, "dense", "f16", 16): 539_840_256,
                (2, 32, "dense", "f16", 16): 179_752_192, (2, 32, "dense", "e4m3", 16): 90_767_360,
                (2, 32, "dense", "int4", 16): 49_910_272}
+# The same for one prefill launch (one layer), keyed by (workload id, batch, chunk length).
+PREFILL_TRAFFIC = {(3, 1, 128): 547_805_184}
 
 
 def capture(fn, device):
@@ -578,7 +580,7 @@ def run_prefill(args, rank, world, local):
         "roofline": {"bound": "tensor", "kernel": "gqa_prefill_attn", "achieved": round(achieved, 1),
                      "peak": peaks["tensor_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["tensor_tflops"], 4),
                      "peak_source": peaks["source"] + " (bf16 sustained; fp16 has the same nominal rate)",
-                     "traffic": None, "flops_per_launch": per_launch_flops,
+                     "traffic": PREFILL_TRAFFIC.get((w.id, w.batch, Q)), "flops_per_launch": per_launch_flops,
                      "us_per_launch": round(s_per_step / w.num_layers * 1e6, 2)},
         "achieved_gbs": round(sum(prefill_bytes(w, s, Q) for s in starts) / s_per_step / 1e9, 1),
         "cpu_baseline": cpu,
