@@ -14,12 +14,14 @@
 //  1. the CTA holding the appended token's page writes the new k, v rows and
 //     that page's min/max (producer warp, made visible to TMA by a proxy
 //     fence); every CTA streams the metadata of its 1/C of the pages with TMA
-//     and scores them into shared-memory keys (U as a dot of
-//     [min(q,0); max(q,0)] with [m; M], since m <= M);
+//     and scores them on the tensor cores into shared-memory keys (U as a dot
+//     of [min(q,0); max(q,0)] with [m; M], since m <= M; pages on the MMA's M
+//     side, the G query rows on N);
 //  2-3. up to 4096 pages, CTA 0 gathers every key (remote stores into its
-//     shared memory), finds the K-th largest with range-narrowing histogram
-//     passes over register-held keys, and writes each CTA its share of the
-//     ascending page list (ties to the lower page index); with more pages,
+//     shared memory) and the scoring warps' key ranges, finds the K-th
+//     largest with range-narrowing histogram passes over the keys, and writes
+//     each CTA its share of the ascending page list (ties to the lower page
+//     index); with more pages,
 //     the cluster runs four 8-bit radix passes, summing the C per-CTA
 //     histograms through distributed shared memory, and each CTA compacts
 //     its own selected pages into every CTA's list;
