@@ -412,7 +412,8 @@ def workload_from_args(args) -> workloads.Workload:
 
 
 def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool = True,
-              quest_kernel: str = "cluster", kv: str = "f16", early_meta: bool = False) -> dict:
+              quest_kernel: str = "cluster", kv: str = "f16", early_meta: bool = False,
+              early_kv: bool = False) -> dict:
     return {"workload": f"{w.name} (config {w.id})", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
             "layers": w.num_layers, "dense_layers": w.num_layers if w.k_pages is None else w.dense_layers,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
@@ -423,8 +424,10 @@ def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool =
             "quest_path": (f"fused (quest_decode_attn, {'GPU-wide work queue' if quest_kernel == 'queue' else 'cluster per unit'})"
                            if fused else "step-by-step calls"),
             "launch": ("programmatic dependent launch" if pdl else "plain stream order")
-                      + ("; first metadata tiles read before the dependency wait"
-                         if early_meta and fused and w.k_pages is not None and quest_kernel == "cluster" else ""),
+                      + ("; Quest: first metadata tiles read before the dependency wait"
+                         if early_meta and fused and w.k_pages is not None and quest_kernel == "cluster" else "")
+                      + ("; dense: first K/V tiles read before the dependency wait"
+                         if early_kv and (w.k_pages is None or w.dense_layers > 0) else ""),
             "kv_cache": {"e4m3": "e4m3 codes, per-tensor fp32 scales",
                          "int4": "int4 levels, per-token fp32 scales"}.get(kv, "f16"),
             "l2": "per-step working set > 4x L2; no flush"}
@@ -604,6 +607,9 @@ def run_ours(args, rank, world, local):
     # every Quest call in the step follows another layer's call, which writes
     # none of this layer's metadata, valid_len or pos
     g.set_option(g.GQAQ_OPT_QUEST_EARLY_META, 0 if args.no_early_meta else 1)
+    # and every dense call follows its own layer's append (or another layer's
+    # call), which writes no cache row but the appended one
+    g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, 0 if args.no_early_kv else 1)
     if args.quest_kernel == "queue":
         g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 2)
     stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused, kv=args.kv)
@@ -697,7 +703,8 @@ def run_ours(args, rank, world, local):
                  "f32 accumulate",
         "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl,
                                                                                        quest_kernel=args.quest_kernel, kv=args.kv,
-                                                                                       early_meta=not args.no_early_meta),
+                                                                                       early_meta=not args.no_early_meta,
+                                                                                       early_kv=not args.no_early_kv),
         "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
         "achieved_frac_of_peak": round(sb["total"] / s_per_step / 1e9 / peaks["hbm_gbs"], 4),
         "bytes_per_step": total_bytes,
@@ -740,6 +747,8 @@ def main(argv=None):
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
     ap.add_argument("--no-early-meta", action="store_true",
                     help="fused Quest kernel: read no metadata before the wait on the previous kernel")
+    ap.add_argument("--no-early-kv", action="store_true",
+                    help="dense attention: read no K/V tile before the wait on the previous kernel")
     ap.add_argument("--prefill", type=int, default=0,
                     help="time gqa_prefill_attn on a chunk of this many tokens per sequence and layer instead")
     ap.add_argument("--kv", choices=("f16", "e4m3", "int4"), default="f16",

@@ -45,6 +45,7 @@ GQAQ_OPT_QUEST_KERNEL = 6
 GQAQ_OPT_PREFILL_SPLITS = 7
 GQAQ_OPT_PREFILL_KERNEL = 8
 GQAQ_OPT_QUEST_EARLY_META = 9
+GQAQ_OPT_DENSE_EARLY_KV = 10
 
 PAGE_SIZE = 16
 

@@ -25,6 +25,7 @@ std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cluster_size{0};
 std::atomic<int64_t> g_opt_pdl{1};
 std::atomic<int64_t> g_opt_quest_early_meta{0};
+std::atomic<int64_t> g_opt_dense_early_kv{0};
 std::atomic<int64_t> g_opt_quest_kernel{0};
 std::atomic<int64_t> g_opt_prefill_splits{0};
 std::atomic<int64_t> g_opt_prefill_kernel{0};
@@ -80,6 +81,7 @@ int make_ctx(LaunchCtx *ctx, void *stream) {
     ctx->prefill_splits = (int)g_opt_prefill_splits.load();
     ctx->prefill_kernel = (int)g_opt_prefill_kernel.load();
     ctx->quest_early_meta = (int)g_opt_quest_early_meta.load();
+    ctx->dense_early_kv = (int)g_opt_dense_early_kv.load();
     ctx->status = s->status;
     return GQAQ_OK;
 }
@@ -215,6 +217,10 @@ int gqaq_set_option(int option, int64_t value) {
         case GQAQ_OPT_PREFILL_KERNEL:
             if (value < 0 || value > 2) return GQAQ_ERR_INVALID_ARG;
             g_opt_prefill_kernel.store(value);
+            return GQAQ_OK;
+        case GQAQ_OPT_DENSE_EARLY_KV:
+            if (value != 0 && value != 1) return GQAQ_ERR_INVALID_ARG;
+            g_opt_dense_early_kv.store(value);
             return GQAQ_OK;
         case GQAQ_OPT_QUEST_EARLY_META:
             if (value != 0 && value != 1) return GQAQ_ERR_INVALID_ARG;

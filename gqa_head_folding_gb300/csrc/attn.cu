@@ -85,6 +85,7 @@ struct AttnParams {
     float v_scale;     // E4M3 cache: V scale (1 otherwise)
     uint64_t timeout_ns;
     int test_stall;
+    int early_kv;      // dense: first K/V tiles issued before the grid dependency wait
 };
 
 // A unit segment of this CTA that was cut by a range boundary (at most the
@@ -284,7 +285,6 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
             prefetch_tensormap(&vsmap);
         }
     }
-    pdl_wait_and_release();
     TileRule rule;
     rule.sparse = SPARSE ? 1 : 0;
     rule.lmax = p.Lmax;
@@ -295,7 +295,32 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
     slots.init(p.S);
     rule.pages_per_tile = slots.ppt;
 
-    if (warp == C::NCW) {
+    // One dense tile (K and V, and INT4's scale rows) into stage s; lane 0 of the producer.
+    auto issue_dense = [&](int s, int unit, int row0, int local, uint64_t pol) {
+        const uint32_t kdst = smem_u32(stages + s * C::STAGE);
+        const uint32_t vdst = kdst + C::KBYTES;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
+        const int y = row0 + local * C::TILE;
+        if (KV4) {  // codes, then the tile's 128 scales (row = unit, x = first token)
+            constexpr int CODE4 = C::TILE * D / 2;
+            tma_load_2d(kdst, &kmap, 0, y, fb, pol);
+            tma_load_2d(kdst + CODE4, &ksmap, local * C::TILE, unit, fb, pol);
+            tma_load_2d(vdst, &vmap, 0, y, fb, pol);
+            tma_load_2d(vdst + CODE4, &vsmap, local * C::TILE, unit, fb, pol);
+        } else if (KV8) {
+            tma_load_2d(kdst, &kmap, 0, y, fb, pol);
+            tma_load_2d(vdst, &vmap, 0, y, fb, pol);
+        } else {
+#pragma unroll
+            for (int kh = 0; kh < C::KH; ++kh) {
+                tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
+                tma_load_2d(vdst + kh * C::KBLK, &vmap, 64 * kh, y, fb, pol);
+            }
+        }
+    };
+    // The producer warp's schedule: this CTA's slice of the tile order.
+    auto schedule = [&]() {
         // Balanced split of the T tiles over min(gridDim.x, ceil(T / 4)) CTAs:
         // every working CTA owns at least one tile, and a small problem keeps
         // about four per CTA (a short pipeline and few parts per split unit
@@ -330,7 +355,33 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
                 sched->unit_off = off_b + (int64_t)(rel / tiles_b) * tiles_b;
             }
         }
+    };
+    // Early K/V (early_kv): the schedule and the first ring-full of tiles of
+    // the first segment are issued before the grid dependency wait, so with a
+    // programmatic launch they stream while the previous kernel finishes. The
+    // caller guarantees that kernel writes neither valid_len nor any cache row
+    // but each sequence's last valid one; the tile holding that row (a unit's
+    // last) is left to the loop below. The loop skips the tiles issued here:
+    // the same tiles, stages and barrier phases.
+    const bool early = !SPARSE && p.early_kv != 0 && p.test_stall == 0;
+    int n_early = 0;
+    if (early && warp == C::NCW) {
+        schedule();
+        __syncwarp();  // lane 0's schedule is visible to the warp
+        if (lane == 0 && sched->t_begin < sched->t_end) {
+            Walk w0;
+            w0.init(*sched);
+            int lim = w0.seg_len();
+            lim = lim < C::NSTAGE ? lim : C::NSTAGE;
+            if (w0.local + lim > w0.tiles_b - 1) lim = w0.tiles_b - 1 - w0.local;  // not the unit's last tile
+            const uint64_t pol0 = l2_policy_evict_first();
+            const int unit = w0.b * p.Hkv + w0.kv;
+            for (int t = 0; t < lim; ++t) issue_dense(t, unit, unit * p.Lmax, w0.local + t, pol0);
+            n_early = lim > 0 ? lim : 0;
+        }
     }
+    pdl_wait_and_release();
+    if (!early && warp == C::NCW) schedule();
     __syncthreads();
 
     if (warp < C::NCW) {
@@ -399,25 +450,8 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
                         }
                     }
                 } else {
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
-                        const int y = row0 + local * C::TILE;
-                        if (KV4) {  // codes, then the tile's 128 scales (row = unit, x = first token)
-                            constexpr int CODE4 = C::TILE * D / 2;
-                            tma_load_2d(kdst, &kmap, 0, y, fb, pol);
-                            tma_load_2d(kdst + CODE4, &ksmap, local * C::TILE, unit, fb, pol);
-                            tma_load_2d(vdst, &vmap, 0, y, fb, pol);
-                            tma_load_2d(vdst + CODE4, &vsmap, local * C::TILE, unit, fb, pol);
-                        } else if (KV8) {
-                            tma_load_2d(kdst, &kmap, 0, y, fb, pol);
-                            tma_load_2d(vdst, &vmap, 0, y, fb, pol);
-                        } else {
-#pragma unroll
-                            for (int kh = 0; kh < C::KH; ++kh) {
-                                tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
-                                tma_load_2d(vdst + kh * C::KBLK, &vmap, 64 * kh, y, fb, pol);
-                            }
-                        }
+                    if (lane == 0 && i >= n_early) {
+                        issue_dense(s, unit, row0, local, pol);
                     }
                 }
             }
@@ -670,6 +704,7 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
     p.v_scale = KV8 ? a.v_scale : 1.f;
     p.timeout_ns = ctx.timeout_ns;
     p.test_stall = ctx.test_stall;
+    p.early_kv = ctx.dense_early_kv;
     if (launch_kernel(attn_partial_kernel<D, G, SPARSE, KV>, dim3(grid), dim3(C::THREADS), C::SMEM, ctx, 0, kmap,
                       vmap, ksmap, vsmap, p) != cudaSuccess)
         return GQAQ_ERR_CUDA;

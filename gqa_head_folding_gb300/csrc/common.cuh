@@ -30,6 +30,7 @@ struct LaunchCtx {
     int prefill_splits;    // prefill context splits per item: 0 automatic, n forced
     int prefill_kernel;    // prefill kernel: 0 automatic (tensor memory), 1 tensor memory, 2 warp MMA
     int quest_early_meta;  // fused Quest kernel: first metadata tiles read before the grid dependency wait
+    int dense_early_kv;    // dense attention: first K/V tiles read before the grid dependency wait
     int *status;           // device status word
 };
 

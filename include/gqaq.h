@@ -321,7 +321,7 @@ enum {
     GQAQ_OPT_PREFILL_KERNEL = 8,  /* gqa_prefill_attn's kernel: 0 (default) or 1 = the
                                      tensor-memory (tcgen05) kernel; 2 = the warp-level
                                      MMA kernel */
-    GQAQ_OPT_QUEST_EARLY_META = 9 /* nonzero: quest_decode_attn's cluster kernel reads
+    GQAQ_OPT_QUEST_EARLY_META = 9, /* nonzero: quest_decode_attn's cluster kernel reads
                                      valid_len, pos and the first metadata tiles of its
                                      first (sequence, KV head) before it waits for the
                                      previous kernel in the stream (with GQAQ_OPT_PDL,
@@ -334,6 +334,16 @@ enum {
                                      previous step, satisfies it; quest_update_meta or
                                      a position update right before does not.
                                      Default 0. */
+    GQAQ_OPT_DENSE_EARLY_KV = 10  /* nonzero: the dense attention calls (fp16, E4M3 and
+                                     INT4 caches) read valid_len and start the first
+                                     K/V tiles of their first context slice before
+                                     they wait for the previous kernel in the stream.
+                                     The tile holding each sequence's last valid row
+                                     (the appended one) is read after the wait. The
+                                     caller guarantees that the previous kernel writes
+                                     neither valid_len nor any other row of the
+                                     caches, as an append of that token or another
+                                     layer's attention do. Default 0. */
 };
 GQAQ_API int gqaq_set_option(int option, int64_t value);
 

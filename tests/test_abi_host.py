@@ -182,6 +182,9 @@ def test_options(L):
     assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_KERNEL, 3) == g.GQAQ_ERR_INVALID_ARG
     for v in (1, 2, 0):
         assert L.gqaq_set_option(g.GQAQ_OPT_PREFILL_KERNEL, v) == g.GQAQ_OK
+    assert L.gqaq_set_option(g.GQAQ_OPT_DENSE_EARLY_KV, 2) == g.GQAQ_ERR_INVALID_ARG
+    for v in (1, 0):
+        assert L.gqaq_set_option(g.GQAQ_OPT_DENSE_EARLY_KV, v) == g.GQAQ_OK
     assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_EARLY_META, 2) == g.GQAQ_ERR_INVALID_ARG
     assert L.gqaq_set_option(g.GQAQ_OPT_QUEST_EARLY_META, -1) == g.GQAQ_ERR_INVALID_ARG
     for v in (1, 0):

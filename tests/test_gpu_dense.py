@@ -26,6 +26,7 @@ DEV = "cuda:0"
 def _reset_options():
     yield
     g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
+    g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, 0)
 
 
 def run_case(B, Hq, Hkv, D, Lmax, valid, seed, max_ctas=0):
@@ -170,3 +171,46 @@ def test_dense_repeatable_and_graph_capturable():
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, first)
+
+
+@pytest.mark.parametrize("D,max_ctas", [(64, 0), (64, 3), (128, 0), (128, 5)])
+def test_dense_early_kv_decode_loop(D, max_ctas):
+    """GQAQ_OPT_DENSE_EARLY_KV: two layers, three decode steps of append then
+    dense attention, every launch right behind the previous one (programmatic
+    launch), as a decode loop does. Lengths cross tile boundaries (the appended
+    row opens a new tile, or is a sequence's only tile); forced small grids cut
+    units across CTAs. Each output is checked against the oracle replaying the
+    appends."""
+    g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, 1)
+    g.set_option(g.GQAQ_OPT_MAX_CTAS, max_ctas)
+    B, Hkv, G, Lmax, nl, nsteps, S = 3, 2, 4, 700, 2, 3, 16
+    w = workloads.Workload(0, "case", batch=B, num_layers=nl, num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                           head_dim=D, max_len=Lmax)
+    xs = [workloads.make_layer(w, l, device="cpu", seed=70 + D + l) for l in range(nl)]
+    gen = torch.Generator().manual_seed(80 + D + max_ctas)
+    knew = torch.randn(nsteps, nl, B, Hkv, D, generator=gen).to(torch.float16)
+    vnew = torch.randn(nsteps, nl, B, Hkv, D, generator=gen).to(torch.float16)
+    vls = [np.array([127, 300, 511]) + s for s in range(nsteps)]
+    vld = [torch.tensor(v, dtype=torch.int32, device=DEV) for v in vls]       # made before the loop:
+    posd = [torch.tensor(v - 1, dtype=torch.int32, device=DEV) for v in vls]  # no kernel writes them in it
+    kd = [x["k_cache"].to(DEV) for x in xs]
+    vd = [x["v_cache"].to(DEV) for x in xs]
+    qd = [x["q"].to(DEV) for x in xs]
+    metas = [g.new_meta(B, Hkv, Lmax, D, DEV) for _ in range(nl)]
+    kn, vn = knew.to(DEV), vnew.to(DEV)
+    outs = torch.empty(nsteps, nl, B, G * Hkv, D, dtype=torch.float16, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+    torch.cuda.synchronize()
+    for s in range(nsteps):
+        for l in range(nl):
+            g.quest_append_kv(kd[l], vd[l], metas[l], kn[s, l], vn[s, l], posd[s], S)
+            g.gqa_decode_attn(qd[l], kd[l], vd[l], vld[s], scale, out=outs[s, l])
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    for l in range(nl):
+        kc = xs[l]["k_cache"].numpy().copy(); vc = xs[l]["v_cache"].numpy().copy()
+        for s in range(nsteps):
+            for b in range(B):
+                kc[b, :, vls[s][b] - 1] = knew[s, l, b].numpy(); vc[b, :, vls[s][b] - 1] = vnew[s, l, b].numpy()
+            ref = oracle.attn_repeat_kv(xs[l]["q"].numpy(), kc, vc, list(vls[s]), scale)
+            assert_attn_close(outs[s, l], ref, f"step {s} layer {l}")

@@ -27,6 +27,7 @@ DEV = "cuda:0"
 def _reset_options():
     yield
     g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
+    g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, 0)
 
 
 def e4m3_case(B, Hq, Hkv, D, Lmax, seed):
@@ -138,8 +139,10 @@ def test_e4m3_append_bad_position_flags_and_skips():
     assert int(kd[0, :, 3].ne(56).sum()) == 0 and int(kd[1].count_nonzero()) == 0
 
 
-def test_e4m3_append_then_attend_matches_oracle():
+@pytest.mark.parametrize("early", [0, 1])
+def test_e4m3_append_then_attend_matches_oracle(early):
     """A decode step over the 8-bit cache: append the token, attend over it."""
+    g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, early)  # the append is the previous kernel: early reads allowed
     B, Hkv, G, D, Lmax = 2, 2, 4, 128, 300
     x, kc, vc, ks, vs = e4m3_case(B, Hkv * G, Hkv, D, Lmax, seed=21)
     vl = np.array([Lmax, 150])

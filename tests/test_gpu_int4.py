@@ -28,6 +28,7 @@ DEV = "cuda:0"
 def _reset_options():
     yield
     g.set_option(g.GQAQ_OPT_MAX_CTAS, 0)
+    g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, 0)
 
 
 def int4_case(B, Hq, Hkv, D, Lmax, seed):
@@ -154,7 +155,9 @@ def test_int4_append_bad_position_flags_and_skips():
     assert int(kd[1].count_nonzero()) == 0 and int(ks[1].count_nonzero()) == 0
 
 
-def test_int4_append_then_attend_matches_oracle():
+@pytest.mark.parametrize("early", [0, 1])
+def test_int4_append_then_attend_matches_oracle(early):
+    g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, early)  # the append is the previous kernel: early reads allowed
     B, Hkv, G, D, Lmax = 2, 2, 4, 128, 300
     x, kc, ks, vc, vs = int4_case(B, Hkv * G, Hkv, D, Lmax, seed=21)
     vl = np.array([Lmax, 150])
