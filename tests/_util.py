@@ -1,7 +1,7 @@
 """Shared helpers for the GPU parity tests: tolerances and comparisons against
 the fp64 oracle. The oracle never sees anything the CUDA library produced
 except the page set it is asked to verify (the sparse attention output is
-judged over the selection the GPU made, once that selection has been checked
+evaluated over the selection the GPU made, once that selection has been checked
 against the oracle's own top-K)."""
 import numpy as np
 import torch
