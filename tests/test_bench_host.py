@@ -95,3 +95,20 @@ def test_max_over_ranks_gloo_world_size_2():
 def test_single_rank_needs_no_collective():
     assert bench.max_over_ranks(0.25, None) == 0.25
     bench.barrier(None)
+
+
+def test_dense_side_and_early_read_flags():
+    """--dense runs a Quest workload's caches all dense; the launch string names
+    the early reads only for the calls that make them."""
+    import argparse
+    ns = argparse.Namespace(workload=5, batch=16, k_pages=0, layers=0, page_size=0, budget=0, dense=True)
+    w = bench.workload_from_args(ns)
+    assert w.k_pages is None and w.batch == 16 and w.max_len == 131072
+    c = bench.config_of(w, 1, early_meta=True, early_kv=True)
+    assert c["dense_layers"] == 1 and c["k_pages"] is None
+    assert "dense: first K/V tiles" in c["launch"] and "Quest:" not in c["launch"]
+    w3 = workloads.WORKLOADS[3]
+    c3 = bench.config_of(w3, 1, early_meta=True, early_kv=True)
+    assert "Quest: first metadata tiles" in c3["launch"] and "dense: first K/V tiles" in c3["launch"]
+    assert bench.config_of(w3, 1)["launch"] == "programmatic dependent launch"
+    assert bench.config_of(w3, 1, pdl=False)["launch"] == "plain stream order"
