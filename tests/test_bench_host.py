@@ -112,3 +112,16 @@ def test_dense_side_and_early_read_flags():
     assert "Quest: first metadata tiles" in c3["launch"] and "dense: first K/V tiles" in c3["launch"]
     assert bench.config_of(w3, 1)["launch"] == "programmatic dependent launch"
     assert bench.config_of(w3, 1, pdl=False)["launch"] == "plain stream order"
+
+
+def test_captured_traffic_is_near_the_bytes_model():
+    """The stored ncu DRAM bytes of the Llama-2-shaped launches sit just above the
+    bytes model (nothing read twice), so the bench's `traffic` is a real cross-check."""
+    w = workloads.WORKLOADS[3]
+    full = [w.max_len]
+    quest = bench.roofline_unit_bytes(w, "quest", full)
+    dense = bench.roofline_unit_bytes(w, "dense", full)
+    assert 1.0 < bench.NCU_TRAFFIC[(3, 1, "quest", "f16", 16)] / quest < 1.02
+    assert 1.0 < bench.NCU_TRAFFIC[(3, 1, "dense", "f16", 16)] / dense < 1.02
+    pf = bench.prefill_bytes(w.with_(batch=1), [w.max_len - 128], 128)
+    assert 1.0 < bench.PREFILL_TRAFFIC[(3, 1, 128)] / pf < 1.03
