@@ -24,7 +24,8 @@
 // fragments pair two tokens' codes with a byte permute before decoding.
 // INT4 caches (KV4): rows of D/2 bytes (channel 2i in the low nibble of byte
 // i) plus one fp32 scale per token row. Nibbles decode exactly to fp16 (the
-// 1024 + n bit trick, minus 1032); the K scale multiplies the token's fp32
+// 1024 + n bit trick, minus 1032; the high nibble of a byte in place, as
+// 1024 + 16 n, then one fma), one shift per word; the K scale multiplies the token's fp32
 // score and the V scale its probability, so both contractions run on the
 // integer levels. The channel order is permuted as for E4M3.
 #pragma once
@@ -73,11 +74,20 @@ __device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t y, uint32_t s
     return r;
 }
 
-// Four nibbles at bit offsets s and s + 16 of w -> fp16x2 of (nibble - 8), exact.
-__device__ __forceinline__ uint32_t nib2_to_f16x2(uint32_t w, int s) {
+// The nibbles at bits 0 and 16 of x -> fp16x2 of (nibble - 8), exact: OR-ing a
+// nibble n into the mantissa of 1024.0 gives 1024 + n, less 1032.
+__device__ __forceinline__ uint32_t nib2_lo_f16x2(uint32_t x) {
     uint32_t t, r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(w >> s), "r"(0x000F000Fu), "r"(0x64006400u));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(x), "r"(0x000F000Fu), "r"(0x64006400u));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64086408u));  // - (1024 + 8)
+    return r;
+}
+// The nibbles at bits 4 and 20 of x, without a shift: in place they give
+// 1024 + 16 n, and (1024 + 16 n) / 16 - 72 = n - 8 is one exact fma.
+__device__ __forceinline__ uint32_t nib2_hi_f16x2(uint32_t x) {
+    uint32_t t, r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(x), "r"(0x00F000F0u), "r"(0x64006400u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x2C002C00u), "r"(0xD480D480u));  // x/16 - 72
     return r;
 }
 
@@ -171,11 +181,12 @@ struct MmaAttn {
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
                 const int e = 2 * (j & 1);
+                const uint32_t xa = wa[j >> 1] >> (4 * e), xb = wb[j >> 1] >> (4 * e);  // nibble pairs at bits 4e, 4e + 4
                 uint32_t a[4];
-                a[0] = nib2_to_f16x2(wa[j >> 1], 4 * e);
-                a[1] = nib2_to_f16x2(wb[j >> 1], 4 * e);
-                a[2] = nib2_to_f16x2(wa[j >> 1], 4 * e + 4);
-                a[3] = nib2_to_f16x2(wb[j >> 1], 4 * e + 4);
+                a[0] = nib2_lo_f16x2(xa);
+                a[1] = nib2_lo_f16x2(xb);
+                a[2] = nib2_hi_f16x2(xa);
+                a[3] = nib2_hi_f16x2(xb);
                 mma_16816(s, a, qb[j][0], qb[j][1]);
             }
             const float ks0 = __uint_as_float(lds32(kbase + (uint32_t)(CODE4 + (row0 + r) * 4)));
@@ -245,11 +256,12 @@ struct MmaAttn {
                 const int sh = 4 * (k & 3);
                 const uint32_t lo = byte_perm(w[0][wd], w[1][wd], sel);  // tokens 2c | 2c+1
                 const uint32_t hi = byte_perm(w[2][wd], w[3][wd], sel);  // tokens 2c+8 | 2c+9
+                const uint32_t xl = lo >> sh, xh = hi >> sh;  // channel k at bits 0 / 16, k + 1 at 4 / 20
                 uint32_t a[4];
-                a[0] = nib2_to_f16x2(lo, sh);
-                a[1] = nib2_to_f16x2(lo, sh + 4);
-                a[2] = nib2_to_f16x2(hi, sh);
-                a[3] = nib2_to_f16x2(hi, sh + 4);
+                a[0] = nib2_lo_f16x2(xl);
+                a[1] = nib2_hi_f16x2(xl);
+                a[2] = nib2_lo_f16x2(xh);
+                a[3] = nib2_hi_f16x2(xh);
                 if (partial) mask_tokens(a, mk0, mk1);
                 mma_16816(o[i], a, pb0, pb1);
             }
