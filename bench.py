@@ -270,7 +270,7 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
 # is taken again.
 NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_695_872, (3, 1, "dense", "f16", 16): 539_982_848,
                (2, 32, "dense", "f16", 16): 180_035_584, (2, 32, "dense", "e4m3", 16): 90_877_440,
-               (2, 32, "dense", "int4", 16): 49_935_104}
+               (2, 32, "dense", "int4", 16): 49_938_432}
 # The same for one prefill launch (one layer), keyed by (workload id, batch, chunk length).
 PREFILL_TRAFFIC = {(3, 1, 128): 547_805_184}
 
