@@ -1,7 +1,10 @@
 // kv_lowbit.cu -- appends to the 8-bit (E4M3) and 4-bit (INT4) KV caches.
 //
-// The Quest review names the cache update path and lower-precision (fp8 /
-// 4-bit) KV caches as the next steps. Each append turns the new token's fp16
+// Neither source page defines a low-bit KV cache. The OPT post's section 5
+// ("KV Cache Update Operations Remain") names the cache-write path as the
+// next target; the Quest review states that its 4-bit figure is weight
+// quantization, not KV storage. The two formats here are this library's own
+// plainest choices. Each append turns the new token's fp16
 // k and v rows into the cache format at row pos[b] of every KV head:
 //  - E4M3: codes RNE-satfinite(fp32(x) * inv_scale), one scale per tensor;
 //  - INT4: per row scale = amax / 7, levels clamp(rne(x / scale), -7, 7)

@@ -15,7 +15,9 @@
 // not use the array's name as a device address. On the host that name is
 // only a stand-in symbol. Its device address is looked up with
 // cudaGetSymbolAddress once per device, with that device current, the first
-// time this entry point runs on it.
+// time this entry point runs on it, and kept for the life of the process: the
+// library must not be used on a device after cudaDeviceReset (which unloads
+// the module and frees the array).
 #include <mutex>
 
 #include "internal.h"
@@ -63,8 +65,9 @@ extern "C" GQAQ_API int gqa_decode_attn_noalloc(const gqaq_dims *dims, const gqa
     void *scratch = nullptr;
     const int rc = gqaq::static_scratch(&scratch);
     if (rc != GQAQ_OK) return rc;
-    const size_t need = gqaq_workspace_bytes(dims, 0);
-    if (need > gqaq::kStaticScratchBytes) return GQAQ_ERR_WORKSPACE;  // shape needs more than 1 MiB
+    // gqa_decode_attn computes this shape's exact scratch need (its grid after
+    // the per-shape cap) and returns GQAQ_ERR_WORKSPACE, launching nothing,
+    // when the 1 MiB array is too small.
     return gqa_decode_attn(dims, q, k_cache, v_cache, valid_len, scale, out, scratch,
                            gqaq::kStaticScratchBytes, stream);
 }

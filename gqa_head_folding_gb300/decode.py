@@ -53,6 +53,27 @@ class Layer:
     v_scale: float = 1.0
     k_scales: Optional[torch.Tensor] = None  # INT4 caches: [B,Hkv,Lmax] fp32 per-token scales
     v_scales: Optional[torch.Tensor] = None
+    page_idx: Optional[torch.Tensor] = None  # [B,Hkv,K] int32: when set, Quest layers also write their page lists
+
+
+def layer_plan(layer: int, k_pages: Optional[int], dense_layers: int, fused: bool, append: bool):
+    """Names of the library calls layer ``layer`` makes in one step, in order.
+
+    Layers below ``dense_layers`` (or every layer when ``k_pages`` is None) are
+    dense: "append" (when the step carries a token) then "dense". Later layers
+    run Quest: one "quest" call (the fused step, which appends itself) or,
+    unfused, "append", "score", "topk", "sparse"."""
+    dense = k_pages is None or layer < dense_layers
+    calls = []
+    if append and (dense or not fused):
+        calls.append("append")
+    if dense:
+        calls.append("dense")
+    elif fused:
+        calls.append("quest")
+    else:
+        calls += ["score", "topk", "sparse"]
+    return tuple(calls)
 
 
 class DecodeStack:
@@ -77,7 +98,7 @@ class DecodeStack:
                          if k_pages else None)
 
     def is_dense(self, layer: int) -> bool:
-        return self.k_pages is None or layer < self.dense_layers
+        return "dense" in layer_plan(layer, self.k_pages, self.dense_layers, self.fused, False)
 
     def new_meta(self) -> torch.Tensor:
         return new_meta(self.batch, self.num_kv_heads, self.max_len, self.head_dim, self.device,
@@ -106,32 +127,41 @@ class DecodeStack:
             gqa_decode_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.scale, out=L.out,
                             workspace=self.workspace)
 
+    def calls(self, layer: int, L: Layer):
+        """The library calls of one layer in launch order, as (family, thunk) pairs."""
+        out = []
+        for name in layer_plan(layer, self.k_pages, self.dense_layers, self.fused, L.k_new is not None):
+            out.append((name, self._thunk(name, L)))
+        return out
+
+    def _thunk(self, name: str, L: Layer):
+        if name == "append":
+            return lambda: self.append(L)
+        if name == "dense":
+            return lambda: self.dense(L)
+        if name == "quest":
+            return lambda: quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages,
+                                             self.scale, k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out,
+                                             page_idx=L.page_idx, page_size=self.page_size,
+                                             workspace=self.workspace)
+        if name == "score":
+            return lambda: quest_score_pages(L.q, L.meta, L.valid_len, self.max_len, scores=self.scores,
+                                             page_size=self.page_size)
+        idx = self.page_idx if L.page_idx is None else L.page_idx
+        if name == "topk":
+            return lambda: quest_topk_pages(self.scores, L.valid_len, self.k_pages, self.max_len, page_idx=idx,
+                                            page_size=self.page_size)
+        if name == "sparse":
+            return lambda: quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, idx, self.scale, out=L.out,
+                                             workspace=self.workspace, page_size=self.page_size)
+        raise ValueError(name)
+
     def families(self, layers: List[Layer]):
         """The library calls of one step, grouped by kind: name -> list of thunks."""
         fam = {}
-
-        def add(name, fn):
-            fam.setdefault(name, []).append(fn)
-
         for i, L in enumerate(layers):
-            dense = self.is_dense(i)
-            if L.k_new is not None and (dense or not self.fused):
-                add("append", lambda L=L: self.append(L))
-            if dense:
-                add("dense", lambda L=L: self.dense(L))
-            elif self.fused:
-                add("quest", lambda L=L: quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len,
-                                                           self.k_pages, self.scale, k_new=L.k_new, v_new=L.v_new,
-                                                           pos=L.pos, out=L.out, page_size=self.page_size,
-                                                           workspace=self.workspace))
-            else:
-                add("score", lambda L=L: quest_score_pages(L.q, L.meta, L.valid_len, self.max_len,
-                                                           scores=self.scores, page_size=self.page_size))
-                add("topk", lambda L=L: quest_topk_pages(self.scores, L.valid_len, self.k_pages, self.max_len,
-                                                         page_idx=self.page_idx, page_size=self.page_size))
-                add("sparse", lambda L=L: quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.page_idx,
-                                                            self.scale, out=L.out, workspace=self.workspace,
-                                                            page_size=self.page_size))
+            for name, fn in self.calls(i, L):
+                fam.setdefault(name, []).append(fn)
         return fam
 
     @staticmethod
@@ -144,19 +174,5 @@ class DecodeStack:
 
     def step(self, layers: List[Layer]):
         for i, L in enumerate(layers):
-            dense = self.is_dense(i)
-            if L.k_new is not None and (dense or not self.fused):
-                self.append(L)
-            if dense:
-                self.dense(L)
-            elif self.fused:
-                quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages, self.scale,
-                                  k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out, page_size=self.page_size,
-                                  workspace=self.workspace)
-            else:
-                quest_score_pages(L.q, L.meta, L.valid_len, self.max_len, scores=self.scores,
-                                  page_size=self.page_size)
-                quest_topk_pages(self.scores, L.valid_len, self.k_pages, self.max_len,
-                                 page_idx=self.page_idx, page_size=self.page_size)
-                quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, self.page_idx, self.scale,
-                                  out=L.out, workspace=self.workspace, page_size=self.page_size)
+            for _, fn in self.calls(i, L):
+                fn()

@@ -209,10 +209,14 @@ GQAQ_API int quest_decode_attn(const gqaq_dims *dims, const gqaq_half *q, gqaq_h
  * holds that array until the process exits.
  * Arguments, layouts and results are those of gqa_decode_attn, without the
  * workspace. Returns GQAQ_ERR_WORKSPACE, launching nothing, when the shape needs
- * more scratch than 1 MiB. That happens for G = 8 with D = 128 on a 152-SM
- * GB300, for example (gqaq_workspace_bytes reports the need).
+ * more scratch than 1 MiB: the split partials of gqa_decode_attn's grid for
+ * this shape (at most one CTA per four 128-token tiles) plus its counters. At
+ * G = 8 and D = 128 (8,320 bytes per CTA) that happens from about 500 tiles
+ * of (sequence, KV head, 128 tokens) on a 152-SM GB300.
  * The first call on each device looks up the array's device address with that
- * device current. Make that first call before any stream capture.
+ * device current and keeps it for the life of the process. Make that first
+ * call before any stream capture, and do not use the library on a device
+ * after cudaDeviceReset.
  * All calls share the one array. It is zero-filled when the library loads,
  * as the workspace contract asks, and every call leaves it so. Calls that
  * overlap on the GPU race on it. It allocates nothing. */
@@ -220,10 +224,13 @@ GQAQ_API int gqa_decode_attn_noalloc(const gqaq_dims *dims, const gqaq_half *q, 
                                      const gqaq_half *v_cache, const int32_t *valid_len, float scale,
                                      gqaq_half *out, void *stream);
 
-/* Human-readable name of a gqaq_status value (static string). */
-/* The 8-bit KV-cache variant ([QUEST] names lower-precision KV caches, after
- * the cache update path, as the next step; the pages fix no format, so this
- * is the plainest one). k_cache / v_cache are [B][Hkv][Lmax][D] bytes of
+/* Low-bit KV caches. The pages define no low-bit KV format: [OPT] section 5
+ * ("KV Cache Update Operations Remain") names the cache-write path as the next
+ * target, and [QUEST]'s section on its 7.03x kernel and 2.23x decode figures
+ * states that its 4-bit condition is weight quantization, not a 4-bit KV
+ * store. The two formats below are this library's own plainest choices.
+ *
+ * The 8-bit KV-cache variant. k_cache / v_cache are [B][Hkv][Lmax][D] bytes of
  * E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
  * infinities, largest finite 448) with one fp32 scale per tensor: a key
  * channel's value is k_scale * value(code), likewise for values.
@@ -246,8 +253,8 @@ GQAQ_API int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_
                             const gqaq_half *v_new, const int32_t *pos, float k_inv_scale, float v_inv_scale,
                             void *stream);
 
-/* The 4-bit KV-cache variant (same [QUEST] "next steps"; the plainest
- * format that keeps both contractions exact on integer levels): symmetric
+/* The 4-bit KV-cache variant (a format chosen here, see above: the plainest
+ * one that keeps both contractions exact on integer levels): symmetric
  * INT4 with one fp32 scale per (token, KV head) row.
  *   k_codes, v_codes   [B][Hkv][Lmax][D/2] bytes: channel 2i of a row in the
  *                      low nibble of byte i, high nibble channel 2i+1; a
@@ -296,6 +303,7 @@ GQAQ_API int gqa_prefill_attn(const gqaq_dims *dims, int q_len, const gqaq_half 
                               const gqaq_half *v_cache, const int32_t *start, float scale, gqaq_half *out,
                               void *workspace, size_t workspace_bytes, void *stream);
 
+/* Human-readable name of a gqaq_status value (static string). */
 GQAQ_API const char *gqaq_status_string(int status);
 
 /* Library options (process-wide, read at launch time). */

@@ -53,7 +53,15 @@ double oracle_f16_to_f64(uint16_t h)
     return sign ? -v : v;
 }
 
-/* 8-bit floating point E4M3 (the fp8 KV-cache variant): 1 sign bit, 4
+/* Low-bit KV caches. Neither page defines one: the OPT post's section 5
+ * ("KV Cache Update Operations Remain") names the cache-write path as the
+ * next target, and the Quest review's section on the 7.03x kernel and 2.23x
+ * decode figures says its 4-bit condition is weight quantization, not a
+ * 4-bit KV store. Both formats below are this library's own plainest choices,
+ * written out here so the GPU variants have a definition to be checked
+ * against.
+ *
+ * 8-bit floating point E4M3 (the fp8 KV-cache variant): 1 sign bit, 4
  * exponent bits with bias 7, 3 mantissa bits; no infinities, and the codes
  * S.1111.111 are NaN. Normal codes are (8 + m) * 2^(e - 10), subnormal ones
  * (e = 0) m * 2^-9; the largest finite magnitude is 448. */
@@ -98,7 +106,7 @@ void oracle_f32_array_to_e4m3(const float *src, uint8_t *dst, int64_t n)
 }
 
 /* ------------------------------------------------------------------------ */
-/* 4-bit KV cache (reading of [QUEST]'s "next steps"): symmetric INT4 with  */
+/* 4-bit KV cache (a format chosen here, see above): symmetric INT4 with   */
 /* one fp32 scale per (token, head) row of D channels.                       */
 /*   scale = amax / 7            (fp32 division; amax = max |x| of the row)  */
 /*   q     = clamp(rne(x / scale), -7, 7)   (fp32 division, ties to even)    */
