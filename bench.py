@@ -19,6 +19,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -233,11 +234,16 @@ def int4_cache(x: torch.Tensor):
     return codes.contiguous(), scale.contiguous()
 
 
+def make_stack(w: workloads.Workload, device, fused: bool = True, kv: str = "f16"):
+    from gqa_head_folding_gb300.decode import DecodeStack
+    return DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
+                       w.dense_layers, device, w.page_size, fused=fused, kv=kv, num_layers=w.num_layers)
+
+
 def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool = True, kv: str = "f16"):
     import gqa_head_folding_gb300 as g
-    from gqa_head_folding_gb300.decode import DecodeStack, Layer
-    stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
-                        w.dense_layers, device, w.page_size, fused=fused, kv=kv, num_layers=w.num_layers)
+    from gqa_head_folding_gb300.decode import Layer
+    stack = make_stack(w, device, fused, kv)
     layers, lens = [], []
     for layer in range(w.num_layers):
         x = workloads.make_layer(w, layer, device=device,
@@ -262,6 +268,50 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
         lens.append([int(v) for v in x["valid_len"].cpu()])
     torch.cuda.synchronize(device)
     return stack, layers, lens
+
+
+def clone_layers(layers):
+    """An independent copy of a step's device state (same values, new memory)."""
+    out = []
+    for L in layers:
+        kw = {f.name: getattr(L, f.name) for f in dataclasses.fields(L)}
+        out.append(type(L)(**{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# L2 residency: a step whose distinct bytes are under 4x L2 is timed over
+# several independent copies of its state, replayed in rotation, so that the
+# bytes touched between two uses of one copy are at least 4x L2.
+# ---------------------------------------------------------------------------
+L2_FALLBACK_BYTES = 126 * 2 ** 20
+MAX_COPIES = 128
+
+
+def l2_bytes() -> int:
+    if torch.cuda.is_available():
+        n = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0) or 0)
+        if n > 0:
+            return n
+    return L2_FALLBACK_BYTES
+
+
+def rotation_copies(bytes_per_step: int, l2: int) -> int:
+    """Number of state copies n with n x bytes_per_step >= 4 x L2 (1 when one step already is)."""
+    if bytes_per_step >= 4 * l2:
+        return 1
+    return max(1, min(MAX_COPIES, -(-4 * l2 // max(1, bytes_per_step))))
+
+
+def l2_note(copies: int, bytes_per_step: int, l2: int) -> str:
+    """What the timing does about L2 (copies = 0: nothing, for a working set under 4x L2)."""
+    mb = bytes_per_step / 1e6
+    if copies == 0:
+        return f"per-step working set {mb:.1f} MB < 4x L2 ({l2 / 1e6:.1f} MB); no flush, no rotation"
+    if copies <= 1:
+        return f"per-step working set {mb:.1f} MB >= 4x L2 ({l2 / 1e6:.1f} MB); no flush, no rotation"
+    return (f"{copies} independent copies of the step's state replayed in rotation "
+            f"({copies} x {mb:.1f} MB >= 4x L2 of {l2 / 1e6:.1f} MB); no flush")
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from one ncu
@@ -289,104 +339,151 @@ def capture(fn, device):
     return graph
 
 
-def time_graph(graph, reps: int, device) -> float:
-    """Mean seconds per replay, CUDA events on the replay stream."""
+def time_rotation(graphs, reps: int, device) -> float:
+    """Mean seconds per replay over `reps` replays of the graphs in rotation,
+    CUDA events on the replay stream."""
     st = torch.cuda.current_stream(device)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(device)
     a.record(st)
-    for _ in range(reps):
-        graph.replay()
+    for i in range(reps):
+        graphs[i % len(graphs)].replay()
     b.record(st)
     b.synchronize()
     return a.elapsed_time(b) / 1e3 / reps
 
 
-def family_timings(stack, layers, w, device, reps: int) -> dict:
-    """Per-call time of each family of the step's calls, each replayed alone in a graph."""
+def family_timings(stack, copies, device, reps: int) -> dict:
+    """Per-call time of each family of the step's calls, each replayed alone in
+    a graph (one graph per state copy, replayed in rotation)."""
     out = {}
-    for name, fns in stack.families(layers).items():
-        graph = capture(lambda: [fn() for fn in fns], device)
-        for _ in range(2):
-            graph.replay()
-        out[name] = {"s_per_launch": time_graph(graph, reps, device) / len(fns), "launches": len(fns)}
-        del graph
+    for name in stack.families(copies[0]):
+        graphs, n = [], 0
+        for layers in copies:
+            fns = stack.families(layers)[name]
+            n = len(fns)
+            graphs.append(capture(lambda fns=fns: [fn() for fn in fns], device))
+        for gr in graphs:
+            gr.replay()
+        out[name] = {"s_per_launch": time_rotation(graphs, reps, device) / n, "launches": n}
+        del graphs
     return out
 
 
 # ---------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle on a bounded sample, scaled to one step
 # ---------------------------------------------------------------------------
-def oracle_step_seconds(w: workloads.Workload, layers, lens, budget_s: float = 15.0, kv: str = "f16") -> dict:
-    """Time the oracle per (sequence, KV head) unit on sampled units of one
-    dense and one Quest layer, and scale by the units of a whole step."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step_seconds(w: workloads.Workload, unit_source, lens, budget_s: float = 10.0, kv: str = "f16",
+                        threads: int = 0, sample_lens=None) -> dict:
+    """Time the fp64 oracle per (sequence, KV head) unit on sampled units of one
+    dense and one Quest layer, on one thread and on `threads` threads (0 = every
+    host core), and scale each per token to the whole step.
+
+    unit_source(layer, b, kv_head) returns that unit's numpy arrays: q [1,G,D],
+    k and v [1,1,Lmax,D] and, for a 4-bit cache, their scale rows. The oracle's
+    C code runs outside the interpreter lock, so threads over units use every
+    core. Half the budget goes to each of the two timings. lens[layer][b] are
+    the step's valid lengths; sample_lens (default lens) those of the sampled
+    units when they were drawn apart from the step's state."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
-    S, G = w.page_size, w.group
-    kv_dtype = kv
+    S = w.page_size
     scale = 1.0 / math.sqrt(w.head_dim)
+    threads = threads or host_cores()
 
-    def unit_arrays(L, b, kv):
-        q = L.q[b, kv * G:(kv + 1) * G].unsqueeze(0).cpu().numpy()
-        k = L.k_cache[b, kv].unsqueeze(0).unsqueeze(0).cpu().numpy()
-        v = L.v_cache[b, kv].unsqueeze(0).unsqueeze(0).cpu().numpy()
-        return q, k, v
-
-    def dense_unit(L, b, kv, length):
-        q, k, v = unit_arrays(L, b, kv)
-        t0 = time.perf_counter()
-        if kv_dtype == "e4m3":
-            oracle.attn_e4m3(q, k, v, L.k_scale, L.v_scale, [length], scale)
-        elif kv_dtype == "int4":
-            oracle.attn_int4(q, k, L.k_scales[b, kv][None, None].cpu().numpy(), v,
-                             L.v_scales[b, kv][None, None].cpu().numpy(), [length], scale)
-        else:
-            oracle.attn_repeat_kv(q, k, v, [length], scale)
-        return time.perf_counter() - t0
-
-    def quest_unit(L, b, kv, length):
-        q, k, v = unit_arrays(L, b, kv)
-        meta = oracle.page_minmax(k, [length], S)          # prefill state, not timed
-        t0 = time.perf_counter()
-        if w.append:                                        # the appended token's page
+    def run_unit(kind, u, length):
+        if kind == "dense":
+            if kv == "e4m3":
+                oracle.attn_e4m3(u["q"], u["k"], u["v"], u["k_scale"], u["v_scale"], [length], scale)
+            elif kv == "int4":
+                oracle.attn_int4(u["q"], u["k"], u["k_scales"], u["v"], u["v_scales"], [length], scale)
+            else:
+                oracle.attn_repeat_kv(u["q"], u["k"], u["v"], [length], scale)
+            return
+        sc = oracle.page_scores(u["q"], u["meta"], [length], S)
+        if w.append:                                        # the appended token's page, rebuilt and rescored
             p = (length - 1) // S
-            rows = k[:, :, p * S:length]
-            meta[:, :, p] = oracle.page_minmax(rows, [rows.shape[2]], S)[:, :, 0]
-        sc = oracle.page_scores(q, meta, [length], S)
+            rows = u["k"][:, :, p * S:length]
+            page = oracle.page_minmax(rows, [rows.shape[2]], S)[:, :, :1]
+            sc[:, :, p] = oracle.page_scores(u["q"], page, [rows.shape[2]], S)[:, :, 0]
         idx = oracle.topk_pages(sc, [length], S, w.k_pages)
-        oracle.sparse_attn(q, k, v, [length], idx, S, scale)
-        return time.perf_counter() - t0
+        oracle.sparse_attn(u["q"], u["k"], u["v"], [length], idx, S, scale)
 
-    dense_layers = [i for i in range(w.num_layers) if w.layer_is_dense(i)]
-    quest_layers = [i for i in range(w.num_layers) if not w.layer_is_dense(i)]
-    units = [(b, kv) for b in range(w.batch) for kv in range(w.num_kv_heads)]
-    rng = np.random.default_rng(0)
-    order = [units[i] for i in rng.permutation(len(units))]
-    per_layer = {}
-    spent = 0.0
-    sampled = {"dense": 0, "quest": 0}
-    for kind, lyr in (("dense", dense_layers), ("quest", quest_layers)):
-        if not lyr:
-            continue
-        li = lyr[0]
-        times = []
-        for (b, kv) in order:
-            fn = dense_unit if kind == "dense" else quest_unit
-            times.append(fn(layers[li], b, kv, lens[li][b]) / max(1, lens[li][b]))  # seconds per token
-            spent += times[-1] * lens[li][b]
-            if spent > budget_s / 2 and len(times) >= 1:
-                break
-        sampled[kind] = len(times)
-        per_layer[kind] = statistics.mean(times)
-    est = 0.0
-    for i in range(w.num_layers):
-        kind = "dense" if w.layer_is_dense(i) else "quest"
-        est += per_layer[kind] * w.num_kv_heads * sum(lens[i])
-    return {"seconds_per_step": est, "sampled_units": sampled,
-            "sample": f"fp64 oracle on {sampled['dense']} dense and {sampled['quest']} Quest (sequence, KV head) "
-                      f"units of one layer each, scaled per token to all {w.num_layers} layers x "
-                      f"{w.batch * w.num_kv_heads} units"}
+    kinds = []
+    for kind in ("dense", "quest"):
+        ids = [i for i in range(w.num_layers) if w.layer_is_dense(i) == (kind == "dense")]
+        if ids:
+            kinds.append((kind, ids[0]))
+    sample_lens = lens if sample_lens is None else sample_lens
+    nb = min(w.batch, len(sample_lens[0]))
+    units = [(b, h) for b in range(nb) for h in range(w.num_kv_heads)]
+    order = [units[i] for i in np.random.default_rng(0).permutation(len(units))]
+    per_tok_1, per_tok_n, sampled = {}, {}, {}
+    for kind, li in kinds:
+        pool = []                                           # distinct units, arrays extracted up front
+        for (b, h) in order[:max(1, min(len(order), threads))]:
+            u = unit_source(li, b, h)
+            if kind == "quest":
+                u["meta"] = oracle.page_minmax(u["k"], [sample_lens[li][b]], S)   # prefill state, not timed
+            pool.append((u, sample_lens[li][b]))
+        # one thread
+        t_spent, toks, n1 = 0.0, 0, 0
+        while n1 < 1 or (t_spent < budget_s / (2 * len(kinds)) and n1 < 4 * len(pool)):
+            u, length = pool[n1 % len(pool)]
+            t0 = time.perf_counter()
+            run_unit(kind, u, length)
+            t_spent += time.perf_counter() - t0
+            toks += length
+            n1 += 1
+        per_tok_1[kind] = t_spent / toks
+        per_unit = t_spent / n1
+        # every core: enough jobs to keep each thread busy for its share of the budget
+        n_jobs = max(threads, int(budget_s / (2 * len(kinds)) * threads / max(per_unit, 1e-6)))
+        n_jobs = min(n_jobs, 64 * threads)
+        jobs = [pool[i % len(pool)] for i in range(n_jobs)]
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(lambda j: run_unit(kind, j[0], j[1]), jobs))
+            wall = time.perf_counter() - t0
+        per_tok_n[kind] = wall / sum(j[1] for j in jobs)
+        sampled[kind] = {"layer": li, "distinct_units": len(pool), "one_thread_units": n1, "all_core_units": n_jobs}
+
+    def extrapolate(per_tok):
+        return sum(per_tok["dense" if w.layer_is_dense(i) else "quest"] * w.num_kv_heads * sum(lens[i])
+                   for i in range(w.num_layers))
+
+    desc = ", ".join(f"{k}: {v['one_thread_units']} units on 1 thread and {v['all_core_units']} on {threads} "
+                     f"threads, drawn from {v['distinct_units']} (sequence, KV head) units of layer {v['layer']}"
+                     for k, v in sampled.items())
+    return {"one_thread_s": extrapolate(per_tok_1), "all_cores_s": extrapolate(per_tok_n), "threads": threads,
+            "sampled": sampled, "extrapolated": True,
+            "sample": f"fp64 oracle ({desc}); time per token scaled to all {w.num_layers} layers x "
+                      f"{w.batch * w.num_kv_heads} units of the step"}
+
+
+def device_unit_source(layers, kv: str):
+    """Units of the device state, copied to the host (outside any timing)."""
+    def src(li, b, h):
+        L = layers[li]
+        G = L.q.shape[1] // L.k_cache.shape[1]
+        u = {"q": L.q[b, h * G:(h + 1) * G].unsqueeze(0).cpu().numpy(),
+             "k": L.k_cache[b, h][None, None].cpu().numpy(), "v": L.v_cache[b, h][None, None].cpu().numpy(),
+             "k_scale": L.k_scale, "v_scale": L.v_scale}
+        if kv == "int4":
+            u["k_scales"] = L.k_scales[b, h][None, None].cpu().numpy()
+            u["v_scales"] = L.v_scales[b, h][None, None].cpu().numpy()
+        return u
+    return src
 
 
 # ---------------------------------------------------------------------------
@@ -413,7 +510,7 @@ def workload_from_args(args) -> workloads.Workload:
 
 def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool = True,
               quest_kernel: str = "cluster", kv: str = "f16", early_meta: bool = False,
-              early_kv: bool = False) -> dict:
+              early_kv: bool = False, l2: str = "") -> dict:
     return {"workload": f"{w.name} (config {w.id})", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
             "layers": w.num_layers, "dense_layers": w.num_layers if w.k_pages is None else w.dense_layers,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
@@ -430,35 +527,75 @@ def config_of(w: workloads.Workload, world: int, fused: bool = True, pdl: bool =
                          if early_kv and (w.k_pages is None or w.dense_layers > 0) else ""),
             "kv_cache": {"e4m3": "e4m3 codes, per-tensor fp32 scales",
                          "int4": "int4 levels, per-token fp32 scales"}.get(kv, "f16"),
-            "l2": "per-step working set > 4x L2; no flush"}
+            "l2": l2}
+
+
+def arm_config(args, w: workloads.Workload, world: int) -> dict:
+    """The config dict both arms print for this command line."""
+    lens = [[int(v) for v in workloads.valid_lengths(w, i)] for i in range(w.num_layers)]
+    nbytes = step_bytes(w, lens, fused=not args.unfused, kv=args.kv)["total"]
+    l2 = l2_bytes()
+    return config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl, quest_kernel=args.quest_kernel,
+                     kv=args.kv, early_meta=not args.no_early_meta, early_kv=not args.no_early_kv,
+                     l2=l2_note(rotation_copies(nbytes, l2), nbytes, l2))
 
 
 def run_reference(args, rank, world):
-    """The fp64 CPU oracle as it stands, on the host cores, on this workload."""
+    """The fp64 CPU oracle as it stands, on the host cores, on this workload.
+
+    Inputs are drawn on the host (the same seeded recipe, a host generator) for
+    the sampled sequences of one dense and one Quest layer; the page metadata
+    comes from the oracle's own min/max. Nothing here loads the CUDA library."""
     if rank != 0:
         return
     w = workload_from_args(args)
-    device = torch.device("cuda:0") if torch.cuda.is_available() else None
-    if device is None:
-        print(json.dumps({"impl": "reference", "unavailable": "inputs are drawn on the GPU; no CUDA device"}))
-        return
-    import gqa_head_folding_gb300 as g  # noqa: F401  (prefill metadata on the device)
-    stack, layers, lens = build_state(w, device, kv=args.kv)
-    per_step = []
+    lens = [[int(v) for v in workloads.valid_lengths(w, i)] for i in range(w.num_layers)]
+    w_host = w.with_(batch=min(w.batch, 2))              # sampled sequences only
+    drawn = {}
+
+    def unit_source(li, b, h):
+        if li not in drawn:
+            x = workloads.make_layer(w_host, li, device="cpu")
+            if args.kv == "e4m3":
+                x["k_cache"], x["k_scale"] = e4m3_cache(x["k_cache"])
+                x["v_cache"], x["v_scale"] = e4m3_cache(x["v_cache"])
+            elif args.kv == "int4":
+                x["k_cache"], x["k_scales"] = int4_cache(x["k_cache"])
+                x["v_cache"], x["v_scales"] = int4_cache(x["v_cache"])
+            drawn[li] = x
+        x = drawn[li]
+        G = w.group
+        u = {"q": x["q"][b, h * G:(h + 1) * G].unsqueeze(0).numpy(), "k": x["k_cache"][b, h][None, None].numpy(),
+             "v": x["v_cache"][b, h][None, None].numpy(), "k_scale": x.get("k_scale", 1.0),
+             "v_scale": x.get("v_scale", 1.0)}
+        if args.kv == "int4":
+            u["k_scales"] = x["k_scales"][b, h][None, None].numpy()
+            u["v_scales"] = x["v_scales"][b, h][None, None].numpy()
+        return u
+
+    host_lens = [[int(v) for v in workloads.valid_lengths(w_host, i)] for i in range(w.num_layers)]
+    per_step, one = [], []
+    r = None
     for i in range(args.warmup + args.steps):
-        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget, kv=args.kv)
+        r = oracle_step_seconds(w, unit_source, lens, budget_s=args.ref_budget, kv=args.kv, sample_lens=host_lens)
         if i >= args.warmup:
-            per_step.append(r["seconds_per_step"])
+            per_step.append(r["all_cores_s"])
+            one.append(r["one_thread_s"])
     value = statistics.mean(per_step) * 1e6
     sb = step_bytes(w, lens, kv=args.kv)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, 1, kv=args.kv),
-            "achieved_gbs": sb["total"] / (value / 1e6) / 1e9,
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": r["sample"]},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (host-drawn, same recipe)",
+            "config": arm_config(args, w, 1),
+            "achieved_gbs": round(sb["total"] / (value / 1e6) / 1e9, 3),
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": r["threads"], "kind": "oracle",
+                             "sample": r["sample"], "extrapolated": True, "sampled": r["sampled"],
+                             "one_thread": {"value": round(statistics.mean(one) * 1e6, 1), "unit": UNIT, "cores": 1}},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+NOMINAL_HBM_GBS = 7900.0     # GB300 HBM3e, nominal
 
 
 def load_peaks() -> dict:
@@ -555,6 +692,7 @@ def run_prefill(args, rank, world, local):
     peaks = load_peaks()
     flops = sum(prefill_flops(w, s, Q) for s in starts)
     per_launch_flops = prefill_flops(w, starts[0], Q)
+    per_launch_bytes = prefill_bytes(w, starts[0], Q)
     achieved = flops / s_per_step / 1e12
     cpu = None
     if not args.no_cpu_baseline:
@@ -577,7 +715,9 @@ def run_prefill(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 in/out, f32 accumulate",
         "data": "synthetic (seeded N(0,1) fp16 q and caches)",
-        "config": dict(config_of(w, world, pdl=not args.no_pdl), q_len=Q,
+        "config": dict(config_of(w, world, pdl=not args.no_pdl,
+                                 l2=l2_note(1 if per_launch_bytes >= 4 * l2_bytes() else 0, per_launch_bytes,
+                                            l2_bytes())), q_len=Q,
                        chunk="last q_len tokens of each sequence's valid length"),
         "achieved_tflops": round(achieved, 1),
         "roofline": {"bound": "tensor", "kernel": "gqa_prefill_attn", "achieved": round(achieved, 1),
@@ -596,6 +736,121 @@ def run_prefill(args, rank, world, local):
     print(json.dumps(line))
 
 
+FAMILY_KERNEL = {"dense": "gqa_decode_attn", "score": "quest_score_pages", "sparse": "quest_sparse_attn",
+                 "quest": "quest_decode_attn"}
+
+
+def measure(w: workloads.Workload, stack, copies, lens, device, steps: int, warmup: int, kv: str = "f16",
+            fused: bool = True, dist=None, soak: float = 0.0, sampler=None, reps: int = 50) -> dict:
+    """Time `steps` graph replays of one full step (state copies in rotation),
+    then each call family alone; return the step time and the roofline of the
+    dominant family."""
+    sb = step_bytes(w, lens, fused=fused, kv=kv)
+    graphs = [capture(lambda ls=ls: stack.step(ls), device) for ls in copies]
+    for i in range(max(3, warmup)):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize(device)
+    if sampler is not None:
+        sampler.start()
+    t_soak = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_soak < soak:
+        for _ in range(8):
+            graphs[i % len(graphs)].replay()
+            i += 1
+        torch.cuda.synchronize(device)
+    # timed region: exactly `steps` steps
+    st = torch.cuda.current_stream(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    ev0.record(st)
+    for i in range(steps):
+        graphs[i % len(graphs)].replay()
+    ev1.record(st)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    clocks = sampler.stop() if sampler is not None else None
+    s_per_step = max_over_ranks(ev0.elapsed_time(ev1) / 1e3 / steps, dist, device)
+    del graphs
+
+    fam = family_timings(stack, copies, device, reps=max(3, min(reps, steps)))
+    per_step_fam = {k: v["s_per_launch"] * sb["launches"][k] for k, v in fam.items()}
+    dominant = max(per_step_fam, key=per_step_fam.get)
+    peaks = load_peaks()
+    roof = None
+    if dominant in FAMILY_KERNEL:
+        layer_of = next(i for i in range(w.num_layers)
+                        if (stack.is_dense(i) if dominant == "dense" else not stack.is_dense(i)))
+        per_launch = roofline_unit_bytes(w, dominant, lens[layer_of], kv=kv)
+        achieved = per_launch / fam[dominant]["s_per_launch"] / 1e9
+        roof = {"bound": "hbm", "kernel": FAMILY_KERNEL[dominant],
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy bandwidth",
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS,
+                "traffic": NCU_TRAFFIC.get((w.id, w.batch, dominant, kv, w.page_size)),
+                "bytes_per_launch": per_launch, "us_per_launch": round(fam[dominant]["s_per_launch"] * 1e6, 2)}
+    return {"s_per_step": s_per_step, "bytes": sb, "fam": fam, "per_step_fam": per_step_fam, "roofline": roof,
+            "clocks": clocks, "peaks": peaks}
+
+
+# Other workloads measured in the same process for the `by_config` object of the
+# default line: (label, workload id, overrides, variants on the same caches).
+# A variant is a k_pages value, or None for every layer dense.
+BY_CONFIG = [
+    ("config 1: EXAONE shape, 1 dense layer, batch 1", 1, {}, ["as-is"]),
+    ("config 2: EXAONE shape, 30 dense layers, batch 1", 2, {"batch": 1}, ["as-is"]),
+    ("config 2: EXAONE shape, 30 dense layers, batch 32", 2, {"batch": 32}, ["as-is"]),
+    ("config 4: GQA Quest 64K, K=256, batch 1", 4, {"batch": 1}, ["as-is", None]),
+    ("config 4: GQA Quest 64K, K=256, batch 4", 4, {"batch": 4}, ["as-is"]),
+    ("config 4: GQA Quest 64K, K=256, batch 8", 4, {"batch": 8}, ["as-is", None]),
+    ("config 5: 128K, batch 1", 5, {"batch": 1}, [128, 512, None]),
+    ("config 5: 128K, batch 16", 5, {"batch": 16}, [128, 512, None]),
+]
+
+
+def run_by_config(args, device) -> dict:
+    """Each BY_CONFIG workload: state built once, its variants timed on the same caches."""
+    out = {"entries": [], "steps": args.by_config_steps, "warmup": 3}
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    t0 = time.perf_counter()
+    l2 = l2_bytes()
+    for label, wid, over, variants in BY_CONFIG:
+        base = workloads.WORKLOADS[wid].with_(**over)
+        stack0, layers, lens = build_state(base, device)
+        del stack0
+        nbytes_min = min(step_bytes(base if v == "as-is" else base.with_(k_pages=v), lens)["total"] for v in variants)
+        n = rotation_copies(nbytes_min, l2)
+        copies = [layers] + [clone_layers(layers) for _ in range(n - 1)]
+        for v in variants:
+            w = base if v == "as-is" else base.with_(k_pages=v)
+            stack = make_stack(w, device)
+            m = measure(w, stack, copies, lens, device, args.by_config_steps, 3)
+            nb = m["bytes"]["total"]
+            e = {"label": label + ("" if v == "as-is" else (", all dense" if v is None else f", K={v}")),
+                 "workload": w.name, "config_id": w.id, "batch": w.batch, "layers": w.num_layers,
+                 "k_pages": w.k_pages, "us_per_step": round(m["s_per_step"] * 1e6, 2), "bytes_per_step": nb,
+                 "gbs_step": round(nb / m["s_per_step"] / 1e9, 1),
+                 "frac_step": round(nb / m["s_per_step"] / 1e9 / m["peaks"]["hbm_gbs"], 4),
+                 "us_per_launch_by_family": {k: round(f["s_per_launch"] * 1e6, 2) for k, f in m["fam"].items()},
+                 "l2": l2_note(n, nb, l2)}
+            if m["roofline"]:
+                r = m["roofline"]
+                e["dominant"] = {"kernel": r["kernel"], "us_per_launch": r["us_per_launch"],
+                                 "bytes_per_launch": r["bytes_per_launch"], "achieved_gbs": r["achieved"],
+                                 "frac": r["frac"], "frac_of_nominal": r["frac_of_nominal"],
+                                 "traffic": r["traffic"]}
+            out["entries"].append(e)
+            del stack
+        del copies, layers
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+    out["clocks"] = sampler.stop()
+    out["seconds"] = round(time.perf_counter() - t0, 1)
+    return out
+
+
 def run_ours(args, rank, world, local):
     import gqa_head_folding_gb300 as g
     device = torch.device(f"cuda:{local}")
@@ -612,88 +867,62 @@ def run_ours(args, rank, world, local):
     g.set_option(g.GQAQ_OPT_DENSE_EARLY_KV, 0 if args.no_early_kv else 1)
     if args.quest_kernel == "queue":
         g.set_option(g.GQAQ_OPT_QUEST_KERNEL, 2)
-    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=not args.unfused, kv=args.kv)
-    sb = step_bytes(w, lens, fused=not args.unfused, kv=args.kv)
-    step = lambda: stack.step(layers)  # noqa: E731
-    graph = capture(step, device)
+    fused = not args.unfused
+    stack, layers, lens = build_state(w, device, seed_offset=rank_seed(rank), fused=fused, kv=args.kv)
+    l2 = l2_bytes()
+    nbytes = step_bytes(w, lens, fused=fused, kv=args.kv)["total"]
+    n_copies = rotation_copies(nbytes, l2)
+    copies = [layers] + [clone_layers(layers) for _ in range(n_copies - 1)]
+    m = measure(w, stack, copies, lens, device, args.steps, args.warmup, kv=args.kv, fused=fused, dist=dist,
+                soak=args.soak, sampler=ClockSampler(local))
+    s_per_step, sb = m["s_per_step"], m["bytes"]
 
-    # warm-up, then a short soak so the clock sampler sees the GPU under load
-    for _ in range(max(3, args.warmup)):
-        graph.replay()
-    torch.cuda.synchronize(device)
-    sampler = ClockSampler(local)
-    sampler.start()
-    t_soak = time.perf_counter()
-    while time.perf_counter() - t_soak < args.soak:
-        for _ in range(8):
-            graph.replay()
-        torch.cuda.synchronize(device)
-
-    # timed region: exactly K steps
-    st = torch.cuda.current_stream(device)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize(device)
-    ev0.record(st)
-    for _ in range(args.steps):
-        graph.replay()
-    ev1.record(st)
-    torch.cuda.synchronize(device)
-    barrier(dist)
-    clocks = sampler.stop()
-    elapsed = ev0.elapsed_time(ev1) / 1e3
-    elapsed = max_over_ranks(elapsed, dist, device)
-    s_per_step = elapsed / args.steps
-
-    # per-family timings for the roofline of the dominant kernel
-    fam = family_timings(stack, layers, w, device, reps=max(3, min(50, args.steps)))
-    per_step_fam = {k: v["s_per_launch"] * sb["launches"][k] for k, v in fam.items()}
-    dominant = max(per_step_fam, key=per_step_fam.get)
-    peaks = load_peaks()
-    roof = None
-    if dominant in ("dense", "score", "sparse", "quest"):
-        layer_of = next(i for i in range(w.num_layers)
-                        if (stack.is_dense(i) if dominant == "dense" else not stack.is_dense(i)))
-        per_launch = roofline_unit_bytes(w, dominant, lens[layer_of], kv=args.kv)
-        achieved = per_launch / fam[dominant]["s_per_launch"] / 1e9
-        roof = {"bound": "hbm", "kernel": {"dense": "gqa_decode_attn", "score": "quest_score_pages",
-                                           "sparse": "quest_sparse_attn", "quest": "quest_decode_attn"}[dominant],
-                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                "traffic": NCU_TRAFFIC.get((w.id, w.batch, dominant, args.kv, w.page_size)), "bytes_per_launch": per_launch,
-                "us_per_launch": round(fam[dominant]["s_per_launch"] * 1e6, 2)}
-
-    # end to end through the public API: host inputs in, host outputs out
-    h2d = [(L.q, torch.empty(L.q.shape, dtype=L.q.dtype, pin_memory=True)) for L in layers]
-    if w.append:
-        h2d += [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for L in layers for t in (L.k_new, L.v_new)]
-    for dst, src in h2d:
-        src.copy_(dst.cpu())
-    d2h = [(L.out, torch.empty(L.out.shape, dtype=L.out.dtype, pin_memory=True)) for L in layers]
-    h2d_bytes = sum(s.numel() * s.element_size() for _, s in h2d)
-    d2h_bytes = sum(d.numel() * d.element_size() for _, d in d2h)
+    # end to end through the public API: host inputs in, host outputs out, every step
+    graphs = [capture(lambda ls=ls: stack.step(ls), device) for ls in copies]
+    xfers = []
+    for ls in copies:
+        h2d = [(L.q, torch.empty(L.q.shape, dtype=L.q.dtype, pin_memory=True)) for L in ls]
+        if w.append:
+            h2d += [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for L in ls for t in (L.k_new, L.v_new)]
+        for dst, src in h2d:
+            src.copy_(dst.cpu())
+        d2h = [(L.out, torch.empty(L.out.shape, dtype=L.out.dtype, pin_memory=True)) for L in ls]
+        xfers.append((h2d, d2h))
+    h2d_bytes = sum(s.numel() * s.element_size() for _, s in xfers[0][0])
+    d2h_bytes = sum(d.numel() * d.element_size() for _, d in xfers[0][1])
     e2e_steps = max(3, args.steps)
     torch.cuda.synchronize(device)
     barrier(dist)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    for i in range(e2e_steps):
+        h2d, d2h = xfers[i % len(xfers)]
         for dst, src in h2d:
             dst.copy_(src, non_blocking=True)
-        graph.replay()
+        graphs[i % len(graphs)].replay()
         for src, dst in d2h:
             dst.copy_(src, non_blocking=True)
         torch.cuda.synchronize(device)
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dist, device)
     barrier(dist)
+    del graphs
+    assert g.device_status() == 0, "the step raised a device status flag"
 
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline:
-        r = oracle_step_seconds(w, layers, lens, budget_s=args.ref_budget, kv=args.kv)
-        cpu = {"value": r["seconds_per_step"] * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": r["sample"]}
+        r = oracle_step_seconds(w, device_unit_source(layers, args.kv), lens, budget_s=args.cpu_budget, kv=args.kv)
+        cpu = {"value": round(r["all_cores_s"] * 1e6, 1), "unit": UNIT, "cores": r["threads"], "kind": "oracle",
+               "sample": r["sample"], "extrapolated": True, "sampled": r["sampled"],
+               "one_thread": {"value": round(r["one_thread_s"] * 1e6, 1), "unit": UNIT, "cores": 1}}
     launches = stack.launches_per_step(layers)
+    del copies, layers, stack
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    by_config = None
+    if world == 1 and args.by_config:
+        by_config = run_by_config(args, device)
+    peaks = m["peaks"]
     total_bytes = sb["total"] * world
     line = {
         "metric": METRIC, "value": round(s_per_step * 1e6, 2), "unit": UNIT, "n_gpus": world,
@@ -701,24 +930,26 @@ def run_ours(args, rank, world, local):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 in/out, " + ({"e4m3": "e4m3 KV cache, ", "int4": "int4 KV cache, "}.get(args.kv, "")) +
                  "f32 accumulate",
-        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)", "config": config_of(w, world, fused=not args.unfused, pdl=not args.no_pdl,
-                                                                                       quest_kernel=args.quest_kernel, kv=args.kv,
-                                                                                       early_meta=not args.no_early_meta,
-                                                                                       early_kv=not args.no_early_kv),
+        "data": "synthetic (seeded N(0,1) fp16 caches, planted pages)",
+        "config": arm_config(args, w, world),
         "achieved_gbs": round(total_bytes / s_per_step / 1e9, 1),
         "achieved_frac_of_peak": round(sb["total"] / s_per_step / 1e9 / peaks["hbm_gbs"], 4),
+        "achieved_frac_of_nominal": round(sb["total"] / s_per_step / 1e9 / NOMINAL_HBM_GBS, 4),
         "bytes_per_step": total_bytes,
         "bytes_by_family": sb["bytes"],
-        "us_per_launch_by_family": {k: round(v["s_per_launch"] * 1e6, 2) for k, v in fam.items()},
-        "us_per_step_by_family": {k: round(v * 1e6, 2) for k, v in per_step_fam.items()},
-        "roofline": roof,
+        "us_per_launch_by_family": {k: round(v["s_per_launch"] * 1e6, 2) for k, v in m["fam"].items()},
+        "us_per_step_by_family": {k: round(v * 1e6, 2) for k, v in m["per_step_fam"].items()},
+        "timing": "mean over the timed steps (CUDA events around all of them)",
+        "roofline": m["roofline"],
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_s * 1e6, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes},
         "gpu_launches": launches * args.steps,
         "gpu_launches_per_step": launches,
-        "clocks": clocks,
+        "clocks": m["clocks"],
     }
+    if by_config is not None:
+        line["by_config"] = by_config
     print(json.dumps(line))
 
 
@@ -739,8 +970,14 @@ def main(argv=None):
     ap.add_argument("--budget", type=int, default=0,
                     help="Quest token budget; sets k_pages = budget / S (page-size sweep at a fixed budget)")
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed replays before timing")
-    ap.add_argument("--ref-budget", type=float, default=6.0, help="seconds of oracle work per sample")
+    ap.add_argument("--ref-budget", type=float, default=3.0,
+                    help="seconds of oracle work per step of --impl reference")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--by-config", dest="by_config", action="store_true", default=None,
+                    help="also time the other workloads in the same process (default: on for the default workload)")
+    ap.add_argument("--no-by-config", dest="by_config", action="store_false")
+    ap.add_argument("--by-config-steps", type=int, default=50)
     ap.add_argument("--unfused", action="store_true", help="run Quest layers as the step-by-step calls")
     ap.add_argument("--quest-kernel", choices=("queue", "cluster"), default="cluster",
                     help="fused Quest kernel: one cluster per unit (default) or the GPU-wide work queue")
@@ -755,6 +992,8 @@ def main(argv=None):
                     help="KV-cache format; e4m3 (8-bit codes, per-tensor scales) and int4 (4-bit levels, per-token "
                          "scales) run all-dense stacks only")
     args = ap.parse_args(argv)
+    if args.by_config is None:
+        args.by_config = default_command(args)
     if args.kv != "f16":
         w = workload_from_args(args)
         if any(not w.layer_is_dense(i) for i in range(w.num_layers)):
@@ -766,6 +1005,13 @@ def main(argv=None):
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)
+
+
+def default_command(args) -> bool:
+    """True when the command line picks the default workload with no overrides."""
+    return (args.workload == 3 and not (args.batch or args.k_pages or args.layers or args.page_size or args.budget
+                                        or args.dense or args.unfused or args.prefill or args.kv != "f16"
+                                        or args.quest_kernel != "cluster"))
 
 
 if __name__ == "__main__":

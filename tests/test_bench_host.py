@@ -125,3 +125,51 @@ def test_captured_traffic_is_near_the_bytes_model():
     assert 1.0 < bench.NCU_TRAFFIC[(3, 1, "dense", "f16", 16)] / dense < 1.02
     pf = bench.prefill_bytes(w.with_(batch=1), [w.max_len - 128], 128)
     assert 1.0 < bench.PREFILL_TRAFFIC[(3, 1, 128)] / pf < 1.03
+
+
+def test_rotation_covers_four_times_l2():
+    l2 = 126 * 2 ** 20
+    for nbytes in (8 * 2 ** 20, 32 * 2 ** 20, 157_000_000, 4 * l2 - 1):
+        n = bench.rotation_copies(nbytes, l2)
+        assert n > 1 and n * nbytes >= 4 * l2 and (n - 1) * nbytes < 4 * l2
+        assert "rotation" in bench.l2_note(n, nbytes, l2)
+    assert bench.rotation_copies(4 * l2, l2) == 1
+    assert bench.rotation_copies(3_087_007_744, l2) == 1
+    assert "no rotation" in bench.l2_note(1, 3_087_007_744, l2)
+    assert "< 4x L2" in bench.l2_note(0, 8 * 2 ** 20, l2)
+
+
+def test_default_command_turns_on_by_config_only_for_the_default_workload():
+    import argparse
+    base = dict(workload=3, batch=0, k_pages=0, layers=0, page_size=0, budget=0, dense=False, unfused=False,
+                prefill=0, kv="f16", quest_kernel="cluster")
+    assert bench.default_command(argparse.Namespace(**base))
+    for k, v in (("workload", 4), ("batch", 2), ("dense", True), ("kv", "e4m3"), ("prefill", 128)):
+        assert not bench.default_command(argparse.Namespace(**dict(base, **{k: v})))
+
+
+def test_reference_arm_never_loads_the_cuda_library():
+    """--impl reference times the oracle on host-drawn inputs: the product
+    package is never imported, and its config equals the GPU arm's."""
+    import subprocess
+    import sys
+    code = ("import sys, json, io, contextlib, bench\n"
+            "buf = io.StringIO()\n"
+            "with contextlib.redirect_stdout(buf):\n"
+            "    bench.main(['--impl', 'reference', '--workload', '1', '--steps', '1', '--warmup', '0',"
+            " '--ref-budget', '0.3'])\n"
+            "line = json.loads(buf.getvalue().strip().splitlines()[-1])\n"
+            "assert not any(m.startswith('gqa_head_folding_gb300') for m in sys.modules), 'product imported'\n"
+            "print(json.dumps(line))\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "us/step" and line["value"] > 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["extrapolated"] and cb["cores"] >= 1 and cb["one_thread"]["cores"] == 1
+    assert line["e2e"] == {"value": line["value"], "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    import argparse
+    args = argparse.Namespace(workload=1, batch=0, k_pages=0, layers=0, page_size=0, budget=0, dense=False, unfused=False, kv="f16",
+              no_pdl=False, quest_kernel="cluster", no_early_meta=False, no_early_kv=False)
+    assert line["config"] == bench.arm_config(args, bench.workload_from_args(args), 1)
