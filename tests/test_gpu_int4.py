@@ -172,3 +172,65 @@ def test_int4_append_then_attend_matches_oracle(early):
         vc[b, :, vl[b] - 1], vs[b, :, vl[b] - 1] = oracle.quantize_int4(x["v_new"][b].numpy())
     assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(ksd.cpu().numpy(), ks)
     assert_attn_close(out, oracle.attn_int4(x["q"].numpy(), kc, ks, vc, vs, vl, 1.0 / math.sqrt(D)))
+
+
+def nibble_rows(D, shift=0):
+    """One code row whose channel c holds nibble (c + shift) mod 16, i.e. every
+    level -8 .. 7 (nibble - 8), channel 2i in the low nibble of byte i."""
+    nib = (np.arange(D) + shift) % 16
+    return (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8), nib.astype(np.float64) - 8.0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_every_level_decodes_exactly(D):
+    """Each of the 16 nibble values decodes to its level exactly, in V and in K.
+
+    V: with one valid token the output is that token's value row, level * scale;
+    the scale is a power of two, so every output is exact in fp16 and must
+    equal it bit for bit. K: query head (b, g) is one-hot on channel
+    c = b * 8 + g, so its score is a * level(k0[c]) * k_scale against a zero
+    second key, and the output over one-hot V rows is (sigmoid, 1 - sigmoid)
+    of it: adjacent levels move it by far more than the fp16 tolerance."""
+    G = 8
+    B = D // G                                    # one query head per channel
+    Lmax = 4
+    # V decode: one valid token per sequence, every level in every row
+    kc = np.zeros((B, 1, Lmax, D // 2), np.uint8)
+    vc = np.zeros((B, 1, Lmax, D // 2), np.uint8)
+    vlev = np.zeros((B, D))
+    for b in range(B):
+        vc[b, 0, 0], vlev[b] = nibble_rows(D, shift=b)
+    ks = np.full((B, 1, Lmax), 0.25, np.float32)
+    vs = np.full((B, 1, Lmax), 0.125, np.float32)
+    q = torch.randn(B, G, D, generator=torch.Generator().manual_seed(3)).to(torch.float16)
+    vl = torch.ones(B, dtype=torch.int32, device=DEV)
+    out = g.gqa_decode_attn_int4(q.to(DEV), dev(kc), dev(ks), dev(vc), dev(vs), vl, 0.125)
+    torch.cuda.synchronize()
+    want = torch.from_numpy(np.repeat((vlev * 0.125)[:, None, :], G, axis=1)).to(torch.float16)
+    assert torch.equal(out.cpu(), want), "V levels decode wrongly"
+
+    # K decode: token 0's key holds every level, token 1's key is all zero
+    # (nibble 8); V rows one-hot on channels 0 and 1 with level 1, scale 1
+    k0, klev = nibble_rows(D)
+    kc = np.zeros((B, 1, Lmax, D // 2), np.uint8)
+    kc[:, 0, 0] = k0
+    kc[:, 0, 1] = 0x88
+    vc = np.full((B, 1, Lmax, D // 2), 0x88, np.uint8)
+    vc[:, 0, 0, 0] = 0x89                         # channel 0 = level 1
+    vc[:, 0, 1, 0] = 0x98                         # channel 1 = level 1
+    vs = np.ones((B, 1, Lmax), np.float32)
+    a = 4.0                                       # score = a * level * 0.25 * 0.5 = level / 2
+    qn = np.zeros((B, G, D), np.float16)
+    for b in range(B):
+        for gg in range(G):
+            qn[b, gg, b * G + gg] = a
+    vl = torch.full((B,), 2, dtype=torch.int32, device=DEV)
+    out = g.gqa_decode_attn_int4(dev(qn.reshape(B, G, D)), dev(kc), dev(ks), dev(vc), dev(vs), vl, 0.5)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().reshape(B * G, D)
+    s = klev / 2.0                                # channel c's score against the zero key
+    p0 = 1.0 / (1.0 + np.exp(-s))
+    assert np.abs(got[:, 0] - p0).max() <= 2e-3 and np.abs(got[:, 1] - (1.0 - p0)).max() <= 2e-3, \
+        "K levels decode wrongly"
+    ref = oracle.attn_int4(qn.reshape(B, G, D), kc, ks, vc, vs, [2] * B, 0.5)
+    assert_attn_close(out, ref)
