@@ -74,6 +74,8 @@ def _load():
         lib.oracle_prefill_repeat_kv.restype = i32
         lib.oracle_page_minmax.argtypes = [i32, i32, i64, i64, i32, _dp, _dp]
         lib.oracle_page_minmax.restype = i32
+        lib.oracle_page_minmax_e4m3.argtypes = [i32, i32, i64, i64, i32, u8p, u8p]
+        lib.oracle_page_minmax_e4m3.restype = i32
         lib.oracle_page_scores.argtypes = [i32, i32, i32, i64, i64, _dp, _dp, _dp]
         lib.oracle_page_scores.restype = i32
         lib.oracle_topk_pages.argtypes = [i32, i64, i64, i32, _dp, _ip]
@@ -251,6 +253,24 @@ def page_minmax(k, valid_len, page_size):
         mb = np.full((Hkv, pmax, 2, D), np.nan, dtype=np.float64)
         _check(_load().oracle_page_minmax(Hkv, D, Lmax, int(valid_len[b]), page_size,
                                           _dptr(kb), _dptr(mb)), "page_minmax")
+        out[b] = mb
+    return out
+
+
+def page_minmax_e4m3(k_codes, valid_len, page_size):
+    """Per-page per-channel min/max of an E4M3 key cache, as E4M3 codes
+    [B,Hkv,Pmax,2,D] uint8 (compared by value; a zero bound is the code 0x00;
+    pages with no valid token hold 0x7F, the NaN code)."""
+    k = np.ascontiguousarray(np.asarray(k_codes, dtype=np.uint8))
+    B, Hkv, Lmax, D = k.shape
+    pmax = num_pages(Lmax, page_size)
+    out = np.full((B, Hkv, pmax, 2, D), 0x7F, dtype=np.uint8)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    for b in range(B):
+        kb = np.ascontiguousarray(k[b])
+        mb = np.ascontiguousarray(out[b])
+        _check(_load().oracle_page_minmax_e4m3(Hkv, D, Lmax, int(valid_len[b]), page_size,
+                                               kb.ctypes.data_as(u8p), mb.ctypes.data_as(u8p)), "page_minmax_e4m3")
         out[b] = mb
     return out
 

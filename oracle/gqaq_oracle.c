@@ -318,6 +318,50 @@ int oracle_page_minmax(int hkv, int d, int64_t lmax, int64_t l, int s,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Page min/max over an E4M3 key cache (the 8-bit variant above): the same  */
+/* per-page, per-channel minimum and maximum as oracle_page_minmax, of the  */
+/* keys' values, kept as E4M3 codes. With one positive scale per tensor the */
+/* dequantized bounds are scale * value(code). Values are compared after    */
+/* decoding; a zero bound is stored as the code 0x00 (+0), so each bound    */
+/* has exactly one code (E4M3 repeats no other value). Caches hold no NaN   */
+/* codes. Pages at or beyond P are left as they are.                        */
+/* ------------------------------------------------------------------------ */
+static uint8_t canonical_e4m3(uint8_t code)
+{
+    return (code & 0x7F) == 0 ? 0 : code;
+}
+
+int oracle_page_minmax_e4m3(int hkv, int d, int64_t lmax, int64_t l, int s,
+                            const uint8_t *k, uint8_t *meta)
+{
+    if (hkv <= 0 || d <= 0 || s <= 0 || l < 0 || l > lmax)
+        return -1;
+    int64_t pmax = (lmax + s - 1) / s;
+    int64_t pvalid = (l + s - 1) / s;
+    for (int kv = 0; kv < hkv; ++kv) {
+        for (int64_t p = 0; p < pvalid; ++p) {
+            int64_t t0 = p * s;
+            int64_t t1 = t0 + s < l ? t0 + s : l;
+            uint8_t *mn = meta + (((int64_t)kv * pmax + p) * 2 + 0) * d;
+            uint8_t *mx = meta + (((int64_t)kv * pmax + p) * 2 + 1) * d;
+            for (int i = 0; i < d; ++i) {
+                uint8_t clo = k[((int64_t)kv * lmax + t0) * d + i], chi = clo;
+                double lo = oracle_e4m3_to_f64(clo), hi = lo;
+                for (int64_t t = t0 + 1; t < t1; ++t) {
+                    uint8_t c = k[((int64_t)kv * lmax + t) * d + i];
+                    double x = oracle_e4m3_to_f64(c);
+                    if (x < lo) { lo = x; clo = c; }
+                    if (x > hi) { hi = x; chi = c; }
+                }
+                mn[i] = canonical_e4m3(clo);
+                mx[i] = canonical_e4m3(chi);
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* [QUEST] page score U(p,q) = sum_i max(q_i m_{p,i}, q_i M_{p,i}).  With    */
 /* grouped query heads, one page set serves a KV head's G query heads, so    */
 /* the KV head's score is the largest U over its G folded query rows.        */

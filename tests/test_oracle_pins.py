@@ -481,3 +481,85 @@ def test_attn_int4_matches_sdpa_on_dequantized_cache():
             qt[b][:, None, :], k[b, :, :L].repeat_interleave(G, dim=0), v[b, :, :L].repeat_interleave(G, dim=0),
             scale=0.125)[:, 0]
         assert np.allclose(got[b], ref.numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Page min/max over an E4M3 key cache: the page-score section's m and M of
+# the keys' values, kept as E4M3 codes (zero bound stored as +0)
+# ---------------------------------------------------------------------------
+def _torch_e4m3_values():
+    """Value of every code, decoded by torch's float8 type (independent of the oracle)."""
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _value_to_code(vals):
+    table = _torch_e4m3_values()
+    lut = {}
+    for c in range(256):
+        v = table[c]
+        if np.isnan(v):
+            continue
+        if v == 0.0:
+            lut[0.0] = 0
+        elif v not in lut:
+            lut[v] = c
+    return np.vectorize(lambda v: lut[float(v)], otypes=[np.uint8])(vals)
+
+
+def test_page_minmax_e4m3_brute_force_against_torch_decoding():
+    rng = np.random.default_rng(11)
+    finite = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    B, Hkv, Lmax, D, S = 2, 3, 16 * 5 + 7, 8, 16
+    codes = rng.choice(finite, size=(B, Hkv, Lmax, D)).astype(np.uint8)
+    valid = [Lmax, 16 * 2 + 3]
+    meta = oracle.page_minmax_e4m3(codes, valid, S)
+    vals = _torch_e4m3_values()[codes]
+    for b in range(B):
+        P = (valid[b] + S - 1) // S
+        for p in range(P):
+            rows = vals[b, :, p * S:min(p * S + S, valid[b])]
+            assert np.array_equal(meta[b, :, p, 0], _value_to_code(rows.min(axis=1)))
+            assert np.array_equal(meta[b, :, p, 1], _value_to_code(rows.max(axis=1)))
+        assert np.all(meta[b, :, P:] == 0x7F)          # pages with no valid token are left alone
+
+
+def test_page_minmax_e4m3_values_equal_fp64_page_minmax_of_dequantized_keys():
+    # scale * value(code) is the dequantized bound: the fp64 page min/max of
+    # the dequantized cache, exactly (scale > 0 keeps the order)
+    rng = np.random.default_rng(12)
+    x = rng.normal(size=(1, 2, 16 * 4 + 9, 64)).astype(np.float16)
+    scale = float(np.abs(x.astype(np.float32)).max()) / 448.0
+    codes = oracle.quantize_e4m3(x, 1.0 / scale)
+    valid = [16 * 4 + 9]
+    meta = oracle.page_minmax_e4m3(codes, valid, 16)
+    deq = oracle.e4m3_to_f64(codes) * scale
+    ref = oracle.page_minmax(deq, valid, 16)
+    assert np.array_equal(oracle.e4m3_to_f64(meta[:, :, :5]) * scale, ref[:, :, :5])
+
+
+def test_page_minmax_e4m3_zero_bounds_are_plus_zero():
+    codes = np.zeros((1, 1, 16, 4), np.uint8)
+    codes[0, 0, :, 0] = 0x80                            # all -0
+    codes[0, 0, ::2, 1] = 0x80                          # -0 and +0 mixed
+    codes[0, 0, :, 2] = 0x38                            # 1.0 everywhere
+    codes[0, 0, 3, 2] = 0x80                            # one -0: the min is zero
+    codes[0, 0, :, 3] = 0xB8                            # -1.0 everywhere
+    codes[0, 0, 5, 3] = 0x80                            # one -0: the max is zero
+    meta = oracle.page_minmax_e4m3(codes, [16], 16)[0, 0, 0]
+    assert meta[0].tolist() == [0x00, 0x00, 0x00, 0xB8]
+    assert meta[1].tolist() == [0x00, 0x00, 0x38, 0x00]
+
+
+def test_e4m3_page_bound_holds_for_every_key():
+    # q.k <= U(p, q) for every key of every page, U from the scaled E4M3 bounds
+    rng = np.random.default_rng(13)
+    x = rng.normal(size=(1, 2, 16 * 6, 32)).astype(np.float16)
+    codes = oracle.quantize_e4m3(x, 40.0)
+    scale = 1.0 / 40.0
+    meta = oracle.e4m3_to_f64(oracle.page_minmax_e4m3(codes, [96], 16)) * scale
+    q = rng.normal(size=(1, 2, 32)).astype(np.float16)
+    U = oracle.page_scores(q, meta, [96], 16)
+    k = oracle.e4m3_to_f64(codes) * scale
+    qk = np.einsum("hd,htd->ht", oracle.f16_to_f64(q[0]), k[0])
+    for p in range(6):
+        assert np.all(qk[:, p * 16:(p + 1) * 16] <= U[0, :, p][:, None] * (1 + 1e-12) + 1e-12)
