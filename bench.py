@@ -58,15 +58,16 @@ def dense_unit_bytes(head_dim: int, length: int, kv: str = "f16") -> int:
     return 2 * kv_vector_bytes(head_dim, kv) * length
 
 
-def meta_unit_bytes(head_dim: int, length: int, page_size: int) -> int:
-    """Min and max vectors of every page of one (sequence, KV head): 2 M ceil(L/S)."""
-    return 2 * kv_vector_bytes(head_dim) * ((length + page_size - 1) // page_size)
+def meta_unit_bytes(head_dim: int, length: int, page_size: int, kv: str = "f16") -> int:
+    """Min and max vectors of every page of one (sequence, KV head): 2 M ceil(L/S)
+    (E4M3 bounds: one code byte per channel)."""
+    return 2 * kv_vector_bytes(head_dim, kv) * ((length + page_size - 1) // page_size)
 
 
-def selected_unit_bytes(head_dim: int, length: int, page_size: int, k_pages: int) -> int:
+def selected_unit_bytes(head_dim: int, length: int, page_size: int, k_pages: int, kv: str = "f16") -> int:
     """Keys and values of the selected pages: 2 M S min(K, P)."""
     pages = (length + page_size - 1) // page_size
-    return 2 * kv_vector_bytes(head_dim) * page_size * min(k_pages, pages)
+    return 2 * kv_vector_bytes(head_dim, kv) * page_size * min(k_pages, pages)
 
 
 def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True, kv: str = "f16") -> dict:
@@ -86,8 +87,10 @@ def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True, kv: st
 
     qo = 2 * G * M                                   # q read + out write per unit
     app_unit = 2 * M + 2 * M + 4 * M                 # new k,v read, row write, page min/max read+write
-    if kv != "f16":                                  # new k,v read (fp16), low-bit rows written, no metadata
+    if kv != "f16":                                  # new k,v read (fp16), low-bit rows written
         app_unit = 2 * M + 2 * kv_vector_bytes(D, kv)
+        if kv == "e4m3" and w.append:                # and the page's E4M3 bounds read and written
+            app_unit += 4 * kv_vector_bytes(D, kv)
     for layer, lens in enumerate(lens_per_layer):
         dense = w.layer_is_dense(layer)
         if w.append and (dense or not fused):
@@ -100,17 +103,17 @@ def step_bytes(w: workloads.Workload, lens_per_layer, fused: bool = True, kv: st
         elif fused:
             count("quest")
             for L in lens:
-                add("quest", w.num_kv_heads * ((app_unit if w.append else 0) + meta_unit_bytes(D, L, S) +
-                                               selected_unit_bytes(D, L, S, w.k_pages) + qo))
+                add("quest", w.num_kv_heads * ((app_unit if w.append else 0) + meta_unit_bytes(D, L, S, kv) +
+                                               selected_unit_bytes(D, L, S, w.k_pages, kv) + qo))
         else:
             for name in ("score", "topk", "sparse"):
                 count(name)
             for L in lens:
                 P = (L + S - 1) // S
                 n = min(w.k_pages, P)
-                add("score", w.num_kv_heads * (meta_unit_bytes(D, L, S) + G * M + 4 * P))
+                add("score", w.num_kv_heads * (meta_unit_bytes(D, L, S, kv) + G * M + 4 * P))
                 add("topk", w.num_kv_heads * (4 * P + 4 * w.k_pages))
-                add("sparse", w.num_kv_heads * (selected_unit_bytes(D, L, S, w.k_pages) + 4 * n + qo))
+                add("sparse", w.num_kv_heads * (selected_unit_bytes(D, L, S, w.k_pages, kv) + 4 * n + qo))
     return {"bytes": fam, "launches": launches, "total": sum(fam.values())}
 
 
@@ -120,11 +123,11 @@ def roofline_unit_bytes(w: workloads.Workload, family: str, lens, kv: str = "f16
     if family == "dense":
         return sum(w.num_kv_heads * dense_unit_bytes(D, L, kv) for L in lens)
     if family == "score":
-        return sum(w.num_kv_heads * meta_unit_bytes(D, L, S) for L in lens)
+        return sum(w.num_kv_heads * meta_unit_bytes(D, L, S, kv) for L in lens)
     if family == "sparse":
-        return sum(w.num_kv_heads * selected_unit_bytes(D, L, S, w.k_pages) for L in lens)
+        return sum(w.num_kv_heads * selected_unit_bytes(D, L, S, w.k_pages, kv) for L in lens)
     if family == "quest":
-        return roofline_unit_bytes(w, "score", lens) + roofline_unit_bytes(w, "sparse", lens)
+        return roofline_unit_bytes(w, "score", lens, kv) + roofline_unit_bytes(w, "sparse", lens, kv)
     raise ValueError(family)
 
 
@@ -254,6 +257,10 @@ def build_state(w: workloads.Workload, device, seed_offset: int = 0, fused: bool
             L.k_cache, L.k_scale = e4m3_cache(x["k_cache"])
             L.v_cache, L.v_scale = e4m3_cache(x["v_cache"])
             del x["k_cache"], x["v_cache"]
+            if w.append or not w.layer_is_dense(layer):
+                L.meta = stack.new_meta()
+                prefill = x["valid_len"] - 1 if w.append else x["valid_len"]
+                g.quest_update_meta_e4m3(L.k_cache, prefill, L.meta, page_size=w.page_size)
         elif kv == "int4":
             L.k_cache, L.k_scales = int4_cache(x["k_cache"])
             L.v_cache, L.v_scales = int4_cache(x["v_cache"])
@@ -410,14 +417,23 @@ def oracle_step_seconds(w: workloads.Workload, unit_source, lens, budget_s: floa
             else:
                 oracle.attn_repeat_kv(u["q"], u["k"], u["v"], [length], scale)
             return
-        sc = oracle.page_scores(u["q"], u["meta"], [length], S)
+        e4 = kv == "e4m3"                                   # bounds and pages decoded, times the scales
+        bounds = oracle.e4m3_to_f64(u["meta"]) * u["k_scale"] if e4 else u["meta"]
+        sc = oracle.page_scores(u["q"], bounds, [length], S)
         if w.append:                                        # the appended token's page, rebuilt and rescored
             p = (length - 1) // S
             rows = u["k"][:, :, p * S:length]
-            page = oracle.page_minmax(rows, [rows.shape[2]], S)[:, :, :1]
+            if e4:
+                page = oracle.e4m3_to_f64(oracle.page_minmax_e4m3(rows, [rows.shape[2]], S)[:, :, :1]) * u["k_scale"]
+            else:
+                page = oracle.page_minmax(rows, [rows.shape[2]], S)[:, :, :1]
             sc[:, :, p] = oracle.page_scores(u["q"], page, [rows.shape[2]], S)[:, :, 0]
         idx = oracle.topk_pages(sc, [length], S, w.k_pages)
-        oracle.sparse_attn(u["q"], u["k"], u["v"], [length], idx, S, scale)
+        if e4:
+            oracle.sparse_attn(u["q"], oracle.e4m3_to_f64(u["k"]) * u["k_scale"],
+                               oracle.e4m3_to_f64(u["v"]) * u["v_scale"], [length], idx, S, scale)
+        else:
+            oracle.sparse_attn(u["q"], u["k"], u["v"], [length], idx, S, scale)
 
     kinds = []
     for kind in ("dense", "quest"):
@@ -433,8 +449,9 @@ def oracle_step_seconds(w: workloads.Workload, unit_source, lens, budget_s: floa
         pool = []                                           # distinct units, arrays extracted up front
         for (b, h) in order[:max(1, min(len(order), threads))]:
             u = unit_source(li, b, h)
-            if kind == "quest":
-                u["meta"] = oracle.page_minmax(u["k"], [sample_lens[li][b]], S)   # prefill state, not timed
+            if kind == "quest":                              # prefill state, not timed
+                u["meta"] = (oracle.page_minmax_e4m3 if kv == "e4m3" else oracle.page_minmax)(
+                    u["k"], [sample_lens[li][b]], S)
             pool.append((u, sample_lens[li][b]))
         # one thread
         t_spent, toks, n1 = 0.0, 0, 0
@@ -784,7 +801,7 @@ def measure(w: workloads.Workload, stack, copies, lens, device, steps: int, warm
                         if (stack.is_dense(i) if dominant == "dense" else not stack.is_dense(i)))
         per_launch = roofline_unit_bytes(w, dominant, lens[layer_of], kv=kv)
         achieved = per_launch / fam[dominant]["s_per_launch"] / 1e9
-        roof = {"bound": "hbm", "kernel": FAMILY_KERNEL[dominant],
+        roof = {"bound": "hbm", "kernel": FAMILY_KERNEL[dominant] + ("" if kv == "f16" else "_" + kv),
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy bandwidth",
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS,
@@ -806,6 +823,7 @@ BY_CONFIG = [
     ("config 4: GQA Quest 64K, K=256, batch 8", 4, {"batch": 8}, ["as-is", None]),
     ("config 5: 128K, batch 1", 5, {"batch": 1}, [128, 512, None]),
     ("config 5: 128K, batch 16", 5, {"batch": 16}, [128, 512, None]),
+    ("config 3 over an E4M3 cache: Llama-2-7B shape, 32 layers, 32K, K=128", 3, {"kv": "e4m3"}, ["as-is"]),
 ]
 
 
@@ -817,19 +835,23 @@ def run_by_config(args, device) -> dict:
     t0 = time.perf_counter()
     l2 = l2_bytes()
     for label, wid, over, variants in BY_CONFIG:
+        over = dict(over)
+        kv = over.pop("kv", "f16")
+        fused = kv == "f16"
         base = workloads.WORKLOADS[wid].with_(**over)
-        stack0, layers, lens = build_state(base, device)
+        stack0, layers, lens = build_state(base, device, fused=fused, kv=kv)
         del stack0
-        nbytes_min = min(step_bytes(base if v == "as-is" else base.with_(k_pages=v), lens)["total"] for v in variants)
+        nbytes_min = min(step_bytes(base if v == "as-is" else base.with_(k_pages=v), lens, fused=fused, kv=kv)["total"]
+                         for v in variants)
         n = rotation_copies(nbytes_min, l2)
         copies = [layers] + [clone_layers(layers) for _ in range(n - 1)]
         for v in variants:
             w = base if v == "as-is" else base.with_(k_pages=v)
-            stack = make_stack(w, device)
-            m = measure(w, stack, copies, lens, device, args.by_config_steps, 3)
+            stack = make_stack(w, device, fused=fused, kv=kv)
+            m = measure(w, stack, copies, lens, device, args.by_config_steps, 3, kv=kv, fused=fused)
             nb = m["bytes"]["total"]
             e = {"label": label + ("" if v == "as-is" else (", all dense" if v is None else f", K={v}")),
-                 "workload": w.name, "config_id": w.id, "batch": w.batch, "layers": w.num_layers,
+                 "workload": w.name, "config_id": w.id, "batch": w.batch, "layers": w.num_layers, "kv_cache": kv,
                  "k_pages": w.k_pages, "us_per_step": round(m["s_per_step"] * 1e6, 2), "bytes_per_step": nb,
                  "gbs_step": round(nb / m["s_per_step"] / 1e9, 1),
                  "frac_step": round(nb / m["s_per_step"] / 1e9 / m["peaks"]["hbm_gbs"], 4),
@@ -989,15 +1011,17 @@ def main(argv=None):
     ap.add_argument("--prefill", type=int, default=0,
                     help="time gqa_prefill_attn on a chunk of this many tokens per sequence and layer instead")
     ap.add_argument("--kv", choices=("f16", "e4m3", "int4"), default="f16",
-                    help="KV-cache format; e4m3 (8-bit codes, per-tensor scales) and int4 (4-bit levels, per-token "
-                         "scales) run all-dense stacks only")
+                    help="KV-cache format; e4m3 (8-bit codes, per-tensor scales; Quest layers run the step-by-step "
+                         "calls) or int4 (4-bit levels, per-token scales; all-dense stacks only)")
     args = ap.parse_args(argv)
     if args.by_config is None:
         args.by_config = default_command(args)
-    if args.kv != "f16":
+    if args.kv == "int4":
         w = workload_from_args(args)
         if any(not w.layer_is_dense(i) for i in range(w.num_layers)):
-            raise SystemExit(f"--kv {args.kv} needs a stack of dense layers only (e.g. --workload 2, or --layers 2)")
+            raise SystemExit("--kv int4 needs a stack of dense layers only (e.g. --workload 2, or --layers 2)")
+    if args.kv == "e4m3":
+        args.unfused = True        # Quest layers over E4M3 bounds run as the step-by-step calls
     rank, world, local = dist_env()
     if args.prefill and args.impl == "ours":
         run_prefill(args, rank, world, local)

@@ -10,8 +10,10 @@ fallback.
 
 Function names follow the C ABI: gqa_decode_attn, quest_append_kv,
 quest_update_meta, quest_score_pages, quest_topk_pages, quest_sparse_attn,
-quest_decode_attn, and the 8-bit cache pair gqa_decode_attn_e4m3 /
-kv_append_e4m3.
+quest_decode_attn, the 8-bit cache calls gqa_decode_attn_e4m3 /
+kv_append_e4m3 and their Quest counterparts (quest_append_kv_e4m3,
+quest_update_meta_e4m3, quest_score_pages_e4m3, quest_sparse_attn_e4m3), the
+4-bit pair and prefill.
 """
 from __future__ import annotations
 
@@ -66,6 +68,7 @@ class Dims(ctypes.Structure):
 EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_update_meta",
            "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "quest_decode_attn",
            "gqa_decode_attn_noalloc", "gqa_decode_attn_e4m3", "kv_append_e4m3",
+           "quest_append_kv_e4m3", "quest_update_meta_e4m3", "quest_score_pages_e4m3", "quest_sparse_attn_e4m3",
            "gqa_decode_attn_int4", "kv_append_int4",
            "gqaq_prefill_workspace_bytes", "gqa_prefill_attn",
            "gqaq_status_string", "gqaq_set_option", "gqaq_device_status", "gqaq_version")
@@ -97,6 +100,10 @@ def lib():
         f32 = ctypes.c_float
         L.gqa_decode_attn_e4m3.argtypes = [dp, vp, vp, vp, f32, f32, vp, f32, vp, vp, ctypes.c_size_t, vp]
         L.kv_append_e4m3.argtypes = [dp, vp, vp, vp, vp, vp, f32, f32, vp]
+        L.quest_append_kv_e4m3.argtypes = [dp, vp, vp, vp, vp, vp, vp, f32, f32, vp]
+        L.quest_update_meta_e4m3.argtypes = [dp, vp, vp, vp, i32, i32, vp]
+        L.quest_score_pages_e4m3.argtypes = [dp, vp, vp, f32, vp, vp, vp]
+        L.quest_sparse_attn_e4m3.argtypes = [dp, vp, vp, vp, f32, f32, vp, vp, i32, f32, vp, vp, ctypes.c_size_t, vp]
         L.gqa_decode_attn_int4.argtypes = [dp, vp, vp, vp, vp, vp, vp, f32, vp, vp, ctypes.c_size_t, vp]
         L.kv_append_int4.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gqaq_prefill_workspace_bytes.argtypes = [dp, i32]
@@ -142,6 +149,22 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _shape(t: torch.Tensor, name: str, shape):
+    """The library reads and writes whole buffers of these shapes: refuse any other."""
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _meta_shape(meta, B, Hkv, Lmax, D, page_size):
+    _shape(meta, "meta", (B, Hkv, num_pages(Lmax, page_size), 2, D))
+
+
+def _new_rows(k_new, v_new, pos, B, Hkv, D):
+    _shape(k_new, "k_new", (B, Hkv, D))
+    _shape(v_new, "v_new", (B, Hkv, D))
+    _shape(pos, "pos", (B,))
 
 
 def make_dims(batch, num_q_heads, num_kv_heads, head_dim, max_len, page_size=PAGE_SIZE) -> Dims:
@@ -237,6 +260,15 @@ def quest_decode_attn(q, k_cache, v_cache, meta, valid_len, k: int, scale: float
     if page_idx is not None:
         _need(page_idx, "page_idx", torch.int32, 3)
     d = dims_of(q, k_cache, page_size)
+    _meta_shape(meta, d.batch, d.num_kv_heads, d.max_len, d.head_dim, page_size)
+    _shape(valid_len, "valid_len", (d.batch,))
+    _shape(v_cache, "v_cache", tuple(k_cache.shape))
+    if pos is not None:
+        _new_rows(k_new, v_new, pos, d.batch, d.num_kv_heads, d.head_dim)
+    if scores is not None:
+        _shape(scores, "scores", (d.batch, d.num_kv_heads, num_pages(d.max_len, page_size)))
+    if page_idx is not None:
+        _shape(page_idx, "page_idx", (d.batch, d.num_kv_heads, int(k)))
     _check("quest_decode_attn", lib().quest_decode_attn(
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(k_new), _ptr(v_new),
         _ptr(pos), _ptr(valid_len), int(k), float(scale), _ptr(out), _ptr(scores), _ptr(page_idx),
@@ -293,6 +325,94 @@ def kv_append_e4m3(k_cache, v_cache, k_new, v_new, pos, k_inv_scale: float, v_in
     _check("kv_append_e4m3", lib().kv_append_e4m3(
         ctypes.byref(d), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos), float(k_inv_scale),
         float(v_inv_scale), _stream(k_cache)))
+
+
+def new_meta_e4m3(batch: int, num_kv_heads: int, max_len: int, head_dim: int, device,
+                  page_size: int = PAGE_SIZE) -> torch.Tensor:
+    """Allocate E4M3 page bounds [B,Hkv,Pmax,2,D] uint8 (contents undefined)."""
+    return torch.empty(batch, num_kv_heads, num_pages(max_len, page_size), 2, head_dim, dtype=torch.uint8,
+                       device=device)
+
+
+def quest_append_kv_e4m3(k_cache, v_cache, meta, k_new, v_new, pos, k_inv_scale: float, v_inv_scale: float,
+                         page_size: int = PAGE_SIZE):
+    """kv_append_e4m3 plus the page's E4M3 bounds (meta [B,Hkv,Pmax,2,D] uint8)."""
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(meta, "meta", torch.uint8, 5)
+    _need(k_new, "k_new", torch.float16, 3)
+    _need(v_new, "v_new", torch.float16, 3)
+    _need(pos, "pos", torch.int32, 1)
+    B, Hkv, Lmax, D = k_cache.shape
+    _shape(v_cache, "v_cache", tuple(k_cache.shape))
+    _meta_shape(meta, B, Hkv, Lmax, D, page_size)
+    _new_rows(k_new, v_new, pos, B, Hkv, D)
+    d = make_dims(B, Hkv, Hkv, D, Lmax, page_size)
+    _check("quest_append_kv_e4m3", lib().quest_append_kv_e4m3(
+        ctypes.byref(d), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(k_new), _ptr(v_new), _ptr(pos),
+        float(k_inv_scale), float(v_inv_scale), _stream(k_cache)))
+
+
+def quest_update_meta_e4m3(k_cache, valid_len, meta, page_begin: int = 0, page_end: Optional[int] = None,
+                           page_size: int = PAGE_SIZE):
+    """Rebuild the E4M3 page bounds of pages [page_begin, page_end) from the cache codes."""
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    _need(meta, "meta", torch.uint8, 5)
+    B, Hkv, Lmax, D = k_cache.shape
+    _meta_shape(meta, B, Hkv, Lmax, D, page_size)
+    _shape(valid_len, "valid_len", (B,))
+    d = make_dims(B, Hkv, Hkv, D, Lmax, page_size)
+    if page_end is None:
+        page_end = num_pages(Lmax, page_size)
+    _check("quest_update_meta_e4m3", lib().quest_update_meta_e4m3(
+        ctypes.byref(d), _ptr(k_cache), _ptr(valid_len), _ptr(meta), int(page_begin), int(page_end),
+        _stream(k_cache)))
+    return meta
+
+
+def quest_score_pages_e4m3(q, meta, k_scale: float, valid_len, max_len: int, scores=None,
+                           page_size: int = PAGE_SIZE):
+    """k_scale * U(p,q) from E4M3 page bounds -> scores [B,Hkv,Pmax] fp32."""
+    _need(q, "q", torch.float16, 3)
+    _need(meta, "meta", torch.uint8, 5)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    B, Hq, D = q.shape
+    Hkv = meta.shape[1]
+    d = make_dims(B, Hq, Hkv, D, max_len, page_size)
+    _meta_shape(meta, B, Hkv, max_len, D, page_size)
+    _shape(valid_len, "valid_len", (B,))
+    if scores is None:
+        scores = torch.empty(B, Hkv, num_pages(max_len, page_size), dtype=torch.float32, device=q.device)
+    _need(scores, "scores", torch.float32, 3)
+    _shape(scores, "scores", (B, Hkv, num_pages(max_len, page_size)))
+    _check("quest_score_pages_e4m3", lib().quest_score_pages_e4m3(
+        ctypes.byref(d), _ptr(q), _ptr(meta), float(k_scale), _ptr(valid_len), _ptr(scores), _stream(q)))
+    return scores
+
+
+def quest_sparse_attn_e4m3(q, k_cache, v_cache, k_scale: float, v_scale: float, valid_len, page_idx, scale: float,
+                           out=None, workspace=None, page_size: int = PAGE_SIZE):
+    """Attention over the selected pages of an E4M3 cache (page_idx [B,Hkv,k])."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    _need(page_idx, "page_idx", torch.int32, 3)
+    d = dims_of(q, k_cache, page_size)
+    _shape(v_cache, "v_cache", tuple(k_cache.shape))
+    _shape(valid_len, "valid_len", (d.batch,))
+    _shape(page_idx, "page_idx", (d.batch, d.num_kv_heads, page_idx.shape[2]))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 3)
+    if workspace is None:
+        workspace = alloc_workspace(d, q.device)
+    _check("quest_sparse_attn_e4m3", lib().quest_sparse_attn_e4m3(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale), _ptr(valid_len),
+        _ptr(page_idx), int(page_idx.shape[2]), float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(q)))
+    return out
 
 
 def prefill_workspace_bytes(dims: Dims, q_len: int) -> int:
@@ -382,6 +502,9 @@ def quest_append_kv(k_cache, v_cache, meta, k_new, v_new, pos, page_size: int = 
     _need(v_new, "v_new", torch.float16, 3)
     _need(pos, "pos", torch.int32, 1)
     B, Hkv, Lmax, D = k_cache.shape
+    _shape(v_cache, "v_cache", tuple(k_cache.shape))
+    _meta_shape(meta, B, Hkv, Lmax, D, page_size)
+    _new_rows(k_new, v_new, pos, B, Hkv, D)
     d = make_dims(B, Hkv, Hkv, D, Lmax, page_size)
     _check("quest_append_kv", lib().quest_append_kv(
         ctypes.byref(d), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(k_new), _ptr(v_new),
@@ -395,6 +518,8 @@ def quest_update_meta(k_cache, valid_len, meta, page_begin: int = 0, page_end: O
     _need(valid_len, "valid_len", torch.int32, 1)
     _need(meta, "meta", torch.float16, 5)
     B, Hkv, Lmax, D = k_cache.shape
+    _meta_shape(meta, B, Hkv, Lmax, D, page_size)
+    _shape(valid_len, "valid_len", (B,))
     d = make_dims(B, Hkv, Hkv, D, Lmax, page_size)
     if page_end is None:
         page_end = num_pages(Lmax, page_size)
@@ -412,9 +537,12 @@ def quest_score_pages(q, meta, valid_len, max_len: int, scores=None, page_size: 
     B, Hq, D = q.shape
     Hkv = meta.shape[1]
     d = make_dims(B, Hq, Hkv, D, max_len, page_size)
+    _meta_shape(meta, B, Hkv, max_len, D, page_size)
+    _shape(valid_len, "valid_len", (B,))
     if scores is None:
         scores = torch.empty(B, Hkv, num_pages(max_len, page_size), dtype=torch.float32, device=q.device)
     _need(scores, "scores", torch.float32, 3)
+    _shape(scores, "scores", (B, Hkv, num_pages(max_len, page_size)))
     _check("quest_score_pages", lib().quest_score_pages(
         ctypes.byref(d), _ptr(q), _ptr(meta), _ptr(valid_len), _ptr(scores), _stream(q)))
     return scores
@@ -425,10 +553,13 @@ def quest_topk_pages(scores, valid_len, k: int, max_len: int, page_idx=None, pag
     _need(scores, "scores", torch.float32, 3)
     _need(valid_len, "valid_len", torch.int32, 1)
     B, Hkv, _ = scores.shape
+    _shape(scores, "scores", (B, Hkv, num_pages(max_len, page_size)))
+    _shape(valid_len, "valid_len", (B,))
     d = make_dims(B, Hkv, Hkv, 64, max_len, page_size)
     if page_idx is None:
         page_idx = torch.empty(B, Hkv, int(k), dtype=torch.int32, device=scores.device)
     _need(page_idx, "page_idx", torch.int32, 3)
+    _shape(page_idx, "page_idx", (B, Hkv, int(k)))
     _check("quest_topk_pages", lib().quest_topk_pages(
         ctypes.byref(d), _ptr(scores), _ptr(valid_len), int(k), _ptr(page_idx), None, 0,
         _stream(scores)))
@@ -444,6 +575,9 @@ def quest_sparse_attn(q, k_cache, v_cache, valid_len, page_idx, scale: float, ou
     _need(valid_len, "valid_len", torch.int32, 1)
     _need(page_idx, "page_idx", torch.int32, 3)
     d = dims_of(q, k_cache, page_size)
+    _shape(v_cache, "v_cache", tuple(k_cache.shape))
+    _shape(valid_len, "valid_len", (d.batch,))
+    _shape(page_idx, "page_idx", (d.batch, d.num_kv_heads, page_idx.shape[2]))
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.float16, 3)

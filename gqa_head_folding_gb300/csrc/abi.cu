@@ -439,6 +439,83 @@ int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_cache, co
                               reinterpret_cast<const __half *>(v_new), pos, k_inv_scale, v_inv_scale, ctx);
 }
 
+int quest_append_kv_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_cache, uint8_t *meta,
+                         const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos, float k_inv_scale,
+                         float v_inv_scale, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(meta) || !aligned16(k_new) || !aligned16(v_new) ||
+        !aligned16(pos))
+        return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(k_inv_scale) || !isfinite(v_inv_scale)) return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_append_e4m3_meta(dims, k_cache, v_cache, meta, reinterpret_cast<const __half *>(k_new),
+                                   reinterpret_cast<const __half *>(v_new), pos, k_inv_scale, v_inv_scale, ctx);
+}
+
+int quest_update_meta_e4m3(const gqaq_dims *dims, const uint8_t *k_cache, const int32_t *valid_len, uint8_t *meta,
+                           int page_begin, int page_end, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(k_cache) || !aligned16(valid_len) || !aligned16(meta)) return GQAQ_ERR_INVALID_ARG;
+    const int pmax = (dims->max_len + dims->page_size - 1) / dims->page_size;
+    if (page_begin < 0 || page_end < page_begin || page_end > pmax) return GQAQ_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_update_meta_e4m3(dims, k_cache, valid_len, meta, page_begin, page_end, ctx);
+}
+
+int quest_score_pages_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *meta, float k_scale,
+                           const int32_t *valid_len, float *scores, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(meta) || !aligned16(valid_len) || !aligned16(scores))
+        return GQAQ_ERR_INVALID_ARG;
+    if (!(isfinite(k_scale) && k_scale > 0.f)) return GQAQ_ERR_INVALID_ARG;  // a positive scale keeps the ranking
+    const int64_t pmax = (dims->max_len + dims->page_size - 1) / dims->page_size;
+    if ((int64_t)dims->batch * dims->num_kv_heads > 65535) return GQAQ_ERR_UNSUPPORTED;  // grid y
+    if ((int64_t)dims->batch * dims->num_kv_heads * pmax > (int64_t)INT32_MAX - 1024) return GQAQ_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    return launch_score_pages_e4m3(dims, reinterpret_cast<const __half *>(q), meta, k_scale, valid_len, scores, ctx);
+}
+
+int quest_sparse_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                           float k_scale, float v_scale, const int32_t *valid_len, const int32_t *page_idx, int k,
+                           float scale, gqaq_half *out, void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(valid_len) ||
+        !aligned16(page_idx))
+        return GQAQ_ERR_INVALID_ARG;
+    if (k < 1 || k > 65536) return GQAQ_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !isfinite(k_scale) || !isfinite(v_scale)) return GQAQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace)) return GQAQ_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    AttnArgs a = {};
+    a.dims = dims;
+    a.q = reinterpret_cast<const __half *>(q);
+    a.k_cache = reinterpret_cast<const __half *>(k_cache);  // byte rows; typed as the kernels take it
+    a.v_cache = reinterpret_cast<const __half *>(v_cache);
+    a.valid_len = valid_len;
+    a.page_idx = page_idx;
+    a.kpages = k;
+    a.scale = scale;
+    a.kv8 = true;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.out = reinterpret_cast<__half *>(out);
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launch_attention(a, ctx);
+}
+
 int gqa_decode_attn_int4(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_codes, const float *k_scales,
                          const uint8_t *v_codes, const float *v_scales, const int32_t *valid_len, float scale,
                          gqaq_half *out, void *workspace, size_t workspace_bytes, void *stream) {

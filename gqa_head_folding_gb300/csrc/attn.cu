@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
                         const AttnParams p) {
     using C = AttnCfg<D, G, KV>;
     constexpr bool KV8 = KV == 1, KV4 = KV == 2;
-    static_assert(!(SPARSE && KV != 0), "the 8-bit and 4-bit variants are dense");
+    static_assert(!(SPARSE && KV4), "the 4-bit variant is dense");
     constexpr int NCT = C::NCW * 32;  // consumer threads
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -438,15 +438,21 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
                     const bool ok = mine && page >= 0 && page < P;
                     if (mine && !ok) raise_flag(p.status, GQAQ_DEV_BAD_PAGE);
                     const unsigned m = __ballot_sync(0xffffffffu, ok);
-                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(p.S * D * 2 * 2));
+                    constexpr int RB = KV8 ? D : 2 * D;  // bytes of one cached row
+                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(m) * (uint32_t)(p.S * RB * 2));
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int pj = __shfl_sync(0xffffffffu, page, j);
                         if (lane == 0 && ((m >> j) & 1u)) {
                             const int y = row0 + pj * p.S;
-                            const uint32_t off = (uint32_t)(j * slots.slot * D * 2);
-                            tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K and V
-                            tma_load_3d(vdst + off, &vmap, 0, 0, y, fb, pol);
+                            const uint32_t off = (uint32_t)(j * slots.slot * RB);
+                            if (KV8) {  // the page's byte rows land where a dense tile's rows would
+                                tma_load_2d(kdst + off, &kmap, 0, y, fb, pol);
+                                tma_load_2d(vdst + off, &vmap, 0, y, fb, pol);
+                            } else {
+                                tma_load_3d(kdst + off, &kmap, 0, 0, y, fb, pol);  // page-major K and V
+                                tma_load_3d(vdst + off, &vmap, 0, 0, y, fb, pol);
+                            }
                         }
                     }
                 } else {
@@ -477,7 +483,9 @@ __global__ void __launch_bounds__(AttnCfg<D, G, KV>::THREADS, AttnCfg<D, G, KV>:
     // the arrival counters in step, so the workspace stays reusable.
     // ----------------------------------------------------------------------
     const int tid = threadIdx.x;  // 0..255 among consumers
-    using WA = MmaAttn<D, G, SPARSE, KV>;  // sparse stages hold K and V page-major
+    // fp16 sparse stages hold K and V page-major; E4M3 page boxes stack into
+    // the dense byte-row layout
+    using WA = MmaAttn<D, G, SPARSE && KV == 0, KV>;
     WA wa;
     wa.init(warp, lane, smem_u32(pbuf));
 
@@ -713,7 +721,7 @@ int launch_t(const AttnArgs &a, const LaunchCtx &ctx) {
 
 template <int D, int G>
 int dispatch_sparse(const AttnArgs &a, const LaunchCtx &ctx) {
-    if (a.kv8) return a.page_idx ? GQAQ_ERR_UNSUPPORTED : launch_t<D, G, false, 1>(a, ctx);
+    if (a.kv8) return a.page_idx ? launch_t<D, G, true, 1>(a, ctx) : launch_t<D, G, false, 1>(a, ctx);
     if (a.kv4) return a.page_idx ? GQAQ_ERR_UNSUPPORTED : launch_t<D, G, false, 2>(a, ctx);
     return a.page_idx ? launch_t<D, G, true>(a, ctx) : launch_t<D, G, false>(a, ctx);
 }
@@ -735,10 +743,12 @@ size_t ws_t(const gqaq_dims &dm, const LaunchCtx &ctx) {
     const int g1 = grid_for<D, G, true>(ctx);
     const int g2 = grid_for<D, G, false, 1>(ctx);
     const int g3 = grid_for<D, G, false, 2>(ctx);
-    if (g0 < 1 || g1 < 1 || g2 < 1 || g3 < 1) return 0;
+    const int g4 = grid_for<D, G, true, 1>(ctx);
+    if (g0 < 1 || g1 < 1 || g2 < 1 || g3 < 1 || g4 < 1) return 0;
     int grid = g0 > g1 ? g0 : g1;
     grid = grid > g2 ? grid : g2;
     grid = grid > g3 ? grid : g3;
+    grid = grid > g4 ? grid : g4;
     return count_bytes(dm) + (size_t)grid * 2 * G * (D + 2) * sizeof(float);
 }
 

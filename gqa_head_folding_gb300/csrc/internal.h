@@ -38,7 +38,7 @@ struct AttnArgs {
     const int *page_idx;  // sparse only
     int kpages;           // sparse only
     float scale;
-    bool kv8;             // caches hold E4M3 codes (dense only)
+    bool kv8;             // caches hold E4M3 codes
     float k_scale, v_scale;  // E4M3: value = code * scale
     bool kv4;             // caches hold INT4 levels (dense only)
     const float *k_scales, *v_scales;  // INT4: [B*Hkv][Lmax] per-token scales
@@ -53,6 +53,15 @@ int launch_append_e4m3(const gqaq_dims *d, uint8_t *k_cache, uint8_t *v_cache, c
                        const LaunchCtx &ctx);
 int launch_append_int4(const gqaq_dims *d, uint8_t *k_codes, float *k_scales, uint8_t *v_codes, float *v_scales,
                        const __half *k_new, const __half *v_new, const int *pos, const LaunchCtx &ctx);
+// Quest over an E4M3 cache (kv_lowbit.cu): the append with the page bounds,
+// the bounds rebuilt from the cache, the page scores.
+int launch_append_e4m3_meta(const gqaq_dims *d, uint8_t *k_cache, uint8_t *v_cache, uint8_t *meta,
+                            const __half *k_new, const __half *v_new, const int *pos, float k_inv_scale,
+                            float v_inv_scale, const LaunchCtx &ctx);
+int launch_update_meta_e4m3(const gqaq_dims *d, const uint8_t *k_cache, const int *valid_len, uint8_t *meta,
+                            int page_begin, int page_end, const LaunchCtx &ctx);
+int launch_score_pages_e4m3(const gqaq_dims *d, const __half *q, const uint8_t *meta, float k_scale,
+                            const int *valid_len, float *scores, const LaunchCtx &ctx);
 size_t attention_workspace_bytes(const gqaq_dims *dims, const LaunchCtx &ctx);
 
 // Causal chunk attention (prefill.cu): q_len new tokens per sequence, the

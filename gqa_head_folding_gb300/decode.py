@@ -10,11 +10,14 @@ each layer's page metadata stays current whatever path reads it.
 
 With ``kv="e4m3"`` the caches hold 8-bit E4M3 codes with one fp32 scale per
 tensor (``Layer.k_scale`` / ``v_scale``): appends quantize
-(``kv_append_e4m3``) and dense layers read them through
-``gqa_decode_attn_e4m3``. With ``kv="int4"`` they hold 4-bit levels
-``[B,Hkv,Lmax,D/2]`` with one fp32 scale per token row (``Layer.k_scales`` /
-``v_scales``), through ``kv_append_int4`` and ``gqa_decode_attn_int4``. The
-Quest kernels take fp16 caches only, so a low-bit stack must be all dense.
+(``kv_append_e4m3``, or ``quest_append_kv_e4m3`` when the layer keeps page
+bounds), dense layers read them through ``gqa_decode_attn_e4m3`` and Quest
+layers run the step-by-step calls over E4M3 page bounds
+(``quest_score_pages_e4m3``, ``quest_topk_pages``, ``quest_sparse_attn_e4m3``;
+the fused kernel reads fp16 caches only). With ``kv="int4"`` they hold 4-bit
+levels ``[B,Hkv,Lmax,D/2]`` with one fp32 scale per token row
+(``Layer.k_scales`` / ``v_scales``), through ``kv_append_int4`` and
+``gqa_decode_attn_int4``; an INT4 stack must be all dense.
 
 By default a Quest layer is one fused launch (``quest_decode_attn``: append,
 score, top-K and sparse attention in one kernel); the library picks its
@@ -33,8 +36,9 @@ from typing import List, Optional
 import torch
 
 from . import (alloc_workspace, gqa_decode_attn, gqa_decode_attn_e4m3, gqa_decode_attn_int4, kv_append_e4m3,
-               kv_append_int4, make_dims, new_meta, num_pages, quest_append_kv, quest_decode_attn, quest_score_pages,
-               quest_sparse_attn, quest_topk_pages, quest_update_meta)
+               kv_append_int4, make_dims, new_meta, new_meta_e4m3, num_pages, quest_append_kv, quest_append_kv_e4m3,
+               quest_decode_attn, quest_score_pages, quest_score_pages_e4m3, quest_sparse_attn, quest_sparse_attn_e4m3,
+               quest_topk_pages, quest_update_meta, quest_update_meta_e4m3)
 
 
 @dataclasses.dataclass
@@ -45,7 +49,7 @@ class Layer:
     v_cache: torch.Tensor
     valid_len: torch.Tensor               # [B] int32 (tokens attended after the append)
     out: torch.Tensor                     # [B,Hq,D] fp16
-    meta: Optional[torch.Tensor] = None   # [B,Hkv,Pmax,2,D] fp16 (Quest layers / appends)
+    meta: Optional[torch.Tensor] = None   # [B,Hkv,Pmax,2,D] fp16 (uint8 E4M3 bounds with kv="e4m3")
     k_new: Optional[torch.Tensor] = None  # [B,Hkv,D] fp16
     v_new: Optional[torch.Tensor] = None
     pos: Optional[torch.Tensor] = None    # [B] int32 row the new token goes to
@@ -82,8 +86,10 @@ class DecodeStack:
                  kv: str = "f16", num_layers: Optional[int] = None):
         if kv not in ("f16", "e4m3", "int4"):
             raise ValueError(f"kv must be 'f16', 'e4m3' or 'int4', got {kv!r}")
-        if kv != "f16" and k_pages is not None and (num_layers is None or num_layers > dense_layers):
-            raise ValueError("a low-bit cache runs dense layers only (the Quest kernels read fp16 caches)")
+        if kv == "int4" and k_pages is not None and (num_layers is None or num_layers > dense_layers):
+            raise ValueError("a 4-bit cache runs dense layers only")
+        if kv == "e4m3":
+            fused = False                  # Quest layers over E4M3 bounds run as the step-by-step calls
         self.fused, self.kv = fused, kv
         self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
         self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
@@ -101,15 +107,19 @@ class DecodeStack:
         return "dense" in layer_plan(layer, self.k_pages, self.dense_layers, self.fused, False)
 
     def new_meta(self) -> torch.Tensor:
-        return new_meta(self.batch, self.num_kv_heads, self.max_len, self.head_dim, self.device,
-                        self.page_size)
+        alloc = new_meta_e4m3 if self.kv == "e4m3" else new_meta
+        return alloc(self.batch, self.num_kv_heads, self.max_len, self.head_dim, self.device, self.page_size)
 
     def build_meta(self, layer: Layer, valid_len: torch.Tensor):
         """Metadata of the pages already in the cache (after a prefill)."""
-        quest_update_meta(layer.k_cache, valid_len, layer.meta, page_size=self.page_size)
+        build = quest_update_meta_e4m3 if self.kv == "e4m3" else quest_update_meta
+        build(layer.k_cache, valid_len, layer.meta, page_size=self.page_size)
 
     def append(self, L: Layer):
-        if self.kv == "e4m3":
+        if self.kv == "e4m3" and L.meta is not None:
+            quest_append_kv_e4m3(L.k_cache, L.v_cache, L.meta, L.k_new, L.v_new, L.pos, 1.0 / L.k_scale,
+                                 1.0 / L.v_scale, self.page_size)
+        elif self.kv == "e4m3":
             kv_append_e4m3(L.k_cache, L.v_cache, L.k_new, L.v_new, L.pos, 1.0 / L.k_scale, 1.0 / L.v_scale)
         elif self.kv == "int4":
             kv_append_int4(L.k_cache, L.k_scales, L.v_cache, L.v_scales, L.k_new, L.v_new, L.pos)
@@ -144,6 +154,9 @@ class DecodeStack:
                                              self.scale, k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out,
                                              page_idx=L.page_idx, page_size=self.page_size,
                                              workspace=self.workspace)
+        if name == "score" and self.kv == "e4m3":
+            return lambda: quest_score_pages_e4m3(L.q, L.meta, L.k_scale, L.valid_len, self.max_len,
+                                                  scores=self.scores, page_size=self.page_size)
         if name == "score":
             return lambda: quest_score_pages(L.q, L.meta, L.valid_len, self.max_len, scores=self.scores,
                                              page_size=self.page_size)
@@ -151,6 +164,10 @@ class DecodeStack:
         if name == "topk":
             return lambda: quest_topk_pages(self.scores, L.valid_len, self.k_pages, self.max_len, page_idx=idx,
                                             page_size=self.page_size)
+        if name == "sparse" and self.kv == "e4m3":
+            return lambda: quest_sparse_attn_e4m3(L.q, L.k_cache, L.v_cache, L.k_scale, L.v_scale, L.valid_len, idx,
+                                                  self.scale, out=L.out, workspace=self.workspace,
+                                                  page_size=self.page_size)
         if name == "sparse":
             return lambda: quest_sparse_attn(L.q, L.k_cache, L.v_cache, L.valid_len, idx, self.scale, out=L.out,
                                              workspace=self.workspace, page_size=self.page_size)

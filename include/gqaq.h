@@ -253,6 +253,45 @@ GQAQ_API int kv_append_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_
                             const gqaq_half *v_new, const int32_t *pos, float k_inv_scale, float v_inv_scale,
                             void *stream);
 
+/* Quest over an E4M3 cache: the page-score section's metadata and score, and
+ * the flowchart's attention over the selected pages, with the 8-bit format
+ * above. meta is [B][Hkv][Pmax][2][D] bytes: per page the E4M3 codes of each
+ * channel's smallest, then largest key value (compared after decoding; a
+ * zero bound is stored as the code 0x00, so each bound has one code; the
+ * dequantized bounds are k_scale * value(code)). The cache holds no NaN
+ * codes. 2*D bytes per page, half the fp16 metadata.
+ *
+ * quest_append_kv_e4m3: kv_append_e4m3's codes for row pos[b], then the
+ * page's bounds as quest_append_kv keeps them (a token starting a page
+ * replaces them). pos[b] outside [0, Lmax) is skipped and raises
+ * GQAQ_DEV_BAD_POS. */
+GQAQ_API int quest_append_kv_e4m3(const gqaq_dims *dims, uint8_t *k_cache, uint8_t *v_cache, uint8_t *meta,
+                                  const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos,
+                                  float k_inv_scale, float v_inv_scale, void *stream);
+
+/* Rebuild the bounds of pages [page_begin, page_end) from the codes of rows
+ * below valid_len[b] (pages with no valid row are left untouched). Errors as
+ * quest_update_meta. */
+GQAQ_API int quest_update_meta_e4m3(const gqaq_dims *dims, const uint8_t *k_cache, const int32_t *valid_len,
+                                    uint8_t *meta, int page_begin, int page_end, void *stream);
+
+/* scores[b][kv][p] = k_scale * max_g sum_i max(q_i value(m_i), q_i value(M_i))
+ * for pages p < ceil(valid_len[b] / S), q the unscaled fp16 query rows of KV
+ * head kv (fp32 arithmetic; the products are exact). Later pages are not
+ * written. k_scale must be finite and > 0, else GQAQ_ERR_INVALID_ARG. The
+ * scores feed quest_topk_pages unchanged. */
+GQAQ_API int quest_score_pages_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *meta, float k_scale,
+                                    const int32_t *valid_len, float *scores, void *stream);
+
+/* quest_sparse_attn over an E4M3 cache: attention over the tokens of the
+ * listed pages with the keys and values dequantized on load (code value *
+ * scale), fp32 accumulation, one rounding to fp16. Arguments, workspace and
+ * errors as quest_sparse_attn and gqa_decode_attn_e4m3. */
+GQAQ_API int quest_sparse_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_cache,
+                                    const uint8_t *v_cache, float k_scale, float v_scale, const int32_t *valid_len,
+                                    const int32_t *page_idx, int k, float scale, gqaq_half *out, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
 /* The 4-bit KV-cache variant (a format chosen here, see above: the plainest
  * one that keeps both contractions exact on integer levels): symmetric
  * INT4 with one fp32 scale per (token, KV head) row.

@@ -179,3 +179,65 @@ def test_benchmark_step_at_full_size_sampled():
             sel = L.page_idx[:, kv:kv + 1].cpu().numpy()
             check_topk(sel, oracle.page_scores(q, ref_meta, vl, S), vl, S, w.k_pages)
             assert_attn_close(out, oracle.sparse_attn(q, k, v, vl, sel, S, scale), f"layer {l} kv {kv}")
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_decode_stack_over_an_e4m3_cache_matches_oracle(G):
+    """The same stack over an E4M3 cache (per-tensor scales): dense layers
+    through gqa_decode_attn_e4m3, Quest layers as the step-by-step E4M3 calls
+    (appends keep the pages' E4M3 bounds), graph-replayed three steps with
+    programmatic launch and early K/V reads."""
+    w, xs, knew, vnew, vls = draw(G)
+    stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
+                        w.dense_layers, DEV, S, kv="e4m3", num_layers=w.num_layers)
+    assert not stack.fused
+    layers, host = [], []
+    for l, x in enumerate(xs):
+        ks = float(x["k_cache"].float().abs().max()) / 448.0
+        vs = float(x["v_cache"].float().abs().max()) / 448.0
+        kc = oracle.quantize_e4m3(x["k_cache"].numpy(), 1.0 / ks)
+        vc = oracle.quantize_e4m3(x["v_cache"].numpy(), 1.0 / vs)
+        L = Layer(q=x["q"].to(DEV), k_cache=torch.from_numpy(kc).to(DEV), v_cache=torch.from_numpy(vc).to(DEV),
+                  valid_len=torch.from_numpy(vls[0, l].copy()).to(DEV), out=torch.empty_like(x["q"], device=DEV),
+                  meta=stack.new_meta().zero_(), k_new=knew[0, l].to(DEV), v_new=vnew[0, l].to(DEV),
+                  pos=torch.from_numpy(vls[0, l] - 1).to(DEV), k_scale=ks, v_scale=vs)
+        stack.build_meta(L, L.valid_len - 1)
+        if not stack.is_dense(l):
+            L.page_idx = torch.full((w.batch, w.num_kv_heads, w.k_pages), -7, dtype=torch.int32, device=DEV)
+        layers.append(L)
+        host.append((kc, vc, ks, vs))
+    torch.cuda.synchronize()
+    graph = bench.capture(lambda: stack.step(layers), torch.device(DEV))
+    scale = 1.0 / math.sqrt(w.head_dim)
+    for s in range(NSTEPS):
+        for l, L in enumerate(layers):
+            L.valid_len.copy_(torch.from_numpy(vls[s, l].copy()))
+            L.pos.copy_(torch.from_numpy(vls[s, l] - 1))
+            L.k_new.copy_(knew[s, l])
+            L.v_new.copy_(vnew[s, l])
+            L.out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g.device_status() == 0
+        for l, L in enumerate(layers):
+            kc, vc, ks, vs = host[l]
+            vl = vls[s, l]
+            for b in range(w.batch):
+                kc[b, :, vl[b] - 1] = oracle.quantize_e4m3(knew[s, l, b].numpy(), 1.0 / ks)
+                vc[b, :, vl[b] - 1] = oracle.quantize_e4m3(vnew[s, l, b].numpy(), 1.0 / vs)
+            ref_meta = oracle.page_minmax_e4m3(kc, vl, S)
+            got_meta = L.meta.cpu().numpy()
+            for b in range(w.batch):
+                P = (int(vl[b]) + S - 1) // S
+                assert np.array_equal(got_meta[b, :, :P], ref_meta[b, :, :P]), f"bounds step {s} layer {l} b={b}"
+            q = xs[l]["q"].numpy()
+            if stack.is_dense(l):
+                assert_attn_close(L.out, oracle.attn_e4m3(q, kc, vc, ks, vs, vl, scale), f"dense step {s} layer {l}")
+            else:
+                sel = L.page_idx.cpu().numpy()
+                bounds = oracle.e4m3_to_f64(ref_meta) * ks
+                check_topk(sel, oracle.page_scores(q, bounds, vl, S), vl, S, w.k_pages)
+                assert_attn_close(L.out, oracle.sparse_attn(q, oracle.e4m3_to_f64(kc) * ks, oracle.e4m3_to_f64(vc) * vs,
+                                                             vl, sel, S, scale), f"quest step {s} layer {l}")
+    for l, L in enumerate(layers):
+        assert np.array_equal(L.k_cache.cpu().numpy(), host[l][0])
