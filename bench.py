@@ -754,7 +754,7 @@ def run_prefill(args, rank, world, local):
 
 
 FAMILY_KERNEL = {"dense": "gqa_decode_attn", "score": "quest_score_pages", "sparse": "quest_sparse_attn",
-                 "quest": "quest_decode_attn"}
+                 "quest": "quest_decode_attn"}  # "_e4m3" appended for the 8-bit cache
 
 
 def measure(w: workloads.Workload, stack, copies, lens, device, steps: int, warmup: int, kv: str = "f16",
@@ -837,7 +837,7 @@ def run_by_config(args, device) -> dict:
     for label, wid, over, variants in BY_CONFIG:
         over = dict(over)
         kv = over.pop("kv", "f16")
-        fused = kv == "f16"
+        fused = True
         base = workloads.WORKLOADS[wid].with_(**over)
         stack0, layers, lens = build_state(base, device, fused=fused, kv=kv)
         del stack0
@@ -1011,8 +1011,8 @@ def main(argv=None):
     ap.add_argument("--prefill", type=int, default=0,
                     help="time gqa_prefill_attn on a chunk of this many tokens per sequence and layer instead")
     ap.add_argument("--kv", choices=("f16", "e4m3", "int4"), default="f16",
-                    help="KV-cache format; e4m3 (8-bit codes, per-tensor scales; Quest layers run the step-by-step "
-                         "calls) or int4 (4-bit levels, per-token scales; all-dense stacks only)")
+                    help="KV-cache format; e4m3 (8-bit codes and page bounds, per-tensor scales) or int4 (4-bit "
+                         "levels, per-token scales; all-dense stacks only)")
     args = ap.parse_args(argv)
     if args.by_config is None:
         args.by_config = default_command(args)
@@ -1020,8 +1020,6 @@ def main(argv=None):
         w = workload_from_args(args)
         if any(not w.layer_is_dense(i) for i in range(w.num_layers)):
             raise SystemExit("--kv int4 needs a stack of dense layers only (e.g. --workload 2, or --layers 2)")
-    if args.kv == "e4m3":
-        args.unfused = True        # Quest layers over E4M3 bounds run as the step-by-step calls
     rank, world, local = dist_env()
     if args.prefill and args.impl == "ours":
         run_prefill(args, rank, world, local)

@@ -69,6 +69,7 @@ EXPORTS = ("gqaq_workspace_bytes", "gqa_decode_attn", "quest_append_kv", "quest_
            "quest_score_pages", "quest_topk_pages", "quest_sparse_attn", "quest_decode_attn",
            "gqa_decode_attn_noalloc", "gqa_decode_attn_e4m3", "kv_append_e4m3",
            "quest_append_kv_e4m3", "quest_update_meta_e4m3", "quest_score_pages_e4m3", "quest_sparse_attn_e4m3",
+           "quest_decode_attn_e4m3",
            "gqa_decode_attn_int4", "kv_append_int4",
            "gqaq_prefill_workspace_bytes", "gqa_prefill_attn",
            "gqaq_status_string", "gqaq_set_option", "gqaq_device_status", "gqaq_version")
@@ -104,6 +105,8 @@ def lib():
         L.quest_update_meta_e4m3.argtypes = [dp, vp, vp, vp, i32, i32, vp]
         L.quest_score_pages_e4m3.argtypes = [dp, vp, vp, f32, vp, vp, vp]
         L.quest_sparse_attn_e4m3.argtypes = [dp, vp, vp, vp, f32, f32, vp, vp, i32, f32, vp, vp, ctypes.c_size_t, vp]
+        L.quest_decode_attn_e4m3.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, f32, f32, f32, f32, vp, i32, f32, vp, vp,
+                                             vp, vp]
         L.gqa_decode_attn_int4.argtypes = [dp, vp, vp, vp, vp, vp, vp, f32, vp, vp, ctypes.c_size_t, vp]
         L.kv_append_int4.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gqaq_prefill_workspace_bytes.argtypes = [dp, i32]
@@ -412,6 +415,43 @@ def quest_sparse_attn_e4m3(q, k_cache, v_cache, k_scale: float, v_scale: float, 
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale), _ptr(valid_len),
         _ptr(page_idx), int(page_idx.shape[2]), float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
         _stream(q)))
+    return out
+
+
+def quest_decode_attn_e4m3(q, k_cache, v_cache, meta, valid_len, k: int, scale: float, k_scale: float,
+                           v_scale: float, k_new=None, v_new=None, pos=None, k_inv_scale: float = 1.0,
+                           v_inv_scale: float = 1.0, out=None, scores=None, page_idx=None,
+                           page_size: int = PAGE_SIZE):
+    """quest_decode_attn over an E4M3 cache (codes [B,Hkv,Lmax,D] uint8, bounds
+    [B,Hkv,Pmax,2,D] uint8) in one launch; the optional append quantizes
+    k_new/v_new with k_inv_scale / v_inv_scale."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(meta, "meta", torch.uint8, 5)
+    _need(valid_len, "valid_len", torch.int32, 1)
+    d = dims_of(q, k_cache, page_size)
+    _shape(v_cache, "v_cache", tuple(k_cache.shape))
+    _meta_shape(meta, d.batch, d.num_kv_heads, d.max_len, d.head_dim, page_size)
+    _shape(valid_len, "valid_len", (d.batch,))
+    if pos is not None:
+        _need(k_new, "k_new", torch.float16, 3)
+        _need(v_new, "v_new", torch.float16, 3)
+        _need(pos, "pos", torch.int32, 1)
+        _new_rows(k_new, v_new, pos, d.batch, d.num_kv_heads, d.head_dim)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float16, 3)
+    if scores is not None:
+        _need(scores, "scores", torch.float32, 3)
+        _shape(scores, "scores", (d.batch, d.num_kv_heads, num_pages(d.max_len, page_size)))
+    if page_idx is not None:
+        _need(page_idx, "page_idx", torch.int32, 3)
+        _shape(page_idx, "page_idx", (d.batch, d.num_kv_heads, int(k)))
+    _check("quest_decode_attn_e4m3", lib().quest_decode_attn_e4m3(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(k_new), _ptr(v_new), _ptr(pos),
+        float(k_inv_scale), float(v_inv_scale), float(k_scale), float(v_scale), _ptr(valid_len), int(k),
+        float(scale), _ptr(out), _ptr(scores), _ptr(page_idx), _stream(q)))
     return out
 
 

@@ -498,6 +498,24 @@ int quest_sparse_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint
     LaunchCtx ctx;
     rc = make_ctx(&ctx, stream);
     if (rc != GQAQ_OK) return rc;
+    if (k <= kFusedMaxPages) {
+        // cluster kernel: attention and the log-sum-exp merge in one launch
+        FusedArgs f = {};
+        f.dims = dims;
+        f.q = reinterpret_cast<const __half *>(q);
+        f.k_cache = const_cast<__half *>(reinterpret_cast<const __half *>(k_cache));
+        f.v_cache = const_cast<__half *>(reinterpret_cast<const __half *>(v_cache));
+        f.meta = nullptr;
+        f.valid_len = valid_len;
+        f.page_idx = const_cast<int32_t *>(page_idx);
+        f.kpages = k;
+        f.scale = scale;
+        f.out = reinterpret_cast<__half *>(out);
+        f.kv8 = true;
+        f.k_scale = k_scale;
+        f.v_scale = v_scale;
+        return launch_quest_fused(f, ctx);
+    }
     AttnArgs a = {};
     a.dims = dims;
     a.q = reinterpret_cast<const __half *>(q);
@@ -514,6 +532,51 @@ int quest_sparse_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, const uint
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     return launch_attention(a, ctx);
+}
+
+int quest_decode_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, uint8_t *k_cache, uint8_t *v_cache,
+                           uint8_t *meta, const gqaq_half *k_new, const gqaq_half *v_new, const int32_t *pos,
+                           float k_inv_scale, float v_inv_scale, float k_scale, float v_scale,
+                           const int32_t *valid_len, int k, float scale, gqaq_half *out, float *scores,
+                           int32_t *page_idx, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != GQAQ_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(meta) || !aligned16(valid_len) ||
+        !aligned16(out))
+        return GQAQ_ERR_INVALID_ARG;
+    if (pos != nullptr && (!aligned16(pos) || !aligned16(k_new) || !aligned16(v_new))) return GQAQ_ERR_INVALID_ARG;
+    if ((scores != nullptr && !aligned16(scores)) || (page_idx != nullptr && !aligned16(page_idx)))
+        return GQAQ_ERR_INVALID_ARG;
+    if (k < 1 || k > kFusedMaxPages) return k < 1 ? GQAQ_ERR_INVALID_ARG : GQAQ_ERR_UNSUPPORTED;
+    if (!isfinite(scale) || !isfinite(v_scale) || !(isfinite(k_scale) && k_scale > 0.f)) return GQAQ_ERR_INVALID_ARG;
+    if (pos != nullptr && (!isfinite(k_inv_scale) || !isfinite(v_inv_scale))) return GQAQ_ERR_INVALID_ARG;
+    const int64_t pmax = (dims->max_len + dims->page_size - 1) / dims->page_size;
+    if ((int64_t)dims->batch * dims->num_kv_heads * pmax > (int64_t)INT32_MAX - 1024) return GQAQ_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    rc = make_ctx(&ctx, stream);
+    if (rc != GQAQ_OK) return rc;
+    if (ctx.quest_kernel == 2) return GQAQ_ERR_UNSUPPORTED;  // the work-queue kernel reads fp16 caches only
+    FusedArgs f = {};
+    f.dims = dims;
+    f.q = reinterpret_cast<const __half *>(q);
+    f.k_cache = reinterpret_cast<__half *>(k_cache);  // byte rows; typed as the kernels take them
+    f.v_cache = reinterpret_cast<__half *>(v_cache);
+    f.meta = reinterpret_cast<__half *>(meta);
+    f.k_new = reinterpret_cast<const __half *>(k_new);
+    f.v_new = reinterpret_cast<const __half *>(v_new);
+    f.pos = pos;
+    f.valid_len = valid_len;
+    f.page_idx = page_idx;
+    f.scores = scores;
+    f.kpages = k;
+    f.scale = scale;
+    f.out = reinterpret_cast<__half *>(out);
+    f.kv8 = true;
+    f.k_inv = k_inv_scale;
+    f.v_inv = v_inv_scale;
+    f.k_scale = k_scale;
+    f.v_scale = v_scale;
+    return launch_quest_fused(f, ctx);
 }
 
 int gqa_decode_attn_int4(const gqaq_dims *dims, const gqaq_half *q, const uint8_t *k_codes, const float *k_scales,

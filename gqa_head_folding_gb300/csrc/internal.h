@@ -117,6 +117,9 @@ struct FusedArgs {
     __half *out;
     void *workspace;  // work-queue kernel only
     size_t workspace_bytes;
+    bool kv8;                // caches and bounds hold E4M3 codes (cluster kernel only)
+    float k_inv, v_inv;      // E4M3: appended rows are quantized as fp32(x) * inv
+    float k_scale, v_scale;  // E4M3: value = code value * scale
 };
 int launch_quest_fused(const FusedArgs &a, const LaunchCtx &ctx);
 // The same step as one work queue over the whole GPU (needs the workspace).

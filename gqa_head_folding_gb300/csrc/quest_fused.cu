@@ -95,16 +95,38 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// E4M3 helpers: two fp32 values -> two codes (`lo` in the low byte; round to
+// nearest even, magnitudes beyond 448 saturated), one code's value, and the
+// canonical code of a bound (zero stored as +0).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2_q(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float e4m3_val(uint32_t code) {
+    const uint32_t h = e4m3x2_to_f16x2(code & 0xffu);
+    return __low2float(*reinterpret_cast<const __half2 *>(&h));
+}
+__device__ __forceinline__ uint32_t e4m3_canonical(uint32_t code) { return (code & 0x7fu) == 0u ? 0u : code; }
+
 enum { FUSED_FULL = 0, FUSED_ATTEND = 1 };
 
-template <int D, int G>
+// KV = 0: fp16 cache and fp16 page bounds; KV = 1: E4M3 codes for both (one
+// byte per channel, one scale per tensor).
+template <int D, int G, int KV = 0>
 struct FusedCfg : TileCfg<D, G> {
     using T = TileCfg<D, G>;
+    static constexpr bool KV8 = KV == 1;
     static constexpr int THREADS = (T::NCW + 1) * 32;
+    static constexpr int RB = KV8 ? D : 2 * D;      // bytes of one cached row
+    static constexpr int KREG = T::TILE * RB;       // K part of a stage (V follows)
+    static constexpr int STAGE = 2 * KREG;
     static constexpr int MT = 128;                  // pages per metadata tile
-    static constexpr int NB = 2 * D / 64;           // 128-byte column blocks per [m; M] record
+    static constexpr int NB = 2 * RB / 128;         // 128-byte column blocks per [m; M] record
     static constexpr int MBLK = MT * 128;
-    static_assert(NB * MBLK == T::STAGE, "a metadata tile fills one ring stage");
+    static_assert(NB * MBLK == STAGE, "a metadata tile fills one ring stage");
     static constexpr int KEYS_MAX = 4096;           // pages one CTA scores per unit
     static constexpr int KSEL_MAX = 1024;           // selected pages per unit
     static constexpr int KEYMERGE = (KEYS_MAX * 4 > T::MERGE) ? KEYS_MAX * 4 : T::MERGE;
@@ -116,10 +138,12 @@ struct FusedCfg : TileCfg<D, G> {
     // [768,800), counts [800,808), scan scratch [808,832), scalars [832,848),
     // then the full/empty mbarriers (8-byte aligned) at word 848.
     static constexpr int MISC_BARRIER_WORD = 848;
-    static constexpr int MISC = MISC_BARRIER_WORD * 4 + 2 * 3 * 8;  // full, empty
+    static constexpr int NSTAGE_CAP = 3;  // more E4M3 stages (half as large) measured no faster
+    static constexpr int MISC = MISC_BARRIER_WORD * 4 + 2 * NSTAGE_CAP * 8;  // full, empty
     static constexpr int FIXED = KEYMERGE + QREGION + T::PBYTES + KSEL_MAX * 4 + INBOX + MISC + 1024;
-    static constexpr int NSTAGE = (3 * T::STAGE + FIXED + 1024 <= 226 * 1024) ? 3 : 2;
-    static constexpr int SMEM = 1024 + NSTAGE * T::STAGE + FIXED;
+    static constexpr int NSTAGE_FIT = (226 * 1024 - FIXED - 1024) / STAGE;
+    static constexpr int NSTAGE = NSTAGE_FIT > NSTAGE_CAP ? NSTAGE_CAP : (NSTAGE_FIT < 2 ? 2 : NSTAGE_FIT);
+    static constexpr int SMEM = 1024 + NSTAGE * STAGE + FIXED;
     static_assert(MISC >= MISC_BARRIER_WORD * 4 + 2 * NSTAGE * 8, "misc region holds the mbarriers");
 };
 
@@ -137,13 +161,17 @@ struct FusedParams {
     float scale_log2;
     uint64_t timeout_ns;
     int early_meta;          // FULL: first metadata tiles of the first unit issued before the grid dependency wait
+    float k_inv, v_inv;      // E4M3 cache: appended rows are quantized as fp32(x) * inv
+    float v_scale;           // E4M3 cache: V scale (1 for fp16)
+    float score_scale;       // E4M3 cache: K scale of the scores output (1 for fp16)
 };
 
-template <int D, int G, int MODE>
-__global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
+template <int D, int G, int MODE, int KV = 0>
+__global__ void __launch_bounds__(FusedCfg<D, G, KV>::THREADS, 1)
     quest_fused_kernel(const __grid_constant__ CUtensorMap mmap, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const FusedParams p) {
-    using C = FusedCfg<D, G>;
+    using C = FusedCfg<D, G, KV>;
+    constexpr bool KV8 = KV == 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -246,7 +274,9 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
     };
 
     const uint64_t pol = l2_policy_evict_first();
-    using WA = MmaAttn<D, G, true>;  // tensor-core tile; K and V stages page-major and swizzled
+    // tensor-core tile: fp16 K and V stages page-major and swizzled; E4M3 byte
+    // rows in the layout the 8-bit tile decodes
+    using WA = MmaAttn<D, G, !KV8, KV>;
     WA wa;
     wa.init(warp, lane, smem_u32(pbuf));
     int it = 0;  // position in the stage ring (same sequence in producer and consumers)
@@ -287,6 +317,46 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 auto append = [&]() {
                     constexpr int EPL = D / 32;
                     const int pos = p.pos[b];
+                    if constexpr (KV8) {  // codes of the new rows, then the page's bounds (canonical codes)
+                        const int64_t row = ((int64_t)u * p.Lmax + pos) * D + lane * EPL;
+                        uint8_t *mrow8 = reinterpret_cast<uint8_t *>(p.meta) + ((int64_t)u * p.Pmax + papp) * 2 * D;
+                        uint32_t kw = 0, vw = 0;
+#pragma unroll
+                        for (int e = 0; e < EPL; e += 2) {
+                            const float2 kf = __half22float2(*reinterpret_cast<const __half2 *>(p.k_new + (int64_t)u * D + lane * EPL + e));
+                            const float2 vf = __half22float2(*reinterpret_cast<const __half2 *>(p.v_new + (int64_t)u * D + lane * EPL + e));
+                            kw |= f32x2_to_e4m3x2_q(kf.x * p.k_inv, kf.y * p.k_inv) << (8 * e);
+                            vw |= f32x2_to_e4m3x2_q(vf.x * p.v_inv, vf.y * p.v_inv) << (8 * e);
+                        }
+                        uint8_t *kc = reinterpret_cast<uint8_t *>(p.k_cache) + row;
+                        uint8_t *vc = reinterpret_cast<uint8_t *>(p.v_cache) + row;
+                        if (EPL == 4) {
+                            *reinterpret_cast<uint32_t *>(kc) = kw;
+                            *reinterpret_cast<uint32_t *>(vc) = vw;
+                        } else {
+                            *reinterpret_cast<uint16_t *>(kc) = (uint16_t)kw;
+                            *reinterpret_cast<uint16_t *>(vc) = (uint16_t)vw;
+                        }
+                        const bool fresh8 = (pos % p.S) == 0;
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) {
+                            const int c = lane * EPL + e;
+                            const uint32_t code = (kw >> (8 * e)) & 0xffu;
+                            uint32_t mn = e4m3_canonical(code), mx = mn;
+                            if (!fresh8) {
+                                const uint32_t om = mrow8[c], oM = mrow8[D + c];
+                                const float x = e4m3_val(code);
+                                mn = x < e4m3_val(om) ? mn : om;
+                                mx = x > e4m3_val(oM) ? mx : oM;
+                            }
+                            mrow8[c] = (uint8_t)mn;
+                            mrow8[D + c] = (uint8_t)mx;
+                        }
+                        fence_proxy_async_global();  // the TMA reads below see these rows
+                        __syncwarp();
+                        fence_proxy_async_global();
+                        return;
+                    }
                     const int64_t row = (int64_t)u * p.Lmax + pos;
                     __half *mrow = p.meta + ((int64_t)u * p.Pmax + papp) * 2 * D;
                     const bool fresh = (pos % p.S) == 0;
@@ -348,7 +418,11 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const int c = ks * 16 + k0 + 8 * h;  // record channel: c < D is the min side
+                            // record channel of this fragment: c < D is the min side. The
+                            // E4M3 record is read as whole 16-byte chunks per lane, so its
+                            // contraction order is permuted: k-step ks of column pair
+                            // lane%4 covers channels (D/2)(lane%4) + 4 ks .. + 3.
+                            const int c = KV8 ? (D / 2) * (lane & 3) + 4 * ks + 2 * h : ks * 16 + k0 + 8 * h;
                             uint32_t v = 0u;
                             if (n < G) {
                                 const uint32_t pr = *reinterpret_cast<const uint32_t *>(qg + n * D + (c < D ? c : c - D));
@@ -371,15 +445,43 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                     const uint32_t sbase = smem_u32(ring + s * C::STAGE);
                     const int first = pr0 + t * C::MT + warp * 16;  // this warp's 16 pages
                     if (ok && first < pr1) {                        // warp-uniform
-                        const int arow = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);  // ldmatrix row address
-                        const uint32_t abase = sbase + (uint32_t)(arow * 128);
                         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        if constexpr (KV8) {
+                            // A fragments decoded from the code bytes: page rows r and r + 8
+                            // of the warp's 16, this lane's D/2 bytes of each record
+                            constexpr int NCH = D / 32;  // 16-byte chunks per lane and row
+                            const int ra = warp * 16 + (lane >> 2), rb = ra + 8;
+                            uint4 xa[NCH], xb[NCH];
 #pragma unroll
-                        for (int ks = 0; ks < KS; ++ks) {
-                            const uint32_t c16 = (uint32_t)((ks & 3) * 2 + (lane >> 4));
-                            uint32_t af[4];
-                            ldsm_x4(abase + (uint32_t)((ks >> 2) * C::MBLK) + ((c16 ^ (uint32_t)(arow & 7)) << 4), af);
-                            mma_16816(acc, af, qb[ks][0], qb[ks][1]);
+                            for (int h = 0; h < NCH; ++h) {
+                                const int x = (D / 2) * (lane & 3) + 16 * h;  // record byte
+                                const uint32_t blk = sbase + (uint32_t)((x >> 7) * C::MBLK);
+                                const uint32_t cx = (uint32_t)((x & 127) >> 4);
+                                xa[h] = lds128(blk + (uint32_t)(ra * 128) + ((cx ^ (uint32_t)(ra & 7)) << 4));
+                                xb[h] = lds128(blk + (uint32_t)(rb * 128) + ((cx ^ (uint32_t)(rb & 7)) << 4));
+                            }
+#pragma unroll
+                            for (int ks = 0; ks < KS; ++ks) {
+                                const uint4 &ua = xa[ks >> 2], &ub = xb[ks >> 2];
+                                const uint32_t wa = (ks & 3) == 0 ? ua.x : (ks & 3) == 1 ? ua.y : (ks & 3) == 2 ? ua.z : ua.w;
+                                const uint32_t wb = (ks & 3) == 0 ? ub.x : (ks & 3) == 1 ? ub.y : (ks & 3) == 2 ? ub.z : ub.w;
+                                uint32_t af[4];
+                                af[0] = e4m3x2_to_f16x2(wa & 0xffffu);
+                                af[1] = e4m3x2_to_f16x2(wb & 0xffffu);
+                                af[2] = e4m3x2_to_f16x2(wa >> 16);
+                                af[3] = e4m3x2_to_f16x2(wb >> 16);
+                                mma_16816(acc, af, qb[ks][0], qb[ks][1]);
+                            }
+                        } else {
+                            const int arow = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);  // ldmatrix row address
+                            const uint32_t abase = sbase + (uint32_t)(arow * 128);
+#pragma unroll
+                            for (int ks = 0; ks < KS; ++ks) {
+                                const uint32_t c16 = (uint32_t)((ks & 3) * 2 + (lane >> 4));
+                                uint32_t af[4];
+                                ldsm_x4(abase + (uint32_t)((ks >> 2) * C::MBLK) + ((c16 ^ (uint32_t)(arow & 7)) << 4), af);
+                                mma_16816(acc, af, qb[ks][0], qb[ks][1]);
+                            }
                         }
                         // C fragment: rows lane/4 and lane/4 + 8, columns 2*(lane%4) + {0, 1}
                         const int g0 = 2 * (lane & 3);
@@ -402,7 +504,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                                 } else {
                                     keys[page - pr0] = key;
                                 }
-                                if (p.scores != nullptr) p.scores[(int64_t)u * p.Pmax + page] = best;
+                                if (p.scores != nullptr) p.scores[(int64_t)u * p.Pmax + page] = best * p.score_scale;
                             }
                         }
                     }
@@ -806,16 +908,30 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 if (page >= 0 && page < P) {
                     const int nv = slots.warp_rows(warp, page, len);
                     const int64_t tok0 = (int64_t)u * p.Lmax + (int64_t)page * p.S + (16 * warp) % slots.slot;
-                    const uint32_t kb = smem_u32(ring + (t % C::NSTAGE) * C::STAGE), vb = kb + C::KBYTES;
-                    constexpr int CPR = D / 8;  // 16-byte chunks per row
-                    for (int idx = lane; idx < nv * CPR; idx += 32) {
-                        const int i = idx / CPR, c = idx - (idx / CPR) * CPR;
-                        const int row = 16 * warp + i;  // stage row
-                        const int line = row * C::KH + (c >> 3);
-                        cp_async16(kb + (uint32_t)(line * 128 + (((c & 7) ^ (line & 7)) << 4)),
-                                   p.k_cache + (tok0 + i) * D + c * 8);
-                        cp_async16(vb + (uint32_t)(line * 128 + (((c & 7) ^ (line & 7)) << 4)),
-                                   p.v_cache + (tok0 + i) * D + c * 8);
+                    const uint32_t kb = smem_u32(ring + (t % C::NSTAGE) * C::STAGE), vb = kb + C::KREG;
+                    if constexpr (KV8) {  // byte rows: 128-byte swizzle at D = 128, 64-byte at D = 64
+                        constexpr int CPR = D / 16;
+                        const uint8_t *kg = reinterpret_cast<const uint8_t *>(p.k_cache);
+                        const uint8_t *vg = reinterpret_cast<const uint8_t *>(p.v_cache);
+                        for (int idx = lane; idx < nv * CPR; idx += 32) {
+                            const int i = idx / CPR, c = idx - (idx / CPR) * CPR;
+                            const int row = 16 * warp + i;
+                            const uint32_t off = D == 128 ? (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4))
+                                                          : (uint32_t)(row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                            cp_async16(kb + off, kg + (tok0 + i) * D + c * 16);
+                            cp_async16(vb + off, vg + (tok0 + i) * D + c * 16);
+                        }
+                    } else {
+                        constexpr int CPR = D / 8;  // 16-byte chunks per row
+                        for (int idx = lane; idx < nv * CPR; idx += 32) {
+                            const int i = idx / CPR, c = idx - (idx / CPR) * CPR;
+                            const int row = 16 * warp + i;  // stage row
+                            const int line = row * C::KH + (c >> 3);
+                            cp_async16(kb + (uint32_t)(line * 128 + (((c & 7) ^ (line & 7)) << 4)),
+                                       p.k_cache + (tok0 + i) * D + c * 8);
+                            cp_async16(vb + (uint32_t)(line * 128 + (((c & 7) ^ (line & 7)) << 4)),
+                                       p.v_cache + (tok0 + i) * D + c * 8);
+                        }
                     }
                 }
                 cp_async_commit();
@@ -832,7 +948,7 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                 if (nv > 0 && live) {
                     const uint32_t kbase = smem_u32(ring + (t % C::NSTAGE) * C::STAGE);
                     const int nvs[1] = {nv};
-                    wa.template tile_n<1>(kbase, kbase + C::KBYTES, 16 * warp, nvs, p.scale_log2);
+                    wa.template tile_n<1>(kbase, kbase + C::KREG, 16 * warp, nvs, p.scale_log2);
                 }
                 __syncwarp();  // the slice is free before tile t + NSTAGE lands in it
                 fetch(t + C::NSTAGE);
@@ -883,7 +999,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
                         as += f * inbox[r * rec + 2 * G + idx - i0];
                     }
                 }
-                p.out[((int64_t)b * Hq + (int64_t)kv * G + g) * D + d] = __float2half_rn(ls > 0.f ? as / ls : 0.f);
+                p.out[((int64_t)b * Hq + (int64_t)kv * G + g) * D + d] =
+                    __float2half_rn(ls > 0.f ? p.v_scale * (as / ls) : 0.f);
             }
         }
         // Before the next unit reuses keys, list and inbox. After the last unit no
@@ -910,13 +1027,13 @@ __global__ void __launch_bounds__(FusedCfg<D, G>::THREADS, 1)
 namespace {
 constexpr int kMaxDev = 64;
 
-template <int D, int G, int MODE>
+template <int D, int G, int MODE, int KV>
 int active_clusters(int device, int csize, int *out) {
-    using C = FusedCfg<D, G>;
+    using C = FusedCfg<D, G, KV>;
     static int cache[kMaxDev][4] = {};
     static bool attr[kMaxDev] = {};
     const int ci = csize == 1 ? 0 : csize == 2 ? 1 : csize == 4 ? 2 : 3;
-    auto kern = quest_fused_kernel<D, G, MODE>;
+    auto kern = quest_fused_kernel<D, G, MODE, KV>;
     if (!attr[device]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return GQAQ_ERR_CUDA;
@@ -942,9 +1059,9 @@ int active_clusters(int device, int csize, int *out) {
     return GQAQ_OK;
 }
 
-template <int D, int G, int MODE>
+template <int D, int G, int MODE, int KV>
 int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
-    using C = FusedCfg<D, G>;
+    using C = FusedCfg<D, G, KV>;
     const gqaq_dims &dm = *a.dims;
     const int Pmax = (dm.max_len + dm.page_size - 1) / dm.page_size;
     const int units = dm.batch * dm.num_kv_heads;
@@ -957,7 +1074,7 @@ int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
         if (MODE == FUSED_FULL && (Pmax + csize - 1) / csize > C::KEYS_MAX) continue;
         if (ctx.cluster_size > 0 && csize != ctx.cluster_size) continue;
         int n = 0;
-        if (active_clusters<D, G, MODE>(ctx.device, csize, &n) != GQAQ_OK) return GQAQ_ERR_CUDA;
+        if (active_clusters<D, G, MODE, KV>(ctx.device, csize, &n) != GQAQ_OK) return GQAQ_ERR_CUDA;
         if (n <= 0) continue;
         if (ctx.max_ctas > 0) n = n < ctx.max_ctas / csize ? n : (ctx.max_ctas / csize > 0 ? ctx.max_ctas / csize : 1);
         const double cost = (double)((units + n - 1) / n) / csize;
@@ -974,12 +1091,18 @@ int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
     CUtensorMap mmap, kmap, vmap;
     if (MODE == FUSED_FULL) {
         const uint64_t mrows = (uint64_t)dm.batch * dm.num_kv_heads * Pmax;
-        if (!encode_tensor_map_2d(&mmap, a.meta, mrows, 2 * D, 64, C::MT, true)) return GQAQ_ERR_CUDA;
+        // a bounds record of 2*RB bytes read as RB halves; 128-byte boxes
+        if (!encode_tensor_map_2d(&mmap, a.meta, mrows, C::RB, 64, C::MT, true)) return GQAQ_ERR_CUDA;
     } else {
         memset(&mmap, 0, sizeof(mmap));
     }
-    if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, (uint32_t)dm.page_size)) return GQAQ_ERR_CUDA;
-    if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, (uint32_t)dm.page_size, false)) return GQAQ_ERR_CUDA;
+    if (KV == 1) {  // byte rows
+        if (!encode_tensor_map_u8(&kmap, a.k_cache, rows, D, (uint32_t)dm.page_size, 0)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_u8(&vmap, a.v_cache, rows, D, (uint32_t)dm.page_size, 0)) return GQAQ_ERR_CUDA;
+    } else {
+        if (!encode_tensor_map_kpage(&kmap, a.k_cache, rows, D, (uint32_t)dm.page_size)) return GQAQ_ERR_CUDA;
+        if (!encode_tensor_map_2d(&vmap, a.v_cache, rows, D, D, (uint32_t)dm.page_size, false)) return GQAQ_ERR_CUDA;
+    }
 
     FusedParams p;
     p.q = a.q;
@@ -1000,33 +1123,40 @@ int launch_fused_t(const FusedArgs &a, const LaunchCtx &ctx) {
     p.Pmax = Pmax;
     p.S = dm.page_size;
     p.kpages = a.kpages;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.scale_log2 = a.scale * (KV == 1 ? a.k_scale : 1.f) * 1.4426950408889634f;
     p.timeout_ns = ctx.timeout_ns;
     p.early_meta = ctx.quest_early_meta;
+    p.k_inv = KV == 1 ? a.k_inv : 1.f;
+    p.v_inv = KV == 1 ? a.v_inv : 1.f;
+    p.v_scale = KV == 1 ? a.v_scale : 1.f;
+    p.score_scale = KV == 1 ? a.k_scale : 1.f;
 
-    if (launch_kernel(quest_fused_kernel<D, G, MODE>, dim3(nclusters * best_c), dim3(C::THREADS), C::SMEM, ctx, best_c,
+    if (launch_kernel(quest_fused_kernel<D, G, MODE, KV>, dim3(nclusters * best_c), dim3(C::THREADS), C::SMEM, ctx, best_c,
                       mmap, kmap, vmap, p) != cudaSuccess)
         return GQAQ_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GQAQ_OK : GQAQ_ERR_CUDA;
 }
 
-template <int D, int MODE>
+template <int D, int MODE, int KV>
 int fused_g(const FusedArgs &a, const LaunchCtx &ctx) {
     switch (a.dims->num_q_heads / a.dims->num_kv_heads) {
-        case 1: return launch_fused_t<D, 1, MODE>(a, ctx);
-        case 2: return launch_fused_t<D, 2, MODE>(a, ctx);
-        case 4: return launch_fused_t<D, 4, MODE>(a, ctx);
-        case 8: return launch_fused_t<D, 8, MODE>(a, ctx);
+        case 1: return launch_fused_t<D, 1, MODE, KV>(a, ctx);
+        case 2: return launch_fused_t<D, 2, MODE, KV>(a, ctx);
+        case 4: return launch_fused_t<D, 4, MODE, KV>(a, ctx);
+        case 8: return launch_fused_t<D, 8, MODE, KV>(a, ctx);
         default: return GQAQ_ERR_UNSUPPORTED;
     }
+}
+template <int D, int KV>
+int fused_mode(const FusedArgs &a, const LaunchCtx &ctx) {
+    return a.meta == nullptr ? fused_g<D, FUSED_ATTEND, KV>(a, ctx) : fused_g<D, FUSED_FULL, KV>(a, ctx);
 }
 }  // namespace
 
 int launch_quest_fused(const FusedArgs &a, const LaunchCtx &ctx) {
-    const bool attend_only = a.meta == nullptr;
     switch (a.dims->head_dim) {
-        case 64: return attend_only ? fused_g<64, FUSED_ATTEND>(a, ctx) : fused_g<64, FUSED_FULL>(a, ctx);
-        case 128: return attend_only ? fused_g<128, FUSED_ATTEND>(a, ctx) : fused_g<128, FUSED_FULL>(a, ctx);
+        case 64: return a.kv8 ? fused_mode<64, 1>(a, ctx) : fused_mode<64, 0>(a, ctx);
+        case 128: return a.kv8 ? fused_mode<128, 1>(a, ctx) : fused_mode<128, 0>(a, ctx);
         default: return GQAQ_ERR_UNSUPPORTED;
     }
 }

@@ -12,9 +12,9 @@ With ``kv="e4m3"`` the caches hold 8-bit E4M3 codes with one fp32 scale per
 tensor (``Layer.k_scale`` / ``v_scale``): appends quantize
 (``kv_append_e4m3``, or ``quest_append_kv_e4m3`` when the layer keeps page
 bounds), dense layers read them through ``gqa_decode_attn_e4m3`` and Quest
-layers run the step-by-step calls over E4M3 page bounds
-(``quest_score_pages_e4m3``, ``quest_topk_pages``, ``quest_sparse_attn_e4m3``;
-the fused kernel reads fp16 caches only). With ``kv="int4"`` they hold 4-bit
+layers over E4M3 page bounds run as one ``quest_decode_attn_e4m3`` launch
+(or, with ``fused=False``, ``quest_score_pages_e4m3``, ``quest_topk_pages``
+and ``quest_sparse_attn_e4m3``). With ``kv="int4"`` they hold 4-bit
 levels ``[B,Hkv,Lmax,D/2]`` with one fp32 scale per token row
 (``Layer.k_scales`` / ``v_scales``), through ``kv_append_int4`` and
 ``gqa_decode_attn_int4``; an INT4 stack must be all dense.
@@ -37,7 +37,7 @@ import torch
 
 from . import (alloc_workspace, gqa_decode_attn, gqa_decode_attn_e4m3, gqa_decode_attn_int4, kv_append_e4m3,
                kv_append_int4, make_dims, new_meta, new_meta_e4m3, num_pages, quest_append_kv, quest_append_kv_e4m3,
-               quest_decode_attn, quest_score_pages, quest_score_pages_e4m3, quest_sparse_attn, quest_sparse_attn_e4m3,
+               quest_decode_attn, quest_decode_attn_e4m3, quest_score_pages, quest_score_pages_e4m3, quest_sparse_attn, quest_sparse_attn_e4m3,
                quest_topk_pages, quest_update_meta, quest_update_meta_e4m3)
 
 
@@ -88,8 +88,6 @@ class DecodeStack:
             raise ValueError(f"kv must be 'f16', 'e4m3' or 'int4', got {kv!r}")
         if kv == "int4" and k_pages is not None and (num_layers is None or num_layers > dense_layers):
             raise ValueError("a 4-bit cache runs dense layers only")
-        if kv == "e4m3":
-            fused = False                  # Quest layers over E4M3 bounds run as the step-by-step calls
         self.fused, self.kv = fused, kv
         self.batch, self.num_q_heads, self.num_kv_heads = batch, num_q_heads, num_kv_heads
         self.head_dim, self.max_len, self.page_size = head_dim, max_len, page_size
@@ -149,6 +147,11 @@ class DecodeStack:
             return lambda: self.append(L)
         if name == "dense":
             return lambda: self.dense(L)
+        if name == "quest" and self.kv == "e4m3":
+            return lambda: quest_decode_attn_e4m3(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages,
+                                                  self.scale, L.k_scale, L.v_scale, k_new=L.k_new, v_new=L.v_new,
+                                                  pos=L.pos, k_inv_scale=1.0 / L.k_scale, v_inv_scale=1.0 / L.v_scale,
+                                                  out=L.out, page_idx=L.page_idx, page_size=self.page_size)
         if name == "quest":
             return lambda: quest_decode_attn(L.q, L.k_cache, L.v_cache, L.meta, L.valid_len, self.k_pages,
                                              self.scale, k_new=L.k_new, v_new=L.v_new, pos=L.pos, out=L.out,

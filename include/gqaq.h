@@ -292,6 +292,20 @@ GQAQ_API int quest_sparse_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, c
                                     const int32_t *page_idx, int k, float scale, gqaq_half *out, void *workspace,
                                     size_t workspace_bytes, void *stream);
 
+/* quest_decode_attn over an E4M3 cache, in one launch: the optional append
+ * (quest_append_kv_e4m3's codes and bounds, with k_inv_scale / v_inv_scale),
+ * quest_score_pages_e4m3's scores, quest_topk_pages' selection and
+ * quest_sparse_attn_e4m3's attention over the selected pages. scores (times
+ * k_scale) and page_idx are optional outputs as in quest_decode_attn. The
+ * cluster kernel only: k <= 1024 (else GQAQ_ERR_UNSUPPORTED) and no
+ * workspace; GQAQ_OPT_QUEST_EARLY_META applies as for quest_decode_attn.
+ * k_scale must be finite and > 0. */
+GQAQ_API int quest_decode_attn_e4m3(const gqaq_dims *dims, const gqaq_half *q, uint8_t *k_cache, uint8_t *v_cache,
+                                    uint8_t *meta, const gqaq_half *k_new, const gqaq_half *v_new,
+                                    const int32_t *pos, float k_inv_scale, float v_inv_scale, float k_scale,
+                                    float v_scale, const int32_t *valid_len, int k, float scale, gqaq_half *out,
+                                    float *scores, int32_t *page_idx, void *stream);
+
 /* The 4-bit KV-cache variant (a format chosen here, see above: the plainest
  * one that keeps both contractions exact on integer levels): symmetric
  * INT4 with one fp32 scale per (token, KV head) row.

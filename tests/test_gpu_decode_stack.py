@@ -181,16 +181,17 @@ def test_benchmark_step_at_full_size_sampled():
             assert_attn_close(out, oracle.sparse_attn(q, k, v, vl, sel, S, scale), f"layer {l} kv {kv}")
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "step-by-step"])
 @pytest.mark.parametrize("G", [1, 4])
-def test_decode_stack_over_an_e4m3_cache_matches_oracle(G):
+def test_decode_stack_over_an_e4m3_cache_matches_oracle(G, fused):
     """The same stack over an E4M3 cache (per-tensor scales): dense layers
-    through gqa_decode_attn_e4m3, Quest layers as the step-by-step E4M3 calls
-    (appends keep the pages' E4M3 bounds), graph-replayed three steps with
-    programmatic launch and early K/V reads."""
+    through gqa_decode_attn_e4m3, Quest layers as one quest_decode_attn_e4m3
+    launch or the step-by-step E4M3 calls (appends keep the pages' E4M3
+    bounds), graph-replayed three steps with programmatic launch and both
+    early-read options."""
     w, xs, knew, vnew, vls = draw(G)
     stack = DecodeStack(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_len, w.k_pages,
-                        w.dense_layers, DEV, S, kv="e4m3", num_layers=w.num_layers)
-    assert not stack.fused
+                        w.dense_layers, DEV, S, kv="e4m3", num_layers=w.num_layers, fused=fused)
     layers, host = [], []
     for l, x in enumerate(xs):
         ks = float(x["k_cache"].float().abs().max()) / 448.0

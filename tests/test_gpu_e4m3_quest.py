@@ -175,3 +175,81 @@ def test_invalid_arguments_are_rejected():
         assert e.value.status == g.GQAQ_ERR_INVALID_ARG
     with pytest.raises(g.GqaqError):
         g.quest_update_meta_e4m3(d, vl, meta, page_begin=3, page_end=2)
+
+
+@pytest.fixture
+def _reset_cluster():
+    yield
+    g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, 0)
+    g.set_option(g.GQAQ_OPT_QUEST_EARLY_META, 0)
+
+
+@pytest.mark.parametrize("D,G,K,csize,S", [
+    (128, 4, 8, 0, 16), (128, 1, 16, 4, 16), (128, 4, 16, 2, 16), (64, 2, 40, 8, 16), (128, 8, 3, 1, 16),
+    (64, 8, 7, 4, 16), (128, 2, 12, 2, 8), (128, 4, 6, 4, 32), (64, 1, 5, 2, 64),
+])
+def test_fused_step_over_an_e4m3_cache(D, G, K, csize, S, _reset_cluster):
+    """quest_decode_attn_e4m3: append (codes and bounds bit exact), scores
+    (times the K scale), page list and attention in one launch, cluster sizes
+    1-8 forced, page sizes 8-64, a decode loop of three steps with early
+    metadata reads crossing page starts."""
+    g.set_option(g.GQAQ_OPT_CLUSTER_SIZE, csize)
+    g.set_option(g.GQAQ_OPT_QUEST_EARLY_META, 1)
+    B, Hkv = 3, 2
+    Lmax = S * 45 + 3
+    x, kc, vc, ks, vs = e4m3_layer(B, G, Hkv, D, Lmax, seed=D + 7 * G + K + csize + S, S=S)
+    valid0 = np.array([S * 30 - 1, S * 23 + 1, 20])
+    kd, vd = dev(kc), dev(vc)
+    meta = g.new_meta_e4m3(B, Hkv, Lmax, D, DEV, page_size=S)
+    g.quest_update_meta_e4m3(kd, dev((valid0 - 1).astype(np.int32)), meta, page_size=S)
+    gen = torch.Generator().manual_seed(D + G)
+    scale = 1.0 / math.sqrt(D)
+    q = x["q"].numpy()
+    Pm = g.num_pages(Lmax, S)
+    for step in range(3):
+        vl = valid0 + step
+        kn = torch.randn(B, Hkv, D, generator=gen).to(torch.float16)
+        vn = torch.randn(B, Hkv, D, generator=gen).to(torch.float16)
+        scores = torch.full((B, Hkv, Pm), float("nan"), dtype=torch.float32, device=DEV)
+        idx = torch.full((B, Hkv, K), -7, dtype=torch.int32, device=DEV)
+        out = g.quest_decode_attn_e4m3(x["q"].to(DEV), kd, vd, meta, dev(vl.astype(np.int32)), K, scale, ks, vs,
+                                       k_new=kn.to(DEV), v_new=vn.to(DEV), pos=dev((vl - 1).astype(np.int32)),
+                                       k_inv_scale=1.0 / ks, v_inv_scale=1.0 / vs, scores=scores, page_idx=idx,
+                                       page_size=S)
+        torch.cuda.synchronize()
+        assert g.device_status() == 0
+        for b in range(B):
+            kc[b, :, vl[b] - 1] = oracle.quantize_e4m3(kn[b].numpy(), 1.0 / ks)
+            vc[b, :, vl[b] - 1] = oracle.quantize_e4m3(vn[b].numpy(), 1.0 / vs)
+        assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(vd.cpu().numpy(), vc)
+        ref_meta = oracle.page_minmax_e4m3(kc, vl, S)
+        got_meta = meta.cpu().numpy()
+        bounds = oracle.e4m3_to_f64(ref_meta) * ks
+        ref_scores = oracle.page_scores(q, bounds, vl, S)
+        tol = score_tolerance(oracle.f16_to_f64(q), np.nan_to_num(bounds), G)
+        got = scores.cpu().numpy().astype(np.float64)
+        for b in range(B):
+            P = (vl[b] + S - 1) // S
+            assert np.array_equal(got_meta[b, :, :P], ref_meta[b, :, :P]), f"bounds step {step} b={b}"
+            assert np.all(np.abs(got[b, :, :P] - ref_scores[b, :, :P]) <= tol[b, :, :P]), f"scores step {step} b={b}"
+        sel = idx.cpu().numpy()
+        check_topk(sel, ref_scores, vl, S, K)
+        assert_attn_close(out, oracle.sparse_attn(q, oracle.e4m3_to_f64(kc) * ks, oracle.e4m3_to_f64(vc) * vs, vl,
+                                                  sel, S, scale), f"step {step}")
+
+
+def test_sparse_attention_above_the_fused_page_limit():
+    # k > 1024 selected pages: the split-context kernel gathers E4M3 page boxes
+    B, G, Hkv, D, S, K = 1, 4, 2, 64, 16, 1100
+    Lmax = 16 * 1200
+    x, kc, vc, ks, vs = e4m3_layer(B, G, Hkv, D, Lmax, seed=41, n_plant=0)
+    rng = np.random.default_rng(4)
+    sel = np.sort(np.stack([rng.choice(1200, K, replace=False) for _ in range(Hkv)]), axis=1)[None].astype(np.int32)
+    valid = np.array([Lmax])
+    out = g.quest_sparse_attn_e4m3(x["q"].to(DEV), dev(kc), dev(vc), ks, vs, dev(valid.astype(np.int32)), dev(sel),
+                                   0.125)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    ref = oracle.sparse_attn(x["q"].numpy(), oracle.e4m3_to_f64(kc) * ks, oracle.e4m3_to_f64(vc) * vs, valid, sel, S,
+                             0.125)
+    assert_attn_close(out, ref)
