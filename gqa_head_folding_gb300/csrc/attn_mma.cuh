@@ -9,9 +9,12 @@
 //   S^T [16 tokens x 8 rows] = K [16 x D] . Q^T [D x 8]          (D/16 MMAs)
 //   O^T [D x 8 rows]        += V^T [D x 16 tokens] . P^T [16 x 8] (D/16 MMAs)
 // Softmax runs in the log2 domain on the S^T fragments (each lane holds two
-// query columns of two tokens), P is rounded to fp16 once and turned into the
-// B operand of the second product with movmatrix.trans. Rows G..7 of the N
-// side are zero queries whose results are never stored.
+// query columns of two tokens) against a lazy reference max: the column max
+// is gathered across lanes, and l and O rescaled, only when a tile holds a
+// score more than 2^8 above the reference, so P <= 256. P is rounded to fp16
+// once and turned into the B operand of the second product with
+// movmatrix.trans. Rows G..7 of the N side are zero queries whose results are
+// never stored.
 //
 // fp16 caches: K and V stages share one layout, KH column blocks of 128-byte
 // lines, 128-byte swizzled (dense: [kh][row] blocks of TILE lines; KPAGE:
@@ -209,10 +212,8 @@ struct MmaAttn {
                 const uint32_t wa = (j & 3) == 0 ? xa.x : (j & 3) == 1 ? xa.y : (j & 3) == 2 ? xa.z : xa.w;
                 const uint32_t wb = (j & 3) == 0 ? xb.x : (j & 3) == 1 ? xb.y : (j & 3) == 2 ? xb.z : xb.w;
                 uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(wa & 0xffffu);
-                a[1] = e4m3x2_to_f16x2(wb & 0xffffu);
-                a[2] = e4m3x2_to_f16x2(wa >> 16);
-                a[3] = e4m3x2_to_f16x2(wb >> 16);
+                e4m3x4_to_f16x2x2(wa, a[0], a[2]);
+                e4m3x4_to_f16x2x2(wb, a[1], a[3]);
                 mma_16816(s, a, qb[j][0], qb[j][1]);
             }
         } else {
@@ -291,10 +292,8 @@ struct MmaAttn {
                 const uint32_t lo = byte_perm(w[0][wd], w[1][wd], sel);  // tokens 2c, 2c+1
                 const uint32_t hi = byte_perm(w[2][wd], w[3][wd], sel);  // tokens 2c+8, 2c+9
                 uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(lo & 0xffffu);
-                a[1] = e4m3x2_to_f16x2(lo >> 16);
-                a[2] = e4m3x2_to_f16x2(hi & 0xffffu);
-                a[3] = e4m3x2_to_f16x2(hi >> 16);
+                e4m3x4_to_f16x2x2(lo, a[0], a[1]);
+                e4m3x4_to_f16x2x2(hi, a[2], a[3]);
                 if (partial) mask_tokens(a, mk0, mk1);
                 mma_16816(o[i], a, pb0, pb1);
             }
@@ -323,43 +322,42 @@ struct MmaAttn {
         float s[NS][4];
 #pragma unroll
         for (int h = 0; h < NS; ++h) qk(kbase, row0 + 16 * h, s[h]);
-        // ---- 2. online softmax per query column (log2 domain) ----
+        // ---- 2. online softmax per query column (log2 domain), lazy reference max ----
         // s[h][0], s[h][1]: token r of sub-tile h, columns 2c, 2c+1; s[h][2], s[h][3]: token r + 8.
+        // m is a reference max shared by the 8 lanes of a column pair; it moves (with
+        // the rescale of l and O) only when some score exceeds it by more than 2^8,
+        // so every P = 2^(s - m) stays at most 256 and fp16 keeps its precision.
         bool v0[NS], v1[NS];
         float t0 = -INFINITY, t1 = -INFINITY;
 #pragma unroll
         for (int h = 0; h < NS; ++h) {
             v0[h] = r < nv[h];
             v1[h] = r + 8 < nv[h];
-            s[h][0] = v0[h] ? s[h][0] * scale_log2 : -INFINITY;
-            s[h][1] = v0[h] ? s[h][1] * scale_log2 : -INFINITY;
-            s[h][2] = v1[h] ? s[h][2] * scale_log2 : -INFINITY;
-            s[h][3] = v1[h] ? s[h][3] * scale_log2 : -INFINITY;
+            s[h][0] *= scale_log2;
+            s[h][1] *= scale_log2;
+            s[h][2] *= scale_log2;
+            s[h][3] *= scale_log2;
+            if (nv[h] < C::SUB) {  // warp-uniform: a sub-tile with rows past the valid prefix
+                s[h][0] = v0[h] ? s[h][0] : -INFINITY;
+                s[h][1] = v0[h] ? s[h][1] : -INFINITY;
+                s[h][2] = v1[h] ? s[h][2] : -INFINITY;
+                s[h][3] = v1[h] ? s[h][3] : -INFINITY;
+            }
             t0 = fmaxf(t0, fmaxf(s[h][0], s[h][2]));
             t1 = fmaxf(t1, fmaxf(s[h][1], s[h][3]));
         }
+        if (__any_sync(0xffffffffu, t0 > m[0] + 8.f || t1 > m[1] + 8.f)) {
 #pragma unroll
-        for (int o_ = 4; o_ < 32; o_ <<= 1) {
-            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o_));
-            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o_));
-        }
-        const float mn0 = fmaxf(m[0], t0), mn1 = fmaxf(m[1], t1);  // some token is valid: finite
-        const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
-        m[0] = mn0;
-        m[1] = mn1;
-        float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-        for (int h = 0; h < NS; ++h) {
-            s[h][0] = fast_exp2(s[h][0] - mn0);
-            s[h][1] = fast_exp2(s[h][1] - mn1);
-            s[h][2] = fast_exp2(s[h][2] - mn0);
-            s[h][3] = fast_exp2(s[h][3] - mn1);
-            ps0 += s[h][0] + s[h][2];
-            ps1 += s[h][1] + s[h][3];
-        }
-        l[0] = l[0] * al0 + ps0;
-        l[1] = l[1] * al1 + ps1;
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+            for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o_));
+                t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o_));
+            }
+            const float mn0 = fmaxf(m[0], t0), mn1 = fmaxf(m[1], t1);  // some token is valid: finite
+            const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
+            m[0] = mn0;
+            m[1] = mn1;
+            l[0] *= al0;
+            l[1] *= al1;
 #pragma unroll
             for (int i = 0; i < KS; ++i) {
                 o[i][0] *= al0;
@@ -368,6 +366,18 @@ struct MmaAttn {
                 o[i][3] *= al1;
             }
         }
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < NS; ++h) {
+            s[h][0] = fast_exp2(s[h][0] - m[0]);
+            s[h][1] = fast_exp2(s[h][1] - m[1]);
+            s[h][2] = fast_exp2(s[h][2] - m[0]);
+            s[h][3] = fast_exp2(s[h][3] - m[1]);
+            ps0 += s[h][0] + s[h][2];
+            ps1 += s[h][1] + s[h][3];
+        }
+        l[0] += ps0;
+        l[1] += ps1;
         // ---- 3. P^T as the B operand: fp16, transposed 8x8 halves; 4. O^T += V^T . P^T ----
 #pragma unroll
         for (int h = 0; h < NS; ++h) {

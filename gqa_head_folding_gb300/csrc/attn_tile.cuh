@@ -64,6 +64,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
     return r;
 }
 
+// Four E4M3 codes (byte 0 first) -> two fp16x2: lo holds bytes 0, 1 and hi
+// bytes 2, 3. The word is split into its 16-bit halves as registers, so no
+// mask or shift is spent on either half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 // K layout in a stage: KPAGE = false: KH column blocks of TILE rows x 128 B
 // ([kh][row]); KPAGE = true: row after row, each row's KH 128-byte blocks
 // side by side ([row][kh]), as one 3-D TMA box per page writes them. Both
@@ -191,8 +200,8 @@ struct WarpAttn {
                     if (KV8) {  // one 16-byte chunk of codes feeds two fp16 chunks of q
                         if ((c & 1) == 0) k8 = lds128(kro + ((kx0 ^ (uint32_t)(c >> 1)) << 4));
                         const uint32_t lo = (c & 1) ? k8.z : k8.x, hi = (c & 1) ? k8.w : k8.y;
-                        kc = make_uint4(e4m3x2_to_f16x2(lo & 0xffffu), e4m3x2_to_f16x2(lo >> 16),
-                                        e4m3x2_to_f16x2(hi & 0xffffu), e4m3x2_to_f16x2(hi >> 16));
+                        e4m3x4_to_f16x2x2(lo, kc.x, kc.y);
+                        e4m3x4_to_f16x2x2(hi, kc.z, kc.w);
                     } else {
                         kc = lds128(kro + ((kx0 ^ (uint32_t)c) << 4));
                     }
@@ -264,10 +273,13 @@ struct WarpAttn {
             if constexpr (KV8 && D == 128) {  // 4 codes per lane per row
                 const uint32_t r0 = lds32(vrow + (uint32_t)(2 * jp * D));
                 const uint32_t r1 = has1 ? lds32(vrow + (uint32_t)((2 * jp + 1) * D)) : 0u;
-                const float2 a0 = half2_bits_to_float2(e4m3x2_to_f16x2(r0 & 0xffffu));
-                const float2 a1 = half2_bits_to_float2(e4m3x2_to_f16x2(r0 >> 16));
-                const float2 b0 = half2_bits_to_float2(e4m3x2_to_f16x2(r1 & 0xffffu));
-                const float2 b1 = half2_bits_to_float2(e4m3x2_to_f16x2(r1 >> 16));
+                uint32_t h0, h1, h2, h3;
+                e4m3x4_to_f16x2x2(r0, h0, h1);
+                e4m3x4_to_f16x2x2(r1, h2, h3);
+                const float2 a0 = half2_bits_to_float2(h0);
+                const float2 a1 = half2_bits_to_float2(h1);
+                const float2 b0 = half2_bits_to_float2(h2);
+                const float2 b1 = half2_bits_to_float2(h3);
                 v0[0] = a0.x; v0[1] = a0.y; v0[C::DPL > 2 ? 2 : 0] = a1.x; v0[C::DPL > 3 ? 3 : 0] = a1.y;
                 v1[0] = b0.x; v1[1] = b0.y; v1[C::DPL > 2 ? 2 : 0] = b1.x; v1[C::DPL > 3 ? 3 : 0] = b1.y;
             } else if constexpr (KV8) {  // D = 64: 2 codes per lane per row

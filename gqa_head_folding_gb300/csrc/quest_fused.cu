@@ -466,10 +466,8 @@ __global__ void __launch_bounds__(FusedCfg<D, G, KV>::THREADS, 1)
                                 const uint32_t wa = (ks & 3) == 0 ? ua.x : (ks & 3) == 1 ? ua.y : (ks & 3) == 2 ? ua.z : ua.w;
                                 const uint32_t wb = (ks & 3) == 0 ? ub.x : (ks & 3) == 1 ? ub.y : (ks & 3) == 2 ? ub.z : ub.w;
                                 uint32_t af[4];
-                                af[0] = e4m3x2_to_f16x2(wa & 0xffffu);
-                                af[1] = e4m3x2_to_f16x2(wb & 0xffffu);
-                                af[2] = e4m3x2_to_f16x2(wa >> 16);
-                                af[3] = e4m3x2_to_f16x2(wb >> 16);
+                                e4m3x4_to_f16x2x2(wa, af[0], af[2]);
+                                e4m3x4_to_f16x2x2(wb, af[1], af[3]);
                                 mma_16816(acc, af, qb[ks][0], qb[ks][1]);
                             }
                         } else {
