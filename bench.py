@@ -325,10 +325,10 @@ def l2_note(copies: int, bytes_per_step: int, l2: int) -> str:
 # capture of the kernel as it stands, keyed by (workload id, batch, family, KV format,
 # page size). A kernel change makes its entry stale: it is then removed until the capture
 # is taken again.
-NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_540_480, (3, 1, "quest", "e4m3", 16): 33_683_456,
-               (3, 1, "dense", "f16", 16): 539_982_848,
-               (2, 32, "dense", "f16", 16): 180_035_584, (2, 32, "dense", "e4m3", 16): 90_877_440,
-               (2, 32, "dense", "int4", 16): 49_938_432}
+NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_763_456, (3, 1, "quest", "e4m3", 16): 33_683_968,
+               (3, 1, "dense", "f16", 16): 539_990_528,
+               (2, 32, "dense", "f16", 16): 179_788_800, (2, 32, "dense", "e4m3", 16): 90_756_352,
+               (2, 32, "dense", "int4", 16): 50_008_576}
 # The same for one prefill launch (one layer), keyed by (workload id, batch, chunk length).
 PREFILL_TRAFFIC = {(3, 1, 128): 547_805_184}
 
