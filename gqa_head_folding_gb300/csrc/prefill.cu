@@ -390,17 +390,21 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::MIN_BLO
 //  - warp 9 (MMA, one thread): S_j = Q K_j^T (M = 128 rows, N = 128 tokens,
 //    K = D; both operands K-major in shared memory) into one of two TMEM S
 //    buffers, and O += P_j V_j (A = P_j from TMEM, B = V_j MN-major in shared
-//    memory, N = 64 per 64-channel block) into the TMEM O block. Issue order
-//    S_0, S_1, PV_0, S_2, PV_1, ...: the S of the next tile overlaps the
-//    softmax of this one, and each S buffer is rewritten only after the PV
-//    that read its P (the tensor core runs one thread's MMAs in order).
-//    Completions arrive on mbarriers through tcgen05.commit.
+//    memory, N = D across the 64-channel blocks) into the TMEM O block. Each
+//    product is issued as soon as its inputs are there (S_j when tile j has
+//    landed, PV_j when its P is written), except that S_j waits for the issue
+//    of PV_{j-2}, which reads the P held in the same S buffer (the tensor core
+//    runs one thread's MMAs in order). Descriptors are computed once; a stage
+//    or K-step is an offset. Completions arrive on mbarriers through
+//    tcgen05.commit.
 //  - warps 0-7 (softmax, two warpgroups taking alternate tiles, one thread
 //    per row): read the row's 128 scores from TMEM, mask the causal limit,
-//    keep a lazy reference max (rescaling the group's O in TMEM only when the
-//    row max grows by more than 2^8, so P stays <= 256 in fp16), write P as
-//    fp16 over the group's S buffer. One group's softmax overlaps the MMAs of
-//    the other's tile. At the end the two (m, l, O) states merge per row.
+//    take P = 2^(x - m_ref) against a reference max without a max pass (a
+//    64-column chunk whose P sum stays <= 2^12 needs nothing more; otherwise
+//    its max becomes the reference and the group's O in TMEM is rescaled),
+//    write P as fp16 over the group's S buffer. One group's softmax overlaps
+//    the MMAs of the other's tile. At the end the two (m, l, O) states merge
+//    per row.
 //  - TMEM (512 columns): S of group g at column 128 g, O of group g at 256 + D g.
 // ===========================================================================
 template <int D>
@@ -419,7 +423,6 @@ struct TcCfg {
     static constexpr int SMEM = 1024 + QBYTES + NSTAGE * STAGE + MISC;
     static constexpr int TMEM_COLS = 512;
     static constexpr int S_COL = 0, O_COL = 256;  // S of group g at 128 g, O of group g at 256 + D g
-    static constexpr float RESCALE_LOG2 = 8.f;    // lazy reference: P <= 2^8
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(RB * kPrefillMaxSplits * 4 <= NSTAGE * STAGE, "merge weights fit the idle ring");
 };
@@ -520,9 +523,13 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sq = smem;
     uint8_t *stages = sq + C::QBYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(stages + C::NSTAGE * C::STAGE);
-    uint64_t *empty = full + C::NSTAGE;
-    uint64_t *qbar = empty + C::NSTAGE;
+    // Each stage holds a K tile and a V tile with barriers of their own: a K
+    // half is reloaded once its S has completed, a V half once its PV has.
+    uint64_t *full = reinterpret_cast<uint64_t *>(stages + C::NSTAGE * C::STAGE);  // K landed
+    uint64_t *empty = full + C::NSTAGE;                                           // K free (S done)
+    uint64_t *vfull = empty + C::NSTAGE;                                          // V landed
+    uint64_t *vempty = vfull + C::NSTAGE;                                         // V free (PV done)
+    uint64_t *qbar = vempty + C::NSTAGE;
     uint64_t *s_ready = qbar + 1;   // [2]
     uint64_t *p_ready = s_ready + 2;  // [2]
     uint64_t *o_done = p_ready + 2;  // [2]: PV_j completes on o_done[j & 1]
@@ -537,6 +544,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&vfull[s]), 1);
+            mbar_init(smem_u32(&vempty[s]), 1);
         }
         mbar_init(smem_u32(qbar), 1);
         for (int b = 0; b < 2; ++b) {
@@ -592,31 +601,54 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
             for (int kh = 0; kh < C::KH; ++kh)
                 tma_load_2d(smem_u32(sq) + kh * C::QBLK, &qmap, 64 * kh, qrow, smem_u32(qbar), pol);
-            int i = 0;
+            // K tile ik and V tile iv, each as soon as its half of the stage is
+            // free; K leads (S needs it first), V follows.
+            int ik = 0, iv = 0;
             bool failed = false;
-            for (; i < n; ++i) {
-                const int s = i % C::NSTAGE;
-                if (i >= C::NSTAGE && !mbar_wait(smem_u32(&empty[s]), ((uint32_t)(i / C::NSTAGE) & 1u) ^ 1u,
-                                                 p.timeout_ns, abort_flag)) {
-                    failed = true;
-                    break;
-                }
-                const uint32_t kdst = smem_u32(stages + s * C::STAGE), vdst = kdst + C::KBYTES;
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, (uint32_t)C::STAGE);
-                const int y = unit * p.Lmax + (j0 + i) * C::TT;
+            uint64_t t_last = global_timer_ns();
+            while (iv < n && !failed) {
+                bool progressed = false;
+                if (ik < n) {
+                    const int s = ik % C::NSTAGE;
+                    if (ik < C::NSTAGE || mbar_try_wait_ns(smem_u32(&empty[s]), ((uint32_t)(ik / C::NSTAGE) & 1u) ^ 1u,
+                                                           iv < ik ? 100u : 2000u)) {
+                        const uint32_t kdst = smem_u32(stages + s * C::STAGE), fb = smem_u32(&full[s]);
+                        mbar_arrive_expect_tx(fb, (uint32_t)C::KBYTES);
+                        const int y = unit * p.Lmax + (j0 + ik) * C::TT;
 #pragma unroll
-                for (int kh = 0; kh < C::KH; ++kh) {
-                    tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
-                    tma_load_2d(vdst + kh * C::KBLK, &vmap, 64 * kh, y, fb, pol);
+                        for (int kh = 0; kh < C::KH; ++kh) tma_load_2d(kdst + kh * C::KBLK, &kmap, 64 * kh, y, fb, pol);
+                        ++ik;
+                        progressed = true;
+                    }
+                }
+                if (iv < ik) {
+                    const int s = iv % C::NSTAGE;
+                    if (iv < C::NSTAGE || mbar_try_wait_ns(smem_u32(&vempty[s]), ((uint32_t)(iv / C::NSTAGE) & 1u) ^ 1u,
+                                                           ik < n ? 100u : 2000u)) {
+                        const uint32_t vdst = smem_u32(stages + s * C::STAGE) + C::KBYTES, fb = smem_u32(&vfull[s]);
+                        mbar_arrive_expect_tx(fb, (uint32_t)C::KBYTES);
+                        const int y = unit * p.Lmax + (j0 + iv) * C::TT;
+#pragma unroll
+                        for (int kh = 0; kh < C::KH; ++kh) tma_load_2d(vdst + kh * C::KBLK, &vmap, 64 * kh, y, fb, pol);
+                        ++iv;
+                        progressed = true;
+                    }
+                }
+                const uint64_t now = global_timer_ns();
+                if (progressed) {
+                    t_last = now;
+                } else if (*abort_flag || now - t_last >= p.timeout_ns) {
+                    failed = true;
                 }
             }
             if (failed) {
                 raise_flag(p.status, GQAQ_DEV_TIMEOUT);
                 *abort_flag = 1;
-                const int first = i - C::NSTAGE > 0 ? i - C::NSTAGE : 0;
-                for (int it = first; it < i; ++it)
+                // let every copy already issued land before this CTA may retire
+                for (int it = ik - C::NSTAGE > 0 ? ik - C::NSTAGE : 0; it < ik; ++it)
                     mbar_wait(smem_u32(&full[it % C::NSTAGE]), (uint32_t)(it / C::NSTAGE) & 1u, p.timeout_ns, nullptr);
+                for (int it = iv - C::NSTAGE > 0 ? iv - C::NSTAGE : 0; it < iv; ++it)
+                    mbar_wait(smem_u32(&vfull[it % C::NSTAGE]), (uint32_t)(it / C::NSTAGE) & 1u, p.timeout_ns, nullptr);
                 mbar_wait(smem_u32(qbar), 0u, p.timeout_ns, nullptr);
             }
         }
@@ -629,45 +661,66 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             if (n > 0) {
                 fail = !mbar_wait(smem_u32(qbar), 0u, p.timeout_ns, abort_flag);
                 constexpr uint32_t IDESC_S = umma_idesc(128, C::TT, 0);
-                constexpr uint32_t IDESC_O = umma_idesc(128, 64, 1);
-                for (int idx = 0; idx <= n && !fail; ++idx) {
-                    if (idx < n) {
-                        const int s = idx % C::NSTAGE;
-                        if (!mbar_wait(smem_u32(&full[s]), (uint32_t)(idx / C::NSTAGE) & 1u, p.timeout_ns, abort_flag)) {
-                            fail = true;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t kst = smem_u32(stages + s * C::STAGE);
+                constexpr uint32_t IDESC_O = umma_idesc(128, D, 1);
+                // Descriptors of the Q block and of stage 0's K and V tiles; a stage,
+                // a K-step or a block is an offset added to the address field.
+                const uint64_t qdesc0 = umma_desc(smem_u32(sq), 16);
+                const uint64_t kdesc0 = umma_desc(smem_u32(stages), 16);
+                const uint64_t vdesc0 = umma_desc(smem_u32(stages) + C::KBYTES, C::KBLK);
+                // Issue each product as soon as its inputs are there: S_is when
+                // its K/V tile has landed (and PV_{is-2}, which reads the P held
+                // in the same S buffer, is issued: the tensor core runs one
+                // thread's MMAs in order), PV_ip when its softmax has written P.
+                // A PV never waits for the next tile's load.
+                int is = 0, ip = 0;
+                uint64_t t_last = global_timer_ns();
+                while (ip < n && !fail) {
+                    bool progressed = false;
+                    const bool s_ok = is < n && ip >= is - 1;
+                    if (s_ok) {
+                        const int s = is % C::NSTAGE;
+                        if (mbar_try_wait_ns(smem_u32(&full[s]), (uint32_t)(is / C::NSTAGE) & 1u, ip < is ? 100u : 2000u)) {
+                            tc_fence_after();
+                            // K-step ks: 16 columns of Q and K, 32 B further along the 128-byte
+                            // row, a 64-column block further every 4 steps (the descriptor's
+                            // address field counts 16-byte units; no carry leaves it).
+                            const uint64_t kd = kdesc0 + (uint64_t)((s * C::STAGE) >> 4);
+                            const uint32_t sd = tbase + C::S_COL + 128u * (is & 1);
 #pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t off = (uint32_t)((ks >> 2) * C::QBLK + (ks & 3) * 32);
-                            const uint32_t koff = (uint32_t)((ks >> 2) * C::KBLK + (ks & 3) * 32);
-                            umma_ss(tbase + C::S_COL + 128u * (idx & 1), umma_desc(smem_u32(sq) + off, 16),
-                                    umma_desc(kst + koff, 16), IDESC_S, ks > 0);
+                            for (int ks = 0; ks < D / 16; ++ks)
+                                umma_ss(sd, qdesc0 + (uint64_t)(((ks >> 2) * C::QBLK + (ks & 3) * 32) >> 4),
+                                        kd + (uint64_t)(((ks >> 2) * C::KBLK + (ks & 3) * 32) >> 4), IDESC_S, ks > 0);
+                            umma_commit(smem_u32(&s_ready[is & 1]));
+                            umma_commit(smem_u32(&empty[s]));  // the K half is free once S has read it
+                            ++is;
+                            progressed = true;
                         }
-                        umma_commit(smem_u32(&s_ready[idx & 1]));
                     }
-                    if (idx >= 1) {
-                        const int jj = idx - 1;
-                        if (!mbar_wait(smem_u32(&p_ready[jj & 1]), (uint32_t)(jj >> 1) & 1u, p.timeout_ns, abort_flag)) {
-                            fail = true;
-                            break;
-                        }
+                    if (ip < is &&
+                        mbar_try_wait_ns(smem_u32(&p_ready[ip & 1]), (uint32_t)(ip >> 1) & 1u, s_ok ? 100u : 2000u) &&
+                        mbar_try_wait_ns(smem_u32(&vfull[ip % C::NSTAGE]), (uint32_t)(ip / C::NSTAGE) & 1u, 100u)) {
                         tc_fence_after();
-                        const int s = jj % C::NSTAGE;
-                        const uint32_t vst = smem_u32(stages + s * C::STAGE) + C::KBYTES;
+                        const int s = ip % C::NSTAGE;
+                        // K-step kk: 16 tokens (rows 16 kk .. of V, 8 TMEM columns of P);
+                        // N = D spans the 64-channel blocks of V through the MN-major
+                        // descriptor's leading byte offset (one block = KBLK bytes).
+                        const uint64_t vd = vdesc0 + (uint64_t)((s * C::STAGE) >> 4);
+                        const uint32_t od = tbase + C::O_COL + (uint32_t)(D * (ip & 1));
+                        const uint32_t pd = tbase + C::S_COL + 128u * (ip & 1);
 #pragma unroll
-                        for (int kk = 0; kk < C::TT / 16; ++kk) {
-#pragma unroll
-                            for (int nb = 0; nb < C::KH; ++nb)
-                                umma_ts(tbase + C::O_COL + (uint32_t)(D * (jj & 1)) + 64u * nb,
-                                        tbase + C::S_COL + 128u * (jj & 1) + 8u * kk,
-                                        umma_desc(vst + nb * C::KBLK + kk * 16 * 128, C::KBLK), IDESC_O,
-                                        (jj > 1 || kk > 0) ? 1 : 0);  // each group's first PV starts its O
-                        }
-                        umma_commit(smem_u32(&o_done[jj & 1]));
-                        umma_commit(smem_u32(&empty[s]));
+                        for (int kk = 0; kk < C::TT / 16; ++kk)
+                            umma_ts(od, pd + 8u * kk, vd + (uint64_t)((kk * 16 * 128) >> 4), IDESC_O,
+                                    (ip > 1 || kk > 0) ? 1 : 0);  // each group's first PV starts its O
+                        umma_commit(smem_u32(&o_done[ip & 1]));
+                        umma_commit(smem_u32(&vempty[s]));
+                        ++ip;
+                        progressed = true;
+                    }
+                    const uint64_t now = global_timer_ns();
+                    if (progressed) {
+                        t_last = now;
+                    } else if (*abort_flag || now - t_last >= p.timeout_ns) {
+                        fail = true;
                     }
                 }
             }
@@ -717,46 +770,55 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             const int tok0 = (j0 + idx) * C::TT;
             const bool need_mask = tok0 + C::TT - 1 > st + t_min;  // uniform over the item
             const uint32_t scol = trow + C::S_COL + 128u * (idx & 1);
-            // One pass over the tile, 64 columns per TMEM round trip: the chunk's
-            // max, then P = 2^(x - m_ref) as fp16 over the S buffer (pairs, low half =
-            // even token). The lazy reference m_ref moves only when a chunk's max
-            // exceeds it by more than 2^8 (so P <= 256 fits fp16); then l, this
-            // group's O (when it holds earlier tiles) and the P already written for
-            // this tile are rescaled by alpha = 2^(old - new). That is rare: after
-            // the first chunks the reference rarely moves.
+            // One pass over the tile, 64 columns per TMEM round trip. Fast path:
+            // P = 2^(x - m_ref) against the current reference, no max pass; the
+            // chunk's sum bounds every P in it, so a sum up to 2^12 means every P
+            // fits fp16 and the chunk is done. Otherwise (the row's first chunk,
+            // or a score well above the reference; rare after the first tiles)
+            // the chunk's max becomes the reference, l, this group's O (when it
+            // holds earlier tiles) and the P already written for this tile are
+            // rescaled by alpha = 2^(old - new), and the chunk is recomputed.
             float ps = 0.f;
 #pragma unroll 1
             for (int ch = 0; ch < C::TT / 64; ++ch) {
                 uint32_t v[64], pk[32];
                 tmem_ld64(scol + 64u * ch, v);
-                // With a positive scale the max is taken on the raw scores and the
-                // scale folds into the exponent's FFMA; otherwise the scores are
-                // scaled first (mul = 1 below).
-                float cm, mul;
-                if (p.scale_log2 > 0.f) {
-                    if (need_mask) {
+                // With a positive scale it folds into the exponent's FFMA (mul);
+                // otherwise the scores are scaled first (mul = 1).
+                float mul = p.scale_log2;
+                if (p.scale_log2 <= 0.f) {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            if (tok0 + 64 * ch + e > lim) v[e] = __float_as_uint(-INFINITY);
-                    }
-                    float r = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) r = fmaxf(r, __uint_as_float(v[e]));
-                    cm = r * p.scale_log2;
-                    mul = p.scale_log2;
-                } else {
-                    cm = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        float x = __uint_as_float(v[e]) * p.scale_log2;
-                        if (need_mask && tok0 + 64 * ch + e > lim) x = -INFINITY;
-                        v[e] = __float_as_uint(x);
-                        cm = fmaxf(cm, x);
-                    }
+                    for (int e = 0; e < 64; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * p.scale_log2);
                     mul = 1.f;
                 }
-                const bool up = cm > m_ref + C::RESCALE_LOG2;
-                if (__any_sync(0xffffffffu, up)) {
+                if (need_mask) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (tok0 + 64 * ch + e > lim) v[e] = __float_as_uint(-INFINITY);
+                }
+                // P of this chunk against reference `ref` into pk; returns the chunk's sum
+                auto chunk_p = [&](float ref) {
+                    const float nref = ref == -INFINITY ? 0.f : -ref;
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        const float e0 = fast_exp2(fmaf(__uint_as_float(v[e]), mul, nref));
+                        const float e1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), mul, nref));
+                        s4[(e >> 1) & 3] += e0 + e1;
+                        pk[e >> 1] = pack_half2(e0, e1);
+                    }
+                    return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                };
+                float cs = 0.f;
+                const bool fast = m_ref != -INFINITY;
+                if (fast) cs = chunk_p(m_ref);
+                const bool redo = !fast || cs > 4096.f;
+                if (__any_sync(0xffffffffu, redo)) {
+                    float r4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) r4[e & 3] = fmaxf(r4[e & 3], __uint_as_float(v[e]));
+                    const float cm = fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3])) * mul;
+                    const bool up = cm > m_ref;
                     const float alpha = up ? fast_exp2(m_ref - cm) : 1.f;  // 0 when m_ref is -inf
                     if (up) {
                         m_ref = cm;
@@ -784,20 +846,21 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                         tmem_st32(scol + 32u * pc, q);
                     }
                     tmem_wait_st();
+                    cs = chunk_p(m_ref);
                 }
-                const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
-#pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const float e0 = fast_exp2(fmaf(__uint_as_float(v[e]), mul, nref));
-                    const float e1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), mul, nref));
-                    ps += e0 + e1;
-                    pk[e >> 1] = pack_half2(e0, e1);
-                }
+                ps += cs;
                 tmem_st32(scol + 32u * ch, pk);  // P of tokens 64 ch .. +63 over S columns 32 ch .. +31
             }
             l += ps;
             tmem_wait_st();
-            if (tok0 + C::TT > kv_end && tok0 + tid >= kv_end) {
+            if (tok0 + C::TT > kv_end) {  // uniform over the item: wait for this tile's V to land
+                ok = warp_wait(smem_u32(&vfull[idx % C::NSTAGE]), (uint32_t)(idx / C::NSTAGE) & 1u, p, abort_flag, lane);
+                if (!ok && lane == 0) {
+                    raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+            }
+            if (ok && tok0 + C::TT > kv_end && tok0 + tid >= kv_end) {
                 // rows past the chunk may hold anything: zero them so 0 * NaN cannot reach O
                 uint8_t *vrow = stages + (idx % C::NSTAGE) * C::STAGE + C::KBYTES + tid * 128;
 #pragma unroll
