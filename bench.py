@@ -330,7 +330,7 @@ NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_763_456, (3, 1, "quest", "e4m3", 1
                (2, 32, "dense", "f16", 16): 179_788_800, (2, 32, "dense", "e4m3", 16): 90_756_352,
                (2, 32, "dense", "int4", 16): 50_008_576}
 # The same for one prefill launch (one layer), keyed by (workload id, batch, chunk length).
-PREFILL_TRAFFIC = {(3, 1, 128): 547_805_184}
+PREFILL_TRAFFIC = {(3, 1, 128): 548_153_856, (3, 1, 1024): 702_687_232}
 
 
 def capture(fn, device):
@@ -628,12 +628,36 @@ def load_peaks() -> dict:
 # ---------------------------------------------------------------------------
 # Prefill mode: a chunk of q_len new tokens per sequence and layer
 # ---------------------------------------------------------------------------
-PREFILL_METRIC = "prefill-attn us/step (causal chunk of q_len tokens per sequence per layer) and TFLOP/s vs tensor peak"
+PREFILL_METRIC = "prefill-attn us/step (causal chunk of q_len tokens per sequence per layer) and achieved vs the binding roofline (tensor or HBM)"
 
 
 def prefill_flops(w: workloads.Workload, starts, q_len: int) -> int:
     """q.k and p.V multiply-adds of one layer: 2 x 2 D flops per (row, attended token)."""
     return sum(4 * w.head_dim * w.num_q_heads * (q_len * s + q_len * (q_len + 1) // 2) for s in starts)
+
+
+def prefill_roofline(flops: int, nbytes: int, s_per_launch: float, peaks: dict, traffic=None) -> dict:
+    """The roofline that binds one prefill launch: tensor when its arithmetic
+    intensity (flops per byte of K, V, q and out) reaches the ridge of the two
+    measured peaks, HBM below it (a short chunk over a long context reads far
+    more K/V per flop). Both fractions are reported; `frac` is the binding one."""
+    tflops = flops / s_per_launch / 1e12
+    gbs = nbytes / s_per_launch / 1e9
+    t_frac = tflops / peaks["tensor_tflops"]
+    h_frac = gbs / peaks["hbm_gbs"]
+    ridge = peaks["tensor_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flops per byte
+    intensity = flops / max(1, nbytes)
+    tensor = intensity >= ridge
+    return {"bound": "tensor" if tensor else "hbm", "kernel": "gqa_prefill_attn",
+            "achieved": round(tflops if tensor else gbs, 1), "peak": peaks["tensor_tflops"] if tensor else peaks["hbm_gbs"],
+            "unit": "TFLOP/s" if tensor else "GB/s", "frac": round(t_frac if tensor else h_frac, 4),
+            "peak_source": peaks["source"] + (" (bf16 sustained; fp16 has the same nominal rate)" if tensor
+                                              else " (device-to-device copy)"),
+            "traffic": traffic, "flops_per_launch": flops, "bytes_per_launch": nbytes,
+            "intensity_flops_per_byte": round(intensity, 1), "ridge_flops_per_byte": round(ridge, 1),
+            "tensor_tflops": round(tflops, 1), "tensor_frac": round(t_frac, 4),
+            "hbm_gbs": round(gbs, 1), "hbm_frac": round(h_frac, 4),
+            "us_per_launch": round(s_per_launch * 1e6, 2)}
 
 
 def prefill_bytes(w: workloads.Workload, starts, q_len: int) -> int:
@@ -738,11 +762,8 @@ def run_prefill(args, rank, world, local):
                                             l2_bytes())), q_len=Q,
                        chunk="last q_len tokens of each sequence's valid length"),
         "achieved_tflops": round(achieved, 1),
-        "roofline": {"bound": "tensor", "kernel": "gqa_prefill_attn", "achieved": round(achieved, 1),
-                     "peak": peaks["tensor_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["tensor_tflops"], 4),
-                     "peak_source": peaks["source"] + " (bf16 sustained; fp16 has the same nominal rate)",
-                     "traffic": PREFILL_TRAFFIC.get((w.id, w.batch, Q)), "flops_per_launch": per_launch_flops,
-                     "us_per_launch": round(s_per_step / w.num_layers * 1e6, 2)},
+        "roofline": prefill_roofline(per_launch_flops, per_launch_bytes, s_per_step / w.num_layers, peaks,
+                                     PREFILL_TRAFFIC.get((w.id, w.batch, Q))),
         "achieved_gbs": round(sum(prefill_bytes(w, s, Q) for s in starts) / s_per_step / 1e9, 1),
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_s * 1e6, 2), "unit": UNIT,
