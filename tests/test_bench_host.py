@@ -173,3 +173,26 @@ def test_reference_arm_never_loads_the_cuda_library():
     args = argparse.Namespace(workload=1, batch=0, k_pages=0, layers=0, page_size=0, budget=0, dense=False, unfused=False, kv="f16",
               no_pdl=False, quest_kernel="cluster", no_early_meta=False, no_early_kv=False)
     assert line["config"] == bench.arm_config(args, bench.workload_from_args(args), 1)
+
+
+def test_prefill_roofline_takes_the_binding_peak():
+    """A prefill launch below the ridge of the two measured peaks (flops per
+    byte) is judged against HBM, above it against the tensor peak; the line
+    carries both fractions."""
+    peaks = {"hbm_gbs": 6766.0, "tensor_tflops": 1716.6, "source": "measured"}
+    ridge = peaks["tensor_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    w = workloads.WORKLOADS[3].with_(batch=1, num_layers=1)
+    for q, bound in ((128, "hbm"), (1024, "tensor")):
+        starts = [w.max_len - q]
+        flops, nbytes = bench.prefill_flops(w, starts, q), bench.prefill_bytes(w, starts, q)
+        assert (flops / nbytes >= ridge) == (bound == "tensor")
+        t = 100e-6
+        r = bench.prefill_roofline(flops, nbytes, t, peaks)
+        assert r["bound"] == bound
+        tf, gb = flops / t / 1e12, nbytes / t / 1e9
+        assert r["tensor_frac"] == pytest.approx(tf / peaks["tensor_tflops"], rel=1e-3)
+        assert r["hbm_frac"] == pytest.approx(gb / peaks["hbm_gbs"], rel=1e-3)
+        assert r["frac"] == (r["tensor_frac"] if bound == "tensor" else r["hbm_frac"])
+        assert r["unit"] == ("TFLOP/s" if bound == "tensor" else "GB/s")
+    pf = bench.prefill_bytes(w, [w.max_len - 1024], 1024)
+    assert 1.0 < bench.PREFILL_TRAFFIC[(3, 1, 1024)] / pf < 1.35  # eight 128-row blocks share K/V through L2
