@@ -388,24 +388,26 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, PrefillCfg<D>::MIN_BLO
 //  - warp 8 (TMA): the item's Q block once, then K and V tiles of 128 tokens
 //    (128-byte-swizzled 64-column boxes) into a 3-5 stage ring.
 //  - warp 9 (MMA, one thread): S_j = Q K_j^T (M = 128 rows, N = 128 tokens,
-//    K = D; both operands K-major in shared memory) into one of two TMEM S
+//    K = D; both operands K-major in shared memory) into one of three TMEM S
 //    buffers, and O += P_j V_j (A = P_j from TMEM, B = V_j MN-major in shared
 //    memory, N = D across the 64-channel blocks) into the TMEM O block. Each
 //    product is issued as soon as its inputs are there (S_j when tile j has
 //    landed, PV_j when its P is written), except that S_j waits for the issue
-//    of PV_{j-2}, which reads the P held in the same S buffer (the tensor core
+//    of PV_{j-3}, which reads the P held in the same S buffer (the tensor core
 //    runs one thread's MMAs in order). Descriptors are computed once; a stage
 //    or K-step is an offset. Completions arrive on mbarriers through
 //    tcgen05.commit.
-//  - warps 0-7 (softmax, two warpgroups taking alternate tiles, one thread
-//    per row): read the row's 128 scores from TMEM, mask the causal limit,
-//    take P = 2^(x - m_ref) against a reference max without a max pass (a
-//    64-column chunk whose P sum stays <= 2^12 needs nothing more; otherwise
-//    its max becomes the reference and the group's O in TMEM is rescaled),
-//    write P as fp16 over the group's S buffer. One group's softmax overlaps
-//    the MMAs of the other's tile. At the end the two (m, l, O) states merge
-//    per row.
-//  - TMEM (512 columns): S of group g at column 128 g, O of group g at 256 + D g.
+//  - warps 0-7 (softmax): all eight on every tile, warp w on the rows of its
+//    TMEM lane quarter (w % 4) and the 64-token half w / 4 of the tile: read
+//    the scores from TMEM, mask the causal limit, take P = 2^(x - m_ref)
+//    against the row's reference max without a max pass (a half whose P sum
+//    stays <= 2^12 needs nothing more; otherwise, for every thread at once,
+//    the row's max over both halves becomes the reference and O in TMEM is
+//    rescaled), and write P as fp16 inside the columns the half read. Two
+//    softmax warps per sub-partition work on the same tile while the tensor
+//    core computes the next tile's S into the other buffer.
+//  - TMEM (512 columns): O at column 0 (D columns), S buffer b (of three) at
+//    128 + 128 b: S_j goes to buffer j % 3 once PV_{j-3} has been issued.
 // ===========================================================================
 template <int D>
 struct TcCfg {
@@ -422,7 +424,8 @@ struct TcCfg {
     static constexpr int MISC = 2048;             // barriers, flags, and group 1's (m, l) per row at +512
     static constexpr int SMEM = 1024 + QBYTES + NSTAGE * STAGE + MISC;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int S_COL = 0, O_COL = 256;  // S of group g at 128 g, O of group g at 256 + D g
+    static constexpr int O_COL = 0, S_COL = 128;  // O (D columns), then S buffer b at 128 + 128 b
+    static constexpr int NSB = 3;                 // S buffers: three tiles between S and PV
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(RB * kPrefillMaxSplits * 4 <= NSTAGE * STAGE, "merge weights fit the idle ring");
 };
@@ -505,6 +508,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Barrier 2 over the 256 softmax threads that also reduces a predicate:
+// true on every thread when any of them passed true.
+__device__ __forceinline__ bool bar_any_256(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 2, 256, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
 // One warp's bounded wait (lane 0 waits, the warp follows): false on timeout or abort.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const PrefillParams &p,
                                           volatile int *abort_flag, int lane) {
@@ -530,9 +545,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     uint64_t *vfull = empty + C::NSTAGE;                                          // V landed
     uint64_t *vempty = vfull + C::NSTAGE;                                         // V free (PV done)
     uint64_t *qbar = vempty + C::NSTAGE;
-    uint64_t *s_ready = qbar + 1;   // [2]
-    uint64_t *p_ready = s_ready + 2;  // [2]
-    uint64_t *o_done = p_ready + 2;  // [2]: PV_j completes on o_done[j & 1]
+    uint64_t *s_ready = qbar + 1;          // [NSB]: S_j complete, on s_ready[j % NSB]
+    uint64_t *p_ready = s_ready + C::NSB;  // [NSB]: P_j written, on p_ready[j % NSB]
+    uint64_t *o_done = p_ready + C::NSB;   // [2]: PV_j completes on o_done[j & 1]
     uint64_t *drain = o_done + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
@@ -548,9 +563,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             mbar_init(smem_u32(&vempty[s]), 1);
         }
         mbar_init(smem_u32(qbar), 1);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::NSB; ++b) {
             mbar_init(smem_u32(&s_ready[b]), 1);
-            mbar_init(smem_u32(&p_ready[b]), 4);  // one arrival per softmax warp
+            mbar_init(smem_u32(&p_ready[b]), 8);  // one arrival per softmax warp
         }
         mbar_init(smem_u32(&o_done[0]), 1);
         mbar_init(smem_u32(&o_done[1]), 1);
@@ -676,7 +691,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                 uint64_t t_last = global_timer_ns();
                 while (ip < n && !fail) {
                     bool progressed = false;
-                    const bool s_ok = is < n && ip >= is - 1;
+                    const bool s_ok = is < n && ip >= is - (C::NSB - 1);  // PV_{is-NSB} issued: its buffer is free
                     if (s_ok) {
                         const int s = is % C::NSTAGE;
                         if (mbar_try_wait_ns(smem_u32(&full[s]), (uint32_t)(is / C::NSTAGE) & 1u, ip < is ? 100u : 2000u)) {
@@ -685,19 +700,19 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                             // row, a 64-column block further every 4 steps (the descriptor's
                             // address field counts 16-byte units; no carry leaves it).
                             const uint64_t kd = kdesc0 + (uint64_t)((s * C::STAGE) >> 4);
-                            const uint32_t sd = tbase + C::S_COL + 128u * (is & 1);
+                            const uint32_t sd = tbase + C::S_COL + 128u * (uint32_t)(is % C::NSB);
 #pragma unroll
                             for (int ks = 0; ks < D / 16; ++ks)
                                 umma_ss(sd, qdesc0 + (uint64_t)(((ks >> 2) * C::QBLK + (ks & 3) * 32) >> 4),
                                         kd + (uint64_t)(((ks >> 2) * C::KBLK + (ks & 3) * 32) >> 4), IDESC_S, ks > 0);
-                            umma_commit(smem_u32(&s_ready[is & 1]));
+                            umma_commit(smem_u32(&s_ready[is % C::NSB]));
                             umma_commit(smem_u32(&empty[s]));  // the K half is free once S has read it
                             ++is;
                             progressed = true;
                         }
                     }
                     if (ip < is &&
-                        mbar_try_wait_ns(smem_u32(&p_ready[ip & 1]), (uint32_t)(ip >> 1) & 1u, s_ok ? 100u : 2000u) &&
+                        mbar_try_wait_ns(smem_u32(&p_ready[ip % C::NSB]), (uint32_t)(ip / C::NSB) & 1u, s_ok ? 100u : 2000u) &&
                         mbar_try_wait_ns(smem_u32(&vfull[ip % C::NSTAGE]), (uint32_t)(ip / C::NSTAGE) & 1u, 100u)) {
                         tc_fence_after();
                         const int s = ip % C::NSTAGE;
@@ -705,12 +720,14 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                         // N = D spans the 64-channel blocks of V through the MN-major
                         // descriptor's leading byte offset (one block = KBLK bytes).
                         const uint64_t vd = vdesc0 + (uint64_t)((s * C::STAGE) >> 4);
-                        const uint32_t od = tbase + C::O_COL + (uint32_t)(D * (ip & 1));
-                        const uint32_t pd = tbase + C::S_COL + 128u * (ip & 1);
+                        const uint32_t od = tbase + C::O_COL;
+                        const uint32_t pd = tbase + C::S_COL + 128u * (uint32_t)(ip % C::NSB);
+                        // P of tokens 0-63 sits in S columns 0-31, of tokens 64-127 in 64-95
+                        // (each softmax half writes inside the columns it read)
 #pragma unroll
                         for (int kk = 0; kk < C::TT / 16; ++kk)
-                            umma_ts(od, pd + 8u * kk, vd + (uint64_t)((kk * 16 * 128) >> 4), IDESC_O,
-                                    (ip > 1 || kk > 0) ? 1 : 0);  // each group's first PV starts its O
+                            umma_ts(od, pd + 8u * kk + (kk >= 4 ? 32u : 0u), vd + (uint64_t)((kk * 16 * 128) >> 4),
+                                    IDESC_O, (ip > 0 || kk > 0) ? 1 : 0);  // the first PV starts O
                         umma_commit(smem_u32(&o_done[ip & 1]));
                         umma_commit(smem_u32(&vempty[s]));
                         ++ip;
@@ -736,209 +753,190 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------------
-        // Softmax, two warpgroups: group g (warps 4g .. 4g+3) takes the
-        // tiles idx = g, g + 2, ... with its own S buffer, O block and (m, l);
-        // thread tid owns row tid of the item (its warp's TMEM lane quarter).
-        // A group's O is never written while its softmax runs (its next PV
-        // waits for its P), and S_idx complete implies PV_{idx-2} complete
-        // (issued before it, in-order completion), so rescaling O needs no wait.
+        // Softmax, all eight warps on every tile: warp w takes the row block
+        // of its TMEM lane quarter (w % 4) and column half h = w / 4 of the
+        // tile (64 tokens), so the two warps of a sub-partition work on the
+        // same tile. Both halves of a row share its reference max m_ref and
+        // keep partial sums l; they agree through shared memory, and only when
+        // some chunk leaves the fast path (a predicate-reducing barrier per
+        // tile tells every thread). P of half h goes to S columns 64 h .. +31,
+        // inside the columns it read. One O for the item: a rescale first
+        // waits for the previous PV (the only one that can still write O).
         // ------------------------------------------------------------------
-        const int grp = warp >> 2;
+        const int half = warp >> 2;
         const int tid = threadIdx.x & 127;
         const bool live = tid < nrows;
         const int lim = st + (rho0 + tid) % p.q_len;
         const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t ocol = trow + C::O_COL + (uint32_t)(D * grp);
+        const uint32_t ocol = trow + C::O_COL + (uint32_t)(half * (D / 2));  // this half's O columns
+        float *xchg = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(full) + 512);  // [2][128] misc region
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        // PV_j's completion, on o_done[j & 1]: its previous use (PV_{j-2}) has
-        // completed whenever this is asked and its next (PV_{j+2}) is not
-        // issued, so the parity wait is never more than one phase behind.
+        // PV_j's completion, on o_done[j & 1]. A parity wait is exact only
+        // while the barrier is at most one phase behind: PV_{j-2} complete and
+        // PV_{j+2} not issued. The slow path asks for PV_{idx-1} once S_idx is
+        // complete, which (in-order MMAs, S_idx issued after PV_{idx-3})
+        // implies PV_{idx-3} complete; PV_{idx+1} needs this thread's P. The
+        // epilogue asks for PV_{n-2} first (S_{n-1} complete implies PV_{n-4})
+        // and then PV_{n-1}.
         auto wait_pv = [&](int j) {
             return warp_wait(smem_u32(&o_done[j & 1]), (uint32_t)(j >> 1) & 1u, p, abort_flag, lane);
         };
-        for (int idx = grp; idx < n; idx += 2) {
-            ok = ok && warp_wait(smem_u32(&s_ready[idx & 1]), (uint32_t)(idx >> 1) & 1u, p, abort_flag, lane);
-            if (!ok) {
-                if (lane == 0) {
-                    raise_flag(p.status, GQAQ_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                break;
+        auto fail = [&]() {
+            if (lane == 0) {
+                raise_flag(p.status, GQAQ_DEV_TIMEOUT);
+                *abort_flag = 1;
             }
+        };
+        for (int idx = 0; idx < n; ++idx) {
+            // every thread of the 256 reaches the same barriers each tile, also after a timeout
+            ok = ok && warp_wait(smem_u32(&s_ready[idx % C::NSB]), (uint32_t)(idx / C::NSB) & 1u, p, abort_flag, lane);
+            if (!ok) fail();
             tc_fence_after();
-            const int tok0 = (j0 + idx) * C::TT;
-            const bool need_mask = tok0 + C::TT - 1 > st + t_min;  // uniform over the item
-            const uint32_t scol = trow + C::S_COL + 128u * (idx & 1);
-            // One pass over the tile, 64 columns per TMEM round trip. Fast path:
-            // P = 2^(x - m_ref) against the current reference, no max pass; the
-            // chunk's sum bounds every P in it, so a sum up to 2^12 means every P
-            // fits fp16 and the chunk is done. Otherwise (the row's first chunk,
-            // or a score well above the reference; rare after the first tiles)
-            // the chunk's max becomes the reference, l, this group's O (when it
-            // holds earlier tiles) and the P already written for this tile are
-            // rescaled by alpha = 2^(old - new), and the chunk is recomputed.
-            float ps = 0.f;
-#pragma unroll 1
-            for (int ch = 0; ch < C::TT / 64; ++ch) {
-                uint32_t v[64], pk[32];
-                tmem_ld64(scol + 64u * ch, v);
-                // With a positive scale it folds into the exponent's FFMA (mul);
-                // otherwise the scores are scaled first (mul = 1).
-                float mul = p.scale_log2;
-                if (p.scale_log2 <= 0.f) {
+            const int tok0 = (j0 + idx) * C::TT + 64 * half;  // this half's first token
+            const bool need_mask = tok0 + 63 > st + t_min;  // uniform over the item
+            const uint32_t sbuf = trow + C::S_COL + 128u * (uint32_t)(idx % C::NSB);
+            const uint32_t scol = sbuf + 64u * half;
+            uint32_t v[64], pk[32];
+            if (ok) {
+                tmem_ld64(scol, v);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * p.scale_log2);
-                    mul = 1.f;
+                for (int e = 0; e < 64; ++e) v[e] = 0u;
+            }
+            // With a positive scale it folds into the exponent's FFMA (mul);
+            // otherwise the scores are scaled first (mul = 1).
+            float mul = p.scale_log2;
+            if (p.scale_log2 <= 0.f) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * p.scale_log2);
+                mul = 1.f;
+            }
+            if (need_mask) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    if (tok0 + e > lim) v[e] = __float_as_uint(-INFINITY);
+            }
+            // P of this half against reference `ref` into pk; returns its sum
+            auto half_p = [&](float ref) {
+                const float nref = ref == -INFINITY ? 0.f : -ref;
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(v[e]), mul, nref));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), mul, nref));
+                    s4[(e >> 1) & 3] += e0 + e1;
+                    pk[e >> 1] = pack_half2(e0, e1);
                 }
-                if (need_mask) {
+                return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            };
+            // Fast path: P against the current reference; the half's sum bounds
+            // every P in it, so a sum <= 2^12 means every P fits fp16.
+            float cs = 0.f;
+            if (m_ref != -INFINITY) cs = half_p(m_ref);
+            const bool redo = m_ref == -INFINITY || cs > 4096.f;
+            if (bar_any_256(redo)) {
+                // Slow path (the first tiles, or a score well above the reference):
+                // the row's max over both halves becomes the reference; l, O and
+                // this half's P follow it.
+                float r4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int e = 0; e < 64; ++e)
-                        if (tok0 + 64 * ch + e > lim) v[e] = __float_as_uint(-INFINITY);
+                for (int e = 0; e < 64; ++e) r4[e & 3] = fmaxf(r4[e & 3], __uint_as_float(v[e]));
+                xchg[half * 128 + tid] = fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3])) * mul;
+                named_bar_sync(2, 256);
+                const float cm = fmaxf(xchg[tid], xchg[128 + tid]);
+                const bool up = cm > m_ref;
+                const float alpha = up ? fast_exp2(m_ref - cm) : 1.f;  // 0 when m_ref is -inf
+                if (up) {
+                    m_ref = cm;
+                    l *= alpha;
                 }
-                // P of this chunk against reference `ref` into pk; returns the chunk's sum
-                auto chunk_p = [&](float ref) {
-                    const float nref = ref == -INFINITY ? 0.f : -ref;
-                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
-                        const float e0 = fast_exp2(fmaf(__uint_as_float(v[e]), mul, nref));
-                        const float e1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), mul, nref));
-                        s4[(e >> 1) & 3] += e0 + e1;
-                        pk[e >> 1] = pack_half2(e0, e1);
-                    }
-                    return (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                };
-                float cs = 0.f;
-                const bool fast = m_ref != -INFINITY;
-                if (fast) cs = chunk_p(m_ref);
-                const bool redo = !fast || cs > 4096.f;
-                if (__any_sync(0xffffffffu, redo)) {
-                    float r4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) r4[e & 3] = fmaxf(r4[e & 3], __uint_as_float(v[e]));
-                    const float cm = fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3])) * mul;
-                    const bool up = cm > m_ref;
-                    const float alpha = up ? fast_exp2(m_ref - cm) : 1.f;  // 0 when m_ref is -inf
-                    if (up) {
-                        m_ref = cm;
-                        l *= alpha;
-                        ps *= alpha;
-                    }
-                    if (__any_sync(0xffffffffu, up && idx >= 2)) {  // this group's O holds earlier tiles
+                if (__any_sync(0xffffffffu, up && idx >= 1)) {  // O holds earlier tiles
+                    ok = ok && wait_pv(idx - 1);                  // the last PV that writes O
+                    if (!ok) fail();
+                    tc_fence_after();
+                    if (ok) {
 #pragma unroll 1
-                        for (int oc = 0; oc < D / 32; ++oc) {
+                        for (int oc = 0; oc < D / 64; ++oc) {
                             uint32_t o[32];
                             tmem_ld32(ocol + 32u * oc, o);
 #pragma unroll
                             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                             tmem_st32(ocol + 32u * oc, o);
                         }
+                        tmem_wait_st();
                     }
-                    for (int pc = 0; pc < ch; ++pc) {  // this tile's P written so far
-                        uint32_t q[32];
-                        tmem_ld32(scol + 32u * pc, q);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q[e]));
-                            q[e] = pack_half2(f.x * alpha, f.y * alpha);
-                        }
-                        tmem_st32(scol + 32u * pc, q);
-                    }
-                    tmem_wait_st();
-                    cs = chunk_p(m_ref);
                 }
-                ps += cs;
-                tmem_st32(scol + 32u * ch, pk);  // P of tokens 64 ch .. +63 over S columns 32 ch .. +31
+                cs = half_p(m_ref);
             }
-            l += ps;
-            tmem_wait_st();
-            if (tok0 + C::TT > kv_end) {  // uniform over the item: wait for this tile's V to land
+            l += cs;
+            if (ok) {
+                tmem_st32(scol, pk);  // P over this half's columns (the first 32 of the 64 it read)
+                tmem_wait_st();
+            }
+            if (ok && (j0 + idx) * C::TT + C::TT > kv_end) {  // uniform: wait for this tile's V to land
                 ok = warp_wait(smem_u32(&vfull[idx % C::NSTAGE]), (uint32_t)(idx / C::NSTAGE) & 1u, p, abort_flag, lane);
-                if (!ok && lane == 0) {
-                    raise_flag(p.status, GQAQ_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                }
+                if (!ok) fail();
             }
-            if (ok && tok0 + C::TT > kv_end && tok0 + tid >= kv_end) {
-                // rows past the chunk may hold anything: zero them so 0 * NaN cannot reach O
-                uint8_t *vrow = stages + (idx % C::NSTAGE) * C::STAGE + C::KBYTES + tid * 128;
+            const int vrow_tok = (j0 + idx) * C::TT + tid;
+            if (ok && (j0 + idx) * C::TT + C::TT > kv_end && vrow_tok >= kv_end && half < C::KH) {
+                // rows past the chunk may hold anything: zero them so 0 * NaN cannot
+                // reach O (half h clears the row's 64-channel block h)
+                uint8_t *vrow = stages + (idx % C::NSTAGE) * C::STAGE + C::KBYTES + half * C::KBLK + tid * 128;
 #pragma unroll
-                for (int kh = 0; kh < C::KH; ++kh)
-#pragma unroll
-                    for (int q16 = 0; q16 < 8; ++q16)
-                        *reinterpret_cast<uint4 *>(vrow + kh * C::KBLK + 16 * q16) = make_uint4(0u, 0u, 0u, 0u);
+                for (int q16 = 0; q16 < 8; ++q16)
+                    *reinterpret_cast<uint4 *>(vrow + 16 * q16) = make_uint4(0u, 0u, 0u, 0u);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // zeroed rows reach the tensor core
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_ready[idx & 1]));
+            if (lane == 0) mbar_arrive(smem_u32(&p_ready[idx % C::NSB]));
         }
-        // ---- epilogue: each group's O after its last PV, then the two merge per row ----
-        const int last = n > grp ? grp + 2 * ((n - 1 - grp) / 2) : -1;  // this group's last tile
-        if (ok && last >= 0) {
-            ok = wait_pv(last);  // every PV of this group is done (in-order completion)
-            if (!ok && lane == 0) {
-                raise_flag(p.status, GQAQ_DEV_TIMEOUT);
-                *abort_flag = 1;
-            }
+        // ---- epilogue: O after the last PV; l of both halves; each half writes its columns ----
+        if (ok && n > 1) {
+            ok = wait_pv(n - 2);
+            if (!ok) fail();
         }
-        // Group 1 hands its (m, l) over in shared memory (outside the ring: the
-        // other group's last PV may still read a stage), group 0 reads both O
-        // blocks and merges:
-        // m* = max(m0, m1), w_g = 2^(m_g - m*), out = (w0 O0 + w1 O1) / (w0 l0 + w1 l1).
-        float2 *hand = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(full) + 512);  // misc region
-        if (grp == 1) hand[tid] = make_float2(m_ref, l);
-        tc_fence_before();
-        named_bar_sync(2, 256);  // both softmax groups: group 1's O and (m, l) are final
-        if (grp == 0) {
-            tc_fence_after();
-            const bool have_a = n > 0, have_b = n > 1;
-            const float2 mlb = have_b ? hand[tid] : make_float2(-INFINITY, 0.f);
-            const float mst = fmaxf(m_ref, mlb.x);
-            const float wa = (mst == -INFINITY || m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - mst);
-            const float wb = (mst == -INFINITY || mlb.x == -INFINITY) ? 0.f : fast_exp2(mlb.x - mst);
-            const float L = wa * l + wb * mlb.y;
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            __half *ob = p.out + ((int64_t)unit * p.R + rho0) * D;
-            float *pml = p.part + (int64_t)blockIdx.x * C::RB * (D + 2);
-            float *pacc = pml + 2 * C::RB;
-            if (p.splits > 1 && live) reinterpret_cast<float2 *>(pml)[tid] = make_float2(mst, L);
+        if (ok && n > 0) {
+            ok = wait_pv(n - 1);  // every PV is done (in-order completion)
+            if (!ok) fail();
+        }
+        tc_fence_after();
+        xchg[half * 128 + tid] = l;
+        named_bar_sync(2, 256);
+        const float L = xchg[tid] + xchg[128 + tid];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        __half *ob = p.out + ((int64_t)unit * p.R + rho0) * D;
+        float *pml = p.part + (int64_t)blockIdx.x * C::RB * (D + 2);
+        float *pacc = pml + 2 * C::RB;
+        if (p.splits > 1 && live && half == 0) reinterpret_cast<float2 *>(pml)[tid] = make_float2(m_ref, L);
 #pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t v[32], w[32];
-                if (ok && have_a) {
-                    tmem_ld32(trow + C::O_COL + 32u * ch, v);
-                } else {
+        for (int ch = 0; ch < D / 64; ++ch) {
+            const int c0 = half * (D / 2) + 32 * ch;  // output channel of column e: c0 + e
+            uint32_t v[32];
+            if (ok && n > 0) {
+                tmem_ld32(trow + C::O_COL + (uint32_t)c0, v);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+            if (!live) continue;
+            if (p.splits == 1) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 h;
+                    h.x = pack_half2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                    h.y = pack_half2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                    h.z = pack_half2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                    h.w = pack_half2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(ob + (int64_t)tid * D + c0 + e) = h;
                 }
-                if (ok && have_b) {
-                    tmem_ld32(trow + C::O_COL + (uint32_t)D + 32u * ch, w);
-                } else {
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) w[e] = 0u;
-                }
-                if (!live) continue;
-                float o[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = wa * __uint_as_float(v[e]) + wb * __uint_as_float(w[e]);
-                if (p.splits == 1) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 h;
-                        h.x = pack_half2(o[e] * inv, o[e + 1] * inv);
-                        h.y = pack_half2(o[e + 2] * inv, o[e + 3] * inv);
-                        h.z = pack_half2(o[e + 4] * inv, o[e + 5] * inv);
-                        h.w = pack_half2(o[e + 6] * inv, o[e + 7] * inv);
-                        *reinterpret_cast<uint4 *>(ob + (int64_t)tid * D + 32 * ch + e) = h;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(pacc + (int64_t)tid * D + 32 * ch + e) =
-                            make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                }
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(pacc + (int64_t)tid * D + c0 + e) =
+                        make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                    __uint_as_float(v[e + 3]));
             }
         }
     }
