@@ -330,7 +330,7 @@ NCU_TRAFFIC = {(3, 1, "quest", "f16", 16): 67_763_456, (3, 1, "quest", "e4m3", 1
                (2, 32, "dense", "f16", 16): 179_788_800, (2, 32, "dense", "e4m3", 16): 90_756_352,
                (2, 32, "dense", "int4", 16): 50_008_576}
 # The same for one prefill launch (one layer), keyed by (workload id, batch, chunk length).
-PREFILL_TRAFFIC = {(3, 1, 128): 548_153_856, (3, 1, 1024): 702_687_232}
+PREFILL_TRAFFIC = {(3, 1, 128): 547_511_296, (3, 1, 1024): 708_610_816}
 
 
 def capture(fn, device):
